@@ -1,0 +1,207 @@
+"""fp64 CPU oracle for exact-softmax attention forward and backward.
+
+TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` use it; the library under
+``attention_backward_preprocess_gb300`` never imports it.
+
+This module is a thin ctypes wrapper around ``fa_oracle.c`` (plain C, fp64,
+optionally OpenMP).  The C source documents the mathematics and where each
+step is stated on the pages; all arrays here are float64 numpy arrays in the
+public layouts:
+
+* dense : q, o, dout, dq ``[B, Sq, Hq, D]``; k, v, dk, dv ``[B, Sk, Hkv, D]``;
+  lse ``[B, Hq, Sq]``
+* varlen: ``cu_q`` / ``cu_k`` int32 prefix sums of the ``nseq`` lengths;
+  q ``[total_q, Hq, D]``; k ``[total_k, Hkv, D]``; lse ``[Hq, total_q]``
+
+Parity status: every function here is pinned by ``tests/test_oracle.py``
+(central finite differences, invariants, a hand-derived 2x2 example, closed
+forms for degenerate inputs).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "fa_oracle.c")
+_LIB = os.path.join(_HERE, "libfa_oracle.so")
+_lock = threading.Lock()
+_default = None
+
+
+def compile_library(src: str, out: str, openmp: bool = True) -> str:
+    """gcc -O2 (no fast-math) shared build of an oracle C source."""
+    tmp = out + ".tmp.%d" % os.getpid()
+    base = ["gcc", "-O2", "-std=c99", "-shared", "-fPIC", src, "-o", tmp, "-lm"]
+    try:
+        if not openmp:
+            raise subprocess.CalledProcessError(1, base)
+        subprocess.run(base[:2] + ["-fopenmp"] + base[2:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile fa_oracle.c into libfa_oracle.so (gcc, -O2, OpenMP if available)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(SOURCE):
+        return _LIB
+    return compile_library(SOURCE, _LIB)
+
+
+def _f64(a):
+    if a is None:
+        return None
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _ptr(a, ctype=ctypes.c_double):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _shape_args(q, k, scale, causal, cu_q, cu_k):
+    if cu_q is None:
+        if q.ndim != 4 or k.ndim != 4:
+            raise ValueError("dense inputs are [B, S, H, D]")
+        B, Sq, Hq, D = q.shape
+        Sk, Hkv = k.shape[1], k.shape[2]
+        cq = ck = None
+    else:
+        cq = np.ascontiguousarray(cu_q, dtype=np.int32)
+        ck = np.ascontiguousarray(cu_k, dtype=np.int32)
+        B = len(cq) - 1
+        Hq, D = q.shape[1], q.shape[2]
+        Hkv = k.shape[1]
+        Sq = int(np.max(np.diff(cq))) if B > 0 else 0
+        Sk = int(np.max(np.diff(ck))) if B > 0 else 0
+    args = [B, Sq, Sk, Hq, Hkv, D, float(scale), int(bool(causal)),
+            _ptr(cq, ctypes.c_int), _ptr(ck, ctypes.c_int)]
+    return args, (cq, ck), (B, Sq, Sk, Hq, Hkv, D)
+
+
+class Oracle:
+    """ctypes front end of one compiled oracle library."""
+
+    def __init__(self, libpath: str):
+        lib = ctypes.CDLL(libpath)
+        dp = ctypes.POINTER(ctypes.c_double)
+        ip = ctypes.POINTER(ctypes.c_int)
+        shape = [ctypes.c_int] * 6 + [ctypes.c_double, ctypes.c_int, ip, ip]
+        lib.oracle_forward.argtypes = [dp, dp, dp] + shape + [dp, dp, ctypes.c_int]
+        lib.oracle_forward.restype = ctypes.c_int
+        lib.oracle_backward.argtypes = [dp] * 6 + shape + [dp, dp, dp, ctypes.c_int]
+        lib.oracle_backward.restype = ctypes.c_int
+        lib.oracle_backward_sampled.argtypes = (
+            [dp] * 6 + shape + [ctypes.c_int, ip, dp, ctypes.c_int, ip, dp, dp, ctypes.c_int])
+        lib.oracle_backward_sampled.restype = ctypes.c_int
+        lib.oracle_head_matrices.argtypes = [dp] * 6 + shape + [ctypes.c_int] * 2 + [dp, dp]
+        lib.oracle_head_matrices.restype = ctypes.c_int
+        lib.oracle_max_threads.restype = ctypes.c_int
+        self.lib = lib
+        self.path = libpath
+
+    def max_threads(self) -> int:
+        return int(self.lib.oracle_max_threads())
+
+    def _threads(self, nthreads):
+        return int(nthreads) if nthreads else self.max_threads()
+
+    def forward(self, q, k, v, scale, causal=False, cu_q=None, cu_k=None, nthreads=None):
+        """Returns (o, lse) in fp64; lse is natural-log, -inf for a row with no key."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        args, keep, (B, Sq, Sk, Hq, Hkv, D) = _shape_args(q, k, scale, causal, cu_q, cu_k)
+        o = np.zeros_like(q)
+        lse = np.zeros((B, Hq, Sq) if cu_q is None else (Hq, q.shape[0]), dtype=np.float64)
+        rc = self.lib.oracle_forward(_ptr(q), _ptr(k), _ptr(v), *args, _ptr(o), _ptr(lse),
+                                     self._threads(nthreads))
+        if rc:
+            raise ValueError("oracle_forward rejected its arguments (%d)" % rc)
+        return o, lse
+
+    def backward(self, q, k, v, dout, scale, causal=False, o=None, lse=None, cu_q=None,
+                 cu_k=None, nthreads=None):
+        """Returns (dq, dk, dv) in fp64.  o / lse None -> the oracle's own fp64 forward."""
+        q, k, v, dout, o, lse = map(_f64, (q, k, v, dout, o, lse))
+        args, keep, _ = _shape_args(q, k, scale, causal, cu_q, cu_k)
+        dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+        rc = self.lib.oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                      _ptr(dout), *args, _ptr(dq), _ptr(dk), _ptr(dv),
+                                      self._threads(nthreads))
+        if rc:
+            raise ValueError("oracle_backward rejected its arguments (%d)" % rc)
+        return dq, dk, dv
+
+    def backward_sampled(self, q, k, v, dout, scale, causal=False, o=None, lse=None, cu_q=None,
+                         cu_k=None, qrows=(), krows=(), nthreads=None):
+        """dQ rows for (b, s, h) triples and dK / dV rows for (b, s, hk) triples.
+
+        Returns (dq_rows [nq, D], dk_rows [nk, D], dv_rows [nk, D]).
+        """
+        q, k, v, dout, o, lse = map(_f64, (q, k, v, dout, o, lse))
+        args, keep, (B, Sq, Sk, Hq, Hkv, D) = _shape_args(q, k, scale, causal, cu_q, cu_k)
+        qr = np.ascontiguousarray(np.asarray(qrows, dtype=np.int32).reshape(-1, 3))
+        kr = np.ascontiguousarray(np.asarray(krows, dtype=np.int32).reshape(-1, 3))
+        dq = np.zeros((len(qr), D))
+        dk = np.zeros((len(kr), D))
+        dv = np.zeros((len(kr), D))
+        rc = self.lib.oracle_backward_sampled(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), *args,
+            len(qr), _ptr(qr, ctypes.c_int), _ptr(dq), len(kr), _ptr(kr, ctypes.c_int),
+            _ptr(dk), _ptr(dv), self._threads(nthreads))
+        if rc:
+            raise ValueError("oracle_backward_sampled rejected its arguments (%d)" % rc)
+        return dq, dk, dv
+
+    def head_matrices(self, q, k, v, dout, scale, causal=False, o=None, lse=None, cu_q=None,
+                      cu_k=None, b=0, h=0):
+        """Dense P and dS [Lq, Lk] of one (sequence, query head) problem (tiny inputs)."""
+        q, k, v, dout, o, lse = map(_f64, (q, k, v, dout, o, lse))
+        args, keep, (B, Sq, Sk, Hq, Hkv, D) = _shape_args(q, k, scale, causal, cu_q, cu_k)
+        if cu_q is None:
+            lq, lk = Sq, Sk
+        else:
+            lq = int(keep[0][b + 1] - keep[0][b])
+            lk = int(keep[1][b + 1] - keep[1][b])
+        P = np.zeros((lq, lk))
+        dS = np.zeros((lq, lk))
+        rc = self.lib.oracle_head_matrices(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                           _ptr(dout), *args, int(b), int(h), _ptr(P), _ptr(dS))
+        if rc:
+            raise ValueError("oracle_head_matrices rejected its arguments (%d)" % rc)
+        return P, dS
+
+
+def default() -> Oracle:
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def max_threads() -> int:
+    return default().max_threads()
+
+
+def forward(*a, **kw):
+    return default().forward(*a, **kw)
+
+
+def backward(*a, **kw):
+    return default().backward(*a, **kw)
+
+
+def backward_sampled(*a, **kw):
+    return default().backward_sampled(*a, **kw)
+
+
+def head_matrices(*a, **kw):
+    return default().head_matrices(*a, **kw)

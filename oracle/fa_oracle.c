@@ -1,0 +1,366 @@
+/*
+ * fa_oracle.c -- fp64 CPU oracle for exact-softmax attention and its analytic
+ * backward pass (dQ, dK, dV).
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the checker, not the product: only
+ * the test suite, the smoke check and the benchmark's CPU-baseline leg load
+ * it.  It shares no code, header, table or helper with the CUDA path.
+ *
+ * What it computes, per sequence b and query head h (kv head hk = h / G,
+ * G = Hq / Hkv, the head-group mapping of CollectiveEpilogueBwdGQA in
+ * "flash-attention/hopper/epilogue_bwd.hpp", to_underlying_arguments):
+ *
+ *   s_ij   = scale * <q_i, k_j>                         (STAGE 1, Q@K Gemm0 of
+ *                                                        the Composable Kernel
+ *                                                        page)
+ *   mask   : key j is visible to query i iff j < Lk and, when causal,
+ *            j <= i + (Lk - Lq)   (bottom-right alignment; the pages do not
+ *            define the mask, this is the reading taken)
+ *   LSE_i  = log sum_{visible j} exp(s_ij)   (natural log; -inf if no key is
+ *            visible)
+ *   P_ij   = exp(s_ij - LSE_i) on visible entries, 0 elsewhere.  A row whose
+ *            LSE is -inf uses 0 instead (get_validated_lse of the Composable
+ *            Kernel page); such a row has no visible entry, so P stays 0.
+ *   O_i    = sum_j P_ij v_j
+ *   dP_ij  = <dO_i, v_j>                                 (STAGE 4, Gemm2)
+ *   Dv_i   = <dO_i, O_i>      (the preprocess quantity; derived from
+ *            Dv_i = sum_j P_ij dP_ij because sum_j P_ij v_j = O_i)
+ *   dS_ij  = P_ij (dP_ij - Dv_i)                         (STAGE 5)
+ *   dV_j   = sum_{g in group} sum_i P_ij dO_i            (STAGE 3, Gemm1)
+ *   dK_j   = scale * sum_{g in group} sum_i dS_ij q_i    (STAGE 6, Gemm3 and
+ *                                                        the final dK scale)
+ *   dQ_i   = scale * sum_j dS_ij k_j                     (STAGE 7, Gemm4 and
+ *                                                        the QGrad scale)
+ *
+ * The backward takes O and LSE either from the caller (the forward's stored,
+ * rounded values, as the GPU sees them) or, when those pointers are NULL,
+ * computes them itself in fp64 ("fully fp64" variant).
+ *
+ * Layouts (row-major, d innermost, like the GPU path's public layout):
+ *   dense : q, o, dout, dq [B, Sq, Hq, D];  k, v, dk, dv [B, Sk, Hkv, D];
+ *           lse [B, Hq, Sq]
+ *   varlen: cu_q / cu_k give prefix sums of nseq = B lengths;
+ *           q [total_q, Hq, D]; k [total_k, Hkv, D]; lse [Hq, total_q]
+ *
+ * Everything is a plain loop over the definition above.  Parallelism is over
+ * independent output rows only (no reductions across threads), so results do
+ * not depend on the thread count.
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+typedef struct {
+    const double *q, *k, *v, *o, *dout, *lse;
+    int B, Sq, Sk, Hq, Hkv, D, G;
+    double scale;
+    int causal;
+    const int *cu_q, *cu_k;
+    long total_q, total_k;
+} prob_t;
+
+static int seq_len_q(const prob_t *p, int b) {
+    return p->cu_q ? p->cu_q[b + 1] - p->cu_q[b] : p->Sq;
+}
+static int seq_len_k(const prob_t *p, int b) {
+    return p->cu_k ? p->cu_k[b + 1] - p->cu_k[b] : p->Sk;
+}
+/* index of the (b, s, head) row in a [.., S, H, D] or packed [total, H, D] tensor */
+static long row_q(const prob_t *p, int b, int s, int h) {
+    long base = p->cu_q ? (long)p->cu_q[b] + s : (long)b * p->Sq + s;
+    return (base * p->Hq + h) * p->D;
+}
+static long row_k(const prob_t *p, int b, int s, int hk) {
+    long base = p->cu_k ? (long)p->cu_k[b] + s : (long)b * p->Sk + s;
+    return (base * p->Hkv + hk) * p->D;
+}
+static long lse_index(const prob_t *p, int b, int s, int h) {
+    if (p->cu_q) return (long)h * p->total_q + p->cu_q[b] + s;
+    return ((long)b * p->Hq + h) * p->Sq + s;
+}
+static int visible(const prob_t *p, int b, int i, int j) {
+    int lq = seq_len_q(p, b), lk = seq_len_k(p, b);
+    if (j < 0 || j >= lk || i < 0 || i >= lq) return 0;
+    if (p->causal && j > i + (lk - lq)) return 0;
+    return 1;
+}
+static double dot(const double *a, const double *b, int n) {
+    double acc = 0.0;
+    for (int t = 0; t < n; ++t) acc += a[t] * b[t];
+    return acc;
+}
+static double score(const prob_t *p, int b, int h, int i, int j) {
+    int hk = h / p->G;
+    return p->scale * dot(p->q + row_q(p, b, i, h), p->k + row_k(p, b, j, hk), p->D);
+}
+
+/* Forward statistics of one query row: LSE_i (natural log) and, if o_out is
+ * not NULL, O_i = sum_j P_ij v_j.  Max-shifted sum for range safety only. */
+static double row_forward(const prob_t *p, int b, int h, int i, double *o_out) {
+    int lk = seq_len_k(p, b), hk = h / p->G, D = p->D;
+    double m = -INFINITY;
+    for (int j = 0; j < lk; ++j)
+        if (visible(p, b, i, j)) {
+            double s = score(p, b, h, i, j);
+            if (s > m) m = s;
+        }
+    if (o_out) for (int d = 0; d < D; ++d) o_out[d] = 0.0;
+    if (m == -INFINITY) return -INFINITY; /* no visible key */
+    double sum = 0.0;
+    for (int j = 0; j < lk; ++j)
+        if (visible(p, b, i, j)) sum += exp(score(p, b, h, i, j) - m);
+    double lse = m + log(sum);
+    if (o_out) {
+        for (int j = 0; j < lk; ++j)
+            if (visible(p, b, i, j)) {
+                double pij = exp(score(p, b, h, i, j) - lse);
+                const double *vj = p->v + row_k(p, b, j, hk);
+                for (int d = 0; d < D; ++d) o_out[d] += pij * vj[d];
+            }
+    }
+    return lse;
+}
+
+/* The LSE the backward uses for row i (given or own), with the -inf guard. */
+static double row_lse_for_backward(const prob_t *p, int b, int h, int i, double *o_scratch) {
+    double lse = p->lse ? p->lse[lse_index(p, b, i, h)] : row_forward(p, b, h, i, o_scratch);
+    if (lse == -INFINITY) lse = 0.0; /* get_validated_lse */
+    return lse;
+}
+
+/* Dv_i = <dO_i, O_i>, O given or recomputed in fp64. */
+static double row_dvec(const prob_t *p, int b, int h, int i, double *o_scratch) {
+    const double *doi = p->dout + row_q(p, b, i, h);
+    if (p->o) return dot(doi, p->o + row_q(p, b, i, h), p->D);
+    row_forward(p, b, h, i, o_scratch);
+    return dot(doi, o_scratch, p->D);
+}
+
+static double prob(const prob_t *p, int b, int h, int i, int j, double lse_i) {
+    if (!visible(p, b, i, j)) return 0.0;
+    return exp(score(p, b, h, i, j) - lse_i);
+}
+static double dprob(const prob_t *p, int b, int h, int i, int j) {
+    int hk = h / p->G;
+    return dot(p->dout + row_q(p, b, i, h), p->v + row_k(p, b, j, hk), p->D);
+}
+
+/* dQ_i = scale * sum_j P_ij (dP_ij - Dv_i) k_j */
+static void row_dq(const prob_t *p, int b, int h, int i, double *dq_out, double *scratch) {
+    int lk = seq_len_k(p, b), hk = h / p->G, D = p->D;
+    double lse = row_lse_for_backward(p, b, h, i, scratch);
+    double dv = row_dvec(p, b, h, i, scratch);
+    for (int d = 0; d < D; ++d) dq_out[d] = 0.0;
+    for (int j = 0; j < lk; ++j) {
+        double pij = prob(p, b, h, i, j, lse);
+        if (pij == 0.0) continue;
+        double ds = pij * (dprob(p, b, h, i, j) - dv);
+        const double *kj = p->k + row_k(p, b, j, hk);
+        for (int d = 0; d < D; ++d) dq_out[d] += ds * kj[d];
+    }
+    for (int d = 0; d < D; ++d) dq_out[d] *= p->scale;
+}
+
+/* dK_j, dV_j for key row j of kv head hk, summed over the G query heads of the
+ * group.  lse_g / dvec_g hold, for each head g of the group, the per-row LSE
+ * (already guarded) and Dv of sequence b. */
+static void col_dkdv(const prob_t *p, int b, int hk, int j, double *const *lse_g,
+                     double *const *dvec_g, double *dk_out, double *dv_out) {
+    int lq = seq_len_q(p, b), D = p->D;
+    for (int d = 0; d < D; ++d) { dk_out[d] = 0.0; dv_out[d] = 0.0; }
+    for (int g = 0; g < p->G; ++g) {
+        int h = hk * p->G + g;
+        for (int i = 0; i < lq; ++i) {
+            double pij = prob(p, b, h, i, j, lse_g[g][i]);
+            if (pij == 0.0) continue;
+            const double *doi = p->dout + row_q(p, b, i, h);
+            const double *qi = p->q + row_q(p, b, i, h);
+            double ds = pij * (dprob(p, b, h, i, j) - dvec_g[g][i]);
+            for (int d = 0; d < D; ++d) {
+                dv_out[d] += pij * doi[d];
+                dk_out[d] += ds * qi[d];
+            }
+        }
+    }
+    for (int d = 0; d < D; ++d) dk_out[d] *= p->scale;
+}
+
+/* Per-row LSE (guarded) and Dv for every query row of the G heads of (b, hk). */
+static void group_row_stats(const prob_t *p, int b, int hk, double **lse_g, double **dvec_g,
+                            int nthreads) {
+    int lq = seq_len_q(p, b);
+    for (int g = 0; g < p->G; ++g) {
+        int h = hk * p->G + g;
+        double *lse = lse_g[g], *dvec = dvec_g[g];
+#pragma omp parallel for schedule(dynamic, 8) num_threads(nthreads)
+        for (int i = 0; i < lq; ++i) {
+            double *scratch = (double *)malloc(sizeof(double) * p->D);
+            lse[i] = row_lse_for_backward(p, b, h, i, scratch);
+            dvec[i] = row_dvec(p, b, h, i, scratch);
+            free(scratch);
+        }
+    }
+}
+
+static int make_prob(prob_t *p, const double *q, const double *k, const double *v,
+                     const double *o, const double *lse, const double *dout, int B, int Sq,
+                     int Sk, int Hq, int Hkv, int D, double scale, int causal, const int *cu_q,
+                     const int *cu_k) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0) return 1;
+    if ((cu_q == NULL) != (cu_k == NULL)) return 1;
+    p->q = q; p->k = k; p->v = v; p->o = o; p->lse = lse; p->dout = dout;
+    p->B = B; p->Sq = Sq; p->Sk = Sk; p->Hq = Hq; p->Hkv = Hkv; p->D = D; p->G = Hq / Hkv;
+    p->scale = scale; p->causal = causal; p->cu_q = cu_q; p->cu_k = cu_k;
+    p->total_q = cu_q ? cu_q[B] : (long)B * Sq;
+    p->total_k = cu_k ? cu_k[B] : (long)B * Sk;
+    return 0;
+}
+
+/* ---------------------------------------------------------------- public */
+
+int oracle_forward(const double *q, const double *k, const double *v, int B, int Sq, int Sk,
+                   int Hq, int Hkv, int D, double scale, int causal, const int *cu_q,
+                   const int *cu_k, double *o, double *lse, int nthreads) {
+    prob_t p;
+    if (make_prob(&p, q, k, v, NULL, NULL, NULL, B, Sq, Sk, Hq, Hkv, D, scale, causal, cu_q,
+                  cu_k))
+        return 1;
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < Hq; ++h) {
+            int lq = seq_len_q(&p, b);
+#pragma omp parallel for schedule(dynamic, 8) num_threads(nthreads)
+            for (int i = 0; i < lq; ++i)
+                lse[lse_index(&p, b, i, h)] = row_forward(&p, b, h, i, o + row_q(&p, b, i, h));
+        }
+    return 0;
+}
+
+/* Full backward.  o / lse may be NULL (then the oracle's own fp64 forward is
+ * used).  dq has q's layout, dk / dv have k's layout. */
+int oracle_backward(const double *q, const double *k, const double *v, const double *o,
+                    const double *lse, const double *dout, int B, int Sq, int Sk, int Hq,
+                    int Hkv, int D, double scale, int causal, const int *cu_q, const int *cu_k,
+                    double *dq, double *dk, double *dv, int nthreads) {
+    prob_t p;
+    if (make_prob(&p, q, k, v, o, lse, dout, B, Sq, Sk, Hq, Hkv, D, scale, causal, cu_q, cu_k))
+        return 1;
+    double **lse_g = (double **)malloc(sizeof(double *) * p.G);
+    double **dvec_g = (double **)malloc(sizeof(double *) * p.G);
+    for (int b = 0; b < B; ++b) {
+        int lq = seq_len_q(&p, b), lk = seq_len_k(&p, b);
+        for (int g = 0; g < p.G; ++g) {
+            lse_g[g] = (double *)malloc(sizeof(double) * (lq > 0 ? lq : 1));
+            dvec_g[g] = (double *)malloc(sizeof(double) * (lq > 0 ? lq : 1));
+        }
+        for (int h = 0; h < Hq; ++h) {
+#pragma omp parallel for schedule(dynamic, 8) num_threads(nthreads)
+            for (int i = 0; i < lq; ++i) {
+                double *scratch = (double *)malloc(sizeof(double) * D);
+                row_dq(&p, b, h, i, dq + row_q(&p, b, i, h), scratch);
+                free(scratch);
+            }
+        }
+        for (int hk = 0; hk < Hkv; ++hk) {
+            group_row_stats(&p, b, hk, lse_g, dvec_g, nthreads);
+#pragma omp parallel for schedule(dynamic, 8) num_threads(nthreads)
+            for (int j = 0; j < lk; ++j)
+                col_dkdv(&p, b, hk, j, lse_g, dvec_g, dk + row_k(&p, b, j, hk),
+                         dv + row_k(&p, b, j, hk));
+        }
+        for (int g = 0; g < p.G; ++g) { free(lse_g[g]); free(dvec_g[g]); }
+    }
+    free(lse_g);
+    free(dvec_g);
+    return 0;
+}
+
+/* Sampled backward: dQ for n_qrows query rows given as (b, s, h) triples, and
+ * dK / dV for n_krows key rows given as (b, s, hk) triples.  Outputs are
+ * packed [n, D].  Each requested row is computed exactly as in the full
+ * backward. */
+int oracle_backward_sampled(const double *q, const double *k, const double *v, const double *o,
+                            const double *lse, const double *dout, int B, int Sq, int Sk, int Hq,
+                            int Hkv, int D, double scale, int causal, const int *cu_q,
+                            const int *cu_k, int n_qrows, const int *qrows, double *dq_rows,
+                            int n_krows, const int *krows, double *dk_rows, double *dv_rows,
+                            int nthreads) {
+    prob_t p;
+    if (make_prob(&p, q, k, v, o, lse, dout, B, Sq, Sk, Hq, Hkv, D, scale, causal, cu_q, cu_k))
+        return 1;
+    for (int r = 0; r < n_qrows; ++r) {
+        int b = qrows[3 * r], s = qrows[3 * r + 1], h = qrows[3 * r + 2];
+        if (b < 0 || b >= B || h < 0 || h >= Hq || s < 0 || s >= seq_len_q(&p, b)) return 2;
+    }
+    for (int r = 0; r < n_krows; ++r) {
+        int b = krows[3 * r], s = krows[3 * r + 1], hk = krows[3 * r + 2];
+        if (b < 0 || b >= B || hk < 0 || hk >= Hkv || s < 0 || s >= seq_len_k(&p, b)) return 2;
+    }
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+    for (int r = 0; r < n_qrows; ++r) {
+        double *scratch = (double *)malloc(sizeof(double) * D);
+        row_dq(&p, qrows[3 * r], qrows[3 * r + 2], qrows[3 * r + 1], dq_rows + (long)r * D,
+               scratch);
+        free(scratch);
+    }
+    /* key rows: group by (b, hk) so that the per-row statistics of each group
+     * are computed once */
+    char *done = (char *)calloc(n_krows > 0 ? n_krows : 1, 1);
+    double **lse_g = (double **)malloc(sizeof(double *) * p.G);
+    double **dvec_g = (double **)malloc(sizeof(double *) * p.G);
+    for (int r0 = 0; r0 < n_krows; ++r0) {
+        if (done[r0]) continue;
+        int b = krows[3 * r0], hk = krows[3 * r0 + 2], lq = seq_len_q(&p, b);
+        for (int g = 0; g < p.G; ++g) {
+            lse_g[g] = (double *)malloc(sizeof(double) * (lq > 0 ? lq : 1));
+            dvec_g[g] = (double *)malloc(sizeof(double) * (lq > 0 ? lq : 1));
+        }
+        group_row_stats(&p, b, hk, lse_g, dvec_g, nthreads);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+        for (int r = r0; r < n_krows; ++r) {
+            if (krows[3 * r] != b || krows[3 * r + 2] != hk) continue;
+            col_dkdv(&p, b, hk, krows[3 * r + 1], lse_g, dvec_g, dk_rows + (long)r * D,
+                     dv_rows + (long)r * D);
+            done[r] = 1;
+        }
+        for (int g = 0; g < p.G; ++g) { free(lse_g[g]); free(dvec_g[g]); }
+    }
+    free(done);
+    free(lse_g);
+    free(dvec_g);
+    return 0;
+}
+
+/* Dense P and dS of one (b, h) head problem, row-major [Lq, Lk] -- for the
+ * invariant checks on tiny inputs. */
+int oracle_head_matrices(const double *q, const double *k, const double *v, const double *o,
+                         const double *lse, const double *dout, int B, int Sq, int Sk, int Hq,
+                         int Hkv, int D, double scale, int causal, const int *cu_q,
+                         const int *cu_k, int b, int h, double *P, double *dS) {
+    prob_t p;
+    if (make_prob(&p, q, k, v, o, lse, dout, B, Sq, Sk, Hq, Hkv, D, scale, causal, cu_q, cu_k))
+        return 1;
+    int lq = seq_len_q(&p, b), lk = seq_len_k(&p, b);
+    double *scratch = (double *)malloc(sizeof(double) * D);
+    for (int i = 0; i < lq; ++i) {
+        double l = row_lse_for_backward(&p, b, h, i, scratch);
+        double dvec = row_dvec(&p, b, h, i, scratch);
+        for (int j = 0; j < lk; ++j) {
+            double pij = prob(&p, b, h, i, j, l);
+            P[(long)i * lk + j] = pij;
+            dS[(long)i * lk + j] = pij * (dprob(&p, b, h, i, j) - dvec);
+        }
+    }
+    free(scratch);
+    return 0;
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,307 @@
+"""Pins that tie the fp64 oracle to something other than itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` instance and raises
+AssertionError when the oracle disagrees with:
+
+* central finite differences of its own forward (the backward is the exact
+  gradient of L = sum(dO * O)),
+* the hand-derived 2x2 worked example in ``tests/golden/worked_2x2.json``,
+* closed forms of degenerate inputs (K = 0, V = 0, a single key, a single
+  query, causal rows with no visible key),
+* invariants (sum_j dS_ij = 0, sum_j P_ij = 1, dV = P^T dO, sum_j dK_j = 0,
+  sum_j dV_j = sum_i dO_i),
+* an independent library forward (scipy softmax + numpy matmul),
+* structural reductions (GQA == MHA with repeated K/V, summed over the group;
+  varlen == each sequence run alone).
+
+``tests/test_oracle.py`` runs every pin on the real oracle and also on
+mutant builds with a planted mistake, each of which must fail at least one
+pin.
+"""
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "worked_2x2.json")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _close(a, b, rtol, what):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    assert a.shape == b.shape, (what, a.shape, b.shape)
+    inf_a, inf_b = np.isinf(a), np.isinf(b)
+    assert np.array_equal(inf_a, inf_b) and np.array_equal(a[inf_a], b[inf_b]), what + ": inf"
+    a = np.where(inf_a, 0.0, a)
+    b = np.where(inf_b, 0.0, b)
+    denom = max(1.0, float(np.max(np.abs(b)))) if b.size else 1.0
+    err = float(np.max(np.abs(a - b))) / denom if a.size else 0.0
+    assert err <= rtol, "%s: max err %.3e > %.1e" % (what, err, rtol)
+
+
+def _dense(rng, B, Sq, Sk, Hq, Hkv, D, scale_in=1.0):
+    q = rng.standard_normal((B, Sq, Hq, D)) * scale_in
+    k = rng.standard_normal((B, Sk, Hkv, D)) * scale_in
+    v = rng.standard_normal((B, Sk, Hkv, D))
+    do = rng.standard_normal((B, Sq, Hq, D))
+    return q, k, v, do
+
+
+def _fd_check(orc, q, k, v, do, scale, causal, cu_q=None, cu_k=None, h=1e-6, rtol=2e-7):
+    """Backward (own fp64 forward) == central differences of L = sum(dO * O)."""
+    dq, dk, dv = orc.backward(q, k, v, do, scale, causal, cu_q=cu_q, cu_k=cu_k)
+
+    def loss(qq, kk, vv):
+        o, _ = orc.forward(qq, kk, vv, scale, causal, cu_q=cu_q, cu_k=cu_k, nthreads=1)
+        return float(np.sum(do * o))
+
+    for X, G, name in ((q, dq, "dq"), (k, dk, "dk"), (v, dv, "dv")):
+        num = np.zeros_like(X)
+        for idx in np.ndindex(X.shape):
+            Xp = X.copy()
+            Xm = X.copy()
+            Xp[idx] += h
+            Xm[idx] -= h
+            args_p = [q, k, v]
+            args_m = [q, k, v]
+            pos = {"dq": 0, "dk": 1, "dv": 2}[name]
+            args_p[pos] = Xp
+            args_m[pos] = Xm
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        _close(G, num, rtol, "finite differences " + name)
+
+
+# ----------------------------------------------------------------- pins
+
+def pin_worked_example(orc):
+    g = json.load(open(GOLDEN))
+    inp = g["inputs"]
+    q = np.array(inp["q"]).reshape(1, 2, 1, 1)
+    k = np.array(inp["k"]).reshape(1, 2, 1, 1)
+    v = np.array(inp["v"]).reshape(1, 2, 1, 1)
+    do = np.array(inp["dout"]).reshape(1, 2, 1, 1)
+    for key, causal in (("non_causal", False), ("causal", True)):
+        e = g[key]
+        o, lse = orc.forward(q, k, v, inp["scale"], causal)
+        _close(o.ravel(), e["o"], 1e-14, key + " o")
+        _close(lse.ravel(), e["lse"], 1e-14, key + " lse")
+        P, dS = orc.head_matrices(q, k, v, do, inp["scale"], causal)
+        _close(P, e["P"], 1e-14, key + " P")
+        _close(dS, e["dS"], 1e-14, key + " dS")
+        for given in (False, True):
+            kw = dict(o=o, lse=lse) if given else {}
+            dq, dk, dv = orc.backward(q, k, v, do, inp["scale"], causal, **kw)
+            _close(dq.ravel(), e["dq"], 1e-14, key + " dq")
+            _close(dk.ravel(), e["dk"], 1e-14, key + " dk")
+            _close(dv.ravel(), e["dv"], 1e-14, key + " dv")
+
+
+def pin_fd_dense(orc):
+    q, k, v, do = _dense(_rng(1), 2, 6, 6, 2, 2, 4)
+    _fd_check(orc, q, k, v, do, 0.7, False)
+
+
+def pin_fd_causal(orc):
+    q, k, v, do = _dense(_rng(2), 1, 9, 9, 1, 1, 3)
+    _fd_check(orc, q, k, v, do, 0.5, True)
+
+
+def pin_fd_causal_rect(orc):
+    # Sq < Sk and Sq > Sk (the latter has query rows with no visible key)
+    for sq, sk, seed in ((5, 8, 3), (8, 5, 4)):
+        q, k, v, do = _dense(_rng(seed), 1, sq, sk, 1, 1, 3)
+        _fd_check(orc, q, k, v, do, 0.6, True)
+
+
+def pin_fd_gqa(orc):
+    q, k, v, do = _dense(_rng(5), 1, 5, 5, 4, 2, 3)
+    _fd_check(orc, q, k, v, do, 0.8, True)
+
+
+def pin_fd_varlen(orc):
+    rng = _rng(6)
+    cu_q = np.array([0, 5, 12], dtype=np.int32)
+    cu_k = np.array([0, 7, 11], dtype=np.int32)
+    q = rng.standard_normal((12, 2, 3))
+    k = rng.standard_normal((11, 2, 3))
+    v = rng.standard_normal((11, 2, 3))
+    do = rng.standard_normal((12, 2, 3))
+    _fd_check(orc, q, k, v, do, 0.9, True, cu_q=cu_q, cu_k=cu_k)
+
+
+def pin_library_forward(orc):
+    """O and LSE against scipy's softmax / logsumexp and numpy matmul."""
+    from scipy.special import logsumexp, softmax
+    for causal, (sq, sk) in ((False, (7, 7)), (True, (7, 7)), (True, (4, 9)), (True, (9, 4))):
+        q, k, v, do = _dense(_rng(7 + sq), 1, sq, sk, 2, 1, 5)
+        o, lse = orc.forward(q, k, v, 0.45, causal)
+        for h in range(2):
+            S = 0.45 * q[0, :, h, :] @ k[0, :, 0, :].T
+            if causal:
+                i = np.arange(sq)[:, None]
+                j = np.arange(sk)[None, :]
+                S = np.where(j <= i + (sk - sq), S, -np.inf)
+            for r in range(sq):
+                if np.all(np.isneginf(S[r])):
+                    assert np.isneginf(lse[0, h, r]), "row without keys must have LSE -inf"
+                    _close(o[0, r, h], np.zeros(5), 0, "row without keys O")
+                    continue
+                _close(lse[0, h, r], logsumexp(S[r]), 1e-13, "lse vs logsumexp")
+                _close(o[0, r, h], softmax(S[r]) @ v[0, :, 0, :], 1e-13, "O vs softmax@V")
+
+
+def pin_closed_forms(orc):
+    rng = _rng(8)
+    B, S, H, D, c = 1, 6, 1, 4, 0.3
+    q, k, v, do = _dense(rng, B, S, S, H, H, D)
+    # K = 0: P uniform -> dV_j = mean_i... = (1/Sk) sum_i dO_i, dQ = 0
+    dq, dk, dv = orc.backward(q, np.zeros_like(k), v, do, c, False)
+    _close(dq, np.zeros_like(dq), 1e-15, "K=0 dq")
+    for j in range(S):
+        _close(dv[0, j, 0], do[0, :, 0].sum(0) / S, 1e-13, "K=0 dv")
+    # V = 0: dP = 0 and D = 0 -> dS = 0 -> dQ = dK = 0
+    dq, dk, dv = orc.backward(q, k, np.zeros_like(v), do, c, False)
+    _close(dq, np.zeros_like(dq), 1e-15, "V=0 dq")
+    _close(dk, np.zeros_like(dk), 1e-15, "V=0 dk")
+    # one key: P = 1, O_i = v_0, dS = 0, dV_0 = sum_i dO_i
+    q1, k1, v1, do1 = _dense(rng, 1, 5, 1, 1, 1, D)
+    o, lse = orc.forward(q1, k1, v1, c, False)
+    for i in range(5):
+        _close(o[0, i, 0], v1[0, 0, 0], 1e-14, "one key O")
+        _close(lse[0, 0, i], c * q1[0, i, 0] @ k1[0, 0, 0], 1e-14, "one key LSE")
+    dq, dk, dv = orc.backward(q1, k1, v1, do1, c, False)
+    _close(dq, np.zeros_like(dq), 1e-14, "one key dq")
+    _close(dk, np.zeros_like(dk), 1e-14, "one key dk")
+    _close(dv[0, 0, 0], do1[0, :, 0].sum(0), 1e-13, "one key dv")
+    # causal, Sq == Sk: query 0 sees key 0 only
+    o, lse = orc.forward(q, k, v, c, True)
+    _close(o[0, 0, 0], v[0, 0, 0], 1e-14, "causal row 0 O")
+    _close(lse[0, 0, 0], c * q[0, 0, 0] @ k[0, 0, 0], 1e-14, "causal row 0 LSE")
+    # causal, bottom-right: one query against 3 keys sees all of them
+    qa, ka, va, doa = _dense(rng, 1, 1, 3, 1, 1, D)
+    oc, lc = orc.forward(qa, ka, va, c, True)
+    on, ln = orc.forward(qa, ka, va, c, False)
+    _close(oc, on, 1e-15, "bottom-right causal Sq=1 == non-causal")
+    _close(lc, ln, 1e-15, "bottom-right causal Sq=1 LSE == non-causal")
+    # causal, 3 queries against 1 key: only the last query sees it
+    qb, kb, vb, dob = _dense(rng, 1, 3, 1, 1, 1, D)
+    ob, lb = orc.forward(qb, kb, vb, c, True)
+    assert np.isneginf(lb[0, 0, 0]) and np.isneginf(lb[0, 0, 1]), "rows 0,1 see no key"
+    _close(ob[0, :2], np.zeros((2, 1, D)), 0, "rows without keys O")
+    _close(ob[0, 2, 0], vb[0, 0, 0], 1e-14, "last row sees the key")
+    dq, dk, dv = orc.backward(qb, kb, vb, dob, c, True)
+    _close(dq[0, :2], np.zeros((2, 1, D)), 0, "rows without keys dq")
+    _close(dv[0, 0, 0], dob[0, 2, 0], 1e-14, "dv from the only visible row")
+
+
+def pin_invariants(orc):
+    for causal, (sq, sk) in ((False, (7, 7)), (True, (7, 7)), (True, (5, 9)), (True, (9, 5))):
+        q, k, v, do = _dense(_rng(20 + sq), 1, sq, sk, 2, 1, 4)
+        c = 0.55
+        dq, dk, dv = orc.backward(q, k, v, do, c, causal)
+        dv_sum = np.zeros(4)
+        do_sum = np.zeros(4)
+        for h in range(2):
+            P, dS = orc.head_matrices(q, k, v, do, c, causal, h=h)
+            has_key = P.sum(1) > 0
+            _close(P.sum(1)[has_key], np.ones(has_key.sum()), 1e-14, "sum_j P = 1")
+            _close(dS.sum(1), np.zeros(sq), 1e-14, "sum_j dS = 0")
+            _close(dq[0, :, h], c * dS @ k[0, :, 0], 1e-13, "dQ = c dS K")
+            dv_sum += do[0, has_key, h].sum(0)
+        # GQA group of 2 heads shares kv head 0
+        P0, dS0 = orc.head_matrices(q, k, v, do, c, causal, h=0)
+        P1, dS1 = orc.head_matrices(q, k, v, do, c, causal, h=1)
+        _close(dv[0, :, 0], P0.T @ do[0, :, 0] + P1.T @ do[0, :, 1], 1e-13, "dV = P^T dO")
+        _close(dk[0, :, 0], c * (dS0.T @ q[0, :, 0] + dS1.T @ q[0, :, 1]), 1e-13, "dK = c dS^T Q")
+        _close(dk[0, :, 0].sum(0), np.zeros(4), 1e-13, "sum_j dK_j = 0")
+        _close(dv[0, :, 0].sum(0), dv_sum, 1e-13, "sum_j dV_j = sum_i dO_i")
+
+
+def pin_gqa_equals_expanded(orc):
+    rng = _rng(30)
+    q, k, v, do = _dense(rng, 2, 6, 6, 4, 2, 3)
+    for causal in (False, True):
+        dq, dk, dv = orc.backward(q, k, v, do, 0.6, causal)
+        ke = np.repeat(k, 2, axis=2)
+        ve = np.repeat(v, 2, axis=2)
+        dqe, dke, dve = orc.backward(q, ke, ve, do, 0.6, causal)
+        _close(dq, dqe, 1e-14, "GQA dq")
+        _close(dk, dke[:, :, 0::2] + dke[:, :, 1::2], 1e-14, "GQA dk = group sum")
+        _close(dv, dve[:, :, 0::2] + dve[:, :, 1::2], 1e-14, "GQA dv = group sum")
+
+
+def pin_varlen_equals_dense(orc):
+    rng = _rng(31)
+    cu_q = np.array([0, 4, 11, 12], dtype=np.int32)
+    cu_k = np.array([0, 6, 9, 13], dtype=np.int32)
+    q = rng.standard_normal((12, 2, 3))
+    k = rng.standard_normal((13, 1, 3))
+    v = rng.standard_normal((13, 1, 3))
+    do = rng.standard_normal((12, 2, 3))
+    for causal in (False, True):
+        o, lse = orc.forward(q, k, v, 0.7, causal, cu_q=cu_q, cu_k=cu_k)
+        dq, dk, dv = orc.backward(q, k, v, do, 0.7, causal, cu_q=cu_q, cu_k=cu_k)
+        for b in range(3):
+            qs, qe, ks, ke = cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1]
+            sub = [x[None] for x in (q[qs:qe], k[ks:ke], v[ks:ke], do[qs:qe])]
+            ob, lb = orc.forward(*sub[:3], 0.7, causal)
+            dqb, dkb, dvb = orc.backward(*sub, 0.7, causal)
+            _close(o[qs:qe], ob[0], 1e-15, "varlen o")
+            _close(lse[:, qs:qe], lb[0], 1e-15, "varlen lse")
+            _close(dq[qs:qe], dqb[0], 1e-15, "varlen dq")
+            _close(dk[ks:ke], dkb[0], 1e-15, "varlen dk")
+            _close(dv[ks:ke], dvb[0], 1e-15, "varlen dv")
+
+
+def pin_sampled_equals_full(orc):
+    q, k, v, do = _dense(_rng(32), 2, 9, 9, 4, 2, 5)
+    dq, dk, dv = orc.backward(q, k, v, do, 0.5, True)
+    qrows = [(0, 0, 0), (1, 8, 3), (0, 4, 2), (1, 3, 1)]
+    krows = [(0, 0, 0), (1, 8, 1), (0, 5, 1), (1, 2, 0)]
+    sq, sk, sv = orc.backward_sampled(q, k, v, do, 0.5, True, qrows=qrows, krows=krows)
+    for r, (b, s, h) in enumerate(qrows):
+        _close(sq[r], dq[b, s, h], 0, "sampled dq")
+    for r, (b, s, hk) in enumerate(krows):
+        _close(sk[r], dk[b, s, hk], 0, "sampled dk")
+        _close(sv[r], dv[b, s, hk], 0, "sampled dv")
+
+
+def pin_given_forward_consistent(orc):
+    q, k, v, do = _dense(_rng(33), 1, 8, 8, 2, 2, 4)
+    o, lse = orc.forward(q, k, v, 0.4, True)
+    a = orc.backward(q, k, v, do, 0.4, True)
+    b = orc.backward(q, k, v, do, 0.4, True, o=o, lse=lse)
+    for x, y, n in zip(a, b, ("dq", "dk", "dv")):
+        _close(x, y, 1e-14, "given O/LSE " + n)
+
+
+ALL_PINS = [
+    pin_worked_example, pin_fd_dense, pin_fd_causal, pin_fd_causal_rect, pin_fd_gqa,
+    pin_fd_varlen, pin_library_forward, pin_closed_forms, pin_invariants,
+    pin_gqa_equals_expanded, pin_varlen_equals_dense, pin_sampled_equals_full,
+    pin_given_forward_consistent,
+]
+
+
+def run_all(orc):
+    """Runs every pin; returns the names of the pins that failed."""
+    failed = []
+    for pin in ALL_PINS:
+        try:
+            pin(orc)
+        except AssertionError:
+            failed.append(pin.__name__)
+    return failed
+
+
+if __name__ == "__main__":  # used by the mutation test: python oracle_pins.py <libpath>
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    from oracle import Oracle
+    print(json.dumps(run_all(Oracle(sys.argv[1]))))

@@ -1,0 +1,91 @@
+"""The fp64 oracle against its pins (CPU only), plus planted-mistake checks.
+
+The oracle is what every GPU parity test compares against, so it is pinned to
+things other than itself first: finite differences, a hand-derived worked
+example, closed forms, invariants, an independent library forward and
+structural reductions (see ``tests/oracle_pins.py``).  The mutation test then
+plants plausible mistakes in a copy of the C source and checks that each one
+fails at least one pin.
+"""
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import oracle_pins
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda p: p.__name__)
+def test_pin(oracle_mod, pin):
+    pin(oracle_mod.default())
+
+
+def test_thread_count_does_not_change_bits(oracle_mod):
+    rng = np.random.default_rng(40)
+    q = rng.standard_normal((2, 33, 4, 8))
+    k = rng.standard_normal((2, 33, 2, 8))
+    v = rng.standard_normal((2, 33, 2, 8))
+    do = rng.standard_normal((2, 33, 4, 8))
+    a = oracle_mod.backward(q, k, v, do, 0.35, True, nthreads=1)
+    b = oracle_mod.backward(q, k, v, do, 0.35, True, nthreads=4)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+def test_rejects_bad_shapes(oracle_mod):
+    rng = np.random.default_rng(41)
+    q = rng.standard_normal((1, 4, 3, 2))
+    k = rng.standard_normal((1, 4, 2, 2))   # Hq % Hkv != 0
+    with pytest.raises(ValueError):
+        oracle_mod.forward(q, k, k, 1.0)
+    q = rng.standard_normal((1, 4, 2, 2))
+    k = rng.standard_normal((1, 4, 1, 2))
+    with pytest.raises(ValueError):
+        oracle_mod.backward_sampled(q, k, k, q, 1.0, qrows=[(0, 4, 0)])  # row out of range
+
+
+# Each mutant replaces one exact snippet of fa_oracle.c.
+MUTANTS = {
+    "dS sign of D": ("ds = pij * (dprob(p, b, h, i, j) - dv);",
+                     "ds = pij * (dprob(p, b, h, i, j) + dv);"),
+    "dS drops D in dK": ("double ds = pij * (dprob(p, b, h, i, j) - dvec_g[g][i]);",
+                         "double ds = pij * dprob(p, b, h, i, j);"),
+    "dK without scale": ("for (int d = 0; d < D; ++d) dk_out[d] *= p->scale;", ""),
+    "dQ without scale": ("for (int d = 0; d < D; ++d) dq_out[d] *= p->scale;", ""),
+    "dV uses dS": ("dv_out[d] += pij * doi[d];", "dv_out[d] += ds * doi[d];"),
+    "dK uses dO": ("dk_out[d] += ds * qi[d];", "dk_out[d] += ds * doi[d];"),
+    "top-left causal": ("if (p->causal && j > i + (lk - lq)) return 0;",
+                        "if (p->causal && j > i) return 0;"),
+    "causal off by one": ("if (p->causal && j > i + (lk - lq)) return 0;",
+                          "if (p->causal && j >= i + (lk - lq)) return 0;"),
+    "GQA head mapping": ("int hk = h / p->G;\n    return p->scale",
+                         "int hk = h % p->Hkv;\n    return p->scale"),
+    "Dv from q": ("return dot(doi, o_scratch, p->D);", "return dot(doi, p->q + row_q(p, b, i, h), p->D);"),
+    "LSE drops max shift": ("double lse = m + log(sum);", "double lse = log(sum);"),
+    "score without scale": ("return p->scale * dot(", "return dot("),
+    "varlen lse index": ("if (p->cu_q) return (long)h * p->total_q + p->cu_q[b] + s;",
+                         "if (p->cu_q) return (long)h * p->total_q + s;"),
+}
+
+
+@pytest.mark.parametrize("name", list(MUTANTS))
+def test_planted_mistake_is_caught(oracle_mod, tmp_path, name):
+    old, new = MUTANTS[name]
+    src = open(oracle_mod.SOURCE).read()
+    assert src.count(old) == 1, "mutant snippet must match exactly once: %r" % old
+    mpath = tmp_path / "mutant.c"
+    mpath.write_text(src.replace(old, new))
+    lib = oracle_mod.compile_library(str(mpath), str(tmp_path / "libmutant.so"), openmp=False)
+    # a subprocess, so that a mutant that crashes counts as caught without
+    # taking the test run down
+    res = subprocess.run([sys.executable, os.path.join(HERE, "oracle_pins.py"), lib],
+                         capture_output=True, text=True, timeout=300)
+    if res.returncode != 0:
+        return
+    failed = json.loads(res.stdout.strip().splitlines()[-1])
+    assert failed, "planted mistake %r passed every pin" % name
