@@ -1,0 +1,239 @@
+"""GB300 (sm_103a) fused exact-softmax attention backward.
+
+Thin ctypes binding of the C ABI in ``include/fa.h`` (``libfa_gb300.so``,
+built in-tree by ``attention_backward_preprocess_gb300.build``).  This module
+only marshals arguments: every step of the computation runs in the library's
+CUDA kernels.  PyTorch supplies device memory and streams.  There is no CPU
+fallback: when the library is missing or cannot load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfa_gb300.so")
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+FA_BF16, FA_FP16 = 0, 1
+
+# entry points declared in include/fa.h and include/fa_selftest.h
+EXPORTED = [
+    "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_with_workspace", "fa_bwd_preprocess",
+    "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_workspace_layout", "fa_fwd",
+    "fa_device_status", "fa_set_wait_timeout_ns", "fa_status_string",
+    "fa_selftest_umma", "fa_selftest_semaphore",
+]
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s failed: %s (status %d)" % (what, status_string(status), status))
+
+
+_lib = None
+_lock = threading.Lock()
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+_SHAPE = [_i] * 6   # B, Sq, Sk, Hq, Hkv, D
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                "libfa_gb300.so is not built (run attention_backward_preprocess_gb300.build."
+                "build()); there is no fallback path")
+        L = ctypes.CDLL(LIB_PATH)
+        L.fa_bwd.argtypes = [_vp] * 9 + _SHAPE + [_f, _i, _vp, _vp, _i, _i, _vp]
+        L.fa_bwd_workspace_bytes.argtypes = _SHAPE + [_i, _i]
+        L.fa_bwd_workspace_bytes.restype = _sz
+        L.fa_bwd_with_workspace.argtypes = ([_vp] * 9 + _SHAPE + [_f, _i, _vp, _vp, _i, _i, _vp,
+                                                                  _sz, _vp])
+        L.fa_bwd_preprocess.argtypes = [_vp] * 3 + _SHAPE + [_vp, _vp, _i, _i, _vp, _sz, _vp]
+        L.fa_bwd_main.argtypes = [_vp] * 5 + _SHAPE + [_f, _i, _vp, _vp, _i, _i, _vp, _sz, _vp]
+        L.fa_bwd_postprocess.argtypes = [_vp] + _SHAPE + [_f, _vp, _vp, _i, _i, _vp, _sz, _vp]
+        L.fa_bwd_workspace_layout.argtypes = _SHAPE + [_i, _i] + [ctypes.POINTER(_sz)] * 4
+        L.fa_fwd.argtypes = [_vp] * 5 + _SHAPE + [_f, _i, _vp, _vp, _i, _vp]
+        L.fa_device_status.argtypes = [_vp, _vp]
+        L.fa_set_wait_timeout_ns.argtypes = [ctypes.c_longlong]
+        L.fa_set_wait_timeout_ns.restype = ctypes.c_longlong
+        L.fa_status_string.argtypes = [_i]
+        L.fa_status_string.restype = ctypes.c_char_p
+        L.fa_selftest_umma.argtypes = [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]
+        L.fa_selftest_semaphore.argtypes = [_vp, _i, ctypes.c_longlong, _vp, _vp]
+        for name in ("fa_bwd", "fa_bwd_with_workspace", "fa_bwd_preprocess", "fa_bwd_main",
+                     "fa_bwd_postprocess", "fa_bwd_workspace_layout", "fa_fwd",
+                     "fa_device_status", "fa_selftest_umma", "fa_selftest_semaphore"):
+            getattr(L, name).restype = _i
+        _lib = L
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().fa_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != FA_OK:
+        raise FaError(status, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    if t.dtype == torch.float16:
+        return FA_FP16
+    raise ValueError("q/k/v/o/dout must be bf16 or fp16, got %s" % t.dtype)
+
+
+def _shape(q, k, cu_q, max_seqlen_q, max_seqlen_k):
+    """(B, Sq, Sk, Hq, Hkv, D) from dense [B,S,H,D] or packed [total,H,D] tensors."""
+    if cu_q is None:
+        if q.dim() != 4 or k.dim() != 4:
+            raise ValueError("dense q/k are [B, S, H, D]")
+        B, Sq, Hq, D = q.shape
+        return B, Sq, k.shape[1], Hq, k.shape[2], D
+    if q.dim() != 3 or k.dim() != 3 or max_seqlen_q is None or max_seqlen_k is None:
+        raise ValueError("varlen q/k are [total, H, D] with max_seqlen_q / max_seqlen_k")
+    return cu_q.numel() - 1, int(max_seqlen_q), int(max_seqlen_k), q.shape[1], k.shape[1], q.shape[2]
+
+
+def default_scale(D: int) -> float:
+    return 1.0 / (D ** 0.5)
+
+
+def fa_fwd(q, k, v, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seqlens_k=None,
+           max_seqlen_q=None, max_seqlen_k=None, stream=None):
+    """Untimed forward helper: returns (o, lse); lse fp32 [B,Hq,Sq] or [Hq,total_q]."""
+    B, Sq, Sk, Hq, Hkv, D = _shape(q, k, cu_seqlens_q, max_seqlen_q, max_seqlen_k)
+    scale = default_scale(D) if softmax_scale is None else float(softmax_scale)
+    o = torch.empty_like(q)
+    if cu_seqlens_q is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    else:
+        lse = torch.empty((Hq, q.shape[0]), dtype=torch.float32, device=q.device)
+    st = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Sq, Sk, Hq, Hkv, D,
+                      scale, int(bool(causal)), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                      _dtype_code(q), _stream(stream))
+    _check(st, "fa_fwd")
+    return o, lse
+
+
+def fa_bwd(q, k, v, o, dout, lse, causal=False, softmax_scale=None, cu_seqlens_q=None,
+           cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, deterministic=False,
+           dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward pass through the C ABI; returns (dq, dk, dv).
+
+    Outputs are allocated when not given.  ``workspace`` (a uint8 CUDA tensor
+    of at least ``workspace_bytes(...)``) selects fa_bwd_with_workspace,
+    otherwise the library's own workspace is used.
+    """
+    B, Sq, Sk, Hq, Hkv, D = _shape(q, k, cu_seqlens_q, max_seqlen_q, max_seqlen_k)
+    scale = default_scale(D) if softmax_scale is None else float(softmax_scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+            _ptr(dv), B, Sq, Sk, Hq, Hkv, D, scale, int(bool(causal)), _ptr(cu_seqlens_q),
+            _ptr(cu_seqlens_k), int(bool(deterministic)), _dtype_code(q)]
+    if workspace is None:
+        st = lib().fa_bwd(*args, _stream(stream))
+        _check(st, "fa_bwd")
+    else:
+        st = lib().fa_bwd_with_workspace(*args, _ptr(workspace), workspace.numel(),
+                                          _stream(stream))
+        _check(st, "fa_bwd_with_workspace")
+    return dq, dk, dv
+
+
+def workspace_bytes(B, Sq, Sk, Hq, Hkv, D, varlen=False, deterministic=False) -> int:
+    return int(lib().fa_bwd_workspace_bytes(B, Sq, Sk, Hq, Hkv, D, int(bool(varlen)),
+                                            int(bool(deterministic))))
+
+
+def workspace_layout(B, Sq, Sk, Hq, Hkv, D, varlen=False, deterministic=False) -> dict:
+    """fp32-element offsets of Dv, LSE2 and the dQ accumulator inside a workspace."""
+    vals = [_sz() for _ in range(4)]
+    st = lib().fa_bwd_workspace_layout(B, Sq, Sk, Hq, Hkv, D, int(bool(varlen)),
+                                       int(bool(deterministic)), *[ctypes.byref(x) for x in vals])
+    _check(st, "fa_bwd_workspace_layout")
+    return dict(dvec=vals[0].value, lse2=vals[1].value, dqacc=vals[2].value, rows=vals[3].value)
+
+
+def fa_bwd_stages(q, k, v, o, dout, lse, workspace, causal=False, softmax_scale=None,
+                  cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None,
+                  deterministic=False, dq=None, dk=None, dv=None, stages=("pre", "main", "post"),
+                  stream=None):
+    """Runs the chosen stages (preprocess / main / postprocess) on ``workspace``."""
+    B, Sq, Sk, Hq, Hkv, D = _shape(q, k, cu_seqlens_q, max_seqlen_q, max_seqlen_k)
+    scale = default_scale(D) if softmax_scale is None else float(softmax_scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    shape = [B, Sq, Sk, Hq, Hkv, D]
+    cu = [_ptr(cu_seqlens_q), _ptr(cu_seqlens_k)]
+    det, dt = int(bool(deterministic)), _dtype_code(q)
+    ws = [_ptr(workspace), workspace.numel(), _stream(stream)]
+    L = lib()
+    if "pre" in stages:
+        _check(L.fa_bwd_preprocess(_ptr(o), _ptr(dout), _ptr(lse), *shape, *cu, det, dt, *ws),
+               "fa_bwd_preprocess")
+    if "main" in stages:
+        _check(L.fa_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(dk), _ptr(dv), *shape, scale,
+                             int(bool(causal)), *cu, det, dt, *ws), "fa_bwd_main")
+    if "post" in stages:
+        _check(L.fa_bwd_postprocess(_ptr(dq), *shape, scale, *cu, det, dt, *ws),
+               "fa_bwd_postprocess")
+    return dq, dk, dv
+
+
+def device_status(workspace=None, stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device error status."""
+    return int(lib().fa_device_status(_ptr(workspace), _stream(stream)))
+
+
+def set_wait_timeout_ns(ns: int) -> int:
+    return int(lib().fa_set_wait_timeout_ns(int(ns)))
+
+
+def selftest_umma(mode: int, A: torch.Tensor, B: torch.Tensor, N: int, K: int, stream=None):
+    """One-CTA tcgen05 GEMM in one of the kernel's operand forms (see fa_selftest.h)."""
+    C = torch.empty((128, N), dtype=torch.float32, device=A.device)
+    err = torch.zeros(1, dtype=torch.int32, device=A.device)
+    st = lib().fa_selftest_umma(mode, N, K, int(A.dtype == torch.bfloat16), _ptr(A), _ptr(B),
+                                _ptr(C), _ptr(err), _stream(stream))
+    if st != 0:
+        raise RuntimeError("fa_selftest_umma returned %d" % st)
+    return C, err
+
+
+def selftest_semaphore(sem: torch.Tensor, target: int, budget_ns: int, stream=None):
+    err = torch.zeros(1, dtype=torch.int32, device=sem.device)
+    st = lib().fa_selftest_semaphore(_ptr(sem), int(target), int(budget_ns), _ptr(err),
+                                     _stream(stream))
+    if st != 0:
+        raise RuntimeError("fa_selftest_semaphore returned %d" % st)
+    return err

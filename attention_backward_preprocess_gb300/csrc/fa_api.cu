@@ -1,0 +1,440 @@
+// fa_api.cu -- the C ABI declared in include/fa.h: argument validation,
+// workspace planning, TMA tensor-map encoding and the kernel launches.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fa.h"
+#include "fa_params.h"
+
+namespace fa {
+cudaError_t launch_schedule(const BwdParams &p, cudaStream_t stream);
+cudaError_t launch_preprocess(const BwdParams &p, int bf16, cudaStream_t stream);
+cudaError_t launch_postprocess(const BwdParams &p, int bf16, cudaStream_t stream);
+cudaError_t launch_fwd(const BwdParams &p, void *o, float *lse, int bf16, cudaStream_t stream);
+cudaError_t launch_bwd_main(const BwdParams &p, const CUtensorMap &q, const CUtensorMap &k,
+                            const CUtensorMap &v, const CUtensorMap &dout, int bf16, int grid,
+                            cudaStream_t stream);
+int main_block_m(int D);
+}  // namespace fa
+
+namespace {
+
+std::atomic<long long> g_budget_ns{2000000000LL};
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Layout {
+    size_t err, ntiles, tiles, dvec, lse2, dqacc, sem, total;  // byte offsets / size
+    long long rows, rows_per_head;
+    int sq_round, max_tiles;
+};
+
+bool plan(int B, int Sq, int Sk, int Hq, int Hkv, int D, int varlen, int deterministic,
+          Layout *L) {
+    if (B <= 0 || Sq <= 0 || Sk <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv) return false;
+    const long long T = fa::kRowTile;
+    L->sq_round = (int)round_up((size_t)Sq, T);
+    if (varlen) {
+        L->rows_per_head = (long long)round_up((size_t)B * ((size_t)Sq + T), T);
+        L->rows = (long long)Hq * L->rows_per_head;
+    } else {
+        L->rows_per_head = L->sq_round;
+        L->rows = (long long)B * Hq * L->sq_round;
+    }
+    const long long tiles = (long long)B * ((Sk + fa::kBlockN - 1) / fa::kBlockN) * Hkv;
+    if (tiles > (1LL << 30)) return false;
+    L->max_tiles = (int)tiles;
+    size_t off = 0;
+    L->err = off;       off += 256;
+    L->ntiles = off;    off += 256;
+    L->tiles = off;     off = round_up(off + (size_t)tiles * 16, 256);
+    L->dvec = off;      off = round_up(off + (size_t)L->rows * 4, 256);
+    L->lse2 = off;      off = round_up(off + (size_t)L->rows * 4, 256);
+    L->dqacc = off;     off = round_up(off + (size_t)L->rows * D * 4, 256);
+    L->sem = off;       off = round_up(off + (deterministic ? (size_t)(L->rows / 64) * 4 : 0), 256);
+    L->total = off;
+    return true;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status check_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (major != 10 || minor != 3) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+fa_status check_shape(int B, int Sq, int Sk, int Hq, int Hkv, int D, fa_dtype dtype,
+                      const int *cu_q, const int *cu_k) {
+    if (B <= 0 || Sq <= 0 || Sk <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return FA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+    if ((cu_q == nullptr) != (cu_k == nullptr)) return FA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_UNSUPPORTED;
+    // TMA coordinates are 32-bit
+    if ((long long)B * Sq > (1LL << 31) - 1 || (long long)B * Sk > (1LL << 31) - 1)
+        return FA_ERR_INVALID_ARG;
+    return FA_OK;
+}
+
+// ----------------------------------------------------------- tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// 4-D map over a [batch, rows, heads, D] 16-bit tensor (d innermost), box of
+// 64 d x 1 head x box_rows rows, 128-byte swizzle, zero fill out of bounds.
+bool encode_rows_map(CUtensorMap *m, const void *base, int D, int H, long long rows, int batch,
+                     int box_rows, int bf16) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows, (cuuint64_t)batch};
+    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2,
+                                   (cuuint64_t)rows * H * D * 2};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                    const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------- library-owned workspace
+struct DeviceWs {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_ws_mutex;
+std::vector<DeviceWs> g_ws;
+
+fa_status library_workspace(size_t need, cudaStream_t stream, void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_ws_mutex);
+    if ((int)g_ws.size() <= dev) g_ws.resize(dev + 1);
+    DeviceWs &w = g_ws[dev];
+    if (w.bytes < need) {
+        if (w.ptr) {
+            if (cudaFreeAsync(w.ptr, stream) != cudaSuccess) return FA_ERR_CUDA;
+            w.ptr = nullptr;
+            w.bytes = 0;
+        }
+        size_t grow = round_up(need + need / 8, 1 << 21);
+        if (cudaMallocAsync(&w.ptr, grow, stream) != cudaSuccess) return FA_ERR_CUDA;
+        w.bytes = grow;
+    }
+    *out = w.ptr;
+    return FA_OK;
+}
+
+void *library_workspace_peek() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    std::lock_guard<std::mutex> lk(g_ws_mutex);
+    if ((int)g_ws.size() <= dev) return nullptr;
+    return g_ws[dev].ptr;
+}
+
+// Totals of the packed varlen tensors (cu[B]); read back from the device.
+fa_status varlen_totals(const int *cu_q, const int *cu_k, int B, cudaStream_t stream,
+                        long long *tq, long long *tk) {
+    int h[2] = {0, 0};
+    if (cudaMemcpyAsync(&h[0], cu_q + B, sizeof(int), cudaMemcpyDeviceToHost, stream) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(&h[1], cu_k + B, sizeof(int), cudaMemcpyDeviceToHost, stream) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (h[0] < 0 || h[1] < 0) return FA_ERR_INVALID_ARG;
+    *tq = h[0];
+    *tk = h[1];
+    return FA_OK;
+}
+
+struct Prepared {
+    fa::BwdParams p;
+    Layout L;
+    long long total_q, total_k;
+};
+
+fa_status prepare(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                  const float *lse, void *dq, void *dk, void *dv, int B, int Sq, int Sk, int Hq,
+                  int Hkv, int D, float scale, int causal, const int *cu_q, const int *cu_k,
+                  int deterministic, fa_dtype dtype, void *ws, size_t ws_bytes,
+                  cudaStream_t stream, Prepared *out) {
+    fa_status st = check_shape(B, Sq, Sk, Hq, Hkv, D, dtype, cu_q, cu_k);
+    if (st != FA_OK) return st;
+    if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return FA_ERR_INVALID_ARG;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return FA_ERR_INVALID_ARG;
+    Layout L;
+    if (!plan(B, Sq, Sk, Hq, Hkv, D, cu_q != nullptr, deterministic, &L)) return FA_ERR_INVALID_ARG;
+    if (ws_bytes < L.total) return FA_ERR_INVALID_ARG;
+    st = check_device();
+    if (st != FA_OK) return st;
+    long long tq = (long long)B * Sq, tk = (long long)B * Sk;
+    if (cu_q) {
+        st = varlen_totals(cu_q, cu_k, B, stream, &tq, &tk);
+        if (st != FA_OK) return st;
+    }
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    fa::BwdParams &p = out->p;
+    std::memset(&p, 0, sizeof(p));
+    p.q = q; p.k = k; p.v = v; p.o = o; p.dout = dout; p.lse = lse;
+    p.dq = dq; p.dk = dk; p.dv = dv;
+    p.B = B; p.Sq = Sq; p.Sk = Sk; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.G = Hq / Hkv;
+    p.scale = scale;
+    p.scale_log2 = scale * kLog2e;
+    p.causal = causal ? 1 : 0;
+    p.deterministic = deterministic ? 1 : 0;
+    p.varlen = cu_q != nullptr;
+    p.cu_q = cu_q; p.cu_k = cu_k;
+    p.err = reinterpret_cast<int *>(w + L.err);
+    p.ntiles = reinterpret_cast<int *>(w + L.ntiles);
+    p.tiles = reinterpret_cast<int4 *>(w + L.tiles);
+    p.max_tiles = L.max_tiles;
+    p.dvec = reinterpret_cast<float *>(w + L.dvec);
+    p.lse2 = reinterpret_cast<float *>(w + L.lse2);
+    p.dqacc = reinterpret_cast<float *>(w + L.dqacc);
+    p.sem = deterministic ? reinterpret_cast<int *>(w + L.sem) : nullptr;
+    p.rows = L.rows;
+    p.rows_per_head = L.rows_per_head;
+    p.sq_round = L.sq_round;
+    p.budget_ns = g_budget_ns.load();
+    out->L = L;
+    out->total_q = tq;
+    out->total_k = tk;
+    return FA_OK;
+}
+
+fa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+fa_status run_preprocess(const Prepared &P, fa_dtype dtype, cudaStream_t stream) {
+    if (cudaMemsetAsync(P.p.err, 0, sizeof(int), stream) != cudaSuccess) return FA_ERR_CUDA;
+    return cuda_status(fa::launch_preprocess(P.p, dtype == FA_BF16, stream));
+}
+
+fa_status run_main(const Prepared &P, fa_dtype dtype, cudaStream_t stream) {
+    const fa::BwdParams &p = P.p;
+    const int bm = fa::main_block_m(p.D);
+    const int bf16 = dtype == FA_BF16;
+    CUtensorMap mq, mk, mv, mdo;
+    const long long rq = p.varlen ? P.total_q : p.Sq, rk = p.varlen ? P.total_k : p.Sk;
+    const int nb = p.varlen ? 1 : p.B;
+    if (rq <= 0 || rk <= 0) return FA_ERR_INVALID_ARG;
+    if (!encode_rows_map(&mq, p.q, p.D, p.Hq, rq, nb, bm, bf16) ||
+        !encode_rows_map(&mdo, p.dout, p.D, p.Hq, rq, nb, bm, bf16) ||
+        !encode_rows_map(&mk, p.k, p.D, p.Hkv, rk, nb, fa::kBlockN, bf16) ||
+        !encode_rows_map(&mv, p.v, p.D, p.Hkv, rk, nb, fa::kBlockN, bf16))
+        return FA_ERR_CUDA;
+    cudaError_t e = fa::launch_schedule(p, stream);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+    const int grid = (int)std::min<long long>(p.max_tiles, sm_count());
+    return cuda_status(fa::launch_bwd_main(p, mq, mk, mv, mdo, bf16, grid, stream));
+}
+
+fa_status run_postprocess(const Prepared &P, fa_dtype dtype, cudaStream_t stream) {
+    return cuda_status(fa::launch_postprocess(P.p, dtype == FA_BF16, stream));
+}
+
+fa_status read_error_word(int *err_dev, cudaStream_t stream, bool clear) {
+    int h = 0;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaMemcpy(&h, err_dev, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (clear && h != 0 && cudaMemset(err_dev, 0, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+    return h ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *fa_status_string(fa_status s) {
+    switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+long long fa_set_wait_timeout_ns(long long ns) {
+    if (ns <= 0) return g_budget_ns.load();
+    return g_budget_ns.exchange(ns);
+}
+
+size_t fa_bwd_workspace_bytes(int B, int Sq, int Sk, int Hq, int Hkv, int D, int varlen,
+                              int deterministic) {
+    Layout L;
+    if (D != 64 && D != 128) return 0;
+    if (!plan(B, Sq, Sk, Hq, Hkv, D, varlen, deterministic, &L)) return 0;
+    return L.total;
+}
+
+fa_status fa_bwd_workspace_layout(int B, int Sq, int Sk, int Hq, int Hkv, int D, int varlen,
+                                  int deterministic, size_t *dvec_off, size_t *lse2_off,
+                                  size_t *dqacc_off, size_t *rows) {
+    Layout L;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if (!plan(B, Sq, Sk, Hq, Hkv, D, varlen, deterministic, &L)) return FA_ERR_INVALID_ARG;
+    if (dvec_off) *dvec_off = L.dvec / 4;
+    if (lse2_off) *lse2_off = L.lse2 / 4;
+    if (dqacc_off) *dqacc_off = L.dqacc / 4;
+    if (rows) *rows = (size_t)L.rows;
+    return FA_OK;
+}
+
+fa_status fa_bwd_preprocess(const void *o, const void *dout, const float *lse, int B, int Sq,
+                            int Sk, int Hq, int Hkv, int D, const int *cu_seqlens_q,
+                            const int *cu_seqlens_k, int deterministic, fa_dtype dtype,
+                            void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!o || !dout || !lse) return FA_ERR_INVALID_ARG;
+    Prepared P;
+    fa_status st = prepare(nullptr, nullptr, nullptr, o, dout, lse, nullptr, nullptr, nullptr, B,
+                           Sq, Sk, Hq, Hkv, D, 1.f, 0, cu_seqlens_q, cu_seqlens_k, deterministic,
+                           dtype, workspace, workspace_bytes, stream, &P);
+    if (st != FA_OK) return st;
+    return run_preprocess(P, dtype, stream);
+}
+
+fa_status fa_bwd_main(const void *q, const void *k, const void *v, void *dk, void *dv, int B,
+                      int Sq, int Sk, int Hq, int Hkv, int D, float softmax_scale, int causal,
+                      const int *cu_seqlens_q, const int *cu_seqlens_k, int deterministic,
+                      fa_dtype dtype, void *workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+    if (!q || !k || !v || !dk || !dv) return FA_ERR_INVALID_ARG;
+    Prepared P;
+    fa_status st = prepare(q, k, v, nullptr, nullptr, nullptr, nullptr, dk, dv, B, Sq, Sk, Hq, Hkv,
+                           D, softmax_scale, causal, cu_seqlens_q, cu_seqlens_k, deterministic,
+                           dtype, workspace, workspace_bytes, stream, &P);
+    if (st != FA_OK) return st;
+    return run_main(P, dtype, stream);
+}
+
+fa_status fa_bwd_postprocess(void *dq, int B, int Sq, int Sk, int Hq, int Hkv, int D,
+                             float softmax_scale, const int *cu_seqlens_q,
+                             const int *cu_seqlens_k, int deterministic, fa_dtype dtype,
+                             void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!dq) return FA_ERR_INVALID_ARG;
+    Prepared P;
+    fa_status st = prepare(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, dq, nullptr,
+                           nullptr, B, Sq, Sk, Hq, Hkv, D, softmax_scale, 0, cu_seqlens_q,
+                           cu_seqlens_k, deterministic, dtype, workspace, workspace_bytes, stream,
+                           &P);
+    if (st != FA_OK) return st;
+    return run_postprocess(P, dtype, stream);
+}
+
+fa_status fa_bwd_with_workspace(const void *q, const void *k, const void *v, const void *o,
+                                const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                                int B, int Sq, int Sk, int Hq, int Hkv, int D,
+                                float softmax_scale, int causal, const int *cu_seqlens_q,
+                                const int *cu_seqlens_k, int deterministic, fa_dtype dtype,
+                                void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+    Prepared P;
+    fa_status st = prepare(q, k, v, o, dout, lse, dq, dk, dv, B, Sq, Sk, Hq, Hkv, D,
+                           softmax_scale, causal, cu_seqlens_q, cu_seqlens_k, deterministic, dtype,
+                           workspace, workspace_bytes, stream, &P);
+    if (st != FA_OK) return st;
+    if ((st = run_preprocess(P, dtype, stream)) != FA_OK) return st;
+    if ((st = run_main(P, dtype, stream)) != FA_OK) return st;
+    if ((st = run_postprocess(P, dtype, stream)) != FA_OK) return st;
+    if (deterministic) return read_error_word(P.p.err, stream, false);
+    return FA_OK;
+}
+
+fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                 const float *lse, void *dq, void *dk, void *dv, int B, int Sq, int Sk, int Hq,
+                 int Hkv, int D, float softmax_scale, int causal, const int *cu_seqlens_q,
+                 const int *cu_seqlens_k, int deterministic, fa_dtype dtype,
+                 cudaStream_t stream) {
+    fa_status st = check_shape(B, Sq, Sk, Hq, Hkv, D, dtype, cu_seqlens_q, cu_seqlens_k);
+    if (st != FA_OK) return st;
+    const size_t need = fa_bwd_workspace_bytes(B, Sq, Sk, Hq, Hkv, D, cu_seqlens_q != nullptr,
+                                               deterministic);
+    if (need == 0) return FA_ERR_INVALID_ARG;
+    void *ws = nullptr;
+    st = library_workspace(need, stream, &ws);
+    if (st != FA_OK) return st;
+    return fa_bwd_with_workspace(q, k, v, o, dout, lse, dq, dk, dv, B, Sq, Sk, Hq, Hkv, D,
+                                 softmax_scale, causal, cu_seqlens_q, cu_seqlens_k, deterministic,
+                                 dtype, ws, need, stream);
+}
+
+fa_status fa_device_status(void *workspace, cudaStream_t stream) {
+    void *ws = workspace ? workspace : library_workspace_peek();
+    if (!ws) {
+        return cudaStreamSynchronize(stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    }
+    return read_error_word(reinterpret_cast<int *>(ws), stream, true);
+}
+
+fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Sq,
+                 int Sk, int Hq, int Hkv, int D, float softmax_scale, int causal,
+                 const int *cu_seqlens_q, const int *cu_seqlens_k, fa_dtype dtype,
+                 cudaStream_t stream) {
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    fa_status st = check_shape(B, Sq, Sk, Hq, Hkv, D, dtype, cu_seqlens_q, cu_seqlens_k);
+    if (st != FA_OK) return st;
+    if (!(std::isfinite(softmax_scale) && softmax_scale > 0.f)) return FA_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, o, lse};
+    for (const void *ptr : ptrs)
+        if (!aligned16(ptr)) return FA_ERR_INVALID_ARG;
+    if ((st = check_device()) != FA_OK) return st;
+    fa::BwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.q = q; p.k = k; p.v = v;
+    p.B = B; p.Sq = Sq; p.Sk = Sk; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.G = Hq / Hkv;
+    p.scale = softmax_scale;
+    p.scale_log2 = softmax_scale * kLog2e;
+    p.causal = causal ? 1 : 0;
+    p.varlen = cu_seqlens_q != nullptr;
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    return cuda_status(fa::launch_fwd(p, o, lse, dtype == FA_BF16, stream));
+}
+
+}  // extern "C"

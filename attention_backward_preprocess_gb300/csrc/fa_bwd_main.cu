@@ -1,0 +1,548 @@
+// fa_bwd_main.cu -- the fused attention-backward main kernel for sm_103a.
+//
+// One work unit = (sequence b, K/V column block of 128 keys, kv head hk).  The
+// unit keeps K and V resident in shared memory and its dK, dV accumulators in
+// tensor memory, and streams the query-row blocks of every query head of the
+// GQA group (the K/V-stationary loop of the Composable Kernel page
+// "block_fmha_bwd_dq_dk_dv_pipeline_trload_kr_ktr_vr.hpp", whose hot loop runs
+// over the Q row blocks of one K/V tile).  Per row block of BM queries:
+//
+//   S^T  = K Q^T          tcgen05.mma SS, M=128 keys, N=BM      (STAGE 1)
+//   P^T  = exp2(S^T c log2e - LSE2)  softmax warps, mask on diagonal tiles
+//                                                                (STAGE 2)
+//   dP^T = V dO^T         tcgen05.mma SS                          (STAGE 4)
+//   dV  += P^T dO         tcgen05.mma TS (P^T bf16 in TMEM)       (STAGE 3)
+//   dS^T = P^T o (dP^T - Dv)  softmax warps                       (STAGE 5)
+//   dK  += dS^T Q         tcgen05.mma TS (dS^T bf16 in TMEM)      (STAGE 6)
+//   dQ   = dS K           tcgen05.mma SS (dS^T in smem), added into the fp32
+//                         accumulator by coalesced red.global.add (STAGE 7;
+//                         the atomic "update_tile" path), or in a fixed
+//                         n-block order through per-row-block semaphores in
+//                         deterministic mode (the wait_eq / arrive_inc
+//                         pattern of CollectiveEpilogueBwdGQA in
+//                         "flash-attention/hopper/epilogue_bwd.hpp")
+//
+// and at the end dK * c, dV are written out (CollectiveEpilogueBwd::store;
+// zeros for a unit with no visible query, store_zero).
+//
+// Warp roles (14 warps):
+//   warp 0        TMA producer: K/V once per unit, Q/dO/LSE2/Dv per row block
+//   warp 1        TMEM allocator and single-thread MMA issuer
+//   warps 2-5     dQ reducers (one TMEM lane quarter each)
+//   warps 6-13    softmax / elementwise, two groups of four; group g handles
+//                 query columns [g BM/2, (g+1) BM/2) of every key row, and
+//                 in the epilogue group 0 writes dK, group 1 writes dV
+// Every wait is bounded (see fa_device.cuh); a wait that gives up sets the
+// CTA abort flag and the device error word and the CTA winds down.
+#include "fa_device.cuh"
+#include "fa_params.h"
+
+namespace fa {
+namespace {
+
+template <int kD, typename T>
+struct MainCfg {
+    static constexpr int D = kD;
+    static constexpr int BN = kBlockN;                 // keys per unit
+    static constexpr int BM = (kD == 128) ? 64 : 128;  // queries per step
+    // dQ GEMM orientation: the MMA's M (=128) is d when D = 128 (dQ^T = K^T dS^T,
+    // TMEM lanes = d) and the query row when D = 64 (dQ = dS K, lanes = query).
+    static constexpr bool kDqT = (kD == 128);
+    static constexpr int kStages = 2;
+    static constexpr int kThreads = 14 * 32;
+    // tensor-memory columns
+    static constexpr int TM_DK = 0;
+    static constexpr int TM_DV = D;
+    static constexpr int TM_S = 2 * D;            // S^T fp32, then P^T bf16 in place
+    static constexpr int TM_DP = 2 * D + BM;      // dP^T fp32, then dS^T bf16 in place
+    static constexpr int TM_DQ = 2 * D + 2 * BM;  // 64 fp32 columns
+    static constexpr int TM_COLS = 512;
+    static_assert(TM_DQ + 64 <= TM_COLS, "tensor memory overflow");
+    // shared memory (byte offsets from a 1024-aligned base)
+    static constexpr int KV_BYTES = BN * D * 2;
+    static constexpr int QO_BYTES = BM * D * 2;
+    static constexpr int DS_BYTES = BN * BM * 2;
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + KV_BYTES;
+    static constexpr int OFF_Q = OFF_V + KV_BYTES;
+    static constexpr int OFF_DO = OFF_Q + kStages * QO_BYTES;
+    static constexpr int OFF_DS = OFF_DO + kStages * QO_BYTES;
+    static constexpr int OFF_LSE = OFF_DS + DS_BYTES;
+    static constexpr int OFF_DV = OFF_LSE + kStages * BM * 4;
+    static constexpr int OFF_BAR = OFF_DV + kStages * BM * 4;
+    static constexpr int NUM_BARS = 16 + 2 * kStages;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+    static constexpr uint32_t IDESC_S = make_idesc(128, BM, Cvt<T>::is_bf16, false, false);
+    static constexpr uint32_t IDESC_KV = make_idesc(128, D, Cvt<T>::is_bf16, false, true);
+    static constexpr uint32_t IDESC_DQ = make_idesc(128, 64, Cvt<T>::is_bf16, true, true);
+};
+
+// barrier indices
+enum {
+    B_KV_FULL = 0, B_KV_EMPTY, B_S_FULL, B_P_FULL, B_DP_FULL, B_DS_FULL, B_DQ_FULL, B_DQ_EMPTY,
+    B_ACC_FULL, B_ACC_EMPTY, B_DRAIN, B_STAGE0
+};
+
+struct Unit {
+    int b, n_block, hk;
+    int lq, lk;
+    int q_row0, k_row0, bidx;   // TMA row offset and batch coordinate
+    int m_begin, nm, iters;     // row blocks [m_begin, m_begin + nm) per head; iters = G * nm
+};
+
+template <int BM>
+__device__ __forceinline__ Unit decode_unit(const BwdParams &p, int t) {
+    Unit u;
+    const int4 e = p.tiles[t];
+    u.b = e.x;
+    u.n_block = e.y;
+    u.hk = e.z;
+    if (p.varlen) {
+        u.q_row0 = p.cu_q[u.b];
+        u.k_row0 = p.cu_k[u.b];
+        u.lq = p.cu_q[u.b + 1] - u.q_row0;
+        u.lk = p.cu_k[u.b + 1] - u.k_row0;
+        u.bidx = 0;
+    } else {
+        u.q_row0 = 0;
+        u.k_row0 = 0;
+        u.lq = p.Sq;
+        u.lk = p.Sk;
+        u.bidx = u.b;
+    }
+    const int n0 = u.n_block * kBlockN;
+    int first_row = 0;
+    if (p.causal) first_row = max(0, n0 - (u.lk - u.lq));   // first query that sees key n0
+    u.m_begin = first_row / BM;
+    const int m_end = (u.lq + BM - 1) / BM;
+    u.nm = max(0, m_end - u.m_begin);
+    if (n0 >= u.lk) u.nm = 0;
+    u.iters = p.G * u.nm;
+    return u;
+}
+
+struct MainMaps {
+    CUtensorMap q, k, v, dout;
+};
+
+template <int kD, typename T>
+__global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
+    bwd_main_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ MainMaps maps) {
+    using C = MainCfg<kD, T>;
+    constexpr int D = C::D, BM = C::BM, BN = C::BN, S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + C::OFF_BAR;
+    auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 16);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        mbar_init(bar(B_KV_FULL), 1);
+        mbar_init(bar(B_KV_EMPTY), 1);
+        mbar_init(bar(B_S_FULL), 1);
+        mbar_init(bar(B_P_FULL), 8);
+        mbar_init(bar(B_DP_FULL), 1);
+        mbar_init(bar(B_DS_FULL), 8);
+        mbar_init(bar(B_DQ_FULL), 1);
+        mbar_init(bar(B_DQ_EMPTY), 4);
+        mbar_init(bar(B_ACC_FULL), 1);
+        mbar_init(bar(B_ACC_EMPTY), 8);
+        mbar_init(bar(B_DRAIN), 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar(B_STAGE0 + s), 1);          // full: producer expect_tx
+            mbar_init(bar(B_STAGE0 + S + s), 1 + 8);  // empty: MMA commit + 8 softmax warps
+        }
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&maps.q);
+        prefetch_tmap(&maps.k);
+        prefetch_tmap(&maps.v);
+        prefetch_tmap(&maps.dout);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtl w{abort_flag, p.err, p.budget_ns};
+    const int ntiles = *p.ntiles;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t kv_ph = 0, st_ph = 0;
+            int stage = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                const Unit u = decode_unit<BM>(p, t);
+                if (u.iters == 0) continue;
+                if (!(ok = mbar_wait(bar(B_KV_EMPTY), kv_ph ^ 1, w))) break;
+                kv_ph ^= 1;
+                mbar_arrive_expect_tx(bar(B_KV_FULL), 2 * C::KV_BYTES);
+                const int krow = u.k_row0 + u.n_block * BN;
+#pragma unroll
+                for (int h = 0; h < D / 64; ++h) {
+                    tma_load_4d(sbase + C::OFF_K + h * BN * 128, &maps.k, bar(B_KV_FULL), h * 64,
+                                u.hk, krow, u.bidx);
+                    tma_load_4d(sbase + C::OFF_V + h * BN * 128, &maps.v, bar(B_KV_FULL), h * 64,
+                                u.hk, krow, u.bidx);
+                }
+                for (int it = 0; it < u.iters; ++it) {
+                    const int g = it / u.nm, m = u.m_begin + it % u.nm;
+                    const int h = u.hk * p.G + g;
+                    if (!(ok = mbar_wait(bar(B_STAGE0 + S + stage), st_ph ^ 1, w))) break;
+                    const uint32_t full = bar(B_STAGE0 + stage);
+                    mbar_arrive_expect_tx(full, 2 * C::QO_BYTES + 2 * BM * 4);
+                    const int qrow = u.q_row0 + m * BM;
+#pragma unroll
+                    for (int hh = 0; hh < D / 64; ++hh) {
+                        tma_load_4d(sbase + C::OFF_Q + stage * C::QO_BYTES + hh * BM * 128, &maps.q,
+                                    full, hh * 64, h, qrow, u.bidx);
+                        tma_load_4d(sbase + C::OFF_DO + stage * C::QO_BYTES + hh * BM * 128,
+                                    &maps.dout, full, hh * 64, h, qrow, u.bidx);
+                    }
+                    const long long r0 = ws_row(p, u.b, h, m * BM);
+                    bulk_load(sbase + C::OFF_LSE + stage * BM * 4, p.lse2 + r0, BM * 4, full);
+                    bulk_load(sbase + C::OFF_DV + stage * BM * 4, p.dvec + r0, BM * 4, full);
+                    if (++stage == S) { stage = 0; st_ph ^= 1; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            uint32_t kv_ph = 0, st_ph = 0, p_ph = 0, ds_ph = 0, dq_ph = 0, acc_ph = 0;
+            int stage = 0;
+            bool ok = true;
+            const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sDS = sbase + C::OFF_DS;
+            const uint32_t dq_a = C::kDqT ? sK : sDS, dq_b = C::kDqT ? sDS : sK;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                const Unit u = decode_unit<BM>(p, t);
+                if (u.iters == 0) continue;
+                if (!(ok = mbar_wait(bar(B_KV_FULL), kv_ph, w))) break;
+                kv_ph ^= 1;
+                tc_fence_after();
+                for (int it = 0; it < u.iters; ++it) {
+                    if (!(ok = mbar_wait(bar(B_STAGE0 + stage), st_ph, w))) break;
+                    tc_fence_after();
+                    const uint32_t sQ = sbase + C::OFF_Q + stage * C::QO_BYTES;
+                    const uint32_t sDO = sbase + C::OFF_DO + stage * C::QO_BYTES;
+                    // S^T = K Q^T  (K-major A and B; a K step of 16 = 32 bytes in a half)
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
+                        const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
+                        mma_ss(tmem + C::TM_S, sw128_desc(sK + ko, 16, 1024),
+                               sw128_desc(sQ + qo, 16, 1024), C::IDESC_S, kk > 0);
+                    }
+                    mma_commit(bar(B_S_FULL));
+                    // dP^T = V dO^T
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
+                        const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
+                        mma_ss(tmem + C::TM_DP, sw128_desc(sV + ko, 16, 1024),
+                               sw128_desc(sDO + qo, 16, 1024), C::IDESC_S, kk > 0);
+                    }
+                    mma_commit(bar(B_DP_FULL));
+                    if (it == 0) {
+                        if (!(ok = mbar_wait(bar(B_ACC_EMPTY), acc_ph ^ 1, w))) break;
+                        acc_ph ^= 1;
+                    }
+                    if (!(ok = mbar_wait(bar(B_P_FULL), p_ph, w))) break;
+                    p_ph ^= 1;
+                    tc_fence_after();
+                    // dV += P^T dO  (P^T bf16 in TMEM; dO MN-major: K step = 16 rows = 2048 B)
+#pragma unroll
+                    for (int kk = 0; kk < BM / 16; ++kk) {
+                        const int g = (16 * kk) / (BM / 2);
+                        const uint32_t acol = C::TM_S + 8 * kk + g * (BM / 4);
+                        mma_ts(tmem + C::TM_DV, tmem + acol, sw128_desc(sDO + kk * 2048, BM * 128, 1024),
+                               C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    if (!(ok = mbar_wait(bar(B_DS_FULL), ds_ph, w))) break;
+                    ds_ph ^= 1;
+                    tc_fence_after();
+                    // dK += dS^T Q
+#pragma unroll
+                    for (int kk = 0; kk < BM / 16; ++kk) {
+                        const int g = (16 * kk) / (BM / 2);
+                        const uint32_t acol = C::TM_DP + 8 * kk + g * (BM / 4);
+                        mma_ts(tmem + C::TM_DK, tmem + acol, sw128_desc(sQ + kk * 2048, BM * 128, 1024),
+                               C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(bar(B_STAGE0 + S + stage));   // Q / dO of this stage consumed
+                    if (!(ok = mbar_wait(bar(B_DQ_EMPTY), dq_ph ^ 1, w))) break;
+                    dq_ph ^= 1;
+                    tc_fence_after();
+                    // dQ (kDqT: dQ^T = K^T dS^T, else dQ = dS K); both operands MN-major
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        mma_ss(tmem + C::TM_DQ, sw128_desc(dq_a + kk * 2048, BN * 128, 1024),
+                               sw128_desc(dq_b + kk * 2048, BN * 128, 1024), C::IDESC_DQ, kk > 0);
+                    }
+                    mma_commit(bar(B_DQ_FULL));
+                    if (++stage == S) { stage = 0; st_ph ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit(bar(B_ACC_FULL));
+                mma_commit(bar(B_KV_EMPTY));
+            }
+            // make sure no MMA is still running before tensor memory is freed
+            mma_commit(bar(B_DRAIN));
+            WaitCtl wd{abort_flag, p.err, p.budget_ns};
+            mbar_wait(bar(B_DRAIN), 0, wd);
+        }
+    } else if (warp < 6) {
+        // --------------------------------------------------------- dQ reducers
+        const int quarter = warp & 3;
+        const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+        const int r = quarter * 32 + lane;   // TMEM lane: d (kDqT) or query row
+        uint32_t dq_ph = 0;
+        bool ok = true;
+        float *const dqacc = p.dqacc;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            const Unit u = decode_unit<BM>(p, t);
+            for (int it = 0; it < u.iters; ++it) {
+                const int g = it / u.nm, m = u.m_begin + it % u.nm;
+                const int h = u.hk * p.G + g;
+                if (!(ok = mbar_wait(bar(B_DQ_FULL), dq_ph, w))) break;
+                dq_ph ^= 1;
+                tc_fence_after();
+                uint32_t v0[32], v1[32];
+                tmem_ld32(lane_addr + C::TM_DQ, v0);
+                tmem_ld32(lane_addr + C::TM_DQ + 32, v1);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_DQ_EMPTY));
+                const long long row0 = ws_row(p, u.b, h, m * BM);
+                int *sem = p.sem + row0 / 64;
+                if (p.deterministic) {
+                    // contributions to this row block arrive in n-block order:
+                    // wait until the 4 reducer warps of every earlier n block added
+                    bool got = true;
+                    if (lane == 0) got = sem_wait_geq(sem, 4 * u.n_block, w);
+                    got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+                    if (!got) { ok = false; break; }
+                    __threadfence();
+                }
+                const int rows_left = u.lq - m * BM;
+                if (C::kDqT) {
+                    // lane r = d; columns = BM (=64) query rows; a warp adds 32
+                    // consecutive d of one row: one 128-byte request
+                    float *dst = dqacc + row0 * D + r;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (i < rows_left)
+                            atomicAdd(dst + (long long)i * D, __uint_as_float(v0[i]));
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (32 + i < rows_left)
+                            atomicAdd(dst + (long long)(32 + i) * D, __uint_as_float(v1[i]));
+                } else {
+                    // lane r = query row; columns = the 64 d of that row
+                    if (r < rows_left) {
+                        float *dst = dqacc + (row0 + r) * D;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(
+                                             dst + 4 * c),
+                                         "f"(__uint_as_float(v0[4 * c])),
+                                         "f"(__uint_as_float(v0[4 * c + 1])),
+                                         "f"(__uint_as_float(v0[4 * c + 2])),
+                                         "f"(__uint_as_float(v0[4 * c + 3]))
+                                         : "memory");
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(
+                                             dst + 32 + 4 * c),
+                                         "f"(__uint_as_float(v1[4 * c])),
+                                         "f"(__uint_as_float(v1[4 * c + 1])),
+                                         "f"(__uint_as_float(v1[4 * c + 2])),
+                                         "f"(__uint_as_float(v1[4 * c + 3]))
+                                         : "memory");
+                    }
+                }
+                if (p.deterministic) {
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) red_release_add_gpu(sem, 1);
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------ softmax / elementwise
+        const int grp = (warp - 6) / 4;            // query-column group
+        const int quarter = warp & 3;
+        const int j = quarter * 32 + lane;          // key row within the block
+        const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+        constexpr int HALF = BM / 2;                // query columns per group
+        constexpr int NCH = HALF / 32;              // 32-column chunks per group
+        uint32_t s_ph = 0, dp_ph = 0, st_ph = 0, acc_ph = 0;
+        int stage = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            const Unit u = decode_unit<BM>(p, t);
+            const int n0 = u.n_block * BN;
+            const int kj = n0 + j;                   // key index within the sequence
+            const bool key_ok = kj < u.lk;
+            const int diag = u.lk - u.lq;            // key kj visible to query qi iff kj <= qi + diag
+            for (int it = 0; it < u.iters; ++it) {
+                const int m = u.m_begin + it % u.nm;
+                const int m0 = m * BM;
+                const bool masked = p.causal && (n0 + BN - 1 > m0 + diag);
+                if (!(ok = mbar_wait(bar(B_STAGE0 + stage), st_ph, w))) break;
+                if (!(ok = mbar_wait(bar(B_S_FULL), s_ph, w))) break;
+                s_ph ^= 1;
+                tc_fence_after();
+                const float *lse2 = reinterpret_cast<const float *>(smem + C::OFF_LSE + stage * BM * 4);
+                const float *dv = reinterpret_cast<const float *>(smem + C::OFF_DV + stage * BM * 4);
+                float P[HALF];
+#pragma unroll
+                for (int ch = 0; ch < NCH; ++ch) {
+                    uint32_t sr[32];
+                    tmem_ld32(lane_addr + C::TM_S + grp * HALF + 32 * ch, sr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const int i = grp * HALF + 32 * ch + c;   // query within the block
+                        float pv = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -lse2[i]));
+                        if (masked && kj > m0 + i + diag) pv = 0.f;
+                        P[32 * ch + c] = key_ok ? pv : 0.f;
+                    }
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) pk[c] = Cvt<T>::pack(P[32 * ch + 2 * c], P[32 * ch + 2 * c + 1]);
+                    tmem_st16(lane_addr + C::TM_S + grp * HALF + 16 * ch, pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_P_FULL));
+                if (!(ok = mbar_wait(bar(B_DP_FULL), dp_ph, w))) break;
+                dp_ph ^= 1;
+                tc_fence_after();
+                uint8_t *sds = smem + C::OFF_DS;
+#pragma unroll
+                for (int ch = 0; ch < NCH; ++ch) {
+                    uint32_t dr[32];
+                    tmem_ld32(lane_addr + C::TM_DP + grp * HALF + 32 * ch, dr);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const int i = grp * HALF + 32 * ch + 2 * c;
+                        const float d0 = P[32 * ch + 2 * c] * (__uint_as_float(dr[2 * c]) - dv[i]);
+                        const float d1 =
+                            P[32 * ch + 2 * c + 1] * (__uint_as_float(dr[2 * c + 1]) - dv[i + 1]);
+                        pk[c] = Cvt<T>::pack(d0, d1);
+                    }
+                    tmem_st16(lane_addr + C::TM_DP + grp * HALF + 16 * ch, pk);
+                    // dS^T row j into shared memory, 128B-swizzled halves of 64 queries
+#pragma unroll
+                    for (int u8 = 0; u8 < 4; ++u8) {
+                        const int i0 = grp * HALF + 32 * ch + 8 * u8;
+                        const int half = i0 / 64, cidx = (i0 % 64) / 8;
+                        const uint32_t off = half * (BN * 128) + j * 128 + ((cidx ^ (j & 7)) << 4);
+                        *reinterpret_cast<uint4 *>(sds + off) =
+                            make_uint4(pk[4 * u8], pk[4 * u8 + 1], pk[4 * u8 + 2], pk[4 * u8 + 3]);
+                    }
+                }
+                tmem_wait_st();
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar(B_DS_FULL));
+                    mbar_arrive(bar(B_STAGE0 + S + stage));
+                }
+                if (++stage == S) { stage = 0; st_ph ^= 1; }
+            }
+            if (!ok) break;
+            // ---------------------------------------------------- dK / dV out
+            T *out = reinterpret_cast<T *>(grp == 0 ? p.dk : p.dv);
+            const long long orow = (long long)(p.varlen ? u.k_row0 + kj : u.b * p.Sk + kj);
+            T *dst = out + (orow * p.Hkv + u.hk) * D;
+            if (u.iters == 0) {
+                if (key_ok && n0 < u.lk) {
+#pragma unroll
+                    for (int c = 0; c < D / 8; ++c)
+                        reinterpret_cast<uint4 *>(dst)[c] = make_uint4(0, 0, 0, 0);
+                }
+                continue;
+            }
+            if (!(ok = mbar_wait(bar(B_ACC_FULL), acc_ph, w))) break;
+            acc_ph ^= 1;
+            tc_fence_after();
+            const float mul = grp == 0 ? p.scale : 1.f;
+            const int col0 = grp == 0 ? C::TM_DK : C::TM_DV;
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+                uint32_t a[32];
+                tmem_ld32(lane_addr + col0 + 32 * ch, a);
+                tmem_wait_ld();
+                if (key_ok) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        pk[c] = Cvt<T>::pack(__uint_as_float(a[2 * c]) * mul,
+                                             __uint_as_float(a[2 * c + 1]) * mul);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        reinterpret_cast<uint4 *>(dst + 32 * ch)[c] =
+                            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_ACC_EMPTY));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
+}
+
+}  // namespace
+
+template <int kD, typename T>
+static cudaError_t launch_main_t(const BwdParams &p, const MainMaps &maps, int grid,
+                                 cudaStream_t stream) {
+    using C = MainCfg<kD, T>;
+    auto kern = bwd_main_kernel<kD, T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, C::kThreads, C::SMEM_BYTES, stream>>>(p, maps);
+    return cudaGetLastError();
+}
+
+// Rows of one TMA box for Q / dO (the main kernel's BM).
+int main_block_m(int D) { return D == 128 ? MainCfg<128, __nv_bfloat16>::BM : MainCfg<64, __nv_bfloat16>::BM; }
+
+cudaError_t launch_bwd_main(const BwdParams &p, const CUtensorMap &q, const CUtensorMap &k,
+                            const CUtensorMap &v, const CUtensorMap &dout, int bf16, int grid,
+                            cudaStream_t stream) {
+    MainMaps maps{q, k, v, dout};
+    if (p.D == 128)
+        return bf16 ? launch_main_t<128, __nv_bfloat16>(p, maps, grid, stream)
+                    : launch_main_t<128, __half>(p, maps, grid, stream);
+    return bf16 ? launch_main_t<64, __nv_bfloat16>(p, maps, grid, stream)
+                : launch_main_t<64, __half>(p, maps, grid, stream);
+}
+
+}  // namespace fa

@@ -1,0 +1,302 @@
+// fa_kernels.cu -- the bandwidth-bound kernels around the main backward kernel:
+//   schedule_kernel     builds the list of work units (sequence, K/V block, kv head)
+//   preprocess_kernel   Dv = rowsum(dO o O), LSE2 = LSE * log2(e), zero dQaccum
+//   postprocess_kernel  dQ = cast(dQaccum * scale)
+//   fwd_kernel          untimed forward (O, LSE) on CUDA cores, inputs for tests
+#include "fa_device.cuh"
+#include "fa_params.h"
+
+namespace fa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ int seq_len_q(const BwdParams &p, int b) {
+    return p.varlen ? p.cu_q[b + 1] - p.cu_q[b] : p.Sq;
+}
+__device__ __forceinline__ int seq_len_k(const BwdParams &p, int b) {
+    return p.varlen ? p.cu_k[b + 1] - p.cu_k[b] : p.Sk;
+}
+
+// ------------------------------------------------------------------ schedule
+// Work units in the order (n_block, sequence, kv head): every unit of a given
+// (sequence, kv head) comes after the units with smaller n_block, which the
+// deterministic dQ order relies on, and under a causal mask the units with the
+// most query blocks (small n_block) come first.  One block of 1024 threads.
+__global__ void __launch_bounds__(1024) schedule_kernel(BwdParams p) {
+    __shared__ int warp_sums[32];
+    __shared__ int total_s;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int max_nb = (p.Sk + kBlockN - 1) / kBlockN;
+    int base = 0;
+    for (int n = 0; n < max_nb; ++n) {
+        for (int b0 = 0; b0 < p.B; b0 += 1024) {
+            const int b = b0 + tid;
+            int flag = 0;
+            if (b < p.B) flag = seq_len_k(p, b) > n * kBlockN;
+            // block-wide exclusive scan of flag
+            int x = flag;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (lane == 31) warp_sums[wid] = x;
+            __syncthreads();
+            if (wid == 0) {
+                int s = warp_sums[lane];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    int y = __shfl_up_sync(0xffffffffu, s, o);
+                    if (lane >= o) s += y;
+                }
+                warp_sums[lane] = s;   // inclusive
+                if (lane == 31) total_s = s;
+            }
+            __syncthreads();
+            const int pos = x - flag + (wid > 0 ? warp_sums[wid - 1] : 0);
+            if (flag) {
+                for (int hk = 0; hk < p.Hkv; ++hk) {
+                    const long long idx = (long long)(base + pos) * p.Hkv + hk;
+                    if (idx < p.max_tiles) p.tiles[idx] = make_int4(b, n, hk, 0);
+                }
+            }
+            base += total_s;
+            __syncthreads();
+        }
+    }
+    if (tid == 0) *p.ntiles = min(base * p.Hkv, p.max_tiles);
+}
+
+// ---------------------------------------------------------------- preprocess
+// grid (row chunks, sequences); D/8 threads per (position, head) row, each
+// reading 16 bytes of O and of dO.  Padding rows up to the next multiple of
+// 128 get Dv = 0 and LSE2 = +inf (so P = 0 there).  Every workspace row of
+// the sequence has its dQ accumulator zeroed, and in deterministic mode its
+// semaphores as well.
+template <int D, typename T>
+__global__ void __launch_bounds__(256) preprocess_kernel(BwdParams p) {
+    constexpr int TPR = D / 8;   // threads per row
+    const int b = blockIdx.y;
+    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long rid = gid / TPR;
+    const int part = (int)(gid % TPR);
+    const int lq = seq_len_q(p, b);
+    const int lq_round = (lq + kRowTile - 1) / kRowTile * kRowTile;
+    const int s = (int)(rid / p.Hq), h = (int)(rid % p.Hq);
+    // no early return: the row sum below is a full-warp shuffle
+    const bool active = s < lq_round;
+    const long long wr = active ? ws_row(p, b, h, s) : 0;
+    float acc = 0.f;
+    if (active && s < lq) {
+        const long long trow = p.varlen ? (long long)p.cu_q[b] + s : (long long)b * p.Sq + s;
+        const long long off = (trow * p.Hq + h) * D + part * 8;
+        const uint4 ov = *reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.o) + off);
+        const uint4 dv = *reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.dout) + off);
+        const uint32_t oa[4] = {ov.x, ov.y, ov.z, ov.w}, da[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const float2 of = Cvt<T>::unpack(oa[t]), df = Cvt<T>::unpack(da[t]);
+            acc = fmaf(of.x, df.x, acc);
+            acc = fmaf(of.y, df.y, acc);
+        }
+    }
+#pragma unroll
+    for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, TPR);
+    if (!active) return;
+    if (part == 0) {
+        float l2 = __int_as_float(0x7f800000);   // +inf on padding rows
+        if (s < lq) {
+            const long long li = p.varlen ? (long long)h * p.cu_q[p.B] + p.cu_q[b] + s
+                                          : ((long long)b * p.Hq + h) * p.Sq + s;
+            float l = p.lse[li];
+            if (l == -__int_as_float(0x7f800000)) l = 0.f;   // get_validated_lse
+            l2 = l * kLog2e;
+        }
+        p.dvec[wr] = (s < lq) ? acc : 0.f;
+        p.lse2[wr] = l2;
+        if (p.deterministic && (s % 64) == 0) p.sem[wr / 64] = 0;
+    }
+    float4 *z = reinterpret_cast<float4 *>(p.dqacc + wr * D) + part * 2;
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// --------------------------------------------------------------- postprocess
+// dQ[row, h, :] = cast(dQaccum[ws_row(b, h, s), :] * scale) for s < Lq
+// (FlashAttentionBackwardPostprocess: acc.load() * scale, then a predicated
+// store clipped to the sequence length).
+template <int D, typename T>
+__global__ void __launch_bounds__(256) postprocess_kernel(BwdParams p) {
+    constexpr int TPR = D / 8;
+    const int b = blockIdx.y;
+    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long rid = gid / TPR;
+    const int part = (int)(gid % TPR);
+    const int lq = seq_len_q(p, b);
+    const int s = (int)(rid / p.Hq), h = (int)(rid % p.Hq);
+    if (s >= lq) return;
+    const long long wr = ws_row(p, b, h, s);
+    const float4 *src = reinterpret_cast<const float4 *>(p.dqacc + wr * D) + part * 2;
+    const float4 a = src[0], c = src[1];
+    const float sc = p.scale;
+    uint4 o;
+    o.x = Cvt<T>::pack(a.x * sc, a.y * sc);
+    o.y = Cvt<T>::pack(a.z * sc, a.w * sc);
+    o.z = Cvt<T>::pack(c.x * sc, c.y * sc);
+    o.w = Cvt<T>::pack(c.z * sc, c.w * sc);
+    const long long trow = p.varlen ? (long long)p.cu_q[b] + s : (long long)b * p.Sq + s;
+    *reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dq) + (trow * p.Hq + h) * D + part * 8) = o;
+}
+
+// ------------------------------------------------------------------- forward
+// Untimed reference-style forward: one warp per query row, 8 rows per block,
+// K/V tiles of 64 keys staged in shared memory as fp32; online softmax in the
+// log2 domain; O = sum_j p_j v_j / l, LSE = (m + log2 l) ln 2.
+template <int D, typename T>
+__global__ void __launch_bounds__(256) fwd_kernel(BwdParams p, void *o_out, float *lse_out) {
+    constexpr int KT = 64, ROWS = 8, DPL = D / 32;
+    extern __shared__ float fsm[];
+    float *Ks = fsm;                   // [KT][D + 1]
+    float *Vs = Ks + KT * (D + 1);     // [KT][D]
+    float *Qs = Vs + KT * D;           // [ROWS][D]
+    const int b = blockIdx.z, h = blockIdx.y, hk = h / p.G;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int lq = seq_len_q(p, b), lk = seq_len_k(p, b);
+    const int row0 = blockIdx.x * ROWS;
+    if (row0 >= lq) return;
+    const int i = row0 + warp;
+    const bool row_ok = i < lq;
+    const int diag = lk - lq;
+    const long long qbase = p.varlen ? (long long)p.cu_q[b] : (long long)b * p.Sq;
+    const long long kbase = p.varlen ? (long long)p.cu_k[b] : (long long)b * p.Sk;
+    const T *q = reinterpret_cast<const T *>(p.q);
+    const T *k = reinterpret_cast<const T *>(p.k);
+    const T *v = reinterpret_cast<const T *>(p.v);
+    for (int idx = threadIdx.x; idx < ROWS * D; idx += blockDim.x) {
+        const int r = idx / D, d = idx % D;
+        float val = 0.f;
+        if (row0 + r < lq) val = (float)q[((qbase + row0 + r) * p.Hq + h) * D + d];
+        Qs[idx] = val;
+    }
+    int kend = lk;
+    if (p.causal) kend = min(lk, max(0, min(lq - 1, row0 + ROWS - 1) + diag + 1));
+    float m = -INFINITY, l = 0.f, acc[DPL];
+#pragma unroll
+    for (int t = 0; t < DPL; ++t) acc[t] = 0.f;
+    for (int k0 = 0; k0 < kend; k0 += KT) {
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < KT * D; idx += blockDim.x) {
+            const int r = idx / D, d = idx % D;
+            float kv = 0.f, vv = 0.f;
+            if (k0 + r < lk) {
+                const long long off = ((kbase + k0 + r) * p.Hkv + hk) * D + d;
+                kv = (float)k[off];
+                vv = (float)v[off];
+            }
+            Ks[r * (D + 1) + d] = kv;
+            Vs[r * D + d] = vv;
+        }
+        __syncthreads();
+        if (!row_ok) continue;
+        float sv[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int jj = lane + 32 * t, j = k0 + jj;
+            float s = 0.f;
+            const float *kr = Ks + jj * (D + 1);
+            const float *qr = Qs + warp * D;
+#pragma unroll 8
+            for (int d = 0; d < D; ++d) s = fmaf(qr[d], kr[d], s);
+            const bool vis = j < lk && (!p.causal || j <= i + diag);
+            sv[t] = vis ? s * p.scale_log2 : -INFINITY;
+        }
+        float mt = fmaxf(sv[0], sv[1]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+        const float mn = fmaxf(m, mt);
+        if (mn == -INFINITY) continue;   // nothing visible yet
+        const float corr = exp2f(m - mn);
+        const float p0 = exp2f(sv[0] - mn), p1 = exp2f(sv[1] - mn);
+        float ps = p0 + p1;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+        l = l * corr + ps;
+#pragma unroll
+        for (int t = 0; t < DPL; ++t) acc[t] *= corr;
+        for (int jj = 0; jj < KT; ++jj) {
+            const float pj = __shfl_sync(0xffffffffu, jj < 32 ? p0 : p1, jj & 31);
+#pragma unroll
+            for (int t = 0; t < DPL; ++t) acc[t] = fmaf(pj, Vs[jj * D + lane + 32 * t], acc[t]);
+        }
+        m = mn;
+    }
+    if (!row_ok) return;
+    T *o = reinterpret_cast<T *>(o_out);
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+    for (int t = 0; t < DPL; ++t) o[((qbase + i) * p.Hq + h) * D + lane + 32 * t] = (T)(acc[t] * inv);
+    if (lane == 0) {
+        const long long li = p.varlen ? (long long)h * p.cu_q[p.B] + p.cu_q[b] + i
+                                      : ((long long)b * p.Hq + h) * p.Sq + i;
+        lse_out[li] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_schedule(const BwdParams &p, cudaStream_t stream) {
+    schedule_kernel<<<1, 1024, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+static dim3 row_grid(const BwdParams &p, int lanes_per_row, int rows_per_seq) {
+    const long long threads = (long long)rows_per_seq * p.Hq * lanes_per_row;
+    return dim3((unsigned)((threads + 255) / 256), (unsigned)p.B, 1);
+}
+
+cudaError_t launch_preprocess(const BwdParams &p, int bf16, cudaStream_t stream) {
+    const dim3 grid = row_grid(p, p.D / 8, p.sq_round);
+    if (p.D == 128) {
+        if (bf16) preprocess_kernel<128, __nv_bfloat16><<<grid, 256, 0, stream>>>(p);
+        else preprocess_kernel<128, __half><<<grid, 256, 0, stream>>>(p);
+    } else {
+        if (bf16) preprocess_kernel<64, __nv_bfloat16><<<grid, 256, 0, stream>>>(p);
+        else preprocess_kernel<64, __half><<<grid, 256, 0, stream>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_postprocess(const BwdParams &p, int bf16, cudaStream_t stream) {
+    const dim3 grid = row_grid(p, p.D / 8, p.Sq);
+    if (p.D == 128) {
+        if (bf16) postprocess_kernel<128, __nv_bfloat16><<<grid, 256, 0, stream>>>(p);
+        else postprocess_kernel<128, __half><<<grid, 256, 0, stream>>>(p);
+    } else {
+        if (bf16) postprocess_kernel<64, __nv_bfloat16><<<grid, 256, 0, stream>>>(p);
+        else postprocess_kernel<64, __half><<<grid, 256, 0, stream>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+template <int D, typename T>
+static cudaError_t launch_fwd_t(const BwdParams &p, void *o, float *lse, cudaStream_t stream) {
+    const int smem = (64 * (D + 1) + 64 * D + 8 * D) * 4;
+    auto kern = fwd_kernel<D, T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((p.Sq + 7) / 8, p.Hq, p.B);
+    kern<<<grid, 256, smem, stream>>>(p, o, lse);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(const BwdParams &p, void *o, float *lse, int bf16, cudaStream_t stream) {
+    if (p.D == 128)
+        return bf16 ? launch_fwd_t<128, __nv_bfloat16>(p, o, lse, stream)
+                    : launch_fwd_t<128, __half>(p, o, lse, stream);
+    return bf16 ? launch_fwd_t<64, __nv_bfloat16>(p, o, lse, stream)
+                : launch_fwd_t<64, __half>(p, o, lse, stream);
+}
+
+}  // namespace fa

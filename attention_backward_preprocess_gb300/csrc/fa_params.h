@@ -1,0 +1,46 @@
+// fa_params.h -- host/device parameter block of the backward kernels and the
+// workspace row mapping they share.
+#pragma once
+
+#include <cstdint>
+
+namespace fa {
+
+constexpr int kRowTile = 128;   // workspace rows are padded per (sequence, head) to this
+constexpr int kBlockN = 128;    // keys per work unit of the main kernel
+
+struct BwdParams {
+    // tensors (public layouts, see fa.h)
+    const void *q, *k, *v, *o, *dout;
+    const float *lse;
+    void *dq, *dk, *dv;
+    int B, Sq, Sk, Hq, Hkv, D, G;
+    float scale;        // c
+    float scale_log2;   // c * log2(e)
+    int causal, deterministic, varlen;
+    const int *cu_q, *cu_k;
+    // workspace
+    int *err;           // device error word
+    int4 *tiles;        // work units (b, n_block, hk, 0)
+    int *ntiles;        // number of work units written by the scheduler
+    int max_tiles;
+    float *dvec;        // Dv per workspace row
+    float *lse2;        // LSE * log2(e) per workspace row (+inf on padding rows)
+    float *dqacc;       // fp32 dQ accumulator [rows, D]
+    int *sem;           // deterministic-order semaphores, one per 64 workspace rows
+    long long rows;     // workspace rows
+    long long rows_per_head;  // varlen: rows of one head; dense: round_up(Sq, 128)
+    int sq_round;       // round_up(Sq, 128)
+    long long budget_ns;      // bound of every device-side wait
+};
+
+// Workspace row of (sequence b, query head h, position s).
+__device__ __forceinline__ long long ws_row(const BwdParams &p, int b, int h, int s) {
+    if (p.varlen) {
+        long long pad = ((long long)p.cu_q[b] + (long long)b * kRowTile) / kRowTile * kRowTile;
+        return (long long)h * p.rows_per_head + pad + s;
+    }
+    return ((long long)b * p.Hq + h) * p.sq_round + s;
+}
+
+}  // namespace fa

@@ -1,0 +1,146 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) fused exact-softmax attention backward.
+ *
+ * The backward of O = softmax(Q K^T * scale + mask) V, given the forward's O
+ * and per-row log-sum-exp LSE, produces dQ, dK, dV without materialising the
+ * S x S probability matrix.  It runs as three kernels in stream order:
+ *
+ *   1. preprocess   Dv_i = sum_d dO_id * O_id (fp32), LSE2_i = LSE_i * log2(e)
+ *                   (LSE = -inf replaced by 0, the get_validated_lse guard of
+ *                   the Composable Kernel page
+ *                   "block_fmha_bwd_dq_dk_dv_pipeline_trload_kr_ktr_vr.hpp"),
+ *                   zero the fp32 dQ accumulator (CollectiveEpilogueBwdGQA's
+ *                   "already zero-initialized" precondition in
+ *                   "flash-attention/hopper/epilogue_bwd.hpp").
+ *   2. main         one work unit per (K/V column block of 128 keys, batch,
+ *                   kv head): recompute S and P = exp2(S*scale*log2e - LSE2)
+ *                   (STAGE 1-2 of the Composable Kernel page), dV += P^T dO
+ *                   (STAGE 3), dP = dO V^T (STAGE 4), dS = P o (dP - Dv)
+ *                   (STAGE 5), dK += dS^T Q (STAGE 6, scaled at the end),
+ *                   dQ += dS K (STAGE 7) into the fp32 accumulator; dK / dV
+ *                   summed over the query heads of a GQA group.
+ *   3. postprocess  dQ = cast(dQaccum * scale) (FlashAttentionBackwardPostprocess
+ *                   of "flash_bwd_postprocess.py").
+ *
+ * Layouts (all contiguous, d innermost, CollectiveEpilogueBwd's
+ * (seqlen, d, head, batch) shape with stride (int64, 1, int64, int64)):
+ *   dense : q, o, dout, dq : [B, Sq, Hq, D];  k, v, dk, dv : [B, Sk, Hkv, D]
+ *           lse : fp32 [B, Hq, Sq], natural log
+ *   varlen: cu_seqlens_q / cu_seqlens_k != NULL (both or neither): int32
+ *           device arrays of B+1 prefix sums; tensors packed [total, H, D];
+ *           lse fp32 [Hq, total_q]; Sq / Sk are the MAXIMUM lengths.
+ * Causal masking is bottom-right aligned: key j is visible to query i iff
+ * j <= i + (Lk - Lq).
+ *
+ * Ownership: the caller owns every tensor and the stream.  All tensor
+ * pointers are device pointers aligned to 16 bytes.  dq, dk, dv are fully
+ * overwritten (key rows no query sees get zeros).  fa_bwd uses a per-device
+ * workspace owned by the library (grown on demand); calls that overlap on
+ * different streams of one device must use fa_bwd_with_workspace with their
+ * own workspaces.
+ *
+ * Errors: arguments are validated before any launch (FA_ERR_INVALID_ARG,
+ * FA_ERR_UNSUPPORTED); a failed launch returns FA_ERR_CUDA.  Otherwise the
+ * call is asynchronous.  Every wait inside the kernels is bounded; a wait
+ * that runs out records FA_ERR_TIMEOUT in a device word that
+ * fa_device_status() reads (deterministic mode reads it before returning).
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misalignment, bad scale */
+    FA_ERR_UNSUPPORTED = 2,  /* head dim not in {64, 128}, dtype, or GPU not sm_103 */
+    FA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    FA_ERR_TIMEOUT = 4       /* a bounded device-side wait ran out */
+} fa_status;
+
+typedef enum { FA_BF16 = 0, FA_FP16 = 1 } fa_dtype;
+
+/* Backward pass.  softmax_scale is the plain scale c (S = c Q K^T); dK and dQ
+ * carry the factor c, dV does not.  deterministic != 0 accumulates dQ in a
+ * fixed order (ordered per-block semaphores) so repeated calls are
+ * bit-identical; it then also synchronises `stream` and returns
+ * FA_ERR_TIMEOUT if a semaphore wait ran out. */
+fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                 const float *lse, void *dq, void *dk, void *dv, int B, int Sq, int Sk, int Hq,
+                 int Hkv, int D, float softmax_scale, int causal, const int *cu_seqlens_q,
+                 const int *cu_seqlens_k, int deterministic, fa_dtype dtype,
+                 cudaStream_t stream);
+
+/* Bytes of device workspace fa_bwd_with_workspace needs for these sizes
+ * (varlen = cu_seqlens given).  0 means the sizes are invalid. */
+size_t fa_bwd_workspace_bytes(int B, int Sq, int Sk, int Hq, int Hkv, int D, int varlen,
+                              int deterministic);
+
+/* fa_bwd on a caller-owned device workspace of at least
+ * fa_bwd_workspace_bytes(...) bytes, 256-byte aligned.  The workspace needs
+ * no initialisation; it must not be used by another call in flight. */
+fa_status fa_bwd_with_workspace(const void *q, const void *k, const void *v, const void *o,
+                                const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                                int B, int Sq, int Sk, int Hq, int Hkv, int D,
+                                float softmax_scale, int causal, const int *cu_seqlens_q,
+                                const int *cu_seqlens_k, int deterministic, fa_dtype dtype,
+                                void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* The three stages of fa_bwd_with_workspace as separate calls (same
+ * arguments, same workspace), for timing and testing each kernel.  They must
+ * run in this order on one stream. */
+fa_status fa_bwd_preprocess(const void *o, const void *dout, const float *lse, int B, int Sq,
+                            int Sk, int Hq, int Hkv, int D, const int *cu_seqlens_q,
+                            const int *cu_seqlens_k, int deterministic, fa_dtype dtype,
+                            void *workspace, size_t workspace_bytes, cudaStream_t stream);
+fa_status fa_bwd_main(const void *q, const void *k, const void *v, void *dk, void *dv, int B,
+                      int Sq, int Sk, int Hq, int Hkv, int D, float softmax_scale, int causal,
+                      const int *cu_seqlens_q, const int *cu_seqlens_k, int deterministic,
+                      fa_dtype dtype, void *workspace, size_t workspace_bytes,
+                      cudaStream_t stream);
+fa_status fa_bwd_postprocess(void *dq, int B, int Sq, int Sk, int Hq, int Hkv, int D,
+                             float softmax_scale, const int *cu_seqlens_q,
+                             const int *cu_seqlens_k, int deterministic, fa_dtype dtype,
+                             void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Where the preprocess outputs live inside a workspace, in fp32 elements
+ * from the workspace base: Dv at *dvec_off, LSE2 at *lse2_off, each indexed
+ * by workspace row; the fp32 dQ accumulator at *dqacc_off, [rows, D].
+ * Workspace row of (sequence b, query head h, position s):
+ *   dense : (b * Hq + h) * round_up(Sq, 128) + s
+ *   varlen: h * rows_per_head + pad(b) + s, pad(b) = (cu_q[b] + 128 b) / 128 * 128,
+ *           rows_per_head = round_up(B * (Sq + 128), 128)
+ * (the padded varlen offset of FlashAttentionBackwardPostprocess).  *rows is
+ * the total row count. */
+fa_status fa_bwd_workspace_layout(int B, int Sq, int Sk, int Hq, int Hkv, int D, int varlen,
+                                  int deterministic, size_t *dvec_off, size_t *lse2_off,
+                                  size_t *dqacc_off, size_t *rows);
+
+/* Forward pass, untimed helper that supplies O and LSE (natural log, -inf
+ * for a query row that sees no key; such rows get O = 0).  Plain CUDA-core
+ * kernel with fp32 accumulation; same layouts and masking as fa_bwd. */
+fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Sq,
+                 int Sk, int Hq, int Hkv, int D, float softmax_scale, int causal,
+                 const int *cu_seqlens_q, const int *cu_seqlens_k, fa_dtype dtype,
+                 cudaStream_t stream);
+
+/* Synchronises `stream`, then returns and clears the device error word of
+ * this device's library workspace (FA_OK or FA_ERR_TIMEOUT).  For a caller
+ * workspace, pass it; NULL means the library's own. */
+fa_status fa_device_status(void *workspace, cudaStream_t stream);
+
+/* Upper limit, in nanoseconds, of every device-side wait (default 2e9).
+ * Returns the previous value; 0 leaves it unchanged. */
+long long fa_set_wait_timeout_ns(long long ns);
+
+const char *fa_status_string(fa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FA_GB300_H */

@@ -104,6 +104,8 @@ class Oracle:
         lib.oracle_backward_sampled.restype = ctypes.c_int
         lib.oracle_head_matrices.argtypes = [dp] * 6 + shape + [ctypes.c_int] * 2 + [dp, dp]
         lib.oracle_head_matrices.restype = ctypes.c_int
+        lib.oracle_preprocess.argtypes = [dp] * 6 + shape + [dp, dp, ctypes.c_int]
+        lib.oracle_preprocess.restype = ctypes.c_int
         lib.oracle_max_threads.restype = ctypes.c_int
         self.lib = lib
         self.path = libpath
@@ -160,6 +162,21 @@ class Oracle:
             raise ValueError("oracle_backward_sampled rejected its arguments (%d)" % rc)
         return dq, dk, dv
 
+    def preprocess(self, q, k, v, dout, scale, causal=False, o=None, lse=None, cu_q=None,
+                   cu_k=None, nthreads=None):
+        """(Dv, LSE_guarded) per query row, in lse's layout: Dv_i = <dO_i, O_i>."""
+        q, k, v, dout, o, lse = map(_f64, (q, k, v, dout, o, lse))
+        args, keep, (B, Sq, Sk, Hq, Hkv, D) = _shape_args(q, k, scale, causal, cu_q, cu_k)
+        shape = (B, Hq, Sq) if cu_q is None else (Hq, q.shape[0])
+        dvec = np.zeros(shape)
+        lse_out = np.zeros(shape)
+        rc = self.lib.oracle_preprocess(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                        _ptr(dout), *args, _ptr(dvec), _ptr(lse_out),
+                                        self._threads(nthreads))
+        if rc:
+            raise ValueError("oracle_preprocess rejected its arguments (%d)" % rc)
+        return dvec, lse_out
+
     def head_matrices(self, q, k, v, dout, scale, causal=False, o=None, lse=None, cu_q=None,
                       cu_k=None, b=0, h=0):
         """Dense P and dS [Lq, Lk] of one (sequence, query head) problem (tiny inputs)."""
@@ -205,3 +222,7 @@ def backward_sampled(*a, **kw):
 
 def head_matrices(*a, **kw):
     return default().head_matrices(*a, **kw)
+
+
+def preprocess(*a, **kw):
+    return default().preprocess(*a, **kw)

@@ -98,29 +98,34 @@ static double score(const prob_t *p, int b, int h, int i, int j) {
 }
 
 /* Forward statistics of one query row: LSE_i (natural log) and, if o_out is
- * not NULL, O_i = sum_j P_ij v_j.  Max-shifted sum for range safety only. */
+ * not NULL, O_i = sum_j P_ij v_j.  The row's scores are computed once into a
+ * scratch row; the max shift is for range safety only. */
 static double row_forward(const prob_t *p, int b, int h, int i, double *o_out) {
     int lk = seq_len_k(p, b), hk = h / p->G, D = p->D;
+    double *s = (double *)malloc(sizeof(double) * (lk > 0 ? lk : 1));
     double m = -INFINITY;
-    for (int j = 0; j < lk; ++j)
-        if (visible(p, b, i, j)) {
-            double s = score(p, b, h, i, j);
-            if (s > m) m = s;
-        }
+    for (int j = 0; j < lk; ++j) {
+        s[j] = visible(p, b, i, j) ? score(p, b, h, i, j) : -INFINITY;
+        if (s[j] > m) m = s[j];
+    }
     if (o_out) for (int d = 0; d < D; ++d) o_out[d] = 0.0;
-    if (m == -INFINITY) return -INFINITY; /* no visible key */
+    if (m == -INFINITY) { /* no visible key */
+        free(s);
+        return -INFINITY;
+    }
     double sum = 0.0;
     for (int j = 0; j < lk; ++j)
-        if (visible(p, b, i, j)) sum += exp(score(p, b, h, i, j) - m);
+        if (s[j] != -INFINITY) sum += exp(s[j] - m);
     double lse = m + log(sum);
     if (o_out) {
         for (int j = 0; j < lk; ++j)
-            if (visible(p, b, i, j)) {
-                double pij = exp(score(p, b, h, i, j) - lse);
+            if (s[j] != -INFINITY) {
+                double pij = exp(s[j] - lse);
                 const double *vj = p->v + row_k(p, b, j, hk);
                 for (int d = 0; d < D; ++d) o_out[d] += pij * vj[d];
             }
     }
+    free(s);
     return lse;
 }
 
@@ -198,8 +203,15 @@ static void group_row_stats(const prob_t *p, int b, int hk, double **lse_g, doub
 #pragma omp parallel for schedule(dynamic, 8) num_threads(nthreads)
         for (int i = 0; i < lq; ++i) {
             double *scratch = (double *)malloc(sizeof(double) * p->D);
-            lse[i] = row_lse_for_backward(p, b, h, i, scratch);
-            dvec[i] = row_dvec(p, b, h, i, scratch);
+            if (!p->lse && !p->o) {
+                /* own forward: LSE and O of the row from one pass */
+                double l = row_forward(p, b, h, i, scratch);
+                lse[i] = (l == -INFINITY) ? 0.0 : l; /* get_validated_lse */
+                dvec[i] = dot(p->dout + row_q(p, b, i, h), scratch, p->D);
+            } else {
+                lse[i] = row_lse_for_backward(p, b, h, i, scratch);
+                dvec[i] = row_dvec(p, b, h, i, scratch);
+            }
             free(scratch);
         }
     }
@@ -330,6 +342,31 @@ int oracle_backward_sampled(const double *q, const double *k, const double *v, c
     free(done);
     free(lse_g);
     free(dvec_g);
+    return 0;
+}
+
+/* The preprocess quantities of every query row: Dv_i = <dO_i, O_i> (O given,
+ * or the oracle's own when NULL) and the guarded natural-log LSE the
+ * backward uses.  Outputs have lse's layout. */
+int oracle_preprocess(const double *q, const double *k, const double *v, const double *o,
+                      const double *lse, const double *dout, int B, int Sq, int Sk, int Hq,
+                      int Hkv, int D, double scale, int causal, const int *cu_q, const int *cu_k,
+                      double *dvec_out, double *lse_out, int nthreads) {
+    prob_t p;
+    if (make_prob(&p, q, k, v, o, lse, dout, B, Sq, Sk, Hq, Hkv, D, scale, causal, cu_q, cu_k))
+        return 1;
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < Hq; ++h) {
+            int lq = seq_len_q(&p, b);
+#pragma omp parallel for schedule(dynamic, 8) num_threads(nthreads)
+            for (int i = 0; i < lq; ++i) {
+                double *scratch = (double *)malloc(sizeof(double) * D);
+                long li = lse_index(&p, b, i, h);
+                lse_out[li] = row_lse_for_backward(&p, b, h, i, scratch);
+                dvec_out[li] = row_dvec(&p, b, h, i, scratch);
+                free(scratch);
+            }
+        }
     return 0;
 }
 

@@ -18,3 +18,24 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def fa():
+    """The library binding, built in-tree first if the sources are newer."""
+    from attention_backward_preprocess_gb300 import build
+    build.build()
+    import attention_backward_preprocess_gb300 as mod
+    mod.lib()
+    return mod
+
+
+@pytest.fixture(scope="session")
+def cuda_device():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    major, minor = torch.cuda.get_device_capability()
+    if (major, minor) != (10, 3):
+        pytest.skip("needs sm_103 (GB300), found sm_%d%d" % (major, minor))
+    return torch.device("cuda")

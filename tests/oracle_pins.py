@@ -281,7 +281,24 @@ def pin_given_forward_consistent(orc):
         _close(x, y, 1e-14, "given O/LSE " + n)
 
 
-ALL_PINS = [
+def pin_preprocess_identity(orc):
+    """Dv_i = <dO_i, O_i> equals sum_j P_ij dP_ij (because O_i = sum_j P_ij v_j),
+    and the guarded LSE is the forward's LSE with -inf replaced by 0."""
+    for causal, (sq, sk) in ((False, (6, 6)), (True, (6, 6)), (True, (8, 5))):
+        q, k, v, do = _dense(_rng(50 + sq + sk), 1, sq, sk, 2, 1, 4)
+        dvec, lse_g = orc.preprocess(q, k, v, do, 0.65, causal)
+        _, lse = orc.forward(q, k, v, 0.65, causal)
+        _close(lse_g, np.where(np.isneginf(lse), 0.0, lse), 0, "guarded LSE")
+        for h in range(2):
+            P, _ = orc.head_matrices(q, k, v, do, 0.65, causal, h=h)
+            dP = do[0, :, h] @ v[0, :, 0].T
+            _close(dvec[0, h], (P * dP).sum(1), 1e-13, "Dv = sum_j P dP")
+        o, _ = orc.forward(q, k, v, 0.65, causal)
+        dvec_given, _ = orc.preprocess(q, k, v, do, 0.65, causal, o=o, lse=lse)
+        _close(dvec_given, dvec, 1e-14, "Dv with the given O")
+
+
+ALL_PINS = [pin_preprocess_identity, 
     pin_worked_example, pin_fd_dense, pin_fd_causal, pin_fd_causal_rect, pin_fd_gqa,
     pin_fd_varlen, pin_library_forward, pin_closed_forms, pin_invariants,
     pin_gqa_equals_expanded, pin_varlen_equals_dense, pin_sampled_equals_full,

@@ -1,0 +1,108 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function the public headers declare, plans workspaces, and rejects bad
+arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_headers_declare_the_boundary():
+    names = declared_functions()
+    for required in ("fa_bwd", "fa_fwd", "fa_bwd_workspace_bytes", "fa_status_string"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(fa):
+    L = fa.lib()
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+    assert sorted(fa.EXPORTED) == declared_functions()
+
+
+def test_status_strings(fa):
+    for s in range(5):
+        assert fa.status_string(s)
+    assert fa.status_string(99) == "unknown status"
+
+
+def test_workspace_planning(fa):
+    # dense: rows = B * Hq * round_up(Sq, 128)
+    n = fa.workspace_bytes(2, 8192, 8192, 32, 8, 128)
+    lay = fa.workspace_layout(2, 8192, 8192, 32, 8, 128)
+    assert lay["rows"] == 2 * 32 * 8192
+    assert lay["dqacc"] * 4 + lay["rows"] * 128 * 4 <= n
+    lay = fa.workspace_layout(1, 130, 130, 2, 2, 64)
+    assert lay["rows"] == 1 * 2 * 256
+    # varlen: rows_per_head = round_up(B * (Sq + 128), 128)
+    lay = fa.workspace_layout(3, 300, 300, 4, 4, 64, varlen=True)
+    assert lay["rows"] == 4 * ((3 * (300 + 128) + 127) // 128 * 128)
+    assert fa.workspace_bytes(2, 100, 100, 4, 4, 128, deterministic=True) > \
+        fa.workspace_bytes(2, 100, 100, 4, 4, 128)
+    assert fa.workspace_bytes(1, 128, 128, 1, 1, 96) == 0          # unsupported head dim
+    assert fa.workspace_bytes(1, 128, 128, 3, 2, 64) == 0          # Hq % Hkv != 0
+    assert fa.workspace_bytes(0, 128, 128, 1, 1, 64) == 0
+
+
+def _call_with_ws(fa, **over):
+    """fa_bwd_with_workspace with fake (never dereferenced) aligned pointers."""
+    L = fa.lib()
+    a = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, dout=0x5000, lse=0x6000, dq=0x7000,
+             dk=0x8000, dv=0x9000, B=1, Sq=128, Sk=128, Hq=2, Hkv=2, D=64, scale=0.125,
+             causal=0, cu_q=None, cu_k=None, det=0, dtype=0, ws=0x100000, ws_bytes=1 << 40)
+    a.update(over)
+    vp = ctypes.c_void_p
+    return L.fa_bwd_with_workspace(
+        vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["o"]), vp(a["dout"]), vp(a["lse"]), vp(a["dq"]),
+        vp(a["dk"]), vp(a["dv"]), a["B"], a["Sq"], a["Sk"], a["Hq"], a["Hkv"], a["D"],
+        a["scale"], a["causal"], vp(a["cu_q"]) if a["cu_q"] else None,
+        vp(a["cu_k"]) if a["cu_k"] else None, a["det"], a["dtype"], vp(a["ws"]), a["ws_bytes"],
+        None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(q=0), 1), (dict(dv=0), 1), (dict(B=0), 1), (dict(Sq=-1), 1), (dict(Hq=3), 1),
+    (dict(D=96), 2), (dict(D=256), 2), (dict(dtype=7), 2),
+    (dict(scale=0.0), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
+    (dict(q=0x1008), 1), (dict(lse=0x6004), 1), (dict(ws=0x100010), 1), (dict(ws=0), 1),
+    (dict(ws_bytes=16), 1), (dict(cu_q=0xA000), 1),
+])
+def test_invalid_arguments_rejected_before_launch(fa, over, status):
+    assert _call_with_ws(fa, **over) == status
+
+
+def test_fa_bwd_rejects_before_device(fa):
+    L = fa.lib()
+    vp = ctypes.c_void_p
+    ptrs = [vp(0x1000 * (i + 1)) for i in range(9)]
+    assert L.fa_bwd(*ptrs, 1, 128, 128, 3, 2, 64, 0.125, 0, None, None, 0, 0, None) == 1
+    assert L.fa_bwd(*ptrs, 1, 128, 128, 2, 2, 80, 0.125, 0, None, None, 0, 0, None) == 2
+    assert L.fa_fwd(*ptrs[:5], 1, 128, 128, 2, 2, 64, -1.0, 0, None, None, 0, None) == 1
+
+
+def test_wait_timeout_setting(fa):
+    old = fa.set_wait_timeout_ns(123456789)
+    assert fa.set_wait_timeout_ns(0) == 123456789
+    fa.set_wait_timeout_ns(old)
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import attention_backward_preprocess_gb300 as mod
+    monkeypatch.setattr(mod, "_lib", None)
+    monkeypatch.setattr(mod, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        mod.lib()

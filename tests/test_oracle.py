@@ -66,6 +66,7 @@ MUTANTS = {
     "GQA head mapping": ("int hk = h / p->G;\n    return p->scale",
                          "int hk = h % p->Hkv;\n    return p->scale"),
     "Dv from q": ("return dot(doi, o_scratch, p->D);", "return dot(doi, p->q + row_q(p, b, i, h), p->D);"),
+    "preprocess skips the LSE guard": ("if (lse == -INFINITY) lse = 0.0; /* get_validated_lse */", ""),
     "LSE drops max shift": ("double lse = m + log(sum);", "double lse = log(sum);"),
     "score without scale": ("return p->scale * dot(", "return dot("),
     "varlen lse index": ("if (p->cu_q) return (long)h * p->total_q + p->cu_q[b] + s;",
