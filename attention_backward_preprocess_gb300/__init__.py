@@ -63,7 +63,7 @@ def lib():
         L.fa_bwd_with_workspace.argtypes = ([_vp] * 9 + _SHAPE + [_f, _i, _vp, _vp, _i, _i, _vp,
                                                                   _sz, _vp])
         L.fa_bwd_preprocess.argtypes = [_vp] * 3 + _SHAPE + [_vp, _vp, _i, _i, _vp, _sz, _vp]
-        L.fa_bwd_main.argtypes = [_vp] * 5 + _SHAPE + [_f, _i, _vp, _vp, _i, _i, _vp, _sz, _vp]
+        L.fa_bwd_main.argtypes = [_vp] * 6 + _SHAPE + [_f, _i, _vp, _vp, _i, _i, _vp, _sz, _vp]
         L.fa_bwd_postprocess.argtypes = [_vp] + _SHAPE + [_f, _vp, _vp, _i, _i, _vp, _sz, _vp]
         L.fa_bwd_workspace_layout.argtypes = _SHAPE + [_i, _i] + [ctypes.POINTER(_sz)] * 4
         L.fa_fwd.argtypes = [_vp] * 5 + _SHAPE + [_f, _i, _vp, _vp, _i, _vp]
@@ -202,7 +202,8 @@ def fa_bwd_stages(q, k, v, o, dout, lse, workspace, causal=False, softmax_scale=
         _check(L.fa_bwd_preprocess(_ptr(o), _ptr(dout), _ptr(lse), *shape, *cu, det, dt, *ws),
                "fa_bwd_preprocess")
     if "main" in stages:
-        _check(L.fa_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(dk), _ptr(dv), *shape, scale,
+        _check(L.fa_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dk), _ptr(dv), *shape,
+                             scale,
                              int(bool(causal)), *cu, det, dt, *ws), "fa_bwd_main")
     if "post" in stages:
         _check(L.fa_bwd_postprocess(_ptr(dq), *shape, scale, *cu, det, dt, *ws),

@@ -249,7 +249,7 @@ int sm_count() {
 }
 
 fa_status run_preprocess(const Prepared &P, fa_dtype dtype, cudaStream_t stream) {
-    if (cudaMemsetAsync(P.p.err, 0, sizeof(int), stream) != cudaSuccess) return FA_ERR_CUDA;
+    if (!P.p.o || !P.p.dout || !P.p.lse) return FA_ERR_INVALID_ARG;
     return cuda_status(fa::launch_preprocess(P.p, dtype == FA_BF16, stream));
 }
 
@@ -261,6 +261,7 @@ fa_status run_main(const Prepared &P, fa_dtype dtype, cudaStream_t stream) {
     const long long rq = p.varlen ? P.total_q : p.Sq, rk = p.varlen ? P.total_k : p.Sk;
     const int nb = p.varlen ? 1 : p.B;
     if (rq <= 0 || rk <= 0) return FA_ERR_INVALID_ARG;
+    if (!p.q || !p.k || !p.v || !p.dout || !p.dk || !p.dv) return FA_ERR_INVALID_ARG;
     if (!encode_rows_map(&mq, p.q, p.D, p.Hq, rq, nb, bm, bf16) ||
         !encode_rows_map(&mdo, p.dout, p.D, p.Hq, rq, nb, bm, bf16) ||
         !encode_rows_map(&mk, p.k, p.D, p.Hkv, rk, nb, fa::kBlockN, bf16) ||
@@ -273,6 +274,7 @@ fa_status run_main(const Prepared &P, fa_dtype dtype, cudaStream_t stream) {
 }
 
 fa_status run_postprocess(const Prepared &P, fa_dtype dtype, cudaStream_t stream) {
+    if (!P.p.dq) return FA_ERR_INVALID_ARG;
     return cuda_status(fa::launch_postprocess(P.p, dtype == FA_BF16, stream));
 }
 
@@ -339,14 +341,14 @@ fa_status fa_bwd_preprocess(const void *o, const void *dout, const float *lse, i
     return run_preprocess(P, dtype, stream);
 }
 
-fa_status fa_bwd_main(const void *q, const void *k, const void *v, void *dk, void *dv, int B,
-                      int Sq, int Sk, int Hq, int Hkv, int D, float softmax_scale, int causal,
-                      const int *cu_seqlens_q, const int *cu_seqlens_k, int deterministic,
-                      fa_dtype dtype, void *workspace, size_t workspace_bytes,
-                      cudaStream_t stream) {
-    if (!q || !k || !v || !dk || !dv) return FA_ERR_INVALID_ARG;
+fa_status fa_bwd_main(const void *q, const void *k, const void *v, const void *dout, void *dk,
+                      void *dv, int B, int Sq, int Sk, int Hq, int Hkv, int D,
+                      float softmax_scale, int causal, const int *cu_seqlens_q,
+                      const int *cu_seqlens_k, int deterministic, fa_dtype dtype,
+                      void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!q || !k || !v || !dout || !dk || !dv) return FA_ERR_INVALID_ARG;
     Prepared P;
-    fa_status st = prepare(q, k, v, nullptr, nullptr, nullptr, nullptr, dk, dv, B, Sq, Sk, Hq, Hkv,
+    fa_status st = prepare(q, k, v, nullptr, dout, nullptr, nullptr, dk, dv, B, Sq, Sk, Hq, Hkv,
                            D, softmax_scale, causal, cu_seqlens_q, cu_seqlens_k, deterministic,
                            dtype, workspace, workspace_bytes, stream, &P);
     if (st != FA_OK) return st;

@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(BwdParams p) {
     const int s = (int)(rid / p.Hq), h = (int)(rid % p.Hq);
     // no early return: the row sum below is a full-warp shuffle
     const bool active = s < lq_round;
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.err = 0;   // per-call error word
     const long long wr = active ? ws_row(p, b, h, s) : 0;
     float acc = 0.f;
     if (active && s < lq) {

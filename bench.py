@@ -1,0 +1,371 @@
+"""Benchmark of the GB300 fused attention backward (one JSON line on rank 0).
+
+A step is one whole backward pass -- preprocess, main kernel, postprocess --
+over the workload the headline metric is quoted on: B=2, Hq=32, Hkv=8 (GQA),
+Sq=Sk=8192, D=128, bf16, causal (seeded synthetic inputs; O and LSE from the
+library's forward, outside the timed region).  The inputs of a step (Q, K, V,
+O, dO: about 470 MB) are larger than the 129 MB L2, so no flush is needed
+between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+value  : TFLOPS over all ranks, FLOP = 10*B*Hq*Sq*Sk*D / 2 (causal), device
+         time from CUDA events with inputs resident in HBM
+e2e    : the same metric through fa_bwd with host (pinned) buffers: each step
+         copies its inputs in and its outputs (dQ, dK, dV) out
+roofline: the main kernel (a dense contraction, tensor-bound) against the
+         measured dense bf16 peak
+cpu_baseline: the fp64 CPU oracle, as it stands, on a bounded sample (a causal
+         prefix of one kv-head group), timed on this host's cores
+--impl reference: the same metric for the oracle alone (the reference arm).
+
+Multi-GPU (torchrun, N>1): independent replicas of the workload, one per GPU,
+no collective on the data path ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attn-bwd TFLOPS/GPU (10·B·H·Sq·Sk·D, causal halved) and % of bf16 tensor peak"
+UNIT = "TFLOPS"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(bf16=d["bf16_tflops"], bf16_sustained=d.get("bf16_tflops_sustained"),
+                    hbm=d["hbm_gbs"], source="measured")
+    return dict(bf16=1900.0, bf16_sustained=1700.0, hbm=6800.0, source="fallback")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, path: str):
+        self.path = path
+        self.proc = None
+        try:
+            self.fh = open(path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-i", str(device_index), "-lms", "200"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(w, inputs_cpu, prefix: int):
+    """Times the oracle's backward on a causal prefix of one kv-head group.
+
+    Sample: batch 0, kv head 0 with its G query heads, positions [0, prefix);
+    the oracle recomputes its own fp64 forward.  Returns (TFLOPS, seconds, cores)."""
+    import numpy as np
+
+    import oracle
+    from attention_backward_preprocess_gb300.workloads import bwd_flops
+    G = w.Hq // w.Hkv
+    q = inputs_cpu["q"][:1, :prefix, :G].double().numpy()
+    k = inputs_cpu["k"][:1, :prefix, :1].double().numpy()
+    v = inputs_cpu["v"][:1, :prefix, :1].double().numpy()
+    do = inputs_cpu["dout"][:1, :prefix, :G].double().numpy()
+    sub = w.with_(B=1, Sq=prefix, Sk=prefix, Hq=G, Hkv=1)
+    cores = oracle.max_threads()
+    t0 = time.perf_counter()
+    oracle.backward(q, k, v, do, w.softmax_scale, w.causal)
+    dt = time.perf_counter() - t0
+    tflops = bwd_flops(sub) / dt / 1e12
+    return tflops, dt, cores, ("oracle fp64 backward (own forward) on seeded inputs shaped like "
+                               "%s: 1 kv head with its %d query heads, %d positions, %s "
+                               "(%.3g algorithmic FLOP)" % (w.name, G, prefix,
+                                                            "causal" if w.causal else "full",
+                                                            bwd_flops(sub)))
+
+
+def run_reference(args, w):
+    """The reference arm: the CPU oracle as it stands, on a bounded sample per step."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import torch
+
+    from attention_backward_preprocess_gb300.workloads import generate
+    x = generate(w.with_(B=1, Sq=args.ref_prefix, Sk=args.ref_prefix), "cpu")
+    times, vals = [], []
+    for i in range(args.warmup + args.steps):
+        tf, dt, cores, sample = cpu_baseline(w, x, args.ref_prefix)
+        if i >= args.warmup:
+            times.append(dt)
+            vals.append(tf)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, torch.Generator)",
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def config_of(w):
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk,
+            "D": w.D, "causal": w.causal, "deterministic": w.deterministic,
+            "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--cpu-prefix", type=int, default=4096)
+    ap.add_argument("--ref-prefix", type=int, default=1024)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from attention_backward_preprocess_gb300.workloads import BENCH_WORKLOAD, WORKLOADS
+    w = WORKLOADS[args.workload or BENCH_WORKLOAD]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+
+    import attention_backward_preprocess_gb300 as fa
+    from attention_backward_preprocess_gb300.workloads import bwd_flops, generate
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    fa.lib()
+    if w.varlen is not None:
+        raise SystemExit("bench.py times dense workloads only")
+
+    x = generate(w, dev)
+    q, k, v, do = x["q"], x["k"], x["v"], x["dout"]
+    o, lse = fa.fa_fwd(q, k, v, causal=w.causal, softmax_scale=w.softmax_scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nbytes = fa.workspace_bytes(w.B, w.Sq, w.Sk, w.Hq, w.Hkv, w.D,
+                                deterministic=w.deterministic)
+    work = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    flops = bwd_flops(w)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fa.fa_bwd_stages(q, k, v, o, do, lse, work, causal=w.causal,
+                         softmax_scale=w.softmax_scale, deterministic=w.deterministic,
+                         dq=dq, dk=dk, dv=dv, stages=("pre",))
+        e1.record(stream)
+        fa.fa_bwd_stages(q, k, v, o, do, lse, work, causal=w.causal,
+                         softmax_scale=w.softmax_scale, deterministic=w.deterministic,
+                         dq=dq, dk=dk, dv=dv, stages=("main",))
+        e2.record(stream)
+        fa.fa_bwd_stages(q, k, v, o, do, lse, work, causal=w.causal,
+                         softmax_scale=w.softmax_scale, deterministic=w.deterministic,
+                         dq=dq, dk=dk, dv=dv, stages=("post",))
+
+    e1 = torch.cuda.Event(enable_timing=True)
+    e2 = torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert fa.device_status(work) == fa.FA_OK
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    clocks = ClockSampler(dev.index, os.path.join(ROOT, "gpurun_out", "bench_clocks.csv")
+                          if os.path.isdir(os.path.join(ROOT, "gpurun_out"))
+                          else "/tmp/bench_clocks.%d.csv" % os.getpid())
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        a, b_, c, d = ev[i]
+        e1, e2 = b_, c
+        a.record(stream)
+        step()
+        d.record(stream)
+    end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(end)
+    pre_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    main_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    post_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(args.steps)]
+    status = fa.device_status(work)
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = flops * ws / (ms_per_step * 1e-3) / 1e12
+
+    # ---------------------------------------------------------------- e2e
+    e2e = None
+    if not args.no_e2e:
+        host = {n: t.cpu().pin_memory() for n, t in (("q", q), ("k", k), ("v", v), ("o", o),
+                                                   ("dout", do), ("lse", lse))}
+        dev_in = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+        outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (q, k, v)]
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = sum(t.numel() * t.element_size() for t in outs_h)
+        e2e_steps = max(3, min(args.steps, 10))
+
+        def e2e_step():
+            for n in host:
+                dev_in[n].copy_(host[n], non_blocking=True)
+            gq, gk, gv = fa.fa_bwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["o"],
+                                   dev_in["dout"], dev_in["lse"], causal=w.causal,
+                                   softmax_scale=w.softmax_scale, deterministic=w.deterministic,
+                                   dq=dq, dk=dk, dv=dv)
+            for hbuf, g in zip(outs_h, (gq, gk, gv)):
+                hbuf.copy_(g, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        s2 = torch.cuda.Event(enable_timing=True)
+        t2 = torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        t2.record(stream)
+        barrier()
+        e2e_ms = s2.elapsed_time(t2) / e2e_steps
+        if ws > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": e2e_steps}
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    pk = peaks()
+    main_avg = statistics.mean(main_ms)
+    achieved = flops / (main_avg * 1e-3) / 1e12
+    elems_q = w.B * w.Sq * w.Hq * w.D
+    rows = w.B * w.Hq * w.Sq
+    pre_bytes = 2 * elems_q * 2 + rows * 4 * 2 + rows * 4 + elems_q * 4    # O, dO in; LSE in; Dv, LSE2 out; dQaccum zero
+    post_bytes = elems_q * 4 + elems_q * 2
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "main_kernel_traffic.json")
+    if os.path.exists(tpath):
+        t = json.load(open(tpath))
+        if t.get("workload") == w.name and t.get("kernel_source_hash") == source_hash():
+            traffic = t.get("dram_bytes_per_launch")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "fp16",
+        "data": "synthetic (seeded N(0,1), torch.Generator on device)",
+        "config": config_of(w),
+        "pct_of_bf16_peak": 100.0 * value / ws / pk["bf16"],
+        "roofline": {"kernel": "bwd_main_kernel", "bound": "tensor", "achieved": achieved,
+                     "peak": pk["bf16"], "unit": "TFLOP/s", "frac": achieved / pk["bf16"],
+                     "traffic": traffic,
+                     "peak_note": "%s dense bf16 burst (bf16_tflops); sustained %s" % (
+                         pk["source"], pk["bf16_sustained"]),
+                     "algorithmic_flop_per_launch": flops},
+        "kernels_ms": {"preprocess": statistics.mean(pre_ms), "main": main_avg,
+                       "postprocess": statistics.mean(post_ms)},
+        "kernels_gbs": {"preprocess": pre_bytes / (statistics.mean(pre_ms) * 1e-3) / 1e9,
+                        "postprocess": post_bytes / (statistics.mean(post_ms) * 1e-3) / 1e9,
+                        "hbm_peak": pk["hbm"]},
+        "gpu_launches": 4 * args.steps,
+        "device_status": status,
+        "e2e": e2e,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        xs = generate(w.with_(B=1, Sq=args.cpu_prefix, Sk=args.cpu_prefix), "cpu")
+        tf, dt, cores, sample = cpu_baseline(w, xs, args.cpu_prefix)
+        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "seconds": dt, "sample": sample}
+    print(json.dumps(line))
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("fa_bwd_main.cu", "fa_device.cuh", "fa_params.h"):
+        h.update(open(os.path.join(ROOT, "attention_backward_preprocess_gb300", "csrc", f),
+                      "rb").read())
+    return h.hexdigest()[:16]
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -98,8 +98,9 @@ fa_status fa_bwd_preprocess(const void *o, const void *dout, const float *lse, i
                             int Sk, int Hq, int Hkv, int D, const int *cu_seqlens_q,
                             const int *cu_seqlens_k, int deterministic, fa_dtype dtype,
                             void *workspace, size_t workspace_bytes, cudaStream_t stream);
-fa_status fa_bwd_main(const void *q, const void *k, const void *v, void *dk, void *dv, int B,
-                      int Sq, int Sk, int Hq, int Hkv, int D, float softmax_scale, int causal,
+fa_status fa_bwd_main(const void *q, const void *k, const void *v, const void *dout, void *dk,
+                      void *dv, int B, int Sq, int Sk, int Hq, int Hkv, int D,
+                      float softmax_scale, int causal,
                       const int *cu_seqlens_q, const int *cu_seqlens_k, int deterministic,
                       fa_dtype dtype, void *workspace, size_t workspace_bytes,
                       cudaStream_t stream);

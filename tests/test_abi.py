@@ -94,6 +94,19 @@ def test_fa_bwd_rejects_before_device(fa):
     assert L.fa_fwd(*ptrs[:5], 1, 128, 128, 2, 2, 64, -1.0, 0, None, None, 0, None) == 1
 
 
+def test_stage_entry_points_reject_null_tensors(fa):
+    L = fa.lib()
+    vp = ctypes.c_void_p
+    ws = vp(0x100000)
+    shape = (1, 128, 128, 2, 2, 64)
+    # fa_bwd_main needs q, k, v, dout, dk, dv
+    assert L.fa_bwd_main(vp(0x1000), vp(0x2000), vp(0x3000), None, vp(0x5000), vp(0x6000),
+                         *shape, 0.125, 0, None, None, 0, 0, ws, 1 << 40, None) == 1
+    assert L.fa_bwd_preprocess(vp(0x1000), None, vp(0x3000), *shape, None, None, 0, 0, ws,
+                               1 << 40, None) == 1
+    assert L.fa_bwd_postprocess(None, *shape, 0.125, None, None, 0, 0, ws, 1 << 40, None) == 1
+
+
 def test_wait_timeout_setting(fa):
     old = fa.set_wait_timeout_ns(123456789)
     assert fa.set_wait_timeout_ns(0) == 123456789
