@@ -19,6 +19,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfa_gb300.so")
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+FA_ERR_SCRATCH_LIMIT = 5
 FA_BF16, FA_FP16 = 0, 1
 
 # entry points declared in include/fa.h and include/fa_selftest.h
@@ -26,7 +27,7 @@ EXPORTED = [
     "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_with_workspace", "fa_bwd_preprocess",
     "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_workspace_layout", "fa_fwd",
     "fa_device_status", "fa_set_wait_timeout_ns", "fa_status_string",
-    "fa_selftest_umma", "fa_selftest_semaphore",
+    "fa_selftest_umma", "fa_selftest_semaphore", "fa_bwd_noalloc", "fa_bwd_noalloc_scratch_bytes",
 ]
 
 
@@ -72,6 +73,10 @@ def lib():
         L.fa_set_wait_timeout_ns.restype = ctypes.c_longlong
         L.fa_status_string.argtypes = [_i]
         L.fa_status_string.restype = ctypes.c_char_p
+        L.fa_bwd_noalloc.argtypes = [_vp] * 9 + _SHAPE + [_f, _i, _vp, _vp, _i, _i, _vp]
+        L.fa_bwd_noalloc.restype = _i
+        L.fa_bwd_noalloc_scratch_bytes.argtypes = []
+        L.fa_bwd_noalloc_scratch_bytes.restype = _sz
         L.fa_selftest_umma.argtypes = [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]
         L.fa_selftest_semaphore.argtypes = [_vp, _i, ctypes.c_longlong, _vp, _vp]
         for name in ("fa_bwd", "fa_bwd_with_workspace", "fa_bwd_preprocess", "fa_bwd_main",
@@ -167,6 +172,26 @@ def fa_bwd(q, k, v, o, dout, lse, causal=False, softmax_scale=None, cu_seqlens_q
                                           _stream(stream))
         _check(st, "fa_bwd_with_workspace")
     return dq, dk, dv
+
+
+def noalloc_scratch_bytes() -> int:
+    """Size of the fixed scratch array fa_bwd_noalloc works in."""
+    return int(lib().fa_bwd_noalloc_scratch_bytes())
+
+
+def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, causal=False, softmax_scale=None,
+                   cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None,
+                   deterministic=False, stream=None) -> int:
+    """fa_bwd without any device allocation, for callers that cannot allocate
+    device memory at call time (its scratch is a fixed array inside the
+    library; see include/fa.h).  The outputs must be given.  Returns the
+    status (FA_OK, or FA_ERR_SCRATCH_LIMIT for a problem too large)."""
+    B, Sq, Sk, Hq, Hkv, D = _shape(q, k, cu_seqlens_q, max_seqlen_q, max_seqlen_k)
+    scale = default_scale(D) if softmax_scale is None else float(softmax_scale)
+    return int(lib().fa_bwd_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+        B, Sq, Sk, Hq, Hkv, D, scale, int(bool(causal)), _ptr(cu_seqlens_q),
+        _ptr(cu_seqlens_k), int(bool(deterministic)), _dtype_code(q), _stream(stream)))
 
 
 def workspace_bytes(B, Sq, Sk, Hq, Hkv, D, varlen=False, deterministic=False) -> int:

@@ -298,6 +298,7 @@ const char *fa_status_string(fa_status s) {
     case FA_ERR_UNSUPPORTED: return "unsupported configuration";
     case FA_ERR_CUDA: return "CUDA error";
     case FA_ERR_TIMEOUT: return "device-side wait timed out";
+    case FA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the fixed no-alloc array";
     }
     return "unknown status";
 }

@@ -60,7 +60,9 @@ typedef enum {
     FA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misalignment, bad scale */
     FA_ERR_UNSUPPORTED = 2,  /* head dim not in {64, 128}, dtype, or GPU not sm_103 */
     FA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
-    FA_ERR_TIMEOUT = 4       /* a bounded device-side wait ran out */
+    FA_ERR_TIMEOUT = 4,      /* a bounded device-side wait ran out */
+    FA_ERR_SCRATCH_LIMIT = 5 /* fa_bwd_noalloc: the problem needs more scratch than
+                                FA_NOALLOC_SCRATCH_BYTES */
 } fa_status;
 
 typedef enum { FA_BF16 = 0, FA_FP16 = 1 } fa_dtype;
@@ -140,6 +142,42 @@ fa_status fa_device_status(void *workspace, cudaStream_t stream);
 long long fa_set_wait_timeout_ns(long long ns);
 
 const char *fa_status_string(fa_status s);
+
+/* ---------------------------------------------------------------------------
+ * Allocation-free backward.  The attention-backward pages have no counterpart
+ * to this entry point; it exists for callers that cannot allocate device
+ * memory when they call the library: an inference-engine plugin whose enqueue
+ * step must not allocate, a framework that owns all device memory through its
+ * own pool and allows no other allocation, or a latency-critical loop that
+ * must not enter the driver's allocator (which can synchronise the device).
+ *
+ * fa_bwd_noalloc takes the same arguments as fa_bwd and computes the same
+ * result, but its scratch (Dv, LSE2, the fp32 dQ accumulator, the work-unit
+ * list, the error word) is a fixed device array of FA_NOALLOC_SCRATCH_BYTES
+ * compiled into the library, which every GPU that loads the library holds
+ * until the process exits.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *   - Problems whose scratch (fa_bwd_workspace_bytes of the same sizes) is
+ *     larger than FA_NOALLOC_SCRATCH_BYTES are rejected with
+ *     FA_ERR_SCRATCH_LIMIT before anything runs.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and remembers it; make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array and leaves its contents behind; each
+ *     call re-initialises what must start at zero, so no clearing is needed
+ *     between calls, but calls that overlap on the GPU (other streams, other
+ *     host threads) race on the array and must be serialised by the caller.
+ * ------------------------------------------------------------------------- */
+#define FA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/* FA_NOALLOC_SCRATCH_BYTES, for callers that load the library dynamically. */
+size_t fa_bwd_noalloc_scratch_bytes(void);
+
+fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                         const void *dout, const float *lse, void *dq, void *dk, void *dv, int B,
+                         int Sq, int Sk, int Hq, int Hkv, int D, float softmax_scale, int causal,
+                         const int *cu_seqlens_q, const int *cu_seqlens_k, int deterministic,
+                         fa_dtype dtype, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(fa):
 
 
 def test_status_strings(fa):
-    for s in range(5):
+    for s in range(6):
         assert fa.status_string(s)
     assert fa.status_string(99) == "unknown status"
 
