@@ -223,8 +223,10 @@ fa_status prepare(const void *q, const void *k, const void *v, const void *o, co
     p.cu_q = cu_q; p.cu_k = cu_k;
     p.err = reinterpret_cast<int *>(w + L.err);
     p.ntiles = reinterpret_cast<int *>(w + L.ntiles);
+    p.unit_counter = reinterpret_cast<int *>(w + L.ntiles) + 1;
     p.tiles = reinterpret_cast<int4 *>(w + L.tiles);
     p.max_tiles = L.max_tiles;
+    p.num_units = L.max_tiles;
     p.dvec = reinterpret_cast<float *>(w + L.dvec);
     p.lse2 = reinterpret_cast<float *>(w + L.lse2);
     p.dqacc = reinterpret_cast<float *>(w + L.dqacc);
@@ -267,8 +269,10 @@ fa_status run_main(const Prepared &P, fa_dtype dtype, cudaStream_t stream) {
         !encode_rows_map(&mk, p.k, p.D, p.Hkv, rk, nb, fa::kBlockN, bf16) ||
         !encode_rows_map(&mv, p.v, p.D, p.Hkv, rk, nb, fa::kBlockN, bf16))
         return FA_ERR_CUDA;
-    cudaError_t e = fa::launch_schedule(p, stream);
-    if (e != cudaSuccess) return FA_ERR_CUDA;
+    if (p.varlen) {
+        // the unit list depends on the device-resident cu_seqlens
+        if (fa::launch_schedule(p, stream) != cudaSuccess) return FA_ERR_CUDA;
+    }
     const int grid = (int)std::min<long long>(p.max_tiles, sm_count());
     return cuda_status(fa::launch_bwd_main(p, mq, mk, mv, mdo, bf16, grid, stream));
 }

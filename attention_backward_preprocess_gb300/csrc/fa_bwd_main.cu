@@ -45,19 +45,53 @@ struct MainCfg {
     static constexpr int D = kD;
     static constexpr int BN = kBlockN;                 // keys per unit
     static constexpr int BM = (kD == 128) ? 64 : 128;  // queries per step
+    static constexpr int HALF = BM / 2;                // query columns per softmax group
+    static constexpr int NCH = HALF / 32;              // 32-column chunks per group
     // dQ GEMM orientation: the MMA's M (=128) is d when D = 128 (dQ^T = K^T dS^T,
     // TMEM lanes = d) and the query row when D = 64 (dQ = dS K, lanes = query).
     static constexpr bool kDqT = (kD == 128);
-    static constexpr int kStages = 2;
+    // Two-deep software pipeline (D = 128): S^T, dP^T and dS^T are double
+    // buffered, so the MMAs of step i+1 (S, dP) run while the softmax warps
+    // turn step i's dP into dS.  TMEM (512 columns):
+    //   dK 128 | dV 128 | S^T x2 (64 each; P^T bf16 and dS^T bf16 written back
+    //   into each buffer) | X x2 (64 each; dP^T of a step, then its dQ^T).
+    // D = 64 (BM = 128) has no room for second buffers and runs the steps one
+    // after the other: dK 64 | dV 64 | S^T 128 | dP^T 128 | dQ 64.
+    static constexpr bool kPipe = (kD == 128);
+    static constexpr int kBuf = kPipe ? 2 : 1;
+    static constexpr int kStages = kPipe ? 3 : 4;
     static constexpr int kThreads = 14 * 32;
-    // tensor-memory columns
     static constexpr int TM_DK = 0;
     static constexpr int TM_DV = D;
-    static constexpr int TM_S = 2 * D;            // S^T fp32, then P^T bf16 in place
-    static constexpr int TM_DP = 2 * D + BM;      // dP^T fp32, then dS^T bf16 in place
-    static constexpr int TM_DQ = 2 * D + 2 * BM;  // 64 fp32 columns
+    static constexpr int TM_S = 2 * D;
+    static constexpr int TM_X = TM_S + kBuf * BM;          // kPipe: dP then dQ per buffer
+    static constexpr int TM_DP = TM_S + BM;                // !kPipe
+    static constexpr int TM_DQ = TM_S + 2 * BM;            // !kPipe
     static constexpr int TM_COLS = 512;
-    static_assert(TM_DQ + 64 <= TM_COLS, "tensor memory overflow");
+    static_assert(kPipe ? (TM_X + 2 * BM <= TM_COLS) : (TM_DQ + 64 <= TM_COLS), "TMEM overflow");
+    // columns (buffer b, softmax group g, 32-query chunk ch)
+    static __device__ __forceinline__ int s_col(int b, int g, int ch) {
+        return kPipe ? TM_S + b * BM + g * HALF : TM_S + g * HALF + 32 * ch;
+    }
+    static __device__ __forceinline__ int p_col(int b, int g, int ch) {   // P^T bf16 pairs
+        return kPipe ? TM_S + b * BM + g * HALF : TM_S + g * HALF + 16 * ch;
+    }
+    static __device__ __forceinline__ int dp_col(int b, int g, int ch) {
+        return kPipe ? TM_X + b * BM + g * HALF : TM_DP + g * HALF + 32 * ch;
+    }
+    static __device__ __forceinline__ int ds_col(int b, int g, int ch) {  // dS^T bf16 pairs
+        return kPipe ? TM_S + b * BM + g * HALF + 16 : TM_DP + g * HALF + 16 * ch;
+    }
+    static __device__ __forceinline__ int dq_col(int b) { return kPipe ? TM_X + b * BM : TM_DQ; }
+    // A-operand column of MMA K step kk (queries 16kk .. 16kk+15) of P^T / dS^T
+    static __device__ __forceinline__ int p_op(int b, int kk) {
+        const int g = (16 * kk) / HALF;
+        return p_col(b, g, 0) + (16 * kk - g * HALF) / 2;
+    }
+    static __device__ __forceinline__ int ds_op(int b, int kk) {
+        const int g = (16 * kk) / HALF;
+        return ds_col(b, g, 0) + (16 * kk - g * HALF) / 2;
+    }
     // shared memory (byte offsets from a 1024-aligned base)
     static constexpr int KV_BYTES = BN * D * 2;
     static constexpr int QO_BYTES = BM * D * 2;
@@ -67,44 +101,91 @@ struct MainCfg {
     static constexpr int OFF_Q = OFF_V + KV_BYTES;
     static constexpr int OFF_DO = OFF_Q + kStages * QO_BYTES;
     static constexpr int OFF_DS = OFF_DO + kStages * QO_BYTES;
-    static constexpr int OFF_LSE = OFF_DS + DS_BYTES;
+    static constexpr int OFF_LSE = OFF_DS + kBuf * DS_BYTES;
     static constexpr int OFF_DV = OFF_LSE + kStages * BM * 4;
     static constexpr int OFF_BAR = OFF_DV + kStages * BM * 4;
-    static constexpr int NUM_BARS = 16 + 2 * kStages;
-    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int NUM_BARS = 48;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // TMEM slot, abort flag, unit ring
     static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+    static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
+    static constexpr int kRing = 4;             // work-unit hand-off ring depth
+    static constexpr int kConsumerWarps = 13;   // MMA + 4 reducers + 8 softmax warps
     static constexpr uint32_t IDESC_S = make_idesc(128, BM, Cvt<T>::is_bf16, false, false);
     static constexpr uint32_t IDESC_KV = make_idesc(128, D, Cvt<T>::is_bf16, false, true);
     static constexpr uint32_t IDESC_DQ = make_idesc(128, 64, Cvt<T>::is_bf16, true, true);
 };
 
-// barrier indices
+// Barrier indices.  Hand-offs that can be committed before their waiter has
+// looked at the previous phase come in pairs, one per TMEM buffer, so that no
+// barrier ever runs two phases ahead of a waiter.
 enum {
-    B_KV_FULL = 0, B_KV_EMPTY, B_S_FULL, B_P_FULL, B_DP_FULL, B_DS_FULL, B_DQ_FULL, B_DQ_EMPTY,
-    B_ACC_FULL, B_ACC_EMPTY, B_DRAIN, B_STAGE0
+    B_KV_FULL = 0, B_KV_EMPTY = 1,
+    B_S_FULL = 2,    // +b
+    B_P_FULL = 4,    // +b
+    B_DP_FULL = 6,   // +b
+    B_DS_FULL = 8,   // +b
+    B_DQ_FULL = 10,  // +b
+    B_DQ_EMPTY = 12, // +b
+    B_ACC_FULL = 14, B_ACC_EMPTY = 15, B_DRAIN = 16,
+    B_UNIT_FULL = 17,   // +k, k < kRing: unit index k of the ring written
+    B_UNIT_EMPTY = 21,  // +k: every consumer warp has read it
+    B_STAGE0 = 25       // full[kStages], then empty[kStages]
 };
+
+// Work units are handed out dynamically: the producer warp takes the next
+// index from a global counter and passes it to the other warps of the CTA
+// through a small ring in shared memory.  Units leave the counter in
+// n_block-major order, so the units of one (sequence, kv head) that run at the
+// same time started close together and sweep the same rows of Q, dO and the
+// dQ accumulator in L2; idle CTAs take the next unit, which balances the
+// uneven causal work.  -1 ends the sequence.
+struct UnitRing {
+    volatile int *slot;   // kRing ints in shared memory
+    uint32_t full0, empty0;
+    int k = 0;
+    uint32_t ph = 0;
+    __device__ __forceinline__ void advance(int ring) {
+        if (++k == ring) { k = 0; ph ^= 1; }
+    }
+};
+
+__device__ __forceinline__ uint32_t bit(uint32_t mask, int b) { return (mask >> b) & 1u; }
 
 struct Unit {
     int b, n_block, hk;
     int lq, lk;
     int q_row0, k_row0, bidx;   // TMA row offset and batch coordinate
     int m_begin, nm, iters;     // row blocks [m_begin, m_begin + nm) per head; iters = G * nm
+    // Iteration order: row blocks from the last to the first, the G query
+    // heads of the group innermost.  Under a causal mask every unit of a
+    // (sequence, kv head) starts at the same last row block, so the units
+    // that run side by side sweep the same Q / dO / dQ-accumulator rows
+    // together and share them in L2.
+    __device__ __forceinline__ int g_of(int it, int G) const { return it % G; }
+    __device__ __forceinline__ int m_of(int it, int G) const { return m_begin + nm - 1 - it / G; }
 };
 
+// Work unit t: dense problems enumerate (n_block, batch, kv head) with the
+// n_block slowest; varlen problems read the list the scheduler kernel wrote.
 template <int BM>
 __device__ __forceinline__ Unit decode_unit(const BwdParams &p, int t) {
     Unit u;
-    const int4 e = p.tiles[t];
-    u.b = e.x;
-    u.n_block = e.y;
-    u.hk = e.z;
     if (p.varlen) {
+        const int4 e = p.tiles[t];
+        u.b = e.x;
+        u.n_block = e.y;
+        u.hk = e.z;
         u.q_row0 = p.cu_q[u.b];
         u.k_row0 = p.cu_k[u.b];
         u.lq = p.cu_q[u.b + 1] - u.q_row0;
         u.lk = p.cu_k[u.b + 1] - u.k_row0;
         u.bidx = 0;
     } else {
+        const int per_n = p.B * p.Hkv;
+        u.n_block = t / per_n;
+        const int r = t - u.n_block * per_n;
+        u.b = r / p.Hkv;
+        u.hk = r - u.b * p.Hkv;
         u.q_row0 = 0;
         u.k_row0 = 0;
         u.lq = p.Sq;
@@ -130,7 +211,7 @@ template <int kD, typename T>
 __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
     bwd_main_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ MainMaps maps) {
     using C = MainCfg<kD, T>;
-    constexpr int D = C::D, BM = C::BM, BN = C::BN, S = C::kStages;
+    constexpr int D = C::D, BM = C::BM, BN = C::BN, S = C::kStages, HALF = C::HALF, NCH = C::NCH;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -146,15 +227,21 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         *abort_flag = 0;
         mbar_init(bar(B_KV_FULL), 1);
         mbar_init(bar(B_KV_EMPTY), 1);
-        mbar_init(bar(B_S_FULL), 1);
-        mbar_init(bar(B_P_FULL), 8);
-        mbar_init(bar(B_DP_FULL), 1);
-        mbar_init(bar(B_DS_FULL), 8);
-        mbar_init(bar(B_DQ_FULL), 1);
-        mbar_init(bar(B_DQ_EMPTY), 4);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(B_S_FULL + b), 1);
+            mbar_init(bar(B_P_FULL + b), 8);
+            mbar_init(bar(B_DP_FULL + b), 1);
+            mbar_init(bar(B_DS_FULL + b), 8);
+            mbar_init(bar(B_DQ_FULL + b), 1);
+            mbar_init(bar(B_DQ_EMPTY + b), 4);
+        }
         mbar_init(bar(B_ACC_FULL), 1);
         mbar_init(bar(B_ACC_EMPTY), 8);
         mbar_init(bar(B_DRAIN), 1);
+        for (int k = 0; k < C::kRing; ++k) {
+            mbar_init(bar(B_UNIT_FULL + k), 1);
+            mbar_init(bar(B_UNIT_EMPTY + k), C::kConsumerWarps);
+        }
         for (int s = 0; s < S; ++s) {
             mbar_init(bar(B_STAGE0 + s), 1);          // full: producer expect_tx
             mbar_init(bar(B_STAGE0 + S + s), 1 + 8);  // empty: MMA commit + 8 softmax warps
@@ -176,7 +263,24 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const WaitCtl w{abort_flag, p.err, p.budget_ns};
-    const int ntiles = *p.ntiles;
+    const int ntiles = p.varlen ? *p.ntiles : p.num_units;
+    UnitRing ring;
+    ring.slot = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 32);
+    ring.full0 = bar(B_UNIT_FULL);
+    ring.empty0 = bar(B_UNIT_EMPTY);
+    // consumer side: next unit index (whole warp, converged), -1 at the end or on abort
+    auto next_unit = [&]() -> int {
+        int t = -1;
+        if (lane == 0) {
+            if (mbar_wait(ring.full0 + 8u * ring.k, ring.ph, w)) {
+                t = ring.slot[ring.k];
+                mbar_arrive(ring.empty0 + 8u * ring.k);
+            }
+        }
+        t = __shfl_sync(0xffffffffu, t, 0);
+        ring.advance(C::kRing);
+        return t;
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -184,7 +288,23 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             uint32_t kv_ph = 0, st_ph = 0;
             int stage = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            while (ok) {
+                // take the next unit and publish it to the other warps
+                if (!(ok = mbar_wait(ring.empty0 + 8u * ring.k, ring.ph ^ 1, w))) break;
+                int t = atomicAdd(p.unit_counter, 1);
+                if (t >= ntiles) {
+                    t = -1;
+                    // the last CTA to run out resets the counters for the next launch
+                    __threadfence();
+                    if (atomicAdd(p.unit_counter + 1, 1) == (int)gridDim.x - 1) {
+                        atomicExch(p.unit_counter, 0);
+                        atomicExch(p.unit_counter + 1, 0);
+                    }
+                }
+                ring.slot[ring.k] = t;
+                mbar_arrive(ring.full0 + 8u * ring.k);
+                ring.advance(C::kRing);
+                if (t < 0) break;
                 const Unit u = decode_unit<BM>(p, t);
                 if (u.iters == 0) continue;
                 if (!(ok = mbar_wait(bar(B_KV_EMPTY), kv_ph ^ 1, w))) break;
@@ -199,7 +319,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                                 u.hk, krow, u.bidx);
                 }
                 for (int it = 0; it < u.iters; ++it) {
-                    const int g = it / u.nm, m = u.m_begin + it % u.nm;
+                    const int g = u.g_of(it, p.G), m = u.m_of(it, p.G);
                     const int h = u.hk * p.G + g;
                     if (!(ok = mbar_wait(bar(B_STAGE0 + S + stage), st_ph ^ 1, w))) break;
                     const uint32_t full = bar(B_STAGE0 + stage);
@@ -221,112 +341,149 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            uint32_t kv_ph = 0, st_ph = 0, p_ph = 0, ds_ph = 0, dq_ph = 0, acc_ph = 0;
-            int stage = 0;
-            bool ok = true;
-            const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sDS = sbase + C::OFF_DS;
-            const uint32_t dq_a = C::kDqT ? sK : sDS, dq_b = C::kDqT ? sDS : sK;
-            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const Unit u = decode_unit<BM>(p, t);
-                if (u.iters == 0) continue;
-                if (!(ok = mbar_wait(bar(B_KV_FULL), kv_ph, w))) break;
-                kv_ph ^= 1;
-                tc_fence_after();
-                for (int it = 0; it < u.iters; ++it) {
-                    if (!(ok = mbar_wait(bar(B_STAGE0 + stage), st_ph, w))) break;
-                    tc_fence_after();
-                    const uint32_t sQ = sbase + C::OFF_Q + stage * C::QO_BYTES;
-                    const uint32_t sDO = sbase + C::OFF_DO + stage * C::QO_BYTES;
-                    // S^T = K Q^T  (K-major A and B; a K step of 16 = 32 bytes in a half)
+        // The whole warp runs this loop in lock-step; elect.sync picks the lane
+        // that issues each MMA / commit.
+        uint32_t kv_ph = 0, acc_ph = 0;
+        uint32_t p_ph = 0, ds_ph = 0, dqe_ph = 0;   // bit b: phase parity of buffer b
+        int s_stage = 0;          // stage of the next step whose S / dP is issued
+        uint32_t s_ph = 0;
+        int c_stage = 0;          // stage of the step whose dV / dK / dQ is issued
+        int nb = 0, cb = 0;       // TMEM buffer of the next step / of the current step
+        bool ok = true;
+        const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+        const uint64_t dK_k = sw128_desc(sK, 16, 1024), dV_k = sw128_desc(sV, 16, 1024);
+        const uint64_t dK_mn = sw128_desc(sK, BN * 128, 1024);
+        // S^T = K Q^T of the next step into S buffer nb (waits for its stage)
+        auto issue_s = [&]() -> bool {
+            if (!mbar_wait_warp(bar(B_STAGE0 + s_stage), s_ph, w)) return false;
+            tc_fence_after();
+            const uint64_t dQ_k = sw128_desc(sbase + C::OFF_Q + s_stage * C::QO_BYTES, 16, 1024);
+            const uint32_t d = tmem + C::s_col(nb, 0, 0);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
-                        const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
-                        mma_ss(tmem + C::TM_S, sw128_desc(sK + ko, 16, 1024),
-                               sw128_desc(sQ + qo, 16, 1024), C::IDESC_S, kk > 0);
-                    }
-                    mma_commit(bar(B_S_FULL));
-                    // dP^T = V dO^T
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
-                        const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
-                        mma_ss(tmem + C::TM_DP, sw128_desc(sV + ko, 16, 1024),
-                               sw128_desc(sDO + qo, 16, 1024), C::IDESC_S, kk > 0);
-                    }
-                    mma_commit(bar(B_DP_FULL));
-                    if (it == 0) {
-                        if (!(ok = mbar_wait(bar(B_ACC_EMPTY), acc_ph ^ 1, w))) break;
-                        acc_ph ^= 1;
-                    }
-                    if (!(ok = mbar_wait(bar(B_P_FULL), p_ph, w))) break;
-                    p_ph ^= 1;
-                    tc_fence_after();
-                    // dV += P^T dO  (P^T bf16 in TMEM; dO MN-major: K step = 16 rows = 2048 B)
-#pragma unroll
-                    for (int kk = 0; kk < BM / 16; ++kk) {
-                        const int g = (16 * kk) / (BM / 2);
-                        const uint32_t acol = C::TM_S + 8 * kk + g * (BM / 4);
-                        mma_ts(tmem + C::TM_DV, tmem + acol, sw128_desc(sDO + kk * 2048, BM * 128, 1024),
-                               C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    if (!(ok = mbar_wait(bar(B_DS_FULL), ds_ph, w))) break;
-                    ds_ph ^= 1;
-                    tc_fence_after();
-                    // dK += dS^T Q
-#pragma unroll
-                    for (int kk = 0; kk < BM / 16; ++kk) {
-                        const int g = (16 * kk) / (BM / 2);
-                        const uint32_t acol = C::TM_DP + 8 * kk + g * (BM / 4);
-                        mma_ts(tmem + C::TM_DK, tmem + acol, sw128_desc(sQ + kk * 2048, BM * 128, 1024),
-                               C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    mma_commit(bar(B_STAGE0 + S + stage));   // Q / dO of this stage consumed
-                    if (!(ok = mbar_wait(bar(B_DQ_EMPTY), dq_ph ^ 1, w))) break;
-                    dq_ph ^= 1;
-                    tc_fence_after();
-                    // dQ (kDqT: dQ^T = K^T dS^T, else dQ = dS K); both operands MN-major
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        mma_ss(tmem + C::TM_DQ, sw128_desc(dq_a + kk * 2048, BN * 128, 1024),
-                               sw128_desc(dq_b + kk * 2048, BN * 128, 1024), C::IDESC_DQ, kk > 0);
-                    }
-                    mma_commit(bar(B_DQ_FULL));
-                    if (++stage == S) { stage = 0; st_ph ^= 1; }
-                }
-                if (!ok) break;
-                mma_commit(bar(B_ACC_FULL));
-                mma_commit(bar(B_KV_EMPTY));
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
+                const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
+                mma_ss_warp(d, desc_add(dK_k, ko), desc_add(dQ_k, qo), C::IDESC_S, kk > 0);
             }
-            // make sure no MMA is still running before tensor memory is freed
-            mma_commit(bar(B_DRAIN));
-            WaitCtl wd{abort_flag, p.err, p.budget_ns};
-            mbar_wait(bar(B_DRAIN), 0, wd);
+            mma_commit_warp(bar(B_S_FULL + nb));
+            return true;
+        };
+        // dP^T = V dO^T of the next step into its dP buffer
+        auto issue_dp = [&]() -> bool {
+            uint32_t d = tmem + C::TM_DP;
+            if (C::kPipe) {
+                // X buffer nb last held a dQ^T: wait until the reducers read it
+                if (!mbar_wait_warp(bar(B_DQ_EMPTY + nb), bit(dqe_ph, nb) ^ 1u, w)) return false;
+                dqe_ph ^= 1u << nb;
+                tc_fence_after();
+                d = tmem + C::dp_col(nb, 0, 0);
+            }
+            const uint64_t dDO_k = sw128_desc(sbase + C::OFF_DO + s_stage * C::QO_BYTES, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
+                const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
+                mma_ss_warp(d, desc_add(dV_k, ko), desc_add(dDO_k, qo), C::IDESC_S, kk > 0);
+            }
+            mma_commit_warp(bar(B_DP_FULL + nb));
+            if (++s_stage == S) { s_stage = 0; s_ph ^= 1; }
+            if (C::kPipe) nb ^= 1;
+            return true;
+        };
+        while (ok) {
+            const int t = next_unit();
+            if (t < 0) break;
+            const Unit u = decode_unit<BM>(p, t);
+            if (u.iters == 0) continue;
+            if (!(ok = mbar_wait_warp(bar(B_KV_FULL), kv_ph, w))) break;
+            kv_ph ^= 1;
+            tc_fence_after();
+            if (C::kPipe && !(ok = issue_s() && issue_dp())) break;   // step 0 of the unit
+            for (int it = 0; it < u.iters; ++it) {
+                const bool more = it + 1 < u.iters;
+                if (C::kPipe) {
+                    if (more && !(ok = issue_s())) break;             // S of step it+1
+                } else {
+                    if (!(ok = issue_s() && issue_dp())) break;       // S, dP of step it
+                }
+                if (it == 0) {
+                    if (!(ok = mbar_wait_warp(bar(B_ACC_EMPTY), acc_ph ^ 1, w))) break;
+                    acc_ph ^= 1;
+                }
+                const uint32_t sQ = sbase + C::OFF_Q + c_stage * C::QO_BYTES;
+                const uint32_t sDO = sbase + C::OFF_DO + c_stage * C::QO_BYTES;
+                if (!(ok = mbar_wait_warp(bar(B_P_FULL + cb), bit(p_ph, cb), w))) break;
+                p_ph ^= 1u << cb;
+                tc_fence_after();
+                // dV += P^T dO  (P^T bf16 in TMEM; dO MN-major: K step = 16 rows = 2048 B)
+                const uint64_t dDO_mn = sw128_desc(sDO, BM * 128, 1024);
+#pragma unroll
+                for (int kk = 0; kk < BM / 16; ++kk)
+                    mma_ts_warp(tmem + C::TM_DV, tmem + C::p_op(cb, kk), desc_add(dDO_mn, kk * 2048),
+                                C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
+                if (C::kPipe && more && !(ok = issue_dp())) break;   // dP of step it+1
+                if (!(ok = mbar_wait_warp(bar(B_DS_FULL + cb), bit(ds_ph, cb), w))) break;
+                ds_ph ^= 1u << cb;
+                tc_fence_after();
+                // dK += dS^T Q
+                const uint64_t dQ_mn = sw128_desc(sQ, BM * 128, 1024);
+#pragma unroll
+                for (int kk = 0; kk < BM / 16; ++kk)
+                    mma_ts_warp(tmem + C::TM_DK, tmem + C::ds_op(cb, kk), desc_add(dQ_mn, kk * 2048),
+                                C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
+                mma_commit_warp(bar(B_STAGE0 + S + c_stage));   // Q / dO of this stage consumed
+                if (!C::kPipe) {
+                    if (!(ok = mbar_wait_warp(bar(B_DQ_EMPTY), bit(dqe_ph, 0) ^ 1u, w))) break;
+                    dqe_ph ^= 1u;
+                    tc_fence_after();
+                }
+                // dQ (kDqT: dQ^T = K^T dS^T, else dQ = dS K); both operands MN-major
+                const uint64_t dDS_mn =
+                    sw128_desc(sbase + C::OFF_DS + cb * C::DS_BYTES, BN * 128, 1024);
+                const uint64_t dq_a = C::kDqT ? dK_mn : dDS_mn;
+                const uint64_t dq_b = C::kDqT ? dDS_mn : dK_mn;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ss_warp(tmem + C::dq_col(cb), desc_add(dq_a, kk * 2048),
+                                desc_add(dq_b, kk * 2048), C::IDESC_DQ, kk > 0);
+                mma_commit_warp(bar(B_DQ_FULL + cb));
+                if (++c_stage == S) c_stage = 0;
+                if (C::kPipe) cb ^= 1;
+            }
+            if (!ok) break;
+            mma_commit_warp(bar(B_ACC_FULL));
+            mma_commit_warp(bar(B_KV_EMPTY));
         }
+        // make sure no MMA is still running before tensor memory is freed
+        mma_commit_warp(bar(B_DRAIN));
+        mbar_wait_warp(bar(B_DRAIN), 0, w);
     } else if (warp < 6) {
         // --------------------------------------------------------- dQ reducers
         const int quarter = warp & 3;
         const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
         const int r = quarter * 32 + lane;   // TMEM lane: d (kDqT) or query row
         uint32_t dq_ph = 0;
+        int cb = 0;
         bool ok = true;
         float *const dqacc = p.dqacc;
-        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        while (ok) {
+            const int t = next_unit();
+            if (t < 0) break;
             const Unit u = decode_unit<BM>(p, t);
             for (int it = 0; it < u.iters; ++it) {
-                const int g = it / u.nm, m = u.m_begin + it % u.nm;
+                const int g = u.g_of(it, p.G), m = u.m_of(it, p.G);
                 const int h = u.hk * p.G + g;
-                if (!(ok = mbar_wait(bar(B_DQ_FULL), dq_ph, w))) break;
-                dq_ph ^= 1;
+                if (!(ok = mbar_wait(bar(B_DQ_FULL + cb), bit(dq_ph, cb), w))) break;
+                dq_ph ^= 1u << cb;
                 tc_fence_after();
                 uint32_t v0[32], v1[32];
-                tmem_ld32(lane_addr + C::TM_DQ, v0);
-                tmem_ld32(lane_addr + C::TM_DQ + 32, v1);
+                tmem_ld32(lane_addr + C::dq_col(cb), v0);
+                tmem_ld32(lane_addr + C::dq_col(cb) + 32, v1);
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_DQ_EMPTY));
+                if (lane == 0) mbar_arrive(bar(B_DQ_EMPTY + cb));
+                if (C::kPipe) cb ^= 1;
                 const long long row0 = ws_row(p, u.b, h, m * BM);
                 int *sem = p.sem + row0 / 64;
                 if (p.deterministic) {
@@ -345,12 +502,11 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     float *dst = dqacc + row0 * D + r;
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        if (i < rows_left)
-                            atomicAdd(dst + (long long)i * D, __uint_as_float(v0[i]));
+                        if (i < rows_left) red_add_f32(dst + (long long)i * D, __uint_as_float(v0[i]));
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         if (32 + i < rows_left)
-                            atomicAdd(dst + (long long)(32 + i) * D, __uint_as_float(v1[i]));
+                            red_add_f32(dst + (long long)(32 + i) * D, __uint_as_float(v1[i]));
                 } else {
                     // lane r = query row; columns = the 64 d of that row
                     if (r < rows_left) {
@@ -388,24 +544,24 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         const int quarter = warp & 3;
         const int j = quarter * 32 + lane;          // key row within the block
         const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-        constexpr int HALF = BM / 2;                // query columns per group
-        constexpr int NCH = HALF / 32;              // 32-column chunks per group
-        uint32_t s_ph = 0, dp_ph = 0, st_ph = 0, acc_ph = 0;
-        int stage = 0;
+        uint32_t s_ph = 0, dp_ph = 0, st_ph = 0, acc_ph = 0;   // s_ph / dp_ph: bit per buffer
+        int stage = 0, cb = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        while (ok) {
+            const int t = next_unit();
+            if (t < 0) break;
             const Unit u = decode_unit<BM>(p, t);
             const int n0 = u.n_block * BN;
             const int kj = n0 + j;                   // key index within the sequence
             const bool key_ok = kj < u.lk;
             const int diag = u.lk - u.lq;            // key kj visible to query qi iff kj <= qi + diag
             for (int it = 0; it < u.iters; ++it) {
-                const int m = u.m_begin + it % u.nm;
+                const int m = u.m_of(it, p.G);
                 const int m0 = m * BM;
                 const bool masked = p.causal && (n0 + BN - 1 > m0 + diag);
                 if (!(ok = mbar_wait(bar(B_STAGE0 + stage), st_ph, w))) break;
-                if (!(ok = mbar_wait(bar(B_S_FULL), s_ph, w))) break;
-                s_ph ^= 1;
+                if (!(ok = mbar_wait(bar(B_S_FULL + cb), bit(s_ph, cb), w))) break;
+                s_ph ^= 1u << cb;
                 tc_fence_after();
                 const float *lse2 = reinterpret_cast<const float *>(smem + C::OFF_LSE + stage * BM * 4);
                 const float *dv = reinterpret_cast<const float *>(smem + C::OFF_DV + stage * BM * 4);
@@ -413,7 +569,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch) {
                     uint32_t sr[32];
-                    tmem_ld32(lane_addr + C::TM_S + grp * HALF + 32 * ch, sr);
+                    tmem_ld32(lane_addr + C::s_col(cb, grp, ch), sr);
                     tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
@@ -425,20 +581,20 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     uint32_t pk[16];
 #pragma unroll
                     for (int c = 0; c < 16; ++c) pk[c] = Cvt<T>::pack(P[32 * ch + 2 * c], P[32 * ch + 2 * c + 1]);
-                    tmem_st16(lane_addr + C::TM_S + grp * HALF + 16 * ch, pk);
+                    tmem_st16(lane_addr + C::p_col(cb, grp, ch), pk);
                 }
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_P_FULL));
-                if (!(ok = mbar_wait(bar(B_DP_FULL), dp_ph, w))) break;
-                dp_ph ^= 1;
+                if (lane == 0) mbar_arrive(bar(B_P_FULL + cb));
+                if (!(ok = mbar_wait(bar(B_DP_FULL + cb), bit(dp_ph, cb), w))) break;
+                dp_ph ^= 1u << cb;
                 tc_fence_after();
-                uint8_t *sds = smem + C::OFF_DS;
+                uint8_t *sds = smem + C::OFF_DS + cb * C::DS_BYTES;
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch) {
                     uint32_t dr[32];
-                    tmem_ld32(lane_addr + C::TM_DP + grp * HALF + 32 * ch, dr);
+                    tmem_ld32(lane_addr + C::dp_col(cb, grp, ch), dr);
                     tmem_wait_ld();
                     uint32_t pk[16];
 #pragma unroll
@@ -449,7 +605,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                             P[32 * ch + 2 * c + 1] * (__uint_as_float(dr[2 * c + 1]) - dv[i + 1]);
                         pk[c] = Cvt<T>::pack(d0, d1);
                     }
-                    tmem_st16(lane_addr + C::TM_DP + grp * HALF + 16 * ch, pk);
+                    tmem_st16(lane_addr + C::ds_col(cb, grp, ch), pk);
                     // dS^T row j into shared memory, 128B-swizzled halves of 64 queries
 #pragma unroll
                     for (int u8 = 0; u8 < 4; ++u8) {
@@ -465,10 +621,11 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(bar(B_DS_FULL));
+                    mbar_arrive(bar(B_DS_FULL + cb));
                     mbar_arrive(bar(B_STAGE0 + S + stage));
                 }
                 if (++stage == S) { stage = 0; st_ph ^= 1; }
+                if (C::kPipe) cb ^= 1;
             }
             if (!ok) break;
             // ---------------------------------------------------- dK / dV out

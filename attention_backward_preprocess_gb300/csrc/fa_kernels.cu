@@ -87,7 +87,11 @@ __global__ void __launch_bounds__(256) preprocess_kernel(BwdParams p) {
     const int s = (int)(rid / p.Hq), h = (int)(rid % p.Hq);
     // no early return: the row sum below is a full-warp shuffle
     const bool active = s < lq_round;
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.err = 0;   // per-call error word
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+        *p.err = 0;            // per-call error word
+        p.unit_counter[0] = 0;   // the main kernel's dynamic work-unit counter ...
+        p.unit_counter[1] = 0;   // ... and its count of CTAs that ran out of units
+    }
     const long long wr = active ? ws_row(p, b, h, s) : 0;
     float acc = 0.f;
     if (active && s < lq) {

@@ -22,7 +22,10 @@ struct BwdParams {
     // workspace
     int *err;           // device error word
     int4 *tiles;        // work units (b, n_block, hk, 0)
-    int *ntiles;        // number of work units written by the scheduler
+    int *ntiles;        // varlen: number of work units written by the scheduler
+    int num_units;      // dense: B * ceil(Sk / 128) * Hkv work units
+    int *unit_counter;  // [0] next work unit to hand out, [1] CTAs that ran out;
+                        // reset by the last CTA of each launch (and by the preprocess)
     int max_tiles;
     float *dvec;        // Dv per workspace row
     float *lse2;        // LSE * log2(e) per workspace row (+inf on padding rows)

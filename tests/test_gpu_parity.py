@@ -168,3 +168,26 @@ def test_stages_match_single_call_and_persistent_units(fa, oracle_mod, cuda_devi
         check_bar(t, r, name)
     # dK / dV have a fixed summation order; dQ accumulates with atomics
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+
+
+def test_main_stage_can_be_repeated(fa, oracle_mod, cuda_device):
+    """The main stage hands out work units from a counter in the workspace; a
+    second main stage after one preprocess must redo the same work (dK / dV
+    are overwritten, dQ accumulates twice)."""
+    w = W("repeat", 2, 300, 300, 4, 2, 128, causal=True)
+    x = small_case(oracle_mod, w)
+    n = fa.workspace_bytes(w.B, w.Sq, w.Sk, w.Hq, w.Hkv, w.D)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    g = {k: v.cuda() for k, v in x.items() if isinstance(v, torch.Tensor)}
+    kw = dict(causal=w.causal, softmax_scale=w.softmax_scale)
+    dq, dk, dv = fa.fa_bwd_stages(g["q"], g["k"], g["v"], g["o"], g["dout"], g["lse"], ws,
+                                  stages=("pre", "main"), **kw)
+    dk1, dv1 = dk.clone(), dv.clone()
+    fa.fa_bwd_stages(g["q"], g["k"], g["v"], g["o"], g["dout"], g["lse"], ws, dq=dq, dk=dk,
+                     dv=dv, stages=("main", "post"), **kw)
+    torch.cuda.synchronize()
+    assert fa.device_status(ws) == fa.FA_OK
+    assert torch.equal(dk, dk1) and torch.equal(dv, dv1)
+    rq, rk, rv = oracle_grads(oracle_mod, w, x)
+    check_bar(dq.double() / 2, rq, "dq accumulated twice")
+    check_bar(dk, rk, "dk")
