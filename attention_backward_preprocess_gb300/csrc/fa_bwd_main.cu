@@ -101,7 +101,17 @@ struct MainCfg {
     static constexpr int OFF_Q = OFF_V + KV_BYTES;
     static constexpr int OFF_DO = OFF_Q + kStages * QO_BYTES;
     static constexpr int OFF_DS = OFF_DO + kStages * QO_BYTES;
-    static constexpr int OFF_LSE = OFF_DS + kBuf * DS_BYTES;
+    // D = 128 (non-deterministic mode): the reducers pass each dQ^T tile (64
+    // query rows x 128 d, fp32) to the accumulator in two chunks of 32 rows,
+    // each staged in shared memory in the workspace's row-major layout and
+    // added by one TMA bulk reduce; two staging buffers let a chunk be
+    // written while the previous one is still being read.
+    static constexpr bool kBulk = kDqT;
+    static constexpr int CHUNK_ROWS = 32;
+    static constexpr int CHUNK_BYTES = CHUNK_ROWS * D * 4;
+    static constexpr int STG_BYTES = kBulk ? 2 * CHUNK_BYTES : 0;
+    static constexpr int OFF_STG = OFF_DS + kBuf * DS_BYTES;
+    static constexpr int OFF_LSE = OFF_STG + STG_BYTES;
     static constexpr int OFF_DV = OFF_LSE + kStages * BM * 4;
     static constexpr int OFF_BAR = OFF_DV + kStages * BM * 4;
     static constexpr int NUM_BARS = 48;
@@ -129,7 +139,9 @@ enum {
     B_ACC_FULL = 14, B_ACC_EMPTY = 15, B_DRAIN = 16,
     B_UNIT_FULL = 17,   // +k, k < kRing: unit index k of the ring written
     B_UNIT_EMPTY = 21,  // +k: every consumer warp has read it
-    B_STAGE0 = 25       // full[kStages], then empty[kStages]
+    B_STG_FULL = 25,    // +b: the 4 reducer warps wrote dQ staging buffer b
+    B_STG_FREE = 27,    // +b: the bulk reduce has read staging buffer b
+    B_STAGE0 = 29       // full[kStages], then empty[kStages]
 };
 
 // Work units are handed out dynamically: the producer warp takes the next
@@ -238,6 +250,10 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         mbar_init(bar(B_ACC_FULL), 1);
         mbar_init(bar(B_ACC_EMPTY), 8);
         mbar_init(bar(B_DRAIN), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(B_STG_FULL + b), 4);
+            mbar_init(bar(B_STG_FREE + b), 1);
+        }
         for (int k = 0; k < C::kRing; ++k) {
             mbar_init(bar(B_UNIT_FULL + k), 1);
             mbar_init(bar(B_UNIT_EMPTY + k), C::kConsumerWarps);
@@ -463,9 +479,14 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
         const int r = quarter * 32 + lane;   // TMEM lane: d (kDqT) or query row
         uint32_t dq_ph = 0;
+        uint32_t stg_full_ph = 0, stg_free_ph = 0;   // bit b: phase parity of staging buffer b
+        int chunk = 0;                                 // chunks issued so far (buffer = chunk & 1)
         int cb = 0;
         bool ok = true;
         float *const dqacc = p.dqacc;
+        const bool bulk = C::kBulk && !p.deterministic;
+        const bool issuer = warp == 2 && lane == 0;   // issues the bulk reduces
+        float *stg = reinterpret_cast<float *>(smem + C::OFF_STG);
         while (ok) {
             const int t = next_unit();
             if (t < 0) break;
@@ -477,6 +498,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 dq_ph ^= 1u << cb;
                 tc_fence_after();
                 uint32_t v0[32], v1[32];
+                __syncwarp();
                 tmem_ld32(lane_addr + C::dq_col(cb), v0);
                 tmem_ld32(lane_addr + C::dq_col(cb) + 32, v1);
                 tmem_wait_ld();
@@ -496,7 +518,38 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     __threadfence();
                 }
                 const int rows_left = u.lq - m * BM;
-                if (C::kDqT) {
+                if (C::kBulk && bulk) {
+                    // lane r = d: column r of each [32 rows x 128 d] chunk, one
+                    // 128-byte row segment per warp store.  Rows past the
+                    // sequence hold zeros (P = 0 there) and land in the
+                    // workspace's padding rows.
+#pragma unroll
+                    for (int hc = 0; hc < 2; ++hc) {
+                        const int sb = chunk & 1;
+                        if (!(ok = mbar_wait(bar(B_STG_FREE + sb), bit(stg_free_ph, sb) ^ 1u, w))) break;
+                        stg_free_ph ^= 1u << sb;
+                        float *stg = reinterpret_cast<float *>(smem + C::OFF_STG + sb * C::CHUNK_BYTES);
+                        const uint32_t *v = hc == 0 ? v0 : v1;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) stg[i * D + r] = __uint_as_float(v[i]);
+                        fence_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(B_STG_FULL + sb));
+                        if (issuer) {
+                            if (!(ok = mbar_wait(bar(B_STG_FULL + sb), bit(stg_full_ph, sb), w))) break;
+                            bulk_reduce_add_f32(dqacc + (row0 + 32 * hc) * D, smem_u32(stg), C::CHUNK_BYTES);
+                            bulk_commit_group();
+                            // the previous chunk (other buffer) has been read once at
+                            // most one group is still reading
+                            bulk_wait_read_all_but_one();
+                            if (chunk > 0) mbar_arrive(bar(B_STG_FREE + (sb ^ 1)));
+                        }
+                        stg_full_ph ^= 1u << sb;
+                        ++chunk;
+                        __syncwarp();   // reconverge before the next .sync.aligned TMEM load
+                    }
+                    if (!ok) break;
+                } else if (C::kDqT) {
                     // lane r = d; columns = BM (=64) query rows; a warp adds 32
                     // consecutive d of one row: one 128-byte request
                     float *dst = dqacc + row0 * D + r;
@@ -538,6 +591,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 }
             }
         }
+        if (C::kBulk && warp == 2 && lane == 0) bulk_wait_all();   // reduces complete
     } else {
         // ------------------------------------------------ softmax / elementwise
         const int grp = (warp - 6) / 4;            // query-column group
@@ -566,15 +620,24 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 const float *lse2 = reinterpret_cast<const float *>(smem + C::OFF_LSE + stage * BM * 4);
                 const float *dv = reinterpret_cast<const float *>(smem + C::OFF_DV + stage * BM * 4);
                 float P[HALF];
+                __syncwarp();
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch) {
                     uint32_t sr[32];
                     tmem_ld32(lane_addr + C::s_col(cb, grp, ch), sr);
+                    // the 32 LSE2 values of this chunk: 8 broadcast 16-byte loads
+                    // (shared-memory bandwidth is the scarce resource here)
+                    float l2[32];
+#pragma unroll
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const float4 v4 = reinterpret_cast<const float4 *>(lse2 + grp * HALF + 32 * ch)[c4];
+                        l2[4 * c4] = v4.x; l2[4 * c4 + 1] = v4.y; l2[4 * c4 + 2] = v4.z; l2[4 * c4 + 3] = v4.w;
+                    }
                     tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
                         const int i = grp * HALF + 32 * ch + c;   // query within the block
-                        float pv = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -lse2[i]));
+                        float pv = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -l2[c]));
                         if (masked && kj > m0 + i + diag) pv = 0.f;
                         P[32 * ch + c] = key_ok ? pv : 0.f;
                     }
@@ -591,18 +654,24 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 dp_ph ^= 1u << cb;
                 tc_fence_after();
                 uint8_t *sds = smem + C::OFF_DS + cb * C::DS_BYTES;
+                __syncwarp();
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch) {
                     uint32_t dr[32];
                     tmem_ld32(lane_addr + C::dp_col(cb, grp, ch), dr);
+                    float dvv[32];
+#pragma unroll
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const float4 v4 = reinterpret_cast<const float4 *>(dv + grp * HALF + 32 * ch)[c4];
+                        dvv[4 * c4] = v4.x; dvv[4 * c4 + 1] = v4.y; dvv[4 * c4 + 2] = v4.z; dvv[4 * c4 + 3] = v4.w;
+                    }
                     tmem_wait_ld();
                     uint32_t pk[16];
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
-                        const int i = grp * HALF + 32 * ch + 2 * c;
-                        const float d0 = P[32 * ch + 2 * c] * (__uint_as_float(dr[2 * c]) - dv[i]);
+                        const float d0 = P[32 * ch + 2 * c] * (__uint_as_float(dr[2 * c]) - dvv[2 * c]);
                         const float d1 =
-                            P[32 * ch + 2 * c + 1] * (__uint_as_float(dr[2 * c + 1]) - dv[i + 1]);
+                            P[32 * ch + 2 * c + 1] * (__uint_as_float(dr[2 * c + 1]) - dvv[2 * c + 1]);
                         pk[c] = Cvt<T>::pack(d0, d1);
                     }
                     tmem_st16(lane_addr + C::ds_col(cb, grp, ch), pk);
@@ -643,6 +712,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             if (!(ok = mbar_wait(bar(B_ACC_FULL), acc_ph, w))) break;
             acc_ph ^= 1;
             tc_fence_after();
+            __syncwarp();
             const float mul = grp == 0 ? p.scale : 1.f;
             const int col0 = grp == 0 ? C::TM_DK : C::TM_DV;
 #pragma unroll

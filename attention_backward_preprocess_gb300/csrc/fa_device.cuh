@@ -71,22 +71,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Waits until the phase with the given parity has completed.  Bounded: gives
-// up (returns false) when another warp has aborted or the budget runs out
-// (then raises the error itself).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl &w) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Bounded slow path of mbar_wait, kept out of line so the common case (the
+// phase has already completed) costs one try_wait and a branch.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                            int *err, long long budget_ns) {
     const uint64_t t0 = globaltimer_ns();
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (*w.abort_flag) return false;
-        if ((long long)(globaltimer_ns() - t0) > w.budget_ns) {
-            raise_error(w, kErrWaitTimeout);
+        if (*abort_flag) return false;
+        if ((long long)(globaltimer_ns() - t0) > budget_ns) {
+            *abort_flag = 1;
+            atomicOr(err, kErrWaitTimeout);
             return false;
         }
     }
+}
+// Waits until the phase with the given parity has completed.  Bounded: gives
+// up (returns false) when another warp has aborted or the budget runs out
+// (then raises the error itself).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl &w) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, w.abort_flag, w.err, w.budget_ns);
 }
 
 // ------------------------------------------------- global-memory semaphores
@@ -139,6 +146,30 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
             "r"(dst),
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
+}
+// Bulk reduce-add of a contiguous shared-memory block into global memory (fp32
+// add performed by the TMA unit; both addresses 16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_reduce_add_f32(float *dst, uint32_t src, uint32_t bytes) {
+    asm volatile(
+        "cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst),
+        "r"(src), "r"(bytes)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until every committed bulk operation of this thread has finished reading
+// its shared-memory source.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Same, but allow the most recent committed group to still be reading.
+__device__ __forceinline__ void bulk_wait_read_all_but_one() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// Wait until every committed bulk operation of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 // Generic-proxy shared-memory writes -> visible to the async proxy (tcgen05.mma, TMA).
 __device__ __forceinline__ void fence_async_smem() {
@@ -210,10 +241,14 @@ __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
             bar)
         : "memory");
 }
-// Bounded wait by lane 0, result broadcast so the warp stays converged.
+// Bounded wait of a whole converged warp: every lane probes once (one
+// instruction, one barrier state); only if that fails does lane 0 wait and
+// broadcast the outcome, so the warp stays converged.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtl &w) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
     int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, w) ? 1 : 0;
+    if ((threadIdx.x & 31) == 0)
+        ok = mbar_wait_slow(bar, parity, w.abort_flag, w.err, w.budget_ns) ? 1 : 0;
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
