@@ -60,7 +60,8 @@ struct MainCfg {
     static constexpr bool kPipe = (kD == 128);
     static constexpr int kBuf = kPipe ? 2 : 1;
     static constexpr int kStages = kPipe ? 3 : 4;
-    static constexpr int kThreads = 14 * 32;
+    // 15 warps: the D = 128 pipeline issues its MMAs from two warps (1 and 14)
+    static constexpr int kThreads = 15 * 32;
     static constexpr int TM_DK = 0;
     static constexpr int TM_DV = D;
     static constexpr int TM_S = 2 * D;
@@ -119,7 +120,8 @@ struct MainCfg {
     static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
     static constexpr int kRing = 4;             // work-unit hand-off ring depth
-    static constexpr int kConsumerWarps = 13;   // MMA + 4 reducers + 8 softmax warps
+    // ring consumers: MMA warp(s) + 4 reducers + 8 softmax warps
+    static constexpr int kConsumerWarps = kPipe ? 14 : 13;
     static constexpr uint32_t IDESC_S = make_idesc(128, BM, Cvt<T>::is_bf16, false, false);
     static constexpr uint32_t IDESC_KV = make_idesc(128, D, Cvt<T>::is_bf16, false, true);
     static constexpr uint32_t IDESC_DQ = make_idesc(128, 64, Cvt<T>::is_bf16, true, true);
@@ -141,7 +143,8 @@ enum {
     B_UNIT_EMPTY = 21,  // +k: every consumer warp has read it
     B_STG_FULL = 25,    // +b: the 4 reducer warps wrote dQ staging buffer b
     B_STG_FREE = 27,    // +b: the bulk reduce has read staging buffer b
-    B_STAGE0 = 29       // full[kStages], then empty[kStages]
+    B_SBUF_FREE = 29,   // +b: dV / dK done reading P^T / dS^T of S buffer b
+    B_STAGE0 = 31       // full[kStages], then empty[kStages]
 };
 
 // Work units are handed out dynamically: the producer warp takes the next
@@ -238,7 +241,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         mbar_init(bar(B_KV_FULL), 1);
-        mbar_init(bar(B_KV_EMPTY), 1);
+        mbar_init(bar(B_KV_EMPTY), C::kPipe ? 2 : 1);   // one commit per MMA warp
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(B_S_FULL + b), 1);
             mbar_init(bar(B_P_FULL + b), 8);
@@ -249,7 +252,8 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         }
         mbar_init(bar(B_ACC_FULL), 1);
         mbar_init(bar(B_ACC_EMPTY), 8);
-        mbar_init(bar(B_DRAIN), 1);
+        mbar_init(bar(B_DRAIN), C::kPipe ? 2 : 1);
+        for (int b = 0; b < 2; ++b) mbar_init(bar(B_SBUF_FREE + b), 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(B_STG_FULL + b), 4);
             mbar_init(bar(B_STG_FREE + b), 1);
@@ -260,7 +264,8 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         }
         for (int s = 0; s < S; ++s) {
             mbar_init(bar(B_STAGE0 + s), 1);          // full: producer expect_tx
-            mbar_init(bar(B_STAGE0 + S + s), 1 + 8);  // empty: MMA commit + 8 softmax warps
+            // empty: a commit per MMA warp + 8 softmax warps
+            mbar_init(bar(B_STAGE0 + S + s), (C::kPipe ? 2 : 1) + 8);
         }
         fence_mbar_init();
     }
@@ -355,7 +360,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 && !C::kPipe) {
         // ---------------------------------------------------------- MMA issuer
         // The whole warp runs this loop in lock-step; elect.sync picks the lane
         // that issues each MMA / commit.
@@ -471,6 +476,117 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             mma_commit_warp(bar(B_KV_EMPTY));
         }
         // make sure no MMA is still running before tensor memory is freed
+        mma_commit_warp(bar(B_DRAIN));
+        mbar_wait_warp(bar(B_DRAIN), 0, w);
+    } else if (warp == 1 && C::kPipe) {
+        // ------------------------------------------- MMA warp A: S and dP
+        // Issues S^T_j = K Q_j^T and dP^T_j = V dO_j^T for every step j, ahead
+        // of warp B.  Before S_j it waits until warp B's dV / dK of step j-2
+        // released S buffer j%2, before dP_j until the reducers drained the
+        // dQ^T of step j-2 from X buffer j%2.
+        uint32_t kv_ph = 0, sfree_ph = 0, dqe_ph = 0;   // bit b: parity of buffer b
+        int s_stage = 0, nb = 0;
+        uint32_t s_ph = 0;
+        bool ok = true;
+        const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+        const uint64_t dK_k = sw128_desc(sK, 16, 1024), dV_k = sw128_desc(sV, 16, 1024);
+        while (ok) {
+            const int t = next_unit();
+            if (t < 0) break;
+            const Unit u = decode_unit<BM>(p, t);
+            if (u.iters == 0) continue;
+            if (!(ok = mbar_wait_warp(bar(B_KV_FULL), kv_ph, w))) break;
+            kv_ph ^= 1;
+            for (int j = 0; j < u.iters; ++j) {
+                if (!(ok = mbar_wait_warp(bar(B_STAGE0 + s_stage), s_ph, w))) break;
+                if (!(ok = mbar_wait_warp(bar(B_SBUF_FREE + nb), bit(sfree_ph, nb) ^ 1u, w))) break;
+                sfree_ph ^= 1u << nb;
+                tc_fence_after();
+                const uint64_t dQ_k = sw128_desc(sbase + C::OFF_Q + s_stage * C::QO_BYTES, 16, 1024);
+                const uint64_t dDO_k = sw128_desc(sbase + C::OFF_DO + s_stage * C::QO_BYTES, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
+                    const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
+                    mma_ss_warp(tmem + C::s_col(nb, 0, 0), desc_add(dK_k, ko), desc_add(dQ_k, qo),
+                                C::IDESC_S, kk > 0);
+                }
+                mma_commit_warp(bar(B_S_FULL + nb));
+                if (!(ok = mbar_wait_warp(bar(B_DQ_EMPTY + nb), bit(dqe_ph, nb) ^ 1u, w))) break;
+                dqe_ph ^= 1u << nb;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
+                    const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
+                    mma_ss_warp(tmem + C::dp_col(nb, 0, 0), desc_add(dV_k, ko), desc_add(dDO_k, qo),
+                                C::IDESC_S, kk > 0);
+                }
+                mma_commit_warp(bar(B_DP_FULL + nb));
+                mma_commit_warp(bar(B_STAGE0 + S + s_stage));   // warp A's share of the stage
+                if (++s_stage == S) { s_stage = 0; s_ph ^= 1; }
+                nb ^= 1;
+            }
+            if (!ok) break;
+            mma_commit_warp(bar(B_KV_EMPTY));
+        }
+        mma_commit_warp(bar(B_DRAIN));
+        mbar_wait_warp(bar(B_DRAIN), 0, w);
+    } else if (warp == 14 && C::kPipe) {
+        // ---------------------------------------- MMA warp B: dV, dK and dQ
+        uint32_t kv_ph = 0, acc_ph = 0, p_ph = 0, ds_ph = 0;   // p / ds: bit per buffer
+        int c_stage = 0, cb = 0;
+        bool ok = true;
+        const uint64_t dK_mn = sw128_desc(sbase + C::OFF_K, BN * 128, 1024);
+        while (ok) {
+            const int t = next_unit();
+            if (t < 0) break;
+            const Unit u = decode_unit<BM>(p, t);
+            if (u.iters == 0) continue;
+            if (!(ok = mbar_wait_warp(bar(B_KV_FULL), kv_ph, w))) break;   // K for dQ
+            kv_ph ^= 1;
+            for (int it = 0; it < u.iters; ++it) {
+                if (it == 0) {
+                    if (!(ok = mbar_wait_warp(bar(B_ACC_EMPTY), acc_ph ^ 1, w))) break;
+                    acc_ph ^= 1;
+                }
+                const uint32_t sQ = sbase + C::OFF_Q + c_stage * C::QO_BYTES;
+                const uint32_t sDO = sbase + C::OFF_DO + c_stage * C::QO_BYTES;
+                if (!(ok = mbar_wait_warp(bar(B_P_FULL + cb), bit(p_ph, cb), w))) break;
+                p_ph ^= 1u << cb;
+                tc_fence_after();
+                // dV += P^T dO  (P^T bf16 in TMEM; dO MN-major: K step = 16 rows = 2048 B)
+                const uint64_t dDO_mn = sw128_desc(sDO, BM * 128, 1024);
+#pragma unroll
+                for (int kk = 0; kk < BM / 16; ++kk)
+                    mma_ts_warp(tmem + C::TM_DV, tmem + C::p_op(cb, kk), desc_add(dDO_mn, kk * 2048),
+                                C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
+                if (!(ok = mbar_wait_warp(bar(B_DS_FULL + cb), bit(ds_ph, cb), w))) break;
+                ds_ph ^= 1u << cb;
+                tc_fence_after();
+                // dK += dS^T Q
+                const uint64_t dQ_mn = sw128_desc(sQ, BM * 128, 1024);
+#pragma unroll
+                for (int kk = 0; kk < BM / 16; ++kk)
+                    mma_ts_warp(tmem + C::TM_DK, tmem + C::ds_op(cb, kk), desc_add(dQ_mn, kk * 2048),
+                                C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
+                mma_commit_warp(bar(B_SBUF_FREE + cb));   // P^T / dS^T of this buffer consumed
+                // dQ^T = K^T dS^T into X buffer cb (its dP^T was read before dS was ready)
+                const uint64_t dDS_mn =
+                    sw128_desc(sbase + C::OFF_DS + cb * C::DS_BYTES, BN * 128, 1024);
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ss_warp(tmem + C::dq_col(cb), desc_add(dK_mn, kk * 2048),
+                                desc_add(dDS_mn, kk * 2048), C::IDESC_DQ, kk > 0);
+                mma_commit_warp(bar(B_DQ_FULL + cb));
+                mma_commit_warp(bar(B_STAGE0 + S + c_stage));   // warp B's share of the stage
+                if (++c_stage == S) c_stage = 0;
+                cb ^= 1;
+            }
+            if (!ok) break;
+            mma_commit_warp(bar(B_ACC_FULL));
+            mma_commit_warp(bar(B_KV_EMPTY));
+        }
         mma_commit_warp(bar(B_DRAIN));
         mbar_wait_warp(bar(B_DRAIN), 0, w);
     } else if (warp < 6) {
@@ -592,7 +708,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             }
         }
         if (C::kBulk && warp == 2 && lane == 0) bulk_wait_all();   // reduces complete
-    } else {
+    } else if (warp < 14) {
         // ------------------------------------------------ softmax / elementwise
         const int grp = (warp - 6) / 4;            // query-column group
         const int quarter = warp & 3;
