@@ -27,7 +27,8 @@ EXPORTED = [
     "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_with_workspace", "fa_bwd_preprocess",
     "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_workspace_layout", "fa_fwd",
     "fa_device_status", "fa_set_wait_timeout_ns", "fa_status_string",
-    "fa_selftest_umma", "fa_selftest_semaphore", "fa_bwd_noalloc", "fa_bwd_noalloc_scratch_bytes",
+    "fa_selftest_umma", "fa_selftest_semaphore", "fa_selftest_tmem_layout", "fa_bwd_noalloc",
+    "fa_bwd_noalloc_scratch_bytes",
 ]
 
 
@@ -79,9 +80,11 @@ def lib():
         L.fa_bwd_noalloc_scratch_bytes.restype = _sz
         L.fa_selftest_umma.argtypes = [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]
         L.fa_selftest_semaphore.argtypes = [_vp, _i, ctypes.c_longlong, _vp, _vp]
+        L.fa_selftest_tmem_layout.argtypes = [_i, _vp, _vp]
         for name in ("fa_bwd", "fa_bwd_with_workspace", "fa_bwd_preprocess", "fa_bwd_main",
                      "fa_bwd_postprocess", "fa_bwd_workspace_layout", "fa_fwd",
-                     "fa_device_status", "fa_selftest_umma", "fa_selftest_semaphore"):
+                     "fa_device_status", "fa_selftest_umma", "fa_selftest_semaphore",
+                     "fa_selftest_tmem_layout"):
             getattr(L, name).restype = _i
         _lib = L
         return _lib
@@ -254,6 +257,16 @@ def selftest_umma(mode: int, A: torch.Tensor, B: torch.Tensor, N: int, K: int, s
     if st != 0:
         raise RuntimeError("fa_selftest_umma returned %d" % st)
     return C, err
+
+
+def selftest_tmem_layout(which: int, device="cuda", stream=None):
+    """The 16-lane tensor-memory access shapes' layout probe (see fa_selftest.h);
+    returns the [128, 32] uint32 result as int64."""
+    out = torch.zeros((128, 32), dtype=torch.int32, device=device)
+    st = lib().fa_selftest_tmem_layout(int(which), _ptr(out), _stream(stream))
+    if st != 0:
+        raise RuntimeError("fa_selftest_tmem_layout returned %d" % st)
+    return out.cpu().to(torch.int64) & 0xFFFFFFFF
 
 
 def selftest_semaphore(sem: torch.Tensor, target: int, budget_ns: int, stream=None):

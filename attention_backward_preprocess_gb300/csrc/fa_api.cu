@@ -187,6 +187,13 @@ struct Prepared {
     long long total_q, total_k;
 };
 
+int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
 fa_status prepare(const void *q, const void *k, const void *v, const void *o, const void *dout,
                   const float *lse, void *dq, void *dk, void *dv, int B, int Sq, int Sk, int Hq,
                   int Hkv, int D, float scale, int causal, const int *cu_q, const int *cu_k,
@@ -227,6 +234,16 @@ fa_status prepare(const void *q, const void *k, const void *v, const void *o, co
     p.tiles = reinterpret_cast<int4 *>(w + L.tiles);
     p.max_tiles = L.max_tiles;
     p.num_units = L.max_tiles;
+    // Unit order of the dense main kernel: the smallest group of (batch, kv
+    // head) pairs -- a divisor of B * Hkv, so that no short group comes last --
+    // whose units number at least 1.5 times the grid.
+    p.unit_group = B * Hkv;
+    if (!cu_q) {
+        const int nblk = (Sk + fa::kBlockN - 1) / fa::kBlockN;
+        const long long grid = std::min<long long>(L.max_tiles, sm_count());
+        for (int g = 1; g <= B * Hkv; ++g)
+            if ((B * Hkv) % g == 0 && 2LL * g * nblk >= 3 * grid) { p.unit_group = g; break; }
+    }
     p.dvec = reinterpret_cast<float *>(w + L.dvec);
     p.lse2 = reinterpret_cast<float *>(w + L.lse2);
     p.dqacc = reinterpret_cast<float *>(w + L.dqacc);
@@ -242,13 +259,6 @@ fa_status prepare(const void *q, const void *k, const void *v, const void *o, co
 }
 
 fa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
-
-int sm_count() {
-    int dev = 0, n = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    return n > 0 ? n : 1;
-}
 
 fa_status run_preprocess(const Prepared &P, fa_dtype dtype, cudaStream_t stream) {
     if (!P.p.o || !P.p.dout || !P.p.lse) return FA_ERR_INVALID_ARG;

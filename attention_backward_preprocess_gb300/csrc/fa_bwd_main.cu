@@ -60,8 +60,12 @@ struct MainCfg {
     static constexpr bool kPipe = (kD == 128);
     static constexpr int kBuf = kPipe ? 2 : 1;
     static constexpr int kStages = kPipe ? 3 : 4;
-    // 15 warps: the D = 128 pipeline issues its MMAs from two warps (1 and 14)
-    static constexpr int kThreads = 15 * 32;
+    // Warp roles: 0 producer | 1 MMA issuer (D = 64) or MMA warp A (S, dP) |
+    // 2 MMA warp B (dV, dK, dQ; D = 128) | 3 bulk-reduce issuer (D = 128) |
+    // 4-7 dQ reducers | 8-15 softmax (two groups of four, one per TMEM lane
+    // quarter).  Warps 2 and 3 idle when D = 64.
+    static constexpr int W_MMA_B = 2, W_ISSUE = 3, W_RED = 4, W_SM = 8;
+    static constexpr int kThreads = 16 * 32;
     static constexpr int TM_DK = 0;
     static constexpr int TM_DV = D;
     static constexpr int TM_S = 2 * D;
@@ -116,7 +120,8 @@ struct MainCfg {
     static constexpr int OFF_DV = OFF_LSE + kStages * BM * 4;
     static constexpr int OFF_BAR = OFF_DV + kStages * BM * 4;
     static constexpr int NUM_BARS = 48;
-    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // TMEM slot, abort flag, unit ring
+    // TMEM slot (+0), abort flag (+16), unit ring (+32), staging rows (+48)
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
     static constexpr int kRing = 4;             // work-unit hand-off ring depth
@@ -149,11 +154,11 @@ enum {
 
 // Work units are handed out dynamically: the producer warp takes the next
 // index from a global counter and passes it to the other warps of the CTA
-// through a small ring in shared memory.  Units leave the counter in
-// n_block-major order, so the units of one (sequence, kv head) that run at the
-// same time started close together and sweep the same rows of Q, dO and the
-// dQ accumulator in L2; idle CTAs take the next unit, which balances the
-// uneven causal work.  -1 ends the sequence.
+// through a small ring in shared memory.  Dense units leave the counter group
+// by group of (sequence, kv head) pairs, n_block-major inside a group, so the
+// units that run at the same time sweep the same rows of Q, dO and the dQ
+// accumulator in L2; idle CTAs take the next unit, which balances the uneven
+// causal work.  -1 ends the sequence.
 struct UnitRing {
     volatile int *slot;   // kRing ints in shared memory
     uint32_t full0, empty0;
@@ -180,8 +185,9 @@ struct Unit {
     __device__ __forceinline__ int m_of(int it, int G) const { return m_begin + nm - 1 - it / G; }
 };
 
-// Work unit t: dense problems enumerate (n_block, batch, kv head) with the
-// n_block slowest; varlen problems read the list the scheduler kernel wrote.
+// Work unit t: dense problems enumerate groups of (batch, kv head) pairs,
+// then n_block, then the pair inside the group; varlen problems read the list
+// the scheduler kernel wrote.
 template <int BM>
 __device__ __forceinline__ Unit decode_unit(const BwdParams &p, int t) {
     Unit u;
@@ -196,11 +202,18 @@ __device__ __forceinline__ Unit decode_unit(const BwdParams &p, int t) {
         u.lk = p.cu_k[u.b + 1] - u.k_row0;
         u.bidx = 0;
     } else {
-        const int per_n = p.B * p.Hkv;
-        u.n_block = t / per_n;
-        const int r = t - u.n_block * per_n;
-        u.b = r / p.Hkv;
-        u.hk = r - u.b * p.Hkv;
+        // groups of unit_group (batch, kv head) pairs, one after the other;
+        // inside a group the n blocks in increasing order (longest causal
+        // units first), the pairs of the group interleaved.  Units that run at
+        // the same time then share their dQ / Q / dO rows in L2.
+        const int gs = p.unit_group;
+        const int nblk = p.num_units / (p.B * p.Hkv);
+        const int grp = t / (gs * nblk);
+        const int r = t - grp * gs * nblk;
+        u.n_block = r / gs;
+        const int bh = grp * gs + (r - u.n_block * gs);
+        u.b = bh / p.Hkv;
+        u.hk = bh - u.b * p.Hkv;
         u.q_row0 = 0;
         u.k_row0 = 0;
         u.lq = p.Sq;
@@ -303,416 +316,499 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         return t;
     };
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            uint32_t kv_ph = 0, st_ph = 0;
-            int stage = 0;
-            bool ok = true;
-            while (ok) {
-                // take the next unit and publish it to the other warps
-                if (!(ok = mbar_wait(ring.empty0 + 8u * ring.k, ring.ph ^ 1, w))) break;
-                int t = atomicAdd(p.unit_counter, 1);
-                if (t >= ntiles) {
-                    t = -1;
-                    // the last CTA to run out resets the counters for the next launch
-                    __threadfence();
-                    if (atomicAdd(p.unit_counter + 1, 1) == (int)gridDim.x - 1) {
-                        atomicExch(p.unit_counter, 0);
-                        atomicExch(p.unit_counter + 1, 0);
+    if (warp < C::W_RED) {
+        // warpgroup 0: producer, MMA issue, bulk-reduce issue
+        if (warp == 0) {
+            // ------------------------------------------------------------ producer
+            if (lane == 0) {
+                uint32_t kv_ph = 0, st_ph = 0;
+                int stage = 0;
+                bool ok = true;
+                while (ok) {
+                    // take the next unit and publish it to the other warps
+                    if (!(ok = mbar_wait(ring.empty0 + 8u * ring.k, ring.ph ^ 1, w))) break;
+                    int t = atomicAdd(p.unit_counter, 1);
+                    if (t >= ntiles) {
+                        t = -1;
+                        // the last CTA to run out resets the counters for the next launch
+                        __threadfence();
+                        if (atomicAdd(p.unit_counter + 1, 1) == (int)gridDim.x - 1) {
+                            atomicExch(p.unit_counter, 0);
+                            atomicExch(p.unit_counter + 1, 0);
+                        }
+                    }
+                    ring.slot[ring.k] = t;
+                    mbar_arrive(ring.full0 + 8u * ring.k);
+                    ring.advance(C::kRing);
+                    if (t < 0) break;
+                    const Unit u = decode_unit<BM>(p, t);
+                    if (u.iters == 0) continue;
+                    if (!(ok = mbar_wait(bar(B_KV_EMPTY), kv_ph ^ 1, w))) break;
+                    kv_ph ^= 1;
+                    mbar_arrive_expect_tx(bar(B_KV_FULL), 2 * C::KV_BYTES);
+                    const int krow = u.k_row0 + u.n_block * BN;
+    #pragma unroll
+                    for (int h = 0; h < D / 64; ++h) {
+                        tma_load_4d(sbase + C::OFF_K + h * BN * 128, &maps.k, bar(B_KV_FULL), h * 64,
+                                    u.hk, krow, u.bidx);
+                        tma_load_4d(sbase + C::OFF_V + h * BN * 128, &maps.v, bar(B_KV_FULL), h * 64,
+                                    u.hk, krow, u.bidx);
+                    }
+                    for (int it = 0; it < u.iters; ++it) {
+                        const int g = u.g_of(it, p.G), m = u.m_of(it, p.G);
+                        const int h = u.hk * p.G + g;
+                        if (!(ok = mbar_wait(bar(B_STAGE0 + S + stage), st_ph ^ 1, w))) break;
+                        const uint32_t full = bar(B_STAGE0 + stage);
+                        mbar_arrive_expect_tx(full, 2 * C::QO_BYTES + 2 * BM * 4);
+                        const int qrow = u.q_row0 + m * BM;
+    #pragma unroll
+                        for (int hh = 0; hh < D / 64; ++hh) {
+                            tma_load_4d(sbase + C::OFF_Q + stage * C::QO_BYTES + hh * BM * 128, &maps.q,
+                                        full, hh * 64, h, qrow, u.bidx);
+                            tma_load_4d(sbase + C::OFF_DO + stage * C::QO_BYTES + hh * BM * 128,
+                                        &maps.dout, full, hh * 64, h, qrow, u.bidx);
+                        }
+                        const long long r0 = ws_row(p, u.b, h, m * BM);
+                        bulk_load(sbase + C::OFF_LSE + stage * BM * 4, p.lse2 + r0, BM * 4, full);
+                        bulk_load(sbase + C::OFF_DV + stage * BM * 4, p.dvec + r0, BM * 4, full);
+                        if (++stage == S) { stage = 0; st_ph ^= 1; }
                     }
                 }
-                ring.slot[ring.k] = t;
-                mbar_arrive(ring.full0 + 8u * ring.k);
-                ring.advance(C::kRing);
+            }
+        } else if (warp == 1 && !C::kPipe) {
+            // ---------------------------------------------------------- MMA issuer
+            // The whole warp runs this loop in lock-step; elect.sync picks the lane
+            // that issues each MMA / commit.
+            uint32_t kv_ph = 0, acc_ph = 0;
+            uint32_t p_ph = 0, ds_ph = 0, dqe_ph = 0;   // bit b: phase parity of buffer b
+            int s_stage = 0;          // stage of the next step whose S / dP is issued
+            uint32_t s_ph = 0;
+            int c_stage = 0;          // stage of the step whose dV / dK / dQ is issued
+            int nb = 0, cb = 0;       // TMEM buffer of the next step / of the current step
+            bool ok = true;
+            const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+            const uint64_t dK_k = sw128_desc(sK, 16, 1024), dV_k = sw128_desc(sV, 16, 1024);
+            const uint64_t dK_mn = sw128_desc(sK, BN * 128, 1024);
+            // S^T = K Q^T of the next step into S buffer nb (waits for its stage)
+            auto issue_s = [&]() -> bool {
+                if (!mbar_wait_warp(bar(B_STAGE0 + s_stage), s_ph, w)) return false;
+                tc_fence_after();
+                const uint64_t dQ_k = sw128_desc(sbase + C::OFF_Q + s_stage * C::QO_BYTES, 16, 1024);
+                const uint32_t d = tmem + C::s_col(nb, 0, 0);
+    #pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
+                    const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
+                    mma_ss_warp(d, desc_add(dK_k, ko), desc_add(dQ_k, qo), C::IDESC_S, kk > 0);
+                }
+                mma_commit_warp(bar(B_S_FULL + nb));
+                return true;
+            };
+            // dP^T = V dO^T of the next step into its dP buffer
+            auto issue_dp = [&]() -> bool {
+                uint32_t d = tmem + C::TM_DP;
+                if (C::kPipe) {
+                    // X buffer nb last held a dQ^T: wait until the reducers read it
+                    if (!mbar_wait_warp(bar(B_DQ_EMPTY + nb), bit(dqe_ph, nb) ^ 1u, w)) return false;
+                    dqe_ph ^= 1u << nb;
+                    tc_fence_after();
+                    d = tmem + C::dp_col(nb, 0, 0);
+                }
+                const uint64_t dDO_k = sw128_desc(sbase + C::OFF_DO + s_stage * C::QO_BYTES, 16, 1024);
+    #pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
+                    const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
+                    mma_ss_warp(d, desc_add(dV_k, ko), desc_add(dDO_k, qo), C::IDESC_S, kk > 0);
+                }
+                mma_commit_warp(bar(B_DP_FULL + nb));
+                if (++s_stage == S) { s_stage = 0; s_ph ^= 1; }
+                if (C::kPipe) nb ^= 1;
+                return true;
+            };
+            while (ok) {
+                const int t = next_unit();
                 if (t < 0) break;
                 const Unit u = decode_unit<BM>(p, t);
                 if (u.iters == 0) continue;
-                if (!(ok = mbar_wait(bar(B_KV_EMPTY), kv_ph ^ 1, w))) break;
+                if (!(ok = mbar_wait_warp(bar(B_KV_FULL), kv_ph, w))) break;
                 kv_ph ^= 1;
-                mbar_arrive_expect_tx(bar(B_KV_FULL), 2 * C::KV_BYTES);
-                const int krow = u.k_row0 + u.n_block * BN;
-#pragma unroll
-                for (int h = 0; h < D / 64; ++h) {
-                    tma_load_4d(sbase + C::OFF_K + h * BN * 128, &maps.k, bar(B_KV_FULL), h * 64,
-                                u.hk, krow, u.bidx);
-                    tma_load_4d(sbase + C::OFF_V + h * BN * 128, &maps.v, bar(B_KV_FULL), h * 64,
-                                u.hk, krow, u.bidx);
-                }
+                tc_fence_after();
+                if (C::kPipe && !(ok = issue_s() && issue_dp())) break;   // step 0 of the unit
                 for (int it = 0; it < u.iters; ++it) {
-                    const int g = u.g_of(it, p.G), m = u.m_of(it, p.G);
-                    const int h = u.hk * p.G + g;
-                    if (!(ok = mbar_wait(bar(B_STAGE0 + S + stage), st_ph ^ 1, w))) break;
-                    const uint32_t full = bar(B_STAGE0 + stage);
-                    mbar_arrive_expect_tx(full, 2 * C::QO_BYTES + 2 * BM * 4);
-                    const int qrow = u.q_row0 + m * BM;
-#pragma unroll
-                    for (int hh = 0; hh < D / 64; ++hh) {
-                        tma_load_4d(sbase + C::OFF_Q + stage * C::QO_BYTES + hh * BM * 128, &maps.q,
-                                    full, hh * 64, h, qrow, u.bidx);
-                        tma_load_4d(sbase + C::OFF_DO + stage * C::QO_BYTES + hh * BM * 128,
-                                    &maps.dout, full, hh * 64, h, qrow, u.bidx);
+                    const bool more = it + 1 < u.iters;
+                    if (C::kPipe) {
+                        if (more && !(ok = issue_s())) break;             // S of step it+1
+                    } else {
+                        if (!(ok = issue_s() && issue_dp())) break;       // S, dP of step it
                     }
-                    const long long r0 = ws_row(p, u.b, h, m * BM);
-                    bulk_load(sbase + C::OFF_LSE + stage * BM * 4, p.lse2 + r0, BM * 4, full);
-                    bulk_load(sbase + C::OFF_DV + stage * BM * 4, p.dvec + r0, BM * 4, full);
-                    if (++stage == S) { stage = 0; st_ph ^= 1; }
-                }
-            }
-        }
-    } else if (warp == 1 && !C::kPipe) {
-        // ---------------------------------------------------------- MMA issuer
-        // The whole warp runs this loop in lock-step; elect.sync picks the lane
-        // that issues each MMA / commit.
-        uint32_t kv_ph = 0, acc_ph = 0;
-        uint32_t p_ph = 0, ds_ph = 0, dqe_ph = 0;   // bit b: phase parity of buffer b
-        int s_stage = 0;          // stage of the next step whose S / dP is issued
-        uint32_t s_ph = 0;
-        int c_stage = 0;          // stage of the step whose dV / dK / dQ is issued
-        int nb = 0, cb = 0;       // TMEM buffer of the next step / of the current step
-        bool ok = true;
-        const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
-        const uint64_t dK_k = sw128_desc(sK, 16, 1024), dV_k = sw128_desc(sV, 16, 1024);
-        const uint64_t dK_mn = sw128_desc(sK, BN * 128, 1024);
-        // S^T = K Q^T of the next step into S buffer nb (waits for its stage)
-        auto issue_s = [&]() -> bool {
-            if (!mbar_wait_warp(bar(B_STAGE0 + s_stage), s_ph, w)) return false;
-            tc_fence_after();
-            const uint64_t dQ_k = sw128_desc(sbase + C::OFF_Q + s_stage * C::QO_BYTES, 16, 1024);
-            const uint32_t d = tmem + C::s_col(nb, 0, 0);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
-                const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
-                mma_ss_warp(d, desc_add(dK_k, ko), desc_add(dQ_k, qo), C::IDESC_S, kk > 0);
-            }
-            mma_commit_warp(bar(B_S_FULL + nb));
-            return true;
-        };
-        // dP^T = V dO^T of the next step into its dP buffer
-        auto issue_dp = [&]() -> bool {
-            uint32_t d = tmem + C::TM_DP;
-            if (C::kPipe) {
-                // X buffer nb last held a dQ^T: wait until the reducers read it
-                if (!mbar_wait_warp(bar(B_DQ_EMPTY + nb), bit(dqe_ph, nb) ^ 1u, w)) return false;
-                dqe_ph ^= 1u << nb;
-                tc_fence_after();
-                d = tmem + C::dp_col(nb, 0, 0);
-            }
-            const uint64_t dDO_k = sw128_desc(sbase + C::OFF_DO + s_stage * C::QO_BYTES, 16, 1024);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
-                const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
-                mma_ss_warp(d, desc_add(dV_k, ko), desc_add(dDO_k, qo), C::IDESC_S, kk > 0);
-            }
-            mma_commit_warp(bar(B_DP_FULL + nb));
-            if (++s_stage == S) { s_stage = 0; s_ph ^= 1; }
-            if (C::kPipe) nb ^= 1;
-            return true;
-        };
-        while (ok) {
-            const int t = next_unit();
-            if (t < 0) break;
-            const Unit u = decode_unit<BM>(p, t);
-            if (u.iters == 0) continue;
-            if (!(ok = mbar_wait_warp(bar(B_KV_FULL), kv_ph, w))) break;
-            kv_ph ^= 1;
-            tc_fence_after();
-            if (C::kPipe && !(ok = issue_s() && issue_dp())) break;   // step 0 of the unit
-            for (int it = 0; it < u.iters; ++it) {
-                const bool more = it + 1 < u.iters;
-                if (C::kPipe) {
-                    if (more && !(ok = issue_s())) break;             // S of step it+1
-                } else {
-                    if (!(ok = issue_s() && issue_dp())) break;       // S, dP of step it
-                }
-                if (it == 0) {
-                    if (!(ok = mbar_wait_warp(bar(B_ACC_EMPTY), acc_ph ^ 1, w))) break;
-                    acc_ph ^= 1;
-                }
-                const uint32_t sQ = sbase + C::OFF_Q + c_stage * C::QO_BYTES;
-                const uint32_t sDO = sbase + C::OFF_DO + c_stage * C::QO_BYTES;
-                if (!(ok = mbar_wait_warp(bar(B_P_FULL + cb), bit(p_ph, cb), w))) break;
-                p_ph ^= 1u << cb;
-                tc_fence_after();
-                // dV += P^T dO  (P^T bf16 in TMEM; dO MN-major: K step = 16 rows = 2048 B)
-                const uint64_t dDO_mn = sw128_desc(sDO, BM * 128, 1024);
-#pragma unroll
-                for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_ts_warp(tmem + C::TM_DV, tmem + C::p_op(cb, kk), desc_add(dDO_mn, kk * 2048),
-                                C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
-                if (C::kPipe && more && !(ok = issue_dp())) break;   // dP of step it+1
-                if (!(ok = mbar_wait_warp(bar(B_DS_FULL + cb), bit(ds_ph, cb), w))) break;
-                ds_ph ^= 1u << cb;
-                tc_fence_after();
-                // dK += dS^T Q
-                const uint64_t dQ_mn = sw128_desc(sQ, BM * 128, 1024);
-#pragma unroll
-                for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_ts_warp(tmem + C::TM_DK, tmem + C::ds_op(cb, kk), desc_add(dQ_mn, kk * 2048),
-                                C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
-                mma_commit_warp(bar(B_STAGE0 + S + c_stage));   // Q / dO of this stage consumed
-                if (!C::kPipe) {
-                    if (!(ok = mbar_wait_warp(bar(B_DQ_EMPTY), bit(dqe_ph, 0) ^ 1u, w))) break;
-                    dqe_ph ^= 1u;
+                    if (it == 0) {
+                        if (!(ok = mbar_wait_warp(bar(B_ACC_EMPTY), acc_ph ^ 1, w))) break;
+                        acc_ph ^= 1;
+                    }
+                    const uint32_t sQ = sbase + C::OFF_Q + c_stage * C::QO_BYTES;
+                    const uint32_t sDO = sbase + C::OFF_DO + c_stage * C::QO_BYTES;
+                    if (!(ok = mbar_wait_warp(bar(B_P_FULL + cb), bit(p_ph, cb), w))) break;
+                    p_ph ^= 1u << cb;
                     tc_fence_after();
+                    // dV += P^T dO  (P^T bf16 in TMEM; dO MN-major: K step = 16 rows = 2048 B)
+                    const uint64_t dDO_mn = sw128_desc(sDO, BM * 128, 1024);
+    #pragma unroll
+                    for (int kk = 0; kk < BM / 16; ++kk)
+                        mma_ts_warp(tmem + C::TM_DV, tmem + C::p_op(cb, kk), desc_add(dDO_mn, kk * 2048),
+                                    C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
+                    if (C::kPipe && more && !(ok = issue_dp())) break;   // dP of step it+1
+                    if (!(ok = mbar_wait_warp(bar(B_DS_FULL + cb), bit(ds_ph, cb), w))) break;
+                    ds_ph ^= 1u << cb;
+                    tc_fence_after();
+                    // dK += dS^T Q
+                    const uint64_t dQ_mn = sw128_desc(sQ, BM * 128, 1024);
+    #pragma unroll
+                    for (int kk = 0; kk < BM / 16; ++kk)
+                        mma_ts_warp(tmem + C::TM_DK, tmem + C::ds_op(cb, kk), desc_add(dQ_mn, kk * 2048),
+                                    C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit_warp(bar(B_STAGE0 + S + c_stage));   // Q / dO of this stage consumed
+                    if (!C::kPipe) {
+                        if (!(ok = mbar_wait_warp(bar(B_DQ_EMPTY), bit(dqe_ph, 0) ^ 1u, w))) break;
+                        dqe_ph ^= 1u;
+                        tc_fence_after();
+                    }
+                    // dQ (kDqT: dQ^T = K^T dS^T, else dQ = dS K); both operands MN-major
+                    const uint64_t dDS_mn =
+                        sw128_desc(sbase + C::OFF_DS + cb * C::DS_BYTES, BN * 128, 1024);
+                    const uint64_t dq_a = C::kDqT ? dK_mn : dDS_mn;
+                    const uint64_t dq_b = C::kDqT ? dDS_mn : dK_mn;
+    #pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        mma_ss_warp(tmem + C::dq_col(cb), desc_add(dq_a, kk * 2048),
+                                    desc_add(dq_b, kk * 2048), C::IDESC_DQ, kk > 0);
+                    mma_commit_warp(bar(B_DQ_FULL + cb));
+                    if (++c_stage == S) c_stage = 0;
+                    if (C::kPipe) cb ^= 1;
                 }
-                // dQ (kDqT: dQ^T = K^T dS^T, else dQ = dS K); both operands MN-major
-                const uint64_t dDS_mn =
-                    sw128_desc(sbase + C::OFF_DS + cb * C::DS_BYTES, BN * 128, 1024);
-                const uint64_t dq_a = C::kDqT ? dK_mn : dDS_mn;
-                const uint64_t dq_b = C::kDqT ? dDS_mn : dK_mn;
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ss_warp(tmem + C::dq_col(cb), desc_add(dq_a, kk * 2048),
-                                desc_add(dq_b, kk * 2048), C::IDESC_DQ, kk > 0);
-                mma_commit_warp(bar(B_DQ_FULL + cb));
-                if (++c_stage == S) c_stage = 0;
-                if (C::kPipe) cb ^= 1;
+                if (!ok) break;
+                mma_commit_warp(bar(B_ACC_FULL));
+                mma_commit_warp(bar(B_KV_EMPTY));
             }
-            if (!ok) break;
-            mma_commit_warp(bar(B_ACC_FULL));
-            mma_commit_warp(bar(B_KV_EMPTY));
-        }
-        // make sure no MMA is still running before tensor memory is freed
-        mma_commit_warp(bar(B_DRAIN));
-        mbar_wait_warp(bar(B_DRAIN), 0, w);
-    } else if (warp == 1 && C::kPipe) {
-        // ------------------------------------------- MMA warp A: S and dP
-        // Issues S^T_j = K Q_j^T and dP^T_j = V dO_j^T for every step j, ahead
-        // of warp B.  Before S_j it waits until warp B's dV / dK of step j-2
-        // released S buffer j%2, before dP_j until the reducers drained the
-        // dQ^T of step j-2 from X buffer j%2.
-        uint32_t kv_ph = 0, sfree_ph = 0, dqe_ph = 0;   // bit b: parity of buffer b
-        int s_stage = 0, nb = 0;
-        uint32_t s_ph = 0;
-        bool ok = true;
-        const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
-        const uint64_t dK_k = sw128_desc(sK, 16, 1024), dV_k = sw128_desc(sV, 16, 1024);
-        while (ok) {
-            const int t = next_unit();
-            if (t < 0) break;
-            const Unit u = decode_unit<BM>(p, t);
-            if (u.iters == 0) continue;
-            if (!(ok = mbar_wait_warp(bar(B_KV_FULL), kv_ph, w))) break;
-            kv_ph ^= 1;
-            for (int j = 0; j < u.iters; ++j) {
-                if (!(ok = mbar_wait_warp(bar(B_STAGE0 + s_stage), s_ph, w))) break;
-                if (!(ok = mbar_wait_warp(bar(B_SBUF_FREE + nb), bit(sfree_ph, nb) ^ 1u, w))) break;
-                sfree_ph ^= 1u << nb;
-                tc_fence_after();
-                const uint64_t dQ_k = sw128_desc(sbase + C::OFF_Q + s_stage * C::QO_BYTES, 16, 1024);
-                const uint64_t dDO_k = sw128_desc(sbase + C::OFF_DO + s_stage * C::QO_BYTES, 16, 1024);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
-                    const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
-                    mma_ss_warp(tmem + C::s_col(nb, 0, 0), desc_add(dK_k, ko), desc_add(dQ_k, qo),
-                                C::IDESC_S, kk > 0);
+            // make sure no MMA is still running before tensor memory is freed
+            mma_commit_warp(bar(B_DRAIN));
+            mbar_wait_warp(bar(B_DRAIN), 0, w);
+        } else if (warp == 1 && C::kPipe) {
+            // ------------------------------------------- MMA warp A: S and dP
+            // Issues S^T_j = K Q_j^T and dP^T_j = V dO_j^T for every step j, ahead
+            // of warp B.  Before S_j it waits until warp B's dV / dK of step j-2
+            // released S buffer j%2, before dP_j until the reducers drained the
+            // dQ^T of step j-2 from X buffer j%2.
+            uint32_t kv_ph = 0, sfree_ph = 0, dqe_ph = 0;   // bit b: parity of buffer b
+            int s_stage = 0, nb = 0;
+            uint32_t s_ph = 0;
+            bool ok = true;
+            const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+            const uint64_t dK_k = sw128_desc(sK, 16, 1024), dV_k = sw128_desc(sV, 16, 1024);
+            while (ok) {
+                const int t = next_unit();
+                if (t < 0) break;
+                const Unit u = decode_unit<BM>(p, t);
+                if (u.iters == 0) continue;
+                if (!(ok = mbar_wait_warp(bar(B_KV_FULL), kv_ph, w))) break;
+                kv_ph ^= 1;
+                for (int j = 0; j < u.iters; ++j) {
+                    if (!(ok = mbar_wait_warp(bar(B_STAGE0 + s_stage), s_ph, w))) break;
+                    if (!(ok = mbar_wait_warp(bar(B_SBUF_FREE + nb), bit(sfree_ph, nb) ^ 1u, w))) break;
+                    sfree_ph ^= 1u << nb;
+                    tc_fence_after();
+                    const uint64_t dQ_k = sw128_desc(sbase + C::OFF_Q + s_stage * C::QO_BYTES, 16, 1024);
+                    const uint64_t dDO_k = sw128_desc(sbase + C::OFF_DO + s_stage * C::QO_BYTES, 16, 1024);
+    #pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
+                        const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
+                        mma_ss_warp(tmem + C::s_col(nb, 0, 0), desc_add(dK_k, ko), desc_add(dQ_k, qo),
+                                    C::IDESC_S, kk > 0);
+                    }
+                    mma_commit_warp(bar(B_S_FULL + nb));
+                    if (!(ok = mbar_wait_warp(bar(B_DQ_EMPTY + nb), bit(dqe_ph, nb) ^ 1u, w))) break;
+                    dqe_ph ^= 1u << nb;
+                    tc_fence_after();
+    #pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
+                        const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
+                        mma_ss_warp(tmem + C::dp_col(nb, 0, 0), desc_add(dV_k, ko), desc_add(dDO_k, qo),
+                                    C::IDESC_S, kk > 0);
+                    }
+                    mma_commit_warp(bar(B_DP_FULL + nb));
+                    mma_commit_warp(bar(B_STAGE0 + S + s_stage));   // warp A's share of the stage
+                    if (++s_stage == S) { s_stage = 0; s_ph ^= 1; }
+                    nb ^= 1;
                 }
-                mma_commit_warp(bar(B_S_FULL + nb));
-                if (!(ok = mbar_wait_warp(bar(B_DQ_EMPTY + nb), bit(dqe_ph, nb) ^ 1u, w))) break;
-                dqe_ph ^= 1u << nb;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
-                    const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
-                    mma_ss_warp(tmem + C::dp_col(nb, 0, 0), desc_add(dV_k, ko), desc_add(dDO_k, qo),
-                                C::IDESC_S, kk > 0);
-                }
-                mma_commit_warp(bar(B_DP_FULL + nb));
-                mma_commit_warp(bar(B_STAGE0 + S + s_stage));   // warp A's share of the stage
-                if (++s_stage == S) { s_stage = 0; s_ph ^= 1; }
-                nb ^= 1;
+                if (!ok) break;
+                mma_commit_warp(bar(B_KV_EMPTY));
             }
-            if (!ok) break;
-            mma_commit_warp(bar(B_KV_EMPTY));
-        }
-        mma_commit_warp(bar(B_DRAIN));
-        mbar_wait_warp(bar(B_DRAIN), 0, w);
-    } else if (warp == 14 && C::kPipe) {
-        // ---------------------------------------- MMA warp B: dV, dK and dQ
-        uint32_t kv_ph = 0, acc_ph = 0, p_ph = 0, ds_ph = 0;   // p / ds: bit per buffer
-        int c_stage = 0, cb = 0;
-        bool ok = true;
-        const uint64_t dK_mn = sw128_desc(sbase + C::OFF_K, BN * 128, 1024);
-        while (ok) {
-            const int t = next_unit();
-            if (t < 0) break;
-            const Unit u = decode_unit<BM>(p, t);
-            if (u.iters == 0) continue;
-            if (!(ok = mbar_wait_warp(bar(B_KV_FULL), kv_ph, w))) break;   // K for dQ
-            kv_ph ^= 1;
-            for (int it = 0; it < u.iters; ++it) {
-                if (it == 0) {
-                    if (!(ok = mbar_wait_warp(bar(B_ACC_EMPTY), acc_ph ^ 1, w))) break;
-                    acc_ph ^= 1;
+            mma_commit_warp(bar(B_DRAIN));
+            mbar_wait_warp(bar(B_DRAIN), 0, w);
+        } else if (warp == C::W_MMA_B && C::kPipe) {
+            // ---------------------------------------- MMA warp B: dV, dK and dQ
+            uint32_t kv_ph = 0, acc_ph = 0, p_ph = 0, ds_ph = 0;   // p / ds: bit per buffer
+            int c_stage = 0, cb = 0;
+            bool ok = true;
+            const uint64_t dK_mn = sw128_desc(sbase + C::OFF_K, BN * 128, 1024);
+            while (ok) {
+                const int t = next_unit();
+                if (t < 0) break;
+                const Unit u = decode_unit<BM>(p, t);
+                if (u.iters == 0) continue;
+                if (!(ok = mbar_wait_warp(bar(B_KV_FULL), kv_ph, w))) break;   // K for dQ
+                kv_ph ^= 1;
+                for (int it = 0; it < u.iters; ++it) {
+                    if (it == 0) {
+                        if (!(ok = mbar_wait_warp(bar(B_ACC_EMPTY), acc_ph ^ 1, w))) break;
+                        acc_ph ^= 1;
+                    }
+                    const uint32_t sQ = sbase + C::OFF_Q + c_stage * C::QO_BYTES;
+                    const uint32_t sDO = sbase + C::OFF_DO + c_stage * C::QO_BYTES;
+                    if (!(ok = mbar_wait_warp(bar(B_P_FULL + cb), bit(p_ph, cb), w))) break;
+                    p_ph ^= 1u << cb;
+                    tc_fence_after();
+                    // dV += P^T dO  (P^T bf16 in TMEM; dO MN-major: K step = 16 rows = 2048 B)
+                    const uint64_t dDO_mn = sw128_desc(sDO, BM * 128, 1024);
+    #pragma unroll
+                    for (int kk = 0; kk < BM / 16; ++kk)
+                        mma_ts_warp(tmem + C::TM_DV, tmem + C::p_op(cb, kk), desc_add(dDO_mn, kk * 2048),
+                                    C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
+                    if (!(ok = mbar_wait_warp(bar(B_DS_FULL + cb), bit(ds_ph, cb), w))) break;
+                    ds_ph ^= 1u << cb;
+                    tc_fence_after();
+                    // dK += dS^T Q
+                    const uint64_t dQ_mn = sw128_desc(sQ, BM * 128, 1024);
+    #pragma unroll
+                    for (int kk = 0; kk < BM / 16; ++kk)
+                        mma_ts_warp(tmem + C::TM_DK, tmem + C::ds_op(cb, kk), desc_add(dQ_mn, kk * 2048),
+                                    C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit_warp(bar(B_SBUF_FREE + cb));   // P^T / dS^T of this buffer consumed
+                    // dQ^T = K^T dS^T into X buffer cb (its dP^T was read before dS was ready)
+                    const uint64_t dDS_mn =
+                        sw128_desc(sbase + C::OFF_DS + cb * C::DS_BYTES, BN * 128, 1024);
+    #pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        mma_ss_warp(tmem + C::dq_col(cb), desc_add(dK_mn, kk * 2048),
+                                    desc_add(dDS_mn, kk * 2048), C::IDESC_DQ, kk > 0);
+                    mma_commit_warp(bar(B_DQ_FULL + cb));
+                    mma_commit_warp(bar(B_STAGE0 + S + c_stage));   // warp B's share of the stage
+                    if (++c_stage == S) c_stage = 0;
+                    cb ^= 1;
                 }
-                const uint32_t sQ = sbase + C::OFF_Q + c_stage * C::QO_BYTES;
-                const uint32_t sDO = sbase + C::OFF_DO + c_stage * C::QO_BYTES;
-                if (!(ok = mbar_wait_warp(bar(B_P_FULL + cb), bit(p_ph, cb), w))) break;
-                p_ph ^= 1u << cb;
-                tc_fence_after();
-                // dV += P^T dO  (P^T bf16 in TMEM; dO MN-major: K step = 16 rows = 2048 B)
-                const uint64_t dDO_mn = sw128_desc(sDO, BM * 128, 1024);
-#pragma unroll
-                for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_ts_warp(tmem + C::TM_DV, tmem + C::p_op(cb, kk), desc_add(dDO_mn, kk * 2048),
-                                C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
-                if (!(ok = mbar_wait_warp(bar(B_DS_FULL + cb), bit(ds_ph, cb), w))) break;
-                ds_ph ^= 1u << cb;
-                tc_fence_after();
-                // dK += dS^T Q
-                const uint64_t dQ_mn = sw128_desc(sQ, BM * 128, 1024);
-#pragma unroll
-                for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_ts_warp(tmem + C::TM_DK, tmem + C::ds_op(cb, kk), desc_add(dQ_mn, kk * 2048),
-                                C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
-                mma_commit_warp(bar(B_SBUF_FREE + cb));   // P^T / dS^T of this buffer consumed
-                // dQ^T = K^T dS^T into X buffer cb (its dP^T was read before dS was ready)
-                const uint64_t dDS_mn =
-                    sw128_desc(sbase + C::OFF_DS + cb * C::DS_BYTES, BN * 128, 1024);
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ss_warp(tmem + C::dq_col(cb), desc_add(dK_mn, kk * 2048),
-                                desc_add(dDS_mn, kk * 2048), C::IDESC_DQ, kk > 0);
-                mma_commit_warp(bar(B_DQ_FULL + cb));
-                mma_commit_warp(bar(B_STAGE0 + S + c_stage));   // warp B's share of the stage
-                if (++c_stage == S) c_stage = 0;
-                cb ^= 1;
+                if (!ok) break;
+                mma_commit_warp(bar(B_ACC_FULL));
+                mma_commit_warp(bar(B_KV_EMPTY));
             }
-            if (!ok) break;
-            mma_commit_warp(bar(B_ACC_FULL));
-            mma_commit_warp(bar(B_KV_EMPTY));
+            mma_commit_warp(bar(B_DRAIN));
+            mbar_wait_warp(bar(B_DRAIN), 0, w);
+        } else if (warp == C::W_ISSUE && C::kBulk) {
+            // ------------------------------------------------ bulk-reduce issuer
+            // One thread adds every staged dQ chunk to the fp32 accumulator, in the
+            // order the reducer warps fill the two staging buffers.  The reducers
+            // put the chunk's first workspace row next to the buffer (-1 after the
+            // last chunk).  At most two chunks are in flight: after issuing chunk
+            // c the issuer waits until chunk c-1 has been read, then frees its buffer.
+            if (lane == 0 && !p.deterministic) {
+                volatile long long *stg_row = reinterpret_cast<volatile long long *>(smem + C::OFF_MISC + 48);
+                uint32_t full_ph = 0;
+                for (int chunk = 0;; ++chunk) {
+                    const int sb = chunk & 1;
+                    if (!mbar_wait(bar(B_STG_FULL + sb), bit(full_ph, sb), w)) break;
+                    full_ph ^= 1u << sb;
+                    const long long row = stg_row[sb];
+                    if (row < 0) break;
+                    bulk_reduce_add_f32(p.dqacc + row * D, sbase + C::OFF_STG + sb * C::CHUNK_BYTES,
+                                        C::CHUNK_BYTES);
+                    bulk_commit_group();
+                    bulk_wait_read_all_but_one();
+                    if (chunk > 0) mbar_arrive(bar(B_STG_FREE + (sb ^ 1)));
+                }
+                bulk_wait_all();
+            }
         }
-        mma_commit_warp(bar(B_DRAIN));
-        mbar_wait_warp(bar(B_DRAIN), 0, w);
-    } else if (warp < 6) {
-        // --------------------------------------------------------- dQ reducers
-        const int quarter = warp & 3;
-        const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-        const int r = quarter * 32 + lane;   // TMEM lane: d (kDqT) or query row
-        uint32_t dq_ph = 0;
-        uint32_t stg_full_ph = 0, stg_free_ph = 0;   // bit b: phase parity of staging buffer b
-        int chunk = 0;                                 // chunks issued so far (buffer = chunk & 1)
-        int cb = 0;
-        bool ok = true;
-        float *const dqacc = p.dqacc;
-        const bool bulk = C::kBulk && !p.deterministic;
-        const bool issuer = warp == 2 && lane == 0;   // issues the bulk reduces
-        float *stg = reinterpret_cast<float *>(smem + C::OFF_STG);
-        while (ok) {
-            const int t = next_unit();
-            if (t < 0) break;
-            const Unit u = decode_unit<BM>(p, t);
-            for (int it = 0; it < u.iters; ++it) {
-                const int g = u.g_of(it, p.G), m = u.m_of(it, p.G);
-                const int h = u.hk * p.G + g;
-                if (!(ok = mbar_wait(bar(B_DQ_FULL + cb), bit(dq_ph, cb), w))) break;
-                dq_ph ^= 1u << cb;
+    } else if (warp < C::W_SM) {
+        // warpgroup 1: dQ reducers
+        if (C::kBulk && !p.deterministic) {
+            // -------------------------------------------- dQ reducers (bulk mode)
+            // Lane r = d of the dQ^T tile (64 query rows x 128 d, fp32) in TMEM X
+            // buffer cb.  A step is read out as two chunks of 32 rows and the X
+            // buffer released at once; each chunk is then written, column r of a
+            // [32 rows x 128 d] block, to the next free staging buffer, which the
+            // issuer warp adds to the accumulator.
+            const int quarter = warp & 3;
+            const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+            const int r = quarter * 32 + lane;
+            volatile long long *stg_row = reinterpret_cast<volatile long long *>(smem + C::OFF_MISC + 48);
+            uint32_t dq_ph = 0, stg_free_ph = 0;   // bit b: parity of buffer b
+            int chunk = 0;                         // chunks written so far (staging buffer = chunk & 1)
+            int cb = 0;                            // TMEM X buffer of the next step
+            bool ok = true;
+            // step iterator over the units of the ring
+            int cur_iters = 0, cur_it = 0;
+            Unit cu{};
+            bool units_done = false;
+            auto next_row = [&](long long &row0) __attribute__((always_inline)) -> bool {
+                while (true) {
+                    if (cur_it < cur_iters) {
+                        const int g = cu.g_of(cur_it, p.G), m = cu.m_of(cur_it, p.G);
+                        row0 = ws_row(p, cu.b, cu.hk * p.G + g, m * BM);
+                        ++cur_it;
+                        return true;
+                    }
+                    if (units_done) return false;
+                    const int t = next_unit();
+                    if (t < 0) { units_done = true; return false; }
+                    cu = decode_unit<BM>(p, t);
+                    cur_iters = cu.iters;
+                    cur_it = 0;
+                }
+            };
+            // dQ^T of the step in TMEM buffer b -> (X, Y); releases the buffer
+            auto load_step = [&](uint32_t (&X)[32], uint32_t (&Y)[32], int b) __attribute__((always_inline)) {
                 tc_fence_after();
-                uint32_t v0[32], v1[32];
                 __syncwarp();
-                tmem_ld32(lane_addr + C::dq_col(cb), v0);
-                tmem_ld32(lane_addr + C::dq_col(cb) + 32, v1);
+                tmem_ld32(lane_addr + C::dq_col(b), X);
+                tmem_ld32(lane_addr + C::dq_col(b) + 32, Y);
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_DQ_EMPTY + cb));
-                if (C::kPipe) cb ^= 1;
-                const long long row0 = ws_row(p, u.b, h, m * BM);
-                int *sem = p.sem + row0 / 64;
-                if (p.deterministic) {
-                    // contributions to this row block arrive in n-block order:
-                    // wait until the 4 reducer warps of every earlier n block added
-                    bool got = true;
-                    if (lane == 0) got = sem_wait_geq(sem, 4 * u.n_block, w);
-                    got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
-                    if (!got) { ok = false; break; }
-                    __threadfence();
+                if (lane == 0) mbar_arrive(bar(B_DQ_EMPTY + b));
+            };
+            auto wait_dq = [&](int b) __attribute__((always_inline)) -> bool {
+                if (!mbar_wait_warp(bar(B_DQ_FULL + b), bit(dq_ph, b), w)) return false;
+                dq_ph ^= 1u << b;
+                return true;
+            };
+            auto wait_stg = [&]() __attribute__((always_inline)) -> bool {
+                const int sb = chunk & 1;
+                if (!mbar_wait_warp(bar(B_STG_FREE + sb), bit(stg_free_ph, sb) ^ 1u, w)) return false;
+                stg_free_ph ^= 1u << sb;
+                return true;
+            };
+            auto write_chunk = [&](const uint32_t (&X)[32], long long row) __attribute__((always_inline)) {
+                const int sb = chunk & 1;
+                const uint32_t stg = sbase + C::OFF_STG + sb * C::CHUNK_BYTES + 4 * r;
+            #pragma unroll
+                for (int i = 0; i < 32; ++i) st_shared_b32(stg + 4 * D * i, X[i]);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (warp == C::W_RED) stg_row[sb] = row;
+                    mbar_arrive(bar(B_STG_FULL + sb));
                 }
-                const int rows_left = u.lq - m * BM;
-                if (C::kBulk && bulk) {
-                    // lane r = d: column r of each [32 rows x 128 d] chunk, one
-                    // 128-byte row segment per warp store.  Rows past the
-                    // sequence hold zeros (P = 0 there) and land in the
-                    // workspace's padding rows.
-#pragma unroll
-                    for (int hc = 0; hc < 2; ++hc) {
-                        const int sb = chunk & 1;
-                        if (!(ok = mbar_wait(bar(B_STG_FREE + sb), bit(stg_free_ph, sb) ^ 1u, w))) break;
-                        stg_free_ph ^= 1u << sb;
-                        float *stg = reinterpret_cast<float *>(smem + C::OFF_STG + sb * C::CHUNK_BYTES);
-                        const uint32_t *v = hc == 0 ? v0 : v1;
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) stg[i * D + r] = __uint_as_float(v[i]);
-                        fence_async_smem();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bar(B_STG_FULL + sb));
-                        if (issuer) {
-                            if (!(ok = mbar_wait(bar(B_STG_FULL + sb), bit(stg_full_ph, sb), w))) break;
-                            bulk_reduce_add_f32(dqacc + (row0 + 32 * hc) * D, smem_u32(stg), C::CHUNK_BYTES);
-                            bulk_commit_group();
-                            // the previous chunk (other buffer) has been read once at
-                            // most one group is still reading
-                            bulk_wait_read_all_but_one();
-                            if (chunk > 0) mbar_arrive(bar(B_STG_FREE + (sb ^ 1)));
-                        }
-                        stg_full_ph ^= 1u << sb;
-                        ++chunk;
-                        __syncwarp();   // reconverge before the next .sync.aligned TMEM load
-                    }
-                    if (!ok) break;
-                } else if (C::kDqT) {
-                    // lane r = d; columns = BM (=64) query rows; a warp adds 32
-                    // consecutive d of one row: one 128-byte request
-                    float *dst = dqacc + row0 * D + r;
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (i < rows_left) red_add_f32(dst + (long long)i * D, __uint_as_float(v0[i]));
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (32 + i < rows_left)
-                            red_add_f32(dst + (long long)(32 + i) * D, __uint_as_float(v1[i]));
-                } else {
-                    // lane r = query row; columns = the 64 d of that row
-                    if (r < rows_left) {
-                        float *dst = dqacc + (row0 + r) * D;
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(
-                                             dst + 4 * c),
-                                         "f"(__uint_as_float(v0[4 * c])),
-                                         "f"(__uint_as_float(v0[4 * c + 1])),
-                                         "f"(__uint_as_float(v0[4 * c + 2])),
-                                         "f"(__uint_as_float(v0[4 * c + 3]))
-                                         : "memory");
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(
-                                             dst + 32 + 4 * c),
-                                         "f"(__uint_as_float(v1[4 * c])),
-                                         "f"(__uint_as_float(v1[4 * c + 1])),
-                                         "f"(__uint_as_float(v1[4 * c + 2])),
-                                         "f"(__uint_as_float(v1[4 * c + 3]))
-                                         : "memory");
-                    }
+                ++chunk;
+            };
+            uint32_t R0[32], R1[32];
+            long long row0 = 0;
+            while (ok && next_row(row0)) {
+                if (!(ok = wait_dq(cb))) break;
+                load_step(R0, R1, cb);
+                cb ^= 1;
+                if (!(ok = wait_stg())) break;
+                write_chunk(R0, row0);
+                if (!(ok = wait_stg())) break;
+                write_chunk(R1, row0 + 32);
+            }
+            // end marker for the issuer
+            if (ok && wait_stg()) {
+                __syncwarp();
+                if (lane == 0) {
+                    if (warp == C::W_RED) stg_row[chunk & 1] = -1;
+                    mbar_arrive(bar(B_STG_FULL + (chunk & 1)));
                 }
-                if (p.deterministic) {
-                    __threadfence();
+            }
+        } else {
+            // ------------------------------ dQ reducers (deterministic mode, D = 64)
+            const int quarter = warp & 3;
+            const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+            const int r = quarter * 32 + lane;   // TMEM lane: d (kDqT) or query row
+            uint32_t dq_ph = 0;
+            int cb = 0;
+            bool ok = true;
+            float *const dqacc = p.dqacc;
+            while (ok) {
+                const int t = next_unit();
+                if (t < 0) break;
+                const Unit u = decode_unit<BM>(p, t);
+                for (int it = 0; it < u.iters; ++it) {
+                    const int g = u.g_of(it, p.G), m = u.m_of(it, p.G);
+                    const int h = u.hk * p.G + g;
+                    if (!(ok = mbar_wait(bar(B_DQ_FULL + cb), bit(dq_ph, cb), w))) break;
+                    dq_ph ^= 1u << cb;
+                    tc_fence_after();
+                    uint32_t v0[32], v1[32];
                     __syncwarp();
-                    if (lane == 0) red_release_add_gpu(sem, 1);
+                    tmem_ld32(lane_addr + C::dq_col(cb), v0);
+                    tmem_ld32(lane_addr + C::dq_col(cb) + 32, v1);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_DQ_EMPTY + cb));
+                    if (C::kPipe) cb ^= 1;
+                    const long long row0 = ws_row(p, u.b, h, m * BM);
+                    int *sem = p.sem + row0 / 64;
+                    if (p.deterministic) {
+                        // contributions to this row block arrive in n-block order:
+                        // wait until the 4 reducer warps of every earlier n block added
+                        bool got = true;
+                        if (lane == 0) got = sem_wait_geq(sem, 4 * u.n_block, w);
+                        got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+                        if (!got) { ok = false; break; }
+                        __threadfence();
+                    }
+                    const int rows_left = u.lq - m * BM;
+                    if (C::kDqT) {
+                        // lane r = d; columns = BM (=64) query rows; a warp adds 32
+                        // consecutive d of one row: one 128-byte request
+                        float *dst = dqacc + row0 * D + r;
+    #pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (i < rows_left) red_add_f32(dst + (long long)i * D, __uint_as_float(v0[i]));
+    #pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (32 + i < rows_left)
+                                red_add_f32(dst + (long long)(32 + i) * D, __uint_as_float(v1[i]));
+                    } else {
+                        // lane r = query row; columns = the 64 d of that row
+                        if (r < rows_left) {
+                            float *dst = dqacc + (row0 + r) * D;
+    #pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(
+                                                 dst + 4 * c),
+                                             "f"(__uint_as_float(v0[4 * c])),
+                                             "f"(__uint_as_float(v0[4 * c + 1])),
+                                             "f"(__uint_as_float(v0[4 * c + 2])),
+                                             "f"(__uint_as_float(v0[4 * c + 3]))
+                                             : "memory");
+    #pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(
+                                                 dst + 32 + 4 * c),
+                                             "f"(__uint_as_float(v1[4 * c])),
+                                             "f"(__uint_as_float(v1[4 * c + 1])),
+                                             "f"(__uint_as_float(v1[4 * c + 2])),
+                                             "f"(__uint_as_float(v1[4 * c + 3]))
+                                             : "memory");
+                        }
+                    }
+                    if (p.deterministic) {
+                        __threadfence();
+                        __syncwarp();
+                        if (lane == 0) red_release_add_gpu(sem, 1);
+                    }
                 }
             }
         }
-        if (C::kBulk && warp == 2 && lane == 0) bulk_wait_all();   // reduces complete
-    } else if (warp < 14) {
+    } else {
         // ------------------------------------------------ softmax / elementwise
-        const int grp = (warp - 6) / 4;            // query-column group
+        const int grp = (warp - C::W_SM) / 4;      // query-column group
         const int quarter = warp & 3;
         const int j = quarter * 32 + lane;          // key row within the block
+        const int g4 = lane >> 2, q4 = lane & 3;     // 16-lane access shapes
         const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
         uint32_t s_ph = 0, dp_ph = 0, st_ph = 0, acc_ph = 0;   // s_ph / dp_ph: bit per buffer
         int stage = 0, cb = 0;
@@ -724,6 +820,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             const int n0 = u.n_block * BN;
             const int kj = n0 + j;                   // key index within the sequence
             const bool key_ok = kj < u.lk;
+            const int kb = n0 + quarter * 32 + g4;   // first key of this thread's 16-lane rows
             const int diag = u.lk - u.lq;            // key kj visible to query qi iff kj <= qi + diag
             for (int it = 0; it < u.iters; ++it) {
                 const int m = u.m_of(it, p.G);
@@ -733,34 +830,49 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 if (!(ok = mbar_wait(bar(B_S_FULL + cb), bit(s_ph, cb), w))) break;
                 s_ph ^= 1u << cb;
                 tc_fence_after();
-                const float *lse2 = reinterpret_cast<const float *>(smem + C::OFF_LSE + stage * BM * 4);
-                const float *dv = reinterpret_cast<const float *>(smem + C::OFF_DV + stage * BM * 4);
+                const uint32_t lse2 = sbase + C::OFF_LSE + stage * BM * 4;   // fp32 [BM]
+                const uint32_t dv = sbase + C::OFF_DV + stage * BM * 4;
+                // Element (h, k, r, e) of a 32-query chunk -- register 4k + 2r + e
+                // of the lane-offset-h load -- is key kb + 16h + 8r, query
+                // column 8k + 2*q4 + e of the chunk.  A thread thus needs 8
+                // LSE2 / Dv values per chunk (4 eight-byte loads) instead of 32.
                 float P[HALF];
                 __syncwarp();
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch) {
-                    uint32_t sr[32];
-                    tmem_ld32(lane_addr + C::s_col(cb, grp, ch), sr);
-                    // the 32 LSE2 values of this chunk: 8 broadcast 16-byte loads
-                    // (shared-memory bandwidth is the scarce resource here)
-                    float l2[32];
+                    uint32_t sr[2][16];
+                    tmem_ld16x256(lane_addr + C::s_col(cb, grp, ch), sr[0]);
+                    tmem_ld16x256(lane_addr + (16u << 16) + C::s_col(cb, grp, ch), sr[1]);
+                    const int c0 = grp * HALF + 32 * ch;     // first query of the chunk
+                    float2 l2[4];
 #pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4) {
-                        const float4 v4 = reinterpret_cast<const float4 *>(lse2 + grp * HALF + 32 * ch)[c4];
-                        l2[4 * c4] = v4.x; l2[4 * c4 + 1] = v4.y; l2[4 * c4 + 2] = v4.z; l2[4 * c4 + 3] = v4.w;
-                    }
+                    for (int k = 0; k < 4; ++k)
+                        l2[k] = ld_shared_f32x2(lse2 + 4 * (c0 + 8 * k + 2 * q4));
                     tmem_wait_ld();
+                    // causal: key kj is masked for query column c iff kj - (m0 + c0 + diag) > c
+                    const int lim = kb - (m0 + c0 + diag) - 2 * q4;
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const int i = grp * HALF + 32 * ch + c;   // query within the block
-                        float pv = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -l2[c]));
-                        if (masked && kj > m0 + i + diag) pv = 0.f;
-                        P[32 * ch + c] = key_ok ? pv : 0.f;
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t pk[8];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+#pragma unroll
+                            for (int r = 0; r < 2; ++r) {
+                                const int kr = 16 * h + 8 * r;    // key offset from kb
+                                float pv0 = ex2(fmaf(__uint_as_float(sr[h][4 * k + 2 * r]), p.scale_log2, -l2[k].x));
+                                float pv1 = ex2(fmaf(__uint_as_float(sr[h][4 * k + 2 * r + 1]), p.scale_log2, -l2[k].y));
+                                if (masked) {
+                                    if (lim + kr > 8 * k) pv0 = 0.f;
+                                    if (lim + kr > 8 * k + 1) pv1 = 0.f;
+                                }
+                                if (kb + kr >= u.lk) { pv0 = 0.f; pv1 = 0.f; }
+                                P[32 * ch + 16 * h + 4 * k + 2 * r] = pv0;
+                                P[32 * ch + 16 * h + 4 * k + 2 * r + 1] = pv1;
+                                pk[2 * k + r] = Cvt<T>::pack(pv0, pv1);
+                            }
+                        }
+                        tmem_st16x128(lane_addr + ((uint32_t)(16 * h) << 16) + C::p_col(cb, grp, ch), pk);
                     }
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) pk[c] = Cvt<T>::pack(P[32 * ch + 2 * c], P[32 * ch + 2 * c + 1]);
-                    tmem_st16(lane_addr + C::p_col(cb, grp, ch), pk);
                 }
                 tmem_wait_st();
                 tc_fence_before();
@@ -769,36 +881,49 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 if (!(ok = mbar_wait(bar(B_DP_FULL + cb), bit(dp_ph, cb), w))) break;
                 dp_ph ^= 1u << cb;
                 tc_fence_after();
-                uint8_t *sds = smem + C::OFF_DS + cb * C::DS_BYTES;
+                const uint32_t sds = sbase + C::OFF_DS + cb * C::DS_BYTES;
                 __syncwarp();
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch) {
-                    uint32_t dr[32];
-                    tmem_ld32(lane_addr + C::dp_col(cb, grp, ch), dr);
-                    float dvv[32];
+                    uint32_t dr[2][16];
+                    tmem_ld16x256(lane_addr + C::dp_col(cb, grp, ch), dr[0]);
+                    tmem_ld16x256(lane_addr + (16u << 16) + C::dp_col(cb, grp, ch), dr[1]);
+                    const int c0 = grp * HALF + 32 * ch;
+                    float2 dd[4];
 #pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4) {
-                        const float4 v4 = reinterpret_cast<const float4 *>(dv + grp * HALF + 32 * ch)[c4];
-                        dvv[4 * c4] = v4.x; dvv[4 * c4 + 1] = v4.y; dvv[4 * c4 + 2] = v4.z; dvv[4 * c4 + 3] = v4.w;
-                    }
+                    for (int k = 0; k < 4; ++k)
+                        dd[k] = ld_shared_f32x2(dv + 4 * (c0 + 8 * k + 2 * q4));
                     tmem_wait_ld();
-                    uint32_t pk[16];
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const float d0 = P[32 * ch + 2 * c] * (__uint_as_float(dr[2 * c]) - dvv[2 * c]);
-                        const float d1 =
-                            P[32 * ch + 2 * c + 1] * (__uint_as_float(dr[2 * c + 1]) - dvv[2 * c + 1]);
-                        pk[c] = Cvt<T>::pack(d0, d1);
-                    }
-                    tmem_st16(lane_addr + C::ds_col(cb, grp, ch), pk);
-                    // dS^T row j into shared memory, 128B-swizzled halves of 64 queries
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t pk[8];
 #pragma unroll
-                    for (int u8 = 0; u8 < 4; ++u8) {
-                        const int i0 = grp * HALF + 32 * ch + 8 * u8;
-                        const int half = i0 / 64, cidx = (i0 % 64) / 8;
-                        const uint32_t off = half * (BN * 128) + j * 128 + ((cidx ^ (j & 7)) << 4);
-                        *reinterpret_cast<uint4 *>(sds + off) =
-                            make_uint4(pk[4 * u8], pk[4 * u8 + 1], pk[4 * u8 + 2], pk[4 * u8 + 3]);
+                        for (int k = 0; k < 4; ++k) {
+#pragma unroll
+                            for (int r = 0; r < 2; ++r) {
+                                const int e0 = 32 * ch + 16 * h + 4 * k + 2 * r;
+                                const float d0 = P[e0] * (__uint_as_float(dr[h][4 * k + 2 * r]) - dd[k].x);
+                                const float d1 = P[e0 + 1] * (__uint_as_float(dr[h][4 * k + 2 * r + 1]) - dd[k].y);
+                                pk[2 * k + r] = Cvt<T>::pack(d0, d1);
+                            }
+                        }
+                        tmem_st16x128(lane_addr + ((uint32_t)(16 * h) << 16) + C::ds_col(cb, grp, ch), pk);
+                        // dS^T rows into shared memory (128B-swizzled halves of 64
+                        // queries): key row jr, queries c0 + 8k + 2*q4, +1 as one
+                        // 4-byte word; the 8 rows x 4 words of one store hit 32
+                        // distinct banks.
+#pragma unroll
+                        for (int r = 0; r < 2; ++r) {
+                            const int jr = quarter * 32 + 16 * h + g4 + 8 * r;
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const int i0 = c0 + 8 * k;
+                                const int half = i0 / 64, cidx = (i0 % 64) / 8;
+                                const uint32_t off = half * (BN * 128) + jr * 128 +
+                                                     ((cidx ^ g4) << 4) + 4 * q4;
+                                st_shared_b32(sds + off, pk[2 * k + r]);
+                            }
+                        }
                     }
                 }
                 tmem_wait_st();
@@ -870,6 +995,7 @@ static cudaError_t launch_main_t(const BwdParams &p, const MainMaps &maps, int g
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
+
     kern<<<grid, C::kThreads, C::SMEM_BYTES, stream>>>(p, maps);
     return cudaGetLastError();
 }

@@ -73,6 +73,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 // Bounded slow path of mbar_wait, kept out of line so the common case (the
 // phase has already completed) costs one try_wait and a branch.
+// Shared-memory accesses by 32-bit shared-window address (base + immediate
+// offsets; no generic-address conversion).
+__device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ float2 ld_shared_f32x2(uint32_t addr) {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+    return v;
+}
+
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                             int *err, long long budget_ns) {
     const uint64_t t0 = globaltimer_ns();
@@ -288,6 +299,33 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
         "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
         "r"(r[15])
+        : "memory");
+}
+
+// 16 lanes x 256 bits (8 columns), 4 repetitions along the columns: with
+// g = t / 4 and q = t % 4, register 4k + e of thread t holds lane
+// lane_base + g + 8 * (e / 2), column col + 8k + 2q + (e % 2) -- the
+// accumulator fragment of a 16x8 mma tile, so a thread sees 8 columns of 2
+// lanes instead of 32 columns of 1.
+__device__ __forceinline__ void tmem_ld16x256(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// 16 lanes x 128 bits (4 columns), 4 repetitions: register 2k + e of thread t
+// goes to lane lane_base + t / 4 + 8e, column col + 4k + t % 4.  With 16-bit
+// pairs packed per column this is the same (lane, element) set as
+// tmem_ld16x256 reads from a 32-bit matrix.
+__device__ __forceinline__ void tmem_st16x128(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x128b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
         : "memory");
 }
 

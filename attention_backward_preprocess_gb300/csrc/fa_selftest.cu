@@ -9,6 +9,9 @@
 //   mode 2: C = At^T * Bt, At [K x 128] and Bt [K x N] both MN-major in shared
 //           memory (the dQ form)
 // C is fp32 [128 x N].  K in {64, 128}, N in {64, 128}.
+// A second kernel writes and reads tensor memory through the 16-lane access
+// shapes the softmax warps use, so their register <-> (lane, column) mapping
+// can be checked against the plain 32-lane shape.
 #include "fa_device.cuh"
 #include "../../include/fa_selftest.h"
 
@@ -124,6 +127,68 @@ __global__ void __launch_bounds__(kThreads) selftest_kernel(int mode, int N, int
     (void)lane;
 }
 
+// which 0: each thread writes (row << 8 | column) into columns 0..31 of its
+//          own lane with the 32-lane shape, then reads them back with
+//          tmem_ld16x256 at lane offsets 0 and 16 of its warp's quarter:
+//          out[thread * 32 + 16 * h + reg].
+// which 1: zeros with the 32-lane shape, then tmem_st16x128 of the values
+//          0x80000000 | thread << 8 | h << 4 | reg at lane offsets h = 0, 1,
+//          read back with the 32-lane shape: out[row * 32 + column].
+__global__ void __launch_bounds__(128) tmem_layout_kernel(int which, uint32_t *out) {
+    __shared__ uint32_t tmem_base_s;
+    const int warp = threadIdx.x / 32;
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&tmem_base_s), 32);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+    const uint32_t lb = (uint32_t)(warp * 32) << 16;
+    const uint32_t row = threadIdx.x;
+    uint32_t a[16], b[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+        a[c] = which == 0 ? (row << 8 | (uint32_t)c) : 0u;
+        b[c] = which == 0 ? (row << 8 | (uint32_t)(16 + c)) : 0u;
+    }
+    tmem_st16(tmem + lb, a);
+    tmem_st16(tmem + lb + 16, b);
+    tmem_wait_st();
+    __syncwarp();
+    if (which == 0) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t r[16];
+            tmem_ld16x256(tmem + lb + ((uint32_t)(16 * h) << 16), r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) out[threadIdx.x * 32 + 16 * h + k] = r[k];
+        }
+    } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t r[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                r[k] = 0x80000000u | (uint32_t)threadIdx.x << 8 | (uint32_t)h << 4 | (uint32_t)k;
+            tmem_st16x128(tmem + lb + ((uint32_t)(16 * h) << 16), r);
+        }
+        tmem_wait_st();
+        __syncwarp();
+        uint32_t r[32];
+        tmem_ld32(tmem + lb, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) out[row * 32 + c] = r[c];
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 32);
+}
+
 __global__ void semaphore_kernel(int *sem, int target, long long budget_ns, int *err) {
     __shared__ int abort_flag;
     if (threadIdx.x == 0) abort_flag = 0;
@@ -155,5 +220,11 @@ extern "C" int fa_selftest_semaphore(int *sem, int target, long long budget_ns, 
                                      cudaStream_t stream) {
     if (!sem || !err || budget_ns <= 0) return 1;
     fa::semaphore_kernel<<<1, 32, 0, stream>>>(sem, target, budget_ns, err);
+    return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+extern "C" int fa_selftest_tmem_layout(int which, unsigned int *out, cudaStream_t stream) {
+    if ((which != 0 && which != 1) || !out) return 1;
+    fa::tmem_layout_kernel<<<1, 128, 0, stream>>>(which, out);
     return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }

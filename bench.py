@@ -342,7 +342,7 @@ def main():
         "kernels_gbs": {"preprocess": pre_bytes / (statistics.mean(pre_ms) * 1e-3) / 1e9,
                         "postprocess": post_bytes / (statistics.mean(post_ms) * 1e-3) / 1e9,
                         "hbm_peak": pk["hbm"]},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 3 * args.steps,    # preprocess, main, postprocess (dense: no scheduler launch)
         "device_status": status,
         "e2e": e2e,
         "clocks": clk,

@@ -31,6 +31,18 @@ int fa_selftest_umma(int mode, int N, int K, int bf16, const void *A, const void
 int fa_selftest_semaphore(int *sem, int target, long long budget_ns, int *err,
                           cudaStream_t stream);
 
+/* Register layout of the 16-lane tensor-memory access shapes: one CTA of 128
+ * threads, 32 allocated columns, out = device uint32 [128 x 32].
+ *   which 0: thread r writes (r << 8 | c) into column c of lane r with the
+ *            32-lane shape, then every thread reads 2 x 16 registers with the
+ *            16x256b.x4 shape at lane offsets 0 and 16 of its warp's quarter
+ *            into out[r * 32 + 16 h + reg].
+ *   which 1: every thread writes 0x80000000 | r << 8 | h << 4 | reg with the
+ *            16x128b.x4 shape at lane offsets h = 0, 1 over zeros; out[lane *
+ *            32 + column] is what the 32-lane shape then reads.
+ * Returns 0, 1 (bad argument) or 3 (CUDA error). */
+int fa_selftest_tmem_layout(int which, unsigned int *out, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -53,3 +53,38 @@ def test_semaphore_wait_that_succeeds(fa, cuda_device):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert int(sem.item()) == 6
+
+
+def test_tmem_16x256b_load_layout(fa, cuda_device):
+    """Register 4k + e of thread t, lane offset h: lane 32 w + 16 h + t/4 + 8 (e/2),
+    column 8k + 2 (t%4) + e%2 (w = warp, t = thread in the warp)."""
+    out = fa.selftest_tmem_layout(0)
+    bad = []
+    for r in range(128):
+        w, t = divmod(r, 32)
+        for h in range(2):
+            for reg in range(16):
+                k, e = divmod(reg, 4)
+                lane = 32 * w + 16 * h + t // 4 + 8 * (e // 2)
+                col = 8 * k + 2 * (t % 4) + e % 2
+                got = int(out[r, 16 * h + reg])
+                if got != (lane << 8 | col):
+                    bad.append((r, h, reg, got >> 8, got & 255, lane, col))
+    assert not bad, bad[:8]
+
+
+def test_tmem_16x128b_store_layout(fa, cuda_device):
+    """Register 2k + e of thread t, lane offset h goes to lane 32 w + 16 h + t/4 + 8e,
+    column 4k + t%4; columns 16..31 stay untouched."""
+    out = fa.selftest_tmem_layout(1)
+    want = torch.zeros((128, 32), dtype=torch.int64)
+    for r in range(128):
+        w, t = divmod(r, 32)
+        for h in range(2):
+            for reg in range(8):
+                k, e = divmod(reg, 2)
+                lane = 32 * w + 16 * h + t // 4 + 8 * e
+                col = 4 * k + t % 4
+                want[lane, col] = 0x80000000 | r << 8 | h << 4 | reg
+    bad = (out != want).nonzero().tolist()
+    assert not bad, [(l, c, hex(int(out[l, c])), hex(int(want[l, c]))) for l, c in bad[:8]]
