@@ -50,15 +50,19 @@ struct MainCfg {
     // dQ GEMM orientation: the MMA's M (=128) is d when D = 128 (dQ^T = K^T dS^T,
     // TMEM lanes = d) and the query row when D = 64 (dQ = dS K, lanes = query).
     static constexpr bool kDqT = (kD == 128);
-    // Two-deep software pipeline (D = 128): S^T, dP^T and dS^T are double
-    // buffered, so the MMAs of step i+1 (S, dP) run while the softmax warps
-    // turn step i's dP into dS.  TMEM (512 columns):
-    //   dK 128 | dV 128 | S^T x2 (64 each; P^T bf16 and dS^T bf16 written back
-    //   into each buffer) | X x2 (64 each; dP^T of a step, then its dQ^T).
+    // Software pipeline (D = 128).  TMEM (512 columns):
+    //   dK 128 | dV 128 | S buffer x3 | X 64
+    // An S buffer (64 columns) carries one step through its life: S^T, then
+    // P^T and dS^T as bf16 pairs in its two halves, then -- once dV and dK
+    // have read those -- that step's dQ^T, until the reducers take it out.
+    // X holds dP^T, which the softmax warps read as soon as it is complete.
+    // With three S buffers, S^T of step j waits only for the dQ^T of step
+    // j-3 to be drained, and dP^T of step j only for the softmax to have read
+    // dP^T of step j-1.
     // D = 64 (BM = 128) has no room for second buffers and runs the steps one
     // after the other: dK 64 | dV 64 | S^T 128 | dP^T 128 | dQ 64.
     static constexpr bool kPipe = (kD == 128);
-    static constexpr int kBuf = kPipe ? 2 : 1;
+    static constexpr int kSBuf = kPipe ? 3 : 1;
     static constexpr int kStages = kPipe ? 3 : 4;
     // Warp roles: 0 producer | 1 MMA issuer (D = 64) or MMA warp A (S, dP) |
     // 2 MMA warp B (dV, dK, dQ; D = 128) | 3 bulk-reduce issuer (D = 128) |
@@ -69,25 +73,25 @@ struct MainCfg {
     static constexpr int TM_DK = 0;
     static constexpr int TM_DV = D;
     static constexpr int TM_S = 2 * D;
-    static constexpr int TM_X = TM_S + kBuf * BM;          // kPipe: dP then dQ per buffer
+    static constexpr int TM_X = TM_S + kSBuf * BM;         // kPipe: dP^T
     static constexpr int TM_DP = TM_S + BM;                // !kPipe
     static constexpr int TM_DQ = TM_S + 2 * BM;            // !kPipe
     static constexpr int TM_COLS = 512;
-    static_assert(kPipe ? (TM_X + 2 * BM <= TM_COLS) : (TM_DQ + 64 <= TM_COLS), "TMEM overflow");
-    // columns (buffer b, softmax group g, 32-query chunk ch)
+    static_assert(kPipe ? (TM_X + BM <= TM_COLS) : (TM_DQ + 64 <= TM_COLS), "TMEM overflow");
+    // columns (S buffer b, softmax group g, 32-query chunk ch)
     static __device__ __forceinline__ int s_col(int b, int g, int ch) {
         return kPipe ? TM_S + b * BM + g * HALF : TM_S + g * HALF + 32 * ch;
     }
     static __device__ __forceinline__ int p_col(int b, int g, int ch) {   // P^T bf16 pairs
         return kPipe ? TM_S + b * BM + g * HALF : TM_S + g * HALF + 16 * ch;
     }
-    static __device__ __forceinline__ int dp_col(int b, int g, int ch) {
-        return kPipe ? TM_X + b * BM + g * HALF : TM_DP + g * HALF + 32 * ch;
+    static __device__ __forceinline__ int dp_col(int g, int ch) {
+        return kPipe ? TM_X + g * HALF : TM_DP + g * HALF + 32 * ch;
     }
     static __device__ __forceinline__ int ds_col(int b, int g, int ch) {  // dS^T bf16 pairs
         return kPipe ? TM_S + b * BM + g * HALF + 16 : TM_DP + g * HALF + 16 * ch;
     }
-    static __device__ __forceinline__ int dq_col(int b) { return kPipe ? TM_X + b * BM : TM_DQ; }
+    static __device__ __forceinline__ int dq_col(int b) { return kPipe ? TM_S + b * BM : TM_DQ; }
     // A-operand column of MMA K step kk (queries 16kk .. 16kk+15) of P^T / dS^T
     static __device__ __forceinline__ int p_op(int b, int kk) {
         const int g = (16 * kk) / HALF;
@@ -115,11 +119,13 @@ struct MainCfg {
     static constexpr int CHUNK_ROWS = 32;
     static constexpr int CHUNK_BYTES = CHUNK_ROWS * D * 4;
     static constexpr int STG_BYTES = kBulk ? 2 * CHUNK_BYTES : 0;
-    static constexpr int OFF_STG = OFF_DS + kBuf * DS_BYTES;
+    static constexpr int kDsBuf = kPipe ? 2 : 1;           // dS^T tiles in shared memory
+    static constexpr int OFF_STG = OFF_DS + kDsBuf * DS_BYTES;
     static constexpr int OFF_LSE = OFF_STG + STG_BYTES;
     static constexpr int OFF_DV = OFF_LSE + kStages * BM * 4;
     static constexpr int OFF_BAR = OFF_DV + kStages * BM * 4;
     static constexpr int NUM_BARS = 48;
+    static_assert(38 + 2 * kStages <= NUM_BARS, "barrier slots");
     // TMEM slot (+0), abort flag (+16), unit ring (+32), staging rows (+48)
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
@@ -133,23 +139,26 @@ struct MainCfg {
 };
 
 // Barrier indices.  Hand-offs that can be committed before their waiter has
-// looked at the previous phase come in pairs, one per TMEM buffer, so that no
-// barrier ever runs two phases ahead of a waiter.
+// looked at the previous phase come one per buffer, so that no barrier ever
+// runs two phases ahead of a waiter.
 enum {
     B_KV_FULL = 0, B_KV_EMPTY = 1,
-    B_S_FULL = 2,    // +b
-    B_P_FULL = 4,    // +b
-    B_DP_FULL = 6,   // +b
-    B_DS_FULL = 8,   // +b
-    B_DQ_FULL = 10,  // +b
-    B_DQ_EMPTY = 12, // +b
-    B_ACC_FULL = 14, B_ACC_EMPTY = 15, B_DRAIN = 16,
-    B_UNIT_FULL = 17,   // +k, k < kRing: unit index k of the ring written
-    B_UNIT_EMPTY = 21,  // +k: every consumer warp has read it
-    B_STG_FULL = 25,    // +b: the 4 reducer warps wrote dQ staging buffer b
-    B_STG_FREE = 27,    // +b: the bulk reduce has read staging buffer b
-    B_SBUF_FREE = 29,   // +b: dV / dK done reading P^T / dS^T of S buffer b
-    B_STAGE0 = 31       // full[kStages], then empty[kStages]
+    B_S_FULL = 2,       // +b, S buffer b: S^T complete
+    B_P_FULL = 5,       // +b: P^T written back
+    B_DS_FULL = 8,      // +b: dS^T written back (TMEM and shared memory)
+    B_DQ_FULL = 11,     // +b: dQ^T complete
+    B_S_FREE = 14,      // +b (D = 128): the reducers took dQ^T out of S buffer b
+    B_DP_FULL = 17,     // dP^T complete
+    B_X_FREE = 18,      // (D = 128) the softmax warps read dP^T
+    B_DQ_EMPTY = 19,    // (D = 64) the reducers took dQ out of TMEM
+    B_DSB_FREE = 20,    // +d (D = 128): dQ^T MMA done reading dS^T tile d
+    B_KDONE = 22,       // (D = 128) dV and dK of the step complete
+    B_ACC_FULL = 23, B_ACC_EMPTY = 24, B_DRAIN = 25,
+    B_UNIT_FULL = 26,   // +k, k < kRing: unit index k of the ring written
+    B_UNIT_EMPTY = 30,  // +k: every consumer warp has read it
+    B_STG_FULL = 34,    // +b: the 4 reducer warps wrote dQ staging buffer b
+    B_STG_FREE = 36,    // +b: the bulk reduce has read staging buffer b
+    B_STAGE0 = 38       // full[kStages], then empty[kStages]
 };
 
 // Work units are handed out dynamically: the producer warp takes the next
@@ -255,18 +264,21 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         *abort_flag = 0;
         mbar_init(bar(B_KV_FULL), 1);
         mbar_init(bar(B_KV_EMPTY), C::kPipe ? 2 : 1);   // one commit per MMA warp
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < 3; ++b) {
             mbar_init(bar(B_S_FULL + b), 1);
             mbar_init(bar(B_P_FULL + b), 8);
-            mbar_init(bar(B_DP_FULL + b), 1);
             mbar_init(bar(B_DS_FULL + b), 8);
             mbar_init(bar(B_DQ_FULL + b), 1);
-            mbar_init(bar(B_DQ_EMPTY + b), 4);
+            mbar_init(bar(B_S_FREE + b), 4);
         }
+        mbar_init(bar(B_DP_FULL), 1);
+        mbar_init(bar(B_X_FREE), 8);
+        mbar_init(bar(B_DQ_EMPTY), 4);
+        for (int d = 0; d < 2; ++d) mbar_init(bar(B_DSB_FREE + d), 1);
+        mbar_init(bar(B_KDONE), 1);
         mbar_init(bar(B_ACC_FULL), 1);
         mbar_init(bar(B_ACC_EMPTY), 8);
         mbar_init(bar(B_DRAIN), C::kPipe ? 2 : 1);
-        for (int b = 0; b < 2; ++b) mbar_init(bar(B_SBUF_FREE + b), 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(B_STG_FULL + b), 4);
             mbar_init(bar(B_STG_FREE + b), 1);
@@ -347,7 +359,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     kv_ph ^= 1;
                     mbar_arrive_expect_tx(bar(B_KV_FULL), 2 * C::KV_BYTES);
                     const int krow = u.k_row0 + u.n_block * BN;
-    #pragma unroll
+#pragma unroll
                     for (int h = 0; h < D / 64; ++h) {
                         tma_load_4d(sbase + C::OFF_K + h * BN * 128, &maps.k, bar(B_KV_FULL), h * 64,
                                     u.hk, krow, u.bidx);
@@ -361,7 +373,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                         const uint32_t full = bar(B_STAGE0 + stage);
                         mbar_arrive_expect_tx(full, 2 * C::QO_BYTES + 2 * BM * 4);
                         const int qrow = u.q_row0 + m * BM;
-    #pragma unroll
+#pragma unroll
                         for (int hh = 0; hh < D / 64; ++hh) {
                             tma_load_4d(sbase + C::OFF_Q + stage * C::QO_BYTES + hh * BM * 128, &maps.q,
                                         full, hh * 64, h, qrow, u.bidx);
@@ -377,55 +389,15 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             }
         } else if (warp == 1 && !C::kPipe) {
             // ---------------------------------------------------------- MMA issuer
-            // The whole warp runs this loop in lock-step; elect.sync picks the lane
+            // D = 64: one warp issues every MMA of a step in order (S, dP, dV,
+            // dK, dQ) with one buffer of each kind; elect.sync picks the lane
             // that issues each MMA / commit.
-            uint32_t kv_ph = 0, acc_ph = 0;
-            uint32_t p_ph = 0, ds_ph = 0, dqe_ph = 0;   // bit b: phase parity of buffer b
-            int s_stage = 0;          // stage of the next step whose S / dP is issued
-            uint32_t s_ph = 0;
-            int c_stage = 0;          // stage of the step whose dV / dK / dQ is issued
-            int nb = 0, cb = 0;       // TMEM buffer of the next step / of the current step
+            uint32_t kv_ph = 0, acc_ph = 0, p_ph = 0, ds_ph = 0, dqe_ph = 0, s_ph = 0;
+            int stage = 0;
             bool ok = true;
             const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
             const uint64_t dK_k = sw128_desc(sK, 16, 1024), dV_k = sw128_desc(sV, 16, 1024);
             const uint64_t dK_mn = sw128_desc(sK, BN * 128, 1024);
-            // S^T = K Q^T of the next step into S buffer nb (waits for its stage)
-            auto issue_s = [&]() -> bool {
-                if (!mbar_wait_warp(bar(B_STAGE0 + s_stage), s_ph, w)) return false;
-                tc_fence_after();
-                const uint64_t dQ_k = sw128_desc(sbase + C::OFF_Q + s_stage * C::QO_BYTES, 16, 1024);
-                const uint32_t d = tmem + C::s_col(nb, 0, 0);
-    #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
-                    const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
-                    mma_ss_warp(d, desc_add(dK_k, ko), desc_add(dQ_k, qo), C::IDESC_S, kk > 0);
-                }
-                mma_commit_warp(bar(B_S_FULL + nb));
-                return true;
-            };
-            // dP^T = V dO^T of the next step into its dP buffer
-            auto issue_dp = [&]() -> bool {
-                uint32_t d = tmem + C::TM_DP;
-                if (C::kPipe) {
-                    // X buffer nb last held a dQ^T: wait until the reducers read it
-                    if (!mbar_wait_warp(bar(B_DQ_EMPTY + nb), bit(dqe_ph, nb) ^ 1u, w)) return false;
-                    dqe_ph ^= 1u << nb;
-                    tc_fence_after();
-                    d = tmem + C::dp_col(nb, 0, 0);
-                }
-                const uint64_t dDO_k = sw128_desc(sbase + C::OFF_DO + s_stage * C::QO_BYTES, 16, 1024);
-    #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
-                    const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
-                    mma_ss_warp(d, desc_add(dV_k, ko), desc_add(dDO_k, qo), C::IDESC_S, kk > 0);
-                }
-                mma_commit_warp(bar(B_DP_FULL + nb));
-                if (++s_stage == S) { s_stage = 0; s_ph ^= 1; }
-                if (C::kPipe) nb ^= 1;
-                return true;
-            };
             while (ok) {
                 const int t = next_unit();
                 if (t < 0) break;
@@ -434,57 +406,64 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 if (!(ok = mbar_wait_warp(bar(B_KV_FULL), kv_ph, w))) break;
                 kv_ph ^= 1;
                 tc_fence_after();
-                if (C::kPipe && !(ok = issue_s() && issue_dp())) break;   // step 0 of the unit
                 for (int it = 0; it < u.iters; ++it) {
-                    const bool more = it + 1 < u.iters;
-                    if (C::kPipe) {
-                        if (more && !(ok = issue_s())) break;             // S of step it+1
-                    } else {
-                        if (!(ok = issue_s() && issue_dp())) break;       // S, dP of step it
+                    if (!(ok = mbar_wait_warp(bar(B_STAGE0 + stage), s_ph, w))) break;
+                    tc_fence_after();
+                    const uint32_t sQ = sbase + C::OFF_Q + stage * C::QO_BYTES;
+                    const uint32_t sDO = sbase + C::OFF_DO + stage * C::QO_BYTES;
+                    // S^T = K Q^T
+                    const uint64_t dQ_k = sw128_desc(sQ, 16, 1024), dDO_k = sw128_desc(sDO, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
+                        const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
+                        mma_ss_warp(tmem + C::s_col(0, 0, 0), desc_add(dK_k, ko), desc_add(dQ_k, qo),
+                                    C::IDESC_S, kk > 0);
                     }
+                    mma_commit_warp(bar(B_S_FULL));
+                    // dP^T = V dO^T
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
+                        const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
+                        mma_ss_warp(tmem + C::TM_DP, desc_add(dV_k, ko), desc_add(dDO_k, qo),
+                                    C::IDESC_S, kk > 0);
+                    }
+                    mma_commit_warp(bar(B_DP_FULL));
                     if (it == 0) {
                         if (!(ok = mbar_wait_warp(bar(B_ACC_EMPTY), acc_ph ^ 1, w))) break;
                         acc_ph ^= 1;
                     }
-                    const uint32_t sQ = sbase + C::OFF_Q + c_stage * C::QO_BYTES;
-                    const uint32_t sDO = sbase + C::OFF_DO + c_stage * C::QO_BYTES;
-                    if (!(ok = mbar_wait_warp(bar(B_P_FULL + cb), bit(p_ph, cb), w))) break;
-                    p_ph ^= 1u << cb;
+                    if (!(ok = mbar_wait_warp(bar(B_P_FULL), p_ph, w))) break;
+                    p_ph ^= 1;
                     tc_fence_after();
                     // dV += P^T dO  (P^T bf16 in TMEM; dO MN-major: K step = 16 rows = 2048 B)
                     const uint64_t dDO_mn = sw128_desc(sDO, BM * 128, 1024);
-    #pragma unroll
+#pragma unroll
                     for (int kk = 0; kk < BM / 16; ++kk)
-                        mma_ts_warp(tmem + C::TM_DV, tmem + C::p_op(cb, kk), desc_add(dDO_mn, kk * 2048),
+                        mma_ts_warp(tmem + C::TM_DV, tmem + C::p_op(0, kk), desc_add(dDO_mn, kk * 2048),
                                     C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
-                    if (C::kPipe && more && !(ok = issue_dp())) break;   // dP of step it+1
-                    if (!(ok = mbar_wait_warp(bar(B_DS_FULL + cb), bit(ds_ph, cb), w))) break;
-                    ds_ph ^= 1u << cb;
+                    if (!(ok = mbar_wait_warp(bar(B_DS_FULL), ds_ph, w))) break;
+                    ds_ph ^= 1;
                     tc_fence_after();
                     // dK += dS^T Q
                     const uint64_t dQ_mn = sw128_desc(sQ, BM * 128, 1024);
-    #pragma unroll
+#pragma unroll
                     for (int kk = 0; kk < BM / 16; ++kk)
-                        mma_ts_warp(tmem + C::TM_DK, tmem + C::ds_op(cb, kk), desc_add(dQ_mn, kk * 2048),
+                        mma_ts_warp(tmem + C::TM_DK, tmem + C::ds_op(0, kk), desc_add(dQ_mn, kk * 2048),
                                     C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit_warp(bar(B_STAGE0 + S + c_stage));   // Q / dO of this stage consumed
-                    if (!C::kPipe) {
-                        if (!(ok = mbar_wait_warp(bar(B_DQ_EMPTY), bit(dqe_ph, 0) ^ 1u, w))) break;
-                        dqe_ph ^= 1u;
-                        tc_fence_after();
-                    }
-                    // dQ (kDqT: dQ^T = K^T dS^T, else dQ = dS K); both operands MN-major
-                    const uint64_t dDS_mn =
-                        sw128_desc(sbase + C::OFF_DS + cb * C::DS_BYTES, BN * 128, 1024);
-                    const uint64_t dq_a = C::kDqT ? dK_mn : dDS_mn;
-                    const uint64_t dq_b = C::kDqT ? dDS_mn : dK_mn;
-    #pragma unroll
+                    mma_commit_warp(bar(B_STAGE0 + S + stage));   // Q / dO of this stage consumed
+                    if (!(ok = mbar_wait_warp(bar(B_DQ_EMPTY), dqe_ph ^ 1u, w))) break;
+                    dqe_ph ^= 1;
+                    tc_fence_after();
+                    // dQ = dS K; both operands MN-major
+                    const uint64_t dDS_mn = sw128_desc(sbase + C::OFF_DS, BN * 128, 1024);
+#pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
-                        mma_ss_warp(tmem + C::dq_col(cb), desc_add(dq_a, kk * 2048),
-                                    desc_add(dq_b, kk * 2048), C::IDESC_DQ, kk > 0);
-                    mma_commit_warp(bar(B_DQ_FULL + cb));
-                    if (++c_stage == S) c_stage = 0;
-                    if (C::kPipe) cb ^= 1;
+                        mma_ss_warp(tmem + C::dq_col(0), desc_add(dDS_mn, kk * 2048),
+                                    desc_add(dK_mn, kk * 2048), C::IDESC_DQ, kk > 0);
+                    mma_commit_warp(bar(B_DQ_FULL));
+                    if (++stage == S) { stage = 0; s_ph ^= 1; }
                 }
                 if (!ok) break;
                 mma_commit_warp(bar(B_ACC_FULL));
@@ -495,13 +474,12 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             mbar_wait_warp(bar(B_DRAIN), 0, w);
         } else if (warp == 1 && C::kPipe) {
             // ------------------------------------------- MMA warp A: S and dP
-            // Issues S^T_j = K Q_j^T and dP^T_j = V dO_j^T for every step j, ahead
-            // of warp B.  Before S_j it waits until warp B's dV / dK of step j-2
-            // released S buffer j%2, before dP_j until the reducers drained the
-            // dQ^T of step j-2 from X buffer j%2.
-            uint32_t kv_ph = 0, sfree_ph = 0, dqe_ph = 0;   // bit b: parity of buffer b
+            // Issues S^T_j = K Q_j^T into S buffer j%3 and dP^T_j = V dO_j^T into
+            // X for every step j, ahead of warp B.  Before S_j it waits until the
+            // reducers took the dQ^T of step j-3 out of that S buffer, before dP_j
+            // until the softmax warps read dP^T of step j-1.
+            uint32_t kv_ph = 0, sfree_ph = 0, xfree_ph = 0, s_ph = 0;   // sfree: bit per buffer
             int s_stage = 0, nb = 0;
-            uint32_t s_ph = 0;
             bool ok = true;
             const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
             const uint64_t dK_k = sw128_desc(sK, 16, 1024), dV_k = sw128_desc(sV, 16, 1024);
@@ -514,12 +492,12 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 kv_ph ^= 1;
                 for (int j = 0; j < u.iters; ++j) {
                     if (!(ok = mbar_wait_warp(bar(B_STAGE0 + s_stage), s_ph, w))) break;
-                    if (!(ok = mbar_wait_warp(bar(B_SBUF_FREE + nb), bit(sfree_ph, nb) ^ 1u, w))) break;
+                    if (!(ok = mbar_wait_warp(bar(B_S_FREE + nb), bit(sfree_ph, nb) ^ 1u, w))) break;
                     sfree_ph ^= 1u << nb;
                     tc_fence_after();
                     const uint64_t dQ_k = sw128_desc(sbase + C::OFF_Q + s_stage * C::QO_BYTES, 16, 1024);
                     const uint64_t dDO_k = sw128_desc(sbase + C::OFF_DO + s_stage * C::QO_BYTES, 16, 1024);
-    #pragma unroll
+#pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
                         const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
@@ -527,20 +505,20 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                                     C::IDESC_S, kk > 0);
                     }
                     mma_commit_warp(bar(B_S_FULL + nb));
-                    if (!(ok = mbar_wait_warp(bar(B_DQ_EMPTY + nb), bit(dqe_ph, nb) ^ 1u, w))) break;
-                    dqe_ph ^= 1u << nb;
+                    if (!(ok = mbar_wait_warp(bar(B_X_FREE), xfree_ph ^ 1u, w))) break;
+                    xfree_ph ^= 1u;
                     tc_fence_after();
-    #pragma unroll
+#pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
                         const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
-                        mma_ss_warp(tmem + C::dp_col(nb, 0, 0), desc_add(dV_k, ko), desc_add(dDO_k, qo),
+                        mma_ss_warp(tmem + C::TM_X, desc_add(dV_k, ko), desc_add(dDO_k, qo),
                                     C::IDESC_S, kk > 0);
                     }
-                    mma_commit_warp(bar(B_DP_FULL + nb));
+                    mma_commit_warp(bar(B_DP_FULL));
                     mma_commit_warp(bar(B_STAGE0 + S + s_stage));   // warp A's share of the stage
                     if (++s_stage == S) { s_stage = 0; s_ph ^= 1; }
-                    nb ^= 1;
+                    if (++nb == C::kSBuf) nb = 0;
                 }
                 if (!ok) break;
                 mma_commit_warp(bar(B_KV_EMPTY));
@@ -549,8 +527,11 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             mbar_wait_warp(bar(B_DRAIN), 0, w);
         } else if (warp == C::W_MMA_B && C::kPipe) {
             // ---------------------------------------- MMA warp B: dV, dK and dQ
-            uint32_t kv_ph = 0, acc_ph = 0, p_ph = 0, ds_ph = 0;   // p / ds: bit per buffer
-            int c_stage = 0, cb = 0;
+            // For step j (S buffer j%3, dS^T tile j%2): dV += P^T dO once P^T is
+            // written back, dK += dS^T Q once dS^T is; then, after dV and dK have
+            // finished reading the S buffer, dQ^T = K^T dS^T into that same buffer.
+            uint32_t kv_ph = 0, acc_ph = 0, p_ph = 0, ds_ph = 0, kd_ph = 0;   // p / ds: bit per buffer
+            int c_stage = 0, cb = 0, db = 0;
             bool ok = true;
             const uint64_t dK_mn = sw128_desc(sbase + C::OFF_K, BN * 128, 1024);
             while (ok) {
@@ -572,7 +553,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     tc_fence_after();
                     // dV += P^T dO  (P^T bf16 in TMEM; dO MN-major: K step = 16 rows = 2048 B)
                     const uint64_t dDO_mn = sw128_desc(sDO, BM * 128, 1024);
-    #pragma unroll
+#pragma unroll
                     for (int kk = 0; kk < BM / 16; ++kk)
                         mma_ts_warp(tmem + C::TM_DV, tmem + C::p_op(cb, kk), desc_add(dDO_mn, kk * 2048),
                                     C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
@@ -581,22 +562,27 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     tc_fence_after();
                     // dK += dS^T Q
                     const uint64_t dQ_mn = sw128_desc(sQ, BM * 128, 1024);
-    #pragma unroll
+#pragma unroll
                     for (int kk = 0; kk < BM / 16; ++kk)
                         mma_ts_warp(tmem + C::TM_DK, tmem + C::ds_op(cb, kk), desc_add(dQ_mn, kk * 2048),
                                     C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit_warp(bar(B_SBUF_FREE + cb));   // P^T / dS^T of this buffer consumed
-                    // dQ^T = K^T dS^T into X buffer cb (its dP^T was read before dS was ready)
+                    mma_commit_warp(bar(B_STAGE0 + S + c_stage));   // warp B's share of the stage
+                    // dQ^T overwrites the P^T / dS^T that dV and dK read: wait for them
+                    mma_commit_warp(bar(B_KDONE));
+                    if (!(ok = mbar_wait_warp(bar(B_KDONE), kd_ph, w))) break;
+                    kd_ph ^= 1u;
+                    tc_fence_after();
                     const uint64_t dDS_mn =
-                        sw128_desc(sbase + C::OFF_DS + cb * C::DS_BYTES, BN * 128, 1024);
-    #pragma unroll
+                        sw128_desc(sbase + C::OFF_DS + db * C::DS_BYTES, BN * 128, 1024);
+#pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
                         mma_ss_warp(tmem + C::dq_col(cb), desc_add(dK_mn, kk * 2048),
                                     desc_add(dDS_mn, kk * 2048), C::IDESC_DQ, kk > 0);
                     mma_commit_warp(bar(B_DQ_FULL + cb));
-                    mma_commit_warp(bar(B_STAGE0 + S + c_stage));   // warp B's share of the stage
+                    mma_commit_warp(bar(B_DSB_FREE + db));   // dS^T tile db read
                     if (++c_stage == S) c_stage = 0;
-                    cb ^= 1;
+                    if (++cb == C::kSBuf) cb = 0;
+                    db ^= 1;
                 }
                 if (!ok) break;
                 mma_commit_warp(bar(B_ACC_FULL));
@@ -646,27 +632,30 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             int chunk = 0;                         // chunks written so far (staging buffer = chunk & 1)
             int cb = 0;                            // TMEM X buffer of the next step
             bool ok = true;
-            // step iterator over the units of the ring
-            int cur_iters = 0, cur_it = 0;
-            Unit cu{};
+            // step iterator over the units of the ring: row of (head g, row block
+            // m) = head0 + g * hstride + m * BM, heads innermost, row blocks
+            // from the last one down (the MMA warps' order)
+            long long head0 = 0, hstride = 0;
+            int g_it = 0, m_it = -1, m_first = 0;
             bool units_done = false;
             auto next_row = [&](long long &row0) __attribute__((always_inline)) -> bool {
-                while (true) {
-                    if (cur_it < cur_iters) {
-                        const int g = cu.g_of(cur_it, p.G), m = cu.m_of(cur_it, p.G);
-                        row0 = ws_row(p, cu.b, cu.hk * p.G + g, m * BM);
-                        ++cur_it;
-                        return true;
-                    }
+                while (m_it < m_first) {
                     if (units_done) return false;
                     const int t = next_unit();
                     if (t < 0) { units_done = true; return false; }
-                    cu = decode_unit<BM>(p, t);
-                    cur_iters = cu.iters;
-                    cur_it = 0;
+                    const Unit u = decode_unit<BM>(p, t);
+                    if (u.nm == 0) continue;
+                    head0 = ws_row(p, u.b, u.hk * p.G, 0);
+                    hstride = ws_row(p, u.b, u.hk * p.G + 1, 0) - head0;
+                    m_first = u.m_begin;
+                    m_it = u.m_begin + u.nm - 1;
+                    g_it = 0;
                 }
+                row0 = head0 + g_it * hstride + (long long)m_it * BM;
+                if (++g_it == p.G) { g_it = 0; --m_it; }
+                return true;
             };
-            // dQ^T of the step in TMEM buffer b -> (X, Y); releases the buffer
+            // dQ^T of the step in S buffer b -> (X, Y); releases the buffer
             auto load_step = [&](uint32_t (&X)[32], uint32_t (&Y)[32], int b) __attribute__((always_inline)) {
                 tc_fence_after();
                 __syncwarp();
@@ -675,7 +664,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_DQ_EMPTY + b));
+                if (lane == 0) mbar_arrive(bar(B_S_FREE + b));
             };
             auto wait_dq = [&](int b) __attribute__((always_inline)) -> bool {
                 if (!mbar_wait_warp(bar(B_DQ_FULL + b), bit(dq_ph, b), w)) return false;
@@ -691,7 +680,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             auto write_chunk = [&](const uint32_t (&X)[32], long long row) __attribute__((always_inline)) {
                 const int sb = chunk & 1;
                 const uint32_t stg = sbase + C::OFF_STG + sb * C::CHUNK_BYTES + 4 * r;
-            #pragma unroll
+#pragma unroll
                 for (int i = 0; i < 32; ++i) st_shared_b32(stg + 4 * D * i, X[i]);
                 fence_async_smem();
                 __syncwarp();
@@ -706,7 +695,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             while (ok && next_row(row0)) {
                 if (!(ok = wait_dq(cb))) break;
                 load_step(R0, R1, cb);
-                cb ^= 1;
+                if (++cb == C::kSBuf) cb = 0;
                 if (!(ok = wait_stg())) break;
                 write_chunk(R0, row0);
                 if (!(ok = wait_stg())) break;
@@ -746,8 +735,8 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     tmem_wait_ld();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(B_DQ_EMPTY + cb));
-                    if (C::kPipe) cb ^= 1;
+                    if (lane == 0) mbar_arrive(bar(C::kPipe ? B_S_FREE + cb : B_DQ_EMPTY));
+                    if (++cb == C::kSBuf) cb = 0;
                     const long long row0 = ws_row(p, u.b, h, m * BM);
                     int *sem = p.sem + row0 / 64;
                     if (p.deterministic) {
@@ -764,10 +753,10 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                         // lane r = d; columns = BM (=64) query rows; a warp adds 32
                         // consecutive d of one row: one 128-byte request
                         float *dst = dqacc + row0 * D + r;
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 32; ++i)
                             if (i < rows_left) red_add_f32(dst + (long long)i * D, __uint_as_float(v0[i]));
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 32; ++i)
                             if (32 + i < rows_left)
                                 red_add_f32(dst + (long long)(32 + i) * D, __uint_as_float(v1[i]));
@@ -775,7 +764,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                         // lane r = query row; columns = the 64 d of that row
                         if (r < rows_left) {
                             float *dst = dqacc + (row0 + r) * D;
-    #pragma unroll
+#pragma unroll
                             for (int c = 0; c < 8; ++c)
                                 asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(
                                                  dst + 4 * c),
@@ -784,7 +773,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                                              "f"(__uint_as_float(v0[4 * c + 2])),
                                              "f"(__uint_as_float(v0[4 * c + 3]))
                                              : "memory");
-    #pragma unroll
+#pragma unroll
                             for (int c = 0; c < 8; ++c)
                                 asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(
                                                  dst + 32 + 4 * c),
@@ -810,8 +799,8 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         const int j = quarter * 32 + lane;          // key row within the block
         const int g4 = lane >> 2, q4 = lane & 3;     // 16-lane access shapes
         const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-        uint32_t s_ph = 0, dp_ph = 0, st_ph = 0, acc_ph = 0;   // s_ph / dp_ph: bit per buffer
-        int stage = 0, cb = 0;
+        uint32_t s_ph = 0, dp_ph = 0, st_ph = 0, acc_ph = 0, dsb_ph = 0;   // s_ph, dsb_ph: bit per buffer
+        int stage = 0, cb = 0, db = 0;   // stage, S buffer, dS^T tile of the step
         bool ok = true;
         while (ok) {
             const int t = next_unit();
@@ -878,22 +867,31 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_P_FULL + cb));
-                if (!(ok = mbar_wait(bar(B_DP_FULL + cb), bit(dp_ph, cb), w))) break;
-                dp_ph ^= 1u << cb;
+                if (!(ok = mbar_wait(bar(B_DP_FULL), dp_ph, w))) break;
+                dp_ph ^= 1u;
                 tc_fence_after();
-                const uint32_t sds = sbase + C::OFF_DS + cb * C::DS_BYTES;
+                const uint32_t sds = sbase + C::OFF_DS + db * C::DS_BYTES;
                 __syncwarp();
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch) {
                     uint32_t dr[2][16];
-                    tmem_ld16x256(lane_addr + C::dp_col(cb, grp, ch), dr[0]);
-                    tmem_ld16x256(lane_addr + (16u << 16) + C::dp_col(cb, grp, ch), dr[1]);
+                    tmem_ld16x256(lane_addr + C::dp_col(grp, ch), dr[0]);
+                    tmem_ld16x256(lane_addr + (16u << 16) + C::dp_col(grp, ch), dr[1]);
                     const int c0 = grp * HALF + 32 * ch;
                     float2 dd[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         dd[k] = ld_shared_f32x2(dv + 4 * (c0 + 8 * k + 2 * q4));
                     tmem_wait_ld();
+                    if (C::kPipe && ch == NCH - 1) {
+                        // dP^T read: X is free for the next step's dP^T.  The dS^T
+                        // tile db may still be read by the dQ^T MMA of step j-2.
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(B_X_FREE));
+                        if (!(ok = mbar_wait(bar(B_DSB_FREE + db), bit(dsb_ph, db) ^ 1u, w))) break;
+                        dsb_ph ^= 1u << db;
+                    }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         uint32_t pk[8];
@@ -935,7 +933,8 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     mbar_arrive(bar(B_STAGE0 + S + stage));
                 }
                 if (++stage == S) { stage = 0; st_ph ^= 1; }
-                if (C::kPipe) cb ^= 1;
+                if (++cb == C::kSBuf) cb = 0;
+                if (C::kPipe) db ^= 1;
             }
             if (!ok) break;
             // ---------------------------------------------------- dK / dV out
