@@ -119,13 +119,14 @@ struct MainCfg {
     static constexpr int CHUNK_ROWS = 32;
     static constexpr int CHUNK_BYTES = CHUNK_ROWS * D * 4;
     static constexpr int STG_BYTES = kBulk ? 2 * CHUNK_BYTES : 0;
+    static_assert(!kBulk || CHUNK_BYTES == DS_BYTES, "a dQ chunk is parked in a dS^T tile");
     static constexpr int kDsBuf = kPipe ? 2 : 1;           // dS^T tiles in shared memory
     static constexpr int OFF_STG = OFF_DS + kDsBuf * DS_BYTES;
     static constexpr int OFF_LSE = OFF_STG + STG_BYTES;
     static constexpr int OFF_DV = OFF_LSE + kStages * BM * 4;
     static constexpr int OFF_BAR = OFF_DV + kStages * BM * 4;
     static constexpr int NUM_BARS = 48;
-    static_assert(38 + 2 * kStages <= NUM_BARS, "barrier slots");
+    static_assert(40 + 2 * kStages <= NUM_BARS, "barrier slots");
     // TMEM slot (+0), abort flag (+16), unit ring (+32), staging rows (+48)
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
@@ -158,7 +159,8 @@ enum {
     B_UNIT_EMPTY = 30,  // +k: every consumer warp has read it
     B_STG_FULL = 34,    // +b: the 4 reducer warps wrote dQ staging buffer b
     B_STG_FREE = 36,    // +b: the bulk reduce has read staging buffer b
-    B_STAGE0 = 38       // full[kStages], then empty[kStages]
+    B_TILE_FULL = 38,   // +d: the reducers wrote a dQ chunk into dS^T tile d
+    B_STAGE0 = 40       // full[kStages], then empty[kStages]
 };
 
 // Work units are handed out dynamically: the producer warp takes the next
@@ -274,7 +276,12 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         mbar_init(bar(B_DP_FULL), 1);
         mbar_init(bar(B_X_FREE), 8);
         mbar_init(bar(B_DQ_EMPTY), 4);
-        for (int d = 0; d < 2; ++d) mbar_init(bar(B_DSB_FREE + d), 1);
+        // dS^T tile d is free once the dQ^T MMA read it and -- bulk mode --
+        // once the dQ chunk the reducers parked in it has been read
+        for (int d = 0; d < 2; ++d) {
+            mbar_init(bar(B_DSB_FREE + d), C::kBulk && !p.deterministic ? 2 : 1);
+            mbar_init(bar(B_TILE_FULL + d), 4);
+        }
         mbar_init(bar(B_KDONE), 1);
         mbar_init(bar(B_ACC_FULL), 1);
         mbar_init(bar(B_ACC_EMPTY), 8);
@@ -592,25 +599,34 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             mbar_wait_warp(bar(B_DRAIN), 0, w);
         } else if (warp == C::W_ISSUE && C::kBulk) {
             // ------------------------------------------------ bulk-reduce issuer
-            // One thread adds every staged dQ chunk to the fp32 accumulator, in the
-            // order the reducer warps fill the two staging buffers.  The reducers
-            // put the chunk's first workspace row next to the buffer (-1 after the
-            // last chunk).  At most two chunks are in flight: after issuing chunk
-            // c the issuer waits until chunk c-1 has been read, then frees its buffer.
+            // One thread adds every dQ chunk to the fp32 accumulator.  Step j's
+            // first chunk (query rows 0-31) waits in dS^T tile j%2, whose dS^T
+            // the dQ^T MMA has consumed by then; its second chunk (rows 32-63)
+            // in staging buffer j%2.  The reducers put the step's first
+            // workspace row next to the buffers (-1 after the last step).  At
+            // most two chunks are in flight: after issuing one the issuer waits
+            // until the one before it has been read, then frees its buffer.
             if (lane == 0 && !p.deterministic) {
                 volatile long long *stg_row = reinterpret_cast<volatile long long *>(smem + C::OFF_MISC + 48);
-                uint32_t full_ph = 0;
-                for (int chunk = 0;; ++chunk) {
-                    const int sb = chunk & 1;
-                    if (!mbar_wait(bar(B_STG_FULL + sb), bit(full_ph, sb), w)) break;
-                    full_ph ^= 1u << sb;
-                    const long long row = stg_row[sb];
+                uint32_t tile_ph = 0, stg_ph = 0;   // bit d: parity of buffer d
+                for (int j = 0;; ++j) {
+                    const int d = j & 1;
+                    if (!mbar_wait(bar(B_TILE_FULL + d), bit(tile_ph, d), w)) break;
+                    tile_ph ^= 1u << d;
+                    const long long row = stg_row[d];
                     if (row < 0) break;
-                    bulk_reduce_add_f32(p.dqacc + row * D, sbase + C::OFF_STG + sb * C::CHUNK_BYTES,
+                    bulk_reduce_add_f32(p.dqacc + row * D, sbase + C::OFF_DS + d * C::DS_BYTES,
                                         C::CHUNK_BYTES);
                     bulk_commit_group();
-                    bulk_wait_read_all_but_one();
-                    if (chunk > 0) mbar_arrive(bar(B_STG_FREE + (sb ^ 1)));
+                    bulk_wait_read_all_but_one();   // second chunk of step j-1 read
+                    if (j > 0) mbar_arrive(bar(B_STG_FREE + (d ^ 1)));
+                    if (!mbar_wait(bar(B_STG_FULL + d), bit(stg_ph, d), w)) break;
+                    stg_ph ^= 1u << d;
+                    bulk_reduce_add_f32(p.dqacc + (row + 32) * D, sbase + C::OFF_STG + d * C::CHUNK_BYTES,
+                                        C::CHUNK_BYTES);
+                    bulk_commit_group();
+                    bulk_wait_read_all_but_one();   // first chunk of step j read
+                    mbar_arrive(bar(B_DSB_FREE + d));
                 }
                 bulk_wait_all();
             }
@@ -619,17 +635,17 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         // warpgroup 1: dQ reducers
         if (C::kBulk && !p.deterministic) {
             // -------------------------------------------- dQ reducers (bulk mode)
-            // Lane r = d of the dQ^T tile (64 query rows x 128 d, fp32) in TMEM X
-            // buffer cb.  A step is read out as two chunks of 32 rows and the X
+            // Lane r = d of the dQ^T tile (64 query rows x 128 d, fp32) in S
+            // buffer cb.  A step is read out as two chunks of 32 rows and the S
             // buffer released at once; each chunk is then written, column r of a
-            // [32 rows x 128 d] block, to the next free staging buffer, which the
-            // issuer warp adds to the accumulator.
+            // [32 rows x 128 d] block, to shared memory -- rows 0-31 into the
+            // step's dS^T tile, rows 32-63 into a staging buffer -- and the
+            // issuer warp adds it to the accumulator.
             const int quarter = warp & 3;
             const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
             const int r = quarter * 32 + lane;
             volatile long long *stg_row = reinterpret_cast<volatile long long *>(smem + C::OFF_MISC + 48);
             uint32_t dq_ph = 0, stg_free_ph = 0;   // bit b: parity of buffer b
-            int chunk = 0;                         // chunks written so far (staging buffer = chunk & 1)
             int cb = 0;                            // TMEM X buffer of the next step
             bool ok = true;
             // step iterator over the units of the ring: row of (head g, row block
@@ -671,42 +687,42 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 dq_ph ^= 1u << b;
                 return true;
             };
-            auto wait_stg = [&]() __attribute__((always_inline)) -> bool {
-                const int sb = chunk & 1;
+            auto wait_stg = [&](int sb) __attribute__((always_inline)) -> bool {
                 if (!mbar_wait_warp(bar(B_STG_FREE + sb), bit(stg_free_ph, sb) ^ 1u, w)) return false;
                 stg_free_ph ^= 1u << sb;
                 return true;
             };
-            auto write_chunk = [&](const uint32_t (&X)[32], long long row) __attribute__((always_inline)) {
-                const int sb = chunk & 1;
-                const uint32_t stg = sbase + C::OFF_STG + sb * C::CHUNK_BYTES + 4 * r;
+            // column r of a [32 rows x 128 d] fp32 block at buf; then tell the issuer
+            auto write_chunk = [&](const uint32_t (&X)[32], uint32_t buf, uint32_t full_bar) __attribute__((always_inline)) {
+                const uint32_t dst = buf + 4 * r;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) st_shared_b32(stg + 4 * D * i, X[i]);
+                for (int i = 0; i < 32; ++i) st_shared_b32(dst + 4 * D * i, X[i]);
                 fence_async_smem();
                 __syncwarp();
-                if (lane == 0) {
-                    if (warp == C::W_RED) stg_row[sb] = row;
-                    mbar_arrive(bar(B_STG_FULL + sb));
-                }
-                ++chunk;
+                if (lane == 0) mbar_arrive(full_bar);
             };
             uint32_t R0[32], R1[32];
             long long row0 = 0;
+            int db = 0;   // dS^T tile / staging buffer of the step
             while (ok && next_row(row0)) {
                 if (!(ok = wait_dq(cb))) break;
                 load_step(R0, R1, cb);
                 if (++cb == C::kSBuf) cb = 0;
-                if (!(ok = wait_stg())) break;
-                write_chunk(R0, row0);
-                if (!(ok = wait_stg())) break;
-                write_chunk(R1, row0 + 32);
+                // rows 0-31 into the dS^T tile the dQ^T MMA has just consumed (its
+                // previous chunk was read before the softmax wrote this step's dS^T)
+                if (lane == 0 && warp == C::W_RED) stg_row[db] = row0;
+                write_chunk(R0, sbase + C::OFF_DS + db * C::DS_BYTES, bar(B_TILE_FULL + db));
+                // rows 32-63 into staging buffer db
+                if (!(ok = wait_stg(db))) break;
+                write_chunk(R1, sbase + C::OFF_STG + db * C::CHUNK_BYTES, bar(B_STG_FULL + db));
+                db ^= 1;
             }
             // end marker for the issuer
-            if (ok && wait_stg()) {
+            if (ok) {
                 __syncwarp();
                 if (lane == 0) {
-                    if (warp == C::W_RED) stg_row[chunk & 1] = -1;
-                    mbar_arrive(bar(B_STG_FULL + (chunk & 1)));
+                    if (warp == C::W_RED) stg_row[db] = -1;
+                    mbar_arrive(bar(B_TILE_FULL + db));
                 }
             }
         } else {
