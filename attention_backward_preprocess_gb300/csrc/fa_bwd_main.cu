@@ -849,10 +849,13 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     tmem_ld16x256(lane_addr + C::s_col(cb, grp, ch), sr[0]);
                     tmem_ld16x256(lane_addr + (16u << 16) + C::s_col(cb, grp, ch), sr[1]);
                     const int c0 = grp * HALF + 32 * ch;     // first query of the chunk
-                    float2 l2[4];
+                    uint64_t nl2[4];   // (-LSE2, -LSE2) of the thread's query pairs
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        l2[k] = ld_shared_f32x2(lse2 + 4 * (c0 + 8 * k + 2 * q4));
+                    for (int k = 0; k < 4; ++k) {
+                        const float2 l = ld_shared_f32x2(lse2 + 4 * (c0 + 8 * k + 2 * q4));
+                        nl2[k] = f2_pack(-l.x, -l.y);
+                    }
+                    const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
                     tmem_wait_ld();
                     // causal: key kj is masked for query column c iff kj - (m0 + c0 + diag) > c
                     const int lim = kb - (m0 + c0 + diag) - 2 * q4;
@@ -864,8 +867,12 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
 #pragma unroll
                             for (int r = 0; r < 2; ++r) {
                                 const int kr = 16 * h + 8 * r;    // key offset from kb
-                                float pv0 = ex2(fmaf(__uint_as_float(sr[h][4 * k + 2 * r]), p.scale_log2, -l2[k].x));
-                                float pv1 = ex2(fmaf(__uint_as_float(sr[h][4 * k + 2 * r + 1]), p.scale_log2, -l2[k].y));
+                                const float2 x = f2_unpack(f2_fma(
+                                    f2_pack(__uint_as_float(sr[h][4 * k + 2 * r]),
+                                            __uint_as_float(sr[h][4 * k + 2 * r + 1])),
+                                    sc2, nl2[k]));
+                                float pv0 = ex2(x.x);
+                                float pv1 = ex2(x.y);
                                 if (masked) {
                                     if (lim + kr > 8 * k) pv0 = 0.f;
                                     if (lim + kr > 8 * k + 1) pv1 = 0.f;
@@ -894,10 +901,12 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     tmem_ld16x256(lane_addr + C::dp_col(grp, ch), dr[0]);
                     tmem_ld16x256(lane_addr + (16u << 16) + C::dp_col(grp, ch), dr[1]);
                     const int c0 = grp * HALF + 32 * ch;
-                    float2 dd[4];
+                    uint64_t dd[4];   // Dv of the thread's query pairs
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        dd[k] = ld_shared_f32x2(dv + 4 * (c0 + 8 * k + 2 * q4));
+                    for (int k = 0; k < 4; ++k) {
+                        const float2 v = ld_shared_f32x2(dv + 4 * (c0 + 8 * k + 2 * q4));
+                        dd[k] = f2_pack(v.x, v.y);
+                    }
                     tmem_wait_ld();
                     if (C::kPipe && ch == NCH - 1) {
                         // dP^T read: X is free for the next step's dP^T.  The dS^T
@@ -916,27 +925,27 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
 #pragma unroll
                             for (int r = 0; r < 2; ++r) {
                                 const int e0 = 32 * ch + 16 * h + 4 * k + 2 * r;
-                                const float d0 = P[e0] * (__uint_as_float(dr[h][4 * k + 2 * r]) - dd[k].x);
-                                const float d1 = P[e0 + 1] * (__uint_as_float(dr[h][4 * k + 2 * r + 1]) - dd[k].y);
-                                pk[2 * k + r] = Cvt<T>::pack(d0, d1);
+                                const float2 ds = f2_unpack(f2_mul(
+                                    f2_pack(P[e0], P[e0 + 1]),
+                                    f2_sub(f2_pack(__uint_as_float(dr[h][4 * k + 2 * r]),
+                                                   __uint_as_float(dr[h][4 * k + 2 * r + 1])),
+                                           dd[k])));
+                                pk[2 * k + r] = Cvt<T>::pack(ds.x, ds.y);
                             }
                         }
                         tmem_st16x128(lane_addr + ((uint32_t)(16 * h) << 16) + C::ds_col(cb, grp, ch), pk);
                         // dS^T rows into shared memory (128B-swizzled halves of 64
-                        // queries): key row jr, queries c0 + 8k + 2*q4, +1 as one
-                        // 4-byte word; the 8 rows x 4 words of one store hit 32
-                        // distinct banks.
+                        // queries): the registers of keys 8r.. and queries 8k.. form
+                        // an 8x8 tile in stmatrix's fragment layout.  Thread t
+                        // addresses row t%8 (key jr) of tile k = t/8, a 16-byte
+                        // chunk of the key's 128-byte row.
 #pragma unroll
                         for (int r = 0; r < 2; ++r) {
-                            const int jr = quarter * 32 + 16 * h + g4 + 8 * r;
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                const int i0 = c0 + 8 * k;
-                                const int half = i0 / 64, cidx = (i0 % 64) / 8;
-                                const uint32_t off = half * (BN * 128) + jr * 128 +
-                                                     ((cidx ^ g4) << 4) + 4 * q4;
-                                st_shared_b32(sds + off, pk[2 * k + r]);
-                            }
+                            const int jr = quarter * 32 + 16 * h + 8 * r + (lane & 7);
+                            const int i0 = c0 + 8 * (lane >> 3);
+                            const int half = i0 / 64, cidx = (i0 % 64) / 8;
+                            const uint32_t row = sds + half * (BN * 128) + jr * 128 + ((cidx ^ (lane & 7)) << 4);
+                            stmatrix_x4(row, pk[r], pk[2 + r], pk[4 + r], pk[6 + r]);
                         }
                     }
                 }
