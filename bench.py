@@ -5,7 +5,9 @@ over the workload the headline metric is quoted on: B=2, Hq=32, Hkv=8 (GQA),
 Sq=Sk=8192, D=128, bf16, causal (seeded synthetic inputs; O and LSE from the
 library's forward, outside the timed region).  The inputs of a step (Q, K, V,
 O, dO: about 470 MB) are larger than the 129 MB L2, so no flush is needed
-between steps.
+between steps.  --workload picks another of the five workloads (varlen
+included); one whose inputs are under 256 MB has a 256 MB buffer written
+between timed steps, outside the per-step events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -116,7 +118,7 @@ def cpu_baseline(w, inputs_cpu, prefix: int):
     k = inputs_cpu["k"][:1, :prefix, :1].double().numpy()
     v = inputs_cpu["v"][:1, :prefix, :1].double().numpy()
     do = inputs_cpu["dout"][:1, :prefix, :G].double().numpy()
-    sub = w.with_(B=1, Sq=prefix, Sk=prefix, Hq=G, Hkv=1)
+    sub = w.with_(B=1, Sq=prefix, Sk=prefix, Hq=G, Hkv=1, varlen=None)
     cores = oracle.max_threads()
     t0 = time.perf_counter()
     oracle.backward(q, k, v, do, w.softmax_scale, w.causal)
@@ -137,7 +139,7 @@ def run_reference(args, w):
     import torch
 
     from attention_backward_preprocess_gb300.workloads import generate
-    x = generate(w.with_(B=1, Sq=args.ref_prefix, Sk=args.ref_prefix), "cpu")
+    x = generate(w.with_(B=1, Sq=args.ref_prefix, Sk=args.ref_prefix, varlen=None), "cpu")
     times, vals = [], []
     for i in range(args.warmup + args.steps):
         tf, dt, cores, sample = cpu_baseline(w, x, args.ref_prefix)
@@ -159,10 +161,15 @@ def run_reference(args, w):
     return 0
 
 
-def config_of(w):
-    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk,
-            "D": w.D, "causal": w.causal, "deterministic": w.deterministic,
-            "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas"}
+def config_of(w, lengths=None, flushed=False):
+    c = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk,
+         "D": w.D, "causal": w.causal, "deterministic": w.deterministic,
+         "l2": ("L2 written over (256 MB) between timed steps" if flushed
+                else "inputs larger than L2 (no flush)"),
+         "parallelism": "replicas"}
+    if lengths is not None:
+        c["varlen_lengths"] = list(lengths)
+    return c
 
 
 def main():
@@ -197,31 +204,35 @@ def main():
     dev = torch.device("cuda", local if ws > 1 else 0)
     torch.cuda.set_device(dev)
     fa.lib()
-    if w.varlen is not None:
-        raise SystemExit("bench.py times dense workloads only")
 
     x = generate(w, dev)
     q, k, v, do = x["q"], x["k"], x["v"], x["dout"]
-    o, lse = fa.fa_fwd(q, k, v, causal=w.causal, softmax_scale=w.softmax_scale)
+    varlen = w.varlen is not None
+    # varlen: packed [total, H, D] tensors and cu_seqlens (main also launches the
+    # kernel that builds the work-unit list from them)
+    vl = dict(cu_seqlens_q=x["cu_q"], cu_seqlens_k=x["cu_k"], max_seqlen_q=x["max_len"],
+              max_seqlen_k=x["max_len"]) if varlen else {}
+    o, lse = fa.fa_fwd(q, k, v, causal=w.causal, softmax_scale=w.softmax_scale, **vl)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    nbytes = fa.workspace_bytes(w.B, w.Sq, w.Sk, w.Hq, w.Hkv, w.D,
-                                deterministic=w.deterministic)
+    Sq = x["max_len"] if varlen else w.Sq
+    nbytes = fa.workspace_bytes(w.B, Sq, Sq if varlen else w.Sk, w.Hq, w.Hkv, w.D,
+                                varlen=varlen, deterministic=w.deterministic)
     work = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    flops = bwd_flops(w)
+    flops = bwd_flops(w, x.get("lengths"))
     stream = torch.cuda.current_stream()
+    kw = dict(causal=w.causal, softmax_scale=w.softmax_scale, deterministic=w.deterministic,
+              dq=dq, dk=dk, dv=dv, **vl)
+    # a step reads Q, K, V, O, dO; below twice the 129 MB L2 the L2 is written
+    # over between timed steps (outside the per-step events)
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, o, do))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if in_bytes < (256 << 20) else None
 
     def step():
-        fa.fa_bwd_stages(q, k, v, o, do, lse, work, causal=w.causal,
-                         softmax_scale=w.softmax_scale, deterministic=w.deterministic,
-                         dq=dq, dk=dk, dv=dv, stages=("pre",))
+        fa.fa_bwd_stages(q, k, v, o, do, lse, work, stages=("pre",), **kw)
         e1.record(stream)
-        fa.fa_bwd_stages(q, k, v, o, do, lse, work, causal=w.causal,
-                         softmax_scale=w.softmax_scale, deterministic=w.deterministic,
-                         dq=dq, dk=dk, dv=dv, stages=("main",))
+        fa.fa_bwd_stages(q, k, v, o, do, lse, work, stages=("main",), **kw)
         e2.record(stream)
-        fa.fa_bwd_stages(q, k, v, o, do, lse, work, causal=w.causal,
-                         softmax_scale=w.softmax_scale, deterministic=w.deterministic,
-                         dq=dq, dk=dk, dv=dv, stages=("post",))
+        fa.fa_bwd_stages(q, k, v, o, do, lse, work, stages=("post",), **kw)
 
     e1 = torch.cuda.Event(enable_timing=True)
     e2 = torch.cuda.Event(enable_timing=True)
@@ -248,6 +259,8 @@ def main():
     for i in range(args.steps):
         a, b_, c, d = ev[i]
         e1, e2 = b_, c
+        if flush is not None:
+            flush.fill_(i & 255)
         a.record(stream)
         step()
         d.record(stream)
@@ -255,6 +268,8 @@ def main():
     barrier()
     clk = clocks.stop()
     total_ms = start.elapsed_time(end)
+    if flush is not None:   # steps only, without the L2 overwrite between them
+        total_ms = sum(ev[i][0].elapsed_time(ev[i][3]) for i in range(args.steps))
     pre_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
     main_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
     post_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(args.steps)]
@@ -271,6 +286,9 @@ def main():
     if not args.no_e2e:
         host = {n: t.cpu().pin_memory() for n, t in (("q", q), ("k", k), ("v", v), ("o", o),
                                                    ("dout", do), ("lse", lse))}
+        if varlen:
+            host["cu_q"] = x["cu_q"].cpu().pin_memory()
+            host["cu_k"] = x["cu_k"].cpu().pin_memory()
         dev_in = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
         outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (q, k, v)]
         h2d = sum(t.numel() * t.element_size() for t in host.values())
@@ -280,10 +298,12 @@ def main():
         def e2e_step():
             for n in host:
                 dev_in[n].copy_(host[n], non_blocking=True)
+            evl = dict(cu_seqlens_q=dev_in["cu_q"], cu_seqlens_k=dev_in["cu_k"],
+                       max_seqlen_q=x["max_len"], max_seqlen_k=x["max_len"]) if varlen else {}
             gq, gk, gv = fa.fa_bwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["o"],
                                    dev_in["dout"], dev_in["lse"], causal=w.causal,
                                    softmax_scale=w.softmax_scale, deterministic=w.deterministic,
-                                   dq=dq, dk=dk, dv=dv)
+                                   dq=dq, dk=dk, dv=dv, **evl)
             for hbuf, g in zip(outs_h, (gq, gk, gv)):
                 hbuf.copy_(g, non_blocking=True)
 
@@ -314,8 +334,9 @@ def main():
     pk = peaks()
     main_avg = statistics.mean(main_ms)
     achieved = flops / (main_avg * 1e-3) / 1e12
-    elems_q = w.B * w.Sq * w.Hq * w.D
-    rows = w.B * w.Hq * w.Sq
+    tokens_q = q.shape[0] if varlen else w.B * w.Sq
+    elems_q = tokens_q * w.Hq * w.D
+    rows = tokens_q * w.Hq
     pre_bytes = 2 * elems_q * 2 + rows * 4 * 2 + rows * 4 + elems_q * 4    # O, dO in; LSE in; Dv, LSE2 out; dQaccum zero
     post_bytes = elems_q * 4 + elems_q * 2
     traffic = None
@@ -329,7 +350,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "fp16",
         "data": "synthetic (seeded N(0,1), torch.Generator on device)",
-        "config": config_of(w),
+        "config": config_of(w, x.get("lengths"), flush is not None),
         "pct_of_bf16_peak": 100.0 * value / ws / pk["bf16"],
         "roofline": {"kernel": "bwd_main_kernel", "bound": "tensor", "achieved": achieved,
                      "peak": pk["bf16"], "unit": "TFLOP/s", "frac": achieved / pk["bf16"],
@@ -342,13 +363,14 @@ def main():
         "kernels_gbs": {"preprocess": pre_bytes / (statistics.mean(pre_ms) * 1e-3) / 1e9,
                         "postprocess": post_bytes / (statistics.mean(post_ms) * 1e-3) / 1e9,
                         "hbm_peak": pk["hbm"]},
-        "gpu_launches": 3 * args.steps,    # preprocess, main, postprocess (dense: no scheduler launch)
+        # preprocess, main, postprocess (+ the varlen work-unit scheduler)
+        "gpu_launches": (4 if varlen else 3) * args.steps,
         "device_status": status,
         "e2e": e2e,
         "clocks": clk,
     }
     if not args.no_cpu_baseline:
-        xs = generate(w.with_(B=1, Sq=args.cpu_prefix, Sk=args.cpu_prefix), "cpu")
+        xs = generate(w.with_(B=1, Sq=args.cpu_prefix, Sk=args.cpu_prefix, varlen=None), "cpu")
         tf, dt, cores, sample = cpu_baseline(w, xs, args.cpu_prefix)
         line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "seconds": dt, "sample": sample}
