@@ -237,8 +237,12 @@ fa_status prepare(const void *q, const void *k, const void *v, const void *o, co
     // Unit order of the dense main kernel: the smallest group of (batch, kv
     // head) pairs -- a divisor of B * Hkv, so that no short group comes last --
     // whose units number at least 1.5 times the grid.
+    // Deterministic mode adds each row block's contributions in n-block
+    // order, so the units of one (sequence, kv head) wait on one another;
+    // there, all pairs are interleaved (plain n-block-major order), so that
+    // few units of any one chain run at the same time.
     p.unit_group = B * Hkv;
-    if (!cu_q) {
+    if (!cu_q && !deterministic) {
         const int nblk = (Sk + fa::kBlockN - 1) / fa::kBlockN;
         const long long grid = std::min<long long>(L.max_tiles, sm_count());
         for (int g = 1; g <= B * Hkv; ++g)

@@ -127,9 +127,10 @@ struct MainCfg {
     static constexpr int OFF_BAR = OFF_DV + kStages * BM * 4;
     static constexpr int NUM_BARS = 48;
     static_assert(40 + 2 * kStages <= NUM_BARS, "barrier slots");
-    // TMEM slot (+0), abort flag (+16), unit ring (+32), staging rows (+48)
+    // TMEM slot (+0), abort flag (+16), unit ring (+32), chunk rows (+48),
+    // chunk n blocks (+64)
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-    static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+    static constexpr int SMEM_BYTES = OFF_MISC + 80 + 1024;  // + alignment slack
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
     static constexpr int kRing = 4;             // work-unit hand-off ring depth
     // ring consumers: MMA warp(s) + 4 reducers + 8 softmax warps
@@ -279,7 +280,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         // dS^T tile d is free once the dQ^T MMA read it and -- bulk mode --
         // once the dQ chunk the reducers parked in it has been read
         for (int d = 0; d < 2; ++d) {
-            mbar_init(bar(B_DSB_FREE + d), C::kBulk && !p.deterministic ? 2 : 1);
+            mbar_init(bar(B_DSB_FREE + d), C::kBulk ? 2 : 1);
             mbar_init(bar(B_TILE_FULL + d), 4);
         }
         mbar_init(bar(B_KDONE), 1);
@@ -603,18 +604,36 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             // first chunk (query rows 0-31) waits in dS^T tile j%2, whose dS^T
             // the dQ^T MMA has consumed by then; its second chunk (rows 32-63)
             // in staging buffer j%2.  The reducers put the step's first
-            // workspace row next to the buffers (-1 after the last step).  At
-            // most two chunks are in flight: after issuing one the issuer waits
-            // until the one before it has been read, then frees its buffer.
-            if (lane == 0 && !p.deterministic) {
+            // workspace row and its n block next to the buffers (row -1 after
+            // the last step).  At most two chunks are in flight: after issuing
+            // one the issuer waits until the one before it has been read, then
+            // frees its buffer.
+            // Deterministic mode: the contributions to a 64-row block of the
+            // accumulator are added in n-block order -- before a step's chunks
+            // the issuer waits until the row block's semaphore counts every
+            // earlier n block, and it counts its own step once both chunks
+            // have completed (checked one step later, so that the issuer rarely
+            // waits for a reduce to finish in L2).
+            if (lane == 0) {
                 volatile long long *stg_row = reinterpret_cast<volatile long long *>(smem + C::OFF_MISC + 48);
+                volatile int *stg_nb = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 64);
+                const bool det = p.deterministic;
                 uint32_t tile_ph = 0, stg_ph = 0;   // bit d: parity of buffer d
+                constexpr int kRelLag = 1;
+                int *pend[kRelLag] = {};            // semaphores of the last kRelLag steps (det)
+                bool done = false;
                 for (int j = 0;; ++j) {
                     const int d = j & 1;
                     if (!mbar_wait(bar(B_TILE_FULL + d), bit(tile_ph, d), w)) break;
                     tile_ph ^= 1u << d;
                     const long long row = stg_row[d];
-                    if (row < 0) break;
+                    if (row < 0) { done = true; break; }
+                    int *sem = nullptr;
+                    if (det) {
+                        sem = p.sem + row / 64;
+                        if (!sem_wait_geq(sem, stg_nb[d], w)) break;
+                        fence_async_global();
+                    }
                     bulk_reduce_add_f32(p.dqacc + row * D, sbase + C::OFF_DS + d * C::DS_BYTES,
                                         C::CHUNK_BYTES);
                     bulk_commit_group();
@@ -625,15 +644,30 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     bulk_reduce_add_f32(p.dqacc + (row + 32) * D, sbase + C::OFF_STG + d * C::CHUNK_BYTES,
                                         C::CHUNK_BYTES);
                     bulk_commit_group();
+                    int *&slot = pend[j % kRelLag];
+                    if (slot) {                      // step j-kRelLag's adds complete: count them
+                        bulk_wait_all_but<2 * kRelLag>();
+                        fence_async_global();
+                        __threadfence();
+                        red_release_add_gpu(slot, 1);
+                    }
+                    slot = sem;
                     bulk_wait_read_all_but_one();   // first chunk of step j read
                     mbar_arrive(bar(B_DSB_FREE + d));
                 }
                 bulk_wait_all();
+                if (done && det) {
+                    fence_async_global();
+                    __threadfence();
+#pragma unroll
+                    for (int i = 0; i < kRelLag; ++i)
+                        if (pend[i]) red_release_add_gpu(pend[i], 1);
+                }
             }
         }
     } else if (warp < C::W_SM) {
         // warpgroup 1: dQ reducers
-        if (C::kBulk && !p.deterministic) {
+        if (C::kBulk) {
             // -------------------------------------------- dQ reducers (bulk mode)
             // Lane r = d of the dQ^T tile (64 query rows x 128 d, fp32) in S
             // buffer cb.  A step is read out as two chunks of 32 rows and the S
@@ -652,7 +686,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             // m) = head0 + g * hstride + m * BM, heads innermost, row blocks
             // from the last one down (the MMA warps' order)
             long long head0 = 0, hstride = 0;
-            int g_it = 0, m_it = -1, m_first = 0;
+            int g_it = 0, m_it = -1, m_first = 0, n_cur = 0;
             bool units_done = false;
             auto next_row = [&](long long &row0) __attribute__((always_inline)) -> bool {
                 while (m_it < m_first) {
@@ -661,6 +695,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     if (t < 0) { units_done = true; return false; }
                     const Unit u = decode_unit<BM>(p, t);
                     if (u.nm == 0) continue;
+                    n_cur = u.n_block;
                     head0 = ws_row(p, u.b, u.hk * p.G, 0);
                     hstride = ws_row(p, u.b, u.hk * p.G + 1, 0) - head0;
                     m_first = u.m_begin;
@@ -710,7 +745,10 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 if (++cb == C::kSBuf) cb = 0;
                 // rows 0-31 into the dS^T tile the dQ^T MMA has just consumed (its
                 // previous chunk was read before the softmax wrote this step's dS^T)
-                if (lane == 0 && warp == C::W_RED) stg_row[db] = row0;
+                if (lane == 0 && warp == C::W_RED) {
+                    stg_row[db] = row0;
+                    reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 64)[db] = n_cur;
+                }
                 write_chunk(R0, sbase + C::OFF_DS + db * C::DS_BYTES, bar(B_TILE_FULL + db));
                 // rows 32-63 into staging buffer db
                 if (!(ok = wait_stg(db))) break;

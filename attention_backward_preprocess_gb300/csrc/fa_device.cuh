@@ -221,6 +221,15 @@ __device__ __forceinline__ void bulk_wait_read_all_but_one() {
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Same, but allow the N most recent committed groups to be still in progress.
+template <int N>
+__device__ __forceinline__ void bulk_wait_all_but() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+// Orders this thread's async-proxy (TMA) global accesses with its generic ones.
+__device__ __forceinline__ void fence_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 // Generic-proxy shared-memory writes -> visible to the async proxy (tcgen05.mma, TMA).
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
