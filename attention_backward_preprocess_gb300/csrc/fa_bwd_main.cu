@@ -50,20 +50,17 @@ struct MainCfg {
     // dQ GEMM orientation: the MMA's M (=128) is d when D = 128 (dQ^T = K^T dS^T,
     // TMEM lanes = d) and the query row when D = 64 (dQ = dS K, lanes = query).
     static constexpr bool kDqT = (kD == 128);
-    // Software pipeline (D = 128).  TMEM (512 columns):
-    //   dK 128 | dV 128 | S buffer x3 | X 64
-    // An S buffer (64 columns) carries one step through its life: S^T, then
-    // P^T and dS^T as bf16 pairs in its two halves, then -- once dV and dK
-    // have read those -- that step's dQ^T, until the reducers take it out.
-    // X holds dP^T, which the softmax warps read as soon as it is complete.
-    // With three S buffers, S^T of step j waits only for the dQ^T of step
-    // j-3 to be drained, and dP^T of step j only for the softmax to have read
-    // dP^T of step j-1.
-    // D = 64 (BM = 128) has no room for second buffers and runs the steps one
-    // after the other: dK 64 | dV 64 | S^T 128 | dP^T 128 | dQ 64.
-    static constexpr bool kPipe = (kD == 128);
-    static constexpr int kSBuf = kPipe ? 3 : 1;
-    static constexpr int kStages = kPipe ? 3 : 4;
+    // Software pipeline.  TMEM (512 columns):
+    //   D = 128 (BM = 64):  dK 128 | dV 128 | S buffer x3 (64 each) | X 64
+    //   D = 64 (BM = 128):  dK 64 | dV 64 | S buffer x2 (128 each) | X 128
+    // An S buffer carries one step through its life: S^T, then P^T and dS^T
+    // as bf16 pairs, then -- once dV and dK have read those -- that step's dQ
+    // (dQ^T for D = 128), until the reducers take it out.  X holds dP^T,
+    // which the softmax warps read as soon as it is complete.  S^T of step j
+    // thus waits only for the dQ of step j - kSBuf to be drained, and dP^T of
+    // step j only for the softmax warps to have read dP^T of step j-1.
+    static constexpr int kSBuf = (kD == 128) ? 3 : 2;
+    static constexpr int kStages = 3;
     // Warp roles: 0 producer | 1 MMA issuer (D = 64) or MMA warp A (S, dP) |
     // 2 MMA warp B (dV, dK, dQ; D = 128) | 3 bulk-reduce issuer (D = 128) |
     // 4-7 dQ reducers | 8-15 softmax (two groups of four, one per TMEM lane
@@ -73,25 +70,25 @@ struct MainCfg {
     static constexpr int TM_DK = 0;
     static constexpr int TM_DV = D;
     static constexpr int TM_S = 2 * D;
-    static constexpr int TM_X = TM_S + kSBuf * BM;         // kPipe: dP^T
-    static constexpr int TM_DP = TM_S + BM;                // !kPipe
-    static constexpr int TM_DQ = TM_S + 2 * BM;            // !kPipe
+    static constexpr int TM_X = TM_S + kSBuf * BM;         // dP^T
     static constexpr int TM_COLS = 512;
-    static_assert(kPipe ? (TM_X + BM <= TM_COLS) : (TM_DQ + 64 <= TM_COLS), "TMEM overflow");
-    // columns (S buffer b, softmax group g, 32-query chunk ch)
+    static_assert(TM_X + BM <= TM_COLS, "TMEM overflow");
+    // Columns (S buffer b, softmax group g, 32-query chunk ch).  In the HALF
+    // columns of group g, the bf16 pairs of P^T fill the first HALF/2 and
+    // those of dS^T the second: chunk ch's P^T lands on S^T columns this group
+    // has already read, and dS^T is written after all of them were read.
     static __device__ __forceinline__ int s_col(int b, int g, int ch) {
-        return kPipe ? TM_S + b * BM + g * HALF : TM_S + g * HALF + 32 * ch;
+        return TM_S + b * BM + g * HALF + 32 * ch;
     }
     static __device__ __forceinline__ int p_col(int b, int g, int ch) {   // P^T bf16 pairs
-        return kPipe ? TM_S + b * BM + g * HALF : TM_S + g * HALF + 16 * ch;
+        return TM_S + b * BM + g * HALF + 16 * ch;
     }
-    static __device__ __forceinline__ int dp_col(int g, int ch) {
-        return kPipe ? TM_X + g * HALF : TM_DP + g * HALF + 32 * ch;
-    }
+    static __device__ __forceinline__ int dp_col(int g, int ch) { return TM_X + g * HALF + 32 * ch; }
     static __device__ __forceinline__ int ds_col(int b, int g, int ch) {  // dS^T bf16 pairs
-        return kPipe ? TM_S + b * BM + g * HALF + 16 : TM_DP + g * HALF + 16 * ch;
+        return TM_S + b * BM + g * HALF + 16 * NCH + 16 * ch;
     }
-    static __device__ __forceinline__ int dq_col(int b) { return kPipe ? TM_S + b * BM : TM_DQ; }
+    // dQ^T (D = 128: 64 query columns) or dQ (D = 64: 64 d columns)
+    static __device__ __forceinline__ int dq_col(int b) { return TM_S + b * BM; }
     // A-operand column of MMA K step kk (queries 16kk .. 16kk+15) of P^T / dS^T
     static __device__ __forceinline__ int p_op(int b, int kk) {
         const int g = (16 * kk) / HALF;
@@ -120,7 +117,7 @@ struct MainCfg {
     static constexpr int CHUNK_BYTES = CHUNK_ROWS * D * 4;
     static constexpr int STG_BYTES = kBulk ? 2 * CHUNK_BYTES : 0;
     static_assert(!kBulk || CHUNK_BYTES == DS_BYTES, "a dQ chunk is parked in a dS^T tile");
-    static constexpr int kDsBuf = kPipe ? 2 : 1;           // dS^T tiles in shared memory
+    static constexpr int kDsBuf = 2;                       // dS^T tiles in shared memory
     static constexpr int OFF_STG = OFF_DS + kDsBuf * DS_BYTES;
     static constexpr int OFF_LSE = OFF_STG + STG_BYTES;
     static constexpr int OFF_DV = OFF_LSE + kStages * BM * 4;
@@ -134,7 +131,7 @@ struct MainCfg {
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
     static constexpr int kRing = 4;             // work-unit hand-off ring depth
     // ring consumers: MMA warp(s) + 4 reducers + 8 softmax warps
-    static constexpr int kConsumerWarps = kPipe ? 14 : 13;
+    static constexpr int kConsumerWarps = 14;
     static constexpr uint32_t IDESC_S = make_idesc(128, BM, Cvt<T>::is_bf16, false, false);
     static constexpr uint32_t IDESC_KV = make_idesc(128, D, Cvt<T>::is_bf16, false, true);
     static constexpr uint32_t IDESC_DQ = make_idesc(128, 64, Cvt<T>::is_bf16, true, true);
@@ -152,7 +149,6 @@ enum {
     B_S_FREE = 14,      // +b (D = 128): the reducers took dQ^T out of S buffer b
     B_DP_FULL = 17,     // dP^T complete
     B_X_FREE = 18,      // (D = 128) the softmax warps read dP^T
-    B_DQ_EMPTY = 19,    // (D = 64) the reducers took dQ out of TMEM
     B_DSB_FREE = 20,    // +d (D = 128): dQ^T MMA done reading dS^T tile d
     B_KDONE = 22,       // (D = 128) dV and dK of the step complete
     B_ACC_FULL = 23, B_ACC_EMPTY = 24, B_DRAIN = 25,
@@ -266,7 +262,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         mbar_init(bar(B_KV_FULL), 1);
-        mbar_init(bar(B_KV_EMPTY), C::kPipe ? 2 : 1);   // one commit per MMA warp
+        mbar_init(bar(B_KV_EMPTY), 2);   // one commit per MMA warp
         for (int b = 0; b < 3; ++b) {
             mbar_init(bar(B_S_FULL + b), 1);
             mbar_init(bar(B_P_FULL + b), 8);
@@ -276,7 +272,6 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         }
         mbar_init(bar(B_DP_FULL), 1);
         mbar_init(bar(B_X_FREE), 8);
-        mbar_init(bar(B_DQ_EMPTY), 4);
         // dS^T tile d is free once the dQ^T MMA read it and -- bulk mode --
         // once the dQ chunk the reducers parked in it has been read
         for (int d = 0; d < 2; ++d) {
@@ -286,7 +281,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         mbar_init(bar(B_KDONE), 1);
         mbar_init(bar(B_ACC_FULL), 1);
         mbar_init(bar(B_ACC_EMPTY), 8);
-        mbar_init(bar(B_DRAIN), C::kPipe ? 2 : 1);
+        mbar_init(bar(B_DRAIN), 2);
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(B_STG_FULL + b), 4);
             mbar_init(bar(B_STG_FREE + b), 1);
@@ -298,7 +293,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         for (int s = 0; s < S; ++s) {
             mbar_init(bar(B_STAGE0 + s), 1);          // full: producer expect_tx
             // empty: a commit per MMA warp + 8 softmax warps
-            mbar_init(bar(B_STAGE0 + S + s), (C::kPipe ? 2 : 1) + 8);
+            mbar_init(bar(B_STAGE0 + S + s), 2 + 8);
         }
         fence_mbar_init();
     }
@@ -395,92 +390,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     }
                 }
             }
-        } else if (warp == 1 && !C::kPipe) {
-            // ---------------------------------------------------------- MMA issuer
-            // D = 64: one warp issues every MMA of a step in order (S, dP, dV,
-            // dK, dQ) with one buffer of each kind; elect.sync picks the lane
-            // that issues each MMA / commit.
-            uint32_t kv_ph = 0, acc_ph = 0, p_ph = 0, ds_ph = 0, dqe_ph = 0, s_ph = 0;
-            int stage = 0;
-            bool ok = true;
-            const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
-            const uint64_t dK_k = sw128_desc(sK, 16, 1024), dV_k = sw128_desc(sV, 16, 1024);
-            const uint64_t dK_mn = sw128_desc(sK, BN * 128, 1024);
-            while (ok) {
-                const int t = next_unit();
-                if (t < 0) break;
-                const Unit u = decode_unit<BM>(p, t);
-                if (u.iters == 0) continue;
-                if (!(ok = mbar_wait_warp(bar(B_KV_FULL), kv_ph, w))) break;
-                kv_ph ^= 1;
-                tc_fence_after();
-                for (int it = 0; it < u.iters; ++it) {
-                    if (!(ok = mbar_wait_warp(bar(B_STAGE0 + stage), s_ph, w))) break;
-                    tc_fence_after();
-                    const uint32_t sQ = sbase + C::OFF_Q + stage * C::QO_BYTES;
-                    const uint32_t sDO = sbase + C::OFF_DO + stage * C::QO_BYTES;
-                    // S^T = K Q^T
-                    const uint64_t dQ_k = sw128_desc(sQ, 16, 1024), dDO_k = sw128_desc(sDO, 16, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
-                        const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
-                        mma_ss_warp(tmem + C::s_col(0, 0, 0), desc_add(dK_k, ko), desc_add(dQ_k, qo),
-                                    C::IDESC_S, kk > 0);
-                    }
-                    mma_commit_warp(bar(B_S_FULL));
-                    // dP^T = V dO^T
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
-                        const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
-                        mma_ss_warp(tmem + C::TM_DP, desc_add(dV_k, ko), desc_add(dDO_k, qo),
-                                    C::IDESC_S, kk > 0);
-                    }
-                    mma_commit_warp(bar(B_DP_FULL));
-                    if (it == 0) {
-                        if (!(ok = mbar_wait_warp(bar(B_ACC_EMPTY), acc_ph ^ 1, w))) break;
-                        acc_ph ^= 1;
-                    }
-                    if (!(ok = mbar_wait_warp(bar(B_P_FULL), p_ph, w))) break;
-                    p_ph ^= 1;
-                    tc_fence_after();
-                    // dV += P^T dO  (P^T bf16 in TMEM; dO MN-major: K step = 16 rows = 2048 B)
-                    const uint64_t dDO_mn = sw128_desc(sDO, BM * 128, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < BM / 16; ++kk)
-                        mma_ts_warp(tmem + C::TM_DV, tmem + C::p_op(0, kk), desc_add(dDO_mn, kk * 2048),
-                                    C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
-                    if (!(ok = mbar_wait_warp(bar(B_DS_FULL), ds_ph, w))) break;
-                    ds_ph ^= 1;
-                    tc_fence_after();
-                    // dK += dS^T Q
-                    const uint64_t dQ_mn = sw128_desc(sQ, BM * 128, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < BM / 16; ++kk)
-                        mma_ts_warp(tmem + C::TM_DK, tmem + C::ds_op(0, kk), desc_add(dQ_mn, kk * 2048),
-                                    C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit_warp(bar(B_STAGE0 + S + stage));   // Q / dO of this stage consumed
-                    if (!(ok = mbar_wait_warp(bar(B_DQ_EMPTY), dqe_ph ^ 1u, w))) break;
-                    dqe_ph ^= 1;
-                    tc_fence_after();
-                    // dQ = dS K; both operands MN-major
-                    const uint64_t dDS_mn = sw128_desc(sbase + C::OFF_DS, BN * 128, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)
-                        mma_ss_warp(tmem + C::dq_col(0), desc_add(dDS_mn, kk * 2048),
-                                    desc_add(dK_mn, kk * 2048), C::IDESC_DQ, kk > 0);
-                    mma_commit_warp(bar(B_DQ_FULL));
-                    if (++stage == S) { stage = 0; s_ph ^= 1; }
-                }
-                if (!ok) break;
-                mma_commit_warp(bar(B_ACC_FULL));
-                mma_commit_warp(bar(B_KV_EMPTY));
-            }
-            // make sure no MMA is still running before tensor memory is freed
-            mma_commit_warp(bar(B_DRAIN));
-            mbar_wait_warp(bar(B_DRAIN), 0, w);
-        } else if (warp == 1 && C::kPipe) {
+        } else if (warp == 1) {
             // ------------------------------------------- MMA warp A: S and dP
             // Issues S^T_j = K Q_j^T into S buffer j%3 and dP^T_j = V dO_j^T into
             // X for every step j, ahead of warp B.  Before S_j it waits until the
@@ -533,7 +443,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             }
             mma_commit_warp(bar(B_DRAIN));
             mbar_wait_warp(bar(B_DRAIN), 0, w);
-        } else if (warp == C::W_MMA_B && C::kPipe) {
+        } else if (warp == C::W_MMA_B) {
             // ---------------------------------------- MMA warp B: dV, dK and dQ
             // For step j (S buffer j%3, dS^T tile j%2): dV += P^T dO once P^T is
             // written back, dK += dS^T Q once dS^T is; then, after dV and dK have
@@ -580,12 +490,16 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     if (!(ok = mbar_wait_warp(bar(B_KDONE), kd_ph, w))) break;
                     kd_ph ^= 1u;
                     tc_fence_after();
+                    // D = 128: dQ^T = K^T dS^T (M = d); D = 64: dQ = dS K (M = query);
+                    // both operands MN-major, K step = 16 keys = 2048 B
                     const uint64_t dDS_mn =
                         sw128_desc(sbase + C::OFF_DS + db * C::DS_BYTES, BN * 128, 1024);
+                    const uint64_t dq_a = C::kDqT ? dK_mn : dDS_mn;
+                    const uint64_t dq_b = C::kDqT ? dDS_mn : dK_mn;
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
-                        mma_ss_warp(tmem + C::dq_col(cb), desc_add(dK_mn, kk * 2048),
-                                    desc_add(dDS_mn, kk * 2048), C::IDESC_DQ, kk > 0);
+                        mma_ss_warp(tmem + C::dq_col(cb), desc_add(dq_a, kk * 2048),
+                                    desc_add(dq_b, kk * 2048), C::IDESC_DQ, kk > 0);
                     mma_commit_warp(bar(B_DQ_FULL + cb));
                     mma_commit_warp(bar(B_DSB_FREE + db));   // dS^T tile db read
                     if (++c_stage == S) c_stage = 0;
@@ -789,7 +703,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     tmem_wait_ld();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(C::kPipe ? B_S_FREE + cb : B_DQ_EMPTY));
+                    if (lane == 0) mbar_arrive(bar(B_S_FREE + cb));
                     if (++cb == C::kSBuf) cb = 0;
                     const long long row0 = ws_row(p, u.b, h, m * BM);
                     int *sem = p.sem + row0 / 64;
@@ -946,7 +860,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                         dd[k] = f2_pack(v.x, v.y);
                     }
                     tmem_wait_ld();
-                    if (C::kPipe && ch == NCH - 1) {
+                    if (ch == NCH - 1) {
                         // dP^T read: X is free for the next step's dP^T.  The dS^T
                         // tile db may still be read by the dQ^T MMA of step j-2.
                         tc_fence_before();
@@ -997,7 +911,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 }
                 if (++stage == S) { stage = 0; st_ph ^= 1; }
                 if (++cb == C::kSBuf) cb = 0;
-                if (C::kPipe) db ^= 1;
+                db ^= 1;
             }
             if (!ok) break;
             // ---------------------------------------------------- dK / dV out
