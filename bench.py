@@ -14,7 +14,8 @@ between timed steps, outside the per-step events.
 value  : TFLOPS over all ranks, FLOP = 10*B*Hq*Sq*Sk*D / 2 (causal), device
          time from CUDA events with inputs resident in HBM
 e2e    : the same metric through fa_bwd with host (pinned) buffers: each step
-         copies its inputs in and its outputs (dQ, dK, dV) out
+         copies its inputs in and its outputs (dQ, dK, dV) out; copies and
+         compute of consecutive steps overlap on separate streams
 roofline: the main kernel (a dense contraction, tensor-bound) against the
          measured dense bf16 peak
 cpu_baseline: the fp64 CPU oracle, as it stands, on a bounded sample (a causal
@@ -289,32 +290,55 @@ def main():
         if varlen:
             host["cu_q"] = x["cu_q"].cpu().pin_memory()
             host["cu_k"] = x["cu_k"].cpu().pin_memory()
-        dev_in = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+        # Steps overlap as in a training loop that prefetches: the inputs of step
+        # i are copied in (own stream) while step i-1 computes, and the results
+        # of step i-1 are read back (own stream) while step i computes.  Two
+        # sets of device buffers alternate; every step still copies all of its
+        # inputs in and all of its results out.
+        dev_in = [{n: torch.empty_like(t, device=dev) for n, t in host.items()} for _ in range(2)]
+        dev_out = [[torch.empty_like(t) for t in (q, k, v)] for _ in range(2)]
         outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (q, k, v)]
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = sum(t.numel() * t.element_size() for t in outs_h)
         e2e_steps = max(3, min(args.steps, 10))
+        h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of set b copied in
+        ev_used = [torch.cuda.Event() for _ in range(2)]   # the step on set b computed
+        ev_out = [torch.cuda.Event() for _ in range(2)]    # results of set b read back
 
-        def e2e_step():
-            for n in host:
-                dev_in[n].copy_(host[n], non_blocking=True)
-            evl = dict(cu_seqlens_q=dev_in["cu_q"], cu_seqlens_k=dev_in["cu_k"],
+        def e2e_step(i):
+            b = i % 2
+            with torch.cuda.stream(h2d_s):
+                h2d_s.wait_event(ev_used[b])
+                for n in host:
+                    dev_in[b][n].copy_(host[n], non_blocking=True)
+                ev_in[b].record(h2d_s)
+            stream.wait_event(ev_in[b])
+            stream.wait_event(ev_out[b])
+            di = dev_in[b]
+            evl = dict(cu_seqlens_q=di["cu_q"], cu_seqlens_k=di["cu_k"],
                        max_seqlen_q=x["max_len"], max_seqlen_k=x["max_len"]) if varlen else {}
-            gq, gk, gv = fa.fa_bwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["o"],
-                                   dev_in["dout"], dev_in["lse"], causal=w.causal,
-                                   softmax_scale=w.softmax_scale, deterministic=w.deterministic,
-                                   dq=dq, dk=dk, dv=dv, **evl)
-            for hbuf, g in zip(outs_h, (gq, gk, gv)):
-                hbuf.copy_(g, non_blocking=True)
+            gq, gk, gv = fa.fa_bwd(di["q"], di["k"], di["v"], di["o"], di["dout"], di["lse"],
+                                   causal=w.causal, softmax_scale=w.softmax_scale,
+                                   deterministic=w.deterministic, dq=dev_out[b][0],
+                                   dk=dev_out[b][1], dv=dev_out[b][2], **evl)
+            ev_used[b].record(stream)
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(ev_used[b])
+                for hbuf, g in zip(outs_h, (gq, gk, gv)):
+                    hbuf.copy_(g, non_blocking=True)
+                ev_out[b].record(d2h_s)
 
-        for _ in range(2):
-            e2e_step()
+        for i in range(2):
+            e2e_step(i)
         barrier()
         s2 = torch.cuda.Event(enable_timing=True)
         t2 = torch.cuda.Event(enable_timing=True)
         s2.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
+        h2d_s.wait_stream(stream)
+        for i in range(e2e_steps):
+            e2e_step(i)
+        stream.wait_stream(d2h_s)
         t2.record(stream)
         barrier()
         e2e_ms = s2.elapsed_time(t2) / e2e_steps
