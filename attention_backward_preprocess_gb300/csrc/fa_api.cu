@@ -1,5 +1,6 @@
 // fa_api.cu -- the C ABI declared in include/fa.h: argument validation,
 // workspace planning, TMA tensor-map encoding and the kernel launches.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -17,7 +18,11 @@ namespace fa {
 cudaError_t launch_schedule(const BwdParams &p, cudaStream_t stream);
 cudaError_t launch_preprocess(const BwdParams &p, int bf16, cudaStream_t stream);
 cudaError_t launch_postprocess(const BwdParams &p, int bf16, cudaStream_t stream);
-cudaError_t launch_fwd(const BwdParams &p, void *o, float *lse, int bf16, cudaStream_t stream);
+cudaError_t launch_fwd_tc(const BwdParams &p, const CUtensorMap &q, const CUtensorMap &k,
+                          const CUtensorMap &v, void *o, float *lse, int max_lq, int bf16,
+                          cudaStream_t stream);
+int fwd_block_m();
+int *fwd_error_word();
 cudaError_t launch_bwd_main(const BwdParams &p, const CUtensorMap &q, const CUtensorMap &k,
                             const CUtensorMap &v, const CUtensorMap &dout, int bf16, int grid,
                             cudaStream_t stream);
@@ -427,10 +432,19 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
 
 fa_status fa_device_status(void *workspace, cudaStream_t stream) {
     void *ws = workspace ? workspace : library_workspace_peek();
-    if (!ws) {
-        return cudaStreamSynchronize(stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    fa_status st = FA_OK;
+    if (!workspace) {
+        // the forward pass records its timeouts in a word of its own
+        int *fwd_err = fa::fwd_error_word();
+        if (!fwd_err) return FA_ERR_CUDA;
+        st = read_error_word(fwd_err, stream, true);
+        if (st == FA_ERR_CUDA) return st;
     }
-    return read_error_word(reinterpret_cast<int *>(ws), stream, true);
+    if (!ws) {
+        return cudaStreamSynchronize(stream) == cudaSuccess ? st : FA_ERR_CUDA;
+    }
+    fa_status st2 = read_error_word(reinterpret_cast<int *>(ws), stream, true);
+    return st2 != FA_OK ? st2 : st;
 }
 
 fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Sq,
@@ -455,7 +469,25 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
     p.varlen = cu_seqlens_q != nullptr;
     p.cu_q = cu_seqlens_q;
     p.cu_k = cu_seqlens_k;
-    return cuda_status(fa::launch_fwd(p, o, lse, dtype == FA_BF16, stream));
+    p.err = fa::fwd_error_word();
+    if (!p.err) return FA_ERR_CUDA;
+    p.budget_ns = g_budget_ns.load();
+    long long rq = Sq, rk = Sk;
+    if (p.varlen) {
+        st = varlen_totals(cu_seqlens_q, cu_seqlens_k, B, stream, &rq, &rk);
+        if (st != FA_OK) return st;
+        if (rq == 0) return FA_OK;
+    }
+    // a map needs at least one row; with no keys at all no K/V tile is loaded
+    rk = std::max<long long>(rk, 1);
+    const int bf16 = dtype == FA_BF16;
+    const int nb = p.varlen ? 1 : B;
+    CUtensorMap mq, mk, mv;
+    if (!encode_rows_map(&mq, q, D, Hq, rq, nb, fa::fwd_block_m(), bf16) ||
+        !encode_rows_map(&mk, k, D, Hkv, rk, nb, fa::kBlockN, bf16) ||
+        !encode_rows_map(&mv, v, D, Hkv, rk, nb, fa::kBlockN, bf16))
+        return FA_ERR_CUDA;
+    return cuda_status(fa::launch_fwd_tc(p, mq, mk, mv, o, lse, Sq, bf16, stream));
 }
 
 }  // extern "C"

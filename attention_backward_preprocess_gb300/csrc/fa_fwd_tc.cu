@@ -1,0 +1,373 @@
+// fa_fwd_tc.cu -- forward pass O = softmax(Q K^T * c + mask) V and the
+// per-row log-sum-exp LSE, on the 5th-generation tensor cores.  It supplies
+// the O and LSE the backward pass consumes (same layouts, same bottom-right
+// causal mask, -inf LSE / zero O for a query row that sees no key).
+//
+// One CTA per (128-query tile, sequence, query head); the tiles of the longest
+// causal rows are launched first.  Per block of 128 keys:
+//   S = Q K^T           tcgen05 SS, M = 128 queries, N = 128 keys, fp32 in TMEM
+//   P = exp2(S c log2e - m), row sums, P written back to TMEM as bf16/fp16 pairs
+//   O += P V            tcgen05 TS (P from TMEM), N = D
+// S is double buffered, so S of block n+1 runs while the softmax warps turn
+// block n into P, and O += P V of block n-1 runs meanwhile too.  The running
+// row maximum m is raised only when a block's maximum exceeds it by more than
+// 2^8 (then O and the row sum are rescaled); otherwise P is taken against the
+// older, smaller m, which keeps P <= 2^8 and the result exact up to rounding.
+// The epilogue divides O by the row sum and writes O and LSE = (m + log2 l) ln 2.
+//
+// Warps: 0 TMA producer (Q once, K/V blocks through a stage ring), 1 MMA
+// issuer, 4-7 softmax (thread = query row of its TMEM lane quarter), 2-3 idle.
+#include "fa_device.cuh"
+#include "fa_params.h"
+
+namespace fa {
+namespace {
+
+template <int kD, typename T>
+struct FwdCfg {
+    static constexpr int D = kD;
+    static constexpr int BM = 128;                 // queries per CTA
+    static constexpr int BN = 128;                 // keys per block
+    static constexpr int kStages = (kD == 128) ? 3 : 4;
+    static constexpr int kThreads = 8 * 32;
+    static constexpr int W_SM = 4;                 // first softmax warp
+    // TMEM: S buffer x2 (BN columns each; P overwrites the first BN/2) | O (D)
+    static constexpr int TM_S = 0;
+    static constexpr int TM_O = 2 * BN;
+    static constexpr int TM_COLS = 512;
+    static_assert(TM_O + D <= TM_COLS, "TMEM overflow");
+    // shared memory
+    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int KV_BYTES = BN * D * 2;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + Q_BYTES;
+    static constexpr int OFF_V = OFF_K + kStages * KV_BYTES;
+    static constexpr int OFF_BAR = OFF_V + kStages * KV_BYTES;
+    static constexpr int NUM_BARS = 16;
+    static constexpr int kv_empty(int st) { return 8 + kStages + st; }
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // TMEM slot, abort flag
+    static constexpr int SMEM_BYTES = OFF_MISC + 32 + 1024;   // + alignment slack
+    static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
+    static_assert(8 + 2 * kStages <= NUM_BARS, "barrier slots");
+    // one CTA per SM: the CTA takes all 512 TMEM columns
+    static_assert(2 * (SMEM_BYTES + 1024) > 233472, "two CTAs would share an SM");
+    static constexpr uint32_t IDESC_S = make_idesc(128, BN, Cvt<T>::is_bf16, false, false);
+    static constexpr uint32_t IDESC_PV = make_idesc(128, D, Cvt<T>::is_bf16, false, true);
+};
+
+enum {
+    F_Q_FULL = 0,
+    F_S_FULL = 1,     // +b: S of the block in S buffer b complete
+    F_P_FULL = 3,     // +b: P written back (and O rescaled) by the 4 softmax warps
+    F_PV_DONE = 5,    // +b: O += P V of the block in S buffer b complete
+    F_O_FINAL = 7,
+    F_KV_FULL = 8,    // +stage; the KV_EMPTY barriers follow them (kv_empty)
+};
+
+// Lazy rescaling threshold (log2 units): P is taken against a running maximum
+// that may lag the true one by up to this much.
+constexpr float kRescaleLog2 = 8.f;
+
+template <int kD, typename T>
+__global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap map_q,
+                  const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                  void *o_out, float *lse_out, int nmb) {
+    using C = FwdCfg<kD, T>;
+    constexpr int D = C::D, BM = C::BM, BN = C::BN, S = C::kStages;
+    // ---- tile of this CTA: longest causal rows first
+    const int bh = blockIdx.x % (p.B * p.Hq);
+    const int m = nmb - 1 - blockIdx.x / (p.B * p.Hq);
+    const int b = bh / p.Hq, h = bh - b * p.Hq, hk = h / p.G;
+    const int q0 = p.varlen ? p.cu_q[b] : 0, k0 = p.varlen ? p.cu_k[b] : 0;
+    const int lq = p.varlen ? p.cu_q[b + 1] - q0 : p.Sq;
+    const int lk = p.varlen ? p.cu_k[b + 1] - k0 : p.Sk;
+    if (m * BM >= lq) return;                       // uniform: the whole CTA leaves
+    const int diag = lk - lq;                       // key j visible to query i iff j <= i + diag
+    int last_key = lk - 1;
+    if (p.causal) last_key = min(last_key, m * BM + BM - 1 + diag);
+    const int n_end = last_key < 0 ? 0 : last_key / BN + 1;   // key blocks [0, n_end)
+    const int bidx = p.varlen ? 0 : b;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + C::OFF_BAR;
+    auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 16);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        mbar_init(bar(F_Q_FULL), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(F_S_FULL + i), 1);
+            mbar_init(bar(F_P_FULL + i), 4);
+            mbar_init(bar(F_PV_DONE + i), 1);
+        }
+        mbar_init(bar(F_O_FINAL), 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar(F_KV_FULL + s), 1);
+            mbar_init(bar(C::kv_empty(s)), 1);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&map_q);
+        prefetch_tmap(&map_k);
+        prefetch_tmap(&map_v);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtl w{abort_flag, p.err, p.budget_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && n_end > 0) {
+            mbar_arrive_expect_tx(bar(F_Q_FULL), C::Q_BYTES);
+#pragma unroll
+            for (int hh = 0; hh < D / 64; ++hh)
+                tma_load_4d(sbase + C::OFF_Q + hh * BM * 128, &map_q, bar(F_Q_FULL), hh * 64, h,
+                            q0 + m * BM, bidx);
+            uint32_t empty_ph = 0;
+            for (int n = 0; n < n_end; ++n) {
+                const int st = n % S;
+                if (n >= S) {
+                    if (!mbar_wait(bar(C::kv_empty(st)), empty_ph >> st & 1u, w)) break;
+                    empty_ph ^= 1u << st;
+                }
+                const uint32_t full = bar(F_KV_FULL + st);
+                mbar_arrive_expect_tx(full, 2 * C::KV_BYTES);
+#pragma unroll
+                for (int hh = 0; hh < D / 64; ++hh) {
+                    tma_load_4d(sbase + C::OFF_K + st * C::KV_BYTES + hh * BN * 128, &map_k, full,
+                                hh * 64, hk, k0 + n * BN, bidx);
+                    tma_load_4d(sbase + C::OFF_V + st * C::KV_BYTES + hh * BN * 128, &map_v, full,
+                                hh * 64, hk, k0 + n * BN, bidx);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ----------------------------------------------------------- MMA issuer
+        // S of block n is issued before O += P V of block n-1, so it runs while
+        // the softmax warps work on block n-1.
+        if (n_end > 0) {
+            bool ok = mbar_wait_warp(bar(F_Q_FULL), 0, w);
+            uint32_t full_ph = 0;
+            const uint64_t dQ_k = sw128_desc(sbase + C::OFF_Q, 16, 1024);
+            auto issue_pv = [&](int n) -> bool {
+                const int bb = n & 1, st = n % S;
+                if (!mbar_wait_warp(bar(F_P_FULL + bb), (uint32_t)(n >> 1) & 1u, w)) return false;
+                tc_fence_after();
+                // O += P V: P (queries x keys) from TMEM, V (keys x d) MN-major,
+                // K step = 16 keys = 2048 bytes of the swizzled tile
+                const uint64_t dV_mn = sw128_desc(sbase + C::OFF_V + st * C::KV_BYTES, BN * 128, 1024);
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts_warp(tmem + C::TM_O, tmem + C::TM_S + bb * BN + 8 * kk,
+                                desc_add(dV_mn, kk * 2048), C::IDESC_PV, (n > 0 || kk > 0) ? 1u : 0u);
+                mma_commit_warp(bar(F_PV_DONE + bb));
+                mma_commit_warp(bar(C::kv_empty(st)));
+                return true;
+            };
+            for (int n = 0; ok && n < n_end; ++n) {
+                const int bb = n & 1, st = n % S;
+                if (!(ok = mbar_wait_warp(bar(F_KV_FULL + st), full_ph >> st & 1u, w))) break;
+                full_ph ^= 1u << st;
+                // S buffer bb last held P of block n-2
+                if (n >= 2 && !(ok = mbar_wait_warp(bar(F_PV_DONE + bb), (uint32_t)((n - 2) >> 1) & 1u, w)))
+                    break;
+                tc_fence_after();
+                const uint64_t dK_k = sw128_desc(sbase + C::OFF_K + st * C::KV_BYTES, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
+                    const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
+                    mma_ss_warp(tmem + C::TM_S + bb * BN, desc_add(dQ_k, qo), desc_add(dK_k, ko),
+                                C::IDESC_S, kk > 0);
+                }
+                mma_commit_warp(bar(F_S_FULL + bb));
+                if (n >= 1 && !(ok = issue_pv(n - 1))) break;
+            }
+            if (ok && issue_pv(n_end - 1)) mma_commit_warp(bar(F_O_FINAL));
+            // make sure no MMA is still running before tensor memory is freed
+            mma_commit_warp(bar(F_Q_FULL));
+            mbar_wait_warp(bar(F_Q_FULL), 1, w);
+        }
+    } else if (warp >= C::W_SM) {
+        // ------------------------------------------------------------- softmax
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;          // query row of the tile
+        const int qi = m * BM + r;                  // query index within the sequence
+        const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+        // keys [0, kmax] are visible to this row (kmax < 0: none)
+        const int kmax = p.causal ? min(lk - 1, qi + diag) : lk - 1;
+        float m_run = -INFINITY, l_run = 0.f;       // running max (log2 units), row sum
+        bool ok = true;
+        for (int n = 0; n < n_end; ++n) {
+            const int bb = n & 1;
+            if (!(ok = mbar_wait_warp(bar(F_S_FULL + bb), (uint32_t)(n >> 1) & 1u, w))) break;
+            tc_fence_after();
+            const uint32_t scol = lane_addr + C::TM_S + bb * BN;
+            const int kb = n * BN;
+            // pass 1: row maximum of the block
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t sr[32];
+                tmem_ld32(scol + 32 * c, sr);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float s2 = __uint_as_float(sr[i]) * p.scale_log2;
+                    mx = (kb + 32 * c + i <= kmax) ? fmaxf(mx, s2) : mx;
+                }
+            }
+            const float m_new = fmaxf(m_run, mx);
+            const float m_use = (m_run == -INFINITY || m_new > m_run + kRescaleLog2) ? m_new : m_run;
+            const float alpha = (m_use == m_run) ? 1.f : ex2(m_run - m_use);
+            const float mref = (m_use == -INFINITY) ? 0.f : m_use;
+            // pass 2: P = exp2(s2 - m) into the first BN/2 columns as pairs;
+            // column j/2 of the buffer holds keys j, j+1 (every S column is
+            // read before a P pair lands on it)
+            float sum = 0.f;
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t sr[32];
+                tmem_ld32(scol + 32 * c, sr);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int j = kb + 32 * c + 2 * i;
+                    const float p0 = (j <= kmax) ? ex2(fmaf(__uint_as_float(sr[2 * i]), p.scale_log2, -mref)) : 0.f;
+                    const float p1 = (j + 1 <= kmax) ? ex2(fmaf(__uint_as_float(sr[2 * i + 1]), p.scale_log2, -mref)) : 0.f;
+                    sum += p0 + p1;
+                    pk[i] = Cvt<T>::pack(p0, p1);
+                }
+                tmem_st16(scol + 16 * c, pk);
+            }
+            l_run = l_run * alpha + sum;
+            m_run = m_use;
+            // O holds blocks < n: rescale it when a row's maximum moved
+            if (n > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                if (!(ok = mbar_wait_warp(bar(F_PV_DONE + ((n - 1) & 1)), (uint32_t)((n - 1) >> 1) & 1u, w)))
+                    break;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t orr[32];
+                    tmem_ld32(lane_addr + C::TM_O + 32 * c, orr);
+                    tmem_wait_ld();
+                    uint32_t lo[16], hi[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        lo[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+                        hi[i] = __float_as_uint(__uint_as_float(orr[16 + i]) * alpha);
+                    }
+                    tmem_st16(lane_addr + C::TM_O + 32 * c, lo);
+                    tmem_st16(lane_addr + C::TM_O + 32 * c + 16, hi);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(F_P_FULL + bb));
+        }
+        // ---------------------------------------------------------- epilogue
+        // O = acc / l, LSE = (m + log2 l) ln 2; a row that sees no key gets
+        // O = 0 and LSE = -inf
+        if (ok && n_end > 0) {
+            ok = mbar_wait_warp(bar(F_O_FINAL), 0, w);
+            tc_fence_after();
+        }
+        if (ok) {
+            const bool live = qi < lq;
+            const long long row = p.varlen ? (long long)q0 + qi : (long long)b * p.Sq + qi;
+            if (live) {
+                float *lse_dst = p.varlen ? lse_out + (long long)h * p.cu_q[p.B] + q0 + qi
+                                          : lse_out + ((long long)b * p.Hq + h) * p.Sq + qi;
+                *lse_dst = l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+            }
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            T *dst = reinterpret_cast<T *>(o_out) + (row * p.Hq + h) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t orr[32];
+                if (n_end > 0) {
+                    tmem_ld32(lane_addr + C::TM_O + 32 * c, orr);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) orr[i] = 0u;
+                }
+                if (live) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        pk[i] = Cvt<T>::pack(__uint_as_float(orr[2 * i]) * inv,
+                                             __uint_as_float(orr[2 * i + 1]) * inv);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        reinterpret_cast<uint4 *>(dst + 32 * c)[i] =
+                            make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
+}
+
+template <int kD, typename T>
+cudaError_t launch_fwd_tc_t(const BwdParams &p, const CUtensorMap &mq, const CUtensorMap &mk,
+                            const CUtensorMap &mv, void *o, float *lse, int max_lq,
+                            cudaStream_t stream) {
+    using C = FwdCfg<kD, T>;
+    auto kern = fwd_tc_kernel<kD, T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int nmb = (max_lq + C::BM - 1) / C::BM;
+    const long long grid = (long long)nmb * p.B * p.Hq;
+    if (grid <= 0) return cudaSuccess;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    kern<<<(unsigned)grid, C::kThreads, C::SMEM_BYTES, stream>>>(p, mq, mk, mv, o, lse, nmb);
+    return cudaGetLastError();
+}
+
+// Error word of the forward pass (its bounded waits record timeouts here).
+__device__ int g_fwd_err;
+
+}  // namespace
+
+int *fwd_error_word() {
+    void *ptr = nullptr;
+    return cudaGetSymbolAddress(&ptr, g_fwd_err) == cudaSuccess ? static_cast<int *>(ptr) : nullptr;
+}
+
+// Query rows of one TMA box for Q in the forward pass.
+int fwd_block_m() { return FwdCfg<128, __nv_bfloat16>::BM; }
+
+cudaError_t launch_fwd_tc(const BwdParams &p, const CUtensorMap &q, const CUtensorMap &k,
+                          const CUtensorMap &v, void *o, float *lse, int max_lq, int bf16,
+                          cudaStream_t stream) {
+    if (p.D == 128)
+        return bf16 ? launch_fwd_tc_t<128, __nv_bfloat16>(p, q, k, v, o, lse, max_lq, stream)
+                    : launch_fwd_tc_t<128, __half>(p, q, k, v, o, lse, max_lq, stream);
+    return bf16 ? launch_fwd_tc_t<64, __nv_bfloat16>(p, q, k, v, o, lse, max_lq, stream)
+                : launch_fwd_tc_t<64, __half>(p, q, k, v, o, lse, max_lq, stream);
+}
+
+}  // namespace fa

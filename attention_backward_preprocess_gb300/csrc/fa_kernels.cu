@@ -2,7 +2,6 @@
 //   schedule_kernel     builds the list of work units (sequence, K/V block, kv head)
 //   preprocess_kernel   Dv = rowsum(dO o O), LSE2 = LSE * log2(e), zero dQaccum
 //   postprocess_kernel  dQ = cast(dQaccum * scale)
-//   fwd_kernel          untimed forward (O, LSE) on CUDA cores, inputs for tests
 #include "fa_device.cuh"
 #include "fa_params.h"
 
@@ -10,7 +9,6 @@ namespace fa {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ __forceinline__ int seq_len_q(const BwdParams &p, int b) {
     return p.varlen ? p.cu_q[b + 1] - p.cu_q[b] : p.Sq;
@@ -155,100 +153,6 @@ __global__ void __launch_bounds__(256) postprocess_kernel(BwdParams p) {
     *reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dq) + (trow * p.Hq + h) * D + part * 8) = o;
 }
 
-// ------------------------------------------------------------------- forward
-// Untimed reference-style forward: one warp per query row, 8 rows per block,
-// K/V tiles of 64 keys staged in shared memory as fp32; online softmax in the
-// log2 domain; O = sum_j p_j v_j / l, LSE = (m + log2 l) ln 2.
-template <int D, typename T>
-__global__ void __launch_bounds__(256) fwd_kernel(BwdParams p, void *o_out, float *lse_out) {
-    constexpr int KT = 64, ROWS = 8, DPL = D / 32;
-    extern __shared__ float fsm[];
-    float *Ks = fsm;                   // [KT][D + 1]
-    float *Vs = Ks + KT * (D + 1);     // [KT][D]
-    float *Qs = Vs + KT * D;           // [ROWS][D]
-    const int b = blockIdx.z, h = blockIdx.y, hk = h / p.G;
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int lq = seq_len_q(p, b), lk = seq_len_k(p, b);
-    const int row0 = blockIdx.x * ROWS;
-    if (row0 >= lq) return;
-    const int i = row0 + warp;
-    const bool row_ok = i < lq;
-    const int diag = lk - lq;
-    const long long qbase = p.varlen ? (long long)p.cu_q[b] : (long long)b * p.Sq;
-    const long long kbase = p.varlen ? (long long)p.cu_k[b] : (long long)b * p.Sk;
-    const T *q = reinterpret_cast<const T *>(p.q);
-    const T *k = reinterpret_cast<const T *>(p.k);
-    const T *v = reinterpret_cast<const T *>(p.v);
-    for (int idx = threadIdx.x; idx < ROWS * D; idx += blockDim.x) {
-        const int r = idx / D, d = idx % D;
-        float val = 0.f;
-        if (row0 + r < lq) val = (float)q[((qbase + row0 + r) * p.Hq + h) * D + d];
-        Qs[idx] = val;
-    }
-    int kend = lk;
-    if (p.causal) kend = min(lk, max(0, min(lq - 1, row0 + ROWS - 1) + diag + 1));
-    float m = -INFINITY, l = 0.f, acc[DPL];
-#pragma unroll
-    for (int t = 0; t < DPL; ++t) acc[t] = 0.f;
-    for (int k0 = 0; k0 < kend; k0 += KT) {
-        __syncthreads();
-        for (int idx = threadIdx.x; idx < KT * D; idx += blockDim.x) {
-            const int r = idx / D, d = idx % D;
-            float kv = 0.f, vv = 0.f;
-            if (k0 + r < lk) {
-                const long long off = ((kbase + k0 + r) * p.Hkv + hk) * D + d;
-                kv = (float)k[off];
-                vv = (float)v[off];
-            }
-            Ks[r * (D + 1) + d] = kv;
-            Vs[r * D + d] = vv;
-        }
-        __syncthreads();
-        if (!row_ok) continue;
-        float sv[2];
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            const int jj = lane + 32 * t, j = k0 + jj;
-            float s = 0.f;
-            const float *kr = Ks + jj * (D + 1);
-            const float *qr = Qs + warp * D;
-#pragma unroll 8
-            for (int d = 0; d < D; ++d) s = fmaf(qr[d], kr[d], s);
-            const bool vis = j < lk && (!p.causal || j <= i + diag);
-            sv[t] = vis ? s * p.scale_log2 : -INFINITY;
-        }
-        float mt = fmaxf(sv[0], sv[1]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
-        const float mn = fmaxf(m, mt);
-        if (mn == -INFINITY) continue;   // nothing visible yet
-        const float corr = exp2f(m - mn);
-        const float p0 = exp2f(sv[0] - mn), p1 = exp2f(sv[1] - mn);
-        float ps = p0 + p1;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-        l = l * corr + ps;
-#pragma unroll
-        for (int t = 0; t < DPL; ++t) acc[t] *= corr;
-        for (int jj = 0; jj < KT; ++jj) {
-            const float pj = __shfl_sync(0xffffffffu, jj < 32 ? p0 : p1, jj & 31);
-#pragma unroll
-            for (int t = 0; t < DPL; ++t) acc[t] = fmaf(pj, Vs[jj * D + lane + 32 * t], acc[t]);
-        }
-        m = mn;
-    }
-    if (!row_ok) return;
-    T *o = reinterpret_cast<T *>(o_out);
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll
-    for (int t = 0; t < DPL; ++t) o[((qbase + i) * p.Hq + h) * D + lane + 32 * t] = (T)(acc[t] * inv);
-    if (lane == 0) {
-        const long long li = p.varlen ? (long long)h * p.cu_q[p.B] + p.cu_q[b] + i
-                                      : ((long long)b * p.Hq + h) * p.Sq + i;
-        lse_out[li] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
-    }
-}
-
 }  // namespace
 
 cudaError_t launch_schedule(const BwdParams &p, cudaStream_t stream) {
@@ -283,25 +187,6 @@ cudaError_t launch_postprocess(const BwdParams &p, int bf16, cudaStream_t stream
         else postprocess_kernel<64, __half><<<grid, 256, 0, stream>>>(p);
     }
     return cudaGetLastError();
-}
-
-template <int D, typename T>
-static cudaError_t launch_fwd_t(const BwdParams &p, void *o, float *lse, cudaStream_t stream) {
-    const int smem = (64 * (D + 1) + 64 * D + 8 * D) * 4;
-    auto kern = fwd_kernel<D, T>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    dim3 grid((p.Sq + 7) / 8, p.Hq, p.B);
-    kern<<<grid, 256, smem, stream>>>(p, o, lse);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_fwd(const BwdParams &p, void *o, float *lse, int bf16, cudaStream_t stream) {
-    if (p.D == 128)
-        return bf16 ? launch_fwd_t<128, __nv_bfloat16>(p, o, lse, stream)
-                    : launch_fwd_t<128, __half>(p, o, lse, stream);
-    return bf16 ? launch_fwd_t<64, __nv_bfloat16>(p, o, lse, stream)
-                : launch_fwd_t<64, __half>(p, o, lse, stream);
 }
 
 }  // namespace fa

@@ -124,9 +124,13 @@ fa_status fa_bwd_workspace_layout(int B, int Sq, int Sk, int Hq, int Hkv, int D,
                                   int deterministic, size_t *dvec_off, size_t *lse2_off,
                                   size_t *dqacc_off, size_t *rows);
 
-/* Forward pass, untimed helper that supplies O and LSE (natural log, -inf
- * for a query row that sees no key; such rows get O = 0).  Plain CUDA-core
- * kernel with fp32 accumulation; same layouts and masking as fa_bwd. */
+/* Forward pass O = softmax(Q K^T * scale + mask) V with LSE (natural log,
+ * -inf for a query row that sees no key; such rows get O = 0): the inputs
+ * fa_bwd consumes, same layouts and masking.  One tcgen05 kernel per call
+ * (S = Q K^T and O += P V on the tensor cores, fp32 accumulation, online
+ * softmax in the log2 domain).  Varlen calls read cu_seqlens_q[B] /
+ * cu_seqlens_k[B] back to the host (one stream synchronisation).  Timeouts
+ * of its bounded waits are reported by fa_device_status(NULL, ...). */
 fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Sq,
                  int Sk, int Hq, int Hkv, int D, float softmax_scale, int causal,
                  const int *cu_seqlens_q, const int *cu_seqlens_k, fa_dtype dtype,

@@ -107,20 +107,50 @@ def test_caller_workspace_matches_library_workspace(fa, oracle_mod, cuda_device)
         assert torch.equal(t, u)
 
 
-@pytest.mark.parametrize("w", [WORKLOADS["b1_h1_s128_d64"],
-                               W("fwd_gqa_causal", 2, 200, 200, 4, 2, 128, causal=True),
-                               W("fwd_sq_gt_sk", 1, 200, 70, 2, 2, 64, "fp16", True)],
-                         ids=lambda w: w.name)
-def test_forward_matches_oracle(fa, oracle_mod, cuda_device, w):
-    x = small_case(oracle_mod, w)
-    o, lse = fa.fa_fwd(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), causal=w.causal,
-                       softmax_scale=w.softmax_scale)
-    torch.cuda.synchronize()
+def _check_forward(o, lse, x):
     check_bar(o, to64(x["o"]), "o")
     l_gpu, l_ref = to64(lse), to64(x["lse"])
     assert np.array_equal(np.isneginf(l_gpu), np.isneginf(l_ref))
     fin = np.isfinite(l_ref)
     assert np.max(np.abs(l_gpu[fin] - l_ref[fin])) < 1e-4
+
+
+FWD_CASES = [
+    WORKLOADS["b1_h1_s128_d64"],
+    W("fwd_gqa_causal", 2, 200, 200, 4, 2, 128, causal=True),
+    W("fwd_sq_gt_sk", 1, 200, 70, 2, 2, 64, "fp16", True),
+    # several key blocks with a ragged last one, no mask
+    W("fwd_d128_sk520", 1, 300, 520, 2, 1, 128),
+    # several query tiles and key blocks under the causal mask
+    W("fwd_d64_causal_s600", 1, 600, 600, 2, 2, 64, causal=True),
+    # wide score range: the running maximum moves by more than 2^8 between
+    # key blocks, so O and the row sum are rescaled
+    W("fwd_rescale", 1, 384, 384, 2, 2, 128, scale=0.37, qk_dist=("normal", 2.0)),
+    W("fwd_rescale_causal_fp16", 1, 384, 384, 2, 1, 64, "fp16", True, scale=0.5,
+      qk_dist=("normal", 2.0)),
+    W("fwd_s1", 1, 1, 1, 1, 1, 128),
+]
+
+
+@pytest.mark.parametrize("w", FWD_CASES, ids=lambda w: w.name)
+def test_forward_matches_oracle(fa, oracle_mod, cuda_device, w):
+    x = small_case(oracle_mod, w)
+    o, lse = fa.fa_fwd(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), causal=w.causal,
+                       softmax_scale=w.softmax_scale)
+    torch.cuda.synchronize()
+    _check_forward(o, lse, x)
+    assert fa.device_status() == 0
+
+
+@pytest.mark.parametrize("w,lengths", VARLEN, ids=lambda v: v.name if hasattr(v, "name") else "")
+def test_varlen_forward_matches_oracle(fa, oracle_mod, cuda_device, w, lengths):
+    x = small_case(oracle_mod, w, lengths=lengths)
+    cu_q, cu_k = x["cu_q"].cuda(), x["cu_k"].cuda()
+    o, lse = fa.fa_fwd(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), causal=w.causal,
+                       softmax_scale=w.softmax_scale, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k,
+                       max_seqlen_q=x["max_len"], max_seqlen_k=x["max_len"])
+    torch.cuda.synchronize()
+    _check_forward(o, lse, x)
 
 
 @pytest.mark.parametrize("w", [W("pre_d128", 2, 200, 200, 2, 2, 128, causal=True),
