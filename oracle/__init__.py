@@ -14,6 +14,12 @@ public layouts:
 * varlen: ``cu_q`` / ``cu_k`` int32 prefix sums of the ``nseq`` lengths;
   q ``[total_q, Hq, D]``; k ``[total_k, Hkv, D]``; lse ``[Hq, total_q]``
 
+Every function also takes the optional extensions as keywords:
+``window=(left, right)`` (a local band around the bottom-right diagonal, -1 =
+unbounded on that side), ``alibi`` (slopes ``[Hq]`` or ``[B, Hq]``) and
+``seqused_q`` / ``seqused_k`` (used lengths per sequence; rows past them are
+neither read nor written, and come back as zeros).
+
 Parity status: every function here is pinned by ``tests/test_oracle.py``
 (central finite differences, invariants, a hand-derived 2x2 example, closed
 forms for degenerate inputs).
@@ -67,6 +73,38 @@ def _ptr(a, ctype=ctypes.c_double):
     return a.ctypes.data_as(ctypes.POINTER(ctype))
 
 
+class _Ext(ctypes.Structure):
+    _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
+                ("alibi", ctypes.POINTER(ctypes.c_double)), ("alibi_bstride", ctypes.c_int),
+                ("seqused_q", ctypes.POINTER(ctypes.c_int)),
+                ("seqused_k", ctypes.POINTER(ctypes.c_int))]
+
+
+def _ext(B, Hq, window=None, alibi=None, seqused_q=None, seqused_k=None):
+    """(ctypes pointer or None, arrays to keep alive) for the extension options."""
+    if window is None and alibi is None and seqused_q is None and seqused_k is None:
+        return None, ()
+    wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
+    keep = []
+    e = _Ext(wl, wr, None, 0, None, None)
+    if alibi is not None:
+        a = np.ascontiguousarray(alibi, dtype=np.float64)
+        if a.shape not in ((Hq,), (B, Hq)):
+            raise ValueError("alibi slopes are [Hq] or [B, Hq]")
+        e.alibi = _ptr(a)
+        e.alibi_bstride = Hq if a.ndim == 2 else 0
+        keep.append(a)
+    for name, arr in (("seqused_q", seqused_q), ("seqused_k", seqused_k)):
+        if arr is not None:
+            a = np.ascontiguousarray(arr, dtype=np.int32)
+            if a.shape != (B,):
+                raise ValueError(name + " is [B]")
+            setattr(e, name, _ptr(a, ctypes.c_int))
+            keep.append(a)
+    keep.append(e)
+    return ctypes.pointer(e), keep
+
+
 def _shape_args(q, k, scale, causal, cu_q, cu_k):
     if cu_q is None:
         if q.ndim != 4 or k.ndim != 4:
@@ -95,16 +133,17 @@ class Oracle:
         dp = ctypes.POINTER(ctypes.c_double)
         ip = ctypes.POINTER(ctypes.c_int)
         shape = [ctypes.c_int] * 6 + [ctypes.c_double, ctypes.c_int, ip, ip]
-        lib.oracle_forward.argtypes = [dp, dp, dp] + shape + [dp, dp, ctypes.c_int]
+        ep = ctypes.POINTER(_Ext)
+        lib.oracle_forward.argtypes = [dp, dp, dp] + shape + [dp, dp, ctypes.c_int, ep]
         lib.oracle_forward.restype = ctypes.c_int
-        lib.oracle_backward.argtypes = [dp] * 6 + shape + [dp, dp, dp, ctypes.c_int]
+        lib.oracle_backward.argtypes = [dp] * 6 + shape + [dp, dp, dp, ctypes.c_int, ep]
         lib.oracle_backward.restype = ctypes.c_int
         lib.oracle_backward_sampled.argtypes = (
-            [dp] * 6 + shape + [ctypes.c_int, ip, dp, ctypes.c_int, ip, dp, dp, ctypes.c_int])
+            [dp] * 6 + shape + [ctypes.c_int, ip, dp, ctypes.c_int, ip, dp, dp, ctypes.c_int, ep])
         lib.oracle_backward_sampled.restype = ctypes.c_int
-        lib.oracle_head_matrices.argtypes = [dp] * 6 + shape + [ctypes.c_int] * 2 + [dp, dp]
+        lib.oracle_head_matrices.argtypes = [dp] * 6 + shape + [ctypes.c_int] * 2 + [dp, dp, ep]
         lib.oracle_head_matrices.restype = ctypes.c_int
-        lib.oracle_preprocess.argtypes = [dp] * 6 + shape + [dp, dp, ctypes.c_int]
+        lib.oracle_preprocess.argtypes = [dp] * 6 + shape + [dp, dp, ctypes.c_int, ep]
         lib.oracle_preprocess.restype = ctypes.c_int
         lib.oracle_max_threads.restype = ctypes.c_int
         self.lib = lib
@@ -116,39 +155,43 @@ class Oracle:
     def _threads(self, nthreads):
         return int(nthreads) if nthreads else self.max_threads()
 
-    def forward(self, q, k, v, scale, causal=False, cu_q=None, cu_k=None, nthreads=None):
+    def forward(self, q, k, v, scale, causal=False, cu_q=None, cu_k=None, nthreads=None,
+                **ext):
         """Returns (o, lse) in fp64; lse is natural-log, -inf for a row with no key."""
         q, k, v = _f64(q), _f64(k), _f64(v)
         args, keep, (B, Sq, Sk, Hq, Hkv, D) = _shape_args(q, k, scale, causal, cu_q, cu_k)
+        e, keep_e = _ext(B, Hq, **ext)
         o = np.zeros_like(q)
         lse = np.zeros((B, Hq, Sq) if cu_q is None else (Hq, q.shape[0]), dtype=np.float64)
         rc = self.lib.oracle_forward(_ptr(q), _ptr(k), _ptr(v), *args, _ptr(o), _ptr(lse),
-                                     self._threads(nthreads))
+                                     self._threads(nthreads), e)
         if rc:
             raise ValueError("oracle_forward rejected its arguments (%d)" % rc)
         return o, lse
 
     def backward(self, q, k, v, dout, scale, causal=False, o=None, lse=None, cu_q=None,
-                 cu_k=None, nthreads=None):
+                 cu_k=None, nthreads=None, **ext):
         """Returns (dq, dk, dv) in fp64.  o / lse None -> the oracle's own fp64 forward."""
         q, k, v, dout, o, lse = map(_f64, (q, k, v, dout, o, lse))
-        args, keep, _ = _shape_args(q, k, scale, causal, cu_q, cu_k)
+        args, keep, (B, Sq, Sk, Hq, Hkv, D) = _shape_args(q, k, scale, causal, cu_q, cu_k)
+        e, keep_e = _ext(B, Hq, **ext)
         dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
         rc = self.lib.oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                       _ptr(dout), *args, _ptr(dq), _ptr(dk), _ptr(dv),
-                                      self._threads(nthreads))
+                                      self._threads(nthreads), e)
         if rc:
             raise ValueError("oracle_backward rejected its arguments (%d)" % rc)
         return dq, dk, dv
 
     def backward_sampled(self, q, k, v, dout, scale, causal=False, o=None, lse=None, cu_q=None,
-                         cu_k=None, qrows=(), krows=(), nthreads=None):
+                         cu_k=None, qrows=(), krows=(), nthreads=None, **ext):
         """dQ rows for (b, s, h) triples and dK / dV rows for (b, s, hk) triples.
 
         Returns (dq_rows [nq, D], dk_rows [nk, D], dv_rows [nk, D]).
         """
         q, k, v, dout, o, lse = map(_f64, (q, k, v, dout, o, lse))
         args, keep, (B, Sq, Sk, Hq, Hkv, D) = _shape_args(q, k, scale, causal, cu_q, cu_k)
+        e, keep_e = _ext(B, Hq, **ext)
         qr = np.ascontiguousarray(np.asarray(qrows, dtype=np.int32).reshape(-1, 3))
         kr = np.ascontiguousarray(np.asarray(krows, dtype=np.int32).reshape(-1, 3))
         dq = np.zeros((len(qr), D))
@@ -157,40 +200,47 @@ class Oracle:
         rc = self.lib.oracle_backward_sampled(
             _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), *args,
             len(qr), _ptr(qr, ctypes.c_int), _ptr(dq), len(kr), _ptr(kr, ctypes.c_int),
-            _ptr(dk), _ptr(dv), self._threads(nthreads))
+            _ptr(dk), _ptr(dv), self._threads(nthreads), e)
         if rc:
             raise ValueError("oracle_backward_sampled rejected its arguments (%d)" % rc)
         return dq, dk, dv
 
     def preprocess(self, q, k, v, dout, scale, causal=False, o=None, lse=None, cu_q=None,
-                   cu_k=None, nthreads=None):
+                   cu_k=None, nthreads=None, **ext):
         """(Dv, LSE_guarded) per query row, in lse's layout: Dv_i = <dO_i, O_i>."""
         q, k, v, dout, o, lse = map(_f64, (q, k, v, dout, o, lse))
         args, keep, (B, Sq, Sk, Hq, Hkv, D) = _shape_args(q, k, scale, causal, cu_q, cu_k)
+        e, keep_e = _ext(B, Hq, **ext)
         shape = (B, Hq, Sq) if cu_q is None else (Hq, q.shape[0])
         dvec = np.zeros(shape)
         lse_out = np.zeros(shape)
         rc = self.lib.oracle_preprocess(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                         _ptr(dout), *args, _ptr(dvec), _ptr(lse_out),
-                                        self._threads(nthreads))
+                                        self._threads(nthreads), e)
         if rc:
             raise ValueError("oracle_preprocess rejected its arguments (%d)" % rc)
         return dvec, lse_out
 
     def head_matrices(self, q, k, v, dout, scale, causal=False, o=None, lse=None, cu_q=None,
-                      cu_k=None, b=0, h=0):
+                      cu_k=None, b=0, h=0, **ext):
         """Dense P and dS [Lq, Lk] of one (sequence, query head) problem (tiny inputs)."""
         q, k, v, dout, o, lse = map(_f64, (q, k, v, dout, o, lse))
         args, keep, (B, Sq, Sk, Hq, Hkv, D) = _shape_args(q, k, scale, causal, cu_q, cu_k)
+        e, keep_e = _ext(B, Hq, **ext)
         if cu_q is None:
             lq, lk = Sq, Sk
         else:
             lq = int(keep[0][b + 1] - keep[0][b])
             lk = int(keep[1][b + 1] - keep[1][b])
+        if ext.get("seqused_q") is not None:
+            lq = int(ext["seqused_q"][b])
+        if ext.get("seqused_k") is not None:
+            lk = int(ext["seqused_k"][b])
         P = np.zeros((lq, lk))
         dS = np.zeros((lq, lk))
         rc = self.lib.oracle_head_matrices(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
-                                           _ptr(dout), *args, int(b), int(h), _ptr(P), _ptr(dS))
+                                           _ptr(dout), *args, int(b), int(h), _ptr(P), _ptr(dS),
+                                           e)
         if rc:
             raise ValueError("oracle_head_matrices rejected its arguments (%d)" % rc)
         return P, dS

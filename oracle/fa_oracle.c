@@ -15,7 +15,19 @@
  *                                                        page)
  *   mask   : key j is visible to query i iff j < Lk and, when causal,
  *            j <= i + (Lk - Lq)   (bottom-right alignment; the pages do not
- *            define the mask, this is the reading taken)
+ *            define the mask, this is the reading taken).  Optional local
+ *            window (window_left wl, window_right wr, -1 = unbounded on that
+ *            side): additionally i + (Lk - Lq) - wl <= j <= i + (Lk - Lq) + wr.
+ *            The Composable Kernel page masks with a generic
+ *            mask.IsOutOfBound(row, col) it does not print; this band, aligned
+ *            like the causal mask, is the reading taken for it.
+ *   ALiBi  : optional per-head slope m_h (the ALIBI bias kind of the
+ *            Composable Kernel page, STAGE 2, added after the scale; the
+ *            page does not print the encoding): s_ij -= m_h |i + (Lk - Lq) - j|
+ *   seqused: optional per-sequence used lengths (seqused of SeqlenInfo in the
+ *            FlashAttention pages): Lq = seqused_q[b], Lk = seqused_k[b]; the
+ *            rows keep their places, rows past the used length are neither
+ *            read nor written.
  *   LSE_i  = log sum_{visible j} exp(s_ij)   (natural log; -inf if no key is
  *            visible)
  *   P_ij   = exp(s_ij - LSE_i) on visible entries, 0 elsewhere.  A row whose
@@ -53,6 +65,14 @@
 #include <omp.h>
 #endif
 
+/* Optional extensions; a NULL pointer means none of them. */
+typedef struct {
+    int window_left, window_right;  /* -1: unbounded on that side */
+    const double *alibi;            /* slopes, alibi[b * alibi_bstride + h]; NULL: none */
+    int alibi_bstride;
+    const int *seqused_q, *seqused_k;  /* [B]; NULL: the full lengths */
+} oracle_ext_t;
+
 typedef struct {
     const double *q, *k, *v, *o, *dout, *lse;
     int B, Sq, Sk, Hq, Hkv, D, G;
@@ -60,13 +80,22 @@ typedef struct {
     int causal;
     const int *cu_q, *cu_k;
     long total_q, total_k;
+    oracle_ext_t ext;
 } prob_t;
 
-static int seq_len_q(const prob_t *p, int b) {
+/* rows the layout reserves for sequence b */
+static int stored_len_q(const prob_t *p, int b) {
     return p->cu_q ? p->cu_q[b + 1] - p->cu_q[b] : p->Sq;
 }
-static int seq_len_k(const prob_t *p, int b) {
+static int stored_len_k(const prob_t *p, int b) {
     return p->cu_k ? p->cu_k[b + 1] - p->cu_k[b] : p->Sk;
+}
+/* rows the attention uses */
+static int seq_len_q(const prob_t *p, int b) {
+    return p->ext.seqused_q ? p->ext.seqused_q[b] : stored_len_q(p, b);
+}
+static int seq_len_k(const prob_t *p, int b) {
+    return p->ext.seqused_k ? p->ext.seqused_k[b] : stored_len_k(p, b);
 }
 /* index of the (b, s, head) row in a [.., S, H, D] or packed [total, H, D] tensor */
 static long row_q(const prob_t *p, int b, int s, int h) {
@@ -83,8 +112,11 @@ static long lse_index(const prob_t *p, int b, int s, int h) {
 }
 static int visible(const prob_t *p, int b, int i, int j) {
     int lq = seq_len_q(p, b), lk = seq_len_k(p, b);
+    int diag = lk - lq;
     if (j < 0 || j >= lk || i < 0 || i >= lq) return 0;
-    if (p->causal && j > i + (lk - lq)) return 0;
+    if (p->causal && j > i + diag) return 0;
+    if (p->ext.window_left >= 0 && j < i + diag - p->ext.window_left) return 0;
+    if (p->ext.window_right >= 0 && j > i + diag + p->ext.window_right) return 0;
     return 1;
 }
 static double dot(const double *a, const double *b, int n) {
@@ -94,7 +126,13 @@ static double dot(const double *a, const double *b, int n) {
 }
 static double score(const prob_t *p, int b, int h, int i, int j) {
     int hk = h / p->G;
-    return p->scale * dot(p->q + row_q(p, b, i, h), p->k + row_k(p, b, j, hk), p->D);
+    double s = p->scale * dot(p->q + row_q(p, b, i, h), p->k + row_k(p, b, j, hk), p->D);
+    if (p->ext.alibi) {
+        double slope = p->ext.alibi[(long)b * p->ext.alibi_bstride + h];
+        int dist = i + (seq_len_k(p, b) - seq_len_q(p, b)) - j;
+        s -= slope * (double)(dist < 0 ? -dist : dist);
+    }
+    return s;
 }
 
 /* Forward statistics of one query row: LSE_i (natural log) and, if o_out is
@@ -220,7 +258,7 @@ static void group_row_stats(const prob_t *p, int b, int hk, double **lse_g, doub
 static int make_prob(prob_t *p, const double *q, const double *k, const double *v,
                      const double *o, const double *lse, const double *dout, int B, int Sq,
                      int Sk, int Hq, int Hkv, int D, double scale, int causal, const int *cu_q,
-                     const int *cu_k) {
+                     const int *cu_k, const oracle_ext_t *ext) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0) return 1;
     if ((cu_q == NULL) != (cu_k == NULL)) return 1;
     p->q = q; p->k = k; p->v = v; p->o = o; p->lse = lse; p->dout = dout;
@@ -228,6 +266,18 @@ static int make_prob(prob_t *p, const double *q, const double *k, const double *
     p->scale = scale; p->causal = causal; p->cu_q = cu_q; p->cu_k = cu_k;
     p->total_q = cu_q ? cu_q[B] : (long)B * Sq;
     p->total_k = cu_k ? cu_k[B] : (long)B * Sk;
+    memset(&p->ext, 0, sizeof(p->ext));
+    p->ext.window_left = p->ext.window_right = -1;
+    if (ext) p->ext = *ext;
+    if (p->ext.window_left < -1 || p->ext.window_right < -1) return 1;
+    for (int b = 0; b < B; ++b) {
+        if (p->ext.seqused_q &&
+            (p->ext.seqused_q[b] < 0 || p->ext.seqused_q[b] > stored_len_q(p, b)))
+            return 1;
+        if (p->ext.seqused_k &&
+            (p->ext.seqused_k[b] < 0 || p->ext.seqused_k[b] > stored_len_k(p, b)))
+            return 1;
+    }
     return 0;
 }
 
@@ -235,10 +285,11 @@ static int make_prob(prob_t *p, const double *q, const double *k, const double *
 
 int oracle_forward(const double *q, const double *k, const double *v, int B, int Sq, int Sk,
                    int Hq, int Hkv, int D, double scale, int causal, const int *cu_q,
-                   const int *cu_k, double *o, double *lse, int nthreads) {
+                   const int *cu_k, double *o, double *lse, int nthreads,
+                   const oracle_ext_t *ext) {
     prob_t p;
     if (make_prob(&p, q, k, v, NULL, NULL, NULL, B, Sq, Sk, Hq, Hkv, D, scale, causal, cu_q,
-                  cu_k))
+                  cu_k, ext))
         return 1;
     for (int b = 0; b < B; ++b)
         for (int h = 0; h < Hq; ++h) {
@@ -255,9 +306,11 @@ int oracle_forward(const double *q, const double *k, const double *v, int B, int
 int oracle_backward(const double *q, const double *k, const double *v, const double *o,
                     const double *lse, const double *dout, int B, int Sq, int Sk, int Hq,
                     int Hkv, int D, double scale, int causal, const int *cu_q, const int *cu_k,
-                    double *dq, double *dk, double *dv, int nthreads) {
+                    double *dq, double *dk, double *dv, int nthreads,
+                    const oracle_ext_t *ext) {
     prob_t p;
-    if (make_prob(&p, q, k, v, o, lse, dout, B, Sq, Sk, Hq, Hkv, D, scale, causal, cu_q, cu_k))
+    if (make_prob(&p, q, k, v, o, lse, dout, B, Sq, Sk, Hq, Hkv, D, scale, causal, cu_q, cu_k,
+                  ext))
         return 1;
     double **lse_g = (double **)malloc(sizeof(double *) * p.G);
     double **dvec_g = (double **)malloc(sizeof(double *) * p.G);
@@ -298,9 +351,10 @@ int oracle_backward_sampled(const double *q, const double *k, const double *v, c
                             int Hkv, int D, double scale, int causal, const int *cu_q,
                             const int *cu_k, int n_qrows, const int *qrows, double *dq_rows,
                             int n_krows, const int *krows, double *dk_rows, double *dv_rows,
-                            int nthreads) {
+                            int nthreads, const oracle_ext_t *ext) {
     prob_t p;
-    if (make_prob(&p, q, k, v, o, lse, dout, B, Sq, Sk, Hq, Hkv, D, scale, causal, cu_q, cu_k))
+    if (make_prob(&p, q, k, v, o, lse, dout, B, Sq, Sk, Hq, Hkv, D, scale, causal, cu_q, cu_k,
+                  ext))
         return 1;
     for (int r = 0; r < n_qrows; ++r) {
         int b = qrows[3 * r], s = qrows[3 * r + 1], h = qrows[3 * r + 2];
@@ -351,9 +405,11 @@ int oracle_backward_sampled(const double *q, const double *k, const double *v, c
 int oracle_preprocess(const double *q, const double *k, const double *v, const double *o,
                       const double *lse, const double *dout, int B, int Sq, int Sk, int Hq,
                       int Hkv, int D, double scale, int causal, const int *cu_q, const int *cu_k,
-                      double *dvec_out, double *lse_out, int nthreads) {
+                      double *dvec_out, double *lse_out, int nthreads,
+                      const oracle_ext_t *ext) {
     prob_t p;
-    if (make_prob(&p, q, k, v, o, lse, dout, B, Sq, Sk, Hq, Hkv, D, scale, causal, cu_q, cu_k))
+    if (make_prob(&p, q, k, v, o, lse, dout, B, Sq, Sk, Hq, Hkv, D, scale, causal, cu_q, cu_k,
+                  ext))
         return 1;
     for (int b = 0; b < B; ++b)
         for (int h = 0; h < Hq; ++h) {
@@ -375,9 +431,11 @@ int oracle_preprocess(const double *q, const double *k, const double *v, const d
 int oracle_head_matrices(const double *q, const double *k, const double *v, const double *o,
                          const double *lse, const double *dout, int B, int Sq, int Sk, int Hq,
                          int Hkv, int D, double scale, int causal, const int *cu_q,
-                         const int *cu_k, int b, int h, double *P, double *dS) {
+                         const int *cu_k, int b, int h, double *P, double *dS,
+                         const oracle_ext_t *ext) {
     prob_t p;
-    if (make_prob(&p, q, k, v, o, lse, dout, B, Sq, Sk, Hq, Hkv, D, scale, causal, cu_q, cu_k))
+    if (make_prob(&p, q, k, v, o, lse, dout, B, Sq, Sk, Hq, Hkv, D, scale, causal, cu_q, cu_k,
+                  ext))
         return 1;
     int lq = seq_len_q(&p, b), lk = seq_len_k(&p, b);
     double *scratch = (double *)malloc(sizeof(double) * D);

@@ -12,7 +12,12 @@ AssertionError when the oracle disagrees with:
   sum_j dV_j = sum_i dO_i),
 * an independent library forward (scipy softmax + numpy matmul),
 * structural reductions (GQA == MHA with repeated K/V, summed over the group;
-  varlen == each sequence run alone).
+  varlen == each sequence run alone),
+* the extensions reduced to the plain, already pinned problem on other inputs:
+  a local window row by row == the unmasked problem on the keys inside the
+  band; causal ALiBi == plain causal attention with one extra head-dimension
+  column (q gets slope / scale, k gets the key position); seqused == the
+  problem cut to the used rows; a (0, 0) window in closed form.
 
 ``tests/test_oracle.py`` runs every pin on the real oracle and also on
 mutant builds with a planted mistake, each of which must fail at least one
@@ -53,12 +58,12 @@ def _dense(rng, B, Sq, Sk, Hq, Hkv, D, scale_in=1.0):
     return q, k, v, do
 
 
-def _fd_check(orc, q, k, v, do, scale, causal, cu_q=None, cu_k=None, h=1e-6, rtol=2e-7):
+def _fd_check(orc, q, k, v, do, scale, causal, cu_q=None, cu_k=None, h=1e-6, rtol=2e-7, **ext):
     """Backward (own fp64 forward) == central differences of L = sum(dO * O)."""
-    dq, dk, dv = orc.backward(q, k, v, do, scale, causal, cu_q=cu_q, cu_k=cu_k)
+    dq, dk, dv = orc.backward(q, k, v, do, scale, causal, cu_q=cu_q, cu_k=cu_k, **ext)
 
     def loss(qq, kk, vv):
-        o, _ = orc.forward(qq, kk, vv, scale, causal, cu_q=cu_q, cu_k=cu_k, nthreads=1)
+        o, _ = orc.forward(qq, kk, vv, scale, causal, cu_q=cu_q, cu_k=cu_k, nthreads=1, **ext)
         return float(np.sum(do * o))
 
     for X, G, name in ((q, dq, "dq"), (k, dk, "dk"), (v, dv, "dv")):
@@ -298,7 +303,162 @@ def pin_preprocess_identity(orc):
         _close(dvec_given, dvec, 1e-14, "Dv with the given O")
 
 
-ALL_PINS = [pin_preprocess_identity, 
+def pin_window_rows_equal_unmasked_band(orc):
+    """Row i of a windowed problem == the unmasked problem of query i against
+    the keys in [i + diag - left, i + diag + right] (cut from the inputs)."""
+    rng = _rng(60)
+    for (Sq, Sk, wl, wr, causal) in ((24, 24, 3, 2, False), (10, 20, 2, 1, False),
+                                     (20, 12, 4, -1, True), (16, 16, -1, 3, False),
+                                     (18, 18, 5, 7, True)):
+        q, k, v, do = _dense(rng, 1, Sq, Sk, 2, 1, 4)
+        o, lse = orc.forward(q, k, v, 0.6, causal, window=(wl, wr))
+        diag = Sk - Sq
+        for i in range(Sq):
+            lo = 0 if wl < 0 else max(0, i + diag - wl)
+            hi = Sk - 1 if wr < 0 else min(Sk - 1, i + diag + wr)
+            if causal:
+                hi = min(hi, i + diag)
+            if hi < lo:
+                assert np.all(o[0, i] == 0) and np.all(np.isneginf(lse[0, :, i])), "empty band"
+                continue
+            o1, l1 = orc.forward(q[:, i:i + 1], k[:, lo:hi + 1], v[:, lo:hi + 1], 0.6, False)
+            _close(o[0, i], o1[0, 0], 1e-13, "window row O")
+            _close(lse[0, :, i], l1[0, :, 0], 1e-13, "window row LSE")
+
+
+def pin_window_zero_closed_form(orc):
+    """Window (0, 0), Sq == Sk: query i sees key i only: O_i = v_i, LSE_i = s_ii,
+    dS = 0 so dQ = dK = 0, and dV_j = sum over the group of dO_j."""
+    q, k, v, do = _dense(_rng(61), 1, 9, 9, 4, 2, 5)
+    o, lse = orc.forward(q, k, v, 0.8, False, window=(0, 0))
+    dq, dk, dv = orc.backward(q, k, v, do, 0.8, False, window=(0, 0))
+    for h in range(4):
+        _close(o[0, :, h], v[0, :, h // 2], 1e-14, "O = v")
+        _close(lse[0, h], 0.8 * np.sum(q[0, :, h] * k[0, :, h // 2], axis=1), 1e-14, "LSE = s_ii")
+    _close(dq, np.zeros_like(dq), 1e-14, "dQ = 0")
+    _close(dk, np.zeros_like(dk), 1e-14, "dK = 0")
+    _close(dv[0, :, 0], do[0, :, 0] + do[0, :, 1], 1e-14, "dV = dO summed")
+    _close(dv[0, :, 1], do[0, :, 2] + do[0, :, 3], 1e-14, "dV = dO summed")
+
+
+def pin_fd_window(orc):
+    q, k, v, do = _dense(_rng(62), 1, 7, 9, 2, 1, 3)
+    _fd_check(orc, q, k, v, do, 0.7, False, window=(2, 1))
+    _fd_check(orc, q, k, v, do, 0.7, True, window=(3, -1))
+
+
+def _augment(q, k, v, do, slopes, scale):
+    """q' = [q, slope_h / scale], k' = [k, j], v' = [v, 0], dO' = [dO, 0]:
+    scale * <q', k'> = s + slope_h * j, and the extra column of O' is 0."""
+    B, Sq, Hq, D = q.shape
+    Sk, Hkv = k.shape[1], k.shape[2]
+    sl = np.broadcast_to(np.asarray(slopes, dtype=np.float64), (B, Hq))
+    qa = np.concatenate([q, np.broadcast_to((sl / scale)[:, None, :, None], (B, Sq, Hq, 1))], 3)
+    pos = np.arange(Sk, dtype=np.float64)[None, :, None, None]
+    ka = np.concatenate([k, np.broadcast_to(pos, (B, Sk, Hkv, 1))], 3)
+    va = np.concatenate([v, np.zeros((B, Sk, Hkv, 1))], 3)
+    da = np.concatenate([do, np.zeros((B, Sq, Hq, 1))], 3)
+    return tuple(np.ascontiguousarray(x) for x in (qa, ka, va, da))
+
+
+def pin_alibi_causal_equals_augmented(orc):
+    """Causal ALiBi: every visible key has j <= i + diag, so the bias
+    -m (i + diag - j) = m j - m (i + diag): plain causal attention on q', k' of
+    one more column (O and the gradients equal; LSE shifts by m (i + diag))."""
+    rng = _rng(63)
+    for (B, Sq, Sk, Hq, Hkv) in ((2, 11, 11, 4, 2), (1, 7, 13, 2, 2)):
+        q, k, v, do = _dense(rng, B, Sq, Sk, Hq, Hkv, 4)
+        slopes = rng.uniform(0.05, 0.6, size=(B, Hq))
+        sc = 0.55
+        o, lse = orc.forward(q, k, v, sc, True, alibi=slopes)
+        qa, ka, va, da = _augment(q, k, v, do, slopes, sc)
+        oa, la = orc.forward(qa, ka, va, sc, True)
+        _close(o, oa[..., :4], 1e-13, "ALiBi O")
+        _close(oa[..., 4], np.zeros_like(oa[..., 4]), 0, "augmented O column")
+        shift = slopes[:, :, None] * (np.arange(Sq) + (Sk - Sq))[None, None, :]
+        fin = np.isfinite(la)
+        _close(lse[fin], (la - shift)[fin], 1e-12, "ALiBi LSE")
+        dq, dk, dv = orc.backward(q, k, v, do, sc, True, alibi=slopes)
+        dqa, dka, dva = orc.backward(qa, ka, va, da, sc, True)
+        _close(dq, dqa[..., :4], 1e-12, "ALiBi dQ")
+        _close(dk, dka[..., :4], 1e-12, "ALiBi dK")
+        _close(dv, dva[..., :4], 1e-12, "ALiBi dV")
+
+
+def pin_alibi_noncausal(orc):
+    """Non-causal ALiBi: a single query at the last position sees every key to
+    its left (the augmented problem again); with Sq == Sk, reversing the order
+    of queries and keys leaves |i - j| unchanged, so the outputs come back
+    reversed; the backward is the gradient of its forward (also Sq != Sk);
+    slopes 0 give plain attention."""
+    rng = _rng(64)
+    q, k, v, do = _dense(rng, 1, 1, 10, 2, 1, 3)
+    slopes = np.array([0.3, 0.9])
+    o, lse = orc.forward(q, k, v, 0.5, False, alibi=slopes)
+    qa, ka, va, _ = _augment(q, k, v, do, slopes, 0.5)
+    oa, la = orc.forward(qa, ka, va, 0.5, False)
+    _close(o, oa[..., :3], 1e-13, "single-query ALiBi O")
+    _close(lse, la - slopes[None, :, None] * 9, 1e-12, "single-query ALiBi LSE")
+    q, k, v, do = _dense(rng, 1, 11, 11, 2, 2, 3)
+    o, lse = orc.forward(q, k, v, 0.5, False, alibi=slopes)
+    dq, dk, dv = orc.backward(q, k, v, do, 0.5, False, alibi=slopes)
+    r = lambda x: np.ascontiguousarray(x[:, ::-1])
+    o2, lse2 = orc.forward(r(q), r(k), r(v), 0.5, False, alibi=slopes)
+    dq2, dk2, dv2 = orc.backward(r(q), r(k), r(v), r(do), 0.5, False, alibi=slopes)
+    _close(o2, r(o), 1e-13, "reversed O")
+    _close(lse2, np.ascontiguousarray(lse[:, :, ::-1]), 1e-13, "reversed LSE")
+    for a, b, n in ((dq2, dq, "dQ"), (dk2, dk, "dK"), (dv2, dv, "dV")):
+        _close(a, r(b), 1e-12, "reversed " + n)
+    o0, _ = orc.forward(q, k, v, 0.5, False, alibi=np.zeros(2))
+    op, _ = orc.forward(q, k, v, 0.5, False)
+    _close(o0, op, 0, "zero slopes")
+    _fd_check(orc, q[:, :5], k[:, :7], v[:, :7], do[:, :5], 0.5, False, alibi=slopes)
+
+
+def pin_seqused_equals_cut(orc):
+    """seqused == the problem cut to the used rows (dense and varlen); rows past
+    the used lengths stay zero."""
+    rng = _rng(65)
+    q, k, v, do = _dense(rng, 2, 20, 20, 2, 1, 4)
+    uq, uk = np.array([12, 20]), np.array([15, 7])
+    for causal in (False, True):
+        ext = dict(seqused_q=uq, seqused_k=uk, window=(5, -1) if causal else None)
+        o, lse = orc.forward(q, k, v, 0.6, causal, **ext)
+        dq, dk, dv = orc.backward(q, k, v, do, 0.6, causal, **ext)
+        w = dict(window=ext["window"])
+        for b in range(2):
+            lq, lk = uq[b], uk[b]
+            sl = slice(b, b + 1)
+            o1, l1 = orc.forward(q[sl, :lq], k[sl, :lk], v[sl, :lk], 0.6, causal, **w)
+            d1 = orc.backward(q[sl, :lq], k[sl, :lk], v[sl, :lk], do[sl, :lq], 0.6, causal, **w)
+            _close(o[sl, :lq], o1, 1e-14, "seqused O")
+            _close(lse[sl, :, :lq], l1, 1e-14, "seqused LSE")
+            _close(dq[sl, :lq], d1[0], 1e-14, "seqused dQ")
+            _close(dk[sl, :lk], d1[1], 1e-14, "seqused dK")
+            _close(dv[sl, :lk], d1[2], 1e-14, "seqused dV")
+            for t, n in ((o[sl, lq:], "O"), (dq[sl, lq:], "dQ"), (dk[sl, lk:], "dK"),
+                         (dv[sl, lk:], "dV")):
+                assert np.all(t == 0), "rows past seqused: " + n
+    # varlen: packed sequences with used prefixes
+    cu = np.array([0, 9, 21, 30], dtype=np.int32)
+    qv = rng.standard_normal((30, 2, 4))
+    kv = rng.standard_normal((30, 1, 4))
+    vv = rng.standard_normal((30, 1, 4))
+    uq, uk = np.array([9, 5, 0]), np.array([4, 12, 6])
+    o, lse = orc.forward(qv, kv, vv, 0.6, True, cu_q=cu, cu_k=cu, seqused_q=uq, seqused_k=uk)
+    for b in range(3):
+        if uq[b] == 0:
+            continue
+        a, c = cu[b], cu[b]
+        o1, l1 = orc.forward(qv[None, a:a + uq[b]], kv[None, c:c + uk[b]], vv[None, c:c + uk[b]],
+                             0.6, True)
+        _close(o[a:a + uq[b]], o1[0], 1e-14, "varlen seqused O")
+        _close(lse[:, a:a + uq[b]], l1[0], 1e-14, "varlen seqused LSE")
+
+
+ALL_PINS = [pin_preprocess_identity, pin_window_rows_equal_unmasked_band,
+    pin_window_zero_closed_form, pin_fd_window, pin_alibi_causal_equals_augmented,
+    pin_alibi_noncausal, pin_seqused_equals_cut,
     pin_worked_example, pin_fd_dense, pin_fd_causal, pin_fd_causal_rect, pin_fd_gqa,
     pin_fd_varlen, pin_library_forward, pin_closed_forms, pin_invariants,
     pin_gqa_equals_expanded, pin_varlen_equals_dense, pin_sampled_equals_full,

@@ -59,16 +59,31 @@ MUTANTS = {
     "dQ without scale": ("for (int d = 0; d < D; ++d) dq_out[d] *= p->scale;", ""),
     "dV uses dS": ("dv_out[d] += pij * doi[d];", "dv_out[d] += ds * doi[d];"),
     "dK uses dO": ("dk_out[d] += ds * qi[d];", "dk_out[d] += ds * doi[d];"),
-    "top-left causal": ("if (p->causal && j > i + (lk - lq)) return 0;",
+    "top-left causal": ("if (p->causal && j > i + diag) return 0;",
                         "if (p->causal && j > i) return 0;"),
-    "causal off by one": ("if (p->causal && j > i + (lk - lq)) return 0;",
-                          "if (p->causal && j >= i + (lk - lq)) return 0;"),
-    "GQA head mapping": ("int hk = h / p->G;\n    return p->scale",
-                         "int hk = h % p->Hkv;\n    return p->scale"),
+    "causal off by one": ("if (p->causal && j > i + diag) return 0;",
+                          "if (p->causal && j >= i + diag) return 0;"),
+    "GQA head mapping": ("int hk = h / p->G;\n    double s = p->scale",
+                         "int hk = h % p->Hkv;\n    double s = p->scale"),
+    "window left off by one": ("j < i + diag - p->ext.window_left", "j <= i + diag - p->ext.window_left"),
+    "window right off by one": ("j > i + diag + p->ext.window_right",
+                                "j >= i + diag + p->ext.window_right"),
+    "window top-left aligned": ("j > i + diag + p->ext.window_right", "j > i + p->ext.window_right"),
+    "ALiBi sign": ("s -= slope *", "s += slope *"),
+    "ALiBi signed distance": ("s -= slope * (double)(dist < 0 ? -dist : dist);",
+                              "s -= slope * (double)dist;"),
+    "ALiBi top-left aligned": ("int dist = i + (seq_len_k(p, b) - seq_len_q(p, b)) - j;",
+                               "int dist = i - j;"),
+    "ALiBi ignores the batch stride": ("p->ext.alibi[(long)b * p->ext.alibi_bstride + h]",
+                                       "p->ext.alibi[h]"),
+    "seqused_k ignored": ("return p->ext.seqused_k ? p->ext.seqused_k[b] : stored_len_k(p, b);",
+                          "return stored_len_k(p, b);"),
+    "seqused_q ignored": ("return p->ext.seqused_q ? p->ext.seqused_q[b] : stored_len_q(p, b);",
+                          "return stored_len_q(p, b);"),
     "Dv from q": ("return dot(doi, o_scratch, p->D);", "return dot(doi, p->q + row_q(p, b, i, h), p->D);"),
     "preprocess skips the LSE guard": ("if (lse == -INFINITY) lse = 0.0; /* get_validated_lse */", ""),
     "LSE drops max shift": ("double lse = m + log(sum);", "double lse = log(sum);"),
-    "score without scale": ("return p->scale * dot(", "return dot("),
+    "score without scale": ("double s = p->scale * dot(", "double s = dot("),
     "varlen lse index": ("if (p->cu_q) return (long)h * p->total_q + p->cu_q[b] + s;",
                          "if (p->cu_q) return (long)h * p->total_q + s;"),
 }
