@@ -28,7 +28,7 @@ EXPORTED = [
     "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_workspace_layout", "fa_fwd",
     "fa_device_status", "fa_set_wait_timeout_ns", "fa_status_string",
     "fa_selftest_umma", "fa_selftest_semaphore", "fa_selftest_tmem_layout", "fa_bwd_noalloc",
-    "fa_bwd_noalloc_scratch_bytes",
+    "fa_bwd_noalloc_scratch_bytes", "fa_fwd_ext", "fa_bwd_ext",
 ]
 
 
@@ -46,6 +46,33 @@ _i = ctypes.c_int
 _f = ctypes.c_float
 _sz = ctypes.c_size_t
 _SHAPE = [_i] * 6   # B, Sq, Sk, Hq, Hkv, D
+
+
+class FaExt(ctypes.Structure):
+    """fa_ext of include/fa.h: local window, ALiBi slopes, used lengths."""
+    _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
+                ("alibi_slopes", ctypes.c_void_p), ("alibi_batch_stride", ctypes.c_int),
+                ("seqused_q", ctypes.c_void_p), ("seqused_k", ctypes.c_void_p)]
+
+
+def _ext(Hq, window=None, alibi_slopes=None, seqused_q=None, seqused_k=None):
+    """A pointer to an FaExt, or None when no extension is asked for."""
+    if window is None and alibi_slopes is None and seqused_q is None and seqused_k is None:
+        return None
+    e = FaExt(-1, -1, None, 0, None, None)
+    if window is not None:
+        e.window_left, e.window_right = int(window[0]), int(window[1])
+    if alibi_slopes is not None:
+        if alibi_slopes.dtype != torch.float32 or not alibi_slopes.is_contiguous():
+            raise ValueError("alibi_slopes: contiguous fp32 [Hq] or [B, Hq]")
+        e.alibi_slopes = alibi_slopes.data_ptr()
+        e.alibi_batch_stride = Hq if alibi_slopes.dim() == 2 else 0
+    for name, t in (("seqused_q", seqused_q), ("seqused_k", seqused_k)):
+        if t is not None:
+            if t.dtype != torch.int32 or not t.is_contiguous():
+                raise ValueError(name + ": contiguous int32 [B]")
+            setattr(e, name, t.data_ptr())
+    return ctypes.pointer(e)
 
 
 def lib():
@@ -69,6 +96,10 @@ def lib():
         L.fa_bwd_postprocess.argtypes = [_vp] + _SHAPE + [_f, _vp, _vp, _i, _i, _vp, _sz, _vp]
         L.fa_bwd_workspace_layout.argtypes = _SHAPE + [_i, _i] + [ctypes.POINTER(_sz)] * 4
         L.fa_fwd.argtypes = [_vp] * 5 + _SHAPE + [_f, _i, _vp, _vp, _i, _vp]
+        _ep = ctypes.POINTER(FaExt)
+        L.fa_fwd_ext.argtypes = [_vp] * 5 + _SHAPE + [_f, _i, _vp, _vp, _ep, _i, _vp]
+        L.fa_bwd_ext.argtypes = ([_vp] * 9 + _SHAPE + [_f, _i, _vp, _vp, _ep, _i, _i, _vp, _sz,
+                                                       _vp])
         L.fa_device_status.argtypes = [_vp, _vp]
         L.fa_set_wait_timeout_ns.argtypes = [ctypes.c_longlong]
         L.fa_set_wait_timeout_ns.restype = ctypes.c_longlong
@@ -82,7 +113,8 @@ def lib():
         L.fa_selftest_semaphore.argtypes = [_vp, _i, ctypes.c_longlong, _vp, _vp]
         L.fa_selftest_tmem_layout.argtypes = [_i, _vp, _vp]
         for name in ("fa_bwd", "fa_bwd_with_workspace", "fa_bwd_preprocess", "fa_bwd_main",
-                     "fa_bwd_postprocess", "fa_bwd_workspace_layout", "fa_fwd",
+                     "fa_bwd_postprocess", "fa_bwd_workspace_layout", "fa_fwd", "fa_fwd_ext",
+                     "fa_bwd_ext",
                      "fa_device_status", "fa_selftest_umma", "fa_selftest_semaphore",
                      "fa_selftest_tmem_layout"):
             getattr(L, name).restype = _i
@@ -134,8 +166,14 @@ def default_scale(D: int) -> float:
 
 
 def fa_fwd(q, k, v, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seqlens_k=None,
-           max_seqlen_q=None, max_seqlen_k=None, stream=None):
-    """Untimed forward helper: returns (o, lse); lse fp32 [B,Hq,Sq] or [Hq,total_q]."""
+           max_seqlen_q=None, max_seqlen_k=None, stream=None, window=None, alibi_slopes=None,
+           seqused_q=None, seqused_k=None):
+    """Forward pass: returns (o, lse); lse fp32 [B,Hq,Sq] or [Hq,total_q].
+
+    ``window=(left, right)`` (-1 = unbounded side), ``alibi_slopes`` (fp32
+    [Hq] or [B, Hq]) and ``seqused_q`` / ``seqused_k`` (int32 [B]) select
+    fa_fwd_ext; rows past the used lengths are left as allocated.
+    """
     B, Sq, Sk, Hq, Hkv, D = _shape(q, k, cu_seqlens_q, max_seqlen_q, max_seqlen_k)
     scale = default_scale(D) if softmax_scale is None else float(softmax_scale)
     o = torch.empty_like(q)
@@ -143,21 +181,26 @@ def fa_fwd(q, k, v, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seql
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
     else:
         lse = torch.empty((Hq, q.shape[0]), dtype=torch.float32, device=q.device)
-    st = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Sq, Sk, Hq, Hkv, D,
-                      scale, int(bool(causal)), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
-                      _dtype_code(q), _stream(stream))
-    _check(st, "fa_fwd")
+    ext = _ext(Hq, window, alibi_slopes, seqused_q, seqused_k)
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Sq, Sk, Hq, Hkv, D, scale,
+            int(bool(causal)), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k)]
+    if ext is None:
+        _check(lib().fa_fwd(*args, _dtype_code(q), _stream(stream)), "fa_fwd")
+    else:
+        _check(lib().fa_fwd_ext(*args, ext, _dtype_code(q), _stream(stream)), "fa_fwd_ext")
     return o, lse
 
 
 def fa_bwd(q, k, v, o, dout, lse, causal=False, softmax_scale=None, cu_seqlens_q=None,
            cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, deterministic=False,
-           dq=None, dk=None, dv=None, workspace=None, stream=None):
+           dq=None, dk=None, dv=None, workspace=None, stream=None, window=None,
+           alibi_slopes=None, seqused_q=None, seqused_k=None):
     """Backward pass through the C ABI; returns (dq, dk, dv).
 
     Outputs are allocated when not given.  ``workspace`` (a uint8 CUDA tensor
     of at least ``workspace_bytes(...)``) selects fa_bwd_with_workspace,
-    otherwise the library's own workspace is used.
+    otherwise the library's own workspace is used.  The extension keywords
+    (as for fa_fwd) select fa_bwd_ext.
     """
     B, Sq, Sk, Hq, Hkv, D = _shape(q, k, cu_seqlens_q, max_seqlen_q, max_seqlen_k)
     scale = default_scale(D) if softmax_scale is None else float(softmax_scale)
@@ -167,7 +210,12 @@ def fa_bwd(q, k, v, o, dout, lse, causal=False, softmax_scale=None, cu_seqlens_q
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
             _ptr(dv), B, Sq, Sk, Hq, Hkv, D, scale, int(bool(causal)), _ptr(cu_seqlens_q),
             _ptr(cu_seqlens_k), int(bool(deterministic)), _dtype_code(q)]
-    if workspace is None:
+    ext = _ext(Hq, window, alibi_slopes, seqused_q, seqused_k)
+    if ext is not None:
+        st = lib().fa_bwd_ext(*args[:19], ext, *args[19:], _ptr(workspace),
+                              0 if workspace is None else workspace.numel(), _stream(stream))
+        _check(st, "fa_bwd_ext")
+    elif workspace is None:
         st = lib().fa_bwd(*args, _stream(stream))
         _check(st, "fa_bwd")
     else:

@@ -199,11 +199,41 @@ int sm_count() {
     return n > 0 ? n : 1;
 }
 
+// The visible band, ALiBi slopes and used lengths of the parameter block
+// (ext NULL: none, only the causal mask).
+fa_status apply_ext(fa::BwdParams &p, int causal, const fa_ext *ext) {
+    int wl = -1, wr = -1;
+    p.alibi = nullptr;
+    p.alibi_bstride = 0;
+    p.seqused_q = p.seqused_k = nullptr;
+    if (ext) {
+        wl = ext->window_left;
+        wr = ext->window_right;
+        if (wl < -1 || wr < -1) return FA_ERR_INVALID_ARG;
+        if (ext->alibi_slopes) {
+            if ((reinterpret_cast<uintptr_t>(ext->alibi_slopes) & 3u) ||
+                (ext->alibi_batch_stride != 0 && ext->alibi_batch_stride != p.Hq))
+                return FA_ERR_INVALID_ARG;
+            p.alibi = ext->alibi_slopes;
+            p.alibi_bstride = ext->alibi_batch_stride;
+        }
+        if ((reinterpret_cast<uintptr_t>(ext->seqused_q) & 3u) ||
+            (reinterpret_cast<uintptr_t>(ext->seqused_k) & 3u))
+            return FA_ERR_INVALID_ARG;
+        p.seqused_q = ext->seqused_q;
+        p.seqused_k = ext->seqused_k;
+    }
+    p.win_lo = (wl < 0 || wl >= fa::kNoWindow) ? fa::kNoWindow : wl;
+    p.win_hi = (wr < 0 || wr >= fa::kNoWindow) ? fa::kNoWindow : wr;
+    if (causal) p.win_hi = std::min(p.win_hi, 0);
+    return FA_OK;
+}
+
 fa_status prepare(const void *q, const void *k, const void *v, const void *o, const void *dout,
                   const float *lse, void *dq, void *dk, void *dv, int B, int Sq, int Sk, int Hq,
                   int Hkv, int D, float scale, int causal, const int *cu_q, const int *cu_k,
                   int deterministic, fa_dtype dtype, void *ws, size_t ws_bytes,
-                  cudaStream_t stream, Prepared *out) {
+                  cudaStream_t stream, Prepared *out, const fa_ext *ext = nullptr) {
     fa_status st = check_shape(B, Sq, Sk, Hq, Hkv, D, dtype, cu_q, cu_k);
     if (st != FA_OK) return st;
     if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
@@ -233,6 +263,7 @@ fa_status prepare(const void *q, const void *k, const void *v, const void *o, co
     p.deterministic = deterministic ? 1 : 0;
     p.varlen = cu_q != nullptr;
     p.cu_q = cu_q; p.cu_k = cu_k;
+    if ((st = apply_ext(p, causal, ext)) != FA_OK) return st;
     p.err = reinterpret_cast<int *>(w + L.err);
     p.ntiles = reinterpret_cast<int *>(w + L.ntiles);
     p.unit_counter = reinterpret_cast<int *>(w + L.ntiles) + 1;
@@ -399,11 +430,33 @@ fa_status fa_bwd_with_workspace(const void *q, const void *k, const void *v, con
                                 float softmax_scale, int causal, const int *cu_seqlens_q,
                                 const int *cu_seqlens_k, int deterministic, fa_dtype dtype,
                                 void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!workspace) return FA_ERR_INVALID_ARG;   // (fa_bwd_ext would take the library's)
+    return fa_bwd_ext(q, k, v, o, dout, lse, dq, dk, dv, B, Sq, Sk, Hq, Hkv, D, softmax_scale,
+                      causal, cu_seqlens_q, cu_seqlens_k, nullptr, deterministic, dtype,
+                      workspace, workspace_bytes, stream);
+}
+
+fa_status fa_bwd_ext(const void *q, const void *k, const void *v, const void *o,
+                     const void *dout, const float *lse, void *dq, void *dk, void *dv, int B,
+                     int Sq, int Sk, int Hq, int Hkv, int D, float softmax_scale, int causal,
+                     const int *cu_seqlens_q, const int *cu_seqlens_k, const fa_ext *ext,
+                     int deterministic, fa_dtype dtype, void *workspace, size_t workspace_bytes,
+                     cudaStream_t stream) {
     if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+    fa_status st;
+    if (!workspace) {
+        // the library's own workspace, grown on demand
+        st = check_shape(B, Sq, Sk, Hq, Hkv, D, dtype, cu_seqlens_q, cu_seqlens_k);
+        if (st != FA_OK) return st;
+        workspace_bytes = fa_bwd_workspace_bytes(B, Sq, Sk, Hq, Hkv, D,
+                                                 cu_seqlens_q != nullptr, deterministic);
+        if (workspace_bytes == 0) return FA_ERR_INVALID_ARG;
+        if ((st = library_workspace(workspace_bytes, stream, &workspace)) != FA_OK) return st;
+    }
     Prepared P;
-    fa_status st = prepare(q, k, v, o, dout, lse, dq, dk, dv, B, Sq, Sk, Hq, Hkv, D,
-                           softmax_scale, causal, cu_seqlens_q, cu_seqlens_k, deterministic, dtype,
-                           workspace, workspace_bytes, stream, &P);
+    st = prepare(q, k, v, o, dout, lse, dq, dk, dv, B, Sq, Sk, Hq, Hkv, D, softmax_scale, causal,
+                 cu_seqlens_q, cu_seqlens_k, deterministic, dtype, workspace, workspace_bytes,
+                 stream, &P, ext);
     if (st != FA_OK) return st;
     if ((st = run_preprocess(P, dtype, stream)) != FA_OK) return st;
     if ((st = run_main(P, dtype, stream)) != FA_OK) return st;
@@ -451,6 +504,14 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
                  int Sk, int Hq, int Hkv, int D, float softmax_scale, int causal,
                  const int *cu_seqlens_q, const int *cu_seqlens_k, fa_dtype dtype,
                  cudaStream_t stream) {
+    return fa_fwd_ext(q, k, v, o, lse, B, Sq, Sk, Hq, Hkv, D, softmax_scale, causal, cu_seqlens_q,
+                      cu_seqlens_k, nullptr, dtype, stream);
+}
+
+fa_status fa_fwd_ext(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                     int Sq, int Sk, int Hq, int Hkv, int D, float softmax_scale, int causal,
+                     const int *cu_seqlens_q, const int *cu_seqlens_k, const fa_ext *ext,
+                     fa_dtype dtype, cudaStream_t stream) {
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
     fa_status st = check_shape(B, Sq, Sk, Hq, Hkv, D, dtype, cu_seqlens_q, cu_seqlens_k);
     if (st != FA_OK) return st;
@@ -469,6 +530,7 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
     p.varlen = cu_seqlens_q != nullptr;
     p.cu_q = cu_seqlens_q;
     p.cu_k = cu_seqlens_k;
+    if ((st = apply_ext(p, causal, ext)) != FA_OK) return st;
     p.err = fa::fwd_error_word();
     if (!p.err) return FA_ERR_CUDA;
     p.budget_ns = g_budget_ns.load();

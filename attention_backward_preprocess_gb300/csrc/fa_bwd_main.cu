@@ -206,8 +206,8 @@ __device__ __forceinline__ Unit decode_unit(const BwdParams &p, int t) {
         u.hk = e.z;
         u.q_row0 = p.cu_q[u.b];
         u.k_row0 = p.cu_k[u.b];
-        u.lq = p.cu_q[u.b + 1] - u.q_row0;
-        u.lk = p.cu_k[u.b + 1] - u.k_row0;
+        u.lq = used_len_q(p, u.b);
+        u.lk = used_len_k(p, u.b);
         u.bidx = 0;
     } else {
         // groups of unit_group (batch, kv head) pairs, one after the other;
@@ -224,26 +224,43 @@ __device__ __forceinline__ Unit decode_unit(const BwdParams &p, int t) {
         u.hk = bh - u.b * p.Hkv;
         u.q_row0 = 0;
         u.k_row0 = 0;
-        u.lq = p.Sq;
-        u.lk = p.Sk;
+        u.lq = used_len_q(p, u.b);
+        u.lk = used_len_k(p, u.b);
         u.bidx = u.b;
     }
+    // queries that see a key of [n0, n0 + kBlockN): i >= n0 - diag - win_hi
+    // (the first key against the upper edge of the band) and
+    // i <= n0 + kBlockN - 1 - diag + win_lo (the last key against the lower edge)
     const int n0 = u.n_block * kBlockN;
-    int first_row = 0;
-    if (p.causal) first_row = max(0, n0 - (u.lk - u.lq));   // first query that sees key n0
-    u.m_begin = first_row / BM;
-    const int m_end = (u.lq + BM - 1) / BM;
-    u.nm = max(0, m_end - u.m_begin);
+    const long long diag = u.lk - u.lq;
+    const long long first_row = max(0LL, (long long)n0 - diag - p.win_hi);
+    const long long last_row = min((long long)u.lq - 1, (long long)n0 + kBlockN - 1 - diag + p.win_lo);
+    u.m_begin = (int)min(first_row / BM, (long long)(u.lq + BM - 1) / BM);
+    u.nm = last_row < first_row ? 0 : (int)(last_row / BM + 1 - u.m_begin);
     if (n0 >= u.lk) u.nm = 0;
     u.iters = p.G * u.nm;
     return u;
+}
+
+// First key block with a key that some query of the rows [m0, ...) of a
+// sequence can see: the block holding key m0 + diag - win_lo.  A row block
+// receives dQ contributions from the key blocks n_first, n_first + 1, ... in
+// turn, so in deterministic mode the unit of key block n waits until its row
+// block's semaphore counts n - n_first earlier contributions.
+__device__ __forceinline__ int first_key_block(const BwdParams &p, int m0, int diag) {
+    const long long j = (long long)m0 + diag - p.win_lo;
+    return j <= 0 ? 0 : (int)(j / kBlockN);
 }
 
 struct MainMaps {
     CUtensorMap q, k, v, dout;
 };
 
-template <int kD, typename T>
+// kExt: the extended instance -- a lower edge of the visible band (a left
+// window) and / or the ALiBi bias (p.alibi).  A separate instance, so that the
+// plain kernel (no mask, or a band with an upper edge only, e.g. causal) keeps
+// its softmax and reducer code as they are.
+template <int kD, typename T, bool kExt>
 __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
     bwd_main_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ MainMaps maps) {
     using C = MainCfg<kD, T>;
@@ -600,9 +617,9 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             // m) = head0 + g * hstride + m * BM, heads innermost, row blocks
             // from the last one down (the MMA warps' order)
             long long head0 = 0, hstride = 0;
-            int g_it = 0, m_it = -1, m_first = 0, n_cur = 0;
+            int g_it = 0, m_it = -1, m_first = 0, n_cur = 0, diag_cur = 0;
             bool units_done = false;
-            auto next_row = [&](long long &row0) __attribute__((always_inline)) -> bool {
+            auto next_row = [&](long long &row0, int &nb) __attribute__((always_inline)) -> bool {
                 while (m_it < m_first) {
                     if (units_done) return false;
                     const int t = next_unit();
@@ -610,6 +627,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     const Unit u = decode_unit<BM>(p, t);
                     if (u.nm == 0) continue;
                     n_cur = u.n_block;
+                    diag_cur = u.lk - u.lq;
                     head0 = ws_row(p, u.b, u.hk * p.G, 0);
                     hstride = ws_row(p, u.b, u.hk * p.G + 1, 0) - head0;
                     m_first = u.m_begin;
@@ -617,6 +635,9 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     g_it = 0;
                 }
                 row0 = head0 + g_it * hstride + (long long)m_it * BM;
+                // deterministic order: contributions counted from the row block's
+                // first key block (block 0 unless the band has a lower edge)
+                nb = kExt ? n_cur - first_key_block(p, m_it * BM, diag_cur) : n_cur;
                 if (++g_it == p.G) { g_it = 0; --m_it; }
                 return true;
             };
@@ -652,8 +673,9 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             };
             uint32_t R0[32], R1[32];
             long long row0 = 0;
+            int nb = 0;   // earlier contributions to the step's row block
             int db = 0;   // dS^T tile / staging buffer of the step
-            while (ok && next_row(row0)) {
+            while (ok && next_row(row0, nb)) {
                 if (!(ok = wait_dq(cb))) break;
                 load_step(R0, R1, cb);
                 if (++cb == C::kSBuf) cb = 0;
@@ -661,7 +683,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 // previous chunk was read before the softmax wrote this step's dS^T)
                 if (lane == 0 && warp == C::W_RED) {
                     stg_row[db] = row0;
-                    reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 64)[db] = n_cur;
+                    reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 64)[db] = nb;
                 }
                 write_chunk(R0, sbase + C::OFF_DS + db * C::DS_BYTES, bar(B_TILE_FULL + db));
                 // rows 32-63 into staging buffer db
@@ -711,7 +733,9 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                         // contributions to this row block arrive in n-block order:
                         // wait until the 4 reducer warps of every earlier n block added
                         bool got = true;
-                        if (lane == 0) got = sem_wait_geq(sem, 4 * u.n_block, w);
+                        const int nb = kExt ? u.n_block - first_key_block(p, m * BM, u.lk - u.lq)
+                                            : u.n_block;
+                        if (lane == 0) got = sem_wait_geq(sem, 4 * nb, w);
                         got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
                         if (!got) { ok = false; break; }
                         __threadfence();
@@ -778,11 +802,21 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             const int kj = n0 + j;                   // key index within the sequence
             const bool key_ok = kj < u.lk;
             const int kb = n0 + quarter * 32 + g4;   // first key of this thread's 16-lane rows
-            const int diag = u.lk - u.lq;            // key kj visible to query qi iff kj <= qi + diag
+            // key kj is visible to query qi iff -win_lo <= kj - qi - diag <= win_hi
+            const int diag = u.lk - u.lq;
+            const int whi = p.win_hi, wlo = p.win_lo;
             for (int it = 0; it < u.iters; ++it) {
                 const int m = u.m_of(it, p.G);
                 const int m0 = m * BM;
-                const bool masked = p.causal && (n0 + BN - 1 > m0 + diag);
+                // the tile crosses the upper / lower edge of the band: mask
+                // element by element (one compare per edge and element)
+                const bool masked_hi = n0 + BN - 1 - (m0 + diag) > whi;
+                const bool masked_lo = kExt && n0 - (m0 + BM - 1 + diag) < -wlo;
+                // ALiBi slope of the step's query head, in log2 units (0: none)
+                float slope2 = 0.f;
+                if (kExt && p.alibi)
+                    slope2 = __ldg(p.alibi + (long long)u.b * p.alibi_bstride + u.hk * p.G + u.g_of(it, p.G)) *
+                             1.4426950408889634f;
                 if (!(ok = mbar_wait(bar(B_STAGE0 + stage), st_ph, w))) break;
                 if (!(ok = mbar_wait(bar(B_S_FULL + cb), bit(s_ph, cb), w))) break;
                 s_ph ^= 1u << cb;
@@ -809,8 +843,11 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     }
                     const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
                     tmem_wait_ld();
-                    // causal: key kj is masked for query column c iff kj - (m0 + c0 + diag) > c
+                    // element (key kb + kr, query column 8k + e) has
+                    // kj - qi - diag = lim + kr - 8k - e
                     const int lim = kb - (m0 + c0 + diag) - 2 * q4;
+                    const int lim_hi = lim - whi, lim_lo = lim + wlo;
+                    const float flim = (float)lim;
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         uint32_t pk[8];
@@ -823,11 +860,22 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                                     f2_pack(__uint_as_float(sr[h][4 * k + 2 * r]),
                                             __uint_as_float(sr[h][4 * k + 2 * r + 1])),
                                     sc2, nl2[k]));
-                                float pv0 = ex2(x.x);
-                                float pv1 = ex2(x.y);
-                                if (masked) {
-                                    if (lim + kr > 8 * k) pv0 = 0.f;
-                                    if (lim + kr > 8 * k + 1) pv1 = 0.f;
+                                float x0 = x.x, x1 = x.y;
+                                if (kExt) {
+                                    // -slope * |qi + diag - kj|
+                                    const float fd = flim + (float)(kr - 8 * k);
+                                    x0 = fmaf(-slope2, fabsf(fd), x0);
+                                    x1 = fmaf(-slope2, fabsf(fd - 1.f), x1);
+                                }
+                                float pv0 = ex2(x0);
+                                float pv1 = ex2(x1);
+                                if (masked_hi) {   // lim + kr - 8k - e > whi
+                                    if (lim_hi + kr > 8 * k) pv0 = 0.f;
+                                    if (lim_hi + kr > 8 * k + 1) pv1 = 0.f;
+                                }
+                                if (kExt && masked_lo) {   // lim + kr - 8k - e < -wlo
+                                    if (lim_lo + kr < 8 * k) pv0 = 0.f;
+                                    if (lim_lo + kr < 8 * k + 1) pv1 = 0.f;
                                 }
                                 if (kb + kr >= u.lk) { pv0 = 0.f; pv1 = 0.f; }
                                 P[32 * ch + 16 * h + 4 * k + 2 * r] = pv0;
@@ -967,7 +1015,8 @@ template <int kD, typename T>
 static cudaError_t launch_main_t(const BwdParams &p, const MainMaps &maps, int grid,
                                  cudaStream_t stream) {
     using C = MainCfg<kD, T>;
-    auto kern = bwd_main_kernel<kD, T>;
+    const bool ext = p.alibi != nullptr || p.win_lo < kNoWindow;
+    auto kern = ext ? bwd_main_kernel<kD, T, true> : bwd_main_kernel<kD, T, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;

@@ -17,6 +17,8 @@
 //
 // Warps: 0 TMA producer (Q once, K/V blocks through a stage ring), 1 MMA
 // issuer, 4-7 softmax (thread = query row of its TMEM lane quarter), 2-3 idle.
+#include <type_traits>
+
 #include "fa_device.cuh"
 #include "fa_params.h"
 
@@ -68,7 +70,8 @@ enum {
 // that may lag the true one by up to this much.
 constexpr float kRescaleLog2 = 8.f;
 
-template <int kD, typename T>
+// kAlibi: the scores carry the ALiBi bias (p.alibi).
+template <int kD, typename T, bool kAlibi>
 __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap map_q,
                   const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
@@ -80,13 +83,15 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
     const int m = nmb - 1 - blockIdx.x / (p.B * p.Hq);
     const int b = bh / p.Hq, h = bh - b * p.Hq, hk = h / p.G;
     const int q0 = p.varlen ? p.cu_q[b] : 0, k0 = p.varlen ? p.cu_k[b] : 0;
-    const int lq = p.varlen ? p.cu_q[b + 1] - q0 : p.Sq;
-    const int lk = p.varlen ? p.cu_k[b + 1] - k0 : p.Sk;
+    const int lq = used_len_q(p, b), lk = used_len_k(p, b);
     if (m * BM >= lq) return;                       // uniform: the whole CTA leaves
-    const int diag = lk - lq;                       // key j visible to query i iff j <= i + diag
-    int last_key = lk - 1;
-    if (p.causal) last_key = min(last_key, m * BM + BM - 1 + diag);
-    const int n_end = last_key < 0 ? 0 : last_key / BN + 1;   // key blocks [0, n_end)
+    // key j is visible to query i iff -win_lo <= j - i - diag <= win_hi, j < lk
+    const int diag = lk - lq;
+    const long long first_key = max(0LL, (long long)m * BM + diag - p.win_lo);
+    const long long last_key = min((long long)lk - 1, (long long)m * BM + BM - 1 + diag + p.win_hi);
+    // key blocks [n_begin, n_begin + nblk) hold every key some row of the tile sees
+    const int n_begin = (int)(first_key / BN);
+    const int nblk = last_key < first_key ? 0 : (int)(last_key / BN) + 1 - n_begin;
     const int bidx = p.varlen ? 0 : b;
 
     extern __shared__ uint8_t smem_raw[];
@@ -131,14 +136,14 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0 && n_end > 0) {
+        if (lane == 0 && nblk > 0) {
             mbar_arrive_expect_tx(bar(F_Q_FULL), C::Q_BYTES);
 #pragma unroll
             for (int hh = 0; hh < D / 64; ++hh)
                 tma_load_4d(sbase + C::OFF_Q + hh * BM * 128, &map_q, bar(F_Q_FULL), hh * 64, h,
                             q0 + m * BM, bidx);
             uint32_t empty_ph = 0;
-            for (int n = 0; n < n_end; ++n) {
+            for (int n = 0; n < nblk; ++n) {
                 const int st = n % S;
                 if (n >= S) {
                     if (!mbar_wait(bar(C::kv_empty(st)), empty_ph >> st & 1u, w)) break;
@@ -149,17 +154,17 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
 #pragma unroll
                 for (int hh = 0; hh < D / 64; ++hh) {
                     tma_load_4d(sbase + C::OFF_K + st * C::KV_BYTES + hh * BN * 128, &map_k, full,
-                                hh * 64, hk, k0 + n * BN, bidx);
+                                hh * 64, hk, k0 + (n_begin + n) * BN, bidx);
                     tma_load_4d(sbase + C::OFF_V + st * C::KV_BYTES + hh * BN * 128, &map_v, full,
-                                hh * 64, hk, k0 + n * BN, bidx);
+                                hh * 64, hk, k0 + (n_begin + n) * BN, bidx);
                 }
             }
         }
     } else if (warp == 1) {
         // ----------------------------------------------------------- MMA issuer
         // S of block n is issued before O += P V of block n-1, so it runs while
-        // the softmax warps work on block n-1.
-        if (n_end > 0) {
+        // the softmax warps work on block n-1 (n counts the tile's blocks from 0).
+        if (nblk > 0) {
             bool ok = mbar_wait_warp(bar(F_Q_FULL), 0, w);
             uint32_t full_ph = 0;
             const uint64_t dQ_k = sw128_desc(sbase + C::OFF_Q, 16, 1024);
@@ -178,7 +183,7 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                 mma_commit_warp(bar(C::kv_empty(st)));
                 return true;
             };
-            for (int n = 0; ok && n < n_end; ++n) {
+            for (int n = 0; ok && n < nblk; ++n) {
                 const int bb = n & 1, st = n % S;
                 if (!(ok = mbar_wait_warp(bar(F_KV_FULL + st), full_ph >> st & 1u, w))) break;
                 full_ph ^= 1u << st;
@@ -197,7 +202,7 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                 mma_commit_warp(bar(F_S_FULL + bb));
                 if (n >= 1 && !(ok = issue_pv(n - 1))) break;
             }
-            if (ok && issue_pv(n_end - 1)) mma_commit_warp(bar(F_O_FINAL));
+            if (ok && issue_pv(nblk - 1)) mma_commit_warp(bar(F_O_FINAL));
             // make sure no MMA is still running before tensor memory is freed
             mma_commit_warp(bar(F_Q_FULL));
             mbar_wait_warp(bar(F_Q_FULL), 1, w);
@@ -208,53 +213,88 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
         const int r = quarter * 32 + lane;          // query row of the tile
         const int qi = m * BM + r;                  // query index within the sequence
         const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-        // keys [0, kmax] are visible to this row (kmax < 0: none)
-        const int kmax = p.causal ? min(lk - 1, qi + diag) : lk - 1;
+        // keys [kmin, kmax] are visible to this row (none if kmax < kmin)
+        const int kmin = (int)max(0LL, (long long)qi + diag - p.win_lo);
+        const int kmax = (int)min((long long)lk - 1, (long long)qi + diag + p.win_hi);
+        // ALiBi slope of this head, log2 units
+        const float slope2 =
+            kAlibi ? __ldg(p.alibi + (long long)b * p.alibi_bstride + h) * 1.4426950408889634f : 0.f;
         float m_run = -INFINITY, l_run = 0.f;       // running max (log2 units), row sum
         bool ok = true;
-        for (int n = 0; n < n_end; ++n) {
+        for (int n = 0; n < nblk; ++n) {
             const int bb = n & 1;
             if (!(ok = mbar_wait_warp(bar(F_S_FULL + bb), (uint32_t)(n >> 1) & 1u, w))) break;
             tc_fence_after();
             const uint32_t scol = lane_addr + C::TM_S + bb * BN;
-            const int kb = n * BN;
-            // pass 1: row maximum of the block
-            float mx = -INFINITY;
+            const int kb = (n_begin + n) * BN;
+            // element e of the block (key kb + e) is visible iff lo <= e <= hi
+            const int lo = kmin - kb, hi = kmax - kb;
+            // ALiBi: key kb + e lies (kb + e) - (qi + diag) = fbase + e from the diagonal
+            const float fbase = (float)(kb - qi - diag);
+            // scaled score of element e, log2 units
+            auto score2 = [&](uint32_t raw, int e) __attribute__((always_inline)) -> float {
+                float x = __uint_as_float(raw) * p.scale_log2;
+                if (kAlibi) x = fmaf(-slope2, fabsf(fbase + (float)e), x);
+                return x;
+            };
+            // Blocks inside every row's band (all but the edge blocks) take the
+            // pass without per-element tests.
+            const bool edge = __any_sync(0xffffffffu, lo > 0 || hi < BN - 1);
+            float alpha = 1.f, sum = 0.f, m_use = m_run;
+            auto block_pass = [&](auto mask_tag) __attribute__((always_inline)) {
+                constexpr bool kMask = decltype(mask_tag)::value;
+                // pass 1: row maximum of the block (without ALiBi the maximum of
+                // the raw scores, scaled once: the scale is positive)
+                float mx = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t sr[32];
-                tmem_ld32(scol + 32 * c, sr);
-                tmem_wait_ld();
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t sr[32];
+                    tmem_ld32(scol + 32 * c, sr);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float s2 = __uint_as_float(sr[i]) * p.scale_log2;
-                    mx = (kb + 32 * c + i <= kmax) ? fmaxf(mx, s2) : mx;
+                    for (int i = 0; i < 32; ++i) {
+                        const int e = 32 * c + i;
+                        const float x = kAlibi ? score2(sr[i], e) : __uint_as_float(sr[i]);
+                        mx = (!kMask || (e >= lo && e <= hi)) ? fmaxf(mx, x) : mx;
+                    }
                 }
-            }
-            const float m_new = fmaxf(m_run, mx);
-            const float m_use = (m_run == -INFINITY || m_new > m_run + kRescaleLog2) ? m_new : m_run;
-            const float alpha = (m_use == m_run) ? 1.f : ex2(m_run - m_use);
-            const float mref = (m_use == -INFINITY) ? 0.f : m_use;
-            // pass 2: P = exp2(s2 - m) into the first BN/2 columns as pairs;
-            // column j/2 of the buffer holds keys j, j+1 (every S column is
-            // read before a P pair lands on it)
-            float sum = 0.f;
+                if (!kAlibi) mx *= p.scale_log2;
+                const float m_new = fmaxf(m_run, mx);
+                m_use = (m_run == -INFINITY || m_new > m_run + kRescaleLog2) ? m_new : m_run;
+                alpha = (m_use == m_run) ? 1.f : ex2(m_run - m_use);
+                const float mref = (m_use == -INFINITY) ? 0.f : m_use;
+                // pass 2: P = exp2(s2 - m) into the first BN/2 columns as pairs;
+                // column j/2 of the buffer holds keys j, j+1 (every S column is
+                // read before a P pair lands on it)
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t sr[32];
-                tmem_ld32(scol + 32 * c, sr);
-                tmem_wait_ld();
-                uint32_t pk[16];
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t sr[32];
+                    tmem_ld32(scol + 32 * c, sr);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int j = kb + 32 * c + 2 * i;
-                    const float p0 = (j <= kmax) ? ex2(fmaf(__uint_as_float(sr[2 * i]), p.scale_log2, -mref)) : 0.f;
-                    const float p1 = (j + 1 <= kmax) ? ex2(fmaf(__uint_as_float(sr[2 * i + 1]), p.scale_log2, -mref)) : 0.f;
-                    sum += p0 + p1;
-                    pk[i] = Cvt<T>::pack(p0, p1);
+                    for (int i = 0; i < 16; ++i) {
+                        const int e = 32 * c + 2 * i;
+                        float p0, p1;
+                        if (kAlibi) {
+                            p0 = ex2(score2(sr[2 * i], e) - mref);
+                            p1 = ex2(score2(sr[2 * i + 1], e + 1) - mref);
+                        } else {
+                            p0 = ex2(fmaf(__uint_as_float(sr[2 * i]), p.scale_log2, -mref));
+                            p1 = ex2(fmaf(__uint_as_float(sr[2 * i + 1]), p.scale_log2, -mref));
+                        }
+                        if (kMask) {
+                            p0 = (e >= lo && e <= hi) ? p0 : 0.f;
+                            p1 = (e + 1 >= lo && e + 1 <= hi) ? p1 : 0.f;
+                        }
+                        sum += p0 + p1;
+                        pk[i] = Cvt<T>::pack(p0, p1);
+                    }
+                    tmem_st16(scol + 16 * c, pk);
                 }
-                tmem_st16(scol + 16 * c, pk);
-            }
+            };
+            if (edge) block_pass(std::true_type{});
+            else block_pass(std::false_type{});
             l_run = l_run * alpha + sum;
             m_run = m_use;
             // O holds blocks < n: rescale it when a row's maximum moved
@@ -285,7 +325,7 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
         // ---------------------------------------------------------- epilogue
         // O = acc / l, LSE = (m + log2 l) ln 2; a row that sees no key gets
         // O = 0 and LSE = -inf
-        if (ok && n_end > 0) {
+        if (ok && nblk > 0) {
             ok = mbar_wait_warp(bar(F_O_FINAL), 0, w);
             tc_fence_after();
         }
@@ -302,7 +342,7 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t orr[32];
-                if (n_end > 0) {
+                if (nblk > 0) {
                     tmem_ld32(lane_addr + C::TM_O + 32 * c, orr);
                     tmem_wait_ld();
                 } else {
@@ -335,7 +375,7 @@ cudaError_t launch_fwd_tc_t(const BwdParams &p, const CUtensorMap &mq, const CUt
                             const CUtensorMap &mv, void *o, float *lse, int max_lq,
                             cudaStream_t stream) {
     using C = FwdCfg<kD, T>;
-    auto kern = fwd_tc_kernel<kD, T>;
+    auto kern = p.alibi ? fwd_tc_kernel<kD, T, true> : fwd_tc_kernel<kD, T, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;

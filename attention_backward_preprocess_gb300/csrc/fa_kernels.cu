@@ -10,12 +10,9 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-__device__ __forceinline__ int seq_len_q(const BwdParams &p, int b) {
-    return p.varlen ? p.cu_q[b + 1] - p.cu_q[b] : p.Sq;
-}
-__device__ __forceinline__ int seq_len_k(const BwdParams &p, int b) {
-    return p.varlen ? p.cu_k[b + 1] - p.cu_k[b] : p.Sk;
-}
+// lengths the attention uses (seqused, when given, else the stored ones)
+__device__ __forceinline__ int seq_len_q(const BwdParams &p, int b) { return used_len_q(p, b); }
+__device__ __forceinline__ int seq_len_k(const BwdParams &p, int b) { return used_len_k(p, b); }
 
 // ------------------------------------------------------------------ schedule
 // Work units in the order (n_block, sequence, kv head): every unit of a given

@@ -8,6 +8,7 @@ namespace fa {
 
 constexpr int kRowTile = 128;   // workspace rows are padded per (sequence, head) to this
 constexpr int kBlockN = 128;    // keys per work unit of the main kernel
+constexpr int kNoWindow = 1 << 30;   // an unbounded side of the visible band
 
 struct BwdParams {
     // tensors (public layouts, see fa.h)
@@ -19,6 +20,17 @@ struct BwdParams {
     float scale_log2;   // c * log2(e)
     int causal, deterministic, varlen;
     const int *cu_q, *cu_k;
+    // Visible band: key j is visible to query i iff j < Lk and
+    // -win_lo <= j - i - (Lk - Lq) <= win_hi (kNoWindow: unbounded; a causal
+    // mask makes win_hi <= 0).
+    int win_lo, win_hi;
+    // ALiBi: slope alibi[b * alibi_bstride + h] (natural-log units), the score
+    // gets -slope * |i + (Lk - Lq) - j|; null: none
+    const float *alibi;
+    int alibi_bstride;
+    // used lengths per sequence (null: the stored lengths); clamped to
+    // [0, stored length]
+    const int *seqused_q, *seqused_k;
     // workspace
     int *err;           // device error word
     int4 *tiles;        // work units (b, n_block, hk, 0)
@@ -38,6 +50,16 @@ struct BwdParams {
     int sq_round;       // round_up(Sq, 128)
     long long budget_ns;      // bound of every device-side wait
 };
+
+// Rows of sequence b the attention uses (query / key side).
+__device__ __forceinline__ int used_len_q(const BwdParams &p, int b) {
+    const int stored = p.varlen ? p.cu_q[b + 1] - p.cu_q[b] : p.Sq;
+    return p.seqused_q ? min(max(p.seqused_q[b], 0), stored) : stored;
+}
+__device__ __forceinline__ int used_len_k(const BwdParams &p, int b) {
+    const int stored = p.varlen ? p.cu_k[b + 1] - p.cu_k[b] : p.Sk;
+    return p.seqused_k ? min(max(p.seqused_k[b], 0), stored) : stored;
+}
 
 // Workspace row of (sequence b, query head h, position s).
 __device__ __forceinline__ long long ws_row(const BwdParams &p, int b, int h, int s) {

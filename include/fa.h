@@ -136,6 +136,55 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
                  const int *cu_seqlens_q, const int *cu_seqlens_k, fa_dtype dtype,
                  cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Extensions: a local window, ALiBi and used lengths.  They do not appear in
+ * the five benchmark workloads; fa_fwd_ext / fa_bwd_ext take them through one
+ * struct (NULL = none, which equals fa_fwd / fa_bwd).
+ *
+ * window_left / window_right (-1 = unbounded on that side): key j stays
+ *   visible to query i only if i + (Lk - Lq) - window_left <= j <= i + (Lk -
+ *   Lq) + window_right, a band around the same bottom-right diagonal as the
+ *   causal mask (the Composable Kernel page masks with a generic
+ *   mask.IsOutOfBound(row, col); this band is the reading taken).  causal
+ *   != 0 intersects it with j <= i + (Lk - Lq).
+ * alibi_slopes: device fp32, [Hq] (alibi_batch_stride 0) or [B, Hq]
+ *   (alibi_batch_stride Hq); the score of (i, j) in head h of sequence b
+ *   becomes scale * <q_i, k_j> - slope * |i + (Lk - Lq) - j| (the ALIBI bias
+ *   kind of the Composable Kernel page, added after the scale).  LSE includes
+ *   the bias; fa_bwd_ext must get the same slopes as the forward.
+ * seqused_q / seqused_k: device int32 [B] (SeqlenInfo's seqused on the
+ *   FlashAttention pages): sequence b uses its first seqused_q[b] query rows
+ *   and seqused_k[b] key rows (values are clamped to [0, stored length]);
+ *   Lq / Lk above are these used lengths.  Rows past them are neither read
+ *   nor written (o, lse, dq, dk, dv keep what they held).
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    int window_left;
+    int window_right;
+    const float *alibi_slopes;
+    int alibi_batch_stride;
+    const int *seqused_q;
+    const int *seqused_k;
+} fa_ext;
+
+/* fa_fwd with extensions.  Errors as fa_fwd, plus FA_ERR_INVALID_ARG for a
+ * window side below -1, an ALiBi stride other than 0 / Hq, or a slope or
+ * seqused pointer not 4-byte aligned. */
+fa_status fa_fwd_ext(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                     int Sq, int Sk, int Hq, int Hkv, int D, float softmax_scale, int causal,
+                     const int *cu_seqlens_q, const int *cu_seqlens_k, const fa_ext *ext,
+                     fa_dtype dtype, cudaStream_t stream);
+
+/* fa_bwd with extensions.  workspace NULL: the library's own (as fa_bwd);
+ * otherwise a caller workspace as for fa_bwd_with_workspace (the extensions
+ * do not change its size). */
+fa_status fa_bwd_ext(const void *q, const void *k, const void *v, const void *o,
+                     const void *dout, const float *lse, void *dq, void *dk, void *dv, int B,
+                     int Sq, int Sk, int Hq, int Hkv, int D, float softmax_scale, int causal,
+                     const int *cu_seqlens_q, const int *cu_seqlens_k, const fa_ext *ext,
+                     int deterministic, fa_dtype dtype, void *workspace, size_t workspace_bytes,
+                     cudaStream_t stream);
+
 /* Synchronises `stream`, then returns and clears the device error word of
  * this device's library workspace (FA_OK or FA_ERR_TIMEOUT).  For a caller
  * workspace, pass it; NULL means the library's own. */
