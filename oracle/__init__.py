@@ -18,7 +18,9 @@ Every function also takes the optional extensions as keywords:
 ``window=(left, right)`` (a local band around the bottom-right diagonal, -1 =
 unbounded on that side), ``alibi`` (slopes ``[Hq]`` or ``[B, Hq]``) and
 ``seqused_q`` / ``seqused_k`` (used lengths per sequence; rows past them are
-neither read nor written, and come back as zeros).
+neither read nor written, and come back as zeros) and ``bias`` (an elementwise
+additive bias ``[B or 1, Hq or 1, Sq, Sk]``, dense only; its gradient dBias =
+dS comes from ``head_matrices``).
 
 Parity status: every function here is pinned by ``tests/test_oracle.py``
 (central finite differences, invariants, a hand-derived 2x2 example, closed
@@ -77,12 +79,18 @@ class _Ext(ctypes.Structure):
     _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
                 ("alibi", ctypes.POINTER(ctypes.c_double)), ("alibi_bstride", ctypes.c_int),
                 ("seqused_q", ctypes.POINTER(ctypes.c_int)),
-                ("seqused_k", ctypes.POINTER(ctypes.c_int))]
+                ("seqused_k", ctypes.POINTER(ctypes.c_int)),
+                ("bias", ctypes.POINTER(ctypes.c_double)), ("bias_bs", ctypes.c_long),
+                ("bias_hs", ctypes.c_long), ("bias_rs", ctypes.c_long)]
 
 
-def _ext(B, Hq, window=None, alibi=None, seqused_q=None, seqused_k=None):
-    """(ctypes pointer or None, arrays to keep alive) for the extension options."""
-    if window is None and alibi is None and seqused_q is None and seqused_k is None:
+def _ext(B, Hq, window=None, alibi=None, seqused_q=None, seqused_k=None, bias=None):
+    """(ctypes pointer or None, arrays to keep alive) for the extension options.
+
+    ``bias`` is a [B or 1, Hq or 1, Sq, Sk] array (dense problems); a size-1
+    batch or head axis is broadcast."""
+    if (window is None and alibi is None and seqused_q is None and seqused_k is None
+            and bias is None):
         return None, ()
     wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
     keep = []
@@ -93,6 +101,15 @@ def _ext(B, Hq, window=None, alibi=None, seqused_q=None, seqused_k=None):
             raise ValueError("alibi slopes are [Hq] or [B, Hq]")
         e.alibi = _ptr(a)
         e.alibi_bstride = Hq if a.ndim == 2 else 0
+        keep.append(a)
+    if bias is not None:
+        a = np.ascontiguousarray(bias, dtype=np.float64)
+        if a.ndim != 4 or a.shape[0] not in (1, B) or a.shape[1] not in (1, Hq):
+            raise ValueError("bias is [B or 1, Hq or 1, Sq, Sk]")
+        e.bias = _ptr(a)
+        e.bias_bs = 0 if a.shape[0] == 1 else a.shape[1] * a.shape[2] * a.shape[3]
+        e.bias_hs = 0 if a.shape[1] == 1 else a.shape[2] * a.shape[3]
+        e.bias_rs = a.shape[3]
         keep.append(a)
     for name, arr in (("seqused_q", seqused_q), ("seqused_k", seqused_k)):
         if arr is not None:

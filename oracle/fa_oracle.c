@@ -24,6 +24,10 @@
  *   ALiBi  : optional per-head slope m_h (the ALIBI bias kind of the
  *            Composable Kernel page, STAGE 2, added after the scale; the
  *            page does not print the encoding): s_ij -= m_h |i + (Lk - Lq) - j|
+ *   bias   : optional elementwise bias (the ELEMENTWISE_BIAS kind of the
+ *            Composable Kernel page, STAGE 2: added to the scaled score in
+ *            natural-log units): s_ij += bias[b, h, i, j]; its gradient is
+ *            dBias_ij = dS_ij (STAGE 5, the dbias tile is the cast ds tile)
  *   seqused: optional per-sequence used lengths (seqused of SeqlenInfo in the
  *            FlashAttention pages): Lq = seqused_q[b], Lk = seqused_k[b]; the
  *            rows keep their places, rows past the used length are neither
@@ -71,6 +75,8 @@ typedef struct {
     const double *alibi;            /* slopes, alibi[b * alibi_bstride + h]; NULL: none */
     int alibi_bstride;
     const int *seqused_q, *seqused_k;  /* [B]; NULL: the full lengths */
+    const double *bias;             /* bias[b * bias_bs + h * bias_hs + i * bias_rs + j]; NULL: none */
+    long bias_bs, bias_hs, bias_rs;
 } oracle_ext_t;
 
 typedef struct {
@@ -132,6 +138,9 @@ static double score(const prob_t *p, int b, int h, int i, int j) {
         int dist = i + (seq_len_k(p, b) - seq_len_q(p, b)) - j;
         s -= slope * (double)(dist < 0 ? -dist : dist);
     }
+    if (p->ext.bias)
+        s += p->ext.bias[(long)b * p->ext.bias_bs + (long)h * p->ext.bias_hs +
+                         (long)i * p->ext.bias_rs + j];
     return s;
 }
 

@@ -17,7 +17,10 @@ AssertionError when the oracle disagrees with:
   a local window row by row == the unmasked problem on the keys inside the
   band; causal ALiBi == plain causal attention with one extra head-dimension
   column (q gets slope / scale, k gets the key position); seqused == the
-  problem cut to the used rows; a (0, 0) window in closed form.
+  problem cut to the used rows; a (0, 0) window in closed form; a bias
+  constant along the keys shifts only LSE; a bias constant along the queries
+  is one more head-dimension column again; a bias equal to the ALiBi terms
+  equals ALiBi; dBias = dS is the gradient of L by finite differences.
 
 ``tests/test_oracle.py`` runs every pin on the real oracle and also on
 mutant builds with a planted mistake, each of which must fail at least one
@@ -456,7 +459,103 @@ def pin_seqused_equals_cut(orc):
         _close(lse[:, a:a + uq[b]], l1[0], 1e-14, "varlen seqused LSE")
 
 
+def pin_bias_key_column_equals_augmented(orc):
+    """bias_ij = u_j (per head): plain attention on q' = [q, 1/scale],
+    k' = [k, u_j], v' = [v, 0], dO' = [dO, 0] (G = 1 so k' is per head);
+    the column sums of dBias = dS are dK'[:, D] (= sum_i dS_ij)."""
+    rng = _rng(70)
+    for causal, (Sq, Sk) in ((False, (9, 13)), (True, (12, 12)), (True, (7, 11))):
+        B, H, D, sc = 2, 2, 3, 0.45
+        q, k, v, do = _dense(rng, B, Sq, Sk, H, H, D)
+        u = rng.standard_normal((B, H, Sk))
+        bias = np.broadcast_to(u[:, :, None, :], (B, H, Sq, Sk)).copy()
+        o, lse = orc.forward(q, k, v, sc, causal, bias=bias)
+        dq, dk, dv = orc.backward(q, k, v, do, sc, causal, bias=bias)
+        qa = np.concatenate([q, np.full((B, Sq, H, 1), 1.0 / sc)], 3)
+        ka = np.concatenate([k, u.transpose(0, 2, 1)[..., None]], 3)
+        va = np.concatenate([v, np.zeros((B, Sk, H, 1))], 3)
+        da = np.concatenate([do, np.zeros((B, Sq, H, 1))], 3)
+        oa, la = orc.forward(qa, ka, va, sc, causal)
+        dqa, dka, dva = orc.backward(qa, ka, va, da, sc, causal)
+        _close(o, oa[..., :D], 1e-13, "key bias O")
+        _close(lse, la, 1e-13, "key bias LSE")
+        _close(dq, dqa[..., :D], 1e-12, "key bias dQ")
+        _close(dk, dka[..., :D], 1e-12, "key bias dK")
+        _close(dv, dva[..., :D], 1e-12, "key bias dV")
+        for b in range(B):
+            for h in range(H):
+                _, dS = orc.head_matrices(q, k, v, do, sc, causal, b=b, h=h, bias=bias)
+                _close(dS.sum(0), dka[b, :, h, D], 1e-12, "column sums of dBias")
+
+
+def pin_bias_query_row_shifts_lse(orc):
+    """bias_ij = c_i (constant along the keys) leaves P, O and the gradients
+    unchanged and adds c_i to LSE; a [1, Hq, ...] bias broadcasts over the batch."""
+    rng = _rng(71)
+    q, k, v, do = _dense(rng, 2, 10, 14, 4, 2, 3)
+    c = rng.standard_normal((1, 4, 10))
+    bias = np.broadcast_to(c[..., None], (1, 4, 10, 14)).copy()
+    for causal in (False, True):
+        o, lse = orc.forward(q, k, v, 0.6, causal, bias=bias)
+        op, lp = orc.forward(q, k, v, 0.6, causal)
+        _close(o, op, 1e-13, "row bias O")
+        fin = np.isfinite(lp)
+        _close(lse[fin], (lp + c)[fin], 1e-13, "row bias LSE")
+        g = orc.backward(q, k, v, do, 0.6, causal, bias=bias)
+        gp = orc.backward(q, k, v, do, 0.6, causal)
+        for a, b_, n in zip(g, gp, ("dQ", "dK", "dV")):
+            _close(a, b_, 1e-12, "row bias " + n)
+
+
+def pin_bias_equals_alibi(orc):
+    """A bias holding -slope_h |i + (Lk - Lq) - j| gives what the ALiBi option
+    gives (forward and backward), and a [B, Hq] bias stack equals the batch
+    broadcast of a [1, Hq] one where the sequences' biases agree."""
+    rng = _rng(72)
+    for causal, (Sq, Sk) in ((False, (8, 12)), (True, (12, 9))):
+        q, k, v, do = _dense(rng, 2, Sq, Sk, 2, 1, 4)
+        sl = np.array([0.3, 0.8])
+        i = np.arange(Sq)[:, None] + (Sk - Sq)
+        j = np.arange(Sk)[None, :]
+        bias1 = (-sl[:, None, None] * np.abs(i - j)[None])[None]
+        bias2 = np.concatenate([bias1, bias1], 0)
+        ref = orc.forward(q, k, v, 0.5, causal, alibi=sl)
+        gref = orc.backward(q, k, v, do, 0.5, causal, alibi=sl)
+        for bias in (bias1, bias2):
+            o, lse = orc.forward(q, k, v, 0.5, causal, bias=bias)
+            _close(o, ref[0], 1e-13, "bias == ALiBi O")
+            fin = np.isfinite(ref[1])
+            _close(lse[fin], ref[1][fin], 1e-13, "bias == ALiBi LSE")
+            for a, b_, n in zip(orc.backward(q, k, v, do, 0.5, causal, bias=bias), gref,
+                                ("dQ", "dK", "dV")):
+                _close(a, b_, 1e-12, "bias == ALiBi " + n)
+
+
+def pin_fd_bias(orc):
+    """dBias = dS (head_matrices) equals central differences of L = sum(dO * O)
+    in each bias entry; dQ, dK, dV with a bias are the gradients of its forward."""
+    rng = _rng(73)
+    q, k, v, do = _dense(rng, 1, 5, 6, 2, 1, 3)
+    bias = rng.standard_normal((1, 2, 5, 6))
+    for causal in (False, True):
+        h = 1e-6
+        num = np.zeros_like(bias)
+        for idx in np.ndindex(bias.shape):
+            bp, bm = bias.copy(), bias.copy()
+            bp[idx] += h
+            bm[idx] -= h
+            lp = np.sum(do * orc.forward(q, k, v, 0.7, causal, nthreads=1, bias=bp)[0])
+            lm = np.sum(do * orc.forward(q, k, v, 0.7, causal, nthreads=1, bias=bm)[0])
+            num[idx] = (lp - lm) / (2 * h)
+        for hh in range(2):
+            _, dS = orc.head_matrices(q, k, v, do, 0.7, causal, h=hh, bias=bias)
+            _close(dS, num[0, hh], 2e-7, "dBias by finite differences")
+        _fd_check(orc, q, k, v, do, 0.7, causal, bias=bias)
+
+
 ALL_PINS = [pin_preprocess_identity, pin_window_rows_equal_unmasked_band,
+    pin_bias_key_column_equals_augmented, pin_bias_query_row_shifts_lse, pin_bias_equals_alibi,
+    pin_fd_bias,
     pin_window_zero_closed_form, pin_fd_window, pin_alibi_causal_equals_augmented,
     pin_alibi_noncausal, pin_seqused_equals_cut,
     pin_worked_example, pin_fd_dense, pin_fd_causal, pin_fd_causal_rect, pin_fd_gqa,

@@ -78,6 +78,10 @@ MUTANTS = {
                                        "p->ext.alibi[h]"),
     "seqused_k ignored": ("return p->ext.seqused_k ? p->ext.seqused_k[b] : stored_len_k(p, b);",
                           "return stored_len_k(p, b);"),
+    "bias sign": ("s += p->ext.bias[", "s -= p->ext.bias["),
+    "bias transposed": ("(long)i * p->ext.bias_rs + j];", "(long)j * p->ext.bias_rs + i];"),
+    "bias ignores the head stride": ("(long)h * p->ext.bias_hs +", "0 +"),
+    "bias scaled": ("        s += p->ext.bias[", "        s += p->scale * p->ext.bias["),
     "seqused_q ignored": ("return p->ext.seqused_q ? p->ext.seqused_q[b] : stored_len_q(p, b);",
                           "return stored_len_q(p, b);"),
     "Dv from q": ("return dot(doi, o_scratch, p->D);", "return dot(doi, p->q + row_q(p, b, i, h), p->D);"),
