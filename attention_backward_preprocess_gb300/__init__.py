@@ -52,14 +52,23 @@ class FaExt(ctypes.Structure):
     """fa_ext of include/fa.h: local window, ALiBi slopes, used lengths."""
     _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
                 ("alibi_slopes", ctypes.c_void_p), ("alibi_batch_stride", ctypes.c_int),
-                ("seqused_q", ctypes.c_void_p), ("seqused_k", ctypes.c_void_p)]
+                ("seqused_q", ctypes.c_void_p), ("seqused_k", ctypes.c_void_p),
+                ("bias", ctypes.c_void_p), ("bias_batch_stride", ctypes.c_longlong),
+                ("bias_head_stride", ctypes.c_longlong), ("bias_row_stride", ctypes.c_longlong),
+                ("dbias", ctypes.c_void_p)]
 
 
-def _ext(Hq, window=None, alibi_slopes=None, seqused_q=None, seqused_k=None):
-    """A pointer to an FaExt, or None when no extension is asked for."""
-    if window is None and alibi_slopes is None and seqused_q is None and seqused_k is None:
+def _ext(Hq, window=None, alibi_slopes=None, seqused_q=None, seqused_k=None, bias=None,
+         dbias=None):
+    """A pointer to an FaExt, or None when no extension is asked for.
+
+    ``bias``: [B or 1, Hq or 1, Sq, >= Sk] in the input dtype, last axis
+    contiguous (a size-1 batch / head axis broadcasts).  ``dbias``: a
+    contiguous [B, Hq, Sq, Sk] output of the input dtype (backward only)."""
+    if (window is None and alibi_slopes is None and seqused_q is None and seqused_k is None
+            and bias is None and dbias is None):
         return None
-    e = FaExt(-1, -1, None, 0, None, None)
+    e = FaExt(-1, -1, None, 0, None, None, None, 0, 0, 0, None)
     if window is not None:
         e.window_left, e.window_right = int(window[0]), int(window[1])
     if alibi_slopes is not None:
@@ -72,6 +81,17 @@ def _ext(Hq, window=None, alibi_slopes=None, seqused_q=None, seqused_k=None):
             if t.dtype != torch.int32 or not t.is_contiguous():
                 raise ValueError(name + ": contiguous int32 [B]")
             setattr(e, name, t.data_ptr())
+    if bias is not None:
+        if bias.dim() != 4 or bias.stride(3) != 1:
+            raise ValueError("bias: [B or 1, Hq or 1, Sq, Sk] with a contiguous last axis")
+        e.bias = bias.data_ptr()
+        e.bias_batch_stride = 0 if bias.shape[0] == 1 else bias.stride(0)
+        e.bias_head_stride = 0 if bias.shape[1] == 1 else bias.stride(1)
+        e.bias_row_stride = bias.stride(2)
+    if dbias is not None:
+        if not dbias.is_contiguous():
+            raise ValueError("dbias: a contiguous [B, Hq, Sq, Sk] tensor")
+        e.dbias = dbias.data_ptr()
     return ctypes.pointer(e)
 
 
@@ -167,12 +187,13 @@ def default_scale(D: int) -> float:
 
 def fa_fwd(q, k, v, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seqlens_k=None,
            max_seqlen_q=None, max_seqlen_k=None, stream=None, window=None, alibi_slopes=None,
-           seqused_q=None, seqused_k=None):
+           seqused_q=None, seqused_k=None, bias=None):
     """Forward pass: returns (o, lse); lse fp32 [B,Hq,Sq] or [Hq,total_q].
 
     ``window=(left, right)`` (-1 = unbounded side), ``alibi_slopes`` (fp32
-    [Hq] or [B, Hq]) and ``seqused_q`` / ``seqused_k`` (int32 [B]) select
-    fa_fwd_ext; rows past the used lengths are left as allocated.
+    [Hq] or [B, Hq]), ``seqused_q`` / ``seqused_k`` (int32 [B]) and ``bias``
+    (see ``_ext``) select fa_fwd_ext; rows past the used lengths are left as
+    allocated.
     """
     B, Sq, Sk, Hq, Hkv, D = _shape(q, k, cu_seqlens_q, max_seqlen_q, max_seqlen_k)
     scale = default_scale(D) if softmax_scale is None else float(softmax_scale)
@@ -181,7 +202,7 @@ def fa_fwd(q, k, v, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seql
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
     else:
         lse = torch.empty((Hq, q.shape[0]), dtype=torch.float32, device=q.device)
-    ext = _ext(Hq, window, alibi_slopes, seqused_q, seqused_k)
+    ext = _ext(Hq, window, alibi_slopes, seqused_q, seqused_k, bias)
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Sq, Sk, Hq, Hkv, D, scale,
             int(bool(causal)), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k)]
     if ext is None:
@@ -194,13 +215,14 @@ def fa_fwd(q, k, v, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seql
 def fa_bwd(q, k, v, o, dout, lse, causal=False, softmax_scale=None, cu_seqlens_q=None,
            cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, deterministic=False,
            dq=None, dk=None, dv=None, workspace=None, stream=None, window=None,
-           alibi_slopes=None, seqused_q=None, seqused_k=None):
+           alibi_slopes=None, seqused_q=None, seqused_k=None, bias=None, dbias=None):
     """Backward pass through the C ABI; returns (dq, dk, dv).
 
     Outputs are allocated when not given.  ``workspace`` (a uint8 CUDA tensor
     of at least ``workspace_bytes(...)``) selects fa_bwd_with_workspace,
     otherwise the library's own workspace is used.  The extension keywords
-    (as for fa_fwd) select fa_bwd_ext.
+    (as for fa_fwd, plus ``dbias``, an output tensor filled with dBias = dS)
+    select fa_bwd_ext.
     """
     B, Sq, Sk, Hq, Hkv, D = _shape(q, k, cu_seqlens_q, max_seqlen_q, max_seqlen_k)
     scale = default_scale(D) if softmax_scale is None else float(softmax_scale)
@@ -210,7 +232,7 @@ def fa_bwd(q, k, v, o, dout, lse, causal=False, softmax_scale=None, cu_seqlens_q
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
             _ptr(dv), B, Sq, Sk, Hq, Hkv, D, scale, int(bool(causal)), _ptr(cu_seqlens_q),
             _ptr(cu_seqlens_k), int(bool(deterministic)), _dtype_code(q)]
-    ext = _ext(Hq, window, alibi_slopes, seqused_q, seqused_k)
+    ext = _ext(Hq, window, alibi_slopes, seqused_q, seqused_k, bias, dbias)
     if ext is not None:
         st = lib().fa_bwd_ext(*args[:19], ext, *args[19:], _ptr(workspace),
                               0 if workspace is None else workspace.numel(), _stream(stream))

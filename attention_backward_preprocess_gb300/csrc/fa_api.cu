@@ -206,6 +206,9 @@ fa_status apply_ext(fa::BwdParams &p, int causal, const fa_ext *ext) {
     p.alibi = nullptr;
     p.alibi_bstride = 0;
     p.seqused_q = p.seqused_k = nullptr;
+    p.bias = nullptr;
+    p.bias_bs = p.bias_hs = p.bias_rs = 0;
+    p.dbias = nullptr;
     if (ext) {
         wl = ext->window_left;
         wr = ext->window_right;
@@ -222,6 +225,22 @@ fa_status apply_ext(fa::BwdParams &p, int causal, const fa_ext *ext) {
             return FA_ERR_INVALID_ARG;
         p.seqused_q = ext->seqused_q;
         p.seqused_k = ext->seqused_k;
+        if (ext->bias) {
+            if (p.varlen) return FA_ERR_UNSUPPORTED;
+            if (!aligned16(ext->bias) || ext->bias_batch_stride < 0 || ext->bias_head_stride < 0 ||
+                ext->bias_row_stride < p.Sk || (ext->bias_batch_stride & 7) ||
+                (ext->bias_head_stride & 7) || (ext->bias_row_stride & 7))
+                return FA_ERR_INVALID_ARG;
+            p.bias = ext->bias;
+            p.bias_bs = ext->bias_batch_stride;
+            p.bias_hs = ext->bias_head_stride;
+            p.bias_rs = ext->bias_row_stride;
+        }
+        if (ext->dbias) {
+            if (p.varlen) return FA_ERR_UNSUPPORTED;
+            if ((reinterpret_cast<uintptr_t>(ext->dbias) & 1u)) return FA_ERR_INVALID_ARG;
+            p.dbias = ext->dbias;
+        }
     }
     p.win_lo = (wl < 0 || wl >= fa::kNoWindow) ? fa::kNoWindow : wl;
     p.win_hi = (wr < 0 || wr >= fa::kNoWindow) ? fa::kNoWindow : wr;
@@ -459,6 +478,11 @@ fa_status fa_bwd_ext(const void *q, const void *k, const void *v, const void *o,
                  stream, &P, ext);
     if (st != FA_OK) return st;
     if ((st = run_preprocess(P, dtype, stream)) != FA_OK) return st;
+    if (P.p.dbias) {
+        // the main kernel writes dS of the tiles it visits; the rest is 0
+        const size_t n = (size_t)B * Hq * Sq * Sk * 2;
+        if (cudaMemsetAsync(P.p.dbias, 0, n, stream) != cudaSuccess) return FA_ERR_CUDA;
+    }
     if ((st = run_main(P, dtype, stream)) != FA_OK) return st;
     if ((st = run_postprocess(P, dtype, stream)) != FA_OK) return st;
     if (deterministic) return read_error_word(P.p.err, stream, false);

@@ -817,6 +817,19 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 if (kExt && p.alibi)
                     slope2 = __ldg(p.alibi + (long long)u.b * p.alibi_bstride + u.hk * p.G + u.g_of(it, p.G)) *
                              1.4426950408889634f;
+                // elementwise bias / dBias of the step's (sequence, query head)
+                // (dense problems): element (query qi, key kj) at qi * stride + kj
+                const T *bias_h = nullptr;
+                uint16_t *dbias_h = nullptr;
+                if (kExt) {
+                    const int hq = u.hk * p.G + u.g_of(it, p.G);
+                    if (p.bias)
+                        bias_h = reinterpret_cast<const T *>(p.bias) + (long long)u.b * p.bias_bs +
+                                 (long long)hq * p.bias_hs;
+                    if (p.dbias)
+                        dbias_h = reinterpret_cast<uint16_t *>(p.dbias) +
+                                  ((long long)u.b * p.Hq + hq) * p.Sq * p.Sk;
+                }
                 if (!(ok = mbar_wait(bar(B_STAGE0 + stage), st_ph, w))) break;
                 if (!(ok = mbar_wait(bar(B_S_FULL + cb), bit(s_ph, cb), w))) break;
                 s_ph ^= 1u << cb;
@@ -866,6 +879,17 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                                     const float fd = flim + (float)(kr - 8 * k);
                                     x0 = fmaf(-slope2, fabsf(fd), x0);
                                     x1 = fmaf(-slope2, fabsf(fd - 1.f), x1);
+                                    if (bias_h) {   // + bias * log2e (0 past the used lengths)
+                                        const int qi0 = m0 + c0 + 8 * k + 2 * q4, kj = kb + kr;
+                                        float b0 = 0.f, b1 = 0.f;
+                                        if (kj < u.lk) {
+                                            if (qi0 < u.lq) b0 = static_cast<float>(bias_h[(long long)qi0 * p.bias_rs + kj]);
+                                            if (qi0 + 1 < u.lq)
+                                                b1 = static_cast<float>(bias_h[(long long)(qi0 + 1) * p.bias_rs + kj]);
+                                        }
+                                        x0 = fmaf(b0, 1.4426950408889634f, x0);
+                                        x1 = fmaf(b1, 1.4426950408889634f, x1);
+                                    }
                                 }
                                 float pv0 = ex2(x0);
                                 float pv1 = ex2(x1);
@@ -931,6 +955,15 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                                                    __uint_as_float(dr[h][4 * k + 2 * r + 1])),
                                            dd[k])));
                                 pk[2 * k + r] = Cvt<T>::pack(ds.x, ds.y);
+                                if (kExt && dbias_h) {   // dBias = dS, inside the used lengths
+                                    const int qi0 = m0 + c0 + 8 * k + 2 * q4, kj = kb + 16 * h + 8 * r;
+                                    if (kj < u.lk) {
+                                        if (qi0 < u.lq)
+                                            dbias_h[(long long)qi0 * p.Sk + kj] = (uint16_t)(pk[2 * k + r] & 0xFFFFu);
+                                        if (qi0 + 1 < u.lq)
+                                            dbias_h[(long long)(qi0 + 1) * p.Sk + kj] = (uint16_t)(pk[2 * k + r] >> 16);
+                                    }
+                                }
                             }
                         }
                         tmem_st16x128(lane_addr + ((uint32_t)(16 * h) << 16) + C::ds_col(cb, grp, ch), pk);
@@ -1015,7 +1048,7 @@ template <int kD, typename T>
 static cudaError_t launch_main_t(const BwdParams &p, const MainMaps &maps, int grid,
                                  cudaStream_t stream) {
     using C = MainCfg<kD, T>;
-    const bool ext = p.alibi != nullptr || p.win_lo < kNoWindow;
+    const bool ext = p.alibi != nullptr || p.win_lo < kNoWindow || p.bias != nullptr || p.dbias != nullptr;
     auto kern = ext ? bwd_main_kernel<kD, T, true> : bwd_main_kernel<kD, T, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);

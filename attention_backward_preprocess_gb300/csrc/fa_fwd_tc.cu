@@ -70,8 +70,9 @@ enum {
 // that may lag the true one by up to this much.
 constexpr float kRescaleLog2 = 8.f;
 
-// kAlibi: the scores carry the ALiBi bias (p.alibi).
-template <int kD, typename T, bool kAlibi>
+// kExt: the scores carry the ALiBi bias (p.alibi) and / or the elementwise
+// bias (p.bias).
+template <int kD, typename T, bool kExt>
 __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap map_q,
                   const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
@@ -217,8 +218,37 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
         const int kmin = (int)max(0LL, (long long)qi + diag - p.win_lo);
         const int kmax = (int)min((long long)lk - 1, (long long)qi + diag + p.win_hi);
         // ALiBi slope of this head, log2 units
-        const float slope2 =
-            kAlibi ? __ldg(p.alibi + (long long)b * p.alibi_bstride + h) * 1.4426950408889634f : 0.f;
+        const float slope2 = (kExt && p.alibi)
+                                 ? __ldg(p.alibi + (long long)b * p.alibi_bstride + h) * 1.4426950408889634f
+                                 : 0.f;
+        // elementwise bias row of this query (null: none, or a padding row)
+        const T *brow = nullptr;
+        if (kExt && p.bias && qi < lq)
+            brow = reinterpret_cast<const T *>(p.bias) + (long long)b * p.bias_bs +
+                   (long long)h * p.bias_hs + (long long)qi * p.bias_rs;
+        // bias of keys k0 .. k0 + 31 in log2 units (0 past lk); 16-byte loads
+        // when the 32 keys are all in range (k0 is a multiple of 32, the row
+        // start 16-byte aligned)
+        auto load_bias = [&](float (&bl)[32], int k0) __attribute__((always_inline)) {
+            if (brow && k0 + 32 <= lk) {
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(brow + k0) + t);
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float2 f = Cvt<T>::unpack(w4[u]);
+                        bl[8 * t + 2 * u] = f.x * 1.4426950408889634f;
+                        bl[8 * t + 2 * u + 1] = f.y * 1.4426950408889634f;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    bl[i] = (brow && k0 + i < lk) ? static_cast<float>(brow[k0 + i]) * 1.4426950408889634f
+                                                  : 0.f;
+            }
+        };
         float m_run = -INFINITY, l_run = 0.f;       // running max (log2 units), row sum
         bool ok = true;
         for (int n = 0; n < nblk; ++n) {
@@ -231,10 +261,10 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
             const int lo = kmin - kb, hi = kmax - kb;
             // ALiBi: key kb + e lies (kb + e) - (qi + diag) = fbase + e from the diagonal
             const float fbase = (float)(kb - qi - diag);
-            // scaled score of element e, log2 units
-            auto score2 = [&](uint32_t raw, int e) __attribute__((always_inline)) -> float {
-                float x = __uint_as_float(raw) * p.scale_log2;
-                if (kAlibi) x = fmaf(-slope2, fabsf(fbase + (float)e), x);
+            // scaled score of element e with its bias (bl: bias * log2e), log2 units
+            auto score2 = [&](uint32_t raw, int e, float bl) __attribute__((always_inline)) -> float {
+                float x = fmaf(__uint_as_float(raw), p.scale_log2, bl);
+                x = fmaf(-slope2, fabsf(fbase + (float)e), x);
                 return x;
             };
             // Blocks inside every row's band (all but the edge blocks) take the
@@ -250,15 +280,17 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t sr[32];
                     tmem_ld32(scol + 32 * c, sr);
+                    float bl[32];
+                    if (kExt) load_bias(bl, kb + 32 * c);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int e = 32 * c + i;
-                        const float x = kAlibi ? score2(sr[i], e) : __uint_as_float(sr[i]);
+                        const float x = kExt ? score2(sr[i], e, bl[i]) : __uint_as_float(sr[i]);
                         mx = (!kMask || (e >= lo && e <= hi)) ? fmaxf(mx, x) : mx;
                     }
                 }
-                if (!kAlibi) mx *= p.scale_log2;
+                if (!kExt) mx *= p.scale_log2;
                 const float m_new = fmaxf(m_run, mx);
                 m_use = (m_run == -INFINITY || m_new > m_run + kRescaleLog2) ? m_new : m_run;
                 alpha = (m_use == m_run) ? 1.f : ex2(m_run - m_use);
@@ -270,15 +302,17 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t sr[32];
                     tmem_ld32(scol + 32 * c, sr);
+                    float bl[32];
+                    if (kExt) load_bias(bl, kb + 32 * c);
                     tmem_wait_ld();
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int e = 32 * c + 2 * i;
                         float p0, p1;
-                        if (kAlibi) {
-                            p0 = ex2(score2(sr[2 * i], e) - mref);
-                            p1 = ex2(score2(sr[2 * i + 1], e + 1) - mref);
+                        if (kExt) {
+                            p0 = ex2(score2(sr[2 * i], e, bl[2 * i]) - mref);
+                            p1 = ex2(score2(sr[2 * i + 1], e + 1, bl[2 * i + 1]) - mref);
                         } else {
                             p0 = ex2(fmaf(__uint_as_float(sr[2 * i]), p.scale_log2, -mref));
                             p1 = ex2(fmaf(__uint_as_float(sr[2 * i + 1]), p.scale_log2, -mref));
@@ -375,7 +409,8 @@ cudaError_t launch_fwd_tc_t(const BwdParams &p, const CUtensorMap &mq, const CUt
                             const CUtensorMap &mv, void *o, float *lse, int max_lq,
                             cudaStream_t stream) {
     using C = FwdCfg<kD, T>;
-    auto kern = p.alibi ? fwd_tc_kernel<kD, T, true> : fwd_tc_kernel<kD, T, false>;
+    const bool ext = p.alibi != nullptr || p.bias != nullptr;
+    auto kern = ext ? fwd_tc_kernel<kD, T, true> : fwd_tc_kernel<kD, T, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;

@@ -31,6 +31,12 @@ struct BwdParams {
     // used lengths per sequence (null: the stored lengths); clamped to
     // [0, stored length]
     const int *seqused_q, *seqused_k;
+    // elementwise bias (dense problems; input dtype), natural-log units:
+    // bias[b * bias_bs + h * bias_hs + i * bias_rs + j]; null: none
+    const void *bias;
+    long long bias_bs, bias_hs, bias_rs;
+    // backward: dBias = dS written as [B, Hq, Sq, Sk] (input dtype); null: not
+    void *dbias;
     // workspace
     int *err;           // device error word
     int4 *tiles;        // work units (b, n_block, hk, 0)

@@ -158,6 +158,17 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
  *   Lq / Lk above are these used lengths.  Rows past them are neither read
  *   nor written (o, lse, dq, dk, dv keep what they held).
  * ------------------------------------------------------------------------- */
+/* bias (dense problems only; FA_ERR_UNSUPPORTED with cu_seqlens): an
+ *   elementwise additive bias in the input dtype, natural-log units, added
+ *   after the scale (the ELEMENTWISE_BIAS kind of the Composable Kernel page,
+ *   STAGE 2): element (b, h, i, j) at bias[b * bias_batch_stride + h *
+ *   bias_head_stride + i * bias_row_stride + j]; a stride of 0 broadcasts.
+ *   The pointer must be 16-byte aligned and the strides multiples of 8.
+ * dbias (fa_bwd_ext, optional, also without bias): dBias = dS = P o (dP - D)
+ *   (the page's dbias tile, STAGE 5), written as a contiguous
+ *   [B, Hq, Sq, Sk] tensor in the input dtype, fully overwritten: 0 wherever
+ *   dS is 0 (masked entries, tiles no work unit visits, rows and columns past
+ *   the used lengths). */
 typedef struct {
     int window_left;
     int window_right;
@@ -165,6 +176,11 @@ typedef struct {
     int alibi_batch_stride;
     const int *seqused_q;
     const int *seqused_k;
+    const void *bias;
+    long long bias_batch_stride;
+    long long bias_head_stride;
+    long long bias_row_stride;
+    void *dbias;
 } fa_ext;
 
 /* fa_fwd with extensions.  Errors as fa_fwd, plus FA_ERR_INVALID_ARG for a

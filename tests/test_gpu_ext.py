@@ -55,6 +55,17 @@ def _options(w, opt, seed=5):
             a = np.asarray(opt[name], dtype=np.int32)
             ok[name] = a
             gk[name] = torch.from_numpy(a).cuda()
+    if "bias" in opt:
+        # "full" [B, Hq, ...], "b1" [1, Hq, ...], "h1" [B, 1, ...]; rows padded
+        # past Sk (a row stride above Sk)
+        g = torch.Generator().manual_seed(seed + 1)
+        nb = 1 if opt["bias"] == "b1" else w.B
+        nh = 1 if opt["bias"] == "h1" else w.Hq
+        pad = (w.Sk + 7) // 8 * 8 + 8
+        full = torch.randn((nb, nh, w.Sq, pad), generator=g).to(w.torch_dtype)
+        view = full.cuda()[..., :w.Sk]
+        ok["bias"] = to64(full[..., :w.Sk].contiguous())
+        gk["bias"] = view
     return ok, gk
 
 
@@ -154,6 +165,55 @@ def test_ext_backward_matches_oracle(fa, oracle_mod, cuda_device, w, opt):
     _check_bwd(oracle_mod, w, x, ok, _run_bwd(fa, w, x, gk))
 
 
+BIAS_CASES = [
+    (W("bias_d128_gqa", 2, 200, 200, 4, 2, 128), dict(bias="full")),
+    (W("bias_causal_d64", 1, 330, 330, 2, 2, 64, causal=True), dict(bias="b1")),
+    (W("bias_sq_lt_sk_d128_fp16", 2, 150, 270, 2, 1, 128, "fp16", causal=True), dict(bias="h1")),
+    (W("bias_alibi_win_d64", 1, 260, 260, 2, 1, 64), dict(bias="full", alibi="h", window=(70, 20))),
+    (W("bias_seqused_d128", 2, 256, 256, 2, 2, 128, causal=True),
+     dict(bias="full", seqused_q=[256, 100], seqused_k=[200, 256])),
+]
+
+
+def _oracle_dbias(oracle_mod, w, x, ok):
+    """dS of every (sequence, query head), [B, Hq, Sq, Sk], zero outside the used rows."""
+    ref = np.zeros((w.B, w.Hq, w.Sq, w.Sk))
+    for b in range(w.B):
+        for h in range(w.Hq):
+            _, dS = oracle_mod.head_matrices(to64(x["q"]), to64(x["k"]), to64(x["v"]),
+                                             to64(x["dout"]), w.softmax_scale, w.causal,
+                                             o=to64(x["o"]), lse=to64(x["lse"]), b=b, h=h, **ok)
+            ref[b, h, :dS.shape[0], :dS.shape[1]] = dS
+    return ref
+
+
+@pytest.mark.parametrize("w,opt", BIAS_CASES, ids=lambda v: v.name if hasattr(v, "name") else "")
+def test_bias_forward_backward_dbias(fa, oracle_mod, cuda_device, w, opt):
+    x, ok, gk = _case(oracle_mod, w, opt)
+    o, lse = fa.fa_fwd(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), causal=w.causal,
+                       softmax_scale=w.softmax_scale, **gk)
+    torch.cuda.synchronize()
+    mq = _used_rows(w, x, ok, "q")
+    check_bar(to64(o)[mq], x["o64"][mq], "o")
+    lg, lr = to64(lse).transpose(0, 2, 1)[mq], x["lse64"].transpose(0, 2, 1)[mq]
+    assert np.array_equal(np.isneginf(lg), np.isneginf(lr))
+    fin = np.isfinite(lr)
+    assert np.max(np.abs(lg[fin] - lr[fin])) < 1e-4
+    dbias = torch.full((w.B, w.Hq, w.Sq, w.Sk), SENTINEL, dtype=w.torch_dtype, device="cuda")
+    outs = _run_bwd(fa, w, x, dict(gk, dbias=dbias))
+    _check_bwd(oracle_mod, w, x, ok, outs)
+    check_bar(dbias, _oracle_dbias(oracle_mod, w, x, ok), "dbias")
+
+
+def test_dbias_without_bias(fa, oracle_mod, cuda_device):
+    w = W("dbias_only", 1, 190, 190, 2, 2, 128, causal=True)
+    x, ok, gk = _case(oracle_mod, w, {})
+    dbias = torch.full((w.B, w.Hq, w.Sq, w.Sk), SENTINEL, dtype=w.torch_dtype, device="cuda")
+    outs = _run_bwd(fa, w, x, dict(dbias=dbias))
+    _check_bwd(oracle_mod, w, x, ok, outs)
+    check_bar(dbias, _oracle_dbias(oracle_mod, w, x, ok), "dbias")
+
+
 VARLEN = [
     (W("vl_win_causal_d64", 3, 0, 0, 2, 2, 64, "bf16", True, varlen=(3, 1, 300)),
      [300, 77, 129], dict(window=(50, -1), seqused_q=[300, 60, 129], seqused_k=[280, 77, 0])),
@@ -199,3 +259,13 @@ def test_ext_rejects_bad_options(fa, cuda_device):
         fa.fa_fwd(q, q, q, window=(0, -5))
     with pytest.raises(ValueError):
         fa.fa_fwd(q, q, q, alibi_slopes=torch.zeros(2, dtype=torch.float64, device="cuda"))
+    bias = torch.zeros((1, 2, 64, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fa.FaError):   # a row stride that is not a multiple of 8
+        fa.fa_fwd(q, q, q, bias=torch.zeros((1, 2, 64, 70), dtype=torch.bfloat16,
+                                            device="cuda")[..., :64])
+    qv = torch.zeros((64, 2, 64), dtype=torch.bfloat16, device="cuda")
+    cu = torch.tensor([0, 64], dtype=torch.int32, device="cuda")
+    with pytest.raises(fa.FaError) as e:   # bias with varlen: unsupported
+        fa.fa_fwd(qv, qv, qv, cu_seqlens_q=cu, cu_seqlens_k=cu, max_seqlen_q=64,
+                  max_seqlen_k=64, bias=bias)
+    assert e.value.status == fa.FA_ERR_UNSUPPORTED
