@@ -256,15 +256,18 @@ struct MainMaps {
     CUtensorMap q, k, v, dout;
 };
 
-// kExt: the extended instance -- a lower edge of the visible band (a left
-// window) and / or the ALiBi bias (p.alibi).  A separate instance, so that the
-// plain kernel (no mask, or a band with an upper edge only, e.g. causal) keeps
-// its softmax and reducer code as they are.
-template <int kD, typename T, bool kExt>
+// kMode 0: the plain kernel (no mask, or a band with an upper edge only, e.g.
+// causal).  1: a band with a lower edge (a left window).  2: as 1 plus ALiBi.
+// 3: as 2 plus the elementwise bias and / or dBias.  Separate instances: the
+// code of each extension slows the softmax warps even when it is skipped at
+// run time (measured: the bias code made a windowed run 1.8x slower, the
+// ALiBi arithmetic 11 %).
+template <int kD, typename T, int kMode>
 __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
     bwd_main_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ MainMaps maps) {
     using C = MainCfg<kD, T>;
     constexpr int D = C::D, BM = C::BM, BN = C::BN, S = C::kStages, HALF = C::HALF, NCH = C::NCH;
+    constexpr bool kExt = kMode >= 1, kAlibi = kMode >= 2, kBias = kMode == 3;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -814,14 +817,14 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 const bool masked_lo = kExt && n0 - (m0 + BM - 1 + diag) < -wlo;
                 // ALiBi slope of the step's query head, in log2 units (0: none)
                 float slope2 = 0.f;
-                if (kExt && p.alibi)
+                if (kAlibi && p.alibi)
                     slope2 = __ldg(p.alibi + (long long)u.b * p.alibi_bstride + u.hk * p.G + u.g_of(it, p.G)) *
                              1.4426950408889634f;
                 // elementwise bias / dBias of the step's (sequence, query head)
                 // (dense problems): element (query qi, key kj) at qi * stride + kj
                 const T *bias_h = nullptr;
                 uint16_t *dbias_h = nullptr;
-                if (kExt) {
+                if (kBias) {
                     const int hq = u.hk * p.G + u.g_of(it, p.G);
                     if (p.bias)
                         bias_h = reinterpret_cast<const T *>(p.bias) + (long long)u.b * p.bias_bs +
@@ -874,12 +877,12 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                                             __uint_as_float(sr[h][4 * k + 2 * r + 1])),
                                     sc2, nl2[k]));
                                 float x0 = x.x, x1 = x.y;
-                                if (kExt) {
+                                if (kAlibi) {
                                     // -slope * |qi + diag - kj|
                                     const float fd = flim + (float)(kr - 8 * k);
                                     x0 = fmaf(-slope2, fabsf(fd), x0);
                                     x1 = fmaf(-slope2, fabsf(fd - 1.f), x1);
-                                    if (bias_h) {   // + bias * log2e (0 past the used lengths)
+                                    if (kBias && bias_h) {   // + bias * log2e (0 past the used lengths)
                                         const int qi0 = m0 + c0 + 8 * k + 2 * q4, kj = kb + kr;
                                         float b0 = 0.f, b1 = 0.f;
                                         if (kj < u.lk) {
@@ -955,7 +958,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                                                    __uint_as_float(dr[h][4 * k + 2 * r + 1])),
                                            dd[k])));
                                 pk[2 * k + r] = Cvt<T>::pack(ds.x, ds.y);
-                                if (kExt && dbias_h) {   // dBias = dS, inside the used lengths
+                                if (kBias && dbias_h) {   // dBias = dS, inside the used lengths
                                     const int qi0 = m0 + c0 + 8 * k + 2 * q4, kj = kb + 16 * h + 8 * r;
                                     if (kj < u.lk) {
                                         if (qi0 < u.lq)
@@ -1048,8 +1051,10 @@ template <int kD, typename T>
 static cudaError_t launch_main_t(const BwdParams &p, const MainMaps &maps, int grid,
                                  cudaStream_t stream) {
     using C = MainCfg<kD, T>;
-    const bool ext = p.alibi != nullptr || p.win_lo < kNoWindow || p.bias != nullptr || p.dbias != nullptr;
-    auto kern = ext ? bwd_main_kernel<kD, T, true> : bwd_main_kernel<kD, T, false>;
+    auto kern = (p.bias || p.dbias) ? bwd_main_kernel<kD, T, 3>
+                : p.alibi               ? bwd_main_kernel<kD, T, 2>
+                : p.win_lo < kNoWindow  ? bwd_main_kernel<kD, T, 1>
+                                        : bwd_main_kernel<kD, T, 0>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;

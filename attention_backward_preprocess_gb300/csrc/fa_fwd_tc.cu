@@ -70,15 +70,17 @@ enum {
 // that may lag the true one by up to this much.
 constexpr float kRescaleLog2 = 8.f;
 
-// kExt: the scores carry the ALiBi bias (p.alibi) and / or the elementwise
-// bias (p.bias).
-template <int kD, typename T, bool kExt>
+// kMode 0: plain scores.  1: with the ALiBi bias (p.alibi).  2: with the
+// elementwise bias (p.bias) and ALiBi if given.  Separate instances: the bias
+// code slows the softmax even when skipped at run time.
+template <int kD, typename T, int kMode>
 __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap map_q,
                   const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                   void *o_out, float *lse_out, int nmb) {
     using C = FwdCfg<kD, T>;
     constexpr int D = C::D, BM = C::BM, BN = C::BN, S = C::kStages;
+    constexpr bool kExt = kMode >= 1, kBias = kMode == 2;
     // ---- tile of this CTA: longest causal rows first
     const int bh = blockIdx.x % (p.B * p.Hq);
     const int m = nmb - 1 - blockIdx.x / (p.B * p.Hq);
@@ -223,7 +225,7 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                                  : 0.f;
         // elementwise bias row of this query (null: none, or a padding row)
         const T *brow = nullptr;
-        if (kExt && p.bias && qi < lq)
+        if (kBias && p.bias && qi < lq)
             brow = reinterpret_cast<const T *>(p.bias) + (long long)b * p.bias_bs +
                    (long long)h * p.bias_hs + (long long)qi * p.bias_rs;
         // bias of keys k0 .. k0 + 31 in log2 units (0 past lk); 16-byte loads
@@ -263,9 +265,8 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
             const float fbase = (float)(kb - qi - diag);
             // scaled score of element e with its bias (bl: bias * log2e), log2 units
             auto score2 = [&](uint32_t raw, int e, float bl) __attribute__((always_inline)) -> float {
-                float x = fmaf(__uint_as_float(raw), p.scale_log2, bl);
-                x = fmaf(-slope2, fabsf(fbase + (float)e), x);
-                return x;
+                float x = fmaf(-slope2, fabsf(fbase + (float)e), kBias ? bl : 0.f);
+                return fmaf(__uint_as_float(raw), p.scale_log2, x);
             };
             // Blocks inside every row's band (all but the edge blocks) take the
             // pass without per-element tests.
@@ -281,7 +282,7 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                     uint32_t sr[32];
                     tmem_ld32(scol + 32 * c, sr);
                     float bl[32];
-                    if (kExt) load_bias(bl, kb + 32 * c);
+                    if (kBias) load_bias(bl, kb + 32 * c);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
@@ -303,7 +304,7 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                     uint32_t sr[32];
                     tmem_ld32(scol + 32 * c, sr);
                     float bl[32];
-                    if (kExt) load_bias(bl, kb + 32 * c);
+                    if (kBias) load_bias(bl, kb + 32 * c);
                     tmem_wait_ld();
                     uint32_t pk[16];
 #pragma unroll
@@ -409,8 +410,7 @@ cudaError_t launch_fwd_tc_t(const BwdParams &p, const CUtensorMap &mq, const CUt
                             const CUtensorMap &mv, void *o, float *lse, int max_lq,
                             cudaStream_t stream) {
     using C = FwdCfg<kD, T>;
-    const bool ext = p.alibi != nullptr || p.bias != nullptr;
-    auto kern = ext ? fwd_tc_kernel<kD, T, true> : fwd_tc_kernel<kD, T, false>;
+    auto kern = p.bias ? fwd_tc_kernel<kD, T, 2> : p.alibi ? fwd_tc_kernel<kD, T, 1> : fwd_tc_kernel<kD, T, 0>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;

@@ -184,6 +184,11 @@ def main():
     ap.add_argument("--ref-prefix", type=int, default=1024)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    # extension runs (fa_fwd_ext / fa_bwd_ext; not the headline line)
+    ap.add_argument("--window", default=None, help="LEFT,RIGHT local window (-1: unbounded)")
+    ap.add_argument("--alibi", action="store_true", help="ALiBi slopes 2^(-8 h / Hq)")
+    ap.add_argument("--bias", action="store_true",
+                    help="elementwise bias [B, Hq, Sq, Sk] and its gradient dBias")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -191,6 +196,8 @@ def main():
     w = WORKLOADS[args.workload or BENCH_WORKLOAD]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.window or args.alibi or args.bias:
+        return run_ext(args, w)
 
     import torch
 
@@ -401,6 +408,115 @@ def main():
     print(json.dumps(line))
     if ws > 1:
         torch.distributed.destroy_process_group()
+    return 0
+
+
+def visible_pairs(lq, lk, causal, wl, wr):
+    """(query, key) pairs of one head that the mask leaves visible: key j is
+    visible to query i iff i + d - wl <= j <= i + d + wr, d = lk - lq (-1:
+    unbounded side), and j <= i + d when causal."""
+    import numpy as np
+    i = np.arange(lq, dtype=np.int64) + (lk - lq)
+    hi = np.full(lq, lk - 1) if wr < 0 else np.minimum(lk - 1, i + wr)
+    if causal:
+        hi = np.minimum(hi, i)
+    lo = np.zeros(lq, dtype=np.int64) if wl < 0 else np.maximum(0, i - wl)
+    return int(np.maximum(hi - lo + 1, 0).sum())
+
+
+def run_ext(args, w):
+    """Times fa_fwd_ext and fa_bwd_ext (one call: preprocess, main, postprocess)
+    on workload w with the requested extensions; one GPU, one JSON line.  The
+    FLOP counts are over the visible pairs: 4 D (forward) and 10 D (backward)
+    per pair."""
+    import torch
+
+    import attention_backward_preprocess_gb300 as fa
+    from attention_backward_preprocess_gb300.workloads import generate
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fa.lib()
+    x = generate(w, dev)
+    q, k, v, do = x["q"], x["k"], x["v"], x["dout"]
+    varlen = w.varlen is not None
+    vl = dict(cu_seqlens_q=x["cu_q"], cu_seqlens_k=x["cu_k"], max_seqlen_q=x["max_len"],
+              max_seqlen_k=x["max_len"]) if varlen else {}
+    wl, wr = (int(t) for t in args.window.split(",")) if args.window else (-1, -1)
+    ext = {}
+    if args.window:
+        ext["window"] = (wl, wr)
+    if args.alibi:
+        ext["alibi_slopes"] = torch.tensor([2.0 ** (-8.0 * (h + 1) / w.Hq) for h in range(w.Hq)],
+                                           dtype=torch.float32, device=dev)
+    dbias = None
+    if args.bias:
+        if varlen:
+            raise SystemExit("--bias: dense workloads only")
+        g = torch.Generator(device=dev).manual_seed(7)
+        ext["bias"] = torch.randn((w.B, w.Hq, w.Sq, w.Sk), generator=g, device=dev).to(q.dtype)
+        dbias = torch.empty_like(ext["bias"])
+    lengths = x.get("lengths") or [w.Sq] * w.B
+    pairs = sum(visible_pairs(L, L if varlen else w.Sk, w.causal, wl, wr) for L in lengths) * w.Hq
+    fl_fwd, fl_bwd = 4.0 * w.D * pairs, 10.0 * w.D * pairs
+    o, lse = fa.fa_fwd(q, k, v, causal=w.causal, softmax_scale=w.softmax_scale, **vl, **ext)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    Sq = x["max_len"] if varlen else w.Sq
+    work = torch.empty(fa.workspace_bytes(w.B, Sq, Sq if varlen else w.Sk, w.Hq, w.Hkv, w.D,
+                                          varlen=varlen, deterministic=w.deterministic),
+                       dtype=torch.uint8, device=dev)
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, o, do))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if in_bytes < (256 << 20) else None
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        fa.fa_fwd(q, k, v, causal=w.causal, softmax_scale=w.softmax_scale, **vl, **ext)
+
+    def bwd():
+        fa.fa_bwd(q, k, v, o, do, lse, causal=w.causal, softmax_scale=w.softmax_scale,
+                  deterministic=w.deterministic, dq=dq, dk=dk, dv=dv, workspace=work, dbias=dbias,
+                  **vl, **ext)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for a, b in ev:
+            if flush is not None:
+                flush.fill_(1)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    clocks = ClockSampler(dev.index, os.path.join(ROOT, "gpurun_out", "bench_ext_clocks.csv")
+                          if os.path.isdir(os.path.join(ROOT, "gpurun_out"))
+                          else "/tmp/bench_ext_clocks.%d.csv" % os.getpid())
+    f_ms = timed(fwd)
+    b_ms = timed(bwd)
+    clk = clocks.stop()
+    status = fa.device_status(work)
+    fstatus = fa.device_status()
+    pk = peaks()
+    exts = {k_: (list(v_) if k_ == "window" else True) for k_, v_ in ext.items()}
+    if dbias is not None:
+        exts["dbias"] = True
+    line = {
+        "metric": "attention-backward TFLOPS with extensions (visible pairs)",
+        "value": fl_bwd / (b_ms * 1e-3) / 1e12, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": b_ms, "higher_is_better": True,
+        "dtype": "bf16" if w.dtype == "bf16" else "fp16", "data": "synthetic",
+        "config": dict(config_of(w, x.get("lengths"), flush is not None), extensions=exts,
+                       visible_pairs=pairs),
+        "pct_of_bf16_peak": 100.0 * fl_bwd / (b_ms * 1e-3) / 1e12 / pk["bf16"],
+        "forward": {"ms": f_ms, "tflops": fl_fwd / (f_ms * 1e-3) / 1e12,
+                    "pct_of_bf16_peak": 100.0 * fl_fwd / (f_ms * 1e-3) / 1e12 / pk["bf16"]},
+        "device_status": [status, fstatus], "clocks": clk,
+    }
+    print(json.dumps(line))
     return 0
 
 
