@@ -37,6 +37,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Tile width a head dim runs at: 64 or 128 (the columns past D are zero-filled
+// by the TMA loads; the FlashAttention postprocess page likewise pads the head
+// dim to a multiple of its block size).
+int pad_d(int D) { return D <= 64 ? 64 : 128; }
+
 struct Layout {
     size_t err, ntiles, tiles, dvec, lse2, dqacc, sem, total;  // byte offsets / size
     long long rows, rows_per_head;
@@ -64,7 +69,7 @@ bool plan(int B, int Sq, int Sk, int Hq, int Hkv, int D, int varlen, int determi
     L->tiles = off;     off = round_up(off + (size_t)tiles * 16, 256);
     L->dvec = off;      off = round_up(off + (size_t)L->rows * 4, 256);
     L->lse2 = off;      off = round_up(off + (size_t)L->rows * 4, 256);
-    L->dqacc = off;     off = round_up(off + (size_t)L->rows * D * 4, 256);
+    L->dqacc = off;     off = round_up(off + (size_t)L->rows * pad_d(D) * 4, 256);
     L->sem = off;       off = round_up(off + (deterministic ? (size_t)(L->rows / 64) * 4 : 0), 256);
     L->total = off;
     return true;
@@ -88,7 +93,7 @@ fa_status check_shape(int B, int Sq, int Sk, int Hq, int Hkv, int D, fa_dtype dt
     if (B <= 0 || Sq <= 0 || Sk <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return FA_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
     if ((cu_q == nullptr) != (cu_k == nullptr)) return FA_ERR_INVALID_ARG;
-    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if (D < 64 || D > 128 || D % 8 != 0) return FA_ERR_UNSUPPORTED;
     if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_UNSUPPORTED;
     // TMA coordinates are 32-bit
     if ((long long)B * Sq > (1LL << 31) - 1 || (long long)B * Sk > (1LL << 31) - 1)
@@ -275,7 +280,8 @@ fa_status prepare(const void *q, const void *k, const void *v, const void *o, co
     std::memset(&p, 0, sizeof(p));
     p.q = q; p.k = k; p.v = v; p.o = o; p.dout = dout; p.lse = lse;
     p.dq = dq; p.dk = dk; p.dv = dv;
-    p.B = B; p.Sq = Sq; p.Sk = Sk; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.G = Hq / Hkv;
+    p.B = B; p.Sq = Sq; p.Sk = Sk; p.Hq = Hq; p.Hkv = Hkv; p.D = pad_d(D); p.Dh = D;
+    p.G = Hq / Hkv;
     p.scale = scale;
     p.scale_log2 = scale * kLog2e;
     p.causal = causal ? 1 : 0;
@@ -333,10 +339,10 @@ fa_status run_main(const Prepared &P, fa_dtype dtype, cudaStream_t stream) {
     const int nb = p.varlen ? 1 : p.B;
     if (rq <= 0 || rk <= 0) return FA_ERR_INVALID_ARG;
     if (!p.q || !p.k || !p.v || !p.dout || !p.dk || !p.dv) return FA_ERR_INVALID_ARG;
-    if (!encode_rows_map(&mq, p.q, p.D, p.Hq, rq, nb, bm, bf16) ||
-        !encode_rows_map(&mdo, p.dout, p.D, p.Hq, rq, nb, bm, bf16) ||
-        !encode_rows_map(&mk, p.k, p.D, p.Hkv, rk, nb, fa::kBlockN, bf16) ||
-        !encode_rows_map(&mv, p.v, p.D, p.Hkv, rk, nb, fa::kBlockN, bf16))
+    if (!encode_rows_map(&mq, p.q, p.Dh, p.Hq, rq, nb, bm, bf16) ||
+        !encode_rows_map(&mdo, p.dout, p.Dh, p.Hq, rq, nb, bm, bf16) ||
+        !encode_rows_map(&mk, p.k, p.Dh, p.Hkv, rk, nb, fa::kBlockN, bf16) ||
+        !encode_rows_map(&mv, p.v, p.Dh, p.Hkv, rk, nb, fa::kBlockN, bf16))
         return FA_ERR_CUDA;
     if (p.varlen) {
         // the unit list depends on the device-resident cu_seqlens
@@ -384,7 +390,7 @@ long long fa_set_wait_timeout_ns(long long ns) {
 size_t fa_bwd_workspace_bytes(int B, int Sq, int Sk, int Hq, int Hkv, int D, int varlen,
                               int deterministic) {
     Layout L;
-    if (D != 64 && D != 128) return 0;
+    if (D < 64 || D > 128 || D % 8 != 0) return 0;
     if (!plan(B, Sq, Sk, Hq, Hkv, D, varlen, deterministic, &L)) return 0;
     return L.total;
 }
@@ -393,7 +399,7 @@ fa_status fa_bwd_workspace_layout(int B, int Sq, int Sk, int Hq, int Hkv, int D,
                                   int deterministic, size_t *dvec_off, size_t *lse2_off,
                                   size_t *dqacc_off, size_t *rows) {
     Layout L;
-    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if (D < 64 || D > 128 || D % 8 != 0) return FA_ERR_UNSUPPORTED;
     if (!plan(B, Sq, Sk, Hq, Hkv, D, varlen, deterministic, &L)) return FA_ERR_INVALID_ARG;
     if (dvec_off) *dvec_off = L.dvec / 4;
     if (lse2_off) *lse2_off = L.lse2 / 4;
@@ -547,7 +553,8 @@ fa_status fa_fwd_ext(const void *q, const void *k, const void *v, void *o, float
     fa::BwdParams p;
     std::memset(&p, 0, sizeof(p));
     p.q = q; p.k = k; p.v = v;
-    p.B = B; p.Sq = Sq; p.Sk = Sk; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.G = Hq / Hkv;
+    p.B = B; p.Sq = Sq; p.Sk = Sk; p.Hq = Hq; p.Hkv = Hkv; p.D = pad_d(D); p.Dh = D;
+    p.G = Hq / Hkv;
     p.scale = softmax_scale;
     p.scale_log2 = softmax_scale * kLog2e;
     p.causal = causal ? 1 : 0;

@@ -1001,12 +1001,13 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             // ---------------------------------------------------- dK / dV out
             T *out = reinterpret_cast<T *>(grp == 0 ? p.dk : p.dv);
             const long long orow = (long long)(p.varlen ? u.k_row0 + kj : u.b * p.Sk + kj);
-            T *dst = out + (orow * p.Hkv + u.hk) * D;
+            // the tensors' rows hold Dh <= D columns (a multiple of 8)
+            T *dst = out + (orow * p.Hkv + u.hk) * p.Dh;
             if (u.iters == 0) {
                 if (key_ok && n0 < u.lk) {
 #pragma unroll
                     for (int c = 0; c < D / 8; ++c)
-                        reinterpret_cast<uint4 *>(dst)[c] = make_uint4(0, 0, 0, 0);
+                        if (8 * c < p.Dh) reinterpret_cast<uint4 *>(dst)[c] = make_uint4(0, 0, 0, 0);
                 }
                 continue;
             }
@@ -1029,8 +1030,9 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                                              __uint_as_float(a[2 * c + 1]) * mul);
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
-                        reinterpret_cast<uint4 *>(dst + 32 * ch)[c] =
-                            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                        if (32 * ch + 8 * c < p.Dh)
+                            reinterpret_cast<uint4 *>(dst + 32 * ch)[c] =
+                                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
                 }
             }
             tc_fence_before();

@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                 *lse_dst = l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
             }
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            T *dst = reinterpret_cast<T *>(o_out) + (row * p.Hq + h) * D;
+            T *dst = reinterpret_cast<T *>(o_out) + (row * p.Hq + h) * p.Dh;   // Dh <= D columns
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t orr[32];
@@ -392,8 +392,9 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                                              __uint_as_float(orr[2 * i + 1]) * inv);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        reinterpret_cast<uint4 *>(dst + 32 * c)[i] =
-                            make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        if (32 * c + 8 * i < p.Dh)
+                            reinterpret_cast<uint4 *>(dst + 32 * c)[i] =
+                                make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                 }
             }
         }

@@ -89,9 +89,10 @@ __global__ void __launch_bounds__(256) preprocess_kernel(BwdParams p) {
     }
     const long long wr = active ? ws_row(p, b, h, s) : 0;
     float acc = 0.f;
-    if (active && s < lq) {
+    // O / dO rows hold Dh <= D columns (a multiple of 8): parts past Dh add 0
+    if (active && s < lq && part * 8 < p.Dh) {
         const long long trow = p.varlen ? (long long)p.cu_q[b] + s : (long long)b * p.Sq + s;
-        const long long off = (trow * p.Hq + h) * D + part * 8;
+        const long long off = (trow * p.Hq + h) * p.Dh + part * 8;
         const uint4 ov = *reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.o) + off);
         const uint4 dv = *reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.dout) + off);
         const uint32_t oa[4] = {ov.x, ov.y, ov.z, ov.w}, da[4] = {dv.x, dv.y, dv.z, dv.w};
@@ -136,7 +137,7 @@ __global__ void __launch_bounds__(256) postprocess_kernel(BwdParams p) {
     const int part = (int)(gid % TPR);
     const int lq = seq_len_q(p, b);
     const int s = (int)(rid / p.Hq), h = (int)(rid % p.Hq);
-    if (s >= lq) return;
+    if (s >= lq || part * 8 >= p.Dh) return;   // dQ rows hold Dh <= D columns
     const long long wr = ws_row(p, b, h, s);
     const float4 *src = reinterpret_cast<const float4 *>(p.dqacc + wr * D) + part * 2;
     const float4 a = src[0], c = src[1];
@@ -147,7 +148,7 @@ __global__ void __launch_bounds__(256) postprocess_kernel(BwdParams p) {
     o.z = Cvt<T>::pack(c.x * sc, c.y * sc);
     o.w = Cvt<T>::pack(c.z * sc, c.w * sc);
     const long long trow = p.varlen ? (long long)p.cu_q[b] + s : (long long)b * p.Sq + s;
-    *reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dq) + (trow * p.Hq + h) * D + part * 8) = o;
+    *reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dq) + (trow * p.Hq + h) * p.Dh + part * 8) = o;
 }
 
 }  // namespace

@@ -16,6 +16,8 @@ struct BwdParams {
     const float *lse;
     void *dq, *dk, *dv;
     int B, Sq, Sk, Hq, Hkv, D, G;
+    int Dh;             // head dim of the tensors; D is the tile width it is padded to
+                        // (64 or 128: columns past Dh are zero in shared memory)
     float scale;        // c
     float scale_log2;   // c * log2(e)
     int causal, deterministic, varlen;

@@ -26,6 +26,9 @@
  * (seqlen, d, head, batch) shape with stride (int64, 1, int64, int64)):
  *   dense : q, o, dout, dq : [B, Sq, Hq, D];  k, v, dk, dv : [B, Sk, Hkv, D]
  *           lse : fp32 [B, Hq, Sq], natural log
+ *   D is a multiple of 8 in [64, 128]; it runs at the tile width 64 (D = 64)
+ *   or 128 (otherwise), the tensor-map loads filling the columns past D with
+ *   zeros (the FlashAttention postprocess page pads the head dim likewise).
  *   varlen: cu_seqlens_q / cu_seqlens_k != NULL (both or neither): int32
  *           device arrays of B+1 prefix sums; tensors packed [total, H, D];
  *           lse fp32 [Hq, total_q]; Sq / Sk are the MAXIMUM lengths.
@@ -58,7 +61,8 @@ extern "C" {
 typedef enum {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misalignment, bad scale */
-    FA_ERR_UNSUPPORTED = 2,  /* head dim not in {64, 128}, dtype, or GPU not sm_103 */
+    FA_ERR_UNSUPPORTED = 2,  /* head dim not a multiple of 8 in [64, 128], dtype, or GPU
+                                not sm_103 */
     FA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
     FA_ERR_TIMEOUT = 4,      /* a bounded device-side wait ran out */
     FA_ERR_SCRATCH_LIMIT = 5 /* fa_bwd_noalloc: the problem needs more scratch than
@@ -113,7 +117,9 @@ fa_status fa_bwd_postprocess(void *dq, int B, int Sq, int Sk, int Hq, int Hkv, i
 
 /* Where the preprocess outputs live inside a workspace, in fp32 elements
  * from the workspace base: Dv at *dvec_off, LSE2 at *lse2_off, each indexed
- * by workspace row; the fp32 dQ accumulator at *dqacc_off, [rows, D].
+ * by workspace row; the fp32 dQ accumulator at *dqacc_off, [rows, Dt], where
+ * Dt is the tile width the head dim runs at (64 for D = 64, else 128; the
+ * columns past D stay 0).
  * Workspace row of (sequence b, query head h, position s):
  *   dense : (b * Hq + h) * round_up(Sq, 128) + s
  *   varlen: h * rows_per_head + pad(b) + s, pad(b) = (cu_q[b] + 128 b) / 128 * 128,

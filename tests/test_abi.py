@@ -53,7 +53,10 @@ def test_workspace_planning(fa):
     assert lay["rows"] == 4 * ((3 * (300 + 128) + 127) // 128 * 128)
     assert fa.workspace_bytes(2, 100, 100, 4, 4, 128, deterministic=True) > \
         fa.workspace_bytes(2, 100, 100, 4, 4, 128)
-    assert fa.workspace_bytes(1, 128, 128, 1, 1, 96) == 0          # unsupported head dim
+    assert fa.workspace_bytes(1, 128, 128, 1, 1, 100) == 0         # unsupported head dim
+    assert fa.workspace_bytes(1, 128, 128, 1, 1, 48) == 0
+    # D = 96 runs at the 128 tile width: the same workspace as D = 128
+    assert fa.workspace_bytes(1, 128, 128, 1, 1, 96) == fa.workspace_bytes(1, 128, 128, 1, 1, 128)
     assert fa.workspace_bytes(1, 128, 128, 3, 2, 64) == 0          # Hq % Hkv != 0
     assert fa.workspace_bytes(0, 128, 128, 1, 1, 64) == 0
 
@@ -76,7 +79,7 @@ def _call_with_ws(fa, **over):
 
 @pytest.mark.parametrize("over,status", [
     (dict(q=0), 1), (dict(dv=0), 1), (dict(B=0), 1), (dict(Sq=-1), 1), (dict(Hq=3), 1),
-    (dict(D=96), 2), (dict(D=256), 2), (dict(dtype=7), 2),
+    (dict(D=100), 2), (dict(D=256), 2), (dict(D=32), 2), (dict(dtype=7), 2),
     (dict(scale=0.0), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
     (dict(q=0x1008), 1), (dict(lse=0x6004), 1), (dict(ws=0x100010), 1), (dict(ws=0), 1),
     (dict(ws_bytes=16), 1), (dict(cu_q=0xA000), 1),
@@ -90,7 +93,7 @@ def test_fa_bwd_rejects_before_device(fa):
     vp = ctypes.c_void_p
     ptrs = [vp(0x1000 * (i + 1)) for i in range(9)]
     assert L.fa_bwd(*ptrs, 1, 128, 128, 3, 2, 64, 0.125, 0, None, None, 0, 0, None) == 1
-    assert L.fa_bwd(*ptrs, 1, 128, 128, 2, 2, 80, 0.125, 0, None, None, 0, 0, None) == 2
+    assert L.fa_bwd(*ptrs, 1, 128, 128, 2, 2, 84, 0.125, 0, None, None, 0, 0, None) == 2
     assert L.fa_fwd(*ptrs[:5], 1, 128, 128, 2, 2, 64, -1.0, 0, None, None, 0, None) == 1
 
 

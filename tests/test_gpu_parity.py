@@ -29,6 +29,11 @@ CASES = [
     W("s17_d128_causal", 2, 17, 17, 1, 1, 128, causal=True),
     W("d128_scale", 1, 256, 256, 2, 2, 128, scale=0.37, qk_dist=("normal", 2.0)),
     W("d64_uniform", 1, 384, 384, 2, 2, 64, vdo_dist=("uniform", 1.0)),
+    # head dims between 64 and 128 run at the 128 tile width, zero-padded
+    W("d96_causal_gqa", 2, 300, 300, 4, 2, 96, causal=True),
+    W("d80_fp16_sq_lt_sk", 1, 200, 260, 2, 2, 80, "fp16"),
+    W("d72_causal", 1, 257, 257, 2, 1, 72, causal=True),
+    W("d120", 1, 130, 130, 2, 2, 120),
 ]
 
 
@@ -49,6 +54,7 @@ VARLEN = [
     (W("varlen_empty_seq", 3, 0, 0, 2, 2, 64, "bf16", True, varlen=(3, 0, 129)), [50, 0, 129]),
     (W("varlen_d128_causal_gqa", 3, 0, 0, 4, 1, 128, "bf16", True, varlen=(3, 1, 260)),
      [260, 128, 33]),
+    (W("varlen_d96_causal", 2, 0, 0, 2, 2, 96, "bf16", True, varlen=(2, 1, 300)), [300, 111]),
 ]
 
 
@@ -62,7 +68,7 @@ def test_varlen_backward_matches_oracle(fa, oracle_mod, cuda_device, w, lengths)
     check_bar(dv, rv, "dv")
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 96, 128])
 def test_deterministic_is_bit_identical_and_correct(fa, oracle_mod, cuda_device, D):
     w = W("det", 2, 300, 300, 4, 2, D, causal=True, deterministic=True)
     x = small_case(oracle_mod, w)
@@ -76,9 +82,11 @@ def test_deterministic_is_bit_identical_and_correct(fa, oracle_mod, cuda_device,
     check_bar(a[2], rv, "dv")
 
 
-def test_outputs_written_in_bounds_only(fa, oracle_mod, cuda_device):
-    """Canary regions around dq/dk/dv stay untouched; ragged tails included."""
-    w = W("canary", 1, 150, 150, 2, 2, 128, causal=True)
+@pytest.mark.parametrize("D", [128, 96])
+def test_outputs_written_in_bounds_only(fa, oracle_mod, cuda_device, D):
+    """Canary regions around dq/dk/dv stay untouched; ragged tails included
+    (with D = 96, a write of the padded columns would run past the end)."""
+    w = W("canary", 1, 150, 150, 2, 2, D, causal=True)
     x = small_case(oracle_mod, w)
     pad = 4096
     outs, bufs = [], []
@@ -129,6 +137,8 @@ FWD_CASES = [
     W("fwd_rescale_causal_fp16", 1, 384, 384, 2, 1, 64, "fp16", True, scale=0.5,
       qk_dist=("normal", 2.0)),
     W("fwd_s1", 1, 1, 1, 1, 1, 128),
+    W("fwd_d96_causal_gqa", 2, 300, 300, 4, 2, 96, causal=True),
+    W("fwd_d80_fp16", 1, 200, 260, 2, 2, 80, "fp16"),
 ]
 
 
