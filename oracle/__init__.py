@@ -18,9 +18,10 @@ Every function also takes the optional extensions as keywords:
 ``window=(left, right)`` (a local band around the bottom-right diagonal, -1 =
 unbounded on that side), ``alibi`` (slopes ``[Hq]`` or ``[B, Hq]``) and
 ``seqused_q`` / ``seqused_k`` (used lengths per sequence; rows past them are
-neither read nor written, and come back as zeros) and ``bias`` (an elementwise
+neither read nor written, and come back as zeros), ``bias`` (an elementwise
 additive bias ``[B or 1, Hq or 1, Sq, Sk]``, dense only; its gradient dBias =
-dS comes from ``head_matrices``).
+dS comes from ``head_matrices``) and ``dropout=(t, seed, offset)`` (drop
+probability t / 256 with a Philox4x32-10 mask, see ``fa_oracle.c``).
 
 Parity status: every function here is pinned by ``tests/test_oracle.py``
 (central finite differences, invariants, a hand-derived 2x2 example, closed
@@ -81,20 +82,27 @@ class _Ext(ctypes.Structure):
                 ("seqused_q", ctypes.POINTER(ctypes.c_int)),
                 ("seqused_k", ctypes.POINTER(ctypes.c_int)),
                 ("bias", ctypes.POINTER(ctypes.c_double)), ("bias_bs", ctypes.c_long),
-                ("bias_hs", ctypes.c_long), ("bias_rs", ctypes.c_long)]
+                ("bias_hs", ctypes.c_long), ("bias_rs", ctypes.c_long),
+                ("dropout_t", ctypes.c_int), ("dropout_seed", ctypes.c_ulonglong),
+                ("dropout_offset", ctypes.c_uint)]
 
 
-def _ext(B, Hq, window=None, alibi=None, seqused_q=None, seqused_k=None, bias=None):
+def _ext(B, Hq, window=None, alibi=None, seqused_q=None, seqused_k=None, bias=None,
+         dropout=None):
     """(ctypes pointer or None, arrays to keep alive) for the extension options.
 
     ``bias`` is a [B or 1, Hq or 1, Sq, Sk] array (dense problems); a size-1
-    batch or head axis is broadcast."""
+    batch or head axis is broadcast.  ``dropout`` is (t, seed, offset): drop
+    probability t / 256, the Philox key and the counter's fourth word."""
     if (window is None and alibi is None and seqused_q is None and seqused_k is None
-            and bias is None):
+            and bias is None and dropout is None):
         return None, ()
     wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
     keep = []
     e = _Ext(wl, wr, None, 0, None, None)
+    if dropout is not None:
+        e.dropout_t, e.dropout_seed, e.dropout_offset = (int(dropout[0]), int(dropout[1]),
+                                                         int(dropout[2]))
     if alibi is not None:
         a = np.ascontiguousarray(alibi, dtype=np.float64)
         if a.shape not in ((Hq,), (B, Hq)):
@@ -163,8 +171,37 @@ class Oracle:
         lib.oracle_preprocess.argtypes = [dp] * 6 + shape + [dp, dp, ctypes.c_int, ep]
         lib.oracle_preprocess.restype = ctypes.c_int
         lib.oracle_max_threads.restype = ctypes.c_int
+        up = ctypes.POINTER(ctypes.c_uint)
+        lib.oracle_philox4x32_10.argtypes = [up, up, up]
+        lib.oracle_philox4x32_10.restype = None
+        lib.oracle_dropout_factors.argtypes = [ctypes.c_int] * 6 + [ip, ip, ctypes.c_int,
+                                                                     ctypes.c_int, dp, ep]
+        lib.oracle_dropout_factors.restype = ctypes.c_int
         self.lib = lib
         self.path = libpath
+
+    def philox(self, ctr, key):
+        """Philox4x32-10 output words of one counter (4 words) and key (2 words)."""
+        c = (ctypes.c_uint * 4)(*[int(x) & 0xFFFFFFFF for x in ctr])
+        k = (ctypes.c_uint * 2)(*[int(x) & 0xFFFFFFFF for x in key])
+        o = (ctypes.c_uint * 4)()
+        self.lib.oracle_philox4x32_10(c, k, o)
+        return [int(x) for x in o]
+
+    def dropout_factors(self, B, Sq, Sk, Hq, Hkv, D, b, h, cu_q=None, cu_k=None, lq=None,
+                        lk=None, **ext):
+        """M * s of every (i, j) of head problem (b, h): [Lq, Lk]."""
+        e, keep_e = _ext(B, Hq, **ext)
+        cq = None if cu_q is None else np.ascontiguousarray(cu_q, dtype=np.int32)
+        ck = None if cu_k is None else np.ascontiguousarray(cu_k, dtype=np.int32)
+        lq = (Sq if cq is None else int(cq[b + 1] - cq[b])) if lq is None else lq
+        lk = (Sk if ck is None else int(ck[b + 1] - ck[b])) if lk is None else lk
+        F = np.zeros((lq, lk))
+        rc = self.lib.oracle_dropout_factors(B, Sq, Sk, Hq, Hkv, D, _ptr(cq, ctypes.c_int),
+                                             _ptr(ck, ctypes.c_int), int(b), int(h), _ptr(F), e)
+        if rc:
+            raise ValueError("oracle_dropout_factors rejected its arguments (%d)" % rc)
+        return F
 
     def max_threads(self) -> int:
         return int(self.lib.oracle_max_threads())
@@ -293,3 +330,11 @@ def head_matrices(*a, **kw):
 
 def preprocess(*a, **kw):
     return default().preprocess(*a, **kw)
+
+
+def philox(*a, **kw):
+    return default().philox(*a, **kw)
+
+
+def dropout_factors(*a, **kw):
+    return default().dropout_factors(*a, **kw)

@@ -28,6 +28,17 @@
  *            Composable Kernel page, STAGE 2: added to the scaled score in
  *            natural-log units): s_ij += bias[b, h, i, j]; its gradient is
  *            dBias_ij = dS_ij (STAGE 5, the dbias tile is the cast ds tile)
+ *   dropout: optional, with drop probability t / 256 (t = the threshold byte)
+ *            and keep scale 256 / (256 - t): entry (i, j) is kept iff its
+ *            random byte is >= t (the Composable Kernel page's FmhaDropout:
+ *            dropped entries carry a negative P, kept ones are scaled by
+ *            rp_undrop).  O_i = sum_j P_ij M_ij s v_j, dV_j = sum_i P_ij M_ij s
+ *            dO_i, dS_ij = P_ij (M_ij s dP_ij - Dv_i).  The random byte of
+ *            (sequence b, query head h, query i, key j) is byte j % 4 of word
+ *            (j / 4) % 4 of Philox4x32-10 (Salmon et al., "Parallel random
+ *            numbers: as easy as 1, 2, 3", SC 2011) with counter
+ *            (j / 16, i, b * Hq + h, offset) and key (seed low, seed high);
+ *            the pages print no generator, this one is the reading taken.
  *   seqused: optional per-sequence used lengths (seqused of SeqlenInfo in the
  *            FlashAttention pages): Lq = seqused_q[b], Lk = seqused_k[b]; the
  *            rows keep their places, rows past the used length are neither
@@ -77,6 +88,9 @@ typedef struct {
     const int *seqused_q, *seqused_k;  /* [B]; NULL: the full lengths */
     const double *bias;             /* bias[b * bias_bs + h * bias_hs + i * bias_rs + j]; NULL: none */
     long bias_bs, bias_hs, bias_rs;
+    int dropout_t;                  /* threshold byte t in [0, 255]; 0: no dropout */
+    unsigned long long dropout_seed;
+    unsigned int dropout_offset;
 } oracle_ext_t;
 
 typedef struct {
@@ -125,6 +139,41 @@ static int visible(const prob_t *p, int b, int i, int j) {
     if (p->ext.window_right >= 0 && j > i + diag + p->ext.window_right) return 0;
     return 1;
 }
+/* Philox4x32-10: ten rounds of the Philox S-box on a 128-bit counter with a
+ * 64-bit key, the key bumped by the Weyl constants between rounds (Salmon et
+ * al., SC 2011, section 3 and table 2). */
+static void philox4x32_10(const unsigned int ctr_in[4], const unsigned int key_in[2],
+                          unsigned int out[4]) {
+    unsigned int c[4] = {ctr_in[0], ctr_in[1], ctr_in[2], ctr_in[3]};
+    unsigned int k0 = key_in[0], k1 = key_in[1];
+    for (int r = 0; r < 10; ++r) {
+        unsigned long long p0 = (unsigned long long)0xD2511F53u * c[0];
+        unsigned long long p1 = (unsigned long long)0xCD9E8D57u * c[2];
+        unsigned int hi0 = (unsigned int)(p0 >> 32), lo0 = (unsigned int)p0;
+        unsigned int hi1 = (unsigned int)(p1 >> 32), lo1 = (unsigned int)p1;
+        unsigned int n0 = hi1 ^ c[1] ^ k0, n1 = lo1, n2 = hi0 ^ c[3] ^ k1, n3 = lo0;
+        c[0] = n0; c[1] = n1; c[2] = n2; c[3] = n3;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    out[0] = c[0]; out[1] = c[1]; out[2] = c[2]; out[3] = c[3];
+}
+
+/* Dropout factor M_ij s of entry (b, h, i, j): 0 when dropped, the keep scale
+ * 256 / (256 - t) when kept; 1 without dropout. */
+static double dropout_factor(const prob_t *p, int b, int h, int i, int j) {
+    if (p->ext.dropout_t <= 0) return 1.0;
+    unsigned int ctr[4] = {(unsigned int)j >> 4, (unsigned int)i, (unsigned int)(b * p->Hq + h),
+                           p->ext.dropout_offset};
+    unsigned int key[2] = {(unsigned int)p->ext.dropout_seed,
+                           (unsigned int)(p->ext.dropout_seed >> 32)};
+    unsigned int out[4];
+    philox4x32_10(ctr, key, out);
+    unsigned int byte = (out[(j >> 2) & 3] >> (8 * (j & 3))) & 0xFFu;
+    if ((int)byte < p->ext.dropout_t) return 0.0;
+    return 256.0 / (256.0 - p->ext.dropout_t);
+}
+
 static double dot(const double *a, const double *b, int n) {
     double acc = 0.0;
     for (int t = 0; t < n; ++t) acc += a[t] * b[t];
@@ -169,7 +218,8 @@ static double row_forward(const prob_t *p, int b, int h, int i, double *o_out) {
             if (s[j] != -INFINITY) {
                 double pij = exp(s[j] - lse);
                 const double *vj = p->v + row_k(p, b, j, hk);
-                for (int d = 0; d < D; ++d) o_out[d] += pij * vj[d];
+                double f = dropout_factor(p, b, h, i, j);
+                for (int d = 0; d < D; ++d) o_out[d] += pij * f * vj[d];
             }
     }
     free(s);
@@ -209,7 +259,7 @@ static void row_dq(const prob_t *p, int b, int h, int i, double *dq_out, double 
     for (int j = 0; j < lk; ++j) {
         double pij = prob(p, b, h, i, j, lse);
         if (pij == 0.0) continue;
-        double ds = pij * (dprob(p, b, h, i, j) - dv);
+        double ds = pij * (dropout_factor(p, b, h, i, j) * dprob(p, b, h, i, j) - dv);
         const double *kj = p->k + row_k(p, b, j, hk);
         for (int d = 0; d < D; ++d) dq_out[d] += ds * kj[d];
     }
@@ -230,9 +280,10 @@ static void col_dkdv(const prob_t *p, int b, int hk, int j, double *const *lse_g
             if (pij == 0.0) continue;
             const double *doi = p->dout + row_q(p, b, i, h);
             const double *qi = p->q + row_q(p, b, i, h);
-            double ds = pij * (dprob(p, b, h, i, j) - dvec_g[g][i]);
+            double f = dropout_factor(p, b, h, i, j);
+            double ds = pij * (f * dprob(p, b, h, i, j) - dvec_g[g][i]);
             for (int d = 0; d < D; ++d) {
-                dv_out[d] += pij * doi[d];
+                dv_out[d] += pij * f * doi[d];
                 dk_out[d] += ds * qi[d];
             }
         }
@@ -279,6 +330,7 @@ static int make_prob(prob_t *p, const double *q, const double *k, const double *
     p->ext.window_left = p->ext.window_right = -1;
     if (ext) p->ext = *ext;
     if (p->ext.window_left < -1 || p->ext.window_right < -1) return 1;
+    if (p->ext.dropout_t < 0 || p->ext.dropout_t > 255) return 1;
     for (int b = 0; b < B; ++b) {
         if (p->ext.seqused_q &&
             (p->ext.seqused_q[b] < 0 || p->ext.seqused_q[b] > stored_len_q(p, b)))
@@ -454,10 +506,28 @@ int oracle_head_matrices(const double *q, const double *k, const double *v, cons
         for (int j = 0; j < lk; ++j) {
             double pij = prob(&p, b, h, i, j, l);
             P[(long)i * lk + j] = pij;
-            dS[(long)i * lk + j] = pij * (dprob(&p, b, h, i, j) - dvec);
+            dS[(long)i * lk + j] = pij * (dropout_factor(&p, b, h, i, j) * dprob(&p, b, h, i, j) - dvec);
         }
     }
     free(scratch);
+    return 0;
+}
+
+/* Philox4x32-10 of one counter and key, for the known-answer pins. */
+void oracle_philox4x32_10(const unsigned int *ctr, const unsigned int *key, unsigned int *out) {
+    philox4x32_10(ctr, key, out);
+}
+
+/* The dropout factor M s of every (i, j) of one head problem, [Lq, Lk]. */
+int oracle_dropout_factors(int B, int Sq, int Sk, int Hq, int Hkv, int D, const int *cu_q,
+                           const int *cu_k, int b, int h, double *F, const oracle_ext_t *ext) {
+    prob_t p;
+    if (make_prob(&p, NULL, NULL, NULL, NULL, NULL, NULL, B, Sq, Sk, Hq, Hkv, D, 1.0, 0, cu_q, cu_k,
+                  ext))
+        return 1;
+    int lq = seq_len_q(&p, b), lk = seq_len_k(&p, b);
+    for (int i = 0; i < lq; ++i)
+        for (int j = 0; j < lk; ++j) F[(long)i * lk + j] = dropout_factor(&p, b, h, i, j);
     return 0;
 }
 

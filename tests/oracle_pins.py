@@ -20,7 +20,11 @@ AssertionError when the oracle disagrees with:
   problem cut to the used rows; a (0, 0) window in closed form; a bias
   constant along the keys shifts only LSE; a bias constant along the queries
   is one more head-dimension column again; a bias equal to the ALiBi terms
-  equals ALiBi; dBias = dS is the gradient of L by finite differences.
+  equals ALiBi; dBias = dS is the gradient of L by finite differences;
+* dropout: the Philox4x32-10 known-answer vectors, the keep rate, t = 0 equal
+  to no dropout, O / dV equal to P o (M s) times V / dO with the mask built
+  from the generator here, and the backward as the gradient of the dropout
+  forward (fixed seed, finite differences).
 
 ``tests/test_oracle.py`` runs every pin on the real oracle and also on
 mutant builds with a planted mistake, each of which must fail at least one
@@ -553,7 +557,78 @@ def pin_fd_bias(orc):
         _fd_check(orc, q, k, v, do, 0.7, causal, bias=bias)
 
 
+# Known-answer vectors of Philox4x32-10 published with the Random123 library
+# (Salmon et al., SC 2011): (counter, key) -> output words.
+PHILOX_KAT = [
+    ((0, 0, 0, 0), (0, 0), (0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8)),
+    ((0xFFFFFFFF,) * 4, (0xFFFFFFFF,) * 2, (0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD)),
+    ((0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344), (0xA4093822, 0x299F31D0),
+     (0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1)),
+]
+
+
+def pin_philox_known_answers(orc):
+    for ctr, key, want in PHILOX_KAT:
+        assert tuple(orc.philox(ctr, key)) == want, ("philox", ctr, key)
+
+
+def _mask_here(orc, b, h, Hq, lq, lk, t, seed, off):
+    """M * s of one head problem, built from the generator: byte j % 4 of word
+    (j / 4) % 4 of Philox(counter (j / 16, i, b Hq + h, off), key (seed))."""
+    F = np.zeros((lq, lk))
+    key = (seed & 0xFFFFFFFF, seed >> 32)
+    for i in range(lq):
+        for j0 in range(0, lk, 16):
+            out = orc.philox((j0 >> 4, i, b * Hq + h, off), key)
+            for j in range(j0, min(lk, j0 + 16)):
+                byte = (out[(j >> 2) & 3] >> (8 * (j & 3))) & 0xFF
+                F[i, j] = 0.0 if byte < t else 256.0 / (256 - t)
+    return F
+
+
+def pin_dropout_mask_and_rate(orc):
+    """The oracle's mask is the generator's (above); the kept fraction is
+    1 - t / 256 within 5 standard deviations; t = 0 keeps everything."""
+    seed, off = 0x123456789ABCDEF0, 7
+    F = orc.dropout_factors(2, 40, 70, 3, 1, 8, b=1, h=2, dropout=(77, seed, off))
+    _close(F, _mask_here(orc, 1, 2, 3, 40, 70, 77, seed, off), 0, "dropout mask")
+    big = orc.dropout_factors(1, 256, 256, 1, 1, 8, b=0, h=0, dropout=(64, seed, off))
+    kept = float(np.mean(big > 0))
+    sd = np.sqrt(0.75 * 0.25 / big.size)
+    assert abs(kept - 0.75) < 5 * sd, ("keep rate", kept)
+    _close(big[big > 0], np.full(int(np.sum(big > 0)), 256.0 / 192), 0, "keep scale")
+    none = orc.dropout_factors(1, 16, 16, 1, 1, 8, b=0, h=0, dropout=(0, seed, off))
+    _close(none, np.ones_like(none), 0, "t = 0")
+
+
+def pin_dropout_outputs(orc):
+    """O = (P o F) V and dV = (P o F)^T dO with F = M s of the mask built here;
+    t = 0 equals no dropout; the backward is the gradient of its forward."""
+    rng = _rng(80)
+    q, k, v, do = _dense(rng, 2, 9, 11, 2, 1, 3)
+    drop = (90, 0xDEADBEEF12345678, 3)
+    for causal in (False, True):
+        o, lse = orc.forward(q, k, v, 0.6, causal, dropout=drop)
+        _, lp = orc.forward(q, k, v, 0.6, causal)
+        fin = np.isfinite(lp)
+        _close(lse[fin], lp[fin], 0, "dropout leaves LSE")
+        dq, dk, dv = orc.backward(q, k, v, do, 0.6, causal, dropout=drop)
+        dv_here = np.zeros_like(dv)
+        for b in range(2):
+            for h in range(2):
+                P, _ = orc.head_matrices(q, k, v, do, 0.6, causal, b=b, h=h)
+                F = _mask_here(orc, b, h, 2, 9, 11, drop[0], drop[1], drop[2])
+                _close(o[b, :, h], (P * F) @ v[b, :, 0], 1e-13, "dropout O")
+                dv_here[b, :, 0] += (P * F).T @ do[b, :, h]
+        _close(dv, dv_here, 1e-13, "dropout dV")
+        z = orc.backward(q, k, v, do, 0.6, causal, dropout=(0, 5, 5))
+        for a, b_, n in zip(z, orc.backward(q, k, v, do, 0.6, causal), ("dQ", "dK", "dV")):
+            _close(a, b_, 0, "t = 0 " + n)
+        _fd_check(orc, q[:1, :5], k[:1, :6], v[:1, :6], do[:1, :5], 0.6, causal, dropout=drop)
+
+
 ALL_PINS = [pin_preprocess_identity, pin_window_rows_equal_unmasked_band,
+    pin_philox_known_answers, pin_dropout_mask_and_rate, pin_dropout_outputs,
     pin_bias_key_column_equals_augmented, pin_bias_query_row_shifts_lse, pin_bias_equals_alibi,
     pin_fd_bias,
     pin_window_zero_closed_form, pin_fd_window, pin_alibi_causal_equals_augmented,

@@ -51,13 +51,13 @@ def test_rejects_bad_shapes(oracle_mod):
 
 # Each mutant replaces one exact snippet of fa_oracle.c.
 MUTANTS = {
-    "dS sign of D": ("ds = pij * (dprob(p, b, h, i, j) - dv);",
-                     "ds = pij * (dprob(p, b, h, i, j) + dv);"),
-    "dS drops D in dK": ("double ds = pij * (dprob(p, b, h, i, j) - dvec_g[g][i]);",
-                         "double ds = pij * dprob(p, b, h, i, j);"),
+    "dS sign of D": ("ds = pij * (dropout_factor(p, b, h, i, j) * dprob(p, b, h, i, j) - dv);",
+                     "ds = pij * (dropout_factor(p, b, h, i, j) * dprob(p, b, h, i, j) + dv);"),
+    "dS drops D in dK": ("double ds = pij * (f * dprob(p, b, h, i, j) - dvec_g[g][i]);",
+                         "double ds = pij * f * dprob(p, b, h, i, j);"),
     "dK without scale": ("for (int d = 0; d < D; ++d) dk_out[d] *= p->scale;", ""),
     "dQ without scale": ("for (int d = 0; d < D; ++d) dq_out[d] *= p->scale;", ""),
-    "dV uses dS": ("dv_out[d] += pij * doi[d];", "dv_out[d] += ds * doi[d];"),
+    "dV uses dS": ("dv_out[d] += pij * f * doi[d];", "dv_out[d] += ds * doi[d];"),
     "dK uses dO": ("dk_out[d] += ds * qi[d];", "dk_out[d] += ds * doi[d];"),
     "top-left causal": ("if (p->causal && j > i + diag) return 0;",
                         "if (p->causal && j > i) return 0;"),
@@ -82,6 +82,16 @@ MUTANTS = {
     "bias transposed": ("(long)i * p->ext.bias_rs + j];", "(long)j * p->ext.bias_rs + i];"),
     "bias ignores the head stride": ("(long)h * p->ext.bias_hs +", "0 +"),
     "bias scaled": ("        s += p->ext.bias[", "        s += p->scale * p->ext.bias["),
+    "Philox key bump sign": ("k0 += 0x9E3779B9u;", "k0 -= 0x9E3779B9u;"),
+    "Philox word order": ("c[0] = n0; c[1] = n1; c[2] = n2; c[3] = n3;",
+                          "c[0] = n2; c[1] = n1; c[2] = n0; c[3] = n3;"),
+    "dropout without the keep scale": ("return 256.0 / (256.0 - p->ext.dropout_t);", "return 1.0;"),
+    "dropout counter query / key swapped": (
+        "unsigned int ctr[4] = {(unsigned int)j >> 4, (unsigned int)i,",
+        "unsigned int ctr[4] = {(unsigned int)i >> 4, (unsigned int)j,"),
+    "dropout mask missing from dS": ("double ds = pij * (f * dprob(p, b, h, i, j) - dvec_g[g][i]);",
+                                     "double ds = pij * (dprob(p, b, h, i, j) - dvec_g[g][i]);"),
+    "dropout mask missing from dV": ("dv_out[d] += pij * f * doi[d];", "dv_out[d] += pij * doi[d];"),
     "seqused_q ignored": ("return p->ext.seqused_q ? p->ext.seqused_q[b] : stored_len_q(p, b);",
                           "return stored_len_q(p, b);"),
     "Dv from q": ("return dot(doi, o_scratch, p->D);", "return dot(doi, p->q + row_q(p, b, i, h), p->D);"),
