@@ -55,20 +55,25 @@ class FaExt(ctypes.Structure):
                 ("seqused_q", ctypes.c_void_p), ("seqused_k", ctypes.c_void_p),
                 ("bias", ctypes.c_void_p), ("bias_batch_stride", ctypes.c_longlong),
                 ("bias_head_stride", ctypes.c_longlong), ("bias_row_stride", ctypes.c_longlong),
-                ("dbias", ctypes.c_void_p)]
+                ("dbias", ctypes.c_void_p), ("dropout_p", ctypes.c_float),
+                ("dropout_seed", ctypes.c_ulonglong), ("dropout_offset", ctypes.c_uint)]
 
 
 def _ext(Hq, window=None, alibi_slopes=None, seqused_q=None, seqused_k=None, bias=None,
-         dbias=None):
+         dbias=None, dropout=None):
     """A pointer to an FaExt, or None when no extension is asked for.
 
     ``bias``: [B or 1, Hq or 1, Sq, >= Sk] in the input dtype, last axis
     contiguous (a size-1 batch / head axis broadcasts).  ``dbias``: a
-    contiguous [B, Hq, Sq, Sk] output of the input dtype (backward only)."""
+    contiguous [B, Hq, Sq, Sk] output of the input dtype (backward only).
+    ``dropout``: (p, seed, offset), see fa_ext in include/fa.h."""
     if (window is None and alibi_slopes is None and seqused_q is None and seqused_k is None
-            and bias is None and dbias is None):
+            and bias is None and dbias is None and dropout is None):
         return None
-    e = FaExt(-1, -1, None, 0, None, None, None, 0, 0, 0, None)
+    e = FaExt(-1, -1, None, 0, None, None, None, 0, 0, 0, None, 0.0, 0, 0)
+    if dropout is not None:
+        e.dropout_p, e.dropout_seed, e.dropout_offset = (float(dropout[0]), int(dropout[1]),
+                                                         int(dropout[2]))
     if window is not None:
         e.window_left, e.window_right = int(window[0]), int(window[1])
     if alibi_slopes is not None:
@@ -187,13 +192,13 @@ def default_scale(D: int) -> float:
 
 def fa_fwd(q, k, v, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seqlens_k=None,
            max_seqlen_q=None, max_seqlen_k=None, stream=None, window=None, alibi_slopes=None,
-           seqused_q=None, seqused_k=None, bias=None):
+           seqused_q=None, seqused_k=None, bias=None, dropout=None):
     """Forward pass: returns (o, lse); lse fp32 [B,Hq,Sq] or [Hq,total_q].
 
     ``window=(left, right)`` (-1 = unbounded side), ``alibi_slopes`` (fp32
     [Hq] or [B, Hq]), ``seqused_q`` / ``seqused_k`` (int32 [B]) and ``bias``
-    (see ``_ext``) select fa_fwd_ext; rows past the used lengths are left as
-    allocated.
+    (see ``_ext``) and ``dropout=(p, seed, offset)`` select fa_fwd_ext; rows
+    past the used lengths are left as allocated.
     """
     B, Sq, Sk, Hq, Hkv, D = _shape(q, k, cu_seqlens_q, max_seqlen_q, max_seqlen_k)
     scale = default_scale(D) if softmax_scale is None else float(softmax_scale)
@@ -202,7 +207,7 @@ def fa_fwd(q, k, v, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seql
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
     else:
         lse = torch.empty((Hq, q.shape[0]), dtype=torch.float32, device=q.device)
-    ext = _ext(Hq, window, alibi_slopes, seqused_q, seqused_k, bias)
+    ext = _ext(Hq, window, alibi_slopes, seqused_q, seqused_k, bias, dropout=dropout)
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Sq, Sk, Hq, Hkv, D, scale,
             int(bool(causal)), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k)]
     if ext is None:
@@ -215,7 +220,8 @@ def fa_fwd(q, k, v, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seql
 def fa_bwd(q, k, v, o, dout, lse, causal=False, softmax_scale=None, cu_seqlens_q=None,
            cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, deterministic=False,
            dq=None, dk=None, dv=None, workspace=None, stream=None, window=None,
-           alibi_slopes=None, seqused_q=None, seqused_k=None, bias=None, dbias=None):
+           alibi_slopes=None, seqused_q=None, seqused_k=None, bias=None, dbias=None,
+           dropout=None):
     """Backward pass through the C ABI; returns (dq, dk, dv).
 
     Outputs are allocated when not given.  ``workspace`` (a uint8 CUDA tensor
@@ -232,7 +238,7 @@ def fa_bwd(q, k, v, o, dout, lse, causal=False, softmax_scale=None, cu_seqlens_q
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
             _ptr(dv), B, Sq, Sk, Hq, Hkv, D, scale, int(bool(causal)), _ptr(cu_seqlens_q),
             _ptr(cu_seqlens_k), int(bool(deterministic)), _dtype_code(q)]
-    ext = _ext(Hq, window, alibi_slopes, seqused_q, seqused_k, bias, dbias)
+    ext = _ext(Hq, window, alibi_slopes, seqused_q, seqused_k, bias, dbias, dropout)
     if ext is not None:
         st = lib().fa_bwd_ext(*args[:19], ext, *args[19:], _ptr(workspace),
                               0 if workspace is None else workspace.numel(), _stream(stream))

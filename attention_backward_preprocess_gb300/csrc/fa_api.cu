@@ -214,6 +214,9 @@ fa_status apply_ext(fa::BwdParams &p, int causal, const fa_ext *ext) {
     p.bias = nullptr;
     p.bias_bs = p.bias_hs = p.bias_rs = 0;
     p.dbias = nullptr;
+    p.drop_t = 0;
+    p.drop_key0 = p.drop_key1 = p.drop_offset = 0;
+    p.drop_scale = 1.f;
     if (ext) {
         wl = ext->window_left;
         wr = ext->window_right;
@@ -246,6 +249,13 @@ fa_status apply_ext(fa::BwdParams &p, int causal, const fa_ext *ext) {
             if ((reinterpret_cast<uintptr_t>(ext->dbias) & 1u)) return FA_ERR_INVALID_ARG;
             p.dbias = ext->dbias;
         }
+        const float dp = ext->dropout_p;
+        if (!(dp >= 0.f && dp < 1.f)) return FA_ERR_INVALID_ARG;
+        p.drop_t = std::min(255, (int)(dp * 256.f + 0.5f));
+        p.drop_key0 = (uint32_t)ext->dropout_seed;
+        p.drop_key1 = (uint32_t)(ext->dropout_seed >> 32);
+        p.drop_offset = ext->dropout_offset;
+        p.drop_scale = 256.f / (float)(256 - p.drop_t);
     }
     p.win_lo = (wl < 0 || wl >= fa::kNoWindow) ? fa::kNoWindow : wl;
     p.win_hi = (wr < 0 || wr >= fa::kNoWindow) ? fa::kNoWindow : wr;

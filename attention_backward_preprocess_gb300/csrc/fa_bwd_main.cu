@@ -258,16 +258,16 @@ struct MainMaps {
 
 // kMode 0: the plain kernel (no mask, or a band with an upper edge only, e.g.
 // causal).  1: a band with a lower edge (a left window).  2: as 1 plus ALiBi.
-// 3: as 2 plus the elementwise bias and / or dBias.  Separate instances: the
-// code of each extension slows the softmax warps even when it is skipped at
-// run time (measured: the bias code made a windowed run 1.8x slower, the
-// ALiBi arithmetic 11 %).
+// 3: as 2 plus the elementwise bias and / or dBias.  4: as 3 plus dropout.
+// Separate instances: the code of each extension slows the softmax warps even
+// when it is skipped at run time (measured: the bias code made a windowed run
+// 1.8x slower, the ALiBi arithmetic 11 %).
 template <int kD, typename T, int kMode>
 __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
     bwd_main_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ MainMaps maps) {
     using C = MainCfg<kD, T>;
     constexpr int D = C::D, BM = C::BM, BN = C::BN, S = C::kStages, HALF = C::HALF, NCH = C::NCH;
-    constexpr bool kExt = kMode >= 1, kAlibi = kMode >= 2, kBias = kMode == 3;
+    constexpr bool kExt = kMode >= 1, kAlibi = kMode >= 2, kBias = kMode >= 3, kDrop = kMode == 4;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -844,6 +844,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 // column 8k + 2*q4 + e of the chunk.  A thread thus needs 8
                 // LSE2 / Dv values per chunk (4 eight-byte loads) instead of 32.
                 float P[HALF];
+                uint32_t kbits[NCH];   // dropout: bit 16h + 4k + 2r + e of chunk ch = kept
                 __syncwarp();
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch) {
@@ -858,6 +859,21 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                         nl2[k] = f2_pack(-l.x, -l.y);
                     }
                     const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+                    // dropout: lane L draws the random bytes of query c0 + L for
+                    // the warp's 32 keys (two Philox outputs of 16 keys); the
+                    // other lanes fetch theirs with shuffles below
+                    uint4 rnd[2];
+                    if (kDrop) {
+                        const uint32_t hq = (uint32_t)(u.hk * p.G + u.g_of(it, p.G));
+#pragma unroll
+                        for (int g = 0; g < 2; ++g)
+                            rnd[g] = philox4x32_10(
+                                make_uint4((uint32_t)((n0 + 32 * quarter) >> 4) + g,
+                                           (uint32_t)(m0 + c0 + lane), (uint32_t)u.b * p.Hq + hq,
+                                           p.drop_offset),
+                                p.drop_key0, p.drop_key1);
+                        kbits[ch] = 0u;
+                    }
                     tmem_wait_ld();
                     // element (key kb + kr, query column 8k + e) has
                     // kj - qi - diag = lim + kr - 8k - e
@@ -896,6 +912,21 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                                 }
                                 float pv0 = ex2(x0);
                                 float pv1 = ex2(x1);
+                                bool keep0 = true, keep1 = true;
+                                if (kDrop) {
+                                    // key kb + kr is byte g4 % 4 of word (g4 / 4) + 2r of
+                                    // output h; query 8k + 2q4 + e was drawn by that lane
+                                    const int src = 8 * k + 2 * q4;
+                                    uint32_t wv[2];
+#pragma unroll
+                                    for (int e = 0; e < 2; ++e) {
+                                        const uint32_t a0 = __shfl_sync(0xffffffffu, r == 0 ? rnd[h].x : rnd[h].z, src + e);
+                                        const uint32_t a1 = __shfl_sync(0xffffffffu, r == 0 ? rnd[h].y : rnd[h].w, src + e);
+                                        wv[e] = (g4 >> 2) ? a1 : a0;
+                                    }
+                                    keep0 = (int)((wv[0] >> (8 * (g4 & 3))) & 0xFFu) >= p.drop_t;
+                                    keep1 = (int)((wv[1] >> (8 * (g4 & 3))) & 0xFFu) >= p.drop_t;
+                                }
                                 if (masked_hi) {   // lim + kr - 8k - e > whi
                                     if (lim_hi + kr > 8 * k) pv0 = 0.f;
                                     if (lim_hi + kr > 8 * k + 1) pv1 = 0.f;
@@ -907,7 +938,14 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                                 if (kb + kr >= u.lk) { pv0 = 0.f; pv1 = 0.f; }
                                 P[32 * ch + 16 * h + 4 * k + 2 * r] = pv0;
                                 P[32 * ch + 16 * h + 4 * k + 2 * r + 1] = pv1;
-                                pk[2 * k + r] = Cvt<T>::pack(pv0, pv1);
+                                if (kDrop) {
+                                    // dV takes the dropped-out, rescaled P
+                                    kbits[ch] |= ((keep0 ? 1u : 0u) | (keep1 ? 2u : 0u)) << (16 * h + 4 * k + 2 * r);
+                                    pk[2 * k + r] = Cvt<T>::pack(keep0 ? pv0 * p.drop_scale : 0.f,
+                                                                 keep1 ? pv1 * p.drop_scale : 0.f);
+                                } else {
+                                    pk[2 * k + r] = Cvt<T>::pack(pv0, pv1);
+                                }
                             }
                         }
                         tmem_st16x128(lane_addr + ((uint32_t)(16 * h) << 16) + C::p_col(cb, grp, ch), pk);
@@ -952,11 +990,14 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
 #pragma unroll
                             for (int r = 0; r < 2; ++r) {
                                 const int e0 = 32 * ch + 16 * h + 4 * k + 2 * r;
-                                const float2 ds = f2_unpack(f2_mul(
-                                    f2_pack(P[e0], P[e0 + 1]),
-                                    f2_sub(f2_pack(__uint_as_float(dr[h][4 * k + 2 * r]),
-                                                   __uint_as_float(dr[h][4 * k + 2 * r + 1])),
-                                           dd[k])));
+                                uint64_t dpv = f2_pack(__uint_as_float(dr[h][4 * k + 2 * r]),
+                                                       __uint_as_float(dr[h][4 * k + 2 * r + 1]));
+                                if (kDrop) {   // dS = P (M s dP - Dv)
+                                    const uint32_t kb2 = kbits[ch] >> (16 * h + 4 * k + 2 * r);
+                                    dpv = f2_mul(dpv, f2_pack((kb2 & 1u) ? p.drop_scale : 0.f,
+                                                              (kb2 & 2u) ? p.drop_scale : 0.f));
+                                }
+                                const float2 ds = f2_unpack(f2_mul(f2_pack(P[e0], P[e0 + 1]), f2_sub(dpv, dd[k])));
                                 pk[2 * k + r] = Cvt<T>::pack(ds.x, ds.y);
                                 if (kBias && dbias_h) {   // dBias = dS, inside the used lengths
                                     const int qi0 = m0 + c0 + 8 * k + 2 * q4, kj = kb + 16 * h + 8 * r;
@@ -1053,7 +1094,8 @@ template <int kD, typename T>
 static cudaError_t launch_main_t(const BwdParams &p, const MainMaps &maps, int grid,
                                  cudaStream_t stream) {
     using C = MainCfg<kD, T>;
-    auto kern = (p.bias || p.dbias) ? bwd_main_kernel<kD, T, 3>
+    auto kern = p.drop_t > 0          ? bwd_main_kernel<kD, T, 4>
+                : (p.bias || p.dbias) ? bwd_main_kernel<kD, T, 3>
                 : p.alibi               ? bwd_main_kernel<kD, T, 2>
                 : p.win_lo < kNoWindow  ? bwd_main_kernel<kD, T, 1>
                                         : bwd_main_kernel<kD, T, 0>;

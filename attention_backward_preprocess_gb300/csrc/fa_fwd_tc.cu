@@ -71,8 +71,9 @@ enum {
 constexpr float kRescaleLog2 = 8.f;
 
 // kMode 0: plain scores.  1: with the ALiBi bias (p.alibi).  2: with the
-// elementwise bias (p.bias) and ALiBi if given.  Separate instances: the bias
-// code slows the softmax even when skipped at run time.
+// elementwise bias (p.bias) and ALiBi if given.  3: dropout, with ALiBi and
+// the bias if given.  Separate instances: the code of an extension slows the
+// softmax even when skipped at run time.
 template <int kD, typename T, int kMode>
 __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap map_q,
@@ -80,7 +81,7 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                   void *o_out, float *lse_out, int nmb) {
     using C = FwdCfg<kD, T>;
     constexpr int D = C::D, BM = C::BM, BN = C::BN, S = C::kStages;
-    constexpr bool kExt = kMode >= 1, kBias = kMode == 2;
+    constexpr bool kExt = kMode >= 1, kBias = kMode >= 2, kDrop = kMode == 3;
     // ---- tile of this CTA: longest causal rows first
     const int bh = blockIdx.x % (p.B * p.Hq);
     const int m = nmb - 1 - blockIdx.x / (p.B * p.Hq);
@@ -305,6 +306,17 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                     tmem_ld32(scol + 32 * c, sr);
                     float bl[32];
                     if (kBias) load_bias(bl, kb + 32 * c);
+                    // dropout: random bytes of keys kb + 32c .. +31 of this row,
+                    // 16 keys per Philox output
+                    uint4 rnd[2];
+                    if (kDrop) {
+#pragma unroll
+                        for (int g = 0; g < 2; ++g)
+                            rnd[g] = philox4x32_10(
+                                make_uint4((uint32_t)((kb + 32 * c) >> 4) + g, (uint32_t)qi,
+                                           (uint32_t)(b * p.Hq + h), p.drop_offset),
+                                p.drop_key0, p.drop_key1);
+                    }
                     tmem_wait_ld();
                     uint32_t pk[16];
 #pragma unroll
@@ -322,7 +334,19 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                             p0 = (e >= lo && e <= hi) ? p0 : 0.f;
                             p1 = (e + 1 >= lo && e + 1 <= hi) ? p1 : 0.f;
                         }
-                        sum += p0 + p1;
+                        sum += p0 + p1;   // the row sum is taken before dropout
+                        if (kDrop) {
+                            // keys 2i, 2i + 1 of the chunk: bytes (2i) % 4, +1 of
+                            // word (2i / 4) % 4 of output 2i / 16
+                            const uint4 &R = rnd[i >> 3];
+                            const int wi = (i >> 1) & 3;
+                            const uint32_t word = wi == 0 ? R.x : wi == 1 ? R.y : wi == 2 ? R.z : R.w;
+                            const int sh = 8 * ((2 * i) & 3);
+                            const bool k0 = (int)((word >> sh) & 0xFFu) >= p.drop_t;
+                            const bool k1 = (int)((word >> (sh + 8)) & 0xFFu) >= p.drop_t;
+                            p0 = k0 ? p0 * p.drop_scale : 0.f;
+                            p1 = k1 ? p1 * p.drop_scale : 0.f;
+                        }
                         pk[i] = Cvt<T>::pack(p0, p1);
                     }
                     tmem_st16(scol + 16 * c, pk);
@@ -411,7 +435,10 @@ cudaError_t launch_fwd_tc_t(const BwdParams &p, const CUtensorMap &mq, const CUt
                             const CUtensorMap &mv, void *o, float *lse, int max_lq,
                             cudaStream_t stream) {
     using C = FwdCfg<kD, T>;
-    auto kern = p.bias ? fwd_tc_kernel<kD, T, 2> : p.alibi ? fwd_tc_kernel<kD, T, 1> : fwd_tc_kernel<kD, T, 0>;
+    auto kern = p.drop_t > 0 ? fwd_tc_kernel<kD, T, 3>
+                : p.bias       ? fwd_tc_kernel<kD, T, 2>
+                : p.alibi      ? fwd_tc_kernel<kD, T, 1>
+                               : fwd_tc_kernel<kD, T, 0>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;

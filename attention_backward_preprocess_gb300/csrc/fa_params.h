@@ -39,6 +39,13 @@ struct BwdParams {
     long long bias_bs, bias_hs, bias_rs;
     // backward: dBias = dS written as [B, Hq, Sq, Sk] (input dtype); null: not
     void *dbias;
+    // dropout: entry (b, h, i, j) kept iff byte j % 4 of word (j / 4) % 4 of
+    // Philox4x32-10(counter (j / 16, i, b * Hq + h, drop_offset), key
+    // (drop_key0, drop_key1)) is >= drop_t; kept entries scaled by drop_scale
+    // = 256 / (256 - drop_t).  drop_t = 0: no dropout
+    int drop_t;
+    uint32_t drop_key0, drop_key1, drop_offset;
+    float drop_scale;
     // workspace
     int *err;           // device error word
     int4 *tiles;        // work units (b, n_block, hk, 0)

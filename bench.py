@@ -189,6 +189,7 @@ def main():
     ap.add_argument("--alibi", action="store_true", help="ALiBi slopes 2^(-8 h / Hq)")
     ap.add_argument("--bias", action="store_true",
                     help="elementwise bias [B, Hq, Sq, Sk] and its gradient dBias")
+    ap.add_argument("--dropout", type=float, default=0.0, help="dropout probability")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -196,7 +197,7 @@ def main():
     w = WORKLOADS[args.workload or BENCH_WORKLOAD]
     if args.impl == "reference":
         return run_reference(args, w)
-    if args.window or args.alibi or args.bias:
+    if args.window or args.alibi or args.bias or args.dropout > 0:
         return run_ext(args, w)
 
     import torch
@@ -456,6 +457,8 @@ def run_ext(args, w):
         g = torch.Generator(device=dev).manual_seed(7)
         ext["bias"] = torch.randn((w.B, w.Hq, w.Sq, w.Sk), generator=g, device=dev).to(q.dtype)
         dbias = torch.empty_like(ext["bias"])
+    if args.dropout > 0:
+        ext["dropout"] = (args.dropout, 0x5EED, 0)
     lengths = x.get("lengths") or [w.Sq] * w.B
     pairs = sum(visible_pairs(L, L if varlen else w.Sk, w.causal, wl, wr) for L in lengths) * w.Hq
     fl_fwd, fl_bwd = 4.0 * w.D * pairs, 10.0 * w.D * pairs
@@ -501,7 +504,7 @@ def run_ext(args, w):
     status = fa.device_status(work)
     fstatus = fa.device_status()
     pk = peaks()
-    exts = {k_: (list(v_) if k_ == "window" else True) for k_, v_ in ext.items()}
+    exts = {k_: (list(v_) if k_ in ("window", "dropout") else True) for k_, v_ in ext.items()}
     if dbias is not None:
         exts["dbias"] = True
     line = {

@@ -175,6 +175,16 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
  *   [B, Hq, Sq, Sk] tensor in the input dtype, fully overwritten: 0 wherever
  *   dS is 0 (masked entries, tiles no work unit visits, rows and columns past
  *   the used lengths). */
+/* dropout_p in [0, 1): dropout on P, as on the Composable Kernel page
+ *   (FmhaDropout: dropped entries drop out of dV and of dP, kept ones are
+ *   scaled by 1 / (1 - p)).  The drop probability is quantised to t / 256,
+ *   t = round(256 p) (at most 255), and the keep scale is 256 / (256 - t).
+ *   The mask is a pure function of (dropout_seed, dropout_offset, sequence,
+ *   query head, i, j): entry (b, h, i, j) is dropped iff byte j % 4 of word
+ *   (j / 4) % 4 of Philox4x32-10 (Salmon et al., SC 2011) with counter
+ *   (j / 16, i, b * Hq + h, dropout_offset) and key (low, high 32 bits of
+ *   dropout_seed) is below t.  fa_bwd_ext must get the forward's seed and
+ *   offset.  The pages print no generator; this one is the reading taken. */
 typedef struct {
     int window_left;
     int window_right;
@@ -187,6 +197,9 @@ typedef struct {
     long long bias_head_stride;
     long long bias_row_stride;
     void *dbias;
+    float dropout_p;
+    unsigned long long dropout_seed;
+    unsigned int dropout_offset;
 } fa_ext;
 
 /* fa_fwd with extensions.  Errors as fa_fwd, plus FA_ERR_INVALID_ARG for a

@@ -66,6 +66,12 @@ def _options(w, opt, seed=5):
         view = full.cuda()[..., :w.Sk]
         ok["bias"] = to64(full[..., :w.Sk].contiguous())
         gk["bias"] = view
+    if "dropout" in opt:
+        # the library quantises p to t / 256, t = round(256 p) in fp32 (at most 255)
+        pr, seed, off = opt["dropout"]
+        t = min(255, int(np.float32(pr) * np.float32(256) + np.float32(0.5)))
+        ok["dropout"] = (t, seed, off)
+        gk["dropout"] = (pr, seed, off)
     return ok, gk
 
 
@@ -203,6 +209,52 @@ def test_bias_forward_backward_dbias(fa, oracle_mod, cuda_device, w, opt):
     outs = _run_bwd(fa, w, x, dict(gk, dbias=dbias))
     _check_bwd(oracle_mod, w, x, ok, outs)
     check_bar(dbias, _oracle_dbias(oracle_mod, w, x, ok), "dbias")
+
+
+DROP_CASES = [
+    (W("drop_causal_d128_gqa", 2, 300, 300, 4, 2, 128, causal=True),
+     dict(dropout=(0.1, 0x0123456789ABCDEF, 0))),
+    (W("drop_d64_fp16_sq_lt_sk", 1, 190, 333, 2, 2, 64, "fp16"),
+     dict(dropout=(0.3, 42, 7))),
+    (W("drop_alibi_win_d128", 1, 260, 260, 2, 1, 128, causal=True),
+     dict(dropout=(0.2, 99, 1), alibi="h", window=(100, -1))),
+    (W("drop_bias_d96", 2, 200, 200, 2, 2, 96), dict(dropout=(0.15, 5, 3), bias="b1")),
+]
+
+
+@pytest.mark.parametrize("w,opt", DROP_CASES, ids=lambda v: v.name if hasattr(v, "name") else "")
+def test_dropout_forward_backward(fa, oracle_mod, cuda_device, w, opt):
+    x, ok, gk = _case(oracle_mod, w, opt)
+    o, lse = fa.fa_fwd(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), causal=w.causal,
+                       softmax_scale=w.softmax_scale, **gk)
+    torch.cuda.synchronize()
+    check_bar(o, x["o64"], "o")
+    fin = np.isfinite(x["lse64"])
+    assert np.max(np.abs(to64(lse)[fin] - x["lse64"][fin])) < 1e-4
+    extra = {}
+    if "bias" in gk:
+        extra["dbias"] = torch.full((w.B, w.Hq, w.Sq, w.Sk), SENTINEL, dtype=w.torch_dtype,
+                                    device="cuda")
+    outs = _run_bwd(fa, w, x, dict(gk, **extra))
+    _check_bwd(oracle_mod, w, x, ok, outs)
+    if extra:
+        check_bar(extra["dbias"], _oracle_dbias(oracle_mod, w, x, ok), "dbias")
+
+
+def test_dropout_varlen_and_deterministic(fa, oracle_mod, cuda_device):
+    w = W("drop_vl_d128", 3, 0, 0, 2, 1, 128, "bf16", True, varlen=(3, 1, 300),
+          deterministic=True)
+    opt = dict(dropout=(0.25, 1234567, 11))
+    x, ok, gk = _case(oracle_mod, w, opt, lengths=[300, 129, 40])
+    o, lse = fa.fa_fwd(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), causal=w.causal,
+                       softmax_scale=w.softmax_scale, **_kw(w, x), **gk)
+    torch.cuda.synchronize()
+    check_bar(o, x["o64"], "o")
+    a = _run_bwd(fa, w, x, gk, deterministic=True)
+    b = _run_bwd(fa, w, x, gk, deterministic=True)
+    for t, u in zip(a, b):
+        assert torch.equal(t.view(torch.int16), u.view(torch.int16))
+    _check_bwd(oracle_mod, w, x, ok, a)
 
 
 def test_dbias_without_bias(fa, oracle_mod, cuda_device):
