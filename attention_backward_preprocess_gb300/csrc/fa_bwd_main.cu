@@ -256,18 +256,24 @@ struct MainMaps {
     CUtensorMap q, k, v, dout;
 };
 
-// kMode 0: the plain kernel (no mask, or a band with an upper edge only, e.g.
-// causal).  1: a band with a lower edge (a left window).  2: as 1 plus ALiBi.
-// 3: as 2 plus the elementwise bias and / or dBias.  4: as 3 plus dropout.
-// Separate instances: the code of each extension slows the softmax warps even
-// when it is skipped at run time (measured: the bias code made a windowed run
-// 1.8x slower, the ALiBi arithmetic 11 %).
-template <int kD, typename T, int kMode>
+// Extension flags of an instance: a band with a lower edge (a left window),
+// ALiBi, the elementwise bias / dBias, dropout.  Without flags: the plain
+// kernel (no mask, or a band with an upper edge only, e.g. causal).  Each
+// extension gets compiled in only where asked for: its code slows the softmax
+// warps even when skipped at run time (measured: the bias code made a
+// windowed run 1.8x slower, the ALiBi arithmetic 11 %).
+enum : int { kFBand = 1, kFAlibi = 2, kFBias = 4, kFDrop = 8 };
+// the instances built, each a superset of the flags before it in its chain
+constexpr int kMainFlagSets[] = {0, kFBand, kFBand | kFAlibi, kFBand | kFAlibi | kFBias,
+                                 kFBand | kFDrop, kFBand | kFAlibi | kFBias | kFDrop};
+
+template <int kD, typename T, int kFlags>
 __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
     bwd_main_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ MainMaps maps) {
     using C = MainCfg<kD, T>;
     constexpr int D = C::D, BM = C::BM, BN = C::BN, S = C::kStages, HALF = C::HALF, NCH = C::NCH;
-    constexpr bool kExt = kMode >= 1, kAlibi = kMode >= 2, kBias = kMode >= 3, kDrop = kMode == 4;
+    constexpr bool kExt = (kFlags & kFBand) != 0, kAlibi = (kFlags & kFAlibi) != 0,
+                   kBias = (kFlags & kFBias) != 0, kDrop = (kFlags & kFDrop) != 0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -833,6 +839,51 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                         dbias_h = reinterpret_cast<uint16_t *>(p.dbias) +
                                   ((long long)u.b * p.Hq + hq) * p.Sq * p.Sk;
                 }
+                // dropout: drawn before S is ready (the wait hides it).  Lane L
+                // draws the random bytes of query c0 + L of each chunk for the
+                // warp's 32 keys (two Philox outputs of 16 keys) and packs the
+                // keep flags into one word (bit l: key n0 + 32 quarter + l); a
+                // thread then takes the words of its 8 queries by shuffles and
+                // keeps the 32 flags of its own elements in one word:
+                // kb32[ch] bit 4 (2k + e) + 2h + r = (key kb + 16h + 8r, query
+                // c0 + 8k + 2q4 + e) kept.
+                uint32_t kb32[NCH];
+                if (kDrop) {
+                    const uint32_t hq = (uint32_t)(u.hk * p.G + u.g_of(it, p.G));
+                    const uint32_t tt4 = (uint32_t)p.drop_t * 0x01010101u;
+#pragma unroll
+                    for (int ch = 0; ch < NCH; ++ch) {
+                        const int c0 = grp * HALF + 32 * ch;
+                        uint32_t kmask = 0u;
+#pragma unroll
+                        for (int g = 0; g < 2; ++g) {
+                            const uint4 R = philox4x32_10(
+                                make_uint4((uint32_t)((n0 + 32 * quarter) >> 4) + g,
+                                           (uint32_t)(m0 + c0 + lane), (uint32_t)u.b * p.Hq + hq,
+                                           p.drop_offset),
+                                p.drop_key0, p.drop_key1);
+                            const uint32_t wd[4] = {R.x, R.y, R.z, R.w};
+#pragma unroll
+                            for (int wi = 0; wi < 4; ++wi) {
+                                // bytes >= t -> 0xFF; the low bits of the 4 bytes
+                                // gathered into bits 28-31 by one product
+                                const uint32_t ge = __vcmpgeu4(wd[wi], tt4) & 0x01010101u;
+                                kmask |= ((ge * 0x10204080u) >> 28) << (16 * g + 4 * wi);
+                            }
+                        }
+                        kb32[ch] = 0u;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                // bits 0, 8, 16, 24 after the shift: (h, r) = (0, 0),
+                                // (0, 1), (1, 0), (1, 1); gathered to 4 bits
+                                const uint32_t x =
+                                    (__shfl_sync(0xffffffffu, kmask, 8 * k + 2 * q4 + e) >> g4) & 0x01010101u;
+                                kb32[ch] |= ((x * 0x10204080u) >> 28) << (4 * (2 * k + e));
+                            }
+                    }
+                }
                 if (!(ok = mbar_wait(bar(B_STAGE0 + stage), st_ph, w))) break;
                 if (!(ok = mbar_wait(bar(B_S_FULL + cb), bit(s_ph, cb), w))) break;
                 s_ph ^= 1u << cb;
@@ -844,7 +895,6 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 // column 8k + 2*q4 + e of the chunk.  A thread thus needs 8
                 // LSE2 / Dv values per chunk (4 eight-byte loads) instead of 32.
                 float P[HALF];
-                uint32_t kbits[NCH];   // dropout: bit 16h + 4k + 2r + e of chunk ch = kept
                 __syncwarp();
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch) {
@@ -859,21 +909,6 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                         nl2[k] = f2_pack(-l.x, -l.y);
                     }
                     const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
-                    // dropout: lane L draws the random bytes of query c0 + L for
-                    // the warp's 32 keys (two Philox outputs of 16 keys); the
-                    // other lanes fetch theirs with shuffles below
-                    uint4 rnd[2];
-                    if (kDrop) {
-                        const uint32_t hq = (uint32_t)(u.hk * p.G + u.g_of(it, p.G));
-#pragma unroll
-                        for (int g = 0; g < 2; ++g)
-                            rnd[g] = philox4x32_10(
-                                make_uint4((uint32_t)((n0 + 32 * quarter) >> 4) + g,
-                                           (uint32_t)(m0 + c0 + lane), (uint32_t)u.b * p.Hq + hq,
-                                           p.drop_offset),
-                                p.drop_key0, p.drop_key1);
-                        kbits[ch] = 0u;
-                    }
                     tmem_wait_ld();
                     // element (key kb + kr, query column 8k + e) has
                     // kj - qi - diag = lim + kr - 8k - e
@@ -898,6 +933,8 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                                     const float fd = flim + (float)(kr - 8 * k);
                                     x0 = fmaf(-slope2, fabsf(fd), x0);
                                     x1 = fmaf(-slope2, fabsf(fd - 1.f), x1);
+                                }
+                                {
                                     if (kBias && bias_h) {   // + bias * log2e (0 past the used lengths)
                                         const int qi0 = m0 + c0 + 8 * k + 2 * q4, kj = kb + kr;
                                         float b0 = 0.f, b1 = 0.f;
@@ -914,18 +951,8 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                                 float pv1 = ex2(x1);
                                 bool keep0 = true, keep1 = true;
                                 if (kDrop) {
-                                    // key kb + kr is byte g4 % 4 of word (g4 / 4) + 2r of
-                                    // output h; query 8k + 2q4 + e was drawn by that lane
-                                    const int src = 8 * k + 2 * q4;
-                                    uint32_t wv[2];
-#pragma unroll
-                                    for (int e = 0; e < 2; ++e) {
-                                        const uint32_t a0 = __shfl_sync(0xffffffffu, r == 0 ? rnd[h].x : rnd[h].z, src + e);
-                                        const uint32_t a1 = __shfl_sync(0xffffffffu, r == 0 ? rnd[h].y : rnd[h].w, src + e);
-                                        wv[e] = (g4 >> 2) ? a1 : a0;
-                                    }
-                                    keep0 = (int)((wv[0] >> (8 * (g4 & 3))) & 0xFFu) >= p.drop_t;
-                                    keep1 = (int)((wv[1] >> (8 * (g4 & 3))) & 0xFFu) >= p.drop_t;
+                                    keep0 = (kb32[ch] >> (4 * (2 * k) + 2 * h + r)) & 1u;
+                                    keep1 = (kb32[ch] >> (4 * (2 * k + 1) + 2 * h + r)) & 1u;
                                 }
                                 if (masked_hi) {   // lim + kr - 8k - e > whi
                                     if (lim_hi + kr > 8 * k) pv0 = 0.f;
@@ -940,7 +967,6 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                                 P[32 * ch + 16 * h + 4 * k + 2 * r + 1] = pv1;
                                 if (kDrop) {
                                     // dV takes the dropped-out, rescaled P
-                                    kbits[ch] |= ((keep0 ? 1u : 0u) | (keep1 ? 2u : 0u)) << (16 * h + 4 * k + 2 * r);
                                     pk[2 * k + r] = Cvt<T>::pack(keep0 ? pv0 * p.drop_scale : 0.f,
                                                                  keep1 ? pv1 * p.drop_scale : 0.f);
                                 } else {
@@ -993,9 +1019,9 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                                 uint64_t dpv = f2_pack(__uint_as_float(dr[h][4 * k + 2 * r]),
                                                        __uint_as_float(dr[h][4 * k + 2 * r + 1]));
                                 if (kDrop) {   // dS = P (M s dP - Dv)
-                                    const uint32_t kb2 = kbits[ch] >> (16 * h + 4 * k + 2 * r);
-                                    dpv = f2_mul(dpv, f2_pack((kb2 & 1u) ? p.drop_scale : 0.f,
-                                                              (kb2 & 2u) ? p.drop_scale : 0.f));
+                                    const uint32_t k0b = (kb32[ch] >> (4 * (2 * k) + 2 * h + r)) & 1u;
+                                    const uint32_t k1b = (kb32[ch] >> (4 * (2 * k + 1) + 2 * h + r)) & 1u;
+                                    dpv = f2_mul(dpv, f2_pack(k0b ? p.drop_scale : 0.f, k1b ? p.drop_scale : 0.f));
                                 }
                                 const float2 ds = f2_unpack(f2_mul(f2_pack(P[e0], P[e0 + 1]), f2_sub(dpv, dd[k])));
                                 pk[2 * k + r] = Cvt<T>::pack(ds.x, ds.y);
@@ -1090,15 +1116,23 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
 
 }  // namespace
 
+template <int kD, typename T, int kI = 0>
+static auto main_kernel_for(int need) {
+    // the first instance built that has every flag needed
+    constexpr int f = kMainFlagSets[kI];
+    if constexpr (kI + 1 < (int)(sizeof(kMainFlagSets) / sizeof(int))) {
+        if ((need & f) != need) return main_kernel_for<kD, T, kI + 1>(need);
+    }
+    return bwd_main_kernel<kD, T, f>;
+}
+
 template <int kD, typename T>
 static cudaError_t launch_main_t(const BwdParams &p, const MainMaps &maps, int grid,
                                  cudaStream_t stream) {
     using C = MainCfg<kD, T>;
-    auto kern = p.drop_t > 0          ? bwd_main_kernel<kD, T, 4>
-                : (p.bias || p.dbias) ? bwd_main_kernel<kD, T, 3>
-                : p.alibi               ? bwd_main_kernel<kD, T, 2>
-                : p.win_lo < kNoWindow  ? bwd_main_kernel<kD, T, 1>
-                                        : bwd_main_kernel<kD, T, 0>;
+    const int need = (p.win_lo < kNoWindow ? kFBand : 0) | (p.alibi ? kFAlibi : 0) |
+                     ((p.bias || p.dbias) ? kFBias : 0) | (p.drop_t > 0 ? kFDrop : 0);
+    auto kern = main_kernel_for<kD, T>(need);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;

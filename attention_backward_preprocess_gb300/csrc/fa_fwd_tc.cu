@@ -70,18 +70,25 @@ enum {
 // that may lag the true one by up to this much.
 constexpr float kRescaleLog2 = 8.f;
 
-// kMode 0: plain scores.  1: with the ALiBi bias (p.alibi).  2: with the
-// elementwise bias (p.bias) and ALiBi if given.  3: dropout, with ALiBi and
-// the bias if given.  Separate instances: the code of an extension slows the
-// softmax even when skipped at run time.
-template <int kD, typename T, int kMode>
+// Extension flags of an instance: ALiBi, the elementwise bias, dropout (the
+// band needs none: only edge blocks test it).  Each extension gets compiled in
+// only where asked for: its code slows the softmax even when skipped at run
+// time.
+enum : int { kFwdAlibi = 2, kFwdBias = 4, kFwdDrop = 8 };
+// the instances built, each a superset of the flags before it in its chain
+constexpr int kFwdFlagSets[] = {0, kFwdAlibi, kFwdAlibi | kFwdBias, kFwdDrop,
+                                kFwdAlibi | kFwdBias | kFwdDrop};
+
+template <int kD, typename T, int kFlags>
 __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap map_q,
                   const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                   void *o_out, float *lse_out, int nmb) {
     using C = FwdCfg<kD, T>;
     constexpr int D = C::D, BM = C::BM, BN = C::BN, S = C::kStages;
-    constexpr bool kExt = kMode >= 1, kBias = kMode >= 2, kDrop = kMode == 3;
+    constexpr bool kAlibi = (kFlags & kFwdAlibi) != 0, kBias = (kFlags & kFwdBias) != 0,
+                   kDrop = (kFlags & kFwdDrop) != 0;
+    constexpr bool kExt = kAlibi || kBias;   // scores other than the plain scaled ones
     // ---- tile of this CTA: longest causal rows first
     const int bh = blockIdx.x % (p.B * p.Hq);
     const int m = nmb - 1 - blockIdx.x / (p.B * p.Hq);
@@ -221,7 +228,7 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
         const int kmin = (int)max(0LL, (long long)qi + diag - p.win_lo);
         const int kmax = (int)min((long long)lk - 1, (long long)qi + diag + p.win_hi);
         // ALiBi slope of this head, log2 units
-        const float slope2 = (kExt && p.alibi)
+        const float slope2 = (kAlibi && p.alibi)
                                  ? __ldg(p.alibi + (long long)b * p.alibi_bstride + h) * 1.4426950408889634f
                                  : 0.f;
         // elementwise bias row of this query (null: none, or a padding row)
@@ -256,17 +263,41 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
         bool ok = true;
         for (int n = 0; n < nblk; ++n) {
             const int bb = n & 1;
+            const int kb = (n_begin + n) * BN;
+            // dropout keep flags of this row's 128 keys (bit l of kw[c]: key
+            // kb + 32c + l), drawn before S is ready (the wait hides them)
+            uint32_t kw[BN / 32];
+            if (kDrop) {
+                const uint32_t tt4 = (uint32_t)p.drop_t * 0x01010101u;
+#pragma unroll
+                for (int g = 0; g < BN / 16; ++g) {
+                    const uint4 R = philox4x32_10(make_uint4((uint32_t)(kb >> 4) + g, (uint32_t)qi,
+                                                             (uint32_t)(b * p.Hq + h), p.drop_offset),
+                                                  p.drop_key0, p.drop_key1);
+                    const uint32_t wd[4] = {R.x, R.y, R.z, R.w};
+                    uint32_t bits = 0u;
+#pragma unroll
+                    for (int wi = 0; wi < 4; ++wi) {
+                        // bytes >= t -> 0xFF; the low bits of the 4 bytes gathered
+                        // into bits 28-31 by one product
+                        const uint32_t ge = __vcmpgeu4(wd[wi], tt4) & 0x01010101u;
+                        bits |= ((ge * 0x10204080u) >> 28) << (4 * wi);
+                    }
+                    if (g & 1) kw[g >> 1] |= bits << 16;
+                    else kw[g >> 1] = bits;
+                }
+            }
             if (!(ok = mbar_wait_warp(bar(F_S_FULL + bb), (uint32_t)(n >> 1) & 1u, w))) break;
             tc_fence_after();
             const uint32_t scol = lane_addr + C::TM_S + bb * BN;
-            const int kb = (n_begin + n) * BN;
             // element e of the block (key kb + e) is visible iff lo <= e <= hi
             const int lo = kmin - kb, hi = kmax - kb;
             // ALiBi: key kb + e lies (kb + e) - (qi + diag) = fbase + e from the diagonal
             const float fbase = (float)(kb - qi - diag);
             // scaled score of element e with its bias (bl: bias * log2e), log2 units
             auto score2 = [&](uint32_t raw, int e, float bl) __attribute__((always_inline)) -> float {
-                float x = fmaf(-slope2, fabsf(fbase + (float)e), kBias ? bl : 0.f);
+                float x = kBias ? bl : 0.f;
+                if (kAlibi) x = fmaf(-slope2, fabsf(fbase + (float)e), x);
                 return fmaf(__uint_as_float(raw), p.scale_log2, x);
             };
             // Blocks inside every row's band (all but the edge blocks) take the
@@ -306,17 +337,6 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                     tmem_ld32(scol + 32 * c, sr);
                     float bl[32];
                     if (kBias) load_bias(bl, kb + 32 * c);
-                    // dropout: random bytes of keys kb + 32c .. +31 of this row,
-                    // 16 keys per Philox output
-                    uint4 rnd[2];
-                    if (kDrop) {
-#pragma unroll
-                        for (int g = 0; g < 2; ++g)
-                            rnd[g] = philox4x32_10(
-                                make_uint4((uint32_t)((kb + 32 * c) >> 4) + g, (uint32_t)qi,
-                                           (uint32_t)(b * p.Hq + h), p.drop_offset),
-                                p.drop_key0, p.drop_key1);
-                    }
                     tmem_wait_ld();
                     uint32_t pk[16];
 #pragma unroll
@@ -335,17 +355,9 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                             p1 = (e + 1 >= lo && e + 1 <= hi) ? p1 : 0.f;
                         }
                         sum += p0 + p1;   // the row sum is taken before dropout
-                        if (kDrop) {
-                            // keys 2i, 2i + 1 of the chunk: bytes (2i) % 4, +1 of
-                            // word (2i / 4) % 4 of output 2i / 16
-                            const uint4 &R = rnd[i >> 3];
-                            const int wi = (i >> 1) & 3;
-                            const uint32_t word = wi == 0 ? R.x : wi == 1 ? R.y : wi == 2 ? R.z : R.w;
-                            const int sh = 8 * ((2 * i) & 3);
-                            const bool k0 = (int)((word >> sh) & 0xFFu) >= p.drop_t;
-                            const bool k1 = (int)((word >> (sh + 8)) & 0xFFu) >= p.drop_t;
-                            p0 = k0 ? p0 * p.drop_scale : 0.f;
-                            p1 = k1 ? p1 * p.drop_scale : 0.f;
+                        if (kDrop) {   // keys 2i, 2i + 1 of the chunk
+                            p0 = ((kw[c] >> (2 * i)) & 1u) ? p0 * p.drop_scale : 0.f;
+                            p1 = ((kw[c] >> (2 * i + 1)) & 1u) ? p1 * p.drop_scale : 0.f;
                         }
                         pk[i] = Cvt<T>::pack(p0, p1);
                     }
@@ -430,15 +442,23 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
 }
 
+template <int kD, typename T, int kI = 0>
+auto fwd_kernel_for(int need) {
+    // the first instance built that has every flag needed
+    constexpr int f = kFwdFlagSets[kI];
+    if constexpr (kI + 1 < (int)(sizeof(kFwdFlagSets) / sizeof(int))) {
+        if ((need & f) != need) return fwd_kernel_for<kD, T, kI + 1>(need);
+    }
+    return fwd_tc_kernel<kD, T, f>;
+}
+
 template <int kD, typename T>
 cudaError_t launch_fwd_tc_t(const BwdParams &p, const CUtensorMap &mq, const CUtensorMap &mk,
                             const CUtensorMap &mv, void *o, float *lse, int max_lq,
                             cudaStream_t stream) {
     using C = FwdCfg<kD, T>;
-    auto kern = p.drop_t > 0 ? fwd_tc_kernel<kD, T, 3>
-                : p.bias       ? fwd_tc_kernel<kD, T, 2>
-                : p.alibi      ? fwd_tc_kernel<kD, T, 1>
-                               : fwd_tc_kernel<kD, T, 0>;
+    const int need = (p.alibi ? kFwdAlibi : 0) | (p.bias ? kFwdBias : 0) | (p.drop_t > 0 ? kFwdDrop : 0);
+    auto kern = fwd_kernel_for<kD, T>(need);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
