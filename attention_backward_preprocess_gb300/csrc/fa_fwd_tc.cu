@@ -304,40 +304,66 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
             // pass without per-element tests.
             const bool edge = __any_sync(0xffffffffu, lo > 0 || hi < BN - 1);
             float alpha = 1.f, sum = 0.f, m_use = m_run;
+            float sumv[4] = {0.f, 0.f, 0.f, 0.f};   // row sum in four independent chains
             auto block_pass = [&](auto mask_tag) __attribute__((always_inline)) {
                 constexpr bool kMask = decltype(mask_tag)::value;
+                // the row's 128 scores: without the bias, held in registers --
+                // four loads in flight and one wait, one round trip to tensor
+                // memory per block instead of eight (the softmax is latency
+                // bound: 0.99 -> see the kernel table); with the bias (more
+                // registers live) or dropout, loaded chunk by chunk in each pass
+                constexpr bool kResident = !kBias && !kDrop;
+                uint32_t srr[kResident ? BN / 32 : 1][32];
+                if (kResident) {
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c) tmem_ld32(scol + 32 * c, srr[kResident ? c : 0]);
+                    tmem_wait_ld();
+                }
+                auto chunk = [&](int c, uint32_t (&dst)[32]) __attribute__((always_inline)) {
+                    if (kResident) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) dst[i] = srr[kResident ? c : 0][i];
+                    } else {
+                        tmem_ld32(scol + 32 * c, dst);
+                        tmem_wait_ld();
+                    }
+                };
                 // pass 1: row maximum of the block (without ALiBi the maximum of
-                // the raw scores, scaled once: the scale is positive)
-                float mx = -INFINITY;
+                // the raw scores, scaled once: the scale is positive), in eight
+                // independent chains
+                float mxv[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mxv[i] = -INFINITY;
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t sr[32];
-                    tmem_ld32(scol + 32 * c, sr);
+                    chunk(c, sr);
                     float bl[32];
                     if (kBias) load_bias(bl, kb + 32 * c);
-                    tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int e = 32 * c + i;
                         const float x = kExt ? score2(sr[i], e, bl[i]) : __uint_as_float(sr[i]);
-                        mx = (!kMask || (e >= lo && e <= hi)) ? fmaxf(mx, x) : mx;
+                        mxv[i & 7] = (!kMask || (e >= lo && e <= hi)) ? fmaxf(mxv[i & 7], x) : mxv[i & 7];
                     }
                 }
+                float mx = fmaxf(fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3])),
+                                 fmaxf(fmaxf(mxv[4], mxv[5]), fmaxf(mxv[6], mxv[7])));
                 if (!kExt) mx *= p.scale_log2;
                 const float m_new = fmaxf(m_run, mx);
                 m_use = (m_run == -INFINITY || m_new > m_run + kRescaleLog2) ? m_new : m_run;
                 alpha = (m_use == m_run) ? 1.f : ex2(m_run - m_use);
                 const float mref = (m_use == -INFINITY) ? 0.f : m_use;
                 // pass 2: P = exp2(s2 - m) into the first BN/2 columns as pairs;
-                // column j/2 of the buffer holds keys j, j+1 (every S column is
-                // read before a P pair lands on it)
+                // column j/2 of the buffer holds keys j, j+1 (with the scores
+                // read chunk by chunk, each S column is read before a P pair
+                // lands on it)
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t sr[32];
-                    tmem_ld32(scol + 32 * c, sr);
+                    chunk(c, sr);
                     float bl[32];
                     if (kBias) load_bias(bl, kb + 32 * c);
-                    tmem_wait_ld();
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -354,7 +380,7 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                             p0 = (e >= lo && e <= hi) ? p0 : 0.f;
                             p1 = (e + 1 >= lo && e + 1 <= hi) ? p1 : 0.f;
                         }
-                        sum += p0 + p1;   // the row sum is taken before dropout
+                        sumv[i & 3] += p0 + p1;   // the row sum is taken before dropout
                         if (kDrop) {   // keys 2i, 2i + 1 of the chunk
                             p0 = ((kw[c] >> (2 * i)) & 1u) ? p0 * p.drop_scale : 0.f;
                             p1 = ((kw[c] >> (2 * i + 1)) & 1u) ? p1 * p.drop_scale : 0.f;
@@ -366,6 +392,7 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
             };
             if (edge) block_pass(std::true_type{});
             else block_pass(std::false_type{});
+            sum = (sumv[0] + sumv[1]) + (sumv[2] + sumv[3]);
             l_run = l_run * alpha + sum;
             m_run = m_use;
             // O holds blocks < n: rescale it when a row's maximum moved
