@@ -66,89 +66,122 @@ __global__ void __launch_bounds__(1024) schedule_kernel(BwdParams p) {
 
 // ---------------------------------------------------------------- preprocess
 // grid (row chunks, sequences); D/8 threads per (position, head) row, each
-// reading 16 bytes of O and of dO.  Padding rows up to the next multiple of
-// 128 get Dv = 0 and LSE2 = +inf (so P = 0 there).  Every workspace row of
-// the sequence has its dQ accumulator zeroed, and in deterministic mode its
-// semaphores as well.
-template <int D, typename T>
+// reading 16 bytes of O and of dO.  With varlen each thread takes RPT = 4 rows
+// whose loads are in flight together (the sequence offsets are read first; one
+// row per thread ran at a third of the HBM bandwidth there); dense problems
+// keep one row per thread (4 was slower there).
+// Padding rows up to the next multiple of 128 get Dv = 0 and LSE2 = +inf (so
+// P = 0 there).  Every workspace row of the sequence has its dQ accumulator
+// zeroed, and in deterministic mode its semaphores as well.
+template <int D, typename T, int RPT>
 __global__ void __launch_bounds__(256) preprocess_kernel(BwdParams p) {
     constexpr int TPR = D / 8;   // threads per row
     const int b = blockIdx.y;
-    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const long long rid = gid / TPR;
-    const int part = (int)(gid % TPR);
-    const int lq = seq_len_q(p, b);
-    const int lq_round = (lq + kRowTile - 1) / kRowTile * kRowTile;
-    const int s = (int)(rid / p.Hq), h = (int)(rid % p.Hq);
-    // no early return: the row sum below is a full-warp shuffle
-    const bool active = s < lq_round;
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
         *p.err = 0;            // per-call error word
         p.unit_counter[0] = 0;   // the main kernel's dynamic work-unit counter ...
         p.unit_counter[1] = 0;   // ... and its count of CTAs that ran out of units
     }
-    const long long wr = active ? ws_row(p, b, h, s) : 0;
-    float acc = 0.f;
-    // O / dO rows hold Dh <= D columns (a multiple of 8): parts past Dh add 0
-    if (active && s < lq && part * 8 < p.Dh) {
-        const long long trow = p.varlen ? (long long)p.cu_q[b] + s : (long long)b * p.Sq + s;
-        const long long off = (trow * p.Hq + h) * p.Dh + part * 8;
-        const uint4 ov = *reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.o) + off);
-        const uint4 dv = *reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.dout) + off);
-        const uint32_t oa[4] = {ov.x, ov.y, ov.z, ov.w}, da[4] = {dv.x, dv.y, dv.z, dv.w};
+    const int lq = seq_len_q(p, b);
+    const int lq_round = (lq + kRowTile - 1) / kRowTile * kRowTile;
+    const long long nrows = (long long)lq_round * p.Hq;   // (position, head) rows, padded
+    // block-uniform exit: no row of this block belongs to the sequence
+    if ((long long)blockIdx.x * (blockDim.x / TPR) * RPT >= nrows) return;
+    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long r0 = gid / TPR * RPT;
+    const int part = (int)(gid % TPR);
+    const long long qbase = p.varlen ? (long long)p.cu_q[b] : (long long)b * p.Sq;
+    const long long ltot = p.varlen ? (long long)p.cu_q[p.B] : 0;   // varlen LSE row length
+    float acc[RPT];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const float2 of = Cvt<T>::unpack(oa[t]), df = Cvt<T>::unpack(da[t]);
-            acc = fmaf(of.x, df.x, acc);
-            acc = fmaf(of.y, df.y, acc);
+    for (int k = 0; k < RPT; ++k) {
+        acc[k] = 0.f;
+        const long long row = r0 + k;
+        const int s = (int)(row / p.Hq), h = (int)(row % p.Hq);
+        // O / dO rows hold Dh <= D columns (a multiple of 8): parts past Dh add 0
+        if (row < nrows && s < lq && part * 8 < p.Dh) {
+            const long long off = ((qbase + s) * p.Hq + h) * p.Dh + part * 8;
+            const uint4 ov = *reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.o) + off);
+            const uint4 dv = *reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.dout) + off);
+            const uint32_t oa[4] = {ov.x, ov.y, ov.z, ov.w}, da[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const float2 of = Cvt<T>::unpack(oa[t]), df = Cvt<T>::unpack(da[t]);
+                acc[k] = fmaf(of.x, df.x, acc[k]);
+                acc[k] = fmaf(of.y, df.y, acc[k]);
+            }
         }
     }
+    // the row sums: full-warp shuffles (every lane of a live warp takes part)
 #pragma unroll
-    for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, TPR);
-    if (!active) return;
-    if (part == 0) {
-        float l2 = __int_as_float(0x7f800000);   // +inf on padding rows
-        if (s < lq) {
-            const long long li = p.varlen ? (long long)h * p.cu_q[p.B] + p.cu_q[b] + s
-                                          : ((long long)b * p.Hq + h) * p.Sq + s;
-            float l = p.lse[li];
-            if (l == -__int_as_float(0x7f800000)) l = 0.f;   // get_validated_lse
-            l2 = l * kLog2e;
+    for (int k = 0; k < RPT; ++k)
+#pragma unroll
+        for (int o = TPR / 2; o > 0; o >>= 1) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], o, TPR);
+#pragma unroll
+    for (int k = 0; k < RPT; ++k) {
+        const long long row = r0 + k;
+        if (row >= nrows) break;
+        const int s = (int)(row / p.Hq), h = (int)(row % p.Hq);
+        const long long wr = ws_row(p, b, h, s);
+        if (part == 0) {
+            float l2 = __int_as_float(0x7f800000);   // +inf on padding rows
+            if (s < lq) {
+                const long long li = p.varlen ? (long long)h * ltot + qbase + s
+                                              : ((long long)b * p.Hq + h) * p.Sq + s;
+                float l = p.lse[li];
+                if (l == -__int_as_float(0x7f800000)) l = 0.f;   // get_validated_lse
+                l2 = l * kLog2e;
+            }
+            p.dvec[wr] = (s < lq) ? acc[k] : 0.f;
+            p.lse2[wr] = l2;
+            if (p.deterministic && (s % 64) == 0) p.sem[wr / 64] = 0;
         }
-        p.dvec[wr] = (s < lq) ? acc : 0.f;
-        p.lse2[wr] = l2;
-        if (p.deterministic && (s % 64) == 0) p.sem[wr / 64] = 0;
+        float4 *z = reinterpret_cast<float4 *>(p.dqacc + wr * D) + part * 2;
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    float4 *z = reinterpret_cast<float4 *>(p.dqacc + wr * D) + part * 2;
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // --------------------------------------------------------------- postprocess
 // dQ[row, h, :] = cast(dQaccum[ws_row(b, h, s), :] * scale) for s < Lq
 // (FlashAttentionBackwardPostprocess: acc.load() * scale, then a predicated
-// store clipped to the sequence length).
-template <int D, typename T>
+// store clipped to the sequence length); RPT rows per thread, as above.
+template <int D, typename T, int RPT>
 __global__ void __launch_bounds__(256) postprocess_kernel(BwdParams p) {
     constexpr int TPR = D / 8;
     const int b = blockIdx.y;
-    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const long long rid = gid / TPR;
-    const int part = (int)(gid % TPR);
     const int lq = seq_len_q(p, b);
-    const int s = (int)(rid / p.Hq), h = (int)(rid % p.Hq);
-    if (s >= lq || part * 8 >= p.Dh) return;   // dQ rows hold Dh <= D columns
-    const long long wr = ws_row(p, b, h, s);
-    const float4 *src = reinterpret_cast<const float4 *>(p.dqacc + wr * D) + part * 2;
-    const float4 a = src[0], c = src[1];
+    const long long nrows = (long long)lq * p.Hq;
+    if ((long long)blockIdx.x * (blockDim.x / TPR) * RPT >= nrows) return;
+    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long r0 = gid / TPR * RPT;
+    const int part = (int)(gid % TPR);
+    if (part * 8 >= p.Dh) return;   // dQ rows hold Dh <= D columns
+    const long long qbase = p.varlen ? (long long)p.cu_q[b] : (long long)b * p.Sq;
     const float sc = p.scale;
-    uint4 o;
-    o.x = Cvt<T>::pack(a.x * sc, a.y * sc);
-    o.y = Cvt<T>::pack(a.z * sc, a.w * sc);
-    o.z = Cvt<T>::pack(c.x * sc, c.y * sc);
-    o.w = Cvt<T>::pack(c.z * sc, c.w * sc);
-    const long long trow = p.varlen ? (long long)p.cu_q[b] + s : (long long)b * p.Sq + s;
-    *reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dq) + (trow * p.Hq + h) * p.Dh + part * 8) = o;
+    float4 a[RPT], c[RPT];
+#pragma unroll
+    for (int k = 0; k < RPT; ++k) {
+        const long long row = r0 + k;
+        if (row < nrows) {
+            const int s = (int)(row / p.Hq), h = (int)(row % p.Hq);
+            const float4 *src = reinterpret_cast<const float4 *>(p.dqacc + ws_row(p, b, h, s) * D) + part * 2;
+            a[k] = src[0];
+            c[k] = src[1];
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < RPT; ++k) {
+        const long long row = r0 + k;
+        if (row >= nrows) break;
+        const int s = (int)(row / p.Hq), h = (int)(row % p.Hq);
+        uint4 o;
+        o.x = Cvt<T>::pack(a[k].x * sc, a[k].y * sc);
+        o.y = Cvt<T>::pack(a[k].z * sc, a[k].w * sc);
+        o.z = Cvt<T>::pack(c[k].x * sc, c[k].y * sc);
+        o.w = Cvt<T>::pack(c[k].z * sc, c[k].w * sc);
+        *reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dq) + ((qbase + s) * p.Hq + h) * p.Dh + part * 8) = o;
+    }
 }
 
 }  // namespace
@@ -158,31 +191,44 @@ cudaError_t launch_schedule(const BwdParams &p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-static dim3 row_grid(const BwdParams &p, int lanes_per_row, int rows_per_seq) {
-    const long long threads = (long long)rows_per_seq * p.Hq * lanes_per_row;
+static dim3 row_grid(const BwdParams &p, int lanes_per_row, int rows_per_seq, int rpt) {
+    const long long threads = ((long long)rows_per_seq * p.Hq + rpt - 1) / rpt * lanes_per_row;
     return dim3((unsigned)((threads + 255) / 256), (unsigned)p.B, 1);
 }
 
+template <int D, typename T>
+static void launch_pre_t(const BwdParams &p, cudaStream_t stream) {
+    if (p.varlen)
+        preprocess_kernel<D, T, 4><<<row_grid(p, D / 8, p.sq_round, 4), 256, 0, stream>>>(p);
+    else
+        preprocess_kernel<D, T, 1><<<row_grid(p, D / 8, p.sq_round, 1), 256, 0, stream>>>(p);
+}
+template <int D, typename T>
+static void launch_post_t(const BwdParams &p, cudaStream_t stream) {
+    if (p.varlen)
+        postprocess_kernel<D, T, 4><<<row_grid(p, D / 8, p.Sq, 4), 256, 0, stream>>>(p);
+    else
+        postprocess_kernel<D, T, 1><<<row_grid(p, D / 8, p.Sq, 1), 256, 0, stream>>>(p);
+}
+
 cudaError_t launch_preprocess(const BwdParams &p, int bf16, cudaStream_t stream) {
-    const dim3 grid = row_grid(p, p.D / 8, p.sq_round);
     if (p.D == 128) {
-        if (bf16) preprocess_kernel<128, __nv_bfloat16><<<grid, 256, 0, stream>>>(p);
-        else preprocess_kernel<128, __half><<<grid, 256, 0, stream>>>(p);
+        if (bf16) launch_pre_t<128, __nv_bfloat16>(p, stream);
+        else launch_pre_t<128, __half>(p, stream);
     } else {
-        if (bf16) preprocess_kernel<64, __nv_bfloat16><<<grid, 256, 0, stream>>>(p);
-        else preprocess_kernel<64, __half><<<grid, 256, 0, stream>>>(p);
+        if (bf16) launch_pre_t<64, __nv_bfloat16>(p, stream);
+        else launch_pre_t<64, __half>(p, stream);
     }
     return cudaGetLastError();
 }
 
 cudaError_t launch_postprocess(const BwdParams &p, int bf16, cudaStream_t stream) {
-    const dim3 grid = row_grid(p, p.D / 8, p.Sq);
     if (p.D == 128) {
-        if (bf16) postprocess_kernel<128, __nv_bfloat16><<<grid, 256, 0, stream>>>(p);
-        else postprocess_kernel<128, __half><<<grid, 256, 0, stream>>>(p);
+        if (bf16) launch_post_t<128, __nv_bfloat16>(p, stream);
+        else launch_post_t<128, __half>(p, stream);
     } else {
-        if (bf16) postprocess_kernel<64, __nv_bfloat16><<<grid, 256, 0, stream>>>(p);
-        else postprocess_kernel<64, __half><<<grid, 256, 0, stream>>>(p);
+        if (bf16) launch_post_t<64, __nv_bfloat16>(p, stream);
+        else launch_post_t<64, __half>(p, stream);
     }
     return cudaGetLastError();
 }
