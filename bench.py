@@ -51,6 +51,14 @@ def peaks():
     return dict(bf16=1900.0, bf16_sustained=1700.0, hbm=6800.0, source="fallback")
 
 
+def clock_log_path(name):
+    """Where the clock sampler writes its raw CSV: $FA_BENCH_LOG_DIR if set,
+    else the system temporary directory (the JSON line carries the summary)."""
+    import tempfile
+    d = os.environ.get("FA_BENCH_LOG_DIR") or tempfile.gettempdir()
+    return os.path.join(d, "%s.%d.csv" % (name, os.getpid()))
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -255,9 +263,7 @@ def main():
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
-    clocks = ClockSampler(dev.index, os.path.join(ROOT, "gpurun_out", "bench_clocks.csv")
-                          if os.path.isdir(os.path.join(ROOT, "gpurun_out"))
-                          else "/tmp/bench_clocks.%d.csv" % os.getpid())
+    clocks = ClockSampler(dev.index, clock_log_path("bench_clocks"))
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
@@ -495,9 +501,7 @@ def run_ext(args, w):
         torch.cuda.synchronize()
         return statistics.mean(a.elapsed_time(b) for a, b in ev)
 
-    clocks = ClockSampler(dev.index, os.path.join(ROOT, "gpurun_out", "bench_ext_clocks.csv")
-                          if os.path.isdir(os.path.join(ROOT, "gpurun_out"))
-                          else "/tmp/bench_ext_clocks.%d.csv" % os.getpid())
+    clocks = ClockSampler(dev.index, clock_log_path("bench_ext_clocks"))
     f_ms = timed(fwd)
     b_ms = timed(bwd)
     clk = clocks.stop()
