@@ -17,9 +17,13 @@
 //
 // Warps: 0 TMA producer (Q once, K/V blocks through a stage ring), 1 MMA
 // issuer, 4-7 softmax (thread = query row of its TMEM lane quarter), 2-3 idle.
+//
+// This kernel serves the instances with one softmax warp per query row (D =
+// 128 without the bias or dropout); the others run in fa_fwd_split.cu.
 #include <type_traits>
 
 #include "fa_device.cuh"
+#include "fa_fwd_common.h"
 #include "fa_params.h"
 
 namespace fa {
@@ -69,15 +73,6 @@ enum {
 // Lazy rescaling threshold (log2 units): P is taken against a running maximum
 // that may lag the true one by up to this much.
 constexpr float kRescaleLog2 = 8.f;
-
-// Extension flags of an instance: ALiBi, the elementwise bias, dropout (the
-// band needs none: only edge blocks test it).  Each extension gets compiled in
-// only where asked for: its code slows the softmax even when skipped at run
-// time.
-enum : int { kFwdAlibi = 2, kFwdBias = 4, kFwdDrop = 8 };
-// the instances built, each a superset of the flags before it in its chain
-constexpr int kFwdFlagSets[] = {0, kFwdAlibi, kFwdAlibi | kFwdBias, kFwdDrop,
-                                kFwdAlibi | kFwdBias | kFwdDrop};
 
 template <int kD, typename T, int kFlags>
 __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
@@ -469,23 +464,29 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
 }
 
+using FwdKernel = void (*)(BwdParams, CUtensorMap, CUtensorMap, CUtensorMap, void *, float *, int);
+
 template <int kD, typename T, int kI = 0>
-auto fwd_kernel_for(int need) {
-    // the first instance built that has every flag needed
+FwdKernel fwd_kernel_for(int need) {
+    // the first instance built that has every flag needed (null: it is one of
+    // fa_fwd_split.cu's)
     constexpr int f = kFwdFlagSets[kI];
-    if constexpr (kI + 1 < (int)(sizeof(kFwdFlagSets) / sizeof(int))) {
+    if constexpr (kI + 1 < kNumFwdFlagSets) {
         if ((need & f) != need) return fwd_kernel_for<kD, T, kI + 1>(need);
     }
-    return fwd_tc_kernel<kD, T, f>;
+    if constexpr (fwd_split(kD, f))
+        return nullptr;
+    else
+        return fwd_tc_kernel<kD, T, f>;
 }
 
 template <int kD, typename T>
 cudaError_t launch_fwd_tc_t(const BwdParams &p, const CUtensorMap &mq, const CUtensorMap &mk,
-                            const CUtensorMap &mv, void *o, float *lse, int max_lq,
+                            const CUtensorMap &mv, void *o, float *lse, int max_lq, int need,
                             cudaStream_t stream) {
     using C = FwdCfg<kD, T>;
-    const int need = (p.alibi ? kFwdAlibi : 0) | (p.bias ? kFwdBias : 0) | (p.drop_t > 0 ? kFwdDrop : 0);
-    auto kern = fwd_kernel_for<kD, T>(need);
+    FwdKernel kern = fwd_kernel_for<kD, T>(need);
+    if (kern == nullptr) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -513,11 +514,12 @@ int fwd_block_m() { return FwdCfg<128, __nv_bfloat16>::BM; }
 cudaError_t launch_fwd_tc(const BwdParams &p, const CUtensorMap &q, const CUtensorMap &k,
                           const CUtensorMap &v, void *o, float *lse, int max_lq, int bf16,
                           cudaStream_t stream) {
-    if (p.D == 128)
-        return bf16 ? launch_fwd_tc_t<128, __nv_bfloat16>(p, q, k, v, o, lse, max_lq, stream)
-                    : launch_fwd_tc_t<128, __half>(p, q, k, v, o, lse, max_lq, stream);
-    return bf16 ? launch_fwd_tc_t<64, __nv_bfloat16>(p, q, k, v, o, lse, max_lq, stream)
-                : launch_fwd_tc_t<64, __half>(p, q, k, v, o, lse, max_lq, stream);
+    const int need = (p.alibi ? kFwdAlibi : 0) | (p.bias ? kFwdBias : 0) | (p.drop_t > 0 ? kFwdDrop : 0);
+    const int f = fwd_instance_flags(need);
+    if (fwd_split(p.D, f)) return launch_fwd_split(p, q, k, v, o, lse, max_lq, bf16, f, stream);
+    if (p.D != 128) return cudaErrorInvalidValue;
+    return bf16 ? launch_fwd_tc_t<128, __nv_bfloat16>(p, q, k, v, o, lse, max_lq, need, stream)
+                : launch_fwd_tc_t<128, __half>(p, q, k, v, o, lse, max_lq, need, stream);
 }
 
 }  // namespace fa
