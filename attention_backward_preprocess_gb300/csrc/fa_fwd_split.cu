@@ -296,27 +296,37 @@ __global__ void __launch_bounds__(SplitCfg<kD, T>::kThreads, 1)
         if (kBias && p.bias && qi < lq)
             brow = reinterpret_cast<const T *>(p.bias) + (long long)b * p.bias_bs +
                    (long long)h * p.bias_hs + (long long)qi * p.bias_rs;
-        // bias of keys k0 .. k0 + 31 in log2 units (0 past lk); 16-byte loads
-        // when the 32 keys are all in range (k0 is a multiple of 32, the row
-        // start 16-byte aligned)
-        auto load_bias = [&](float (&bl)[32], int k0) __attribute__((always_inline)) {
-            if (brow && k0 + 32 <= lk) {
+        // the bias of this half's HK keys k0 .. k0 + HK - 1 of a block as
+        // packed pairs (0 past lk), fetched before the block's S is waited for
+        // so the loads' latency hides behind it; 16-byte loads when all HK are
+        // in range (k0 is a multiple of 64, the row start 16-byte aligned)
+        auto fetch_bias = [&](uint32_t (&bw)[HK / 2], int k0) __attribute__((always_inline)) {
+            if (brow && k0 + HK <= lk) {
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
+                for (int t = 0; t < HK / 8; ++t) {
                     const uint4 v = __ldg(reinterpret_cast<const uint4 *>(brow + k0) + t);
-                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float2 f = Cvt<T>::unpack(w4[u]);
-                        bl[8 * t + 2 * u] = f.x * 1.4426950408889634f;
-                        bl[8 * t + 2 * u + 1] = f.y * 1.4426950408889634f;
-                    }
+                    bw[4 * t] = v.x;
+                    bw[4 * t + 1] = v.y;
+                    bw[4 * t + 2] = v.z;
+                    bw[4 * t + 3] = v.w;
                 }
             } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    bl[i] = (brow && k0 + i < lk) ? static_cast<float>(brow[k0 + i]) * 1.4426950408889634f
-                                                  : 0.f;
+                for (int i = 0; i < HK / 2; ++i) {
+                    const float f0 = (brow && k0 + 2 * i < lk) ? static_cast<float>(brow[k0 + 2 * i]) : 0.f;
+                    const float f1 =
+                        (brow && k0 + 2 * i + 1 < lk) ? static_cast<float>(brow[k0 + 2 * i + 1]) : 0.f;
+                    bw[i] = Cvt<T>::pack(f0, f1);
+                }
+            }
+        };
+        // bias of keys 32c .. 32c + 31 of the half in log2 units
+        auto load_bias = [&](float (&bl)[32], const uint32_t (&bw)[HK / 2], int c) __attribute__((always_inline)) {
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const float2 f = Cvt<T>::unpack(bw[16 * c + u]);
+                bl[2 * u] = f.x * 1.4426950408889634f;
+                bl[2 * u + 1] = f.y * 1.4426950408889634f;
             }
         };
         // Exchange of one value per row with the other warp of the quarter, at
@@ -376,6 +386,8 @@ __global__ void __launch_bounds__(SplitCfg<kD, T>::kThreads, 1)
                     else kw[g >> 1] = bits;
                 }
             }
+            uint32_t bw[kBias ? HK / 2 : 1];
+            if constexpr (kBias) fetch_bias(bw, kh);
             if (!(ok = mbar_wait_warp(bar(C::s_full(bb)), (uint32_t)(n / NB) & 1u, w))) break;
             tc_fence_after();
             const uint32_t scol = lane_addr + C::TM_S + bb * BN + HK * hf;
@@ -423,7 +435,7 @@ __global__ void __launch_bounds__(SplitCfg<kD, T>::kThreads, 1)
                     uint32_t sr[32];
                     chunk(c, sr);
                     float bl[32];
-                    if (kBias) load_bias(bl, kh + 32 * c);
+                    if constexpr (kBias) load_bias(bl, bw, c);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int e = 32 * c + i;
@@ -454,7 +466,7 @@ __global__ void __launch_bounds__(SplitCfg<kD, T>::kThreads, 1)
                     uint32_t sr[32];
                     chunk(c, sr);
                     float bl[32];
-                    if (kBias) load_bias(bl, kh + 32 * c);
+                    if constexpr (kBias) load_bias(bl, bw, c);
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {

@@ -226,6 +226,10 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
         const float slope2 = (kAlibi && p.alibi)
                                  ? __ldg(p.alibi + (long long)b * p.alibi_bstride + h) * 1.4426950408889634f
                                  : 0.f;
+        // ALiBi in raw-score units, and whether it is linear over every
+        // visible key (no key right of the diagonal)
+        const float slope_u = slope2 / p.scale_log2;
+        const bool lin = p.win_hi <= 0;
         // elementwise bias row of this query (null: none, or a padding row)
         const T *brow = nullptr;
         if (kBias && p.bias && qi < lq)
@@ -300,8 +304,15 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
             const bool edge = __any_sync(0xffffffffu, lo > 0 || hi < BN - 1);
             float alpha = 1.f, sum = 0.f, m_use = m_run;
             float sumv[4] = {0.f, 0.f, 0.f, 0.f};   // row sum in four independent chains
-            auto block_pass = [&](auto mask_tag) __attribute__((always_inline)) {
+            // kLin: ALiBi with no visible key right of the diagonal (win_hi <= 0,
+            // e.g. causal), where -slope |fbase + e| = slope (fbase + e) is linear
+            // in e: pass 1 takes the maximum of raw + (slope / scale) e (one FMA
+            // per score, scaled once), pass 2 adds slope e to a per-block
+            // constant (two FMAs per score instead of an add, an abs-FMA and an
+            // FMA, and one subtraction fewer)
+            auto block_pass = [&](auto mask_tag, auto lin_tag) __attribute__((always_inline)) {
                 constexpr bool kMask = decltype(mask_tag)::value;
+                constexpr bool kLin = decltype(lin_tag)::value;
                 // the row's 128 scores: without the bias, held in registers --
                 // four loads in flight and one wait, one round trip to tensor
                 // memory per block instead of eight (the softmax is latency
@@ -338,17 +349,21 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int e = 32 * c + i;
-                        const float x = kExt ? score2(sr[i], e, bl[i]) : __uint_as_float(sr[i]);
+                        const float x = kLin   ? fmaf(slope_u, (float)e, __uint_as_float(sr[i]))
+                                        : kExt ? score2(sr[i], e, bl[i])
+                                               : __uint_as_float(sr[i]);
                         mxv[i & 7] = (!kMask || (e >= lo && e <= hi)) ? fmaxf(mxv[i & 7], x) : mxv[i & 7];
                     }
                 }
                 float mx = fmaxf(fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3])),
                                  fmaxf(fmaxf(mxv[4], mxv[5]), fmaxf(mxv[6], mxv[7])));
-                if (!kExt) mx *= p.scale_log2;
+                if (!kExt || kLin) mx *= p.scale_log2;
+                if (kLin) mx += slope2 * fbase;
                 const float m_new = fmaxf(m_run, mx);
                 m_use = (m_run == -INFINITY || m_new > m_run + kRescaleLog2) ? m_new : m_run;
                 alpha = (m_use == m_run) ? 1.f : ex2(m_run - m_use);
                 const float mref = (m_use == -INFINITY) ? 0.f : m_use;
+                const float cl = kLin ? fmaf(slope2, fbase, -mref) : 0.f;
                 // pass 2: P = exp2(s2 - m) into the first BN/2 columns as pairs;
                 // column j/2 of the buffer holds keys j, j+1 (with the scores
                 // read chunk by chunk, each S column is read before a P pair
@@ -364,7 +379,11 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                     for (int i = 0; i < 16; ++i) {
                         const int e = 32 * c + 2 * i;
                         float p0, p1;
-                        if (kExt) {
+                        if (kLin) {
+                            p0 = ex2(fmaf(__uint_as_float(sr[2 * i]), p.scale_log2, fmaf(slope2, (float)e, cl)));
+                            p1 = ex2(fmaf(__uint_as_float(sr[2 * i + 1]), p.scale_log2,
+                                          fmaf(slope2, (float)(e + 1), cl)));
+                        } else if (kExt) {
                             p0 = ex2(score2(sr[2 * i], e, bl[2 * i]) - mref);
                             p1 = ex2(score2(sr[2 * i + 1], e + 1, bl[2 * i + 1]) - mref);
                         } else {
@@ -385,8 +404,16 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                     tmem_st16(scol + 16 * c, pk);
                 }
             };
-            if (edge) block_pass(std::true_type{});
-            else block_pass(std::false_type{});
+            auto run = [&](auto mask_tag) __attribute__((always_inline)) {
+                if constexpr (kAlibi && !kBias) {
+                    if (lin) block_pass(mask_tag, std::true_type{});
+                    else block_pass(mask_tag, std::false_type{});
+                } else {
+                    block_pass(mask_tag, std::false_type{});
+                }
+            };
+            if (edge) run(std::true_type{});
+            else run(std::false_type{});
             sum = (sumv[0] + sumv[1]) + (sumv[2] + sumv[3]);
             l_run = l_run * alpha + sum;
             m_run = m_use;
