@@ -32,6 +32,11 @@ CASES = [
     (W("alibi_d64_fp16", 2, 200, 260, 2, 2, 64, "fp16"), dict(alibi="bh")),
     (W("alibi_win_causal_d128", 1, 300, 300, 2, 1, 128, causal=True),
      dict(alibi="h", window=(90, -1))),
+    # ALiBi at D = 128 with keys right of the diagonal (the |.| form), and
+    # causal with Sq < Sk (the linear form with diag > 0)
+    (W("alibi_noncausal_d128", 1, 260, 300, 2, 2, 128), dict(alibi="bh")),
+    (W("alibi_win_right_d128", 1, 300, 300, 2, 1, 128), dict(alibi="h", window=(50, 40))),
+    (W("alibi_causal_sq_lt_sk_d128", 1, 200, 450, 2, 2, 128, causal=True), dict(alibi="h")),
     (W("seqused_causal_d128", 2, 300, 300, 2, 1, 128, causal=True),
      dict(seqused_q=[300, 170], seqused_k=[257, 300])),
     (W("seqused_win_d64", 2, 256, 256, 2, 2, 64), dict(seqused_q=[100, 256], seqused_k=[256, 31],
