@@ -261,11 +261,19 @@ struct MainMaps {
 // kernel (no mask, or a band with an upper edge only, e.g. causal).  Each
 // extension gets compiled in only where asked for: its code slows the softmax
 // warps even when skipped at run time (measured: the bias code made a
-// windowed run 1.8x slower, the ALiBi arithmetic 11 %).
-enum : int { kFBand = 1, kFAlibi = 2, kFBias = 4, kFDrop = 8 };
+// windowed run 1.8x slower, the ALiBi arithmetic 11 %).  kFAbs: ALiBi where a
+// visible key may lie right of the diagonal (a band with an upper edge above
+// it), which needs -slope |i + diag - j|; without it (e.g. causal) the bias is
+// linear in the key, slope (j - i - diag), and costs one add per pair.
+enum : int { kFBand = 1, kFAlibi = 2, kFBias = 4, kFDrop = 8, kFAbs = 16 };
 // the instances built, each a superset of the flags before it in its chain
-constexpr int kMainFlagSets[] = {0, kFBand, kFBand | kFAlibi, kFBand | kFAlibi | kFBias,
-                                 kFBand | kFDrop, kFBand | kFAlibi | kFBias | kFDrop};
+constexpr int kMainFlagSets[] = {0,
+                                 kFBand,
+                                 kFBand | kFAlibi,
+                                 kFBand | kFAlibi | kFAbs,
+                                 kFBand | kFAlibi | kFAbs | kFBias,
+                                 kFBand | kFDrop,
+                                 kFBand | kFAlibi | kFAbs | kFBias | kFDrop};
 
 template <int kD, typename T, int kFlags>
 __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
@@ -274,6 +282,8 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
     constexpr int D = C::D, BM = C::BM, BN = C::BN, S = C::kStages, HALF = C::HALF, NCH = C::NCH;
     constexpr bool kExt = (kFlags & kFBand) != 0, kAlibi = (kFlags & kFAlibi) != 0,
                    kBias = (kFlags & kFBias) != 0, kDrop = (kFlags & kFDrop) != 0;
+    // ALiBi with no visible key right of the diagonal: -slope |d| = slope d
+    constexpr bool kAlibiLin = kAlibi && (kFlags & kFAbs) == 0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -970,6 +980,15 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     const int lim = kb - (m0 + c0 + diag) - 2 * q4;
                     const int lim_hi = lim - whi, lim_lo = lim + wlo;
                     const float flim = (float)lim;
+                    if (kAlibiLin) {
+                        // linear ALiBi: slope (lim - 8k - e) joins -LSE2 here and
+                        // slope kr is added per key offset below
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float a0 = slope2 * (flim - (float)(8 * k));
+                            nl2[k] = f2_add(nl2[k], f2_pack(a0, a0 - slope2));
+                        }
+                    }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         uint32_t pk[8];
@@ -978,12 +997,15 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
 #pragma unroll
                             for (int r = 0; r < 2; ++r) {
                                 const int kr = 16 * h + 8 * r;    // key offset from kb
+                                uint64_t addend = nl2[k];
+                                if (kAlibiLin && kr > 0)
+                                    addend = f2_add(addend, f2_pack(slope2 * (float)kr, slope2 * (float)kr));
                                 const float2 x = f2_unpack(f2_fma(
                                     f2_pack(__uint_as_float(sr[h][4 * k + 2 * r]),
                                             __uint_as_float(sr[h][4 * k + 2 * r + 1])),
-                                    sc2, nl2[k]));
+                                    sc2, addend));
                                 float x0 = x.x, x1 = x.y;
-                                if (kAlibi) {
+                                if (kAlibi && !kAlibiLin) {
                                     // -slope * |qi + diag - kj|
                                     const float fd = flim + (float)(kr - 8 * k);
                                     x0 = fmaf(-slope2, fabsf(fd), x0);
@@ -1185,7 +1207,8 @@ template <int kD, typename T>
 static cudaError_t launch_main_t(const BwdParams &p, const MainMaps &maps, int grid,
                                  cudaStream_t stream) {
     using C = MainCfg<kD, T>;
-    const int need = (p.win_lo < kNoWindow ? kFBand : 0) | (p.alibi ? kFAlibi : 0) |
+    const int need = (p.win_lo < kNoWindow ? kFBand : 0) |
+                     (p.alibi ? kFAlibi | (p.win_hi > 0 ? kFAbs : 0) : 0) |
                      ((p.bias || p.dbias) ? kFBias : 0) | (p.drop_t > 0 ? kFDrop : 0);
     auto kern = main_kernel_for<kD, T>(need);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
