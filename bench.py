@@ -188,7 +188,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=None)
-    ap.add_argument("--cpu-prefix", type=int, default=4096)
+    ap.add_argument("--cpu-prefix", type=int, default=8192)
     ap.add_argument("--ref-prefix", type=int, default=1024)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
