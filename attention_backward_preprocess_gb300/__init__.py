@@ -56,7 +56,18 @@ class FaExt(ctypes.Structure):
                 ("bias", ctypes.c_void_p), ("bias_batch_stride", ctypes.c_longlong),
                 ("bias_head_stride", ctypes.c_longlong), ("bias_row_stride", ctypes.c_longlong),
                 ("dbias", ctypes.c_void_p), ("dropout_p", ctypes.c_float),
-                ("dropout_seed", ctypes.c_ulonglong), ("dropout_offset", ctypes.c_uint)]
+                ("dropout_seed", ctypes.c_ulonglong), ("dropout_offset", ctypes.c_uint),
+                ("dropout_mask", ctypes.c_void_p)]
+
+
+def dropout_mask_shape(q, k, cu_seqlens_q=None, max_seqlen_k=None):
+    """Shape of the int32 keep-flag buffer fa_fwd / fa_bwd take with dropout:
+    [B, Hq, Sq, W] (dense) or [Hq, total_q, W] (varlen), W = ceil(Sk / 32)
+    words of 32 keys per query row, Sk the key length (max_seqlen_k)."""
+    if cu_seqlens_q is not None:
+        Sk = int(max_seqlen_k)
+        return (q.shape[1], q.shape[0], (Sk + 31) // 32)
+    return (q.shape[0], q.shape[2], q.shape[1], (k.shape[1] + 31) // 32)
 
 
 def _ext(Hq, window=None, alibi_slopes=None, seqused_q=None, seqused_k=None, bias=None,
@@ -66,14 +77,21 @@ def _ext(Hq, window=None, alibi_slopes=None, seqused_q=None, seqused_k=None, bia
     ``bias``: [B or 1, Hq or 1, Sq, >= Sk] in the input dtype, last axis
     contiguous (a size-1 batch / head axis broadcasts).  ``dbias``: a
     contiguous [B, Hq, Sq, Sk] output of the input dtype (backward only).
-    ``dropout``: (p, seed, offset), see fa_ext in include/fa.h."""
+    ``dropout``: (p, seed, offset), or (p, seed, offset, mask) with ``mask`` an
+    int32 tensor of ``dropout_mask_shape(...)`` that fa_fwd fills with the keep
+    flags and fa_bwd reads back; see fa_ext in include/fa.h."""
     if (window is None and alibi_slopes is None and seqused_q is None and seqused_k is None
             and bias is None and dbias is None and dropout is None):
         return None
-    e = FaExt(-1, -1, None, 0, None, None, None, 0, 0, 0, None, 0.0, 0, 0)
+    e = FaExt(-1, -1, None, 0, None, None, None, 0, 0, 0, None, 0.0, 0, 0, None)
     if dropout is not None:
         e.dropout_p, e.dropout_seed, e.dropout_offset = (float(dropout[0]), int(dropout[1]),
                                                          int(dropout[2]))
+        if len(dropout) > 3 and dropout[3] is not None:
+            m = dropout[3]
+            if m.dtype != torch.int32 or not m.is_contiguous():
+                raise ValueError("dropout mask: a contiguous int32 tensor of dropout_mask_shape(...)")
+            e.dropout_mask = m.data_ptr()
     if window is not None:
         e.window_left, e.window_right = int(window[0]), int(window[1])
     if alibi_slopes is not None:

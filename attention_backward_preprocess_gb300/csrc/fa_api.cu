@@ -217,6 +217,8 @@ fa_status apply_ext(fa::BwdParams &p, int causal, const fa_ext *ext) {
     p.drop_t = 0;
     p.drop_key0 = p.drop_key1 = p.drop_offset = 0;
     p.drop_scale = 1.f;
+    p.drop_mask = nullptr;
+    p.drop_mask_w = 0;
     if (ext) {
         wl = ext->window_left;
         wr = ext->window_right;
@@ -256,6 +258,11 @@ fa_status apply_ext(fa::BwdParams &p, int causal, const fa_ext *ext) {
         p.drop_key1 = (uint32_t)(ext->dropout_seed >> 32);
         p.drop_offset = ext->dropout_offset;
         p.drop_scale = 256.f / (float)(256 - p.drop_t);
+        if (ext->dropout_mask && p.drop_t > 0) {
+            if (reinterpret_cast<uintptr_t>(ext->dropout_mask) & 3u) return FA_ERR_INVALID_ARG;
+            p.drop_mask = ext->dropout_mask;
+            p.drop_mask_w = (p.Sk + 31) / 32;
+        }
     }
     p.win_lo = (wl < 0 || wl >= fa::kNoWindow) ? fa::kNoWindow : wl;
     p.win_hi = (wr < 0 || wr >= fa::kNoWindow) ? fa::kNoWindow : wr;

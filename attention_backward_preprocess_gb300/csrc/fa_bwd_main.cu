@@ -920,20 +920,32 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     for (int ch = 0; ch < NCH; ++ch) {
                         const int c0 = grp * HALF + 32 * ch;
                         uint32_t kmask = 0u;
+                        if (p.drop_mask) {
+                            // the forward's flags: word (n0 + 32 quarter) / 32 of
+                            // query m0 + c0 + lane (0 past the used lengths)
+                            const int qi = m0 + c0 + lane, kw0 = (n0 + 32 * quarter) >> 5;
+                            if (qi < u.lq && n0 + 32 * quarter < u.lk && kw0 < p.drop_mask_w) {
+                                const long long mrow =
+                                    p.varlen ? (long long)hq * p.cu_q[p.B] + u.q_row0 + qi
+                                             : ((long long)u.b * p.Hq + hq) * p.Sq + qi;
+                                kmask = __ldg(p.drop_mask + mrow * p.drop_mask_w + kw0);
+                            }
+                        } else {
 #pragma unroll
-                        for (int g = 0; g < 2; ++g) {
-                            const uint4 R = philox4x32_10(
-                                make_uint4((uint32_t)((n0 + 32 * quarter) >> 4) + g,
-                                           (uint32_t)(m0 + c0 + lane), (uint32_t)u.b * p.Hq + hq,
-                                           p.drop_offset),
-                                p.drop_key0, p.drop_key1);
-                            const uint32_t wd[4] = {R.x, R.y, R.z, R.w};
+                            for (int g = 0; g < 2; ++g) {
+                                const uint4 R = philox4x32_10(
+                                    make_uint4((uint32_t)((n0 + 32 * quarter) >> 4) + g,
+                                               (uint32_t)(m0 + c0 + lane), (uint32_t)u.b * p.Hq + hq,
+                                               p.drop_offset),
+                                    p.drop_key0, p.drop_key1);
+                                const uint32_t wd[4] = {R.x, R.y, R.z, R.w};
 #pragma unroll
-                            for (int wi = 0; wi < 4; ++wi) {
-                                // bytes >= t -> 0xFF; the low bits of the 4 bytes
-                                // gathered into bits 28-31 by one product
-                                const uint32_t ge = __vcmpgeu4(wd[wi], tt4) & 0x01010101u;
-                                kmask |= ((ge * 0x10204080u) >> 28) << (16 * g + 4 * wi);
+                                for (int wi = 0; wi < 4; ++wi) {
+                                    // bytes >= t -> 0xFF; the low bits of the 4 bytes
+                                    // gathered into bits 28-31 by one product
+                                    const uint32_t ge = __vcmpgeu4(wd[wi], tt4) & 0x01010101u;
+                                    kmask |= ((ge * 0x10204080u) >> 28) << (16 * g + 4 * wi);
+                                }
                             }
                         }
                         kb32[ch] = 0u;

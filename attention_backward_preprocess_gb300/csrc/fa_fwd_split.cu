@@ -385,6 +385,18 @@ __global__ void __launch_bounds__(SplitCfg<kD, T>::kThreads, 1)
                     if (g & 1) kw[g >> 1] |= bits << 16;
                     else kw[g >> 1] = bits;
                 }
+                if (p.drop_mask && qi < lq) {
+                    // the flags for the backward: word (kh + 32c) / 32 of this
+                    // query row, for the words that hold a key below lk
+                    const long long mrow = p.varlen ? (long long)h * p.cu_q[p.B] + q0 + qi
+                                                    : ((long long)b * p.Hq + h) * p.Sq + qi;
+                    uint32_t *mdst = p.drop_mask + mrow * p.drop_mask_w;
+#pragma unroll
+                    for (int c = 0; c < HK / 32; ++c) {
+                        const int wi = (kh >> 5) + c;
+                        if (kh + 32 * c < lk && wi < p.drop_mask_w) mdst[wi] = kw[c];
+                    }
+                }
             }
             uint32_t bw[kBias ? HK / 2 : 1];
             if constexpr (kBias) fetch_bias(bw, kh);

@@ -46,6 +46,13 @@ struct BwdParams {
     int drop_t;
     uint32_t drop_key0, drop_key1, drop_offset;
     float drop_scale;
+    // optional keep flags as bits (null: none): word w of query row r (the
+    // LSE row order: (b * Hq + h) * Sq + i, varlen h * total_q + cu_q[b] + i)
+    // at drop_mask[r * drop_mask_w + w], bit l = key 32 w + l kept.  The
+    // forward writes the words of the key blocks it visits; the backward reads
+    // them instead of drawing the mask again.
+    uint32_t *drop_mask;
+    int drop_mask_w;
     // workspace
     int *err;           // device error word
     int4 *tiles;        // work units (b, n_block, hk, 0)

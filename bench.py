@@ -198,6 +198,8 @@ def main():
     ap.add_argument("--bias", action="store_true",
                     help="elementwise bias [B, Hq, Sq, Sk] and its gradient dBias")
     ap.add_argument("--dropout", type=float, default=0.0, help="dropout probability")
+    ap.add_argument("--dropout-mask", action="store_true",
+                    help="with --dropout: the forward stores the keep flags, the backward reads them")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -465,6 +467,12 @@ def run_ext(args, w):
         dbias = torch.empty_like(ext["bias"])
     if args.dropout > 0:
         ext["dropout"] = (args.dropout, 0x5EED, 0)
+        if args.dropout_mask:
+            # the forward writes the keep flags, the backward reads them
+            mask = torch.empty(fa.dropout_mask_shape(q, k, vl.get("cu_seqlens_q"),
+                                                     vl.get("max_seqlen_k")),
+                               dtype=torch.int32, device=dev)
+            ext["dropout"] = (args.dropout, 0x5EED, 0, mask)
     lengths = x.get("lengths") or [w.Sq] * w.B
     pairs = sum(visible_pairs(L, L if varlen else w.Sk, w.causal, wl, wr) for L in lengths) * w.Hq
     fl_fwd, fl_bwd = 4.0 * w.D * pairs, 10.0 * w.D * pairs
@@ -508,7 +516,9 @@ def run_ext(args, w):
     status = fa.device_status(work)
     fstatus = fa.device_status()
     pk = peaks()
-    exts = {k_: (list(v_) if k_ in ("window", "dropout") else True) for k_, v_ in ext.items()}
+    exts = {k_: (list(v_[:3]) if k_ in ("window", "dropout") else True) for k_, v_ in ext.items()}
+    if len(ext.get("dropout", ())) > 3:
+        exts["dropout_mask"] = "stored by the forward, read by the backward"
     if dbias is not None:
         exts["dbias"] = True
     line = {

@@ -184,7 +184,16 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
  *   (j / 4) % 4 of Philox4x32-10 (Salmon et al., SC 2011) with counter
  *   (j / 16, i, b * Hq + h, dropout_offset) and key (low, high 32 bits of
  *   dropout_seed) is below t.  fa_bwd_ext must get the forward's seed and
- *   offset.  The pages print no generator; this one is the reading taken. */
+ *   offset.  The pages print no generator; this one is the reading taken.
+ * dropout_mask (optional, device, 4-byte aligned; used only when t > 0): the
+ *   keep flags as bits, W = ceil(Sk / 32) uint32 words per query row, rows in
+ *   the order of lse ([B, Hq, Sq], or [Hq, total_q] with cu_seqlens; Sk is
+ *   then the max_seqlen_k given).  Bit l of word w of row (b, h, i) is 1 iff
+ *   key 32 w + l is kept.  fa_fwd_ext writes the words of the key blocks it
+ *   visits (others are left as they were); fa_bwd_ext given the same buffer
+ *   reads them instead of running Philox again (in deterministic mode the
+ *   results are bit-identical to drawing the mask).  The buffer must hold
+ *   B * Hq * Sq * W words (Hq * total_q * W with cu_seqlens). */
 typedef struct {
     int window_left;
     int window_right;
@@ -200,6 +209,7 @@ typedef struct {
     float dropout_p;
     unsigned long long dropout_seed;
     unsigned int dropout_offset;
+    unsigned int *dropout_mask;
 } fa_ext;
 
 /* fa_fwd with extensions.  Errors as fa_fwd, plus FA_ERR_INVALID_ARG for a

@@ -262,6 +262,62 @@ def test_dropout_varlen_and_deterministic(fa, oracle_mod, cuda_device):
     _check_bwd(oracle_mod, w, x, ok, a)
 
 
+# The keep-flag buffer: fa_fwd writes the flags, fa_bwd reads them instead of
+# running Philox again (workload, options, varlen lengths).
+MASK_CASES = [
+    (W("drop_mask_causal_d128_gqa", 2, 300, 300, 4, 2, 128, causal=True),
+     dict(dropout=(0.1, 77, 5)), None),
+    (W("drop_mask_d64_fp16_sq_lt_sk", 1, 190, 333, 2, 2, 64, "fp16"),
+     dict(dropout=(0.3, 42, 7)), None),
+    (W("drop_mask_bias_alibi_d128", 1, 260, 260, 2, 1, 128, causal=True),
+     dict(dropout=(0.2, 9, 1), bias="b1", alibi="h"), None),
+    (W("drop_mask_vl_d128", 3, 0, 0, 2, 1, 128, "bf16", True, varlen=(3, 1, 300)),
+     dict(dropout=(0.25, 1234567, 11)), [300, 129, 40]),
+]
+
+
+@pytest.mark.parametrize("w,opt,lengths", MASK_CASES,
+                         ids=lambda v: v.name if hasattr(v, "name") else "")
+def test_dropout_mask_buffer(fa, oracle_mod, cuda_device, w, opt, lengths):
+    x, ok, gk = _case(oracle_mod, w, opt, lengths=lengths)
+    kw = _kw(w, x)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    shape = fa.dropout_mask_shape(q, k, kw.get("cu_seqlens_q"), kw.get("max_seqlen_k"))
+    mask = torch.full(shape, -1, dtype=torch.int32, device="cuda")
+    gk_m = dict(gk, dropout=tuple(gk["dropout"]) + (mask,))
+    o, lse = fa.fa_fwd(q, k, v, causal=w.causal, softmax_scale=w.softmax_scale, **kw, **gk_m)
+    torch.cuda.synchronize()
+    assert fa.device_status() == 0
+    check_bar(o, x["o64"], "o")
+    # reading the flags gives the gradients drawing them gives, bit for bit in
+    # deterministic mode (otherwise the dQ sums' order varies from run to run)
+    drawn = _run_bwd(fa, w, x, gk, deterministic=True)
+    read = _run_bwd(fa, w, x, gk_m, deterministic=True)
+    for a, b, n in zip(drawn, read, ("dq", "dk", "dv")):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), n
+    _check_bwd(oracle_mod, w, x, ok, read)
+    # the stored flags against the oracle's mask on every visible entry
+    words = mask.cpu().numpy().view(np.uint32)
+    cu = x.get("cu_q")
+    cu_np = None if cu is None else cu.numpy()
+    for b in sorted({0, x["q"].shape[0] - 1 if cu is None else len(lengths) - 1}):
+        for h in sorted({0, w.Hq - 1}):
+            S_o = (w.Sq, w.Sk) if cu is None else (x["max_len"], x["max_len"])
+            F = oracle_mod.dropout_factors(w.B, S_o[0], S_o[1], w.Hq, w.Hkv, w.D, b, h,
+                                           cu_q=cu_np, cu_k=cu_np, **ok)
+            lq, lk = F.shape
+            if cu is None:
+                rows = words[b, h, :lq]
+            else:
+                rows = words[h, int(cu_np[b]):int(cu_np[b]) + lq]
+            j = np.arange(lk)
+            bits = (rows[:, j // 32] >> (j % 32).astype(np.uint32)) & 1
+            vis = np.ones((lq, lk), dtype=bool)
+            if w.causal:
+                vis = j[None, :] <= np.arange(lq)[:, None] + (lk - lq)
+            assert np.array_equal(bits[vis].astype(bool), (F > 0)[vis]), (b, h)
+
+
 def test_dbias_without_bias(fa, oracle_mod, cuda_device):
     w = W("dbias_only", 1, 190, 190, 2, 2, 128, causal=True)
     x, ok, gk = _case(oracle_mod, w, {})
