@@ -122,3 +122,44 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(mod, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no fallback"):
         mod.lib()
+
+
+def test_fa_ext_layout_matches_the_header(fa, tmp_path):
+    """The binding's FaExt has the size and field offsets of fa_ext in
+    include/fa.h, as a C compiler lays it out."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    cuda_inc = None
+    for d in (os.environ.get("CUDA_HOME"), "/usr/local/cuda"):
+        if d and os.path.exists(os.path.join(d, "include", "cuda_runtime_api.h")):
+            cuda_inc = os.path.join(d, "include")
+    if cc is None or cuda_inc is None:
+        pytest.skip("no C compiler or CUDA headers")
+    fields = [f[0] for f in fa.FaExt._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text(
+        "#include <stdio.h>\n#include <stddef.h>\n#include \"fa.h\"\n"
+        "int main(void) {\n  printf(\"%zu\\n\", sizeof(fa_ext));\n" +
+        "".join("  printf(\"%%zu\\n\", offsetof(fa_ext, %s));\n" % f for f in fields) +
+        "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src), "-o",
+                    str(exe)], check=True, capture_output=True)
+    out = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True,
+                                          text=True).stdout.split()]
+    assert out[0] == ctypes.sizeof(fa.FaExt)
+    for f, off in zip(fields, out[1:]):
+        assert getattr(fa.FaExt, f).offset == off, f
+
+
+def test_dropout_mask_shape():
+    import torch
+    import attention_backward_preprocess_gb300 as m
+    q = torch.empty(2, 300, 4, 64)
+    k = torch.empty(2, 333, 2, 64)
+    assert m.dropout_mask_shape(q, k) == (2, 4, 300, 11)
+    qv = torch.empty(469, 4, 64)
+    kv = torch.empty(469, 2, 64)
+    cu = torch.tensor([0, 300, 429, 469], dtype=torch.int32)
+    assert m.dropout_mask_shape(qv, kv, cu, 300) == (4, 469, 10)
