@@ -81,9 +81,10 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                   void *o_out, float *lse_out, int nmb) {
     using C = FwdCfg<kD, T>;
     constexpr int D = C::D, BM = C::BM, BN = C::BN, S = C::kStages;
-    constexpr bool kAlibi = (kFlags & kFwdAlibi) != 0, kBias = (kFlags & kFwdBias) != 0,
-                   kDrop = (kFlags & kFwdDrop) != 0;
-    constexpr bool kExt = kAlibi || kBias;   // scores other than the plain scaled ones
+    static_assert((kFlags & (kFwdBias | kFwdDrop)) == 0,
+                  "the bias and dropout instances run in fa_fwd_split.cu");
+    constexpr bool kAlibi = (kFlags & kFwdAlibi) != 0;
+    constexpr bool kExt = kAlibi;   // scores other than the plain scaled ones
     // ---- tile of this CTA: longest causal rows first
     const int bh = blockIdx.x % (p.B * p.Hq);
     const int m = nmb - 1 - blockIdx.x / (p.B * p.Hq);
@@ -230,62 +231,11 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
         // visible key (no key right of the diagonal)
         const float slope_u = slope2 / p.scale_log2;
         const bool lin = p.win_hi <= 0;
-        // elementwise bias row of this query (null: none, or a padding row)
-        const T *brow = nullptr;
-        if (kBias && p.bias && qi < lq)
-            brow = reinterpret_cast<const T *>(p.bias) + (long long)b * p.bias_bs +
-                   (long long)h * p.bias_hs + (long long)qi * p.bias_rs;
-        // bias of keys k0 .. k0 + 31 in log2 units (0 past lk); 16-byte loads
-        // when the 32 keys are all in range (k0 is a multiple of 32, the row
-        // start 16-byte aligned)
-        auto load_bias = [&](float (&bl)[32], int k0) __attribute__((always_inline)) {
-            if (brow && k0 + 32 <= lk) {
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(brow + k0) + t);
-                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float2 f = Cvt<T>::unpack(w4[u]);
-                        bl[8 * t + 2 * u] = f.x * 1.4426950408889634f;
-                        bl[8 * t + 2 * u + 1] = f.y * 1.4426950408889634f;
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    bl[i] = (brow && k0 + i < lk) ? static_cast<float>(brow[k0 + i]) * 1.4426950408889634f
-                                                  : 0.f;
-            }
-        };
         float m_run = -INFINITY, l_run = 0.f;       // running max (log2 units), row sum
         bool ok = true;
         for (int n = 0; n < nblk; ++n) {
             const int bb = n & 1;
             const int kb = (n_begin + n) * BN;
-            // dropout keep flags of this row's 128 keys (bit l of kw[c]: key
-            // kb + 32c + l), drawn before S is ready (the wait hides them)
-            uint32_t kw[BN / 32];
-            if (kDrop) {
-                const uint32_t tt4 = (uint32_t)p.drop_t * 0x01010101u;
-#pragma unroll
-                for (int g = 0; g < BN / 16; ++g) {
-                    const uint4 R = philox4x32_10(make_uint4((uint32_t)(kb >> 4) + g, (uint32_t)qi,
-                                                             (uint32_t)(b * p.Hq + h), p.drop_offset),
-                                                  p.drop_key0, p.drop_key1);
-                    const uint32_t wd[4] = {R.x, R.y, R.z, R.w};
-                    uint32_t bits = 0u;
-#pragma unroll
-                    for (int wi = 0; wi < 4; ++wi) {
-                        // bytes >= t -> 0xFF; the low bits of the 4 bytes gathered
-                        // into bits 28-31 by one product
-                        const uint32_t ge = __vcmpgeu4(wd[wi], tt4) & 0x01010101u;
-                        bits |= ((ge * 0x10204080u) >> 28) << (4 * wi);
-                    }
-                    if (g & 1) kw[g >> 1] |= bits << 16;
-                    else kw[g >> 1] = bits;
-                }
-            }
             if (!(ok = mbar_wait_warp(bar(F_S_FULL + bb), (uint32_t)(n >> 1) & 1u, w))) break;
             tc_fence_after();
             const uint32_t scol = lane_addr + C::TM_S + bb * BN;
@@ -293,10 +243,9 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
             const int lo = kmin - kb, hi = kmax - kb;
             // ALiBi: key kb + e lies (kb + e) - (qi + diag) = fbase + e from the diagonal
             const float fbase = (float)(kb - qi - diag);
-            // scaled score of element e with its bias (bl: bias * log2e), log2 units
-            auto score2 = [&](uint32_t raw, int e, float bl) __attribute__((always_inline)) -> float {
-                float x = kBias ? bl : 0.f;
-                if (kAlibi) x = fmaf(-slope2, fabsf(fbase + (float)e), x);
+            // scaled score of element e with its ALiBi term, log2 units
+            auto score2 = [&](uint32_t raw, int e) __attribute__((always_inline)) -> float {
+                const float x = fmaf(-slope2, fabsf(fbase + (float)e), 0.f);
                 return fmaf(__uint_as_float(raw), p.scale_log2, x);
             };
             // Blocks inside every row's band (all but the edge blocks) take the
@@ -313,26 +262,16 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
             auto block_pass = [&](auto mask_tag, auto lin_tag) __attribute__((always_inline)) {
                 constexpr bool kMask = decltype(mask_tag)::value;
                 constexpr bool kLin = decltype(lin_tag)::value;
-                // the row's 128 scores: without the bias, held in registers --
-                // four loads in flight and one wait, one round trip to tensor
-                // memory per block instead of eight (the softmax is latency
-                // bound: 0.99 -> see the kernel table); with the bias (more
-                // registers live) or dropout, loaded chunk by chunk in each pass
-                constexpr bool kResident = !kBias && !kDrop;
-                uint32_t srr[kResident ? BN / 32 : 1][32];
-                if (kResident) {
+                // the row's 128 scores, held in registers: four loads in
+                // flight and one wait, one round trip to tensor memory per
+                // block instead of eight (the softmax is latency bound)
+                uint32_t srr[BN / 32][32];
 #pragma unroll
-                    for (int c = 0; c < BN / 32; ++c) tmem_ld32(scol + 32 * c, srr[kResident ? c : 0]);
-                    tmem_wait_ld();
-                }
+                for (int c = 0; c < BN / 32; ++c) tmem_ld32(scol + 32 * c, srr[c]);
+                tmem_wait_ld();
                 auto chunk = [&](int c, uint32_t (&dst)[32]) __attribute__((always_inline)) {
-                    if (kResident) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) dst[i] = srr[kResident ? c : 0][i];
-                    } else {
-                        tmem_ld32(scol + 32 * c, dst);
-                        tmem_wait_ld();
-                    }
+                    for (int i = 0; i < 32; ++i) dst[i] = srr[c][i];
                 };
                 // pass 1: row maximum of the block (without ALiBi the maximum of
                 // the raw scores, scaled once: the scale is positive), in eight
@@ -344,13 +283,11 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t sr[32];
                     chunk(c, sr);
-                    float bl[32];
-                    if (kBias) load_bias(bl, kb + 32 * c);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int e = 32 * c + i;
                         const float x = kLin   ? fmaf(slope_u, (float)e, __uint_as_float(sr[i]))
-                                        : kExt ? score2(sr[i], e, bl[i])
+                                        : kExt ? score2(sr[i], e)
                                                : __uint_as_float(sr[i]);
                         mxv[i & 7] = (!kMask || (e >= lo && e <= hi)) ? fmaxf(mxv[i & 7], x) : mxv[i & 7];
                     }
@@ -372,8 +309,6 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t sr[32];
                     chunk(c, sr);
-                    float bl[32];
-                    if (kBias) load_bias(bl, kb + 32 * c);
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -384,8 +319,8 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                             p1 = ex2(fmaf(__uint_as_float(sr[2 * i + 1]), p.scale_log2,
                                           fmaf(slope2, (float)(e + 1), cl)));
                         } else if (kExt) {
-                            p0 = ex2(score2(sr[2 * i], e, bl[2 * i]) - mref);
-                            p1 = ex2(score2(sr[2 * i + 1], e + 1, bl[2 * i + 1]) - mref);
+                            p0 = ex2(score2(sr[2 * i], e) - mref);
+                            p1 = ex2(score2(sr[2 * i + 1], e + 1) - mref);
                         } else {
                             p0 = ex2(fmaf(__uint_as_float(sr[2 * i]), p.scale_log2, -mref));
                             p1 = ex2(fmaf(__uint_as_float(sr[2 * i + 1]), p.scale_log2, -mref));
@@ -394,18 +329,14 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                             p0 = (e >= lo && e <= hi) ? p0 : 0.f;
                             p1 = (e + 1 >= lo && e + 1 <= hi) ? p1 : 0.f;
                         }
-                        sumv[i & 3] += p0 + p1;   // the row sum is taken before dropout
-                        if (kDrop) {   // keys 2i, 2i + 1 of the chunk
-                            p0 = ((kw[c] >> (2 * i)) & 1u) ? p0 * p.drop_scale : 0.f;
-                            p1 = ((kw[c] >> (2 * i + 1)) & 1u) ? p1 * p.drop_scale : 0.f;
-                        }
+                        sumv[i & 3] += p0 + p1;
                         pk[i] = Cvt<T>::pack(p0, p1);
                     }
                     tmem_st16(scol + 16 * c, pk);
                 }
             };
             auto run = [&](auto mask_tag) __attribute__((always_inline)) {
-                if constexpr (kAlibi && !kBias) {
+                if constexpr (kAlibi) {
                     if (lin) block_pass(mask_tag, std::true_type{});
                     else block_pass(mask_tag, std::false_type{});
                 } else {
