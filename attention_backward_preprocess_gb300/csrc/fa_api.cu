@@ -285,13 +285,6 @@ fa_status prepare(const void *q, const void *k, const void *v, const void *o, co
     Layout L;
     if (!plan(B, Sq, Sk, Hq, Hkv, D, cu_q != nullptr, deterministic, &L)) return FA_ERR_INVALID_ARG;
     if (ws_bytes < L.total) return FA_ERR_INVALID_ARG;
-    st = check_device();
-    if (st != FA_OK) return st;
-    long long tq = (long long)B * Sq, tk = (long long)B * Sk;
-    if (cu_q) {
-        st = varlen_totals(cu_q, cu_k, B, stream, &tq, &tk);
-        if (st != FA_OK) return st;
-    }
     uint8_t *w = static_cast<uint8_t *>(ws);
     fa::BwdParams &p = out->p;
     std::memset(&p, 0, sizeof(p));
@@ -305,7 +298,15 @@ fa_status prepare(const void *q, const void *k, const void *v, const void *o, co
     p.deterministic = deterministic ? 1 : 0;
     p.varlen = cu_q != nullptr;
     p.cu_q = cu_q; p.cu_k = cu_k;
+    // the extensions are host arguments too: checked before the device is
     if ((st = apply_ext(p, causal, ext)) != FA_OK) return st;
+    st = check_device();
+    if (st != FA_OK) return st;
+    long long tq = (long long)B * Sq, tk = (long long)B * Sk;
+    if (cu_q) {
+        st = varlen_totals(cu_q, cu_k, B, stream, &tq, &tk);
+        if (st != FA_OK) return st;
+    }
     p.err = reinterpret_cast<int *>(w + L.err);
     p.ntiles = reinterpret_cast<int *>(w + L.ntiles);
     p.unit_counter = reinterpret_cast<int *>(w + L.ntiles) + 1;
@@ -566,7 +567,6 @@ fa_status fa_fwd_ext(const void *q, const void *k, const void *v, void *o, float
     const void *ptrs[] = {q, k, v, o, lse};
     for (const void *ptr : ptrs)
         if (!aligned16(ptr)) return FA_ERR_INVALID_ARG;
-    if ((st = check_device()) != FA_OK) return st;
     fa::BwdParams p;
     std::memset(&p, 0, sizeof(p));
     p.q = q; p.k = k; p.v = v;
@@ -579,6 +579,7 @@ fa_status fa_fwd_ext(const void *q, const void *k, const void *v, void *o, float
     p.cu_q = cu_seqlens_q;
     p.cu_k = cu_seqlens_k;
     if ((st = apply_ext(p, causal, ext)) != FA_OK) return st;
+    if ((st = check_device()) != FA_OK) return st;
     p.err = fa::fwd_error_word();
     if (!p.err) return FA_ERR_CUDA;
     p.budget_ns = g_budget_ns.load();

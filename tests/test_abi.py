@@ -163,3 +163,47 @@ def test_dropout_mask_shape():
     kv = torch.empty(469, 2, 64)
     cu = torch.tensor([0, 300, 429, 469], dtype=torch.int32)
     assert m.dropout_mask_shape(qv, kv, cu, 300) == (4, 469, 10)
+
+
+# Extension arguments the library must refuse on the host, before it looks at
+# the device (every case here fails validation, so nothing is launched).
+EXT_BAD = [
+    (dict(window_left=-2), 1),
+    (dict(window_right=-5), 1),
+    (dict(alibi_slopes=0x2000, alibi_batch_stride=3), 1),   # stride neither 0 nor Hq
+    (dict(alibi_slopes=0x2002), 1),                         # slopes not 4-byte aligned
+    (dict(seqused_q=0x2001), 1),
+    (dict(dropout_p=1.0), 1),
+    (dict(dropout_p=-0.25), 1),
+    (dict(dropout_p=0.1, dropout_mask=0x3002), 1),          # mask not 4-byte aligned
+    (dict(bias=0x4008), 1),                                 # bias not 16-byte aligned
+]
+
+
+def _fa_ext(fa, over):
+    e = fa.FaExt(-1, -1, None, 0, None, None, None, 0, 0, 0, None, 0.0, 0, 0, None)
+    for name, val in over.items():
+        setattr(e, name, val)
+    return e
+
+
+@pytest.mark.parametrize("over,status", EXT_BAD, ids=lambda v: ",".join(v) if isinstance(v, dict) else "")
+def test_extension_arguments_rejected_on_the_host(fa, over, status):
+    L = fa.lib()
+    vp = ctypes.c_void_p
+    ptrs = [vp(0x1000 * (i + 1)) for i in range(9)]
+    e = _fa_ext(fa, over)
+    shape = (1, 128, 128, 2, 2, 64)
+    assert L.fa_fwd_ext(*ptrs[:5], *shape, 0.125, 1, None, None, ctypes.byref(e), 0, None) == status
+    assert L.fa_bwd_ext(*ptrs, *shape, 0.125, 1, None, None, ctypes.byref(e), 0, 0,
+                        vp(0x100000), ctypes.c_size_t(1 << 40), None) == status
+
+
+def test_bias_with_varlen_is_unsupported(fa):
+    L = fa.lib()
+    vp = ctypes.c_void_p
+    ptrs = [vp(0x1000 * (i + 1)) for i in range(9)]
+    e = _fa_ext(fa, dict(bias=0x4000, bias_row_stride=128))
+    cu = vp(0x8000)
+    assert L.fa_fwd_ext(*ptrs[:5], 2, 128, 128, 2, 2, 64, 0.125, 1, cu, cu, ctypes.byref(e), 0,
+                        None) == 2
