@@ -59,6 +59,23 @@ def clock_log_path(name):
     return os.path.join(d, "%s.%d.csv" % (name, os.getpid()))
 
 
+def max_over_ranks(x, device):
+    """The largest value of x over all ranks of the process group (x itself
+    without one): the job's time is that of its slowest rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flop_per_rank, world_size, ms_per_step):
+    """Whole-job TFLOPS: the work of every rank over the slowest rank's time."""
+    return flop_per_rank * world_size / (ms_per_step * 1e-3) / 1e12
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -291,12 +308,9 @@ def main():
     main_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
     post_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(args.steps)]
     status = fa.device_status(work)
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / args.steps
-    value = flops * ws / (ms_per_step * 1e-3) / 1e12
+    value = job_throughput(flops, ws, ms_per_step)
 
     # ---------------------------------------------------------------- e2e
     e2e = None
@@ -357,12 +371,8 @@ def main():
         stream.wait_stream(d2h_s)
         t2.record(stream)
         barrier()
-        e2e_ms = s2.elapsed_time(t2) / e2e_steps
-        if ws > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        e2e_ms = max_over_ranks(s2.elapsed_time(t2) / e2e_steps, dev)
+        e2e = {"value": job_throughput(flops, ws, e2e_ms), "unit": UNIT,
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": e2e_steps}
 
