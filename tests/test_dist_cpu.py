@@ -60,3 +60,27 @@ def test_single_rank_needs_no_process_group(monkeypatch):
     assert bench.dist_env() == (1, 0, 0)
     assert bench.max_over_ranks(3.5, "cpu") == 3.5
     assert bench.job_throughput(1.0e12, 1, 1.0) == pytest.approx(1000.0)
+
+
+def test_reference_arm_prints_the_contract_line():
+    """bench.py --impl reference: the oracle on a bounded sample, one JSON line
+    with the keys the benchmark contract asks for (CPU only)."""
+    import json
+    import subprocess
+    env = dict(os.environ)
+    for name in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        env.pop(name, None)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--ref-prefix", "128", "--steps", "1", "--warmup", "0"],
+                       capture_output=True, text=True, env=env, timeout=600, check=True)
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["config"]["workload"] == "b2_hq32_hkv8_s8192_d128_causal_gqa"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
