@@ -207,3 +207,46 @@ def test_bias_with_varlen_is_unsupported(fa):
     cu = vp(0x8000)
     assert L.fa_fwd_ext(*ptrs[:5], 2, 128, 128, 2, 2, 64, 0.125, 1, cu, cu, ctypes.byref(e), 0,
                         None) == 2
+
+
+def test_forward_instance_choice(tmp_path):
+    """The forward's instance choice (fa_fwd_common.h, host code): for every
+    set of extensions a call needs, the instance picked has all of them and is
+    the first such in the built list; the bias, dropout and D = 64 instances
+    go to the two-warps-per-row kernel, the others to the one-warp kernel."""
+    import shutil
+    import subprocess
+    cxx = shutil.which("g++") or shutil.which("c++")
+    cuda_inc = None
+    for d in (os.environ.get("CUDA_HOME"), "/usr/local/cuda"):
+        if d and os.path.exists(os.path.join(d, "include", "cuda.h")):
+            cuda_inc = os.path.join(d, "include")
+    if cxx is None or cuda_inc is None:
+        pytest.skip("no C++ compiler or CUDA headers")
+    csrc = os.path.join(ROOT, "attention_backward_preprocess_gb300", "csrc")
+    src = tmp_path / "choice.cpp"
+    src.write_text(
+        # the header's inline helpers use CUDA's min / max; the host build
+        # takes the standard ones
+        '#include <cstdio>\n#include <algorithm>\nusing std::max;\nusing std::min;\n'
+        '#include "fa_fwd_common.h"\n'
+        "int main() {\n"
+        "  for (int i = 0; i < fa::kNumFwdFlagSets; ++i) std::printf(\"set %d\\n\", fa::kFwdFlagSets[i]);\n"
+        "  for (int need = 0; need < 16; need += 2)\n"
+        "    std::printf(\"pick %d %d %d %d\\n\", need, fa::fwd_instance_flags(need),\n"
+        "                fa::fwd_split(128, fa::fwd_instance_flags(need)),\n"
+        "                fa::fwd_split(64, fa::fwd_instance_flags(need)));\n"
+        "  return 0;\n}\n")
+    exe = tmp_path / "choice"
+    subprocess.run([cxx, "-std=c++17", "-I", csrc, "-I", os.path.join(ROOT, "include"), "-I",
+                    cuda_inc, str(src), "-o", str(exe)], check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    sets = [int(ln.split()[1]) for ln in out if ln.startswith("set")]
+    picks = [tuple(int(t) for t in ln.split()[1:]) for ln in out if ln.startswith("pick")]
+    assert len(picks) == 8
+    ALIBI, BIAS, DROP = 2, 4, 8
+    for need, got, split128, split64 in picks:
+        assert got & need == need
+        assert got == next(s for s in sets if s & need == need)
+        assert split128 == (1 if got & (BIAS | DROP) else 0)
+        assert split64 == 1
