@@ -28,7 +28,8 @@ EXPORTED = [
     "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_workspace_layout", "fa_fwd",
     "fa_device_status", "fa_set_wait_timeout_ns", "fa_status_string",
     "fa_selftest_umma", "fa_selftest_semaphore", "fa_selftest_tmem_layout", "fa_bwd_noalloc",
-    "fa_bwd_noalloc_scratch_bytes", "fa_fwd_ext", "fa_bwd_ext",
+    "fa_bwd_noalloc_scratch_bytes", "fa_fwd_ext", "fa_bwd_ext", "fa_bwd_workspace_sync_layout",
+    "fa_bwd_noalloc_status",
 ]
 
 
@@ -57,7 +58,8 @@ class FaExt(ctypes.Structure):
                 ("bias_head_stride", ctypes.c_longlong), ("bias_row_stride", ctypes.c_longlong),
                 ("dbias", ctypes.c_void_p), ("dropout_p", ctypes.c_float),
                 ("dropout_seed", ctypes.c_ulonglong), ("dropout_offset", ctypes.c_uint),
-                ("dropout_mask", ctypes.c_void_p)]
+                ("dropout_mask", ctypes.c_void_p), ("total_q", ctypes.c_longlong),
+                ("total_k", ctypes.c_longlong)]
 
 
 def dropout_mask_shape(q, k, cu_seqlens_q=None, max_seqlen_k=None):
@@ -71,7 +73,7 @@ def dropout_mask_shape(q, k, cu_seqlens_q=None, max_seqlen_k=None):
 
 
 def _ext(Hq, window=None, alibi_slopes=None, seqused_q=None, seqused_k=None, bias=None,
-         dbias=None, dropout=None):
+         dbias=None, dropout=None, totals=None):
     """A pointer to an FaExt, or None when no extension is asked for.
 
     ``bias``: [B or 1, Hq or 1, Sq, >= Sk] in the input dtype, last axis
@@ -79,11 +81,15 @@ def _ext(Hq, window=None, alibi_slopes=None, seqused_q=None, seqused_k=None, bia
     contiguous [B, Hq, Sq, Sk] output of the input dtype (backward only).
     ``dropout``: (p, seed, offset), or (p, seed, offset, mask) with ``mask`` an
     int32 tensor of ``dropout_mask_shape(...)`` that fa_fwd fills with the keep
-    flags and fa_bwd reads back; see fa_ext in include/fa.h."""
+    flags and fa_bwd reads back; see fa_ext in include/fa.h.  ``totals``:
+    (total_q, total_k), the packed row counts of a varlen call (cu_seqlens[B]),
+    so that the library need not read them back (no stream synchronisation)."""
     if (window is None and alibi_slopes is None and seqused_q is None and seqused_k is None
-            and bias is None and dbias is None and dropout is None):
+            and bias is None and dbias is None and dropout is None and totals is None):
         return None
-    e = FaExt(-1, -1, None, 0, None, None, None, 0, 0, 0, None, 0.0, 0, 0, None)
+    e = FaExt(-1, -1, None, 0, None, None, None, 0, 0, 0, None, 0.0, 0, 0, None, 0, 0)
+    if totals is not None:
+        e.total_q, e.total_k = int(totals[0]), int(totals[1])
     if dropout is not None:
         e.dropout_p, e.dropout_seed, e.dropout_offset = (float(dropout[0]), int(dropout[1]),
                                                          int(dropout[2]))
@@ -152,6 +158,10 @@ def lib():
         L.fa_bwd_noalloc.restype = _i
         L.fa_bwd_noalloc_scratch_bytes.argtypes = []
         L.fa_bwd_noalloc_scratch_bytes.restype = _sz
+        L.fa_bwd_noalloc_status.argtypes = [_vp]
+        L.fa_bwd_noalloc_status.restype = _i
+        L.fa_bwd_workspace_sync_layout.argtypes = _SHAPE + [_i, _i] + [ctypes.POINTER(_sz)] * 3
+        L.fa_bwd_workspace_sync_layout.restype = _i
         L.fa_selftest_umma.argtypes = [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]
         L.fa_selftest_semaphore.argtypes = [_vp, _i, ctypes.c_longlong, _vp, _vp]
         L.fa_selftest_tmem_layout.argtypes = [_i, _vp, _vp]
@@ -210,13 +220,15 @@ def default_scale(D: int) -> float:
 
 def fa_fwd(q, k, v, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seqlens_k=None,
            max_seqlen_q=None, max_seqlen_k=None, stream=None, window=None, alibi_slopes=None,
-           seqused_q=None, seqused_k=None, bias=None, dropout=None):
+           seqused_q=None, seqused_k=None, bias=None, dropout=None, totals=None):
     """Forward pass: returns (o, lse); lse fp32 [B,Hq,Sq] or [Hq,total_q].
 
     ``window=(left, right)`` (-1 = unbounded side), ``alibi_slopes`` (fp32
     [Hq] or [B, Hq]), ``seqused_q`` / ``seqused_k`` (int32 [B]) and ``bias``
     (see ``_ext``) and ``dropout=(p, seed, offset)`` select fa_fwd_ext; rows
-    past the used lengths are left as allocated.
+    past the used lengths are left as allocated.  ``totals=(total_q, total_k)``
+    (varlen: cu_seqlens_q[B], cu_seqlens_k[B]) spares the read-back of the
+    packed totals, so the call does not synchronise the stream.
     """
     B, Sq, Sk, Hq, Hkv, D = _shape(q, k, cu_seqlens_q, max_seqlen_q, max_seqlen_k)
     scale = default_scale(D) if softmax_scale is None else float(softmax_scale)
@@ -225,7 +237,8 @@ def fa_fwd(q, k, v, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seql
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
     else:
         lse = torch.empty((Hq, q.shape[0]), dtype=torch.float32, device=q.device)
-    ext = _ext(Hq, window, alibi_slopes, seqused_q, seqused_k, bias, dropout=dropout)
+    ext = _ext(Hq, window, alibi_slopes, seqused_q, seqused_k, bias, dropout=dropout,
+               totals=totals)
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Sq, Sk, Hq, Hkv, D, scale,
             int(bool(causal)), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k)]
     if ext is None:
@@ -239,14 +252,16 @@ def fa_bwd(q, k, v, o, dout, lse, causal=False, softmax_scale=None, cu_seqlens_q
            cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, deterministic=False,
            dq=None, dk=None, dv=None, workspace=None, stream=None, window=None,
            alibi_slopes=None, seqused_q=None, seqused_k=None, bias=None, dbias=None,
-           dropout=None):
+           dropout=None, totals=None):
     """Backward pass through the C ABI; returns (dq, dk, dv).
 
     Outputs are allocated when not given.  ``workspace`` (a uint8 CUDA tensor
     of at least ``workspace_bytes(...)``) selects fa_bwd_with_workspace,
     otherwise the library's own workspace is used.  The extension keywords
     (as for fa_fwd, plus ``dbias``, an output tensor filled with dBias = dS)
-    select fa_bwd_ext.
+    select fa_bwd_ext, and so does ``totals=(total_q, total_k)`` (varlen: the
+    packed row counts, which spare the stream synchronisation of reading them
+    back).
     """
     B, Sq, Sk, Hq, Hkv, D = _shape(q, k, cu_seqlens_q, max_seqlen_q, max_seqlen_k)
     scale = default_scale(D) if softmax_scale is None else float(softmax_scale)
@@ -256,7 +271,7 @@ def fa_bwd(q, k, v, o, dout, lse, causal=False, softmax_scale=None, cu_seqlens_q
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
             _ptr(dv), B, Sq, Sk, Hq, Hkv, D, scale, int(bool(causal)), _ptr(cu_seqlens_q),
             _ptr(cu_seqlens_k), int(bool(deterministic)), _dtype_code(q)]
-    ext = _ext(Hq, window, alibi_slopes, seqused_q, seqused_k, bias, dbias, dropout)
+    ext = _ext(Hq, window, alibi_slopes, seqused_q, seqused_k, bias, dbias, dropout, totals)
     if ext is not None:
         st = lib().fa_bwd_ext(*args[:19], ext, *args[19:], _ptr(workspace),
                               0 if workspace is None else workspace.numel(), _stream(stream))
@@ -289,6 +304,23 @@ def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, causal=False, softmax_scal
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
         B, Sq, Sk, Hq, Hkv, D, scale, int(bool(causal)), _ptr(cu_seqlens_q),
         _ptr(cu_seqlens_k), int(bool(deterministic)), _dtype_code(q), _stream(stream)))
+
+
+def noalloc_status(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the error status of
+    the fixed scratch array fa_bwd_noalloc works in."""
+    return int(lib().fa_bwd_noalloc_status(_stream(stream)))
+
+
+def workspace_sync_layout(B, Sq, Sk, Hq, Hkv, D, varlen=False, deterministic=False) -> dict:
+    """Byte offsets of the error word and of the deterministic-order
+    semaphores inside a workspace, and the number of semaphores."""
+    vals = [_sz() for _ in range(3)]
+    st = lib().fa_bwd_workspace_sync_layout(B, Sq, Sk, Hq, Hkv, D, int(bool(varlen)),
+                                            int(bool(deterministic)),
+                                            *[ctypes.byref(x) for x in vals])
+    _check(st, "fa_bwd_workspace_sync_layout")
+    return dict(err=vals[0].value, sem=vals[1].value, n_sem=vals[2].value)
 
 
 def workspace_bytes(B, Sq, Sk, Hq, Hkv, D, varlen=False, deterministic=False) -> int:

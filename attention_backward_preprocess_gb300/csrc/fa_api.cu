@@ -191,6 +191,33 @@ fa_status varlen_totals(const int *cu_q, const int *cu_k, int B, cudaStream_t st
     return FA_OK;
 }
 
+// The packed row counts of a varlen call: the caller's (fa_ext total_q /
+// total_k, both > 0), which need no host synchronisation, else cu[B] read
+// back from the device.  Every sequence fits the planned layout only if the
+// totals are at most B times the maximum lengths; the kernels check
+// cu_seqlens against the totals and the maximum lengths (kErrBadLength).
+fa_status packed_totals(const fa_ext *ext, const int *cu_q, const int *cu_k, int B, int Sq,
+                        int Sk, cudaStream_t stream, long long *tq, long long *tk) {
+    if (ext && (ext->total_q != 0 || ext->total_k != 0)) {
+        *tq = ext->total_q;
+        *tk = ext->total_k;
+    } else {
+        fa_status st = varlen_totals(cu_q, cu_k, B, stream, tq, tk);
+        if (st != FA_OK) return st;
+    }
+    if (*tq > (long long)B * Sq || *tk > (long long)B * Sk) return FA_ERR_INVALID_ARG;
+    return FA_OK;
+}
+
+// Host check of the caller's packed totals (before the device is touched):
+// varlen only, both positive, at most B times the maximum lengths.
+fa_status check_ext_totals(const fa_ext *ext, bool varlen, int B, int Sq, int Sk) {
+    if (!ext || (ext->total_q == 0 && ext->total_k == 0)) return FA_OK;
+    if (!varlen || ext->total_q <= 0 || ext->total_k <= 0) return FA_ERR_INVALID_ARG;
+    if (ext->total_q > (long long)B * Sq || ext->total_k > (long long)B * Sk) return FA_ERR_INVALID_ARG;
+    return FA_OK;
+}
+
 struct Prepared {
     fa::BwdParams p;
     Layout L;
@@ -300,12 +327,14 @@ fa_status prepare(const void *q, const void *k, const void *v, const void *o, co
     p.cu_q = cu_q; p.cu_k = cu_k;
     // the extensions are host arguments too: checked before the device is
     if ((st = apply_ext(p, causal, ext)) != FA_OK) return st;
+    if ((st = check_ext_totals(ext, cu_q != nullptr, B, Sq, Sk)) != FA_OK) return st;
     st = check_device();
     if (st != FA_OK) return st;
     long long tq = (long long)B * Sq, tk = (long long)B * Sk;
     if (cu_q) {
-        st = varlen_totals(cu_q, cu_k, B, stream, &tq, &tk);
-        if (st != FA_OK) return st;
+        if ((st = packed_totals(ext, cu_q, cu_k, B, Sq, Sk, stream, &tq, &tk)) != FA_OK) return st;
+        p.total_q = tq;
+        p.total_k = tk;
     }
     p.err = reinterpret_cast<int *>(w + L.err);
     p.ntiles = reinterpret_cast<int *>(w + L.ntiles);
@@ -381,6 +410,7 @@ fa_status read_error_word(int *err_dev, cudaStream_t stream, bool clear) {
     if (cudaMemcpy(&h, err_dev, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
         return FA_ERR_CUDA;
     if (clear && h != 0 && cudaMemset(err_dev, 0, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+    if (h & 4) return FA_ERR_INVALID_ARG;   // kErrBadLength: cu_seqlens against the sizes given
     return h ? FA_ERR_TIMEOUT : FA_OK;
 }
 
@@ -423,6 +453,18 @@ fa_status fa_bwd_workspace_layout(int B, int Sq, int Sk, int Hq, int Hkv, int D,
     if (lse2_off) *lse2_off = L.lse2 / 4;
     if (dqacc_off) *dqacc_off = L.dqacc / 4;
     if (rows) *rows = (size_t)L.rows;
+    return FA_OK;
+}
+
+fa_status fa_bwd_workspace_sync_layout(int B, int Sq, int Sk, int Hq, int Hkv, int D, int varlen,
+                                       int deterministic, size_t *err_off, size_t *sem_off,
+                                       size_t *n_sem) {
+    Layout L;
+    if (D < 64 || D > 128 || D % 8 != 0) return FA_ERR_UNSUPPORTED;
+    if (!plan(B, Sq, Sk, Hq, Hkv, D, varlen, deterministic, &L)) return FA_ERR_INVALID_ARG;
+    if (err_off) *err_off = L.err;
+    if (sem_off) *sem_off = deterministic ? L.sem : 0;
+    if (n_sem) *n_sem = deterministic ? (size_t)(L.rows / 64) : 0;
     return FA_OK;
 }
 
@@ -579,14 +621,17 @@ fa_status fa_fwd_ext(const void *q, const void *k, const void *v, void *o, float
     p.cu_q = cu_seqlens_q;
     p.cu_k = cu_seqlens_k;
     if ((st = apply_ext(p, causal, ext)) != FA_OK) return st;
+    if ((st = check_ext_totals(ext, p.varlen, B, Sq, Sk)) != FA_OK) return st;
     if ((st = check_device()) != FA_OK) return st;
     p.err = fa::fwd_error_word();
     if (!p.err) return FA_ERR_CUDA;
     p.budget_ns = g_budget_ns.load();
     long long rq = Sq, rk = Sk;
     if (p.varlen) {
-        st = varlen_totals(cu_seqlens_q, cu_seqlens_k, B, stream, &rq, &rk);
+        st = packed_totals(ext, cu_seqlens_q, cu_seqlens_k, B, Sq, Sk, stream, &rq, &rk);
         if (st != FA_OK) return st;
+        p.total_q = rq;
+        p.total_k = rk;
         if (rq == 0) return FA_OK;
     }
     // a map needs at least one row; with no keys at all no K/V tile is loaded

@@ -375,6 +375,10 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 uint32_t kv_ph = 0, st_ph = 0;
                 int stage = 0;
                 bool ok = true;
+                // the phase parity of the last load armed on each barrier, so that
+                // every load still in flight can be waited for before the CTA exits
+                int kv_armed = 0;
+                uint32_t st_armed = 0, st_last = 0;   // bit s: stage s armed / its parity
                 while (ok) {
                     // take the next unit and publish it to the other warps
                     if (!(ok = mbar_wait(ring.empty0 + 8u * ring.k, ring.ph ^ 1, w))) break;
@@ -397,6 +401,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     if (!(ok = mbar_wait(bar(B_KV_EMPTY), kv_ph ^ 1, w))) break;
                     kv_ph ^= 1;
                     mbar_arrive_expect_tx(bar(B_KV_FULL), 2 * C::KV_BYTES);
+                    ++kv_armed;
                     const int krow = u.k_row0 + u.n_block * BN;
 #pragma unroll
                     for (int h = 0; h < D / 64; ++h) {
@@ -411,6 +416,8 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                         if (!(ok = mbar_wait(bar(B_STAGE0 + S + stage), st_ph ^ 1, w))) break;
                         const uint32_t full = bar(B_STAGE0 + stage);
                         mbar_arrive_expect_tx(full, 2 * C::QO_BYTES + 2 * BM * 4);
+                        st_armed |= 1u << stage;
+                        st_last = (st_last & ~(1u << stage)) | (st_ph << stage);
                         const int qrow = u.q_row0 + m * BM;
 #pragma unroll
                         for (int hh = 0; hh < D / 64; ++hh) {
@@ -425,6 +432,11 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                         if (++stage == S) { stage = 0; st_ph ^= 1; }
                     }
                 }
+                // wind-down (after an abort some loads may not have been waited
+                // for by their consumers): none may land after the CTA exits
+                if (kv_armed > 0) mbar_wait_drain(bar(B_KV_FULL), (uint32_t)(kv_armed - 1) & 1u, p.err, p.budget_ns);
+                for (int s2 = 0; s2 < S; ++s2)
+                    if (bit(st_armed, s2)) mbar_wait_drain(bar(B_STAGE0 + s2), bit(st_last, s2), p.err, p.budget_ns);
             }
         } else if (warp == 1) {
             // ------------------------------------------- MMA warp A: S and dP
@@ -477,8 +489,10 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 if (!ok) break;
                 mma_commit_warp(bar(B_KV_EMPTY));
             }
+            // every MMA this warp issued completes before tensor memory is freed
+            // (also after an abort)
             mma_commit_warp(bar(B_DRAIN));
-            mbar_wait_warp(bar(B_DRAIN), 0, w);
+            mbar_wait_drain_warp(bar(B_DRAIN), 0, p.err, p.budget_ns);
         } else if (warp == C::W_MMA_B) {
             // ---------------------------------------- MMA warp B: dV, dK and dQ
             // For step j (S buffer j%3, dS^T tile j%2): dV += P^T dO once P^T is
@@ -547,7 +561,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 mma_commit_warp(bar(B_KV_EMPTY));
             }
             mma_commit_warp(bar(B_DRAIN));
-            mbar_wait_warp(bar(B_DRAIN), 0, w);
+            mbar_wait_drain_warp(bar(B_DRAIN), 0, p.err, p.budget_ns);
         } else if (warp == C::W_ISSUE && C::kBulk) {
             // ------------------------------------------------ bulk-reduce issuer
             // One thread adds every dQ chunk to the fp32 accumulator.  Step j's

@@ -13,10 +13,13 @@
 namespace fa {
 
 // ------------------------------------------------------------------ errors
-// Device error word bits (the host maps any non-zero value to FA_ERR_TIMEOUT).
+// Device error word bits (the host reports kErrBadLength as FA_ERR_INVALID_ARG,
+// any other non-zero value as FA_ERR_TIMEOUT).
 enum : int {
     kErrWaitTimeout = 1,       // an mbarrier wait ran out
     kErrSemaphoreTimeout = 2,  // a deterministic-order semaphore wait ran out
+    kErrBadLength = 4,         // a varlen sequence longer than the maximum given, or
+                               // cu_seqlens[B] different from the packed total given
 };
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
@@ -71,8 +74,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded slow path of mbar_wait, kept out of line so the common case (the
-// phase has already completed) costs one try_wait and a branch.
 // Packed fp32 pairs (two lanes of one 64-bit register): the f32x2 forms of
 // fma / sub / mul issue one instruction per pair, each lane rounded as the
 // scalar instruction would be.
@@ -128,6 +129,8 @@ __device__ __forceinline__ float2 ld_shared_f32x2(uint32_t addr) {
     return v;
 }
 
+// Bounded slow path of mbar_wait, kept out of line so the common case (the
+// phase has already completed) costs one try_wait and a branch.
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                             int *err, long long budget_ns) {
     const uint64_t t0 = globaltimer_ns();
@@ -138,6 +141,24 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
         if (*abort_flag) return false;
         if ((long long)(globaltimer_ns() - t0) > budget_ns) {
             *abort_flag = 1;
+            atomicOr(err, kErrWaitTimeout);
+            return false;
+        }
+    }
+}
+// Wind-down wait: the phase with the given parity of a barrier that tracks
+// this CTA's own asynchronous work (MMAs, TMA loads) already issued.  Unlike
+// mbar_wait it does not give up when the CTA aborts -- that work must finish
+// before tensor memory is freed or the CTA exits -- but it is still bounded
+// by the budget (then it raises the error and returns false).
+static __device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, int *err,
+                                                    long long budget_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if ((long long)(globaltimer_ns() - t0) > budget_ns) {
             atomicOr(err, kErrWaitTimeout);
             return false;
         }
@@ -313,6 +334,15 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, co
     int ok = 1;
     if ((threadIdx.x & 31) == 0)
         ok = mbar_wait_slow(bar, parity, w.abort_flag, w.err, w.budget_ns) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// mbar_wait_drain for a whole converged warp (lane 0 waits, the outcome is
+// broadcast).
+__device__ __forceinline__ bool mbar_wait_drain_warp(uint32_t bar, uint32_t parity, int *err,
+                                                     long long budget_ns) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait_drain(bar, parity, err, budget_ns) ? 1 : 0;
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 

@@ -123,6 +123,12 @@ __global__ void __launch_bounds__(SplitCfg<kD, T>::kThreads, 1)
     const int bh = blockIdx.x % (p.B * p.Hq);
     const int m = nmb - 1 - blockIdx.x / (p.B * p.Hq);
     const int b = bh / p.Hq, h = bh - b * p.Hq, hk = h / p.G;
+    // varlen lengths outside the planned maps: the sequence is left alone and
+    // the call reports the error (uniform: the whole CTA leaves)
+    if (p.varlen && !varlen_seq_ok(p, b)) {
+        if (threadIdx.x == 0 && h == 0 && m == nmb - 1) atomicOr(p.err, kErrBadLength);
+        return;
+    }
     const int q0 = p.varlen ? p.cu_q[b] : 0, k0 = p.varlen ? p.cu_k[b] : 0;
     const int lq = used_len_q(p, b), lk = used_len_k(p, b);
     if (m * BM >= lq) return;                       // uniform: the whole CTA leaves
@@ -192,6 +198,7 @@ __global__ void __launch_bounds__(SplitCfg<kD, T>::kThreads, 1)
                 tma_load_4d(sbase + C::OFF_Q + hh * BM * 128, &map_q, bar(F_Q_FULL), hh * 64, h,
                             q0 + m * BM, bidx);
             uint32_t k_ph = 0, v_ph = 0;   // empty-barrier phase bit of each slot
+            int k_armed = -1, v_armed = -1;  // the last block whose K / V load was issued
             auto load = [&](int j, bool is_k) -> bool {
                 const int st = j % S;
                 if (j >= S) {
@@ -202,6 +209,7 @@ __global__ void __launch_bounds__(SplitCfg<kD, T>::kThreads, 1)
                 }
                 const uint32_t full = bar(is_k ? C::k_full(st) : C::v_full(st));
                 mbar_arrive_expect_tx(full, C::KV_BYTES);
+                (is_k ? k_armed : v_armed) = j;
                 const uint32_t dst = sbase + (is_k ? C::OFF_K : C::OFF_V) + st * C::KV_BYTES;
 #pragma unroll
                 for (int hh = 0; hh < D / 64; ++hh)
@@ -212,6 +220,20 @@ __global__ void __launch_bounds__(SplitCfg<kD, T>::kThreads, 1)
             for (int j = 0; j < nblk + NB - 1; ++j) {
                 if (j < nblk && !load(j, true)) break;
                 if (j >= NB - 1 && !load(j - (NB - 1), false)) break;
+            }
+            // wind-down: no K/V load may land after the CTA exits (after an
+            // abort its consumers may not have waited for it).  The Q load needs
+            // no wait here: it is issued first, and the MMA warp waits for it
+            // with the whole budget before any wait can run out.
+            for (int st = 0; st < S; ++st) {
+                if (st <= k_armed) {
+                    const int jl = k_armed - ((k_armed - st) % S);   // last K block in slot st
+                    mbar_wait_drain(bar(C::k_full(st)), (uint32_t)(jl / S) & 1u, p.err, p.budget_ns);
+                }
+                if (st <= v_armed) {
+                    const int jl = v_armed - ((v_armed - st) % S);
+                    mbar_wait_drain(bar(C::v_full(st)), (uint32_t)(jl / S) & 1u, p.err, p.budget_ns);
+                }
             }
         }
     } else if (warp == 1) {
@@ -270,7 +292,7 @@ __global__ void __launch_bounds__(SplitCfg<kD, T>::kThreads, 1)
             if (ok) mma_commit_warp(bar(C::O_FINAL));
             // make sure no MMA is still running before tensor memory is freed
             mma_commit_warp(bar(F_Q_FULL));
-            mbar_wait_warp(bar(F_Q_FULL), 1, w);
+            mbar_wait_drain_warp(bar(F_Q_FULL), 1, p.err, p.budget_ns);
         }
     } else if (warp >= C::W_SM) {
         // ------------------------------------------------------------- softmax

@@ -89,6 +89,12 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
     const int bh = blockIdx.x % (p.B * p.Hq);
     const int m = nmb - 1 - blockIdx.x / (p.B * p.Hq);
     const int b = bh / p.Hq, h = bh - b * p.Hq, hk = h / p.G;
+    // varlen lengths outside the planned maps: the sequence is left alone and
+    // the call reports the error (uniform: the whole CTA leaves)
+    if (p.varlen && !varlen_seq_ok(p, b)) {
+        if (threadIdx.x == 0 && h == 0 && m == nmb - 1) atomicOr(p.err, kErrBadLength);
+        return;
+    }
     const int q0 = p.varlen ? p.cu_q[b] : 0, k0 = p.varlen ? p.cu_k[b] : 0;
     const int lq = used_len_q(p, b), lk = used_len_k(p, b);
     if (m * BM >= lq) return;                       // uniform: the whole CTA leaves
@@ -150,6 +156,7 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                 tma_load_4d(sbase + C::OFF_Q + hh * BM * 128, &map_q, bar(F_Q_FULL), hh * 64, h,
                             q0 + m * BM, bidx);
             uint32_t empty_ph = 0;
+            int armed = -1;   // the last block whose K/V load was issued
             for (int n = 0; n < nblk; ++n) {
                 const int st = n % S;
                 if (n >= S) {
@@ -158,6 +165,7 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                 }
                 const uint32_t full = bar(F_KV_FULL + st);
                 mbar_arrive_expect_tx(full, 2 * C::KV_BYTES);
+                armed = n;
 #pragma unroll
                 for (int hh = 0; hh < D / 64; ++hh) {
                     tma_load_4d(sbase + C::OFF_K + st * C::KV_BYTES + hh * BN * 128, &map_k, full,
@@ -165,6 +173,14 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                     tma_load_4d(sbase + C::OFF_V + st * C::KV_BYTES + hh * BN * 128, &map_v, full,
                                 hh * 64, hk, k0 + (n_begin + n) * BN, bidx);
                 }
+            }
+            // wind-down: no K/V load may land after the CTA exits (after an
+            // abort its consumers may not have waited for it).  The Q load needs
+            // no wait here: it is issued first, and the MMA warp waits for it
+            // with the whole budget before any wait can run out.
+            for (int st = 0; st < S && st <= armed; ++st) {
+                const int nl = armed - ((armed - st) % S);   // last block loaded into slot st
+                mbar_wait_drain(bar(F_KV_FULL + st), (uint32_t)(nl / S) & 1u, p.err, p.budget_ns);
             }
         }
     } else if (warp == 1) {
@@ -212,7 +228,7 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
             if (ok && issue_pv(nblk - 1)) mma_commit_warp(bar(F_O_FINAL));
             // make sure no MMA is still running before tensor memory is freed
             mma_commit_warp(bar(F_Q_FULL));
-            mbar_wait_warp(bar(F_Q_FULL), 1, w);
+            mbar_wait_drain_warp(bar(F_Q_FULL), 1, p.err, p.budget_ns);
         }
     } else if (warp >= C::W_SM) {
         // ------------------------------------------------------------- softmax

@@ -29,7 +29,15 @@ __global__ void __launch_bounds__(1024) schedule_kernel(BwdParams p) {
         for (int b0 = 0; b0 < p.B; b0 += 1024) {
             const int b = b0 + tid;
             int flag = 0;
-            if (b < p.B) flag = seq_len_k(p, b) > n * kBlockN;
+            if (b < p.B) {
+                // a sequence whose lengths break the planned layout gets no unit
+                // (and the call reports the error)
+                if (p.varlen && !varlen_seq_ok(p, b)) {
+                    if (n == 0) atomicOr(p.err, kErrBadLength);
+                } else {
+                    flag = seq_len_k(p, b) > n * kBlockN;
+                }
+            }
             // block-wide exclusive scan of flag
             int x = flag;
 #pragma unroll
@@ -82,6 +90,9 @@ __global__ void __launch_bounds__(256) preprocess_kernel(BwdParams p) {
         p.unit_counter[0] = 0;   // the main kernel's dynamic work-unit counter ...
         p.unit_counter[1] = 0;   // ... and its count of CTAs that ran out of units
     }
+    // varlen lengths outside the planned layout: nothing of this sequence is
+    // touched (the scheduler reports the error)
+    if (p.varlen && !varlen_seq_ok(p, b)) return;
     const int lq = seq_len_q(p, b);
     const int lq_round = (lq + kRowTile - 1) / kRowTile * kRowTile;
     const long long nrows = (long long)lq_round * p.Hq;   // (position, head) rows, padded
@@ -150,6 +161,7 @@ template <int D, typename T, int RPT>
 __global__ void __launch_bounds__(256) postprocess_kernel(BwdParams p) {
     constexpr int TPR = D / 8;
     const int b = blockIdx.y;
+    if (p.varlen && !varlen_seq_ok(p, b)) return;
     const int lq = seq_len_q(p, b);
     const long long nrows = (long long)lq * p.Hq;
     if ((long long)blockIdx.x * (blockDim.x / TPR) * RPT >= nrows) return;

@@ -23,13 +23,14 @@ std::mutex g_setup_mutex;
 void *g_scratch_addr[kMaxDevices] = {};
 
 // Device address of g_scratch on the current device; looked up on the first
-// call for that device.
-fa_status scratch_address(void **out) {
+// call for that device (lookup = false: only what an earlier call found,
+// possibly null).
+fa_status scratch_address(void **out, bool lookup = true) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lk(g_setup_mutex);
-    if (!g_scratch_addr[dev]) {
+    if (!g_scratch_addr[dev] && lookup) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr)
             return FA_ERR_CUDA;
@@ -65,6 +66,25 @@ fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v, const void
     return fa_bwd_with_workspace(q, k, v, o, dout, lse, dq, dk, dv, B, Sq, Sk, Hq, Hkv, D,
                                  softmax_scale, causal, cu_seqlens_q, cu_seqlens_k, deterministic,
                                  dtype, scratch, (size_t)FA_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+fa_status fa_bwd_noalloc_status(cudaStream_t stream) {
+    void *scratch = nullptr;
+    fa_status st = scratch_address(&scratch, false);
+    if (st != FA_OK) return st;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+    if (!scratch) return FA_OK;   // no call has used the array on this device
+    // the error word sits at the start of the backward's workspace layout
+    size_t err_off = 0;
+    int h = 0;
+    if (cudaMemcpy(&h, static_cast<unsigned char *>(scratch) + err_off, sizeof(int),
+                   cudaMemcpyDeviceToHost) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (h != 0 && cudaMemset(static_cast<unsigned char *>(scratch) + err_off, 0, sizeof(int)) !=
+                      cudaSuccess)
+        return FA_ERR_CUDA;
+    if (h & 4) return FA_ERR_INVALID_ARG;   // a varlen length out of bounds
+    return h ? FA_ERR_TIMEOUT : FA_OK;
 }
 
 }  // extern "C"

@@ -22,6 +22,9 @@ struct BwdParams {
     float scale_log2;   // c * log2(e)
     int causal, deterministic, varlen;
     const int *cu_q, *cu_k;
+    // varlen: the packed row counts the tensor maps were built for; the
+    // kernels check them against cu_q[B] / cu_k[B] before touching a row
+    long long total_q, total_k;
     // Visible band: key j is visible to query i iff j < Lk and
     // -win_lo <= j - i - (Lk - Lq) <= win_hi (kNoWindow: unbounded; a causal
     // mask makes win_hi <= 0).
@@ -72,6 +75,16 @@ struct BwdParams {
     int sq_round;       // round_up(Sq, 128)
     long long budget_ns;      // bound of every device-side wait
 };
+
+// Varlen: cu_seqlens agree with the packed totals and with the maximum
+// lengths the workspace was planned for (Sq / Sk), for sequence b.  A call
+// where this fails reports kErrBadLength, and no kernel touches the
+// sequence's rows.
+__device__ __forceinline__ bool varlen_seq_ok(const BwdParams &p, int b) {
+    if (p.cu_q[p.B] != p.total_q || p.cu_k[p.B] != p.total_k) return false;
+    const int lq = p.cu_q[b + 1] - p.cu_q[b], lk = p.cu_k[b + 1] - p.cu_k[b];
+    return lq >= 0 && lk >= 0 && lq <= p.Sq && lk <= p.Sk;
+}
 
 // Rows of sequence b the attention uses (query / key side).
 __device__ __forceinline__ int used_len_q(const BwdParams &p, int b) {

@@ -31,7 +31,12 @@
  *   zeros (the FlashAttention postprocess page pads the head dim likewise).
  *   varlen: cu_seqlens_q / cu_seqlens_k != NULL (both or neither): int32
  *           device arrays of B+1 prefix sums; tensors packed [total, H, D];
- *           lse fp32 [Hq, total_q]; Sq / Sk are the MAXIMUM lengths.
+ *           lse fp32 [Hq, total_q]; Sq / Sk are the MAXIMUM lengths.  A
+ *           sequence longer than Sq / Sk, or packed totals above B * Sq /
+ *           B * Sk, make the call fail with FA_ERR_INVALID_ARG: the totals
+ *           are checked on the host before any launch, each sequence on the
+ *           device (no row of an offending sequence is read or written, and
+ *           the error is reported through the device error word).
  * Causal masking is bottom-right aligned: key j is visible to query i iff
  * j <= i + (Lk - Lq).
  *
@@ -44,9 +49,13 @@
  *
  * Errors: arguments are validated before any launch (FA_ERR_INVALID_ARG,
  * FA_ERR_UNSUPPORTED); a failed launch returns FA_ERR_CUDA.  Otherwise the
- * call is asynchronous.  Every wait inside the kernels is bounded; a wait
- * that runs out records FA_ERR_TIMEOUT in a device word that
- * fa_device_status() reads (deterministic mode reads it before returning).
+ * call is asynchronous, except that deterministic calls, and varlen calls
+ * whose packed totals are not given (fa_ext total_q / total_k), synchronise
+ * `stream` before returning.  Every wait inside the kernels is bounded; a
+ * wait that runs out records FA_ERR_TIMEOUT in a device word that
+ * fa_device_status() reads (deterministic mode reads it before returning),
+ * and so does a varlen length the device finds out of bounds
+ * (FA_ERR_INVALID_ARG).
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -130,6 +139,20 @@ fa_status fa_bwd_workspace_layout(int B, int Sq, int Sk, int Hq, int Hkv, int D,
                                   int deterministic, size_t *dvec_off, size_t *lse2_off,
                                   size_t *dqacc_off, size_t *rows);
 
+/* Where a workspace keeps its synchronisation state, in bytes from the
+ * workspace base: the device error word (*err_off; int32, 0 while no error
+ * was recorded), and in deterministic mode the ordering semaphores (*sem_off,
+ * *n_sem int32 entries, one per 64 workspace rows: the row block at
+ * workspace rows [64 i, 64 i + 64) has entry i, which counts the key blocks
+ * whose dQ contributions to that row block have been added -- the
+ * arrive_inc / wait_eq counters of CollectiveEpilogueBwdGQA on the
+ * FlashAttention page "flash-attention/hopper/epilogue_bwd.hpp").  Without
+ * deterministic mode *sem_off and *n_sem are 0.  The preprocess stage
+ * zeroes both; this call exists for tests and tools that inspect them. */
+fa_status fa_bwd_workspace_sync_layout(int B, int Sq, int Sk, int Hq, int Hkv, int D, int varlen,
+                                       int deterministic, size_t *err_off, size_t *sem_off,
+                                       size_t *n_sem);
+
 /* Forward pass O = softmax(Q K^T * scale + mask) V with LSE (natural log,
  * -inf for a query row that sees no key; such rows get O = 0): the inputs
  * fa_bwd consumes, same layouts and masking.  One tcgen05 kernel per call
@@ -194,6 +217,15 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
  *   reads them instead of running Philox again (in deterministic mode the
  *   results are bit-identical to drawing the mask).  The buffer must hold
  *   B * Hq * Sq * W words (Hq * total_q * W with cu_seqlens). */
+/* total_q / total_k (varlen only; both 0 = not given): the packed row counts
+ *   cu_seqlens_q[B] and cu_seqlens_k[B], which the tensor maps are built
+ *   for.  Given, the call needs no read-back of cu_seqlens and does not
+ *   synchronise the stream.  They must equal cu_seqlens[B] and be at most
+ *   B * Sq / B * Sk; the device checks the first and reports a mismatch as
+ *   FA_ERR_INVALID_ARG through the error word, without reading or writing
+ *   any row of the offending sequences.  The tensors must hold at least
+ *   that many rows: a count larger than the rows allocated lets the tiled
+ *   loads of the last rows run past the end of the tensors. */
 typedef struct {
     int window_left;
     int window_right;
@@ -210,6 +242,8 @@ typedef struct {
     unsigned long long dropout_seed;
     unsigned int dropout_offset;
     unsigned int *dropout_mask;
+    long long total_q;
+    long long total_k;
 } fa_ext;
 
 /* fa_fwd with extensions.  Errors as fa_fwd, plus FA_ERR_INVALID_ARG for a
@@ -259,12 +293,20 @@ const char *fa_status_string(fa_status s);
  *     larger than FA_NOALLOC_SCRATCH_BYTES are rejected with
  *     FA_ERR_SCRATCH_LIMIT before anything runs.
  *   - The first call on a device looks up the array's device address (with
- *     that device current) and remembers it; make that first call before any
- *     stream capture.
+ *     that device current) and remembers it for the life of the process;
+ *     make that first call before any stream capture.  The remembered
+ *     address does not survive cudaDeviceReset: do not call fa_bwd_noalloc
+ *     again on a device after resetting it.
  *   - Every call shares the one array and leaves its contents behind; each
  *     call re-initialises what must start at zero, so no clearing is needed
  *     between calls, but calls that overlap on the GPU (other streams, other
  *     host threads) race on the array and must be serialised by the caller.
+ *   - Deterministic calls, and varlen calls (their packed totals are read
+ *     back from cu_seqlens), synchronise `stream` before returning, as
+ *     fa_bwd does.
+ *   - Device-side errors (a bounded wait that ran out, a varlen length out
+ *     of bounds) are recorded in the array's own error word, which
+ *     fa_bwd_noalloc_status reads; fa_device_status does not see it.
  * ------------------------------------------------------------------------- */
 #define FA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 
@@ -276,6 +318,13 @@ fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v, const void
                          int Sq, int Sk, int Hq, int Hkv, int D, float softmax_scale, int causal,
                          const int *cu_seqlens_q, const int *cu_seqlens_k, int deterministic,
                          fa_dtype dtype, cudaStream_t stream);
+
+/* Synchronises `stream`, then returns and clears the device error word of
+ * the fixed scratch array on the current device: FA_OK, FA_ERR_TIMEOUT (a
+ * bounded wait ran out) or FA_ERR_INVALID_ARG (a varlen sequence longer than
+ * the maximum given).  Allocates nothing either; before the first
+ * fa_bwd_noalloc on the device it returns FA_OK. */
+fa_status fa_bwd_noalloc_status(cudaStream_t stream);
 
 #ifdef __cplusplus
 }

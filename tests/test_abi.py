@@ -181,7 +181,7 @@ EXT_BAD = [
 
 
 def _fa_ext(fa, over):
-    e = fa.FaExt(-1, -1, None, 0, None, None, None, 0, 0, 0, None, 0.0, 0, 0, None)
+    e = fa.FaExt(-1, -1, None, 0, None, None, None, 0, 0, 0, None, 0.0, 0, 0, None, 0, 0)
     for name, val in over.items():
         setattr(e, name, val)
     return e
@@ -197,6 +197,49 @@ def test_extension_arguments_rejected_on_the_host(fa, over, status):
     assert L.fa_fwd_ext(*ptrs[:5], *shape, 0.125, 1, None, None, ctypes.byref(e), 0, None) == status
     assert L.fa_bwd_ext(*ptrs, *shape, 0.125, 1, None, None, ctypes.byref(e), 0, 0,
                         vp(0x100000), ctypes.c_size_t(1 << 40), None) == status
+
+
+# packed totals given by the caller: varlen only, both positive, at most B * max
+TOTALS_BAD = [
+    (dict(total_q=100, total_k=100), False),          # a dense call
+    (dict(total_q=100, total_k=0), True),             # one of the two missing
+    (dict(total_q=-1, total_k=100), True),
+    (dict(total_q=2 * 128 + 1, total_k=100), True),   # above B * Sq
+    (dict(total_q=100, total_k=2 * 128 + 1), True),   # above B * Sk
+]
+
+
+@pytest.mark.parametrize("over,varlen", TOTALS_BAD, ids=[str(i) for i in range(len(TOTALS_BAD))])
+def test_packed_totals_rejected_on_the_host(fa, over, varlen):
+    L = fa.lib()
+    vp = ctypes.c_void_p
+    ptrs = [vp(0x1000 * (i + 1)) for i in range(9)]
+    e = _fa_ext(fa, over)
+    cu = vp(0x8000) if varlen else None
+    shape = (2, 128, 128, 2, 2, 64)
+    assert L.fa_fwd_ext(*ptrs[:5], *shape, 0.125, 1, cu, cu, ctypes.byref(e), 0, None) == 1
+    assert L.fa_bwd_ext(*ptrs, *shape, 0.125, 1, cu, cu, ctypes.byref(e), 0, 0,
+                        vp(0x100000), ctypes.c_size_t(1 << 40), None) == 1
+
+
+@pytest.mark.parametrize("varlen", [False, True])
+@pytest.mark.parametrize("det", [False, True])
+def test_workspace_sync_layout(fa, varlen, det):
+    """The error word opens the workspace; the semaphores (deterministic only)
+    are one int32 per 64 workspace rows and lie inside the workspace, after
+    the dQ accumulator."""
+    shape = (3, 200, 300, 4, 2, 96)
+    sync = fa.workspace_sync_layout(*shape, varlen=varlen, deterministic=det)
+    lay = fa.workspace_layout(*shape, varlen=varlen, deterministic=det)
+    total = fa.workspace_bytes(*shape, varlen=varlen, deterministic=det)
+    assert sync["err"] == 0
+    if det:
+        assert sync["n_sem"] == lay["rows"] // 64
+        assert sync["sem"] >= 4 * (lay["dqacc"] + lay["rows"] * 128)
+        assert sync["sem"] % 4 == 0
+        assert sync["sem"] + 4 * sync["n_sem"] <= total
+    else:
+        assert sync["sem"] == 0 and sync["n_sem"] == 0
 
 
 def test_bias_with_varlen_is_unsupported(fa):
