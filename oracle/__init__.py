@@ -9,10 +9,13 @@ optionally OpenMP).  The C source documents the mathematics and where each
 step is stated on the pages; all arrays here are float64 numpy arrays in the
 public layouts:
 
-* dense : q, o, dout, dq ``[B, Sq, Hq, D]``; k, v, dk, dv ``[B, Sk, Hkv, D]``;
-  lse ``[B, Hq, Sq]``
+* dense : q, dq ``[B, Sq, Hq, D]``; k, dk ``[B, Sk, Hkv, D]``; o, dout
+  ``[B, Sq, Hq, Dv]``; v, dv ``[B, Sk, Hkv, Dv]``; lse ``[B, Hq, Sq]``
 * varlen: ``cu_q`` / ``cu_k`` int32 prefix sums of the ``nseq`` lengths;
-  q ``[total_q, Hq, D]``; k ``[total_k, Hkv, D]``; lse ``[Hq, total_q]``
+  q ``[total_q, Hq, D]``; k ``[total_k, Hkv, D]`` (o, dout, v likewise with
+  Dv); lse ``[Hq, total_q]``
+
+The value-side head dim Dv is v's last axis; it may differ from D.
 
 Every function also takes the optional extensions as keywords:
 ``window=(left, right)`` (a local band around the bottom-right diagonal, -1 =
@@ -84,22 +87,24 @@ class _Ext(ctypes.Structure):
                 ("bias", ctypes.POINTER(ctypes.c_double)), ("bias_bs", ctypes.c_long),
                 ("bias_hs", ctypes.c_long), ("bias_rs", ctypes.c_long),
                 ("dropout_t", ctypes.c_int), ("dropout_seed", ctypes.c_ulonglong),
-                ("dropout_offset", ctypes.c_uint)]
+                ("dropout_offset", ctypes.c_uint), ("head_dim_v", ctypes.c_int)]
 
 
 def _ext(B, Hq, window=None, alibi=None, seqused_q=None, seqused_k=None, bias=None,
-         dropout=None):
+         dropout=None, head_dim_v=0):
     """(ctypes pointer or None, arrays to keep alive) for the extension options.
 
     ``bias`` is a [B or 1, Hq or 1, Sq, Sk] array (dense problems); a size-1
     batch or head axis is broadcast.  ``dropout`` is (t, seed, offset): drop
-    probability t / 256, the Philox key and the counter's fourth word."""
+    probability t / 256, the Philox key and the counter's fourth word.
+    ``head_dim_v``: the value-side head dim when it differs from D (else 0)."""
     if (window is None and alibi is None and seqused_q is None and seqused_k is None
-            and bias is None and dropout is None):
+            and bias is None and dropout is None and not head_dim_v):
         return None, ()
     wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
     keep = []
     e = _Ext(wl, wr, None, 0, None, None)
+    e.head_dim_v = int(head_dim_v)
     if dropout is not None:
         e.dropout_t, e.dropout_seed, e.dropout_offset = (int(dropout[0]), int(dropout[1]),
                                                          int(dropout[2]))
@@ -148,6 +153,11 @@ def _shape_args(q, k, scale, causal, cu_q, cu_k):
     args = [B, Sq, Sk, Hq, Hkv, D, float(scale), int(bool(causal)),
             _ptr(cq, ctypes.c_int), _ptr(ck, ctypes.c_int)]
     return args, (cq, ck), (B, Sq, Sk, Hq, Hkv, D)
+
+
+def _dv(D, Dv):
+    """head_dim_v for the C side: 0 when the value head dim equals D."""
+    return 0 if int(Dv) == int(D) else int(Dv)
 
 
 class Oracle:
@@ -214,8 +224,9 @@ class Oracle:
         """Returns (o, lse) in fp64; lse is natural-log, -inf for a row with no key."""
         q, k, v = _f64(q), _f64(k), _f64(v)
         args, keep, (B, Sq, Sk, Hq, Hkv, D) = _shape_args(q, k, scale, causal, cu_q, cu_k)
-        e, keep_e = _ext(B, Hq, **ext)
-        o = np.zeros_like(q)
+        Dv = v.shape[-1]
+        e, keep_e = _ext(B, Hq, head_dim_v=_dv(D, Dv), **ext)
+        o = np.zeros(q.shape[:-1] + (Dv,))
         lse = np.zeros((B, Hq, Sq) if cu_q is None else (Hq, q.shape[0]), dtype=np.float64)
         rc = self.lib.oracle_forward(_ptr(q), _ptr(k), _ptr(v), *args, _ptr(o), _ptr(lse),
                                      self._threads(nthreads), e)
@@ -228,7 +239,8 @@ class Oracle:
         """Returns (dq, dk, dv) in fp64.  o / lse None -> the oracle's own fp64 forward."""
         q, k, v, dout, o, lse = map(_f64, (q, k, v, dout, o, lse))
         args, keep, (B, Sq, Sk, Hq, Hkv, D) = _shape_args(q, k, scale, causal, cu_q, cu_k)
-        e, keep_e = _ext(B, Hq, **ext)
+        Dv = v.shape[-1]
+        e, keep_e = _ext(B, Hq, head_dim_v=_dv(D, Dv), **ext)
         dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
         rc = self.lib.oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                       _ptr(dout), *args, _ptr(dq), _ptr(dk), _ptr(dv),
@@ -245,12 +257,13 @@ class Oracle:
         """
         q, k, v, dout, o, lse = map(_f64, (q, k, v, dout, o, lse))
         args, keep, (B, Sq, Sk, Hq, Hkv, D) = _shape_args(q, k, scale, causal, cu_q, cu_k)
-        e, keep_e = _ext(B, Hq, **ext)
+        Dv = v.shape[-1]
+        e, keep_e = _ext(B, Hq, head_dim_v=_dv(D, Dv), **ext)
         qr = np.ascontiguousarray(np.asarray(qrows, dtype=np.int32).reshape(-1, 3))
         kr = np.ascontiguousarray(np.asarray(krows, dtype=np.int32).reshape(-1, 3))
         dq = np.zeros((len(qr), D))
         dk = np.zeros((len(kr), D))
-        dv = np.zeros((len(kr), D))
+        dv = np.zeros((len(kr), Dv))
         rc = self.lib.oracle_backward_sampled(
             _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), *args,
             len(qr), _ptr(qr, ctypes.c_int), _ptr(dq), len(kr), _ptr(kr, ctypes.c_int),
@@ -264,7 +277,8 @@ class Oracle:
         """(Dv, LSE_guarded) per query row, in lse's layout: Dv_i = <dO_i, O_i>."""
         q, k, v, dout, o, lse = map(_f64, (q, k, v, dout, o, lse))
         args, keep, (B, Sq, Sk, Hq, Hkv, D) = _shape_args(q, k, scale, causal, cu_q, cu_k)
-        e, keep_e = _ext(B, Hq, **ext)
+        Dv = v.shape[-1]
+        e, keep_e = _ext(B, Hq, head_dim_v=_dv(D, Dv), **ext)
         shape = (B, Hq, Sq) if cu_q is None else (Hq, q.shape[0])
         dvec = np.zeros(shape)
         lse_out = np.zeros(shape)
@@ -280,7 +294,8 @@ class Oracle:
         """Dense P and dS [Lq, Lk] of one (sequence, query head) problem (tiny inputs)."""
         q, k, v, dout, o, lse = map(_f64, (q, k, v, dout, o, lse))
         args, keep, (B, Sq, Sk, Hq, Hkv, D) = _shape_args(q, k, scale, causal, cu_q, cu_k)
-        e, keep_e = _ext(B, Hq, **ext)
+        Dv = v.shape[-1]
+        e, keep_e = _ext(B, Hq, head_dim_v=_dv(D, Dv), **ext)
         if cu_q is None:
             lq, lk = Sq, Sk
         else:

@@ -63,11 +63,18 @@
  * rounded values, as the GPU sees them) or, when those pointers are NULL,
  * computes them itself in fp64 ("fully fp64" variant).
  *
+ * Head dims: D for the query / key side (q, k, dq, dk) and Dv for the value
+ * side (v, o, dout, dv); Dv = D unless given (the Composable Kernel page's
+ * problem traits carry the two as kQKHeaddim and kVHeaddim).  Every dot
+ * product above runs over its own side's dim: <q_i, k_j> over D, <dO_i, v_j>
+ * and <dO_i, O_i> over Dv.
+ *
  * Layouts (row-major, d innermost, like the GPU path's public layout):
- *   dense : q, o, dout, dq [B, Sq, Hq, D];  k, v, dk, dv [B, Sk, Hkv, D];
- *           lse [B, Hq, Sq]
+ *   dense : q, dq [B, Sq, Hq, D];  o, dout [B, Sq, Hq, Dv];
+ *           k, dk [B, Sk, Hkv, D];  v, dv [B, Sk, Hkv, Dv];  lse [B, Hq, Sq]
  *   varlen: cu_q / cu_k give prefix sums of nseq = B lengths;
- *           q [total_q, Hq, D]; k [total_k, Hkv, D]; lse [Hq, total_q]
+ *           q [total_q, Hq, D]; k [total_k, Hkv, D] (v, o, dout likewise with
+ *           Dv); lse [Hq, total_q]
  *
  * Everything is a plain loop over the definition above.  Parallelism is over
  * independent output rows only (no reductions across threads), so results do
@@ -91,11 +98,12 @@ typedef struct {
     int dropout_t;                  /* threshold byte t in [0, 255]; 0: no dropout */
     unsigned long long dropout_seed;
     unsigned int dropout_offset;
+    int head_dim_v;                 /* Dv, the value-side head dim; 0: equal to D */
 } oracle_ext_t;
 
 typedef struct {
     const double *q, *k, *v, *o, *dout, *lse;
-    int B, Sq, Sk, Hq, Hkv, D, G;
+    int B, Sq, Sk, Hq, Hkv, D, Dv, G;
     double scale;
     int causal;
     const int *cu_q, *cu_k;
@@ -117,7 +125,9 @@ static int seq_len_q(const prob_t *p, int b) {
 static int seq_len_k(const prob_t *p, int b) {
     return p->ext.seqused_k ? p->ext.seqused_k[b] : stored_len_k(p, b);
 }
-/* index of the (b, s, head) row in a [.., S, H, D] or packed [total, H, D] tensor */
+/* index of the (b, s, head) row in a [.., S, H, D] or packed [total, H, D]
+ * tensor: q / dq (row_q), k / dk (row_k), o / dout (row_o, Dv wide), v / dv
+ * (row_v, Dv wide) */
 static long row_q(const prob_t *p, int b, int s, int h) {
     long base = p->cu_q ? (long)p->cu_q[b] + s : (long)b * p->Sq + s;
     return (base * p->Hq + h) * p->D;
@@ -125,6 +135,14 @@ static long row_q(const prob_t *p, int b, int s, int h) {
 static long row_k(const prob_t *p, int b, int s, int hk) {
     long base = p->cu_k ? (long)p->cu_k[b] + s : (long)b * p->Sk + s;
     return (base * p->Hkv + hk) * p->D;
+}
+static long row_o(const prob_t *p, int b, int s, int h) {
+    long base = p->cu_q ? (long)p->cu_q[b] + s : (long)b * p->Sq + s;
+    return (base * p->Hq + h) * p->Dv;
+}
+static long row_v(const prob_t *p, int b, int s, int hk) {
+    long base = p->cu_k ? (long)p->cu_k[b] + s : (long)b * p->Sk + s;
+    return (base * p->Hkv + hk) * p->Dv;
 }
 static long lse_index(const prob_t *p, int b, int s, int h) {
     if (p->cu_q) return (long)h * p->total_q + p->cu_q[b] + s;
@@ -197,14 +215,14 @@ static double score(const prob_t *p, int b, int h, int i, int j) {
  * not NULL, O_i = sum_j P_ij v_j.  The row's scores are computed once into a
  * scratch row; the max shift is for range safety only. */
 static double row_forward(const prob_t *p, int b, int h, int i, double *o_out) {
-    int lk = seq_len_k(p, b), hk = h / p->G, D = p->D;
+    int lk = seq_len_k(p, b), hk = h / p->G, Dv = p->Dv;
     double *s = (double *)malloc(sizeof(double) * (lk > 0 ? lk : 1));
     double m = -INFINITY;
     for (int j = 0; j < lk; ++j) {
         s[j] = visible(p, b, i, j) ? score(p, b, h, i, j) : -INFINITY;
         if (s[j] > m) m = s[j];
     }
-    if (o_out) for (int d = 0; d < D; ++d) o_out[d] = 0.0;
+    if (o_out) for (int d = 0; d < Dv; ++d) o_out[d] = 0.0;
     if (m == -INFINITY) { /* no visible key */
         free(s);
         return -INFINITY;
@@ -217,9 +235,9 @@ static double row_forward(const prob_t *p, int b, int h, int i, double *o_out) {
         for (int j = 0; j < lk; ++j)
             if (s[j] != -INFINITY) {
                 double pij = exp(s[j] - lse);
-                const double *vj = p->v + row_k(p, b, j, hk);
+                const double *vj = p->v + row_v(p, b, j, hk);
                 double f = dropout_factor(p, b, h, i, j);
-                for (int d = 0; d < D; ++d) o_out[d] += pij * f * vj[d];
+                for (int d = 0; d < Dv; ++d) o_out[d] += pij * f * vj[d];
             }
     }
     free(s);
@@ -235,10 +253,10 @@ static double row_lse_for_backward(const prob_t *p, int b, int h, int i, double 
 
 /* Dv_i = <dO_i, O_i>, O given or recomputed in fp64. */
 static double row_dvec(const prob_t *p, int b, int h, int i, double *o_scratch) {
-    const double *doi = p->dout + row_q(p, b, i, h);
-    if (p->o) return dot(doi, p->o + row_q(p, b, i, h), p->D);
+    const double *doi = p->dout + row_o(p, b, i, h);
+    if (p->o) return dot(doi, p->o + row_o(p, b, i, h), p->Dv);
     row_forward(p, b, h, i, o_scratch);
-    return dot(doi, o_scratch, p->D);
+    return dot(doi, o_scratch, p->Dv);
 }
 
 static double prob(const prob_t *p, int b, int h, int i, int j, double lse_i) {
@@ -247,7 +265,7 @@ static double prob(const prob_t *p, int b, int h, int i, int j, double lse_i) {
 }
 static double dprob(const prob_t *p, int b, int h, int i, int j) {
     int hk = h / p->G;
-    return dot(p->dout + row_q(p, b, i, h), p->v + row_k(p, b, j, hk), p->D);
+    return dot(p->dout + row_o(p, b, i, h), p->v + row_v(p, b, j, hk), p->Dv);
 }
 
 /* dQ_i = scale * sum_j P_ij (dP_ij - Dv_i) k_j */
@@ -271,21 +289,20 @@ static void row_dq(const prob_t *p, int b, int h, int i, double *dq_out, double 
  * (already guarded) and Dv of sequence b. */
 static void col_dkdv(const prob_t *p, int b, int hk, int j, double *const *lse_g,
                      double *const *dvec_g, double *dk_out, double *dv_out) {
-    int lq = seq_len_q(p, b), D = p->D;
-    for (int d = 0; d < D; ++d) { dk_out[d] = 0.0; dv_out[d] = 0.0; }
+    int lq = seq_len_q(p, b), D = p->D, Dv = p->Dv;
+    for (int d = 0; d < D; ++d) dk_out[d] = 0.0;
+    for (int d = 0; d < Dv; ++d) dv_out[d] = 0.0;
     for (int g = 0; g < p->G; ++g) {
         int h = hk * p->G + g;
         for (int i = 0; i < lq; ++i) {
             double pij = prob(p, b, h, i, j, lse_g[g][i]);
             if (pij == 0.0) continue;
-            const double *doi = p->dout + row_q(p, b, i, h);
+            const double *doi = p->dout + row_o(p, b, i, h);
             const double *qi = p->q + row_q(p, b, i, h);
             double f = dropout_factor(p, b, h, i, j);
             double ds = pij * (f * dprob(p, b, h, i, j) - dvec_g[g][i]);
-            for (int d = 0; d < D; ++d) {
-                dv_out[d] += pij * f * doi[d];
-                dk_out[d] += ds * qi[d];
-            }
+            for (int d = 0; d < Dv; ++d) dv_out[d] += pij * f * doi[d];
+            for (int d = 0; d < D; ++d) dk_out[d] += ds * qi[d];
         }
     }
     for (int d = 0; d < D; ++d) dk_out[d] *= p->scale;
@@ -300,12 +317,12 @@ static void group_row_stats(const prob_t *p, int b, int hk, double **lse_g, doub
         double *lse = lse_g[g], *dvec = dvec_g[g];
 #pragma omp parallel for schedule(dynamic, 8) num_threads(nthreads)
         for (int i = 0; i < lq; ++i) {
-            double *scratch = (double *)malloc(sizeof(double) * p->D);
+            double *scratch = (double *)malloc(sizeof(double) * p->Dv);
             if (!p->lse && !p->o) {
                 /* own forward: LSE and O of the row from one pass */
                 double l = row_forward(p, b, h, i, scratch);
                 lse[i] = (l == -INFINITY) ? 0.0 : l; /* get_validated_lse */
-                dvec[i] = dot(p->dout + row_q(p, b, i, h), scratch, p->D);
+                dvec[i] = dot(p->dout + row_o(p, b, i, h), scratch, p->Dv);
             } else {
                 lse[i] = row_lse_for_backward(p, b, h, i, scratch);
                 dvec[i] = row_dvec(p, b, h, i, scratch);
@@ -331,6 +348,8 @@ static int make_prob(prob_t *p, const double *q, const double *k, const double *
     if (ext) p->ext = *ext;
     if (p->ext.window_left < -1 || p->ext.window_right < -1) return 1;
     if (p->ext.dropout_t < 0 || p->ext.dropout_t > 255) return 1;
+    if (p->ext.head_dim_v < 0) return 1;
+    p->Dv = p->ext.head_dim_v > 0 ? p->ext.head_dim_v : D;
     for (int b = 0; b < B; ++b) {
         if (p->ext.seqused_q &&
             (p->ext.seqused_q[b] < 0 || p->ext.seqused_q[b] > stored_len_q(p, b)))
@@ -357,13 +376,13 @@ int oracle_forward(const double *q, const double *k, const double *v, int B, int
             int lq = seq_len_q(&p, b);
 #pragma omp parallel for schedule(dynamic, 8) num_threads(nthreads)
             for (int i = 0; i < lq; ++i)
-                lse[lse_index(&p, b, i, h)] = row_forward(&p, b, h, i, o + row_q(&p, b, i, h));
+                lse[lse_index(&p, b, i, h)] = row_forward(&p, b, h, i, o + row_o(&p, b, i, h));
         }
     return 0;
 }
 
 /* Full backward.  o / lse may be NULL (then the oracle's own fp64 forward is
- * used).  dq has q's layout, dk / dv have k's layout. */
+ * used).  dq has q's layout, dk k's, dv v's. */
 int oracle_backward(const double *q, const double *k, const double *v, const double *o,
                     const double *lse, const double *dout, int B, int Sq, int Sk, int Hq,
                     int Hkv, int D, double scale, int causal, const int *cu_q, const int *cu_k,
@@ -384,7 +403,7 @@ int oracle_backward(const double *q, const double *k, const double *v, const dou
         for (int h = 0; h < Hq; ++h) {
 #pragma omp parallel for schedule(dynamic, 8) num_threads(nthreads)
             for (int i = 0; i < lq; ++i) {
-                double *scratch = (double *)malloc(sizeof(double) * D);
+                double *scratch = (double *)malloc(sizeof(double) * p.Dv);
                 row_dq(&p, b, h, i, dq + row_q(&p, b, i, h), scratch);
                 free(scratch);
             }
@@ -394,7 +413,7 @@ int oracle_backward(const double *q, const double *k, const double *v, const dou
 #pragma omp parallel for schedule(dynamic, 8) num_threads(nthreads)
             for (int j = 0; j < lk; ++j)
                 col_dkdv(&p, b, hk, j, lse_g, dvec_g, dk + row_k(&p, b, j, hk),
-                         dv + row_k(&p, b, j, hk));
+                         dv + row_v(&p, b, j, hk));
         }
         for (int g = 0; g < p.G; ++g) { free(lse_g[g]); free(dvec_g[g]); }
     }
@@ -405,8 +424,8 @@ int oracle_backward(const double *q, const double *k, const double *v, const dou
 
 /* Sampled backward: dQ for n_qrows query rows given as (b, s, h) triples, and
  * dK / dV for n_krows key rows given as (b, s, hk) triples.  Outputs are
- * packed [n, D].  Each requested row is computed exactly as in the full
- * backward. */
+ * packed [n, D] (dV rows [n, Dv]).  Each requested row is computed exactly as
+ * in the full backward. */
 int oracle_backward_sampled(const double *q, const double *k, const double *v, const double *o,
                             const double *lse, const double *dout, int B, int Sq, int Sk, int Hq,
                             int Hkv, int D, double scale, int causal, const int *cu_q,
@@ -427,7 +446,7 @@ int oracle_backward_sampled(const double *q, const double *k, const double *v, c
     }
 #pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
     for (int r = 0; r < n_qrows; ++r) {
-        double *scratch = (double *)malloc(sizeof(double) * D);
+        double *scratch = (double *)malloc(sizeof(double) * p.Dv);
         row_dq(&p, qrows[3 * r], qrows[3 * r + 2], qrows[3 * r + 1], dq_rows + (long)r * D,
                scratch);
         free(scratch);
@@ -449,7 +468,7 @@ int oracle_backward_sampled(const double *q, const double *k, const double *v, c
         for (int r = r0; r < n_krows; ++r) {
             if (krows[3 * r] != b || krows[3 * r + 2] != hk) continue;
             col_dkdv(&p, b, hk, krows[3 * r + 1], lse_g, dvec_g, dk_rows + (long)r * D,
-                     dv_rows + (long)r * D);
+                     dv_rows + (long)r * p.Dv);
             done[r] = 1;
         }
         for (int g = 0; g < p.G; ++g) { free(lse_g[g]); free(dvec_g[g]); }
@@ -477,7 +496,7 @@ int oracle_preprocess(const double *q, const double *k, const double *v, const d
             int lq = seq_len_q(&p, b);
 #pragma omp parallel for schedule(dynamic, 8) num_threads(nthreads)
             for (int i = 0; i < lq; ++i) {
-                double *scratch = (double *)malloc(sizeof(double) * D);
+                double *scratch = (double *)malloc(sizeof(double) * p.Dv);
                 long li = lse_index(&p, b, i, h);
                 lse_out[li] = row_lse_for_backward(&p, b, h, i, scratch);
                 dvec_out[li] = row_dvec(&p, b, h, i, scratch);
@@ -499,7 +518,7 @@ int oracle_head_matrices(const double *q, const double *k, const double *v, cons
                   ext))
         return 1;
     int lq = seq_len_q(&p, b), lk = seq_len_k(&p, b);
-    double *scratch = (double *)malloc(sizeof(double) * D);
+    double *scratch = (double *)malloc(sizeof(double) * p.Dv);
     for (int i = 0; i < lq; ++i) {
         double l = row_lse_for_backward(&p, b, h, i, scratch);
         double dvec = row_dvec(&p, b, h, i, scratch);

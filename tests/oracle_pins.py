@@ -24,7 +24,10 @@ AssertionError when the oracle disagrees with:
 * dropout: the Philox4x32-10 known-answer vectors, the keep rate, t = 0 equal
   to no dropout, O / dV equal to P o (M s) times V / dO with the mask built
   from the generator here, and the backward as the gradient of the dropout
-  forward (fixed seed, finite differences).
+  forward (fixed seed, finite differences);
+* a value head dim Dv different from D: finite differences both ways, the
+  problem with zero columns padded onto the narrower side (which has one
+  head dim again), and the invariants with the two dims apart.
 
 ``tests/test_oracle.py`` runs every pin on the real oracle and also on
 mutant builds with a planted mistake, each of which must fail at least one
@@ -627,7 +630,93 @@ def pin_dropout_outputs(orc):
         _fd_check(orc, q[:1, :5], k[:1, :6], v[:1, :6], do[:1, :5], 0.6, causal, dropout=drop)
 
 
-ALL_PINS = [pin_preprocess_identity, pin_window_rows_equal_unmasked_band,
+def _dense_dv(rng, B, Sq, Sk, Hq, Hkv, D, Dv):
+    q = rng.standard_normal((B, Sq, Hq, D))
+    k = rng.standard_normal((B, Sk, Hkv, D))
+    v = rng.standard_normal((B, Sk, Hkv, Dv))
+    do = rng.standard_normal((B, Sq, Hq, Dv))
+    return q, k, v, do
+
+
+def pin_fd_value_dim(orc):
+    """A value head dim Dv different from the query / key dim D (both
+    directions; causal GQA, rectangular causal, varlen): the backward is the
+    gradient of L = sum(dO * O) by central differences."""
+    for (D, Dv), causal, shape in (((5, 3), True, (1, 6, 6, 2, 1)), ((3, 5), True, (1, 5, 7, 2, 2)),
+                                   ((4, 2), False, (2, 4, 5, 2, 1))):
+        q, k, v, do = _dense_dv(_rng(90 + D), *shape, D, Dv)
+        _fd_check(orc, q, k, v, do, 0.7, causal)
+    rng = _rng(95)
+    cu_q = np.array([0, 4, 9], dtype=np.int32)
+    cu_k = np.array([0, 6, 9], dtype=np.int32)
+    q = rng.standard_normal((9, 2, 4))
+    k = rng.standard_normal((9, 1, 4))
+    v = rng.standard_normal((9, 1, 2))
+    do = rng.standard_normal((9, 2, 2))
+    _fd_check(orc, q, k, v, do, 0.8, True, cu_q=cu_q, cu_k=cu_k)
+
+
+def pin_value_dim_equals_zero_padded(orc):
+    """Dv < D: V and dO padded with zero columns to D give the same dQ, dK and
+    O, LSE, and a dV whose extra columns are zero.  Dv > D: Q and K padded
+    with zero columns to Dv leave every score unchanged, so the padded problem
+    gives the same O, LSE, dV and a dQ / dK with zero extra columns.  The
+    padded problems have one head dim, pinned by every other pin."""
+    for causal in (False, True):
+        q, k, v, do = _dense_dv(_rng(97), 2, 7, 9, 4, 2, 6, 3)
+        zpad = lambda a, n: np.concatenate([a, np.zeros(a.shape[:-1] + (n,))], axis=-1)
+        o, lse = orc.forward(q, k, v, 0.5, causal)
+        op, lsep = orc.forward(q, k, zpad(v, 3), 0.5, causal)
+        _close(o, op[..., :3], 1e-14, "O, zero-padded V")
+        _close(lse, lsep, 1e-14, "LSE, zero-padded V")
+        g = orc.backward(q, k, v, do, 0.5, causal)
+        gp = orc.backward(q, k, zpad(v, 3), zpad(do, 3), 0.5, causal)
+        _close(g[0], gp[0], 1e-13, "dQ, zero-padded V / dO")
+        _close(g[1], gp[1], 1e-13, "dK, zero-padded V / dO")
+        _close(g[2], gp[2][..., :3], 1e-13, "dV, zero-padded V / dO")
+        _close(gp[2][..., 3:], np.zeros_like(gp[2][..., 3:]), 0, "dV padding")
+        q2, k2, v2, do2 = _dense_dv(_rng(98), 1, 8, 8, 2, 1, 2, 5)
+        o2, lse2 = orc.forward(q2, k2, v2, 0.5, causal)
+        o2p, lse2p = orc.forward(zpad(q2, 3), zpad(k2, 3), v2, 0.5, causal)
+        _close(o2, o2p, 1e-14, "O, zero-padded Q / K")
+        _close(lse2, lse2p, 1e-14, "LSE, zero-padded Q / K")
+        h = orc.backward(q2, k2, v2, do2, 0.5, causal)
+        hp = orc.backward(zpad(q2, 3), zpad(k2, 3), v2, do2, 0.5, causal)
+        _close(h[0], hp[0][..., :2], 1e-13, "dQ, zero-padded Q / K")
+        _close(h[1], hp[1][..., :2], 1e-13, "dK, zero-padded Q / K")
+        _close(h[2], hp[2], 1e-13, "dV, zero-padded Q / K")
+        _close(hp[0][..., 2:], np.zeros_like(hp[0][..., 2:]), 0, "dQ padding")
+        _close(hp[1][..., 2:], np.zeros_like(hp[1][..., 2:]), 0, "dK padding")
+
+
+def pin_value_dim_invariants(orc):
+    """dV = P^T dO, dK = c dS^T Q, dQ = c dS K and Dv_i = <dO_i, O_i> with
+    Dv != D, against P and dS from the head matrices; the sampled rows equal
+    the full backward."""
+    c = 0.6
+    q, k, v, do = _dense_dv(_rng(99), 1, 9, 9, 2, 1, 5, 3)
+    o, lse = orc.forward(q, k, v, c, True)
+    dq, dk, dv = orc.backward(q, k, v, do, c, True)
+    Ps = [orc.head_matrices(q, k, v, do, c, True, h=h) for h in range(2)]
+    _close(dv[0, :, 0], sum(P.T @ do[0, :, h] for h, (P, _) in enumerate(Ps)), 1e-13, "dV = P^T dO")
+    _close(dk[0, :, 0], c * sum(dS.T @ q[0, :, h] for h, (_, dS) in enumerate(Ps)), 1e-13,
+           "dK = c dS^T Q")
+    for h, (P, dS) in enumerate(Ps):
+        _close(dq[0, :, h], c * dS @ k[0, :, 0], 1e-13, "dQ = c dS K")
+    dvec, _ = orc.preprocess(q, k, v, do, c, True, o=o, lse=lse)
+    _close(dvec[0], np.einsum("shd,shd->hs", do[0], o[0]), 1e-13, "Dv = <dO, O>")
+    qr = [(0, 3, 1), (0, 8, 0)]
+    kr = [(0, 2, 0), (0, 7, 0)]
+    sq, sk, sv = orc.backward_sampled(q, k, v, do, c, True, qrows=qr, krows=kr)
+    for r, (b, s_, h) in enumerate(qr):
+        _close(sq[r], dq[b, s_, h], 0, "sampled dQ")
+    for r, (b, s_, hk) in enumerate(kr):
+        _close(sk[r], dk[b, s_, hk], 0, "sampled dK")
+        _close(sv[r], dv[b, s_, hk], 0, "sampled dV")
+
+
+ALL_PINS = [pin_fd_value_dim, pin_value_dim_equals_zero_padded, pin_value_dim_invariants,
+    pin_preprocess_identity, pin_window_rows_equal_unmasked_band,
     pin_philox_known_answers, pin_dropout_mask_and_rate, pin_dropout_outputs,
     pin_bias_key_column_equals_augmented, pin_bias_query_row_shifts_lse, pin_bias_equals_alibi,
     pin_fd_bias,

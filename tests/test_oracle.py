@@ -94,7 +94,14 @@ MUTANTS = {
     "dropout mask missing from dV": ("dv_out[d] += pij * f * doi[d];", "dv_out[d] += pij * doi[d];"),
     "seqused_q ignored": ("return p->ext.seqused_q ? p->ext.seqused_q[b] : stored_len_q(p, b);",
                           "return stored_len_q(p, b);"),
-    "Dv from q": ("return dot(doi, o_scratch, p->D);", "return dot(doi, p->q + row_q(p, b, i, h), p->D);"),
+    "Dv from q": ("return dot(doi, o_scratch, p->Dv);", "return dot(doi, p->q + row_q(p, b, i, h), p->Dv);"),
+    "dP over the query / key dim": ("p->v + row_v(p, b, j, hk), p->Dv);", "p->v + row_v(p, b, j, hk), p->D);"),
+    "dV rows at the key stride": ("dv + row_v(&p, b, j, hk));", "dv + row_k(&p, b, j, hk));"),
+    "O rows at the query stride": ("row_forward(&p, b, h, i, o + row_o(&p, b, i, h));",
+                                   "row_forward(&p, b, h, i, o + row_q(&p, b, i, h));"),
+    "dV summed over D columns": ("for (int d = 0; d < Dv; ++d) dv_out[d] += pij * f * doi[d];",
+                                 "for (int d = 0; d < D; ++d) dv_out[d] += pij * f * doi[d];"),
+    "value dim taken as D": ("p->Dv = p->ext.head_dim_v > 0 ? p->ext.head_dim_v : D;", "p->Dv = D;"),
     "preprocess skips the LSE guard": ("if (lse == -INFINITY) lse = 0.0; /* get_validated_lse */", ""),
     "LSE drops max shift": ("double lse = m + log(sum);", "double lse = log(sum);"),
     "score without scale": ("double s = p->scale * dot(", "double s = dot("),
