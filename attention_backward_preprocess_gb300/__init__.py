@@ -59,7 +59,7 @@ class FaExt(ctypes.Structure):
                 ("dbias", ctypes.c_void_p), ("dropout_p", ctypes.c_float),
                 ("dropout_seed", ctypes.c_ulonglong), ("dropout_offset", ctypes.c_uint),
                 ("dropout_mask", ctypes.c_void_p), ("total_q", ctypes.c_longlong),
-                ("total_k", ctypes.c_longlong)]
+                ("total_k", ctypes.c_longlong), ("head_dim_v", ctypes.c_int)]
 
 
 def dropout_mask_shape(q, k, cu_seqlens_q=None, max_seqlen_k=None):
@@ -73,7 +73,7 @@ def dropout_mask_shape(q, k, cu_seqlens_q=None, max_seqlen_k=None):
 
 
 def _ext(Hq, window=None, alibi_slopes=None, seqused_q=None, seqused_k=None, bias=None,
-         dbias=None, dropout=None, totals=None):
+         dbias=None, dropout=None, totals=None, head_dim_v=0):
     """A pointer to an FaExt, or None when no extension is asked for.
 
     ``bias``: [B or 1, Hq or 1, Sq, >= Sk] in the input dtype, last axis
@@ -83,11 +83,14 @@ def _ext(Hq, window=None, alibi_slopes=None, seqused_q=None, seqused_k=None, bia
     int32 tensor of ``dropout_mask_shape(...)`` that fa_fwd fills with the keep
     flags and fa_bwd reads back; see fa_ext in include/fa.h.  ``totals``:
     (total_q, total_k), the packed row counts of a varlen call (cu_seqlens[B]),
-    so that the library need not read them back (no stream synchronisation)."""
+    so that the library need not read them back (no stream synchronisation).
+    ``head_dim_v``: the value head dim when it differs from q's (else 0)."""
     if (window is None and alibi_slopes is None and seqused_q is None and seqused_k is None
-            and bias is None and dbias is None and dropout is None and totals is None):
+            and bias is None and dbias is None and dropout is None and totals is None
+            and not head_dim_v):
         return None
-    e = FaExt(-1, -1, None, 0, None, None, None, 0, 0, 0, None, 0.0, 0, 0, None, 0, 0)
+    e = FaExt(-1, -1, None, 0, None, None, None, 0, 0, 0, None, 0.0, 0, 0, None, 0, 0, 0)
+    e.head_dim_v = int(head_dim_v)
     if totals is not None:
         e.total_q, e.total_k = int(totals[0]), int(totals[1])
     if dropout is not None:
@@ -214,6 +217,12 @@ def _shape(q, k, cu_q, max_seqlen_q, max_seqlen_k):
     return cu_q.numel() - 1, int(max_seqlen_q), int(max_seqlen_k), q.shape[1], k.shape[1], q.shape[2]
 
 
+def _value_dim(D, v) -> int:
+    """head_dim_v of fa_ext: v's last axis when it differs from the query /
+    key head dim, else 0."""
+    return 0 if v.shape[-1] == D else int(v.shape[-1])
+
+
 def default_scale(D: int) -> float:
     return 1.0 / (D ** 0.5)
 
@@ -232,13 +241,13 @@ def fa_fwd(q, k, v, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seql
     """
     B, Sq, Sk, Hq, Hkv, D = _shape(q, k, cu_seqlens_q, max_seqlen_q, max_seqlen_k)
     scale = default_scale(D) if softmax_scale is None else float(softmax_scale)
-    o = torch.empty_like(q)
+    o = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
     if cu_seqlens_q is None:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
     else:
         lse = torch.empty((Hq, q.shape[0]), dtype=torch.float32, device=q.device)
     ext = _ext(Hq, window, alibi_slopes, seqused_q, seqused_k, bias, dropout=dropout,
-               totals=totals)
+               totals=totals, head_dim_v=_value_dim(D, v))
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Sq, Sk, Hq, Hkv, D, scale,
             int(bool(causal)), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k)]
     if ext is None:
@@ -271,7 +280,8 @@ def fa_bwd(q, k, v, o, dout, lse, causal=False, softmax_scale=None, cu_seqlens_q
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
             _ptr(dv), B, Sq, Sk, Hq, Hkv, D, scale, int(bool(causal)), _ptr(cu_seqlens_q),
             _ptr(cu_seqlens_k), int(bool(deterministic)), _dtype_code(q)]
-    ext = _ext(Hq, window, alibi_slopes, seqused_q, seqused_k, bias, dbias, dropout, totals)
+    ext = _ext(Hq, window, alibi_slopes, seqused_q, seqused_k, bias, dbias, dropout, totals,
+               _value_dim(D, v))
     if ext is not None:
         st = lib().fa_bwd_ext(*args[:19], ext, *args[19:], _ptr(workspace),
                               0 if workspace is None else workspace.numel(), _stream(stream))

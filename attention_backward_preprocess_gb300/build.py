@@ -17,9 +17,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfa_gb300.so")
-SOURCES = ["fa_api.cu", "fa_bwd_main.cu", "fa_fwd_tc.cu", "fa_fwd_split.cu", "fa_kernels.cu", "fa_selftest.cu",
-           "fa_noalloc.cu"]
-HEADERS = ["fa_device.cuh", "fa_params.h", "fa_fwd_common.h"]
+SOURCES = ["fa_api.cu", "fa_bwd_main.cu", "fa_bwd_wide.cu", "fa_fwd_tc.cu", "fa_fwd_split.cu",
+           "fa_kernels.cu", "fa_selftest.cu", "fa_noalloc.cu"]
+HEADERS = ["fa_device.cuh", "fa_params.h", "fa_fwd_common.h", "fa_bwd_units.cuh"]
 PUBLIC_HEADERS = [os.path.join(ROOT, "include", h) for h in ("fa.h", "fa_selftest.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -27,6 +27,11 @@ cudaError_t launch_bwd_main(const BwdParams &p, const CUtensorMap &q, const CUte
                             const CUtensorMap &v, const CUtensorMap &dout, int bf16, int grid,
                             cudaStream_t stream);
 int main_block_m(int D);
+cudaError_t launch_bwd_wide(const BwdParams &p, const CUtensorMap &q, const CUtensorMap &k,
+                            const CUtensorMap &v, const CUtensorMap &dout, int bf16, int grid,
+                            cudaStream_t stream);
+int wide_block_m();
+int wide_halves(int Dq_tile, int Dv_tile);
 }  // namespace fa
 
 namespace {
@@ -37,10 +42,24 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Tile width a head dim runs at: 64 or 128 (the columns past D are zero-filled
-// by the TMA loads; the FlashAttention postprocess page likewise pads the head
-// dim to a multiple of its block size).
-int pad_d(int D) { return D <= 64 ? 64 : 128; }
+// Tile width a head dim runs at: 64, 128 or 256 (the columns past D are
+// zero-filled by the TMA loads; the FlashAttention postprocess page likewise
+// pads the head dim to a multiple of its block size).
+int pad_d(int D) { return D <= 64 ? 64 : D <= 128 ? 128 : 256; }
+
+// Head dims with a kernel: a query / key dim D that is a multiple of 8 in
+// [64, 256]; a value dim Dv (0: equal to D) that is a multiple of 8 in
+// [8, 256].  One head dim of at most 128 runs in the main kernel; a head dim
+// above 128, or Dv != D (then D > 64), runs in the wide kernel.
+bool head_dims_ok(int D, int Dv) {
+    if (D < 64 || D > 256 || D % 8 != 0) return false;
+    if (Dv == 0 || Dv == D) return true;
+    return Dv >= 8 && Dv <= 256 && Dv % 8 == 0 && D > 64;
+}
+bool wide_dims(int D, int Dv) { return D > 128 || (Dv != 0 && Dv != D); }
+int value_tile(int D, int Dv) {   // tile width of the value side
+    return wide_dims(D, Dv) ? ((Dv == 0 ? D : Dv) <= 128 ? 128 : 256) : pad_d(D);
+}
 
 struct Layout {
     size_t err, ntiles, tiles, dvec, lse2, dqacc, sem, total;  // byte offsets / size
@@ -93,7 +112,7 @@ fa_status check_shape(int B, int Sq, int Sk, int Hq, int Hkv, int D, fa_dtype dt
     if (B <= 0 || Sq <= 0 || Sk <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return FA_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
     if ((cu_q == nullptr) != (cu_k == nullptr)) return FA_ERR_INVALID_ARG;
-    if (D < 64 || D > 128 || D % 8 != 0) return FA_ERR_UNSUPPORTED;
+    if (!head_dims_ok(D, 0)) return FA_ERR_UNSUPPORTED;
     if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_UNSUPPORTED;
     // TMA coordinates are 32-bit
     if ((long long)B * Sq > (1LL << 31) - 1 || (long long)B * Sk > (1LL << 31) - 1)
@@ -246,7 +265,13 @@ fa_status apply_ext(fa::BwdParams &p, int causal, const fa_ext *ext) {
     p.drop_scale = 1.f;
     p.drop_mask = nullptr;
     p.drop_mask_w = 0;
+    p.Dhv = p.Dh;
+    p.Dv = p.D;
     if (ext) {
+        if (ext->head_dim_v != 0) {
+            if (!head_dims_ok(p.Dh, ext->head_dim_v)) return FA_ERR_UNSUPPORTED;
+            p.Dhv = ext->head_dim_v;
+        }
         wl = ext->window_left;
         wr = ext->window_right;
         if (wl < -1 || wr < -1) return FA_ERR_INVALID_ARG;
@@ -294,6 +319,14 @@ fa_status apply_ext(fa::BwdParams &p, int causal, const fa_ext *ext) {
     p.win_lo = (wl < 0 || wl >= fa::kNoWindow) ? fa::kNoWindow : wl;
     p.win_hi = (wr < 0 || wr >= fa::kNoWindow) ? fa::kNoWindow : wr;
     if (causal) p.win_hi = std::min(p.win_hi, 0);
+    if (wide_dims(p.Dh, p.Dhv)) {
+        // the wide kernel's tile widths (128 or 256 on each side); it has the
+        // plain mask only (causal or an upper band edge, used lengths)
+        p.D = p.Dh <= 128 ? 128 : 256;
+        p.Dv = value_tile(p.Dh, p.Dhv);
+        if (p.win_lo < fa::kNoWindow || p.alibi || p.bias || p.dbias || p.drop_t > 0)
+            return FA_ERR_UNSUPPORTED;
+    }
     return FA_OK;
 }
 
@@ -328,6 +361,8 @@ fa_status prepare(const void *q, const void *k, const void *v, const void *o, co
     // the extensions are host arguments too: checked before the device is
     if ((st = apply_ext(p, causal, ext)) != FA_OK) return st;
     if ((st = check_ext_totals(ext, cu_q != nullptr, B, Sq, Sk)) != FA_OK) return st;
+    // the wide kernel adds dQ without the deterministic order
+    if (deterministic && wide_dims(p.Dh, p.Dhv)) return FA_ERR_UNSUPPORTED;
     st = check_device();
     if (st != FA_OK) return st;
     long long tq = (long long)B * Sq, tk = (long long)B * Sk;
@@ -379,7 +414,8 @@ fa_status run_preprocess(const Prepared &P, fa_dtype dtype, cudaStream_t stream)
 
 fa_status run_main(const Prepared &P, fa_dtype dtype, cudaStream_t stream) {
     const fa::BwdParams &p = P.p;
-    const int bm = fa::main_block_m(p.D);
+    const bool wide = wide_dims(p.Dh, p.Dhv);
+    const int bm = wide ? fa::wide_block_m() : fa::main_block_m(p.D);
     const int bf16 = dtype == FA_BF16;
     CUtensorMap mq, mk, mv, mdo;
     const long long rq = p.varlen ? P.total_q : p.Sq, rk = p.varlen ? P.total_k : p.Sk;
@@ -387,13 +423,19 @@ fa_status run_main(const Prepared &P, fa_dtype dtype, cudaStream_t stream) {
     if (rq <= 0 || rk <= 0) return FA_ERR_INVALID_ARG;
     if (!p.q || !p.k || !p.v || !p.dout || !p.dk || !p.dv) return FA_ERR_INVALID_ARG;
     if (!encode_rows_map(&mq, p.q, p.Dh, p.Hq, rq, nb, bm, bf16) ||
-        !encode_rows_map(&mdo, p.dout, p.Dh, p.Hq, rq, nb, bm, bf16) ||
+        !encode_rows_map(&mdo, p.dout, p.Dhv, p.Hq, rq, nb, bm, bf16) ||
         !encode_rows_map(&mk, p.k, p.Dh, p.Hkv, rk, nb, fa::kBlockN, bf16) ||
-        !encode_rows_map(&mv, p.v, p.Dh, p.Hkv, rk, nb, fa::kBlockN, bf16))
+        !encode_rows_map(&mv, p.v, p.Dhv, p.Hkv, rk, nb, fa::kBlockN, bf16))
         return FA_ERR_CUDA;
     if (p.varlen) {
         // the unit list depends on the device-resident cu_seqlens
         if (fa::launch_schedule(p, stream) != cudaSuccess) return FA_ERR_CUDA;
+    }
+    if (wide) {
+        // units: key-block units times column halves
+        const long long units = (long long)p.max_tiles * fa::wide_halves(p.D, p.Dv);
+        const int grid = (int)std::min<long long>(units, sm_count());
+        return cuda_status(fa::launch_bwd_wide(p, mq, mk, mv, mdo, bf16, grid, stream));
     }
     const int grid = (int)std::min<long long>(p.max_tiles, sm_count());
     return cuda_status(fa::launch_bwd_main(p, mq, mk, mv, mdo, bf16, grid, stream));
@@ -438,7 +480,7 @@ long long fa_set_wait_timeout_ns(long long ns) {
 size_t fa_bwd_workspace_bytes(int B, int Sq, int Sk, int Hq, int Hkv, int D, int varlen,
                               int deterministic) {
     Layout L;
-    if (D < 64 || D > 128 || D % 8 != 0) return 0;
+    if (!head_dims_ok(D, 0)) return 0;
     if (!plan(B, Sq, Sk, Hq, Hkv, D, varlen, deterministic, &L)) return 0;
     return L.total;
 }
@@ -447,7 +489,7 @@ fa_status fa_bwd_workspace_layout(int B, int Sq, int Sk, int Hq, int Hkv, int D,
                                   int deterministic, size_t *dvec_off, size_t *lse2_off,
                                   size_t *dqacc_off, size_t *rows) {
     Layout L;
-    if (D < 64 || D > 128 || D % 8 != 0) return FA_ERR_UNSUPPORTED;
+    if (!head_dims_ok(D, 0)) return FA_ERR_UNSUPPORTED;
     if (!plan(B, Sq, Sk, Hq, Hkv, D, varlen, deterministic, &L)) return FA_ERR_INVALID_ARG;
     if (dvec_off) *dvec_off = L.dvec / 4;
     if (lse2_off) *lse2_off = L.lse2 / 4;
@@ -460,7 +502,7 @@ fa_status fa_bwd_workspace_sync_layout(int B, int Sq, int Sk, int Hq, int Hkv, i
                                        int deterministic, size_t *err_off, size_t *sem_off,
                                        size_t *n_sem) {
     Layout L;
-    if (D < 64 || D > 128 || D % 8 != 0) return FA_ERR_UNSUPPORTED;
+    if (!head_dims_ok(D, 0)) return FA_ERR_UNSUPPORTED;
     if (!plan(B, Sq, Sk, Hq, Hkv, D, varlen, deterministic, &L)) return FA_ERR_INVALID_ARG;
     if (err_off) *err_off = L.err;
     if (sem_off) *sem_off = deterministic ? L.sem : 0;
@@ -622,6 +664,7 @@ fa_status fa_fwd_ext(const void *q, const void *k, const void *v, void *o, float
     p.cu_k = cu_seqlens_k;
     if ((st = apply_ext(p, causal, ext)) != FA_OK) return st;
     if ((st = check_ext_totals(ext, p.varlen, B, Sq, Sk)) != FA_OK) return st;
+    if (wide_dims(p.Dh, p.Dhv)) return FA_ERR_UNSUPPORTED;   // no forward kernel for these yet
     if ((st = check_device()) != FA_OK) return st;
     p.err = fa::fwd_error_word();
     if (!p.err) return FA_ERR_CUDA;

@@ -14,26 +14,42 @@
 //   dV  += P^T dO         tcgen05.mma TS (P^T bf16 in TMEM)       (STAGE 3)
 //   dS^T = P^T o (dP^T - Dv)  softmax warps                       (STAGE 5)
 //   dK  += dS^T Q         tcgen05.mma TS (dS^T bf16 in TMEM)      (STAGE 6)
-//   dQ   = dS K           tcgen05.mma SS (dS^T in smem), added into the fp32
-//                         accumulator by coalesced red.global.add (STAGE 7;
-//                         the atomic "update_tile" path), or in a fixed
-//                         n-block order through per-row-block semaphores in
-//                         deterministic mode (the wait_eq / arrive_inc
-//                         pattern of CollectiveEpilogueBwdGQA in
+//   dQ^T = K^T dS^T       tcgen05.mma SS (dS^T staged in shared memory;
+//                         D = 64: dQ = dS K), added into the fp32
+//                         accumulator in the workspace (STAGE 7): at D = 128
+//                         each 32-row chunk goes through shared memory and
+//                         one TMA bulk reduce-add (cp.reduce.async.bulk), at
+//                         D = 64 through red.global.add.v4.f32 (the atomic
+//                         "update_tile" path); in deterministic mode in a
+//                         fixed n-block order through per-row-block
+//                         semaphores (the wait_eq / arrive_inc pattern of
+//                         CollectiveEpilogueBwdGQA in
 //                         "flash-attention/hopper/epilogue_bwd.hpp")
 //
 // and at the end dK * c, dV are written out (CollectiveEpilogueBwd::store;
 // zeros for a unit with no visible query, store_zero).
 //
-// Warp roles (14 warps):
-//   warp 0        TMA producer: K/V once per unit, Q/dO/LSE2/Dv per row block
-//   warp 1        TMEM allocator and single-thread MMA issuer
-//   warps 2-5     dQ reducers (one TMEM lane quarter each)
-//   warps 6-13    softmax / elementwise, two groups of four; group g handles
+// Persistent CTAs (one per SM) take units from a global counter.  Warp roles
+// (16 warps, 512 threads):
+//   warp 0        TMA producer: K and V once per unit (they swap shared-memory
+//                 slots from one unit to the next, so the next unit's K loads
+//                 while this unit's last dQ still reads its K), Q / dO / LSE2
+//                 / Dv per step through a 3-stage ring; takes the units and
+//                 passes them on through a ring in shared memory
+//   warp 1        MMA warp A: S^T and dP^T of every step; also allocates and
+//                 frees tensor memory
+//   warp 2        MMA warp B: dV, dK, then dQ^T of every step
+//   warp 3        bulk-reduce issuer (D = 128): adds each staged dQ chunk to
+//                 the accumulator, and orders the adds in deterministic mode
+//   warps 4-7     dQ reducers: dQ^T out of tensor memory into the staging
+//                 buffers (one TMEM lane quarter each)
+//   warps 8-15    softmax / elementwise, two groups of four; group g handles
 //                 query columns [g BM/2, (g+1) BM/2) of every key row, and
 //                 in the epilogue group 0 writes dK, group 1 writes dV
 // Every wait is bounded (see fa_device.cuh); a wait that gives up sets the
-// CTA abort flag and the device error word and the CTA winds down.
+// CTA abort flag and the device error word, and the CTA winds down: every
+// MMA and TMA load it issued completes before tensor memory is freed.
+#include "fa_bwd_units.cuh"
 #include "fa_device.cuh"
 #include "fa_params.h"
 
@@ -61,10 +77,10 @@ struct MainCfg {
     // step j only for the softmax warps to have read dP^T of step j-1.
     static constexpr int kSBuf = (kD == 128) ? 3 : 2;
     static constexpr int kStages = 3;
-    // Warp roles: 0 producer | 1 MMA issuer (D = 64) or MMA warp A (S, dP) |
-    // 2 MMA warp B (dV, dK, dQ; D = 128) | 3 bulk-reduce issuer (D = 128) |
-    // 4-7 dQ reducers | 8-15 softmax (two groups of four, one per TMEM lane
-    // quarter).  Warps 2 and 3 idle when D = 64.
+    // Warp roles: 0 producer | 1 MMA warp A (S, dP) | 2 MMA warp B (dV, dK,
+    // dQ) | 3 bulk-reduce issuer (D = 128) | 4-7 dQ reducers | 8-15 softmax
+    // (two groups of four, one per TMEM lane quarter).  Warp 3 idles when
+    // D = 64.
     static constexpr int W_MMA_B = 2, W_ISSUE = 3, W_RED = 4, W_SM = 8;
     static constexpr int kThreads = 16 * 32;
     static constexpr int TM_DK = 0;
@@ -122,8 +138,8 @@ struct MainCfg {
     static constexpr int OFF_LSE = OFF_STG + STG_BYTES;
     static constexpr int OFF_DV = OFF_LSE + kStages * BM * 4;
     static constexpr int OFF_BAR = OFF_DV + kStages * BM * 4;
-    static constexpr int NUM_BARS = 48;
-    static_assert(40 + 2 * kStages <= NUM_BARS, "barrier slots");
+    static constexpr int NUM_BARS = 50;
+    static_assert(40 + 2 * kStages <= 46, "barrier slots");
     // TMEM slot (+0), abort flag (+16), unit ring (+32), chunk rows (+48),
     // chunk n blocks (+64)
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
@@ -141,7 +157,12 @@ struct MainCfg {
 // looked at the previous phase come one per buffer, so that no barrier ever
 // runs two phases ahead of a waiter.
 enum {
-    B_KV_FULL = 0, B_KV_EMPTY = 1,
+    // K and V swap shared-memory slots from one unit to the next: unit u (u-th
+    // unit of the CTA) keeps K in slot u % 2 and V in the other, so the next
+    // unit's K can land in the slot whose V only warp A's dP^T reads, while
+    // warp B still reads this unit's K for its last dQ.
+    B_K_FULL = 0,       // +s: a K tile landed in slot s
+    B_V_FULL = 46,      // +s: a V tile landed in slot s
     B_S_FULL = 2,       // +b, S buffer b: S^T complete
     B_P_FULL = 5,       // +b: P^T written back
     B_DS_FULL = 8,      // +b: dS^T written back (TMEM and shared memory)
@@ -157,100 +178,10 @@ enum {
     B_STG_FULL = 34,    // +b: the 4 reducer warps wrote dQ staging buffer b
     B_STG_FREE = 36,    // +b: the bulk reduce has read staging buffer b
     B_TILE_FULL = 38,   // +d: the reducers wrote a dQ chunk into dS^T tile d
-    B_STAGE0 = 40       // full[kStages], then empty[kStages]
+    B_STAGE0 = 40,      // full[kStages], then empty[kStages]
+    B_FREE_A = 48,      // warp A's MMAs of a unit completed (its reads of both slots)
+    B_FREE_B = 49       // warp B's MMAs of a unit completed (its reads of the K slot)
 };
-
-// Work units are handed out dynamically: the producer warp takes the next
-// index from a global counter and passes it to the other warps of the CTA
-// through a small ring in shared memory.  Dense units leave the counter group
-// by group of (sequence, kv head) pairs, n_block-major inside a group, so the
-// units that run at the same time sweep the same rows of Q, dO and the dQ
-// accumulator in L2; idle CTAs take the next unit, which balances the uneven
-// causal work.  -1 ends the sequence.
-struct UnitRing {
-    volatile int *slot;   // kRing ints in shared memory
-    uint32_t full0, empty0;
-    int k = 0;
-    uint32_t ph = 0;
-    __device__ __forceinline__ void advance(int ring) {
-        if (++k == ring) { k = 0; ph ^= 1; }
-    }
-};
-
-__device__ __forceinline__ uint32_t bit(uint32_t mask, int b) { return (mask >> b) & 1u; }
-
-struct Unit {
-    int b, n_block, hk;
-    int lq, lk;
-    int q_row0, k_row0, bidx;   // TMA row offset and batch coordinate
-    int m_begin, nm, iters;     // row blocks [m_begin, m_begin + nm) per head; iters = G * nm
-    // Iteration order: row blocks from the last to the first, the G query
-    // heads of the group innermost.  Under a causal mask every unit of a
-    // (sequence, kv head) starts at the same last row block, so the units
-    // that run side by side sweep the same Q / dO / dQ-accumulator rows
-    // together and share them in L2.
-    __device__ __forceinline__ int g_of(int it, int G) const { return it % G; }
-    __device__ __forceinline__ int m_of(int it, int G) const { return m_begin + nm - 1 - it / G; }
-};
-
-// Work unit t: dense problems enumerate groups of (batch, kv head) pairs,
-// then n_block, then the pair inside the group; varlen problems read the list
-// the scheduler kernel wrote.
-template <int BM>
-__device__ __forceinline__ Unit decode_unit(const BwdParams &p, int t) {
-    Unit u;
-    if (p.varlen) {
-        const int4 e = p.tiles[t];
-        u.b = e.x;
-        u.n_block = e.y;
-        u.hk = e.z;
-        u.q_row0 = p.cu_q[u.b];
-        u.k_row0 = p.cu_k[u.b];
-        u.lq = used_len_q(p, u.b);
-        u.lk = used_len_k(p, u.b);
-        u.bidx = 0;
-    } else {
-        // groups of unit_group (batch, kv head) pairs, one after the other;
-        // inside a group the n blocks in increasing order (longest causal
-        // units first), the pairs of the group interleaved.  Units that run at
-        // the same time then share their dQ / Q / dO rows in L2.
-        const int gs = p.unit_group;
-        const int nblk = p.num_units / (p.B * p.Hkv);
-        const int grp = t / (gs * nblk);
-        const int r = t - grp * gs * nblk;
-        u.n_block = r / gs;
-        const int bh = grp * gs + (r - u.n_block * gs);
-        u.b = bh / p.Hkv;
-        u.hk = bh - u.b * p.Hkv;
-        u.q_row0 = 0;
-        u.k_row0 = 0;
-        u.lq = used_len_q(p, u.b);
-        u.lk = used_len_k(p, u.b);
-        u.bidx = u.b;
-    }
-    // queries that see a key of [n0, n0 + kBlockN): i >= n0 - diag - win_hi
-    // (the first key against the upper edge of the band) and
-    // i <= n0 + kBlockN - 1 - diag + win_lo (the last key against the lower edge)
-    const int n0 = u.n_block * kBlockN;
-    const long long diag = u.lk - u.lq;
-    const long long first_row = max(0LL, (long long)n0 - diag - p.win_hi);
-    const long long last_row = min((long long)u.lq - 1, (long long)n0 + kBlockN - 1 - diag + p.win_lo);
-    u.m_begin = (int)min(first_row / BM, (long long)(u.lq + BM - 1) / BM);
-    u.nm = last_row < first_row ? 0 : (int)(last_row / BM + 1 - u.m_begin);
-    if (n0 >= u.lk) u.nm = 0;
-    u.iters = p.G * u.nm;
-    return u;
-}
-
-// First key block with a key that some query of the rows [m0, ...) of a
-// sequence can see: the block holding key m0 + diag - win_lo.  A row block
-// receives dQ contributions from the key blocks n_first, n_first + 1, ... in
-// turn, so in deterministic mode the unit of key block n waits until its row
-// block's semaphore counts n - n_first earlier contributions.
-__device__ __forceinline__ int first_key_block(const BwdParams &p, int m0, int diag) {
-    const long long j = (long long)m0 + diag - p.win_lo;
-    return j <= 0 ? 0 : (int)(j / kBlockN);
-}
 
 struct MainMaps {
     CUtensorMap q, k, v, dout;
@@ -297,8 +228,12 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
-        mbar_init(bar(B_KV_FULL), 1);
-        mbar_init(bar(B_KV_EMPTY), 2);   // one commit per MMA warp
+        for (int sl = 0; sl < 2; ++sl) {
+            mbar_init(bar(B_K_FULL + sl), 1);
+            mbar_init(bar(B_V_FULL + sl), 1);
+        }
+        mbar_init(bar(B_FREE_A), 1);
+        mbar_init(bar(B_FREE_B), 1);
         for (int b = 0; b < 3; ++b) {
             mbar_init(bar(B_S_FULL + b), 1);
             mbar_init(bar(B_P_FULL + b), 8);
@@ -372,13 +307,49 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         if (warp == 0) {
             // ------------------------------------------------------------ producer
             if (lane == 0) {
-                uint32_t kv_ph = 0, st_ph = 0;
+                uint32_t st_ph = 0;
                 int stage = 0;
                 bool ok = true;
+                // K / V tiles issued so far: unit v (the v-th unit with work) has its
+                // K in slot v % 2 and its V in the other, as phase v / 2 of the
+                // slot's K / V barrier
+                int kn = 0, vn = 0;
                 // the phase parity of the last load armed on each barrier, so that
                 // every load still in flight can be waited for before the CTA exits
-                int kv_armed = 0;
                 uint32_t st_armed = 0, st_last = 0;   // bit s: stage s armed / its parity
+                // one Q / dO / LSE2 / Dv stage of step it of unit u
+                auto load_stage = [&](const Unit &u, int it) __attribute__((always_inline)) -> bool {
+                    const int g = u.g_of(it, p.G), m = u.m_of(it, p.G);
+                    const int h = u.hk * p.G + g;
+                    if (!mbar_wait(bar(B_STAGE0 + S + stage), st_ph ^ 1, w)) return false;
+                    const uint32_t full = bar(B_STAGE0 + stage);
+                    mbar_arrive_expect_tx(full, 2 * C::QO_BYTES + 2 * BM * 4);
+                    st_armed |= 1u << stage;
+                    st_last = (st_last & ~(1u << stage)) | (st_ph << stage);
+                    const int qrow = u.q_row0 + m * BM;
+#pragma unroll
+                    for (int hh = 0; hh < D / 64; ++hh) {
+                        tma_load_4d(sbase + C::OFF_Q + stage * C::QO_BYTES + hh * BM * 128, &maps.q,
+                                    full, hh * 64, h, qrow, u.bidx);
+                        tma_load_4d(sbase + C::OFF_DO + stage * C::QO_BYTES + hh * BM * 128,
+                                    &maps.dout, full, hh * 64, h, qrow, u.bidx);
+                    }
+                    const long long r0 = ws_row(p, u.b, h, m * BM);
+                    bulk_load(sbase + C::OFF_LSE + stage * BM * 4, p.lse2 + r0, BM * 4, full);
+                    bulk_load(sbase + C::OFF_DV + stage * BM * 4, p.dvec + r0, BM * 4, full);
+                    if (++stage == S) { stage = 0; st_ph ^= 1; }
+                    return true;
+                };
+                // a K or V tile of 128 keys into slot sl
+                auto load_kv = [&](const Unit &u, const CUtensorMap *map, uint32_t full, int sl)
+                    __attribute__((always_inline)) {
+                    mbar_arrive_expect_tx(full, C::KV_BYTES);
+                    const int krow = u.k_row0 + u.n_block * BN;
+#pragma unroll
+                    for (int hh = 0; hh < D / 64; ++hh)
+                        tma_load_4d(sbase + C::OFF_K + sl * C::KV_BYTES + hh * BN * 128, map, full,
+                                    hh * 64, u.hk, krow, u.bidx);
+                };
                 while (ok) {
                     // take the next unit and publish it to the other warps
                     if (!(ok = mbar_wait(ring.empty0 + 8u * ring.k, ring.ph ^ 1, w))) break;
@@ -398,43 +369,29 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     if (t < 0) break;
                     const Unit u = decode_unit<BM>(p, t);
                     if (u.iters == 0) continue;
-                    if (!(ok = mbar_wait(bar(B_KV_EMPTY), kv_ph ^ 1, w))) break;
-                    kv_ph ^= 1;
-                    mbar_arrive_expect_tx(bar(B_KV_FULL), 2 * C::KV_BYTES);
-                    ++kv_armed;
-                    const int krow = u.k_row0 + u.n_block * BN;
-#pragma unroll
-                    for (int h = 0; h < D / 64; ++h) {
-                        tma_load_4d(sbase + C::OFF_K + h * BN * 128, &maps.k, bar(B_KV_FULL), h * 64,
-                                    u.hk, krow, u.bidx);
-                        tma_load_4d(sbase + C::OFF_V + h * BN * 128, &maps.v, bar(B_KV_FULL), h * 64,
-                                    u.hk, krow, u.bidx);
-                    }
-                    for (int it = 0; it < u.iters; ++it) {
-                        const int g = u.g_of(it, p.G), m = u.m_of(it, p.G);
-                        const int h = u.hk * p.G + g;
-                        if (!(ok = mbar_wait(bar(B_STAGE0 + S + stage), st_ph ^ 1, w))) break;
-                        const uint32_t full = bar(B_STAGE0 + stage);
-                        mbar_arrive_expect_tx(full, 2 * C::QO_BYTES + 2 * BM * 4);
-                        st_armed |= 1u << stage;
-                        st_last = (st_last & ~(1u << stage)) | (st_ph << stage);
-                        const int qrow = u.q_row0 + m * BM;
-#pragma unroll
-                        for (int hh = 0; hh < D / 64; ++hh) {
-                            tma_load_4d(sbase + C::OFF_Q + stage * C::QO_BYTES + hh * BM * 128, &maps.q,
-                                        full, hh * 64, h, qrow, u.bidx);
-                            tma_load_4d(sbase + C::OFF_DO + stage * C::QO_BYTES + hh * BM * 128,
-                                        &maps.dout, full, hh * 64, h, qrow, u.bidx);
-                        }
-                        const long long r0 = ws_row(p, u.b, h, m * BM);
-                        bulk_load(sbase + C::OFF_LSE + stage * BM * 4, p.lse2 + r0, BM * 4, full);
-                        bulk_load(sbase + C::OFF_DV + stage * BM * 4, p.dvec + r0, BM * 4, full);
-                        if (++stage == S) { stage = 0; st_ph ^= 1; }
-                    }
+                    const int nu = kn, ks = nu & 1;         // K slot; V goes to the other
+                    // K into the slot that held the previous unit's V, once warp
+                    // A's MMAs of that unit completed
+                    if (nu > 0 && !(ok = mbar_wait(bar(B_FREE_A), (uint32_t)(nu - 1) & 1u, w))) break;
+                    load_kv(u, &maps.k, bar(B_K_FULL + ks), ks);
+                    ++kn;
+                    // the first step's Q / dO, so that S^T of the unit can start
+                    if (!(ok = load_stage(u, 0))) break;
+                    // V into the slot of the previous unit's K, once warp B's dQ^T
+                    // read it too
+                    if (nu > 0 && !(ok = mbar_wait(bar(B_FREE_B), (uint32_t)(nu - 1) & 1u, w))) break;
+                    load_kv(u, &maps.v, bar(B_V_FULL + (ks ^ 1)), ks ^ 1);
+                    ++vn;
+                    for (int it = 1; it < u.iters; ++it)
+                        if (!(ok = load_stage(u, it))) break;
                 }
                 // wind-down (after an abort some loads may not have been waited
                 // for by their consumers): none may land after the CTA exits
-                if (kv_armed > 0) mbar_wait_drain(bar(B_KV_FULL), (uint32_t)(kv_armed - 1) & 1u, p.err, p.budget_ns);
+                for (int v = max(kn - 2, 0); v < kn; ++v)
+                    mbar_wait_drain(bar(B_K_FULL + (v & 1)), (uint32_t)(v >> 1) & 1u, p.err, p.budget_ns);
+                for (int v = max(vn - 2, 0); v < vn; ++v)
+                    mbar_wait_drain(bar(B_V_FULL + ((v & 1) ^ 1)), (uint32_t)(v >> 1) & 1u, p.err,
+                                    p.budget_ns);
                 for (int s2 = 0; s2 < S; ++s2)
                     if (bit(st_armed, s2)) mbar_wait_drain(bar(B_STAGE0 + s2), bit(st_last, s2), p.err, p.budget_ns);
             }
@@ -444,18 +401,20 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             // X for every step j, ahead of warp B.  Before S_j it waits until the
             // reducers took the dQ^T of step j-3 out of that S buffer, before dP_j
             // until the softmax warps read dP^T of step j-1.
-            uint32_t kv_ph = 0, sfree_ph = 0, xfree_ph = 0, s_ph = 0;   // sfree: bit per buffer
+            uint32_t sfree_ph = 0, xfree_ph = 0, s_ph = 0;   // sfree: bit per buffer
             int s_stage = 0, nb = 0;
             bool ok = true;
-            const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
-            const uint64_t dK_k = sw128_desc(sK, 16, 1024), dV_k = sw128_desc(sV, 16, 1024);
+            int nu = 0;   // units with work so far: K in slot nu % 2, V in the other
             while (ok) {
                 const int t = next_unit();
                 if (t < 0) break;
                 const Unit u = decode_unit<BM>(p, t);
                 if (u.iters == 0) continue;
-                if (!(ok = mbar_wait_warp(bar(B_KV_FULL), kv_ph, w))) break;
-                kv_ph ^= 1;
+                const int ks = nu & 1;
+                const uint32_t uph = (uint32_t)(nu >> 1) & 1u;
+                const uint64_t dK_k = sw128_desc(sbase + C::OFF_K + ks * C::KV_BYTES, 16, 1024);
+                const uint64_t dV_k = sw128_desc(sbase + C::OFF_K + (ks ^ 1) * C::KV_BYTES, 16, 1024);
+                if (!(ok = mbar_wait_warp(bar(B_K_FULL + ks), uph, w))) break;
                 for (int j = 0; j < u.iters; ++j) {
                     if (!(ok = mbar_wait_warp(bar(B_STAGE0 + s_stage), s_ph, w))) break;
                     if (!(ok = mbar_wait_warp(bar(B_S_FREE + nb), bit(sfree_ph, nb) ^ 1u, w))) break;
@@ -473,6 +432,8 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     mma_commit_warp(bar(B_S_FULL + nb));
                     if (!(ok = mbar_wait_warp(bar(B_X_FREE), xfree_ph ^ 1u, w))) break;
                     xfree_ph ^= 1u;
+                    // V of the unit lands after K (its slot frees later)
+                    if (j == 0 && !(ok = mbar_wait_warp(bar(B_V_FULL + (ks ^ 1)), uph, w))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
@@ -487,7 +448,8 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     if (++nb == C::kSBuf) nb = 0;
                 }
                 if (!ok) break;
-                mma_commit_warp(bar(B_KV_EMPTY));
+                mma_commit_warp(bar(B_FREE_A));   // both slots' reads by this warp done
+                ++nu;
             }
             // every MMA this warp issued completes before tensor memory is freed
             // (also after an abort)
@@ -498,17 +460,19 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             // For step j (S buffer j%3, dS^T tile j%2): dV += P^T dO once P^T is
             // written back, dK += dS^T Q once dS^T is; then, after dV and dK have
             // finished reading the S buffer, dQ^T = K^T dS^T into that same buffer.
-            uint32_t kv_ph = 0, acc_ph = 0, p_ph = 0, ds_ph = 0, kd_ph = 0;   // p / ds: bit per buffer
+            uint32_t acc_ph = 0, p_ph = 0, ds_ph = 0, kd_ph = 0;   // p / ds: bit per buffer
             int c_stage = 0, cb = 0, db = 0;
             bool ok = true;
-            const uint64_t dK_mn = sw128_desc(sbase + C::OFF_K, BN * 128, 1024);
+            int nu = 0;   // units with work so far: K in slot nu % 2
             while (ok) {
                 const int t = next_unit();
                 if (t < 0) break;
                 const Unit u = decode_unit<BM>(p, t);
                 if (u.iters == 0) continue;
-                if (!(ok = mbar_wait_warp(bar(B_KV_FULL), kv_ph, w))) break;   // K for dQ
-                kv_ph ^= 1;
+                const int ks = nu & 1;
+                const uint64_t dK_mn = sw128_desc(sbase + C::OFF_K + ks * C::KV_BYTES, BN * 128, 1024);
+                // K for dQ
+                if (!(ok = mbar_wait_warp(bar(B_K_FULL + ks), (uint32_t)(nu >> 1) & 1u, w))) break;
                 for (int it = 0; it < u.iters; ++it) {
                     if (it == 0) {
                         if (!(ok = mbar_wait_warp(bar(B_ACC_EMPTY), acc_ph ^ 1, w))) break;
@@ -535,6 +499,9 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                         mma_ts_warp(tmem + C::TM_DK, tmem + C::ds_op(cb, kk), desc_add(dQ_mn, kk * 2048),
                                     C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
                     mma_commit_warp(bar(B_STAGE0 + S + c_stage));   // warp B's share of the stage
+                    // after the unit's last dK the accumulators are final: the
+                    // softmax warps write them out while dQ^T of the step runs
+                    if (it == u.iters - 1) mma_commit_warp(bar(B_ACC_FULL));
                     // dQ^T overwrites the P^T / dS^T that dV and dK read: wait for them
                     mma_commit_warp(bar(B_KDONE));
                     if (!(ok = mbar_wait_warp(bar(B_KDONE), kd_ph, w))) break;
@@ -557,8 +524,8 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     db ^= 1;
                 }
                 if (!ok) break;
-                mma_commit_warp(bar(B_ACC_FULL));
-                mma_commit_warp(bar(B_KV_EMPTY));
+                mma_commit_warp(bar(B_FREE_B));   // the K slot's reads by this warp done
+                ++nu;
             }
             mma_commit_warp(bar(B_DRAIN));
             mbar_wait_drain_warp(bar(B_DRAIN), 0, p.err, p.budget_ns);

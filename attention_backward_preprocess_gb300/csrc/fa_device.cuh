@@ -118,6 +118,17 @@ __device__ __forceinline__ void stmatrix_x4(uint32_t row_addr, uint32_t r0, uint
                  : "memory");
 }
 
+// The same four 8x8 matrices stored transposed: element (row t/4, column
+// 2(t%4) + e) of matrix i lands in row 2(t%4) + e, column t/4 of it; thread
+// t supplies the address of (transposed) row t%8 of matrix t/8.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t row_addr, uint32_t r0, uint32_t r1,
+                                                  uint32_t r2, uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(
+                     row_addr),
+                 "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+}
+
 // Shared-memory accesses by 32-bit shared-window address (base + immediate
 // offsets; no generic-address conversion).
 __device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {

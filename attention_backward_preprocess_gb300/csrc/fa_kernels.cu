@@ -80,10 +80,14 @@ __global__ void __launch_bounds__(1024) schedule_kernel(BwdParams p) {
 // keep one row per thread (4 was slower there).
 // Padding rows up to the next multiple of 128 get Dv = 0 and LSE2 = +inf (so
 // P = 0 there).  Every workspace row of the sequence has its dQ accumulator
-// zeroed, and in deterministic mode its semaphores as well.
-template <int D, typename T, int RPT>
+// zeroed, and in deterministic mode its semaphores as well.  DV is the tile
+// width of O / dO (the value side), DQ that of the accumulator (the query /
+// key side); each of the DV / 8 threads of a row zeroes DQ / (DV / 8) floats.
+template <int DQ, int DV, typename T, int RPT>
 __global__ void __launch_bounds__(256) preprocess_kernel(BwdParams p) {
-    constexpr int TPR = D / 8;   // threads per row
+    constexpr int TPR = DV / 8;   // threads per row
+    constexpr int ZF = DQ / TPR;  // accumulator floats each thread zeroes
+    static_assert(ZF % 4 == 0, "whole float4 stores");
     const int b = blockIdx.y;
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
         *p.err = 0;            // per-call error word
@@ -109,9 +113,9 @@ __global__ void __launch_bounds__(256) preprocess_kernel(BwdParams p) {
         acc[k] = 0.f;
         const long long row = r0 + k;
         const int s = (int)(row / p.Hq), h = (int)(row % p.Hq);
-        // O / dO rows hold Dh <= D columns (a multiple of 8): parts past Dh add 0
-        if (row < nrows && s < lq && part * 8 < p.Dh) {
-            const long long off = ((qbase + s) * p.Hq + h) * p.Dh + part * 8;
+        // O / dO rows hold Dhv <= DV columns (a multiple of 8): parts past Dhv add 0
+        if (row < nrows && s < lq && part * 8 < p.Dhv) {
+            const long long off = ((qbase + s) * p.Hq + h) * p.Dhv + part * 8;
             const uint4 ov = *reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.o) + off);
             const uint4 dv = *reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.dout) + off);
             const uint32_t oa[4] = {ov.x, ov.y, ov.z, ov.w}, da[4] = {dv.x, dv.y, dv.z, dv.w};
@@ -147,9 +151,9 @@ __global__ void __launch_bounds__(256) preprocess_kernel(BwdParams p) {
             p.lse2[wr] = l2;
             if (p.deterministic && (s % 64) == 0) p.sem[wr / 64] = 0;
         }
-        float4 *z = reinterpret_cast<float4 *>(p.dqacc + wr * D) + part * 2;
-        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 *z = reinterpret_cast<float4 *>(p.dqacc + wr * DQ + part * ZF);
+#pragma unroll
+        for (int c = 0; c < ZF / 4; ++c) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
 
@@ -208,12 +212,24 @@ static dim3 row_grid(const BwdParams &p, int lanes_per_row, int rows_per_seq, in
     return dim3((unsigned)((threads + 255) / 256), (unsigned)p.B, 1);
 }
 
-template <int D, typename T>
+template <int DQ, int DV, typename T>
 static void launch_pre_t(const BwdParams &p, cudaStream_t stream) {
     if (p.varlen)
-        preprocess_kernel<D, T, 4><<<row_grid(p, D / 8, p.sq_round, 4), 256, 0, stream>>>(p);
+        preprocess_kernel<DQ, DV, T, 4><<<row_grid(p, DV / 8, p.sq_round, 4), 256, 0, stream>>>(p);
     else
-        preprocess_kernel<D, T, 1><<<row_grid(p, D / 8, p.sq_round, 1), 256, 0, stream>>>(p);
+        preprocess_kernel<DQ, DV, T, 1><<<row_grid(p, DV / 8, p.sq_round, 1), 256, 0, stream>>>(p);
+}
+template <typename T>
+static cudaError_t launch_pre_dt(const BwdParams &p, cudaStream_t stream) {
+    // (accumulator, value) tile widths: one head dim of 64 or 128, or the
+    // wide kernel's 128 / 256 on either side
+    if (p.D == 64 && p.Dv == 64) launch_pre_t<64, 64, T>(p, stream);
+    else if (p.D == 128 && p.Dv == 128) launch_pre_t<128, 128, T>(p, stream);
+    else if (p.D == 256 && p.Dv == 256) launch_pre_t<256, 256, T>(p, stream);
+    else if (p.D == 256 && p.Dv == 128) launch_pre_t<256, 128, T>(p, stream);
+    else if (p.D == 128 && p.Dv == 256) launch_pre_t<128, 256, T>(p, stream);
+    else return cudaErrorInvalidValue;
+    return cudaGetLastError();
 }
 template <int D, typename T>
 static void launch_post_t(const BwdParams &p, cudaStream_t stream) {
@@ -224,18 +240,14 @@ static void launch_post_t(const BwdParams &p, cudaStream_t stream) {
 }
 
 cudaError_t launch_preprocess(const BwdParams &p, int bf16, cudaStream_t stream) {
-    if (p.D == 128) {
-        if (bf16) launch_pre_t<128, __nv_bfloat16>(p, stream);
-        else launch_pre_t<128, __half>(p, stream);
-    } else {
-        if (bf16) launch_pre_t<64, __nv_bfloat16>(p, stream);
-        else launch_pre_t<64, __half>(p, stream);
-    }
-    return cudaGetLastError();
+    return bf16 ? launch_pre_dt<__nv_bfloat16>(p, stream) : launch_pre_dt<__half>(p, stream);
 }
 
 cudaError_t launch_postprocess(const BwdParams &p, int bf16, cudaStream_t stream) {
-    if (p.D == 128) {
+    if (p.D == 256) {
+        if (bf16) launch_post_t<256, __nv_bfloat16>(p, stream);
+        else launch_post_t<256, __half>(p, stream);
+    } else if (p.D == 128) {
         if (bf16) launch_post_t<128, __nv_bfloat16>(p, stream);
         else launch_post_t<128, __half>(p, stream);
     } else {

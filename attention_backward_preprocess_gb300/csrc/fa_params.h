@@ -17,7 +17,9 @@ struct BwdParams {
     void *dq, *dk, *dv;
     int B, Sq, Sk, Hq, Hkv, D, G;
     int Dh;             // head dim of the tensors; D is the tile width it is padded to
-                        // (64 or 128: columns past Dh are zero in shared memory)
+                        // (64, 128 or 256: columns past Dh are zero in shared memory)
+    int Dv, Dhv;        // the value side (v, o, dout, dv): tile width and head dim
+                        // (equal to D / Dh unless the value head dim differs)
     float scale;        // c
     float scale_log2;   // c * log2(e)
     int causal, deterministic, varlen;

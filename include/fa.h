@@ -26,9 +26,17 @@
  * (seqlen, d, head, batch) shape with stride (int64, 1, int64, int64)):
  *   dense : q, o, dout, dq : [B, Sq, Hq, D];  k, v, dk, dv : [B, Sk, Hkv, D]
  *           lse : fp32 [B, Hq, Sq], natural log
- *   D is a multiple of 8 in [64, 128]; it runs at the tile width 64 (D = 64)
- *   or 128 (otherwise), the tensor-map loads filling the columns past D with
- *   zeros (the FlashAttention postprocess page pads the head dim likewise).
+ *   D is a multiple of 8 in [64, 256]; it runs at the tile width 64 (D = 64),
+ *   128 (D <= 128) or 256, the tensor-map loads filling the columns past D
+ *   with zeros (the FlashAttention postprocess page pads the head dim
+ *   likewise).  Head dims up to 128 run in the main kernel (64 queries x 128
+ *   keys per step); above 128, and for a value head dim different from D
+ *   (fa_ext head_dim_v: v, o, dout, dv then have Dv columns), in a second
+ *   kernel that produces dK / dV / dQ in 128-column halves (32 queries x 128
+ *   keys per step, S and dP recomputed per half).  That kernel has the causal
+ *   mask, an upper band edge, varlen and used lengths, but not the lower
+ *   band edge, ALiBi, the bias, dropout or the deterministic order
+ *   (FA_ERR_UNSUPPORTED), and the forward does not run these head dims yet.
  *   varlen: cu_seqlens_q / cu_seqlens_k != NULL (both or neither): int32
  *           device arrays of B+1 prefix sums; tensors packed [total, H, D];
  *           lse fp32 [Hq, total_q]; Sq / Sk are the MAXIMUM lengths.  A
@@ -70,8 +78,8 @@ extern "C" {
 typedef enum {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misalignment, bad scale */
-    FA_ERR_UNSUPPORTED = 2,  /* head dim not a multiple of 8 in [64, 128], dtype, or GPU
-                                not sm_103 */
+    FA_ERR_UNSUPPORTED = 2,  /* head dims without a kernel (see the layouts above),
+                                dtype, or GPU not sm_103 */
     FA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
     FA_ERR_TIMEOUT = 4,      /* a bounded device-side wait ran out */
     FA_ERR_SCRATCH_LIMIT = 5 /* fa_bwd_noalloc: the problem needs more scratch than
@@ -217,7 +225,10 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
  *   reads them instead of running Philox again (in deterministic mode the
  *   results are bit-identical to drawing the mask).  The buffer must hold
  *   B * Hq * Sq * W words (Hq * total_q * W with cu_seqlens). */
-/* total_q / total_k (varlen only; both 0 = not given): the packed row counts
+/* head_dim_v (0 = equal to D): the value head dim Dv of v, o, dout and dv
+ *   (kVHeaddim next to kQKHeaddim in the Composable Kernel page's problem
+ *   traits); a multiple of 8 in [8, 256], with D > 64 when it differs from D.
+ * total_q / total_k (varlen only; both 0 = not given): the packed row counts
  *   cu_seqlens_q[B] and cu_seqlens_k[B], which the tensor maps are built
  *   for.  Given, the call needs no read-back of cu_seqlens and does not
  *   synchronise the stream.  They must equal cu_seqlens[B] and be at most
@@ -244,6 +255,7 @@ typedef struct {
     unsigned int *dropout_mask;
     long long total_q;
     long long total_k;
+    int head_dim_v;
 } fa_ext;
 
 /* fa_fwd with extensions.  Errors as fa_fwd, plus FA_ERR_INVALID_ARG for a

@@ -79,7 +79,7 @@ def _call_with_ws(fa, **over):
 
 @pytest.mark.parametrize("over,status", [
     (dict(q=0), 1), (dict(dv=0), 1), (dict(B=0), 1), (dict(Sq=-1), 1), (dict(Hq=3), 1),
-    (dict(D=100), 2), (dict(D=256), 2), (dict(D=32), 2), (dict(dtype=7), 2),
+    (dict(D=100), 2), (dict(D=264), 2), (dict(D=32), 2), (dict(dtype=7), 2),
     (dict(scale=0.0), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
     (dict(q=0x1008), 1), (dict(lse=0x6004), 1), (dict(ws=0x100010), 1), (dict(ws=0), 1),
     (dict(ws_bytes=16), 1), (dict(cu_q=0xA000), 1),
@@ -240,6 +240,43 @@ def test_workspace_sync_layout(fa, varlen, det):
         assert sync["sem"] + 4 * sync["n_sem"] <= total
     else:
         assert sync["sem"] == 0 and sync["n_sem"] == 0
+
+
+# head dims: (D, Dv (0 = D), extension overrides, deterministic) -> status on the host
+HEAD_DIMS = [
+    ((264, 0), {}, 0, 2),          # D above 256
+    ((56, 0), {}, 0, 2),           # D below 64
+    ((100, 0), {}, 0, 2),          # not a multiple of 8
+    ((64, 128), {}, 0, 2),         # Dv != D needs D > 64
+    ((128, 4), {}, 0, 2),          # Dv below 8
+    ((128, 260), {}, 0, 2),        # Dv above 256
+    ((192, 0), {}, 1, 2),          # wide kernel: no deterministic order
+    ((192, 0), dict(window_left=8), 0, 2),
+    ((128, 96), dict(dropout_p=0.1), 0, 2),
+    ((192, 0), dict(alibi_slopes=0x2000), 0, 2),
+]
+
+
+@pytest.mark.parametrize("dims,over,det,status", HEAD_DIMS,
+                         ids=[str(i) for i in range(len(HEAD_DIMS))])
+def test_head_dims_refused_on_the_host(fa, dims, over, det, status):
+    L = fa.lib()
+    vp = ctypes.c_void_p
+    ptrs = [vp(0x1000 * (i + 1)) for i in range(9)]
+    D, Dv = dims
+    e = _fa_ext(fa, dict(over, head_dim_v=Dv))
+    shape = (1, 128, 128, 2, 2, D)
+    assert L.fa_bwd_ext(*ptrs, *shape, 0.125, 1, None, None, ctypes.byref(e), det, 0,
+                        vp(0x100000), ctypes.c_size_t(1 << 40), None) == status
+
+
+def test_wide_head_dim_workspace(fa):
+    """The dQ accumulator runs at the tile width of D: 256 above 128."""
+    for D, width in ((192, 256), (256, 256), (136, 256), (128, 128), (64, 64)):
+        lay = fa.workspace_layout(1, 128, 128, 2, 2, D)
+        n = fa.workspace_bytes(1, 128, 128, 2, 2, D)
+        assert n >= 4 * (lay["dqacc"] + lay["rows"] * width)
+        assert n < 4 * (lay["dqacc"] + lay["rows"] * width) + 4096
 
 
 def test_bias_with_varlen_is_unsupported(fa):
