@@ -22,6 +22,7 @@ cudaError_t launch_fwd_tc(const BwdParams &p, const CUtensorMap &q, const CUtens
                           const CUtensorMap &v, void *o, float *lse, int max_lq, int bf16,
                           cudaStream_t stream);
 int fwd_block_m();
+int fwd_block_n(int Dq_tile, int Dv_tile);
 int *fwd_error_word();
 cudaError_t launch_bwd_main(const BwdParams &p, const CUtensorMap &q, const CUtensorMap &k,
                             const CUtensorMap &v, const CUtensorMap &dout, int bf16, int grid,
@@ -664,7 +665,6 @@ fa_status fa_fwd_ext(const void *q, const void *k, const void *v, void *o, float
     p.cu_k = cu_seqlens_k;
     if ((st = apply_ext(p, causal, ext)) != FA_OK) return st;
     if ((st = check_ext_totals(ext, p.varlen, B, Sq, Sk)) != FA_OK) return st;
-    if (wide_dims(p.Dh, p.Dhv)) return FA_ERR_UNSUPPORTED;   // no forward kernel for these yet
     if ((st = check_device()) != FA_OK) return st;
     p.err = fa::fwd_error_word();
     if (!p.err) return FA_ERR_CUDA;
@@ -682,9 +682,10 @@ fa_status fa_fwd_ext(const void *q, const void *k, const void *v, void *o, float
     const int bf16 = dtype == FA_BF16;
     const int nb = p.varlen ? 1 : B;
     CUtensorMap mq, mk, mv;
+    const int bn = fa::fwd_block_n(p.D, p.Dv);
     if (!encode_rows_map(&mq, q, D, Hq, rq, nb, fa::fwd_block_m(), bf16) ||
-        !encode_rows_map(&mk, k, D, Hkv, rk, nb, fa::kBlockN, bf16) ||
-        !encode_rows_map(&mv, v, D, Hkv, rk, nb, fa::kBlockN, bf16))
+        !encode_rows_map(&mk, k, D, Hkv, rk, nb, bn, bf16) ||
+        !encode_rows_map(&mv, v, p.Dhv, Hkv, rk, nb, bn, bf16))
         return FA_ERR_CUDA;
     return cuda_status(fa::launch_fwd_tc(p, mq, mk, mv, o, lse, Sq, bf16, stream));
 }

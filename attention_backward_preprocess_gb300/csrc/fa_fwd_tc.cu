@@ -29,26 +29,35 @@
 namespace fa {
 namespace {
 
-template <int kD, typename T>
+// kDQ / kDV: tile widths of the query / key side and of the value side (128
+// or 256; 128 and 128 for one head dim of at most 128), kBN keys per block
+// (128; 64 when a side is 256 wide, so that the K / V ring still has two or
+// three slots next to the 64 KB Q tile).
+template <int kDQ, int kDV, int kBN, typename T>
 struct FwdCfg {
-    static constexpr int D = kD;
+    static constexpr int DQ = kDQ, DV = kDV;
     static constexpr int BM = 128;                 // queries per CTA
-    static constexpr int BN = 128;                 // keys per block
-    static constexpr int kStages = (kD == 128) ? 3 : 4;
+    static constexpr int BN = kBN;                 // keys per block
     static constexpr int kThreads = 8 * 32;
     static constexpr int W_SM = 4;                 // first softmax warp
-    // TMEM: S buffer x2 (BN columns each; P overwrites the first BN/2) | O (D)
+    // TMEM: S buffer x2 (BN columns each; P overwrites the first BN/2) | O (DV)
     static constexpr int TM_S = 0;
     static constexpr int TM_O = 2 * BN;
     static constexpr int TM_COLS = 512;
-    static_assert(TM_O + D <= TM_COLS, "TMEM overflow");
+    static_assert(TM_O + DV <= TM_COLS, "TMEM overflow");
     // shared memory
-    static constexpr int Q_BYTES = BM * D * 2;
-    static constexpr int KV_BYTES = BN * D * 2;
+    static constexpr int Q_BYTES = BM * DQ * 2;
+    static constexpr int K_BYTES = BN * DQ * 2;
+    static constexpr int V_BYTES = BN * DV * 2;
+    // ring slots: as many as fit next to the barriers, the misc words and the
+    // alignment slack, at most four
+    static constexpr int kFixed = 16 * 8 + 32 + 1024;
+    static constexpr int kStages = (Q_BYTES + 4 * (K_BYTES + V_BYTES) + kFixed <= 232448) ? 4
+                                   : (Q_BYTES + 3 * (K_BYTES + V_BYTES) + kFixed <= 232448) ? 3 : 2;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + Q_BYTES;
-    static constexpr int OFF_V = OFF_K + kStages * KV_BYTES;
-    static constexpr int OFF_BAR = OFF_V + kStages * KV_BYTES;
+    static constexpr int OFF_V = OFF_K + kStages * K_BYTES;
+    static constexpr int OFF_BAR = OFF_V + kStages * V_BYTES;
     static constexpr int NUM_BARS = 16;
     static constexpr int kv_empty(int st) { return 8 + kStages + st; }
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // TMEM slot, abort flag
@@ -58,7 +67,7 @@ struct FwdCfg {
     // one CTA per SM: the CTA takes all 512 TMEM columns
     static_assert(2 * (SMEM_BYTES + 1024) > 233472, "two CTAs would share an SM");
     static constexpr uint32_t IDESC_S = make_idesc(128, BN, Cvt<T>::is_bf16, false, false);
-    static constexpr uint32_t IDESC_PV = make_idesc(128, D, Cvt<T>::is_bf16, false, true);
+    static constexpr uint32_t IDESC_PV = make_idesc(128, DV, Cvt<T>::is_bf16, false, true);
 };
 
 enum {
@@ -74,13 +83,13 @@ enum {
 // that may lag the true one by up to this much.
 constexpr float kRescaleLog2 = 8.f;
 
-template <int kD, typename T, int kFlags>
-__global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
+template <int kDQ, int kDV, int kBN, typename T, int kFlags>
+__global__ void __launch_bounds__(FwdCfg<kDQ, kDV, kBN, T>::kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap map_q,
                   const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                   void *o_out, float *lse_out, int nmb) {
-    using C = FwdCfg<kD, T>;
-    constexpr int D = C::D, BM = C::BM, BN = C::BN, S = C::kStages;
+    using C = FwdCfg<kDQ, kDV, kBN, T>;
+    constexpr int DQ = C::DQ, DV = C::DV, BM = C::BM, BN = C::BN, S = C::kStages;
     static_assert((kFlags & (kFwdBias | kFwdDrop)) == 0,
                   "the bias and dropout instances run in fa_fwd_split.cu");
     constexpr bool kAlibi = (kFlags & kFwdAlibi) != 0;
@@ -152,7 +161,7 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
         if (lane == 0 && nblk > 0) {
             mbar_arrive_expect_tx(bar(F_Q_FULL), C::Q_BYTES);
 #pragma unroll
-            for (int hh = 0; hh < D / 64; ++hh)
+            for (int hh = 0; hh < DQ / 64; ++hh)
                 tma_load_4d(sbase + C::OFF_Q + hh * BM * 128, &map_q, bar(F_Q_FULL), hh * 64, h,
                             q0 + m * BM, bidx);
             uint32_t empty_ph = 0;
@@ -164,15 +173,16 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                     empty_ph ^= 1u << st;
                 }
                 const uint32_t full = bar(F_KV_FULL + st);
-                mbar_arrive_expect_tx(full, 2 * C::KV_BYTES);
+                mbar_arrive_expect_tx(full, C::K_BYTES + C::V_BYTES);
                 armed = n;
 #pragma unroll
-                for (int hh = 0; hh < D / 64; ++hh) {
-                    tma_load_4d(sbase + C::OFF_K + st * C::KV_BYTES + hh * BN * 128, &map_k, full,
+                for (int hh = 0; hh < DQ / 64; ++hh)
+                    tma_load_4d(sbase + C::OFF_K + st * C::K_BYTES + hh * BN * 128, &map_k, full,
                                 hh * 64, hk, k0 + (n_begin + n) * BN, bidx);
-                    tma_load_4d(sbase + C::OFF_V + st * C::KV_BYTES + hh * BN * 128, &map_v, full,
+#pragma unroll
+                for (int hh = 0; hh < DV / 64; ++hh)
+                    tma_load_4d(sbase + C::OFF_V + st * C::V_BYTES + hh * BN * 128, &map_v, full,
                                 hh * 64, hk, k0 + (n_begin + n) * BN, bidx);
-                }
             }
             // wind-down: no K/V load may land after the CTA exits (after an
             // abort its consumers may not have waited for it).  The Q load needs
@@ -197,7 +207,7 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                 tc_fence_after();
                 // O += P V: P (queries x keys) from TMEM, V (keys x d) MN-major,
                 // K step = 16 keys = 2048 bytes of the swizzled tile
-                const uint64_t dV_mn = sw128_desc(sbase + C::OFF_V + st * C::KV_BYTES, BN * 128, 1024);
+                const uint64_t dV_mn = sw128_desc(sbase + C::OFF_V + st * C::V_BYTES, BN * 128, 1024);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
                     mma_ts_warp(tmem + C::TM_O, tmem + C::TM_S + bb * BN + 8 * kk,
@@ -214,9 +224,9 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                 if (n >= 2 && !(ok = mbar_wait_warp(bar(F_PV_DONE + bb), (uint32_t)((n - 2) >> 1) & 1u, w)))
                     break;
                 tc_fence_after();
-                const uint64_t dK_k = sw128_desc(sbase + C::OFF_K + st * C::KV_BYTES, 16, 1024);
+                const uint64_t dK_k = sw128_desc(sbase + C::OFF_K + st * C::K_BYTES, 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
+                for (int kk = 0; kk < DQ / 16; ++kk) {
                     const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
                     const uint32_t qo = (kk / 4) * (BM * 128) + (kk % 4) * 32;
                     mma_ss_warp(tmem + C::TM_S + bb * BN, desc_add(dQ_k, qo), desc_add(dK_k, ko),
@@ -370,7 +380,7 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                     break;
                 tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < DV / 32; ++c) {
                     uint32_t orr[32];
                     tmem_ld32(lane_addr + C::TM_O + 32 * c, orr);
                     tmem_wait_ld();
@@ -405,9 +415,9 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                 *lse_dst = l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
             }
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            T *dst = reinterpret_cast<T *>(o_out) + (row * p.Hq + h) * p.Dh;   // Dh <= D columns
+            T *dst = reinterpret_cast<T *>(o_out) + (row * p.Hq + h) * p.Dhv;   // Dhv <= DV columns
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < DV / 32; ++c) {
                 uint32_t orr[32];
                 if (nblk > 0) {
                     tmem_ld32(lane_addr + C::TM_O + 32 * c, orr);
@@ -424,7 +434,7 @@ __global__ void __launch_bounds__(FwdCfg<kD, T>::kThreads, 1)
                                              __uint_as_float(orr[2 * i + 1]) * inv);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        if (32 * c + 8 * i < p.Dh)
+                        if (32 * c + 8 * i < p.Dhv)
                             reinterpret_cast<uint4 *>(dst + 32 * c)[i] =
                                 make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                 }
@@ -451,15 +461,14 @@ FwdKernel fwd_kernel_for(int need) {
     if constexpr (fwd_split(kD, f))
         return nullptr;
     else
-        return fwd_tc_kernel<kD, T, f>;
+        return fwd_tc_kernel<kD, kD, 128, T, f>;
 }
 
-template <int kD, typename T>
-cudaError_t launch_fwd_tc_t(const BwdParams &p, const CUtensorMap &mq, const CUtensorMap &mk,
-                            const CUtensorMap &mv, void *o, float *lse, int max_lq, int need,
-                            cudaStream_t stream) {
-    using C = FwdCfg<kD, T>;
-    FwdKernel kern = fwd_kernel_for<kD, T>(need);
+template <int kDQ, int kDV, int kBN, typename T>
+cudaError_t launch_fwd_cfg(FwdKernel kern, const BwdParams &p, const CUtensorMap &mq,
+                           const CUtensorMap &mk, const CUtensorMap &mv, void *o, float *lse,
+                           int max_lq, cudaStream_t stream) {
+    using C = FwdCfg<kDQ, kDV, kBN, T>;
     if (kern == nullptr) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
@@ -472,6 +481,35 @@ cudaError_t launch_fwd_tc_t(const BwdParams &p, const CUtensorMap &mq, const CUt
     return cudaGetLastError();
 }
 
+template <int kD, typename T>
+cudaError_t launch_fwd_tc_t(const BwdParams &p, const CUtensorMap &mq, const CUtensorMap &mk,
+                            const CUtensorMap &mv, void *o, float *lse, int max_lq, int need,
+                            cudaStream_t stream) {
+    return launch_fwd_cfg<kD, kD, 128, T>(fwd_kernel_for<kD, T>(need), p, mq, mk, mv, o, lse,
+                                          max_lq, stream);
+}
+
+// Wide or unequal head dims (plain mask only): 64 keys per block when a side
+// is 256 wide, else the 128-key block of the plain D = 128 instance.
+template <typename T>
+cudaError_t launch_fwd_wide_t(const BwdParams &p, const CUtensorMap &mq, const CUtensorMap &mk,
+                              const CUtensorMap &mv, void *o, float *lse, int max_lq,
+                              cudaStream_t stream) {
+    if (p.D == 256 && p.Dv == 256)
+        return launch_fwd_cfg<256, 256, 64, T>(fwd_tc_kernel<256, 256, 64, T, 0>, p, mq, mk, mv, o, lse,
+                                               max_lq, stream);
+    if (p.D == 256 && p.Dv == 128)
+        return launch_fwd_cfg<256, 128, 64, T>(fwd_tc_kernel<256, 128, 64, T, 0>, p, mq, mk, mv, o, lse,
+                                               max_lq, stream);
+    if (p.D == 128 && p.Dv == 256)
+        return launch_fwd_cfg<128, 256, 64, T>(fwd_tc_kernel<128, 256, 64, T, 0>, p, mq, mk, mv, o, lse,
+                                               max_lq, stream);
+    if (p.D == 128 && p.Dv == 128)
+        return launch_fwd_cfg<128, 128, 128, T>(fwd_tc_kernel<128, 128, 128, T, 0>, p, mq, mk, mv, o,
+                                                lse, max_lq, stream);
+    return cudaErrorInvalidValue;
+}
+
 // Error word of the forward pass (its bounded waits record timeouts here).
 __device__ int g_fwd_err;
 
@@ -482,12 +520,17 @@ int *fwd_error_word() {
     return cudaGetSymbolAddress(&ptr, g_fwd_err) == cudaSuccess ? static_cast<int *>(ptr) : nullptr;
 }
 
-// Query rows of one TMA box for Q in the forward pass.
-int fwd_block_m() { return FwdCfg<128, __nv_bfloat16>::BM; }
+// Query rows of one TMA box for Q in the forward pass, and key rows of one box
+// for K / V (tile widths of the two sides).
+int fwd_block_m() { return FwdCfg<128, 128, 128, __nv_bfloat16>::BM; }
+int fwd_block_n(int Dq_tile, int Dv_tile) { return (Dq_tile > 128 || Dv_tile > 128) ? 64 : 128; }
 
 cudaError_t launch_fwd_tc(const BwdParams &p, const CUtensorMap &q, const CUtensorMap &k,
                           const CUtensorMap &v, void *o, float *lse, int max_lq, int bf16,
                           cudaStream_t stream) {
+    if (p.D != p.Dv || p.D > 128 || p.Dh != p.Dhv)   // wide or unequal head dims
+        return bf16 ? launch_fwd_wide_t<__nv_bfloat16>(p, q, k, v, o, lse, max_lq, stream)
+                    : launch_fwd_wide_t<__half>(p, q, k, v, o, lse, max_lq, stream);
     const int need = (p.alibi ? kFwdAlibi : 0) | (p.bias ? kFwdBias : 0) | (p.drop_t > 0 ? kFwdDrop : 0);
     const int f = fwd_instance_flags(need);
     if (fwd_split(p.D, f)) return launch_fwd_split(p, q, k, v, o, lse, max_lq, bf16, f, stream);

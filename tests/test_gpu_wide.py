@@ -126,5 +126,44 @@ def test_wide_refusals(fa, oracle_mod, cuda_device):
             fa.fa_bwd(*args, causal=True, **kw)
         assert e.value.status == fa.FA_ERR_UNSUPPORTED
     with pytest.raises(fa.FaError) as e:
-        fa.fa_fwd(g["q"], g["k"], g["v"], causal=True)
+        fa.fa_fwd(g["q"], g["k"], g["v"], causal=True, window=(16, -1))
     assert e.value.status == fa.FA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "b%d_sq%d_sk%d_hq%d_hkv%d_d%d_dv%d_%s%s" % (
+    c[0], c[1], c[2], c[3], c[4], c[5], c[6], "bf16" if c[7] == torch.bfloat16 else "fp16",
+    "_causal" if c[8] else ""))
+def test_wide_forward_matches_oracle(fa, oracle_mod, cuda_device, case):
+    B, Sq, Sk, Hq, Hkv, D, Dv, dtype, causal = case
+    x = make_case(oracle_mod, B, Sq, Sk, Hq, Hkv, D, Dv, dtype, causal, seed=D + Dv + Sq)
+    o, lse = fa.fa_fwd(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), causal=causal,
+                       softmax_scale=x["scale"])
+    torch.cuda.synchronize()
+    assert fa.device_status() == fa.FA_OK
+    assert o.shape[-1] == Dv
+    check_bar(o, to64(x["o"]), "o")
+    lg, lr = to64(lse), to64(x["lse"])
+    assert np.array_equal(np.isneginf(lg), np.isneginf(lr))
+    fin = np.isfinite(lr)
+    assert np.max(np.abs(lg[fin] - lr[fin])) < 1e-4
+
+
+@pytest.mark.parametrize("D,Dv", [(256, 256), (192, 128)])
+def test_wide_varlen_forward_then_backward(fa, oracle_mod, cuda_device, D, Dv):
+    """The library's forward feeds its backward (as a training step does):
+    both against the oracle's fp64 forward and backward on the same inputs."""
+    x = make_case(oracle_mod, 3, 0, 0, 4, 2, D, Dv, torch.bfloat16, True, lengths=[200, 77, 131],
+                  seed=9)
+    cu = torch.from_numpy(x["cu"]).cuda()
+    vl = dict(cu_seqlens_q=cu, cu_seqlens_k=cu, max_seqlen_q=x["max_len"], max_seqlen_k=x["max_len"])
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "dout"))
+    o, lse = fa.fa_fwd(q, k, v, causal=True, softmax_scale=x["scale"], **vl)
+    torch.cuda.synchronize()
+    check_bar(o, to64(x["o"]), "o")
+    dq, dk, dv = fa.fa_bwd(q, k, v, o, do, lse, causal=True, softmax_scale=x["scale"], **vl)
+    torch.cuda.synchronize()
+    rq, rk, rv = oracle_mod.backward(to64(x["q"]), to64(x["k"]), to64(x["v"]), to64(x["dout"]),
+                                     x["scale"], True, cu_q=x["cu"], cu_k=x["cu"])
+    check_bar(dq, rq, "dq")
+    check_bar(dk, rk, "dk")
+    check_bar(dv, rv, "dv")
