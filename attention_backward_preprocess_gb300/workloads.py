@@ -35,6 +35,11 @@ class Workload:
     vdo_dist: tuple = ("normal", 1.0)
     varlen: Optional[tuple] = None     # (nseq, lo, hi): lengths uniform in [lo, hi]
     seed: int = 0
+    Dv: Optional[int] = None           # value head dim (v, o, dout, dv); None -> D
+
+    @property
+    def value_dim(self) -> int:
+        return self.D if self.Dv is None else self.Dv
 
     @property
     def softmax_scale(self) -> float:
@@ -106,17 +111,19 @@ def generate(w: Workload, device="cpu", seed: Optional[int] = None) -> dict:
             cu.append(cu[-1] + L)
         total = cu[-1]
         qshape, kshape = (total, w.Hq, w.D), (total, w.Hkv, w.D)
+        oshape, vshape = (total, w.Hq, w.value_dim), (total, w.Hkv, w.value_dim)
         out["lengths"] = lengths
         out["max_len"] = max(lengths)
         out["cu_q"] = torch.tensor(cu, dtype=torch.int32, device=device)
         out["cu_k"] = out["cu_q"].clone()
     else:
         qshape, kshape = (w.B, w.Sq, w.Hq, w.D), (w.B, w.Sk, w.Hkv, w.D)
+        oshape, vshape = (w.B, w.Sq, w.Hq, w.value_dim), (w.B, w.Sk, w.Hkv, w.value_dim)
     dt = w.torch_dtype
     out["q"] = _draw(qshape, w.qk_dist, gen, device).to(dt)
     out["k"] = _draw(kshape, w.qk_dist, gen, device).to(dt)
-    out["v"] = _draw(kshape, w.vdo_dist, gen, device).to(dt)
-    out["dout"] = _draw(qshape, w.vdo_dist, gen, device).to(dt)
+    out["v"] = _draw(vshape, w.vdo_dist, gen, device).to(dt)
+    out["dout"] = _draw(oshape, w.vdo_dist, gen, device).to(dt)
     return out
 
 
@@ -133,5 +140,7 @@ def attention_pairs(w: Workload, lengths=None) -> float:
 
 
 def bwd_flops(w: Workload, lengths=None) -> float:
-    """Algorithmic FLOPs of one backward pass: 10 * pairs * D (five GEMMs)."""
-    return 10.0 * attention_pairs(w, lengths) * w.D
+    """Algorithmic FLOPs of one backward pass: five GEMMs of 2 FLOPs per pair
+    and head-dim column each -- S and dQ, dK over D, dP and dV over Dv:
+    (6 D + 4 Dv) per pair, 10 D per pair when Dv = D."""
+    return attention_pairs(w, lengths) * (6.0 * w.D + 4.0 * w.value_dim)

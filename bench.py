@@ -190,6 +190,7 @@ def run_reference(args, w):
 def config_of(w, lengths=None, flushed=False):
     c = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk,
          "D": w.D, "causal": w.causal, "deterministic": w.deterministic,
+         **({} if w.Dv is None else {"Dv": w.Dv}),
          "l2": ("L2 written over (256 MB) between timed steps" if flushed
                 else "inputs larger than L2 (no flush)"),
          "parallelism": "replicas"}
@@ -217,11 +218,20 @@ def main():
     ap.add_argument("--dropout", type=float, default=0.0, help="dropout probability")
     ap.add_argument("--dropout-mask", action="store_true",
                     help="with --dropout: the forward stores the keep flags, the backward reads them")
+    ap.add_argument("--head-dim", type=int, default=None,
+                    help="query / key head dim other than the workload's (up to 256)")
+    ap.add_argument("--head-dim-v", type=int, default=None,
+                    help="value head dim other than the query / key one (one fa_bwd call per step)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     from attention_backward_preprocess_gb300.workloads import BENCH_WORKLOAD, WORKLOADS
     w = WORKLOADS[args.workload or BENCH_WORKLOAD]
+    if args.head_dim or args.head_dim_v:
+        D = args.head_dim or w.D
+        Dv = args.head_dim_v if args.head_dim_v and args.head_dim_v != D else None
+        w = w.with_(name="%s_dqk%d%s" % (w.name, D, "" if Dv is None else "_dv%d" % Dv), D=D, Dv=Dv,
+                    scale=w.softmax_scale if w.scale is not None else None)
     if args.impl == "reference":
         return run_reference(args, w)
     if args.window or args.alibi or args.bias or args.dropout > 0:
@@ -264,6 +274,12 @@ def main():
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if in_bytes < (256 << 20) else None
 
     def step():
+        if w.Dv is not None:
+            # the stage calls carry no value head dim: one whole call per step
+            e1.record(stream)
+            fa.fa_bwd(q, k, v, o, do, lse, workspace=work, **kw)
+            e2.record(stream)
+            return
         fa.fa_bwd_stages(q, k, v, o, do, lse, work, stages=("pre",), **kw)
         e1.record(stream)
         fa.fa_bwd_stages(q, k, v, o, do, lse, work, stages=("main",), **kw)
@@ -386,8 +402,9 @@ def main():
     achieved = flops / (main_avg * 1e-3) / 1e12
     tokens_q = q.shape[0] if varlen else w.B * w.Sq
     elems_q = tokens_q * w.Hq * w.D
+    elems_o = tokens_q * w.Hq * w.value_dim
     rows = tokens_q * w.Hq
-    pre_bytes = 2 * elems_q * 2 + rows * 4 * 2 + rows * 4 + elems_q * 4    # O, dO in; LSE in; Dv, LSE2 out; dQaccum zero
+    pre_bytes = 2 * elems_o * 2 + rows * 4 * 2 + rows * 4 + elems_q * 4    # O, dO in; LSE in; Dv, LSE2 out; dQaccum zero
     post_bytes = elems_q * 4 + elems_q * 2
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "main_kernel_traffic.json")
@@ -402,17 +419,19 @@ def main():
         "data": "synthetic (seeded N(0,1), torch.Generator on device)",
         "config": config_of(w, x.get("lengths"), flush is not None),
         "pct_of_bf16_peak": 100.0 * value / ws / pk["bf16"],
-        "roofline": {"kernel": "bwd_main_kernel", "bound": "tensor", "achieved": achieved,
+        "roofline": {"kernel": "bwd_main_kernel" if (w.D <= 128 and w.Dv is None) else "bwd_wide_kernel",
+                     "bound": "tensor", "achieved": achieved,
                      "peak": pk["bf16"], "unit": "TFLOP/s", "frac": achieved / pk["bf16"],
                      "traffic": traffic,
                      "peak_note": "%s dense bf16 burst (bf16_tflops); sustained %s" % (
                          pk["source"], pk["bf16_sustained"]),
                      "algorithmic_flop_per_launch": flops},
-        "kernels_ms": {"preprocess": statistics.mean(pre_ms), "main": main_avg,
-                       "postprocess": statistics.mean(post_ms)},
-        "kernels_gbs": {"preprocess": pre_bytes / (statistics.mean(pre_ms) * 1e-3) / 1e9,
-                        "postprocess": post_bytes / (statistics.mean(post_ms) * 1e-3) / 1e9,
-                        "hbm_peak": pk["hbm"]},
+        "kernels_ms": ({"preprocess": statistics.mean(pre_ms), "main": main_avg,
+                        "postprocess": statistics.mean(post_ms)} if w.Dv is None
+                       else {"whole_call": main_avg}),
+        "kernels_gbs": ({"preprocess": pre_bytes / (statistics.mean(pre_ms) * 1e-3) / 1e9,
+                         "postprocess": post_bytes / (statistics.mean(post_ms) * 1e-3) / 1e9,
+                         "hbm_peak": pk["hbm"]} if w.Dv is None else None),
         # preprocess, main, postprocess (+ the varlen work-unit scheduler)
         "gpu_launches": (4 if varlen else 3) * args.steps,
         "device_status": status,
