@@ -84,8 +84,11 @@ def dist_env():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 50 ms while running."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks / throttle reasons, sampled every 10 ms from start()
+    (before the warm-up, since the tool takes a while to come up) to stop();
+    stop(window) keeps the samples whose timestamps fall inside the host-clock
+    window of the timed region."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -96,12 +99,22 @@ class ClockSampler:
             self.fh = open(path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-i", str(device_index), "-lms", "50"], stdout=self.fh,
+                 "-i", str(device_index), "-lms", "10"], stdout=self.fh,
                 stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def stop(self):
+    @staticmethod
+    def _seconds(stamp):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(stamp, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
+    def stop(self, window=None):
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -110,24 +123,28 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        sm, smax, reasons = [], [], set()
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                rows.append((self._seconds(parts[0]), float(parts[2]), float(parts[3]),
+                             [n for n, v in zip(names, parts[6:10]) if v.lower() == "active"]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        scope = "whole run"
+        if window is not None:
+            inside = [r for r in rows if r[0] is not None and window[0] <= r[0] <= window[1]]
+            if inside:
+                rows, scope = inside, "timed region"
+        if not rows:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        sm = [r[1] for r in rows]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[2] for r in rows),
+                "reasons": sorted({n for r in rows for n in r[3]}), "samples": len(rows),
+                "scope": scope}
 
 
 def cpu_baseline(w, inputs_cpu, prefix: int):
@@ -288,6 +305,7 @@ def main():
 
     e1 = torch.cuda.Event(enable_timing=True)
     e2 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index, clock_log_path("bench_clocks"))
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -298,11 +316,11 @@ def main():
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
-    clocks = ClockSampler(dev.index, clock_log_path("bench_clocks"))
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     barrier()
+    t_host0 = time.time()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
@@ -316,7 +334,7 @@ def main():
         d.record(stream)
     end.record(stream)
     barrier()
-    clk = clocks.stop()
+    clk = clocks.stop((t_host0, time.time()))
     total_ms = start.elapsed_time(end)
     if flush is not None:   # steps only, without the L2 overwrite between them
         total_ms = sum(ev[i][0].elapsed_time(ev[i][3]) for i in range(args.steps))
