@@ -587,7 +587,7 @@ def run_ext(args, w):
 def source_hash():
     import hashlib
     h = hashlib.sha256()
-    for f in ("fa_bwd_main.cu", "fa_device.cuh", "fa_params.h"):
+    for f in ("fa_bwd_main.cu", "fa_bwd_units.cuh", "fa_device.cuh", "fa_params.h"):
         h.update(open(os.path.join(ROOT, "attention_backward_preprocess_gb300", "csrc", f),
                       "rb").read())
     return h.hexdigest()[:16]
