@@ -215,6 +215,9 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                    kBias = (kFlags & kFBias) != 0, kDrop = (kFlags & kFDrop) != 0;
     // ALiBi with no visible key right of the diagonal: -slope |d| = slope d
     constexpr bool kAlibiLin = kAlibi && (kFlags & kFAbs) == 0;
+    // two 32-query chunks per softmax warp (D = 64): the two 16-lane halves of
+    // a TMEM tile are loaded one after the other (register pressure)
+    constexpr bool kSplitH = NCH == 2;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -638,8 +641,9 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                             if (npend == kRelBatch) {   // all adds of the batch complete: count them
                                 bulk_wait_all();
                                 fence_async_global();
+                                fence_acq_rel_gpu();     // one release fence for the batch
 #pragma unroll
-                                for (int i = 0; i < kRelBatch; ++i) red_release_add_gpu(pend[i], 1);
+                                for (int i = 0; i < kRelBatch; ++i) red_relaxed_add_gpu(pend[i], 1);
                                 npend = 0;
                             }
                         }
@@ -974,9 +978,13 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 __syncwarp();
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch) {
+                    // Two 32-query chunks per warp (D = 64, kSplitH): each 16-lane
+                    // half of S^T is loaded when it is processed, so that the
+                    // registers of one half are free again for the other (the
+                    // chunk's P stays live into the dS pass next to them).
                     uint32_t sr[2][16];
                     tmem_ld16x256(lane_addr + C::s_col(cb, grp, ch), sr[0]);
-                    tmem_ld16x256(lane_addr + (16u << 16) + C::s_col(cb, grp, ch), sr[1]);
+                    if (!kSplitH) tmem_ld16x256(lane_addr + (16u << 16) + C::s_col(cb, grp, ch), sr[1]);
                     const int c0 = grp * HALF + 32 * ch;     // first query of the chunk
                     uint64_t nl2[4];   // (-LSE2, -LSE2) of the thread's query pairs
 #pragma unroll
@@ -1002,6 +1010,10 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
+                        if (kSplitH && h == 1) {
+                            tmem_ld16x256(lane_addr + (16u << 16) + C::s_col(cb, grp, ch), sr[1]);
+                            tmem_wait_ld();
+                        }
                         uint32_t pk[8];
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
@@ -1078,7 +1090,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 for (int ch = 0; ch < NCH; ++ch) {
                     uint32_t dr[2][16];
                     tmem_ld16x256(lane_addr + C::dp_col(grp, ch), dr[0]);
-                    tmem_ld16x256(lane_addr + (16u << 16) + C::dp_col(grp, ch), dr[1]);
+                    if (!kSplitH) tmem_ld16x256(lane_addr + (16u << 16) + C::dp_col(grp, ch), dr[1]);
                     const int c0 = grp * HALF + 32 * ch;
                     uint64_t dd[4];   // Dv of the thread's query pairs
 #pragma unroll
@@ -1088,16 +1100,23 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     }
                     tmem_wait_ld();
                     if (ch == NCH - 1) {
-                        // dP^T read: X is free for the next step's dP^T.  The dS^T
-                        // tile db may still be read by the dQ^T MMA of step j-2.
+                        // dP^T read: X is free for the next step's dP^T
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bar(B_X_FREE));
+                    }
+                    if (ch == 0) {
+                        // the dS^T tile db may still be read by the dQ MMA of step
+                        // j-2: wait before the first write into it
                         if (!(ok = mbar_wait(bar(B_DSB_FREE + db), bit(dsb_ph, db) ^ 1u, w))) break;
                         dsb_ph ^= 1u << db;
                     }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
+                        if (kSplitH && h == 1) {
+                            tmem_ld16x256(lane_addr + (16u << 16) + C::dp_col(grp, ch), dr[1]);
+                            tmem_wait_ld();
+                        }
                         uint32_t pk[8];
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {

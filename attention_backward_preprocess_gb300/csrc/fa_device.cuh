@@ -192,6 +192,15 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
 __device__ __forceinline__ void red_release_add_gpu(int *p, int v) {
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+// A release fence at GPU scope followed by relaxed adds: each add is then a
+// release of everything before the fence (the fence-then-strong-write release
+// pattern of the PTX memory model), and several adds share one fence.
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+__device__ __forceinline__ void red_relaxed_add_gpu(int *p, int v) {
+    asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 // Fire-and-forget fp32 add in global memory (no value returned).
 __device__ __forceinline__ void red_add_f32(float *p, float v) {
     asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
