@@ -1099,7 +1099,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                         dd[k] = f2_pack(v.x, v.y);
                     }
                     tmem_wait_ld();
-                    if (ch == NCH - 1) {
+                    if (!kSplitH && ch == NCH - 1) {
                         // dP^T read: X is free for the next step's dP^T
                         tc_fence_before();
                         __syncwarp();
@@ -1116,6 +1116,12 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                         if (kSplitH && h == 1) {
                             tmem_ld16x256(lane_addr + (16u << 16) + C::dp_col(grp, ch), dr[1]);
                             tmem_wait_ld();
+                            if (ch == NCH - 1) {
+                                // the last half of dP^T read: X is free again
+                                tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(bar(B_X_FREE));
+                            }
                         }
                         uint32_t pk[8];
 #pragma unroll
