@@ -138,10 +138,9 @@ struct MainCfg {
     static constexpr int OFF_LSE = OFF_STG + STG_BYTES;
     static constexpr int OFF_DV = OFF_LSE + kStages * BM * 4;
     static constexpr int OFF_BAR = OFF_DV + kStages * BM * 4;
-    static constexpr int NUM_BARS = 50;
+    static constexpr int NUM_BARS = 51;
     static_assert(40 + 2 * kStages <= 46, "barrier slots");
-    // TMEM slot (+0), abort flag (+16), unit ring (+32), chunk rows (+48),
-    // chunk n blocks (+64)
+    // TMEM slot (+0), abort flag (+16), unit ring (+32), chunk rows (+48)
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 80 + 1024;  // + alignment slack
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
@@ -180,7 +179,8 @@ enum {
     B_TILE_FULL = 38,   // +d: the reducers wrote a dQ chunk into dS^T tile d
     B_STAGE0 = 40,      // full[kStages], then empty[kStages]
     B_FREE_A = 48,      // warp A's MMAs of a unit completed (its reads of both slots)
-    B_FREE_B = 49       // warp B's MMAs of a unit completed (its reads of the K slot)
+    B_FREE_B = 49,      // warp B's MMAs of a unit completed (its reads of the K slot)
+    B_RED_DONE = 50     // (D = 128) each reducer warp made its last chunk arrivals
 };
 
 struct MainMaps {
@@ -237,6 +237,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         }
         mbar_init(bar(B_FREE_A), 1);
         mbar_init(bar(B_FREE_B), 1);
+        mbar_init(bar(B_RED_DONE), 4);
         for (int b = 0; b < 3; ++b) {
             mbar_init(bar(B_S_FULL + b), 1);
             mbar_init(bar(B_P_FULL + b), 8);
@@ -538,23 +539,19 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             // first chunk (query rows 0-31) waits in dS^T tile j%2, whose dS^T
             // the dQ^T MMA has consumed by then; its second chunk (rows 32-63)
             // in staging buffer j%2.  The reducers put the step's first
-            // workspace row and its n block next to the buffers (row -1 after
-            // the last step).  At most two chunks are in flight: after issuing
+            // workspace row next to the buffers (row -1 after the last step).  At most two chunks are in flight: after issuing
             // one the issuer waits until the one before it has been read, then
             // frees its buffer.
             // Deterministic mode: the contributions to a 64-row block of the
-            // accumulator are added in n-block order -- before a step's chunks
-            // the issuer waits until the row block's semaphore counts every
-            // earlier n block, and it counts its own steps once their chunks
-            // have completed, two steps at a time: the completed bulk groups,
-            // the async-proxy fence and release adds, as the GQA epilogue of
-            // the FlashAttention pages orders its bulk reduce and arrive_inc.
-            // The acquire load of the next step's semaphore is issued as soon
-            // as that step's row is known, so its round trip overlaps the
-            // current step.
+            // accumulator are added in n-block order -- a step's first chunk is
+            // marked parked only once the row block's semaphore counts every
+            // earlier n block (the reducers wait), and the issuer counts its
+            // own steps once their chunks have completed, two steps at a time:
+            // the completed bulk groups, the async-proxy fence and release
+            // adds, as the GQA epilogue of the FlashAttention pages orders its
+            // bulk reduce and arrive_inc.
             if (lane == 0) {
                 volatile long long *stg_row = reinterpret_cast<volatile long long *>(smem + C::OFF_MISC + 48);
-                volatile int *stg_nb = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 64);
                 const bool det = p.deterministic;
                 uint32_t tile_ph = 0, stg_ph = 0;   // bit d: parity of buffer d
                 // deterministic mode: the counts of kRelBatch steps are released
@@ -569,19 +566,6 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 int *pend[kRelBatch] = {};          // semaphores of the steps not yet counted
                 int npend = 0;
                 bool done = false;
-                // prefetched semaphore of the next step (det): address, value read
-                const int *pf_sem = nullptr;
-                int pf_val = 0;
-                // once step j + 1's row is known (its first chunk parked), read
-                // its semaphore with an acquire load whose result is used only then
-                auto prefetch = [&](int j) __attribute__((always_inline)) {
-                    const int dn = (j + 1) & 1;
-                    if (pf_sem || !mbar_try_wait(bar(B_TILE_FULL + dn), bit(tile_ph, dn))) return;
-                    const long long rn = stg_row[dn];
-                    if (rn < 0) return;
-                    pf_sem = p.sem + rn / 64;
-                    pf_val = ld_acquire_gpu(pf_sem);
-                };
                 if (!det) {
                     // the plain loop: no semaphores
                     for (int j = 0;; ++j) {
@@ -610,15 +594,14 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                         tile_ph ^= 1u << d;
                         const long long row = stg_row[d];
                         if (row < 0) { done = true; break; }
+                        // the reducer that parked the chunk saw the row block's
+                        // semaphore count every earlier n block (acquire), and
+                        // TILE_FULL passed that on to this thread
                         int *sem = p.sem + row / 64;
-                        const bool ready = pf_sem == sem && pf_val >= stg_nb[d];
-                        pf_sem = nullptr;
-                        if (!ready && !sem_wait_geq(sem, stg_nb[d], w)) break;
                         fence_async_global();
                         bulk_reduce_add_f32(p.dqacc + row * D, sbase + C::OFF_DS + d * C::DS_BYTES,
                                             C::CHUNK_BYTES);
                         bulk_commit_group();
-                        prefetch(j);
                         bulk_wait_read_all_but_one();   // second chunk of step j-1 read
                         if (j > 0) mbar_arrive(bar(B_STG_FREE + (d ^ 1)));
                         if (!mbar_wait(bar(B_STG_FULL + d), bit(stg_ph, d), w)) break;
@@ -626,7 +609,6 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                         bulk_reduce_add_f32(p.dqacc + (row + 32) * D, sbase + C::OFF_STG + d * C::CHUNK_BYTES,
                                             C::CHUNK_BYTES);
                         bulk_commit_group();
-                        prefetch(j);
                         if (kRelBatch == 1) {
                             // one step late: step j-1's adds complete, count them
                             if (npend) {
@@ -739,15 +721,25 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             long long row0 = 0;
             int nb = 0;   // earlier contributions to the step's row block
             int db = 0;   // dS^T tile / staging buffer of the step
+            // deterministic mode: lane 0 of the first reducer warp waits until
+            // the step's row block counts nb earlier contributions before it
+            // marks the first chunk parked; the issuer acquires that through
+            // TILE_FULL.  The first read goes out before the dQ^T wait, so its
+            // round trip falls in time this warp spends waiting anyway.
+            const bool det_w = p.deterministic && warp == C::W_RED;
+            int sem_v = 0;
             while (ok && next_row(row0, nb)) {
+                if (det_w && lane == 0) sem_v = ld_acquire_gpu(p.sem + row0 / 64);
                 if (!(ok = wait_dq(cb))) break;
                 load_step(R0, R1, cb);
                 if (++cb == C::kSBuf) cb = 0;
                 // rows 0-31 into the dS^T tile the dQ^T MMA has just consumed (its
                 // previous chunk was read before the softmax wrote this step's dS^T)
-                if (lane == 0 && warp == C::W_RED) {
-                    stg_row[db] = row0;
-                    reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 64)[db] = nb;
+                if (lane == 0 && warp == C::W_RED) stg_row[db] = row0;
+                if (det_w) {
+                    int got = 1;
+                    if (lane == 0 && sem_v < nb) got = sem_wait_geq(p.sem + row0 / 64, nb, w) ? 1 : 0;
+                    if (!(ok = __shfl_sync(0xffffffffu, got, 0) != 0)) break;
                 }
                 write_chunk(R0, sbase + C::OFF_DS + db * C::DS_BYTES, bar(B_TILE_FULL + db));
                 // rows 32-63 into staging buffer db
@@ -755,12 +747,17 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 write_chunk(R1, sbase + C::OFF_STG + db * C::CHUNK_BYTES, bar(B_STG_FULL + db));
                 db ^= 1;
             }
-            // end marker for the issuer
+            // End marker for the issuer, sent by the first reducer warp for
+            // all four once each of them has made its last chunk arrivals: a
+            // warp that finished early must not arrive on a TILE_FULL phase
+            // that a slower warp (one waiting on a semaphore) has yet to
+            // arrive on for a real step.
             if (ok) {
                 __syncwarp();
-                if (lane == 0) {
-                    if (warp == C::W_RED) stg_row[db] = -1;
-                    mbar_arrive(bar(B_TILE_FULL + db));
+                if (lane == 0) mbar_arrive(bar(B_RED_DONE));
+                if (warp == C::W_RED && mbar_wait_warp(bar(B_RED_DONE), 0, w) && lane == 0) {
+                    stg_row[db] = -1;
+                    mbar_arrive_cnt(bar(B_TILE_FULL + db), 4);
                 }
             }
         } else {
