@@ -25,8 +25,8 @@ int fwd_block_m();
 int fwd_block_n(int Dq_tile, int Dv_tile);
 int *fwd_error_word();
 cudaError_t launch_bwd_main(const BwdParams &p, const CUtensorMap &q, const CUtensorMap &k,
-                            const CUtensorMap &v, const CUtensorMap &dout, int bf16, int grid,
-                            cudaStream_t stream);
+                            const CUtensorMap &v, const CUtensorMap &dout, const CUtensorMap &dk,
+                            const CUtensorMap &dv, int bf16, int grid, cudaStream_t stream);
 int main_block_m(int D);
 cudaError_t launch_bwd_wide(const BwdParams &p, const CUtensorMap &q, const CUtensorMap &k,
                             const CUtensorMap &v, const CUtensorMap &dout, int bf16, int grid,
@@ -438,8 +438,13 @@ fa_status run_main(const Prepared &P, fa_dtype dtype, cudaStream_t stream) {
         const int grid = (int)std::min<long long>(units, sm_count());
         return cuda_status(fa::launch_bwd_wide(p, mq, mk, mv, mdo, bf16, grid, stream));
     }
+    // dK / dV leave the main kernel through tensor stores of the same geometry as K / V
+    CUtensorMap mdk, mdv;
+    if (!encode_rows_map(&mdk, p.dk, p.Dh, p.Hkv, rk, nb, fa::kBlockN, bf16) ||
+        !encode_rows_map(&mdv, p.dv, p.Dhv, p.Hkv, rk, nb, fa::kBlockN, bf16))
+        return FA_ERR_CUDA;
     const int grid = (int)std::min<long long>(p.max_tiles, sm_count());
-    return cuda_status(fa::launch_bwd_main(p, mq, mk, mv, mdo, bf16, grid, stream));
+    return cuda_status(fa::launch_bwd_main(p, mq, mk, mv, mdo, mdk, mdv, bf16, grid, stream));
 }
 
 fa_status run_postprocess(const Prepared &P, fa_dtype dtype, cudaStream_t stream) {

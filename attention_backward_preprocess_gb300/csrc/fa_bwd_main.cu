@@ -138,11 +138,11 @@ struct MainCfg {
     static constexpr int OFF_LSE = OFF_STG + STG_BYTES;
     static constexpr int OFF_DV = OFF_LSE + kStages * BM * 4;
     static constexpr int OFF_BAR = OFF_DV + kStages * BM * 4;
-    static constexpr int NUM_BARS = 51;
+    static constexpr int NUM_BARS = 54;
     static_assert(40 + 2 * kStages <= 46, "barrier slots");
     // TMEM slot (+0), abort flag (+16), unit ring (+32), chunk rows (+48)
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-    static constexpr int SMEM_BYTES = OFF_MISC + 80 + 1024;  // + alignment slack
+    static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
     static constexpr int kRing = 4;             // work-unit hand-off ring depth
     // ring consumers: MMA warp(s) + 4 reducers + 8 softmax warps
@@ -169,6 +169,7 @@ enum {
     B_S_FREE = 14,      // +b (D = 128): the reducers took dQ^T out of S buffer b
     B_DP_FULL = 17,     // dP^T complete
     B_X_FREE = 18,      // (D = 128) the softmax warps read dP^T
+    B_RED_DONE = 19,    // (D = 128) each reducer warp made its last chunk arrivals
     B_DSB_FREE = 20,    // +d (D = 128): dQ^T MMA done reading dS^T tile d
     B_KDONE = 22,       // (D = 128) dV and dK of the step complete
     B_ACC_FULL = 23, B_ACC_EMPTY = 24, B_DRAIN = 25,
@@ -180,11 +181,13 @@ enum {
     B_STAGE0 = 40,      // full[kStages], then empty[kStages]
     B_FREE_A = 48,      // warp A's MMAs of a unit completed (its reads of both slots)
     B_FREE_B = 49,      // warp B's MMAs of a unit completed (its reads of the K slot)
-    B_RED_DONE = 50     // (D = 128) each reducer warp made its last chunk arrivals
+    B_EPI_FULL = 50,    // +g: softmax group g wrote a dK / dV slice into its staging tile
+    B_EPI_FREE = 52     // +g: the tensor store of group g has read its staging tile
 };
 
 struct MainMaps {
     CUtensorMap q, k, v, dout;
+    CUtensorMap dk, dv;   // outputs, the geometry of k and v
 };
 
 // Extension flags of an instance: a band with a lower edge (a left window),
@@ -238,6 +241,10 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         mbar_init(bar(B_FREE_A), 1);
         mbar_init(bar(B_FREE_B), 1);
         mbar_init(bar(B_RED_DONE), 4);
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(bar(B_EPI_FULL + g), 4);
+            mbar_init(bar(B_EPI_FREE + g), 1);
+        }
         for (int b = 0; b < 3; ++b) {
             mbar_init(bar(B_S_FULL + b), 1);
             mbar_init(bar(B_P_FULL + b), 8);
@@ -853,6 +860,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         const int g4 = lane >> 2, q4 = lane & 3;     // 16-lane access shapes
         const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
         uint32_t s_ph = 0, dp_ph = 0, st_ph = 0, acc_ph = 0, dsb_ph = 0;   // s_ph, dsb_ph: bit per buffer
+        uint32_t epi_ph = 0;             // parity of this group's staging-tile barriers
         int stage = 0, cb = 0, db = 0;   // stage, S buffer, dS^T tile of the step
         bool ok = true;
         while (ok) {
@@ -1194,6 +1202,65 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
             __syncwarp();
             const float mul = grp == 0 ? p.scale : 1.f;
             const int col0 = grp == 0 ? C::TM_DK : C::TM_DV;
+            if (n0 + BN <= u.lk) {
+                // Every key row of the block is inside the used length: the
+                // tile leaves by tensor stores.  Group g stages 64-column slices
+                // of its [128 keys x D] tile in dS^T tile g (free once the last
+                // dQ^T MMA -- and, D = 128, the issuer -- finished with both
+                // tiles) in the store's 128-byte swizzle; the group's first
+                // lane issues the store and waits until it has read the tile.
+                bool free_ok = true;
+                for (int d = 0; d < 2; ++d)
+                    free_ok = free_ok && mbar_wait(bar(B_DSB_FREE + d), bit(dsb_ph, d) ^ 1u, w);
+                if (!(ok = free_ok)) break;
+                const uint32_t tile = sbase + C::OFF_DS + grp * C::DS_BYTES;
+                const CUtensorMap *omap = grp == 0 ? &maps.dk : &maps.dv;
+#pragma unroll 1
+                for (int sl = 0; sl < D / 64; ++sl) {
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        uint32_t a[32];
+                        tmem_ld32(lane_addr + col0 + 64 * sl + 32 * h2, a);
+                        tmem_wait_ld();
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int c = 0; c < 16; ++c)
+                            pk[c] = Cvt<T>::pack(__uint_as_float(a[2 * c]) * mul,
+                                                 __uint_as_float(a[2 * c + 1]) * mul);
+                        // key row j: 16-byte chunk c of its 128-byte row at c ^ (j % 8)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            st_shared_v4(tile + j * 128 + (((4 * h2 + c) ^ (j & 7)) << 4), pk[4 * c],
+                                         pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                    }
+                    if (sl == D / 64 - 1) {
+                        // the accumulators are read: the next unit may use them
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(B_ACC_EMPTY));
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_EPI_FULL + grp));
+                    if (quarter == 0) {
+                        if (!(ok = mbar_wait_warp(bar(B_EPI_FULL + grp), epi_ph, w))) break;
+                        if (lane == 0) {
+                            tma_store_4d(omap, tile, 64 * sl, u.hk, u.k_row0 + n0, u.bidx);
+                            bulk_commit_group();
+                            bulk_wait_read_all();
+                            mbar_arrive(bar(B_EPI_FREE + grp));
+                        }
+                        __syncwarp();
+                    }
+                    if (!(ok = mbar_wait_warp(bar(B_EPI_FREE + grp), epi_ph, w))) break;
+                    epi_ph ^= 1;
+                }
+                if (!ok) break;
+                // the other group's store has read its tile too before the next
+                // unit's dS^T may land in either tile
+                if (!(ok = mbar_wait_warp(bar(B_EPI_FREE + (grp ^ 1)), epi_ph ^ 1u, w))) break;
+                continue;
+            }
 #pragma unroll
             for (int ch = 0; ch < D / 32; ++ch) {
                 uint32_t a[32];
@@ -1256,9 +1323,9 @@ static cudaError_t launch_main_t(const BwdParams &p, const MainMaps &maps, int g
 int main_block_m(int D) { return D == 128 ? MainCfg<128, __nv_bfloat16>::BM : MainCfg<64, __nv_bfloat16>::BM; }
 
 cudaError_t launch_bwd_main(const BwdParams &p, const CUtensorMap &q, const CUtensorMap &k,
-                            const CUtensorMap &v, const CUtensorMap &dout, int bf16, int grid,
-                            cudaStream_t stream) {
-    MainMaps maps{q, k, v, dout};
+                            const CUtensorMap &v, const CUtensorMap &dout, const CUtensorMap &dk,
+                            const CUtensorMap &dv, int bf16, int grid, cudaStream_t stream) {
+    MainMaps maps{q, k, v, dout, dk, dv};
     if (p.D == 128)
         return bf16 ? launch_main_t<128, __nv_bfloat16>(p, maps, grid, stream)
                     : launch_main_t<128, __half>(p, maps, grid, stream);

@@ -82,6 +82,31 @@ def test_deterministic_is_bit_identical_and_correct(fa, oracle_mod, cuda_device,
     check_bar(a[2], rv, "dv")
 
 
+@pytest.mark.parametrize("D,dtype", [(128, "bf16"), (64, "fp16"), (96, "bf16")])
+def test_dk_dv_tensor_store_and_plain_tails(fa, oracle_mod, cuda_device, D, dtype):
+    """dK / dV of whole 128-key blocks leave by tensor stores, the blocks that
+    end past a sequence's last key by plain stores: packed sequences of 384,
+    130, 128 and 1 keys mix both, next to each other in the same rows, with
+    canaries around the outputs."""
+    lengths = [384, 130, 128, 1]
+    w = W("store_paths", 4, 0, 0, 4, 2, D, dtype, True, varlen=(4, 1, 384))
+    x = small_case(oracle_mod, w, lengths=lengths)
+    pad = 4096
+    outs, bufs = [], []
+    for t in (x["q"], x["k"], x["v"]):
+        n = t.numel()
+        buf = torch.full((n + 2 * pad,), -7.0, dtype=t.dtype, device="cuda")
+        bufs.append(buf)
+        outs.append(buf[pad:pad + n].view(t.shape))
+    run_gpu_bwd(fa, w, x, outs=outs)
+    for buf in bufs:
+        assert bool((buf[:pad] == -7.0).all()) and bool((buf[-pad:] == -7.0).all())
+    rq, rk, rv = oracle_grads(oracle_mod, w, x)
+    check_bar(outs[0], rq, "dq")
+    check_bar(outs[1], rk, "dk")
+    check_bar(outs[2], rv, "dv")
+
+
 @pytest.mark.parametrize("D", [128, 96])
 def test_outputs_written_in_bounds_only(fa, oracle_mod, cuda_device, D):
     """Canary regions around dq/dk/dv stay untouched; ragged tails included
