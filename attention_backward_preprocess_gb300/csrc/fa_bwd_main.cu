@@ -562,14 +562,16 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 const bool det = p.deterministic;
                 uint32_t tile_ph = 0, stg_ph = 0;   // bit d: parity of buffer d
                 // deterministic mode: the counts of kRelBatch steps are released
-                // together, after one wait for all their adds to complete.  A
-                // release add waits for every bulk reduce still in flight (about
-                // 2200 cycles, an L2 reduce), so releasing with nothing in flight,
-                // once per batch, halves those waits; longer batches lengthen the
-                // ordering chains between units.  Measured on B = 1, 16 heads,
-                // 32768 keys, D = 128: 29.2 ms (one step late, one at a time),
-                // 25.4 ms (batches of 2), 31.9 ms (batches of 4).
-                constexpr int kRelBatch = 2;
+                // together, after one wait for all their adds to complete, and so
+                // are those of a unit's last steps.  A release waits for every
+                // bulk reduce still in flight (about 2200 cycles, an L2 reduce),
+                // so it goes out with nothing in flight, once per batch; longer
+                // batches lengthen the ordering chains between units.  Measured
+                // on B = 1, 16 heads, 32768 keys, D = 128 (median main ms): 21.4
+                // (batches of 2, no flush at a unit's end), 21.9 / 21.7 / 21.0 /
+                // 21.4 / 20.2-21.0 / 27.3 / 28.9 (batches of 2 / 3 / 4 / 6 / 8 /
+                // 12 / 16 with the flush).
+                constexpr int kRelBatch = 8;
                 int *pend[kRelBatch] = {};          // semaphores of the steps not yet counted
                 int npend = 0;
                 bool done = false;
@@ -599,8 +601,10 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                         const int d = j & 1;
                         if (!mbar_wait(bar(B_TILE_FULL + d), bit(tile_ph, d), w)) break;
                         tile_ph ^= 1u << d;
-                        const long long row = stg_row[d];
+                        long long row = stg_row[d];
                         if (row < 0) { done = true; break; }
+                        const bool unit_end = (row >> 62) & 1;
+                        row &= ~(1ll << 62);
                         // the reducer that parked the chunk saw the row block's
                         // semaphore count every earlier n block (acquire), and
                         // TILE_FULL passed that on to this thread
@@ -627,12 +631,15 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                             npend = 1;
                         } else {
                             pend[npend++] = sem;
-                            if (npend == kRelBatch) {   // all adds of the batch complete: count them
+                            // all adds of the batch complete (or of a unit's last
+                            // steps: the next unit's steps would delay them): count them
+                            if (npend == kRelBatch || unit_end) {
                                 bulk_wait_all();
                                 fence_async_global();
                                 fence_acq_rel_gpu();     // one release fence for the batch
 #pragma unroll
-                                for (int i = 0; i < kRelBatch; ++i) red_relaxed_add_gpu(pend[i], 1);
+                                for (int i = 0; i < kRelBatch; ++i)
+                                    if (i < npend) red_relaxed_add_gpu(pend[i], 1);
                                 npend = 0;
                             }
                         }
@@ -742,7 +749,10 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 if (++cb == C::kSBuf) cb = 0;
                 // rows 0-31 into the dS^T tile the dQ^T MMA has just consumed (its
                 // previous chunk was read before the softmax wrote this step's dS^T)
-                if (lane == 0 && warp == C::W_RED) stg_row[db] = row0;
+                // deterministic mode: bit 62 marks a unit's last step, whose
+                // count the issuer then releases at once
+                if (lane == 0 && warp == C::W_RED)
+                    stg_row[db] = row0 | (det_w && m_it < m_first ? (1ll << 62) : 0ll);
                 if (det_w) {
                     int got = 1;
                     if (lane == 0 && sem_v < nb) got = sem_wait_geq(p.sem + row0 / 64, nb, w) ? 1 : 0;
