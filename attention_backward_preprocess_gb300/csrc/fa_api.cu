@@ -48,6 +48,18 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // pads the head dim to a multiple of its block size).
 int pad_d(int D) { return D <= 64 ? 64 : D <= 128 ? 128 : 256; }
 
+// Backward tile width of a query / key head dim.  D = 64 runs in the 128-wide
+// tile (its upper 64 columns zero) for dense problems of at least 4096 keys:
+// its softmax, not the tensor core, sets the step time, and the wider tile's
+// 64-query steps carry half the elementwise work per step (B = 2, 32 / 8
+// heads, 8192 keys, causal: main kernel 2.204 -> 1.911 ms).  Shorter and
+// varlen problems keep the 64-wide tile, whose 128-query steps halve the unit
+// transitions (16 sequences of 256..2048 keys: 0.378 against 0.435 ms).
+int bwd_pad_d(int D, int Sk, bool varlen) {
+    if (D <= 64 && !varlen && Sk >= 4096) return 128;
+    return pad_d(D);
+}
+
 // Head dims with a kernel: a query / key dim D that is a multiple of 8 in
 // [64, 256]; a value dim Dv (0: equal to D) that is a multiple of 8 in
 // [8, 256].  One head dim of at most 128 runs in the main kernel; a head dim
@@ -89,7 +101,7 @@ bool plan(int B, int Sq, int Sk, int Hq, int Hkv, int D, int varlen, int determi
     L->tiles = off;     off = round_up(off + (size_t)tiles * 16, 256);
     L->dvec = off;      off = round_up(off + (size_t)L->rows * 4, 256);
     L->lse2 = off;      off = round_up(off + (size_t)L->rows * 4, 256);
-    L->dqacc = off;     off = round_up(off + (size_t)L->rows * pad_d(D) * 4, 256);
+    L->dqacc = off;     off = round_up(off + (size_t)L->rows * bwd_pad_d(D, Sk, varlen) * 4, 256);
     L->sem = off;       off = round_up(off + (deterministic ? (size_t)(L->rows / 64) * 4 : 0), 256);
     L->total = off;
     return true;
@@ -351,7 +363,8 @@ fa_status prepare(const void *q, const void *k, const void *v, const void *o, co
     std::memset(&p, 0, sizeof(p));
     p.q = q; p.k = k; p.v = v; p.o = o; p.dout = dout; p.lse = lse;
     p.dq = dq; p.dk = dk; p.dv = dv;
-    p.B = B; p.Sq = Sq; p.Sk = Sk; p.Hq = Hq; p.Hkv = Hkv; p.D = pad_d(D); p.Dh = D;
+    p.B = B; p.Sq = Sq; p.Sk = Sk; p.Hq = Hq; p.Hkv = Hkv; p.D = bwd_pad_d(D, Sk, cu_q != nullptr);
+    p.Dh = D;
     p.G = Hq / Hkv;
     p.scale = scale;
     p.scale_log2 = scale * kLog2e;

@@ -82,6 +82,29 @@ def test_deterministic_is_bit_identical_and_correct(fa, oracle_mod, cuda_device,
     check_bar(a[2], rv, "dv")
 
 
+# D = 64 with at least 4096 keys (dense) runs in the 128-wide tile, its upper
+# columns zero
+LONG_D64 = [
+    W("d64_s4096_causal_gqa", 1, 4096, 4096, 4, 2, 64, causal=True),
+    W("d64_s4096_fp16", 1, 4096, 4096, 2, 2, 64, "fp16"),
+    W("d64_s4100_det", 1, 4100, 4100, 2, 1, 64, causal=True, deterministic=True),
+]
+
+
+@pytest.mark.parametrize("w", LONG_D64, ids=lambda w: w.name)
+def test_long_d64_matches_oracle(fa, oracle_mod, cuda_device, w):
+    x = small_case(oracle_mod, w)
+    dq, dk, dv = run_gpu_bwd(fa, w, x)
+    rq, rk, rv = oracle_grads(oracle_mod, w, x)
+    check_bar(dq, rq, "dq")
+    check_bar(dk, rk, "dk")
+    check_bar(dv, rv, "dv")
+    if w.deterministic:
+        again = run_gpu_bwd(fa, w, x)
+        for t, u in zip((dq, dk, dv), again):
+            assert torch.equal(t.view(torch.int16), u.view(torch.int16))
+
+
 @pytest.mark.parametrize("D,dtype", [(128, "bf16"), (64, "fp16"), (96, "bf16")])
 def test_dk_dv_tensor_store_and_plain_tails(fa, oracle_mod, cuda_device, D, dtype):
     """dK / dV of whole 128-key blocks leave by tensor stores, the blocks that
