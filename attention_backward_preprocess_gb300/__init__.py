@@ -28,7 +28,7 @@ EXPORTED = [
     "fa_bwd_main", "fa_bwd_postprocess", "fa_bwd_workspace_layout", "fa_fwd",
     "fa_device_status", "fa_set_wait_timeout_ns", "fa_status_string",
     "fa_selftest_umma", "fa_selftest_semaphore", "fa_selftest_tmem_layout", "fa_bwd_noalloc",
-    "fa_bwd_noalloc_scratch_bytes", "fa_fwd_ext", "fa_bwd_ext", "fa_bwd_workspace_sync_layout",
+    "fa_bwd_noalloc_scratch_bytes", "fa_fwd_ext", "fa_bwd_ext", "fa_bwd_stages_ext", "fa_bwd_workspace_sync_layout",
     "fa_bwd_noalloc_status",
 ]
 
@@ -152,6 +152,8 @@ def lib():
         L.fa_fwd_ext.argtypes = [_vp] * 5 + _SHAPE + [_f, _i, _vp, _vp, _ep, _i, _vp]
         L.fa_bwd_ext.argtypes = ([_vp] * 9 + _SHAPE + [_f, _i, _vp, _vp, _ep, _i, _i, _vp, _sz,
                                                        _vp])
+        L.fa_bwd_stages_ext.argtypes = ([_i] + [_vp] * 9 + _SHAPE +
+                                        [_f, _i, _vp, _vp, _ep, _i, _i, _vp, _sz, _vp])
         L.fa_device_status.argtypes = [_vp, _vp]
         L.fa_set_wait_timeout_ns.argtypes = [ctypes.c_longlong]
         L.fa_set_wait_timeout_ns.restype = ctypes.c_longlong
@@ -350,14 +352,28 @@ def workspace_layout(B, Sq, Sk, Hq, Hkv, D, varlen=False, deterministic=False) -
 def fa_bwd_stages(q, k, v, o, dout, lse, workspace, causal=False, softmax_scale=None,
                   cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None,
                   deterministic=False, dq=None, dk=None, dv=None, stages=("pre", "main", "post"),
-                  stream=None):
-    """Runs the chosen stages (preprocess / main / postprocess) on ``workspace``."""
+                  stream=None, totals=None):
+    """Runs the chosen stages (preprocess / main / postprocess) on ``workspace``.
+
+    ``totals=(total_q, total_k)`` (varlen) goes through fa_bwd_stages_ext with
+    the packed row counts, so that no stage synchronises the stream."""
     B, Sq, Sk, Hq, Hkv, D = _shape(q, k, cu_seqlens_q, max_seqlen_q, max_seqlen_k)
     scale = default_scale(D) if softmax_scale is None else float(softmax_scale)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     shape = [B, Sq, Sk, Hq, Hkv, D]
+    if totals is not None:
+        mask = ((1 if "pre" in stages else 0) | (2 if "main" in stages else 0) |
+                (4 if "post" in stages else 0))
+        ext = _ext(Hq, totals=totals)
+        _check(lib().fa_bwd_stages_ext(mask, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout),
+                                       _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), *shape, scale,
+                                       int(bool(causal)), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                                       ext, int(bool(deterministic)), _dtype_code(q),
+                                       _ptr(workspace), workspace.numel(), _stream(stream)),
+               "fa_bwd_stages_ext")
+        return dq, dk, dv
     cu = [_ptr(cu_seqlens_q), _ptr(cu_seqlens_k)]
     det, dt = int(bool(deterministic)), _dtype_code(q)
     ws = [_ptr(workspace), workspace.numel(), _stream(stream)]

@@ -616,6 +616,32 @@ fa_status fa_bwd_ext(const void *q, const void *k, const void *v, const void *o,
     return FA_OK;
 }
 
+fa_status fa_bwd_stages_ext(int stages, const void *q, const void *k, const void *v,
+                            const void *o, const void *dout, const float *lse, void *dq,
+                            void *dk, void *dv, int B, int Sq, int Sk, int Hq, int Hkv, int D,
+                            float softmax_scale, int causal, const int *cu_seqlens_q,
+                            const int *cu_seqlens_k, const fa_ext *ext, int deterministic,
+                            fa_dtype dtype, void *workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+    const int all = FA_STAGE_PRE | FA_STAGE_MAIN | FA_STAGE_POST;
+    if (stages <= 0 || (stages & ~all) || !workspace) return FA_ERR_INVALID_ARG;
+    Prepared P;
+    fa_status st = prepare(q, k, v, o, dout, lse, dq, dk, dv, B, Sq, Sk, Hq, Hkv, D, softmax_scale,
+                           causal, cu_seqlens_q, cu_seqlens_k, deterministic, dtype, workspace,
+                           workspace_bytes, stream, &P, ext);
+    if (st != FA_OK) return st;
+    if ((stages & FA_STAGE_PRE) && (st = run_preprocess(P, dtype, stream)) != FA_OK) return st;
+    if (stages & FA_STAGE_MAIN) {
+        if (P.p.dbias) {
+            const size_t n = (size_t)B * Hq * Sq * Sk * 2;
+            if (cudaMemsetAsync(P.p.dbias, 0, n, stream) != cudaSuccess) return FA_ERR_CUDA;
+        }
+        if ((st = run_main(P, dtype, stream)) != FA_OK) return st;
+    }
+    if ((stages & FA_STAGE_POST) && (st = run_postprocess(P, dtype, stream)) != FA_OK) return st;
+    return FA_OK;
+}
+
 fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
                  const float *lse, void *dq, void *dk, void *dv, int B, int Sq, int Sk, int Hq,
                  int Hkv, int D, float softmax_scale, int causal, const int *cu_seqlens_q,

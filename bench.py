@@ -285,6 +285,10 @@ def main():
     stream = torch.cuda.current_stream()
     kw = dict(causal=w.causal, softmax_scale=w.softmax_scale, deterministic=w.deterministic,
               dq=dq, dk=dk, dv=dv, **vl)
+    if varlen:
+        # the packed row counts, known here: no call reads cu_seqlens[B] back
+        # (which would synchronise the stream every call)
+        kw["totals"] = (sum(x["lengths"]), sum(x["lengths"]))
     # a step reads Q, K, V, O, dO; below twice the 129 MB L2 the L2 is written
     # over between timed steps (outside the per-step events)
     in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, o, do))
@@ -381,7 +385,8 @@ def main():
             stream.wait_event(ev_out[b])
             di = dev_in[b]
             evl = dict(cu_seqlens_q=di["cu_q"], cu_seqlens_k=di["cu_k"],
-                       max_seqlen_q=x["max_len"], max_seqlen_k=x["max_len"]) if varlen else {}
+                       max_seqlen_q=x["max_len"], max_seqlen_k=x["max_len"],
+                       totals=kw["totals"]) if varlen else {}
             gq, gk, gv = fa.fa_bwd(di["q"], di["k"], di["v"], di["o"], di["dout"], di["lse"],
                                    causal=w.causal, softmax_scale=w.softmax_scale,
                                    deterministic=w.deterministic, dq=dev_out[b][0],
@@ -497,7 +502,8 @@ def run_ext(args, w):
     q, k, v, do = x["q"], x["k"], x["v"], x["dout"]
     varlen = w.varlen is not None
     vl = dict(cu_seqlens_q=x["cu_q"], cu_seqlens_k=x["cu_k"], max_seqlen_q=x["max_len"],
-              max_seqlen_k=x["max_len"]) if varlen else {}
+              max_seqlen_k=x["max_len"],
+              totals=(sum(x["lengths"]), sum(x["lengths"]))) if varlen else {}
     wl, wr = (int(t) for t in args.window.split(",")) if args.window else (-1, -1)
     ext = {}
     if args.window:

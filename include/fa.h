@@ -135,7 +135,8 @@ fa_status fa_bwd_postprocess(void *dq, int B, int Sq, int Sk, int Hq, int Hkv, i
 /* Where the preprocess outputs live inside a workspace, in fp32 elements
  * from the workspace base: Dv at *dvec_off, LSE2 at *lse2_off, each indexed
  * by workspace row; the fp32 dQ accumulator at *dqacc_off, [rows, Dt], where
- * Dt is the tile width the head dim runs at (64 for D = 64, else 128; the
+ * Dt is the tile width the head dim runs at (64 for D = 64, except 128 for
+ * dense problems of at least 4096 keys; 128 for D up to 128; 256 above; the
  * columns past D stay 0).
  * Workspace row of (sequence b, query head h, position s):
  *   dense : (b * Hq + h) * round_up(Sq, 128) + s
@@ -275,6 +276,30 @@ fa_status fa_bwd_ext(const void *q, const void *k, const void *v, const void *o,
                      const int *cu_seqlens_q, const int *cu_seqlens_k, const fa_ext *ext,
                      int deterministic, fa_dtype dtype, void *workspace, size_t workspace_bytes,
                      cudaStream_t stream);
+
+/* The stages of fa_bwd_ext as separate calls on a caller-owned workspace:
+ * `stages` is a bit mask of FA_STAGE_PRE (the preprocess), FA_STAGE_MAIN (the
+ * work-unit scheduler for varlen, and the main kernel; with ext->dbias also
+ * the zeroing of dBias before it) and FA_STAGE_POST (the dQ postprocess), run
+ * in that order; the other arguments as fa_bwd_ext, where ext may be NULL and
+ * workspace may not.  Across calls the stages must run in this order, on one
+ * stream and one workspace, with the same arguments.  Pointers a chosen
+ * stage does not read may be NULL (preprocess: o, dout, lse; main: q, k, v,
+ * dout, dk, dv; postprocess: dq).  The call never waits for the device when
+ * varlen totals are given in ext (or the problem is dense): a deterministic
+ * call's device status is then read afterwards with fa_device_status on the
+ * same workspace.  Errors as fa_bwd_ext, plus FA_ERR_INVALID_ARG for an
+ * empty or unknown stage mask.  Defined by the same passages as fa_bwd. */
+#define FA_STAGE_PRE 1
+#define FA_STAGE_MAIN 2
+#define FA_STAGE_POST 4
+fa_status fa_bwd_stages_ext(int stages, const void *q, const void *k, const void *v,
+                            const void *o, const void *dout, const float *lse, void *dq,
+                            void *dk, void *dv, int B, int Sq, int Sk, int Hq, int Hkv, int D,
+                            float softmax_scale, int causal, const int *cu_seqlens_q,
+                            const int *cu_seqlens_k, const fa_ext *ext, int deterministic,
+                            fa_dtype dtype, void *workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
 
 /* Synchronises `stream`, then returns and clears the device error word of
  * this device's library workspace (FA_OK or FA_ERR_TIMEOUT).  For a caller

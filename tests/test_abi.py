@@ -279,6 +279,29 @@ def test_wide_head_dim_workspace(fa):
         assert n < 4 * (lay["dqacc"] + lay["rows"] * width) + 4096
 
 
+def test_d64_tile_width_follows_the_problem(fa):
+    """D = 64 runs at the 128-wide tile for dense problems of 4096 keys or more
+    (the accumulator is then 128 wide), at the 64-wide tile otherwise."""
+    for Sk, varlen, width in ((4096, False, 128), (8192, False, 128), (4095, False, 64),
+                              (8192, True, 64)):
+        lay = fa.workspace_layout(2, Sk, Sk, 2, 2, 64, varlen=varlen)
+        n = fa.workspace_bytes(2, Sk, Sk, 2, 2, 64, varlen=varlen)
+        assert n >= 4 * (lay["dqacc"] + lay["rows"] * width)
+        assert n < 4 * (lay["dqacc"] + lay["rows"] * width) + 4096
+
+
+def test_stage_call_refusals(fa):
+    """fa_bwd_stages_ext refuses an empty or unknown stage mask and a missing
+    workspace before it touches the device."""
+    L = fa.lib()
+    vp = ctypes.c_void_p
+    ptrs = [vp(0x1000 * (i + 1)) for i in range(9)]
+    shape = (1, 128, 128, 2, 2, 64)
+    for mask, ws in ((0, vp(0x100000)), (8, vp(0x100000)), (-1, vp(0x100000)), (7, None)):
+        assert L.fa_bwd_stages_ext(mask, *ptrs, *shape, 0.125, 1, None, None, None, 0, 0, ws,
+                                   ctypes.c_size_t(1 << 40), None) == fa.FA_ERR_INVALID_ARG
+
+
 def test_bias_with_varlen_is_unsupported(fa):
     L = fa.lib()
     vp = ctypes.c_void_p

@@ -142,7 +142,7 @@ def test_varlen_totals_mismatch_is_refused_on_the_device(fa, oracle_mod, cuda_de
     assert bool((dq == 3.0).all())
 
 
-@pytest.mark.parametrize("which", ["bwd", "fwd"])
+@pytest.mark.parametrize("which", ["bwd", "fwd", "stages"])
 def test_varlen_call_with_totals_does_not_wait_for_the_stream(fa, oracle_mod, cuda_device, which):
     lengths = [130, 1, 300, 64]
     w, x = _varlen_case(oracle_mod, lengths, dtype="fp16")
@@ -158,6 +158,15 @@ def test_varlen_call_with_totals_does_not_wait_for_the_stream(fa, oracle_mod, cu
         if which == "bwd":
             return fa.fa_bwd(g["q"], g["k"], g["v"], g["o"], g["dout"], g["lse"], workspace=ws,
                              **kw, **vl)
+        if which == "stages":
+            # the three stages as separate calls (fa_bwd_stages_ext)
+            out = None
+            for st in ("pre", "main", "post"):
+                out = fa.fa_bwd_stages(g["q"], g["k"], g["v"], g["o"], g["dout"], g["lse"], ws,
+                                       stages=(st,), dq=out[0] if out else None,
+                                       dk=out[1] if out else None, dv=out[2] if out else None,
+                                       **kw, **vl)
+            return out
         return fa.fa_fwd(g["q"], g["k"], g["v"], **kw, **vl)
 
     call()                      # first use of the kernels (module loading) outside the timing
@@ -170,7 +179,7 @@ def test_varlen_call_with_totals_does_not_wait_for_the_stream(fa, oracle_mod, cu
     t_all = time.perf_counter() - t0
     assert t_all > 0.2, "the sleep kernel did not hold the stream"
     assert t_call < 0.25 * t_all, (t_call, t_all)
-    if which == "bwd":
+    if which in ("bwd", "stages"):
         assert fa.device_status(ws) == fa.FA_OK
         for t, r, name in zip(out, oracle_grads(oracle_mod, w, x), ("dq", "dk", "dv")):
             check_bar(t, r, name)
