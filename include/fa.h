@@ -277,6 +277,17 @@ fa_status fa_bwd_ext(const void *q, const void *k, const void *v, const void *o,
                      int deterministic, fa_dtype dtype, void *workspace, size_t workspace_bytes,
                      cudaStream_t stream);
 
+/* CUDA graphs.  A backward call that issues only launches and memsets on
+ * `stream` can be captured into a CUDA graph and replayed: fa_bwd_ext /
+ * fa_bwd_with_workspace with a caller workspace for dense problems, and for
+ * varlen problems when ext gives the packed totals; fa_bwd_stages_ext (or
+ * the three stage calls, dense) in every mode.  A deterministic fa_bwd /
+ * fa_bwd_ext reads its device status back before returning (a host wait) and
+ * cannot be captured; capture its stages instead and read the status with
+ * fa_device_status after the replay.  Make one uncaptured call with the same
+ * sizes first (it loads the kernels).  Each replay reads the buffers that
+ * were captured, so new inputs are written into them. */
+
 /* The stages of fa_bwd_ext as separate calls on a caller-owned workspace:
  * `stages` is a bit mask of FA_STAGE_PRE (the preprocess), FA_STAGE_MAIN (the
  * work-unit scheduler for varlen, and the main kernel; with ext->dbias also
