@@ -26,8 +26,10 @@
 //                         CollectiveEpilogueBwdGQA in
 //                         "flash-attention/hopper/epilogue_bwd.hpp")
 //
-// and at the end dK * c, dV are written out (CollectiveEpilogueBwd::store;
-// zeros for a unit with no visible query, store_zero).
+// and at the end dK * c, dV are written out (CollectiveEpilogueBwd::store:
+// registers -> shared memory, staged in the dS^T tiles, -> TMA tensor store;
+// plain stores for a block that ends past the used key length; zeros for a
+// unit with no visible query, store_zero).
 //
 // Persistent CTAs (one per SM) take units from a global counter.  Warp roles
 // (16 warps, 512 threads):
@@ -40,9 +42,12 @@
 //                 frees tensor memory
 //   warp 2        MMA warp B: dV, dK, then dQ^T of every step
 //   warp 3        bulk-reduce issuer (D = 128): adds each staged dQ chunk to
-//                 the accumulator, and orders the adds in deterministic mode
+//                 the accumulator and, in deterministic mode, counts the
+//                 completed adds on the row blocks' semaphores
 //   warps 4-7     dQ reducers: dQ^T out of tensor memory into the staging
-//                 buffers (one TMEM lane quarter each)
+//                 buffers (one TMEM lane quarter each); in deterministic mode
+//                 the first of them waits for the row block's semaphore before
+//                 a step's chunks are handed to the issuer
 //   warps 8-15    softmax / elementwise, two groups of four; group g handles
 //                 query columns [g BM/2, (g+1) BM/2) of every key row, and
 //                 in the epilogue group 0 writes dK, group 1 writes dV

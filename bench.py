@@ -590,12 +590,22 @@ def run_ext(args, w):
     return 0
 
 
-def source_hash():
+def code_text(text):
+    """C++ source without comments and whitespace: what the compiler sees of it
+    (a comment edit leaves the kernel, and its counters, unchanged)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return re.sub(r"\s+", "", text)
+
+
+def source_hash(read=None):
     import hashlib
     h = hashlib.sha256()
     for f in ("fa_bwd_main.cu", "fa_bwd_units.cuh", "fa_device.cuh", "fa_params.h"):
-        h.update(open(os.path.join(ROOT, "attention_backward_preprocess_gb300", "csrc", f),
-                      "rb").read())
+        path = os.path.join("attention_backward_preprocess_gb300", "csrc", f)
+        text = read(path) if read else open(os.path.join(ROOT, path)).read()
+        h.update(code_text(text).encode())
     return h.hexdigest()[:16]
 
 
