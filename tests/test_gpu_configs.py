@@ -162,3 +162,38 @@ def test_full_size_extension(fa, oracle_mod, cuda_device, name, opt):
     check_bar(pick(dq, qrows), rq, name + " dq rows")
     check_bar(pick(dk, krows), rk, name + " dk rows")
     check_bar(pick(dv, krows), rv, name + " dv rows")
+
+
+def test_accumulator_past_2_31_elements(fa, oracle_mod, cuda_device):
+    """The bench workload at B = 65: the fp32 dQ accumulator holds 65 x 32 x
+    8192 rows x 128 = 2.18 G elements, past 2^31, so every index into it and
+    into the outputs of the last sequences needs 64-bit arithmetic (about
+    30 GB on the device).  Rows of the
+    first and the last sequence are checked against the oracle, which takes
+    that one sequence alone."""
+    w = WORKLOADS["b2_hq32_hkv8_s8192_d128_causal_gqa"].with_(name="b65_hq32_hkv8_s8192", B=65)
+    dev = torch.device("cuda")
+    x = generate(w, dev)
+    q, k, v, do = x["q"], x["k"], x["v"], x["dout"]
+    lay = fa.workspace_layout(w.B, w.Sq, w.Sk, w.Hq, w.Hkv, w.D)
+    assert lay["rows"] * 128 > 2 ** 31
+    o, lse = fa.fa_fwd(q, k, v, causal=True, softmax_scale=w.softmax_scale)
+    dq, dk, dv = fa.fa_bwd(q, k, v, o, do, lse, causal=True, softmax_scale=w.softmax_scale)
+    torch.cuda.synchronize()
+    assert fa.device_status() == fa.FA_OK
+    rng = np.random.default_rng(11)
+    for b in (w.B - 1, 0):
+        one = {n: x[n][b:b + 1].cpu() for n in ("q", "k", "v", "dout")}
+        qrows = _rows(rng, 16, [w.Sq], w.Hq)
+        krows = _rows(rng, 8, [w.Sk], w.Hkv, groups=[(0, w.Hkv - 1)])
+        rq, rk, rv = oracle_mod.backward_sampled(
+            to64(one["q"]), to64(one["k"]), to64(one["v"]), to64(one["dout"]), w.softmax_scale,
+            True, qrows=qrows, krows=krows)
+        got_q = torch.stack([dq[b, s, h] for (_, s, h) in qrows])
+        got_k = torch.stack([dk[b, s, h] for (_, s, h) in krows])
+        got_v = torch.stack([dv[b, s, h] for (_, s, h) in krows])
+        check_bar(got_q, rq, "dq rows of sequence %d" % b)
+        check_bar(got_k, rk, "dk rows of sequence %d" % b)
+        check_bar(got_v, rv, "dv rows of sequence %d" % b)
+    del q, k, v, do, o, lse, dq, dk, dv, x
+    torch.cuda.empty_cache()
