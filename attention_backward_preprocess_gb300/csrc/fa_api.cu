@@ -398,12 +398,18 @@ fa_status prepare(const void *q, const void *k, const void *v, const void *o, co
     // order, so the units of one (sequence, kv head) wait on one another;
     // there, all pairs are interleaved (plain n-block-major order), so that
     // few units of any one chain run at the same time.
+    // Varlen (the scheduler kernel builds the list): groups of consecutive
+    // sequences of at least 1.5 grids of units each, the same idea; in
+    // deterministic mode none (0: the plain order).
     p.unit_group = B * Hkv;
     if (!cu_q && !deterministic) {
         const int nblk = (Sk + fa::kBlockN - 1) / fa::kBlockN;
         const long long grid = std::min<long long>(L.max_tiles, sm_count());
         for (int g = 1; g <= B * Hkv; ++g)
             if ((B * Hkv) % g == 0 && 2LL * g * nblk >= 3 * grid) { p.unit_group = g; break; }
+    } else if (cu_q) {
+        const long long grid = std::min<long long>(L.max_tiles, sm_count());
+        p.unit_group = deterministic ? 0 : (int)std::max<long long>(1, 3 * grid / 2);
     }
     p.dvec = reinterpret_cast<float *>(w + L.dvec);
     p.lse2 = reinterpret_cast<float *>(w + L.lse2);

@@ -15,57 +15,120 @@ __device__ __forceinline__ int seq_len_q(const BwdParams &p, int b) { return use
 __device__ __forceinline__ int seq_len_k(const BwdParams &p, int b) { return used_len_k(p, b); }
 
 // ------------------------------------------------------------------ schedule
-// Work units in the order (n_block, sequence, kv head): every unit of a given
-// (sequence, kv head) comes after the units with smaller n_block, which the
-// deterministic dQ order relies on, and under a causal mask the units with the
-// most query blocks (small n_block) come first.  One block of 1024 threads.
-__global__ void __launch_bounds__(1024) schedule_kernel(BwdParams p) {
-    __shared__ int warp_sums[32];
-    __shared__ int total_s;
+// Block-wide exclusive scan of one int per thread (1024 threads); returns the
+// exclusive prefix and leaves the block total in *total.
+__device__ __forceinline__ int block_excl_scan(int v, int *warp_sums, int *total) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int s = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        warp_sums[lane] = s;   // inclusive
+        if (lane == 31) *total = s;
+    }
+    __syncthreads();
+    const int r = x - v + (wid > 0 ? warp_sums[wid - 1] : 0);
+    __syncthreads();
+    return r;
+}
+
+// Work units of a varlen problem.  Consecutive sequences form a group once
+// their units reach p.unit_group (about 1.5 grids of the main kernel), and
+// inside a group the units go in the order (n_block, sequence, kv head): the
+// units that run at the same time then sweep the rows of a few sequences,
+// whose Q, dO and dQ-accumulator rows stay in L2 (over all sequences at once
+// they did not: the varlen workload's main kernel moved 1.07 GB of DRAM
+// traffic against about 0.4 GB algorithmic).  Every unit of a (sequence, kv
+// head) still comes after those with a smaller n_block, which the
+// deterministic dQ order relies on, and under a causal mask a group's units
+// with the most query blocks come first.  One block of 1024 threads; more
+// than kSchedSeqs sequences, and the deterministic order (unit_group 0: few
+// units of one ordering chain should run at once), take the ungrouped order.
+constexpr int kSchedSeqs = 4096;
+__global__ void __launch_bounds__(1024) schedule_kernel(BwdParams p) {
+    __shared__ int s_nb[kSchedSeqs];    // key blocks of sequence b (0: none)
+    __shared__ int s_off[kSchedSeqs];   // units of the sequences before b
+    __shared__ int warp_sums[32];
+    __shared__ int chunk_total;
+    const int tid = threadIdx.x;
     const int max_nb = (p.Sk + kBlockN - 1) / kBlockN;
+    if (p.unit_group > 0 && p.B <= kSchedSeqs) {
+        for (int b = tid; b < p.B; b += 1024) {
+            int nb = 0;
+            // a sequence whose lengths break the planned layout gets no unit
+            // (and the call reports the error)
+            if (!varlen_seq_ok(p, b)) atomicOr(p.err, kErrBadLength);
+            else nb = (seq_len_k(p, b) + kBlockN - 1) / kBlockN;
+            s_nb[b] = nb;
+        }
+        __syncthreads();
+        int carry = 0;
+        for (int b0 = 0; b0 < p.B; b0 += 1024) {
+            const int b = b0 + tid;
+            const int c = b < p.B ? s_nb[b] * p.Hkv : 0;
+            const int e = block_excl_scan(c, warp_sums, &chunk_total);
+            if (b < p.B) s_off[b] = carry + e;
+            carry += chunk_total;
+            __syncthreads();
+        }
+        const int T = max(p.unit_group, 1);
+        for (int b = tid; b < p.B; b += 1024) {
+            const int nb = s_nb[b];
+            if (nb == 0) continue;
+            const int g = s_off[b] / T;
+            int bs = b, be = b + 1;   // the group: sequences [bs, be)
+            while (bs > 0 && s_off[bs - 1] / T == g) --bs;
+            while (be < p.B && s_off[be] / T == g) ++be;
+            long long idx0 = s_off[bs];   // the group's first unit, then past smaller n blocks
+            for (int n = 0; n < nb; ++n) {
+                int rank = 0, act = 0;    // group sequences with block n: before b, in all
+                for (int b2 = bs; b2 < be; ++b2)
+                    if (s_nb[b2] > n) {
+                        ++act;
+                        if (b2 < b) ++rank;
+                    }
+                for (int hk = 0; hk < p.Hkv; ++hk) {
+                    const long long idx = idx0 + (long long)rank * p.Hkv + hk;
+                    if (idx < p.max_tiles) p.tiles[idx] = make_int4(b, n, hk, 0);
+                }
+                idx0 += (long long)act * p.Hkv;
+            }
+        }
+        if (tid == 0) *p.ntiles = min(carry, p.max_tiles);
+        return;
+    }
+    // ungrouped: (n_block, sequence, kv head)
     int base = 0;
     for (int n = 0; n < max_nb; ++n) {
         for (int b0 = 0; b0 < p.B; b0 += 1024) {
             const int b = b0 + tid;
             int flag = 0;
             if (b < p.B) {
-                // a sequence whose lengths break the planned layout gets no unit
-                // (and the call reports the error)
-                if (p.varlen && !varlen_seq_ok(p, b)) {
+                if (!varlen_seq_ok(p, b)) {
                     if (n == 0) atomicOr(p.err, kErrBadLength);
                 } else {
                     flag = seq_len_k(p, b) > n * kBlockN;
                 }
             }
-            // block-wide exclusive scan of flag
-            int x = flag;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                int y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
-            }
-            if (lane == 31) warp_sums[wid] = x;
-            __syncthreads();
-            if (wid == 0) {
-                int s = warp_sums[lane];
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    int y = __shfl_up_sync(0xffffffffu, s, o);
-                    if (lane >= o) s += y;
-                }
-                warp_sums[lane] = s;   // inclusive
-                if (lane == 31) total_s = s;
-            }
-            __syncthreads();
-            const int pos = x - flag + (wid > 0 ? warp_sums[wid - 1] : 0);
+            const int pos = block_excl_scan(flag, warp_sums, &chunk_total);
             if (flag) {
                 for (int hk = 0; hk < p.Hkv; ++hk) {
                     const long long idx = (long long)(base + pos) * p.Hkv + hk;
                     if (idx < p.max_tiles) p.tiles[idx] = make_int4(b, n, hk, 0);
                 }
             }
-            base += total_s;
+            base += chunk_total;
             __syncthreads();
         }
     }

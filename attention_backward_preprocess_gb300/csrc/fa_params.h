@@ -63,8 +63,9 @@ struct BwdParams {
     int4 *tiles;        // work units (b, n_block, hk, 0)
     int *ntiles;        // varlen: number of work units written by the scheduler
     int num_units;      // dense: B * ceil(Sk / 128) * Hkv work units
-    int unit_group;     // dense: (batch, kv head) pairs per group of the unit order;
-                        // divides B * Hkv
+    int unit_group;     // dense: (batch, kv head) pairs per group of the unit order,
+                        // divides B * Hkv; varlen: units per group of sequences
+                        // (0: no groups)
     int *unit_counter;  // [0] next work unit to hand out, [1] CTAs that ran out;
                         // reset by the last CTA of each launch (and by the preprocess)
     int max_tiles;
