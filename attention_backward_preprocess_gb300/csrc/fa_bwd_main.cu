@@ -226,6 +226,10 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
     // two 32-query chunks per softmax warp (D = 64): the two 16-lane halves of
     // a TMEM tile are loaded one after the other (register pressure)
     constexpr bool kSplitH = NCH == 2;
+    // D = 64 without dropout: the dS pass reads P^T back from tensor memory
+    // (the rounded operand of dV) instead of keeping the step's 64 fp32
+    // values of P per thread in registers between the passes
+    constexpr bool kPFromTmem = NCH == 2 && !kDrop;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1095,8 +1099,10 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                                     if (lim_lo + kr < 8 * k + 1) pv1 = 0.f;
                                 }
                                 if (kb + kr >= u.lk) { pv0 = 0.f; pv1 = 0.f; }
-                                P[32 * ch + 16 * h + 4 * k + 2 * r] = pv0;
-                                P[32 * ch + 16 * h + 4 * k + 2 * r + 1] = pv1;
+                                if (!kPFromTmem) {
+                                    P[32 * ch + 16 * h + 4 * k + 2 * r] = pv0;
+                                    P[32 * ch + 16 * h + 4 * k + 2 * r + 1] = pv1;
+                                }
                                 if (kDrop) {
                                     // dV takes the dropped-out, rescaled P
                                     pk[2 * k + r] = Cvt<T>::pack(keep0 ? pv0 * p.drop_scale : 0.f,
@@ -1121,7 +1127,9 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch) {
                     uint32_t dr[2][16];
+                    uint32_t pt[2][8];   // kPFromTmem: P^T pairs of the chunk, per 16-lane half
                     tmem_ld16x256(lane_addr + C::dp_col(grp, ch), dr[0]);
+                    if (kPFromTmem) tmem_ld16x128(lane_addr + C::p_col(cb, grp, ch), pt[0]);
                     if (!kSplitH) tmem_ld16x256(lane_addr + (16u << 16) + C::dp_col(grp, ch), dr[1]);
                     const int c0 = grp * HALF + 32 * ch;
                     uint64_t dd[4];   // Dv of the thread's query pairs
@@ -1147,6 +1155,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     for (int h = 0; h < 2; ++h) {
                         if (kSplitH && h == 1) {
                             tmem_ld16x256(lane_addr + (16u << 16) + C::dp_col(grp, ch), dr[1]);
+                            if (kPFromTmem) tmem_ld16x128(lane_addr + (16u << 16) + C::p_col(cb, grp, ch), pt[1]);
                             tmem_wait_ld();
                             if (ch == NCH - 1) {
                                 // the last half of dP^T read: X is free again
@@ -1168,7 +1177,10 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                                     const uint32_t k1b = (kb32[ch] >> (4 * (2 * k + 1) + 2 * h + r)) & 1u;
                                     dpv = f2_mul(dpv, f2_pack(k0b ? p.drop_scale : 0.f, k1b ? p.drop_scale : 0.f));
                                 }
-                                const float2 ds = f2_unpack(f2_mul(f2_pack(P[e0], P[e0 + 1]), f2_sub(dpv, dd[k])));
+                                float2 pp;
+                                if (kPFromTmem) pp = Cvt<T>::unpack(pt[h][2 * k + r]);
+                                else pp = make_float2(P[e0], P[e0 + 1]);
+                                const float2 ds = f2_unpack(f2_mul(f2_pack(pp.x, pp.y), f2_sub(dpv, dd[k])));
                                 pk[2 * k + r] = Cvt<T>::pack(ds.x, ds.y);
                                 if (kBias && dbias_h) {   // dBias = dS, inside the used lengths
                                     const int qi0 = m0 + c0 + 8 * k + 2 * q4, kj = kb + 16 * h + 8 * r;

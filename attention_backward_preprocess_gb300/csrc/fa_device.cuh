@@ -444,6 +444,14 @@ __device__ __forceinline__ void tmem_ld16x256(uint32_t taddr, uint32_t (&r)[16])
 // goes to lane lane_base + t / 4 + 8e, column col + 4k + t % 4.  With 16-bit
 // pairs packed per column this is the same (lane, element) set as
 // tmem_ld16x256 reads from a 32-bit matrix.
+// The 16x128b shape read back: the registers tmem_st16x128 wrote.
+__device__ __forceinline__ void tmem_ld16x128(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.16x128b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_st16x128(uint32_t taddr, const uint32_t (&r)[8]) {
     asm volatile(
         "tcgen05.st.sync.aligned.16x128b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
