@@ -223,13 +223,14 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                    kBias = (kFlags & kFBias) != 0, kDrop = (kFlags & kFDrop) != 0;
     // ALiBi with no visible key right of the diagonal: -slope |d| = slope d
     constexpr bool kAlibiLin = kAlibi && (kFlags & kFAbs) == 0;
-    // two 32-query chunks per softmax warp (D = 64): the two 16-lane halves of
-    // a TMEM tile are loaded one after the other (register pressure)
-    constexpr bool kSplitH = NCH == 2;
     // D = 64 without dropout: the dS pass reads P^T back from tensor memory
     // (the rounded operand of dV) instead of keeping the step's 64 fp32
     // values of P per thread in registers between the passes
     constexpr bool kPFromTmem = NCH == 2 && !kDrop;
+    // two 32-query chunks per softmax warp (D = 64) with P kept in registers:
+    // the two 16-lane halves of a TMEM tile are loaded one after the other
+    // (register pressure)
+    constexpr bool kSplitH = NCH == 2 && !kPFromTmem;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1131,6 +1132,8 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                     tmem_ld16x256(lane_addr + C::dp_col(grp, ch), dr[0]);
                     if (kPFromTmem) tmem_ld16x128(lane_addr + C::p_col(cb, grp, ch), pt[0]);
                     if (!kSplitH) tmem_ld16x256(lane_addr + (16u << 16) + C::dp_col(grp, ch), dr[1]);
+                    if (kPFromTmem && !kSplitH)
+                        tmem_ld16x128(lane_addr + (16u << 16) + C::p_col(cb, grp, ch), pt[1]);
                     const int c0 = grp * HALF + 32 * ch;
                     uint64_t dd[4];   // Dv of the thread's query pairs
 #pragma unroll
