@@ -334,11 +334,10 @@ fa_status apply_ext(fa::BwdParams &p, int causal, const fa_ext *ext) {
     if (causal) p.win_hi = std::min(p.win_hi, 0);
     if (wide_dims(p.Dh, p.Dhv)) {
         // the wide kernel's tile widths (128 or 256 on each side); it has the
-        // plain mask only (causal or an upper band edge, used lengths)
+        // band masks (causal, both window edges) and used lengths
         p.D = p.Dh <= 128 ? 128 : 256;
         p.Dv = value_tile(p.Dh, p.Dhv);
-        if (p.win_lo < fa::kNoWindow || p.alibi || p.bias || p.dbias || p.drop_t > 0)
-            return FA_ERR_UNSUPPORTED;
+        if (p.alibi || p.bias || p.dbias || p.drop_t > 0) return FA_ERR_UNSUPPORTED;
     }
     return FA_OK;
 }

@@ -22,9 +22,10 @@
 //
 // Tile widths DQ, DV are 128 or 256; the tensor maps fill the columns past
 // Dqk / Dv with zeros, which adds nothing to the products.  The masks, causal
-// skipping, varlen units and used lengths are those of the main kernel; the
-// band with a lower edge, ALiBi, the bias, dropout and the deterministic order
-// are not built for these head dims (the host refuses them).
+// skipping, varlen units and used lengths are those of the main kernel, the
+// band with a lower edge (a left window) in an instance of its own (kBand);
+// ALiBi, the bias, dropout and the deterministic order are not built for these
+// head dims (the host refuses them).
 //
 // Warp roles (12 warps): 0 TMA producer | 1 MMA warp A (S^T, dP^T; allocates
 // tensor memory) | 2 MMA warp B (dV, dK, dQ^T) | 3 idle | 4-7 dQ reducers |
@@ -101,7 +102,7 @@ struct WideMaps {
     CUtensorMap q, k, v, dout;
 };
 
-template <int kDQ, int kDV, typename T>
+template <int kDQ, int kDV, typename T, bool kBand>
 __global__ void __launch_bounds__(WideCfg<kDQ, kDV, T>::kThreads, 1)
     bwd_wide_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ WideMaps maps) {
     using C = WideCfg<kDQ, kDV, T>;
@@ -423,10 +424,12 @@ __global__ void __launch_bounds__(WideCfg<kDQ, kDV, T>::kThreads, 1)
             const bool key_ok = kj < u.lk;
             const int kb = n0 + quarter * 32 + g4;  // first key of this thread's 16-lane rows
             const int diag = u.lk - u.lq;
-            const int whi = p.win_hi;
+            const int whi = p.win_hi, wlo = p.win_lo;
             for (int it = 0; it < u.iters; ++it) {
                 const int m0 = u.m_of(it, p.G) * BM;
                 const bool masked_hi = n0 + BN - 1 - (m0 + diag) > whi;
+                // kBand: some element of the tile lies below the band's lower edge
+                const bool masked_lo = kBand && n0 - (m0 + BM - 1 + diag) < -wlo;
                 if (!(ok = mbar_wait(bar(W_STAGE0 + stage), st_ph, w))) break;
                 if (!(ok = mbar_wait(bar(W_S_FULL + cb), bit(s_ph, cb), w))) break;
                 s_ph ^= 1u << cb;
@@ -449,6 +452,7 @@ __global__ void __launch_bounds__(WideCfg<kDQ, kDV, T>::kThreads, 1)
                     const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
                     tmem_wait_ld();
                     const int lim_hi = kb - (m0 + diag) - 2 * q4 - whi;
+                    const int lim_lo = kb - (m0 + diag) - 2 * q4 + wlo;
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         uint32_t pk[8];
@@ -465,6 +469,10 @@ __global__ void __launch_bounds__(WideCfg<kDQ, kDV, T>::kThreads, 1)
                                 if (masked_hi) {   // key - query - diag > whi
                                     if (lim_hi + kr > 8 * k) pv0 = 0.f;
                                     if (lim_hi + kr > 8 * k + 1) pv1 = 0.f;
+                                }
+                                if (kBand && masked_lo) {   // key - query - diag < -wlo
+                                    if (lim_lo + kr < 8 * k) pv0 = 0.f;
+                                    if (lim_lo + kr < 8 * k + 1) pv1 = 0.f;
                                 }
                                 if (kb + kr >= u.lk) { pv0 = 0.f; pv1 = 0.f; }
                                 P[16 * h + 4 * k + 2 * r] = pv0;
@@ -603,7 +611,9 @@ __global__ void __launch_bounds__(WideCfg<kDQ, kDV, T>::kThreads, 1)
 template <int kDQ, int kDV, typename T>
 static cudaError_t launch_wide_t(const BwdParams &p, const WideMaps &maps, int grid, cudaStream_t stream) {
     using C = WideCfg<kDQ, kDV, T>;
-    auto kern = bwd_wide_kernel<kDQ, kDV, T>;
+    // a lower band edge has an instance of its own: its per-element test slows
+    // the plain kernel even when skipped
+    auto kern = p.win_lo < kNoWindow ? bwd_wide_kernel<kDQ, kDV, T, true> : bwd_wide_kernel<kDQ, kDV, T, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     kern<<<grid, C::kThreads, C::SMEM_BYTES, stream>>>(p, maps);

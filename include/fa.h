@@ -34,9 +34,10 @@
  *   (fa_ext head_dim_v: v, o, dout, dv then have Dv columns), in a second
  *   kernel that produces dK / dV / dQ in 128-column halves (32 queries x 128
  *   keys per step, S and dP recomputed per half).  That kernel has the causal
- *   mask, an upper band edge, varlen and used lengths, but not the lower
- *   band edge, ALiBi, the bias, dropout or the deterministic order
- *   (FA_ERR_UNSUPPORTED), and the forward does not run these head dims yet.
+ *   mask, both band edges of a local window, varlen and used lengths, but
+ *   not ALiBi, the bias, dropout or the deterministic order
+ *   (FA_ERR_UNSUPPORTED); fa_fwd / fa_fwd_ext run these head dims with the
+ *   same masks.
  *   varlen: cu_seqlens_q / cu_seqlens_k != NULL (both or neither): int32
  *           device arrays of B+1 prefix sums; tensors packed [total, H, D];
  *           lse fp32 [Hq, total_q]; Sq / Sk are the MAXIMUM lengths.  A

@@ -251,7 +251,6 @@ HEAD_DIMS = [
     ((128, 4), {}, 0, 2),          # Dv below 8
     ((128, 260), {}, 0, 2),        # Dv above 256
     ((192, 0), {}, 1, 2),          # wide kernel: no deterministic order
-    ((192, 0), dict(window_left=8), 0, 2),
     ((128, 96), dict(dropout_p=0.1), 0, 2),
     ((192, 0), dict(alibi_slopes=0x2000), 0, 2),
 ]

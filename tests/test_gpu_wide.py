@@ -40,10 +40,11 @@ def make_case(oracle_mod, B, Sq, Sk, Hq, Hkv, D, Dv, dtype=torch.bfloat16, causa
     return x
 
 
-def oracle_grads(oracle_mod, x):
+def oracle_grads(oracle_mod, x, window=None):
+    kw = {} if window is None else dict(window=window)
     return oracle_mod.backward(to64(x["q"]), to64(x["k"]), to64(x["v"]), to64(x["dout"]),
                                x["scale"], x["causal"], o=to64(x["o"]), lse=to64(x["lse"]),
-                               cu_q=x["cu"], cu_k=x["cu"])
+                               cu_q=x["cu"], cu_k=x["cu"], **kw)
 
 
 def gpu_grads(fa, x, outs=None, **kw):
@@ -120,13 +121,12 @@ def test_wide_refusals(fa, oracle_mod, cuda_device):
     x = make_case(oracle_mod, 1, 64, 64, 2, 2, 192, 192, torch.bfloat16, True, seed=1)
     g = {n: x[n].cuda() for n in ("q", "k", "v", "dout", "o", "lse")}
     args = (g["q"], g["k"], g["v"], g["o"], g["dout"], g["lse"])
-    for kw in (dict(deterministic=True), dict(window=(16, -1)),
-               dict(alibi_slopes=torch.ones(2, device="cuda"))):
+    for kw in (dict(deterministic=True), dict(alibi_slopes=torch.ones(2, device="cuda"))):
         with pytest.raises(fa.FaError) as e:
             fa.fa_bwd(*args, causal=True, **kw)
         assert e.value.status == fa.FA_ERR_UNSUPPORTED
     with pytest.raises(fa.FaError) as e:
-        fa.fa_fwd(g["q"], g["k"], g["v"], causal=True, window=(16, -1))
+        fa.fa_fwd(g["q"], g["k"], g["v"], causal=True, alibi_slopes=torch.ones(2, device="cuda"))
     assert e.value.status == fa.FA_ERR_UNSUPPORTED
 
 
@@ -164,6 +164,48 @@ def test_wide_varlen_forward_then_backward(fa, oracle_mod, cuda_device, D, Dv):
     torch.cuda.synchronize()
     rq, rk, rv = oracle_mod.backward(to64(x["q"]), to64(x["k"]), to64(x["v"]), to64(x["dout"]),
                                      x["scale"], True, cu_q=x["cu"], cu_k=x["cu"])
+    check_bar(dq, rq, "dq")
+    check_bar(dk, rk, "dk")
+    check_bar(dv, rv, "dv")
+
+
+WINDOWS = [
+    # (B, Sq, Sk, Hq, Hkv, D, Dv, causal, window, lengths)
+    (1, 300, 300, 4, 2, 256, 256, True, (100, 0), None),
+    (2, 260, 260, 2, 1, 192, 128, False, (64, 32), None),
+    (1, 200, 330, 2, 2, 128, 256, True, (40, -1), None),
+    (3, 0, 0, 4, 2, 256, 256, True, (70, 0), [260, 1, 131]),
+]
+
+
+@pytest.mark.parametrize("case", WINDOWS, ids=lambda c: "d%d_dv%d_w%d_%d%s" % (
+    c[5], c[6], c[8][0], c[8][1], "_varlen" if c[9] else ""))
+def test_wide_window_matches_oracle(fa, oracle_mod, cuda_device, case):
+    """A left (and right) window at head dims above 128 or Dv != D: the
+    forward against the oracle's fp64 forward, then the backward from the
+    oracle's O / LSE against its gradients."""
+    B, Sq, Sk, Hq, Hkv, D, Dv, causal, window, lengths = case
+    x = make_case(oracle_mod, B, Sq, Sk, Hq, Hkv, D, Dv, torch.bfloat16, causal,
+                  lengths=lengths, seed=D + Dv + window[0])
+    # the inputs' O / LSE from the oracle's forward with the window
+    o64, lse64 = oracle_mod.forward(to64(x["q"]), to64(x["k"]), to64(x["v"]), x["scale"], causal,
+                                    cu_q=x["cu"], cu_k=x["cu"], window=window)
+    x["o"] = torch.from_numpy(o64).to(torch.bfloat16)
+    x["lse"] = torch.from_numpy(lse64).float()
+    kw = dict(window=window)
+    vl = {}
+    if x["cu"] is not None:
+        cu = torch.from_numpy(x["cu"]).cuda()
+        vl = dict(cu_seqlens_q=cu, cu_seqlens_k=cu, max_seqlen_q=x["max_len"],
+                  max_seqlen_k=x["max_len"])
+    q, k, v = x["q"].cuda(), x["k"].cuda(), x["v"].cuda()
+    o, lse = fa.fa_fwd(q, k, v, causal=causal, softmax_scale=x["scale"], **vl, **kw)
+    torch.cuda.synchronize()
+    assert fa.device_status() == fa.FA_OK
+    check_bar(o, to64(x["o"]), "o")
+    dq, dk, dv = gpu_grads(fa, x, **kw)
+    assert fa.device_status() == fa.FA_OK
+    rq, rk, rv = oracle_grads(oracle_mod, x, window=window)
     check_bar(dq, rq, "dq")
     check_bar(dk, rk, "dk")
     check_bar(dv, rv, "dv")
