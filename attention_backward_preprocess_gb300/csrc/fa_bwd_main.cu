@@ -883,11 +883,14 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         uint32_t epi_ph = 0;             // parity of this group's staging-tile barriers
         int stage = 0, cb = 0, db = 0;   // stage, S buffer, dS^T tile of the step
         bool ok = true;
-        // D = 128: the next unit is taken from the ring and decoded before the
-        // current one's dK / dV epilogue, while the accumulators are still
-        // being completed, rather than after it (about 1300 cycles per unit).
-        // D = 64 keeps the order (measured: the early fetch cost it spills).
-        constexpr bool kEarlyFetch = D == 128;
+        // Taking the next unit from the ring and decoding it before the dK / dV
+        // epilogue, rather than after it (about 1300 cycles per unit), was
+        // measured and is off: 1 % faster on the 2k causal workload, but the
+        // build that had it ran the deterministic order 25 % slower (24.6-24.9
+        // against 19.2-20.0 ms on B = 1, 16 heads, 32768 keys), even with the
+        // early fetch switched off at run time there -- register allocation at
+        // the 128-register cap, not the order of the fetch.
+        constexpr bool kEarlyFetch = false;
         int t = -1;
         Unit un;
         auto fetch = [&]() __attribute__((always_inline)) {
