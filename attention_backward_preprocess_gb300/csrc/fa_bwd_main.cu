@@ -214,6 +214,58 @@ constexpr int kMainFlagSets[] = {0,
                                  kFBand | kFDrop,
                                  kFBand | kFAlibi | kFAbs | kFBias | kFDrop};
 
+// The elementwise bias of one 32-query chunk (from query qc) x a softmax
+// warp's 32 keys (from key kw), 8 queries (k) at a time: one 16-byte load per
+// lane (lane L: query 8k + 2(L%4) + (L/4)%2, keys 8(L/8) .. +7), all 32 lanes
+// together 8 rows of 64 contiguous bytes.  0 past the used lengths lq / lk.
+// Rows start on 16-byte boundaries (base and row stride are checked on the
+// host); the ragged end of the used keys is read element by element.
+template <typename T>
+__device__ __forceinline__ void load_bias_chunk(uint32_t (&bw)[4][4], const T *bias_h, long long rs, int qc,
+                                                int kw, int lq, int lk, int lane) {
+    const int bq = ((lane & 3) << 1) | ((lane >> 2) & 1);
+    const int bk = kw + 8 * (lane >> 3);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int qi = qc + 8 * k + bq;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (qi < lq && bk < lk) {
+            const T *src = bias_h + (long long)qi * rs + bk;
+            if (bk + 8 <= lk) {
+                v = __ldg(reinterpret_cast<const uint4 *>(src));
+            } else {
+                const uint16_t *s16 = reinterpret_cast<const uint16_t *>(src);
+                uint32_t e[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) e[i] = bk + i < lk ? (uint32_t)__ldg(s16 + i) : 0u;
+                v = make_uint4(e[0] | e[1] << 16, e[2] | e[3] << 16, e[4] | e[5] << 16, e[6] | e[7] << 16);
+            }
+        }
+        bw[k][0] = v.x;
+        bw[k][1] = v.y;
+        bw[k][2] = v.z;
+        bw[k][3] = v.w;
+    }
+}
+
+// load_bias_chunk's words into the order of the S^T registers: bw[k][2h + r]
+// = the (query 8k + 2q4, 8k + 2q4 + 1) pair of key g4 + 16h + 8r (lane = 4 g4
+// + q4).  As loaded, the lane bits (from the top) hold key bits 4, 3, query
+// bit 0 and query bits 2, 1, the register bits key bits 2, 1 and the half
+// key bit 0; key bits 4 and 3 trade places with the register bits, query bit
+// 0 with the half.
+__device__ __forceinline__ void bias_to_st_order(uint32_t (&bw)[4][4], int lane) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        xchg_lane_reg(bw[k][0], bw[k][2], 16, lane & 16);
+        xchg_lane_reg(bw[k][1], bw[k][3], 16, lane & 16);
+        xchg_lane_reg(bw[k][0], bw[k][1], 8, lane & 8);
+        xchg_lane_reg(bw[k][2], bw[k][3], 8, lane & 8);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) bw[k][i] = xchg_lane_half(bw[k][i], 4, lane & 4);
+    }
+}
+
 template <int kD, typename T, int kFlags>
 __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
     bwd_main_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ MainMaps maps) {
@@ -223,14 +275,17 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                    kBias = (kFlags & kFBias) != 0, kDrop = (kFlags & kFDrop) != 0;
     // ALiBi with no visible key right of the diagonal: -slope |d| = slope d
     constexpr bool kAlibiLin = kAlibi && (kFlags & kFAbs) == 0;
-    // D = 64 without dropout: the dS pass reads P^T back from tensor memory
-    // (the rounded operand of dV) instead of keeping the step's 64 fp32
-    // values of P per thread in registers between the passes
-    constexpr bool kPFromTmem = NCH == 2 && !kDrop;
+    // D = 64, or an elementwise bias, without dropout: the dS pass reads P^T
+    // back from tensor memory (the rounded operand of dV) instead of keeping
+    // the step's fp32 values of P per thread in registers between the passes
+    // (with a bias the registers hold the bias chunk meanwhile)
+    constexpr bool kPFromTmem = (NCH == 2 || kBias) && !kDrop;
     // two 32-query chunks per softmax warp (D = 64) with P kept in registers:
     // the two 16-lane halves of a TMEM tile are loaded one after the other
     // (register pressure)
     constexpr bool kSplitH = NCH == 2 && !kPFromTmem;
+    // the bias chunk loaded at the top of the step (else at the chunk's start)
+    constexpr bool kEarlyBias = kBias && NCH == 1 && kPFromTmem;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -883,6 +938,8 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
         uint32_t epi_ph = 0;             // parity of this group's staging-tile barriers
         int stage = 0, cb = 0, db = 0;   // stage, S buffer, dS^T tile of the step
         bool ok = true;
+        // dBias rows take 16-byte stores when every row starts on a 16-byte boundary
+        const bool dbias_v4 = kBias && (reinterpret_cast<uintptr_t>(p.dbias) & 15u) == 0 && (p.Sk & 7) == 0;
         // Taking the next unit from the ring and decoding it before the dK / dV
         // epilogue, rather than after it (about 1300 cycles per unit), was
         // measured and is off: 1 % faster on the 2k causal workload, but the
@@ -925,27 +982,22 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 // (dense problems): element (query qi, key kj) at qi * stride + kj
                 const T *bias_h = nullptr;
                 uint16_t *dbias_h = nullptr;
-                if (kBias) {
+                uint32_t bw[4][4];   // bias of one 32-query chunk (load_bias_chunk)
+                if constexpr (kBias) {
                     const int hq = u.hk * p.G + u.g_of(it, p.G);
-                    if (p.bias)
+                    if (p.bias) {
                         bias_h = reinterpret_cast<const T *>(p.bias) + (long long)u.b * p.bias_bs +
                                  (long long)hq * p.bias_hs;
+                        // one chunk per warp (D = 128) and P not held in
+                        // registers: loaded before S is ready, so that the
+                        // wait covers the loads' latency
+                        if (kEarlyBias)
+                            load_bias_chunk(bw, bias_h, p.bias_rs, m0 + grp * HALF, n0 + quarter * 32, u.lq,
+                                            u.lk, lane);
+                    }
                     if (p.dbias)
                         dbias_h = reinterpret_cast<uint16_t *>(p.dbias) +
                                   ((long long)u.b * p.Hq + hq) * p.Sq * p.Sk;
-                    // bring the step's bias tile (BM query rows x 128 keys, two
-                    // 128-byte lines per row) into L1 before S is ready: the
-                    // loads below then wait on L1, not on HBM (C2 with a bias:
-                    // 1.24 -> 1.04 ms; prefetching one step further ahead gained
-                    // nothing more)
-                    if (bias_h) {
-                        const int t = (warp - C::W_SM) * 32 + lane;   // 0 .. 8 * 32 - 1
-                        for (int li = t; li < 2 * BM; li += 8 * 32) {
-                            const int qi = m0 + (li >> 1), kj = n0 + 64 * (li & 1);
-                            if (qi < u.lq && kj < u.lk)
-                                asm volatile("prefetch.global.L1 [%0];" ::"l"(bias_h + (long long)qi * p.bias_rs + kj));
-                        }
-                    }
                 }
                 // dropout: drawn before S is ready (the wait hides it).  Lane L
                 // draws the random bytes of query c0 + L of each chunk for the
@@ -1032,8 +1084,15 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                         const float2 l = ld_shared_f32x2(lse2 + 4 * (c0 + 8 * k + 2 * q4));
                         nl2[k] = f2_pack(-l.x, -l.y);
                     }
+                    if constexpr (kBias) {
+                        if (!kEarlyBias && bias_h)
+                            load_bias_chunk(bw, bias_h, p.bias_rs, m0 + c0, n0 + quarter * 32, u.lq, u.lk, lane);
+                    }
                     const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
                     tmem_wait_ld();
+                    if constexpr (kBias) {
+                        if (bias_h) bias_to_st_order(bw, lane);
+                    }
                     // element (key kb + kr, query column 8k + e) has
                     // kj - qi - diag = lim + kr - 8k - e
                     const int lim = kb - (m0 + c0 + diag) - 2 * q4;
@@ -1074,18 +1133,10 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                                     x0 = fmaf(-slope2, fabsf(fd), x0);
                                     x1 = fmaf(-slope2, fabsf(fd - 1.f), x1);
                                 }
-                                {
-                                    if (kBias && bias_h) {   // + bias * log2e (0 past the used lengths)
-                                        const int qi0 = m0 + c0 + 8 * k + 2 * q4, kj = kb + kr;
-                                        float b0 = 0.f, b1 = 0.f;
-                                        if (kj < u.lk) {
-                                            if (qi0 < u.lq) b0 = static_cast<float>(bias_h[(long long)qi0 * p.bias_rs + kj]);
-                                            if (qi0 + 1 < u.lq)
-                                                b1 = static_cast<float>(bias_h[(long long)(qi0 + 1) * p.bias_rs + kj]);
-                                        }
-                                        x0 = fmaf(b0, 1.4426950408889634f, x0);
-                                        x1 = fmaf(b1, 1.4426950408889634f, x1);
-                                    }
+                                if (kBias && bias_h) {   // + bias * log2e (0 past the used lengths)
+                                    const float2 bb = Cvt<T>::unpack(bw[k][2 * h + r]);
+                                    x0 = fmaf(bb.x, 1.4426950408889634f, x0);
+                                    x1 = fmaf(bb.y, 1.4426950408889634f, x1);
                                 }
                                 float pv0 = ex2(x0);
                                 float pv1 = ex2(x1);
@@ -1188,15 +1239,6 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                                 else pp = make_float2(P[e0], P[e0 + 1]);
                                 const float2 ds = f2_unpack(f2_mul(f2_pack(pp.x, pp.y), f2_sub(dpv, dd[k])));
                                 pk[2 * k + r] = Cvt<T>::pack(ds.x, ds.y);
-                                if (kBias && dbias_h) {   // dBias = dS, inside the used lengths
-                                    const int qi0 = m0 + c0 + 8 * k + 2 * q4, kj = kb + 16 * h + 8 * r;
-                                    if (kj < u.lk) {
-                                        if (qi0 < u.lq)
-                                            dbias_h[(long long)qi0 * p.Sk + kj] = (uint16_t)(pk[2 * k + r] & 0xFFFFu);
-                                        if (qi0 + 1 < u.lq)
-                                            dbias_h[(long long)(qi0 + 1) * p.Sk + kj] = (uint16_t)(pk[2 * k + r] >> 16);
-                                    }
-                                }
                             }
                         }
                         tmem_st16x128(lane_addr + ((uint32_t)(16 * h) << 16) + C::ds_col(cb, grp, ch), pk);
@@ -1212,6 +1254,43 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                             const int half = i0 / 64, cidx = (i0 % 64) / 8;
                             const uint32_t row = sds + half * (BN * 128) + jr * 128 + ((cidx ^ (lane & 7)) << 4);
                             stmatrix_x4(row, pk[r], pk[2 + r], pk[4 + r], pk[6 + r]);
+                        }
+                    }
+                    if (kBias && dbias_h) {
+                        // dBias = dS, inside the used lengths: the warp's 32 keys x
+                        // the chunk's queries, read back transposed from its own
+                        // part of the dS^T tile (before the MMAs are told it is
+                        // full; nothing else writes that part meanwhile), 8
+                        // queries at a time.  Thread t supplies key row t of the
+                        // warp (matrix t/8) and gets query 8k + t/4, keys 8i +
+                        // 2(t%4) (+1) in register i; two exchanges give it keys
+                        // 8(t%4) .. +7 instead: one 16-byte store, 8 rows of 64
+                        // contiguous bytes per warp.
+                        __syncwarp();
+                        const int jr = quarter * 32 + lane;
+                        const int kj = n0 + quarter * 32 + 8 * (lane & 3);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int i0 = c0 + 8 * k;
+                            const int half = i0 / 64, cidx = (i0 % 64) / 8;
+                            uint32_t d[4];
+                            ldmatrix_x4_trans(sds + half * (BN * 128) + jr * 128 + ((cidx ^ (lane & 7)) << 4), d[0],
+                                              d[1], d[2], d[3]);
+                            xchg_lane_reg(d[0], d[2], 2, lane & 2);
+                            xchg_lane_reg(d[1], d[3], 2, lane & 2);
+                            xchg_lane_reg(d[0], d[1], 1, lane & 1);
+                            xchg_lane_reg(d[2], d[3], 1, lane & 1);
+                            const int qi = m0 + i0 + (lane >> 2);
+                            if (qi < u.lq && kj < u.lk) {
+                                uint16_t *dst = dbias_h + (long long)qi * p.Sk + kj;
+                                if (dbias_v4 && kj + 8 <= u.lk) {
+                                    *reinterpret_cast<uint4 *>(dst) = make_uint4(d[0], d[1], d[2], d[3]);
+                                } else {
+#pragma unroll
+                                    for (int i = 0; i < 8; ++i)
+                                        if (kj + i < u.lk) dst[i] = (uint16_t)(d[i >> 1] >> (16 * (i & 1)));
+                                }
+                            }
                         }
                     }
                 }

@@ -135,6 +135,36 @@ __device__ __forceinline__ void stmatrix_x4_trans(uint32_t row_addr, uint32_t r0
                  : "memory");
 }
 
+// Four 8x8 16-bit matrices from shared memory, transposed: register i of
+// thread t holds elements (row 2(t%4) + e, column t/4), e = 0 (low half) and
+// 1, of matrix i; thread t supplies the address of row t%8 of matrix t/8.
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t row_addr, uint32_t &r0, uint32_t &r1,
+                                                  uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(row_addr)
+                 : "memory");
+}
+
+// Warp-wide exchanges that move one bit of an element's position between the
+// lane index and its place in the thread's registers (transposes across
+// lanes).  Lane bit `mask` trades places with the register bit that selects
+// x1 over x0: afterwards a lane whose bit is 0 holds, in x0 / x1, what lanes
+// without / with the bit held in x0, and a lane whose bit is set what they
+// held in x1.  `set` is (lane & mask) != 0.
+__device__ __forceinline__ void xchg_lane_reg(uint32_t &x0, uint32_t &x1, int mask, bool set) {
+    const uint32_t r = __shfl_xor_sync(0xffffffffu, set ? x0 : x1, mask);
+    if (set) x0 = r;
+    else x1 = r;
+}
+// The same with the 16-bit half of a word: afterwards a lane whose bit is 0
+// holds the low halves of itself and its partner (low: the lane without the
+// bit), a lane whose bit is set their high halves.
+__device__ __forceinline__ uint32_t xchg_lane_half(uint32_t w, int mask, bool set) {
+    const uint32_t r = __shfl_xor_sync(0xffffffffu, w, mask);
+    return set ? __byte_perm(w, r, 0x3276) : __byte_perm(w, r, 0x5410);
+}
+
 // Shared-memory accesses by 32-bit shared-window address (base + immediate
 // offsets; no generic-address conversion).
 __device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
