@@ -248,6 +248,23 @@ __device__ __forceinline__ void load_bias_chunk(uint32_t (&bw)[4][4], const T *b
     }
 }
 
+// Dropout: a softmax thread's 32 keep flags of a chunk from the lanes' words
+// (lane L: query c0 + L, bit l = key kb - g4 + l): bit 4 (2k + e) + 2h + r =
+// (key kb + 16h + 8r, query c0 + 8k + 2q4 + e) kept.
+__device__ __forceinline__ uint32_t thread_keep_flags(uint32_t kmask, int q4, int g4) {
+    uint32_t f = 0u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            // bits 0, 8, 16, 24 after the shift: (h, r) = (0, 0), (0, 1), (1, 0),
+            // (1, 1); gathered to 4 bits
+            const uint32_t x = (__shfl_sync(0xffffffffu, kmask, 8 * k + 2 * q4 + e) >> g4) & 0x01010101u;
+            f |= ((x * 0x10204080u) >> 28) << (4 * (2 * k + e));
+        }
+    return f;
+}
+
 // load_bias_chunk's words into the order of the S^T registers: bw[k][2h + r]
 // = the (query 8k + 2q4, 8k + 2q4 + 1) pair of key g4 + 16h + 8r (lane = 4 g4
 // + q4).  As loaded, the lane bits (from the top) hold key bits 4, 3, query
@@ -284,6 +301,9 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
     // the two 16-lane halves of a TMEM tile are loaded one after the other
     // (register pressure)
     constexpr bool kSplitH = NCH == 2 && !kPFromTmem;
+    // dropout with the forward's stored flags: the lanes' words gathered into
+    // each thread's flags after the S wait (else right after their loads)
+    constexpr bool kLateKeep = kDrop && NCH == 2;
     // the bias chunk loaded at the top of the step (else at the chunk's start)
     constexpr bool kEarlyBias = kBias && NCH == 1 && kPFromTmem;
     extern __shared__ uint8_t smem_raw[];
@@ -1007,7 +1027,7 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                 // keeps the 32 flags of its own elements in one word:
                 // kb32[ch] bit 4 (2k + e) + 2h + r = (key kb + 16h + 8r, query
                 // c0 + 8k + 2q4 + e) kept.
-                uint32_t kb32[NCH];
+                uint32_t kb32[NCH], kraw[NCH];
                 if (kDrop) {
                     const uint32_t hq = (uint32_t)(u.hk * p.G + u.g_of(it, p.G));
                     const uint32_t tt4 = (uint32_t)p.drop_t * 0x01010101u;
@@ -1043,21 +1063,20 @@ __global__ void __launch_bounds__(MainCfg<kD, T>::kThreads, 1)
                                 }
                             }
                         }
-                        kb32[ch] = 0u;
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-#pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                // bits 0, 8, 16, 24 after the shift: (h, r) = (0, 0),
-                                // (0, 1), (1, 0), (1, 1); gathered to 4 bits
-                                const uint32_t x =
-                                    (__shfl_sync(0xffffffffu, kmask, 8 * k + 2 * q4 + e) >> g4) & 0x01010101u;
-                                kb32[ch] |= ((x * 0x10204080u) >> 28) << (4 * (2 * k + e));
-                            }
+                        // loaded flags at D = 64: gathered after the S wait, which
+                        // then covers the load (0.357 -> 0.313 ms on B = 4, H =
+                        // 16, 2048 keys, causal; at D = 128 the same order cost
+                        // 3-6 %)
+                        kraw[ch] = kmask;
+                        if (!(kLateKeep && p.drop_mask)) kb32[ch] = thread_keep_flags(kmask, q4, g4);
                     }
                 }
                 if (!(ok = mbar_wait(bar(B_STAGE0 + stage), st_ph, w))) break;
                 if (!(ok = mbar_wait(bar(B_S_FULL + cb), bit(s_ph, cb), w))) break;
+                if (kDrop && kLateKeep && p.drop_mask) {
+#pragma unroll
+                    for (int ch = 0; ch < NCH; ++ch) kb32[ch] = thread_keep_flags(kraw[ch], q4, g4);
+                }
                 s_ph ^= 1u << cb;
                 tc_fence_after();
                 const uint32_t lse2 = sbase + C::OFF_LSE + stage * BM * 4;   // fp32 [BM]
