@@ -183,6 +183,12 @@ BIAS_CASES = [
     (W("bias_alibi_win_d64", 1, 260, 260, 2, 1, 64), dict(bias="full", alibi="h", window=(70, 20))),
     (W("bias_seqused_d128", 2, 256, 256, 2, 2, 128, causal=True),
      dict(bias="full", seqused_q=[256, 100], seqused_k=[200, 256])),
+    # Sk a multiple of 8 (dBias rows by 16-byte stores) with used key lengths
+    # that are not: the last 8-key group of a row is written element by element
+    (W("bias_seqused_ragged_d128", 2, 256, 256, 2, 1, 128, causal=True),
+     dict(bias="full", seqused_q=[250, 77], seqused_k=[203, 131])),
+    (W("bias_seqused_ragged_d64_fp16", 1, 192, 320, 2, 2, 64, "fp16"),
+     dict(bias="h1", seqused_k=[77])),
 ]
 
 
