@@ -18,6 +18,7 @@ namespace fa {
 cudaError_t launch_schedule(const BwdParams &p, cudaStream_t stream);
 cudaError_t launch_preprocess(const BwdParams &p, int bf16, cudaStream_t stream);
 cudaError_t launch_postprocess(const BwdParams &p, int bf16, cudaStream_t stream);
+cudaError_t launch_dbias_zero(const BwdParams &p, int bm, cudaStream_t stream);
 cudaError_t launch_fwd_tc(const BwdParams &p, const CUtensorMap &q, const CUtensorMap &k,
                           const CUtensorMap &v, void *o, float *lse, int max_lq, int bf16,
                           cudaStream_t stream);
@@ -431,6 +432,18 @@ fa_status run_preprocess(const Prepared &P, fa_dtype dtype, cudaStream_t stream)
     return cuda_status(fa::launch_preprocess(P.p, dtype == FA_BF16, stream));
 }
 
+// dBias (dense, main kernel only): the main kernel writes dS of the tiles it
+// visits, the rest is 0.  A kernel that decodes the same units writes those
+// zeros when 16-byte stores fit the tensor; else the whole tensor is zeroed
+// first.
+fa_status zero_dbias(const Prepared &P, cudaStream_t stream) {
+    const fa::BwdParams &p = P.p;
+    if ((reinterpret_cast<uintptr_t>(p.dbias) & 15u) == 0 && (p.Sk & 7) == 0)
+        return cuda_status(fa::launch_dbias_zero(p, fa::main_block_m(p.D), stream));
+    const size_t n = (size_t)p.B * p.Hq * p.Sq * p.Sk * 2;
+    return cudaMemsetAsync(p.dbias, 0, n, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 fa_status run_main(const Prepared &P, fa_dtype dtype, cudaStream_t stream) {
     const fa::BwdParams &p = P.p;
     const bool wide = wide_dims(p.Dh, p.Dhv);
@@ -610,11 +623,7 @@ fa_status fa_bwd_ext(const void *q, const void *k, const void *v, const void *o,
                  stream, &P, ext);
     if (st != FA_OK) return st;
     if ((st = run_preprocess(P, dtype, stream)) != FA_OK) return st;
-    if (P.p.dbias) {
-        // the main kernel writes dS of the tiles it visits; the rest is 0
-        const size_t n = (size_t)B * Hq * Sq * Sk * 2;
-        if (cudaMemsetAsync(P.p.dbias, 0, n, stream) != cudaSuccess) return FA_ERR_CUDA;
-    }
+    if (P.p.dbias && (st = zero_dbias(P, stream)) != FA_OK) return st;
     if ((st = run_main(P, dtype, stream)) != FA_OK) return st;
     if ((st = run_postprocess(P, dtype, stream)) != FA_OK) return st;
     if (deterministic) return read_error_word(P.p.err, stream, false);
@@ -637,10 +646,7 @@ fa_status fa_bwd_stages_ext(int stages, const void *q, const void *k, const void
     if (st != FA_OK) return st;
     if ((stages & FA_STAGE_PRE) && (st = run_preprocess(P, dtype, stream)) != FA_OK) return st;
     if (stages & FA_STAGE_MAIN) {
-        if (P.p.dbias) {
-            const size_t n = (size_t)B * Hq * Sq * Sk * 2;
-            if (cudaMemsetAsync(P.p.dbias, 0, n, stream) != cudaSuccess) return FA_ERR_CUDA;
-        }
+        if (P.p.dbias && (st = zero_dbias(P, stream)) != FA_OK) return st;
         if ((st = run_main(P, dtype, stream)) != FA_OK) return st;
     }
     if ((stages & FA_STAGE_POST) && (st = run_postprocess(P, dtype, stream)) != FA_OK) return st;

@@ -2,6 +2,8 @@
 //   schedule_kernel     builds the list of work units (sequence, K/V block, kv head)
 //   preprocess_kernel   Dv = rowsum(dO o O), LSE2 = LSE * log2(e), zero dQaccum
 //   postprocess_kernel  dQ = cast(dQaccum * scale)
+//   dbias_zero_kernel   0 in the dBias entries the main kernel does not write
+#include "fa_bwd_units.cuh"
 #include "fa_device.cuh"
 #include "fa_params.h"
 
@@ -263,7 +265,65 @@ __global__ void __launch_bounds__(256) postprocess_kernel(BwdParams p) {
     }
 }
 
+// ------------------------------------------------------------- dBias zeros
+// dBias (dense problems) is the whole [B, Hq, Sq, Sk] tensor dS.  The main
+// kernel writes the entries of the row blocks its work units visit, inside
+// the used lengths; this kernel writes 0 to every other entry (tiles the mask
+// leaves out, rows and keys past the used lengths), before the main kernel
+// runs.  One block per (batch, query head, key block); the visited rows come
+// from the main kernel's own unit decoding (BM: its query rows per step), so
+// the two cover the tensor exactly once.  16-byte stores, 16 threads per
+// 128-key row segment: the tensor must start on a 16-byte boundary and Sk be
+// a multiple of 8 (the host zeroes the whole tensor otherwise).
+template <int BM>
+__global__ void __launch_bounds__(256) dbias_zero_kernel(BwdParams p) {
+    const int nblk = (p.Sk + kBlockN - 1) / kBlockN;
+    const int n = (int)(blockIdx.x % (unsigned)nblk);
+    const int bh = (int)(blockIdx.x / (unsigned)nblk);   // b * Hq + query head
+    const int b = bh / p.Hq, hq = bh - b * p.Hq;
+    // the dense unit order: groups of unit_group (batch, kv head) pairs (a
+    // divisor of B * Hkv), n-block-major inside a group
+    const int pair = b * p.Hkv + hq / p.G, gs = p.unit_group;
+    const Unit u = decode_unit<BM>(p, (pair / gs) * gs * nblk + n * gs + pair % gs);
+    const int n0 = n * kBlockN, c_end = min(n0 + kBlockN, p.Sk);
+    // rows [r0, r1) get dS from the main kernel in the keys [n0, ck)
+    const int r0 = u.nm > 0 ? u.m_begin * BM : 0;
+    const int r1 = u.nm > 0 ? max(r0, min((u.m_begin + u.nm) * BM, u.lq)) : 0;
+    const int ck = min(max(u.lk, n0), c_end);
+    uint16_t *base = reinterpret_cast<uint16_t *>(p.dbias) + (long long)bh * p.Sq * p.Sk;
+    const int seg = threadIdx.x & 15, sub = threadIdx.x >> 4;   // 8 keys, one of 16 rows
+    const int col = n0 + 8 * seg;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    // whole rows: [0, r0) and [r1, Sq)
+    const int nfull = r0 + (p.Sq - r1);
+    if (col < c_end) {
+        for (int v = sub; v < nfull; v += 16) {
+            const int row = v < r0 ? v : v - r0 + r1;
+            *reinterpret_cast<uint4 *>(base + (long long)row * p.Sk + col) = z;
+        }
+    }
+    // rows [r0, r1) past the used keys: [ck, c_end)
+    if (ck < c_end) {
+        for (int row = r0 + sub; row < r1; row += 16) {
+            uint16_t *dst = base + (long long)row * p.Sk;
+            if (col >= ck) {
+                if (col < c_end) *reinterpret_cast<uint4 *>(dst + col) = z;
+            } else if (col + 8 > ck) {
+                for (int c = ck; c < col + 8; ++c) dst[c] = 0;
+            }
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_dbias_zero(const BwdParams &p, int bm, cudaStream_t stream) {
+    const long long blocks = (long long)p.B * p.Hq * ((p.Sk + kBlockN - 1) / kBlockN);
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (bm == 64) dbias_zero_kernel<64><<<(unsigned)blocks, 256, 0, stream>>>(p);
+    else dbias_zero_kernel<128><<<(unsigned)blocks, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_schedule(const BwdParams &p, cudaStream_t stream) {
     schedule_kernel<<<1, 1024, 0, stream>>>(p);
